@@ -1,0 +1,180 @@
+"""CPU oracle for row-wise RMSNorm, fused residual-add RMSNorm and
+reduce + residual-add RMSNorm.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The product path
+(``residual_add_rmsnorm_gb300``) never imports it and shares no code with it.
+
+The arithmetic lives in ``rarn_oracle.c`` (plain C, binary64 except for the
+binary32 partial/residual sum the method prescribes); this module only
+marshals numpy arrays through ctypes.  Arrays hold the raw storage bits:
+``np.float32`` for f32 and ``np.uint16`` for f16 / bf16.
+
+Sources followed (by page title and section):
+  * "RMSNorm kernel", 1 Background / 2 Abstraction: y = x * gamma / RMS(x),
+    RMS over the last dimension, mean of squares plus eps under the root.
+  * "Tokenweave fused-RMSNorm-AR kernel", Code walkthrough: sum the partial
+    buffers, add the residual, write the sum back as the residual, take the
+    squares of that stored value, rsqrt(variance / hidden_size + eps), then
+    scale by the reciprocal RMS and the weight.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against values
+fixed by the formats' definitions, closed forms and exact rational arithmetic.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
+STORAGE = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16}
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _check(rc):
+    if rc < 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+    return rc
+
+
+class Result:
+    """Outputs of one oracle call.
+
+    y         storage bits of the normalised output, shape [T, H]
+    residual  storage bits of the updated residual (fused / reduce), or None
+    inv       binary64 reciprocal RMS per row, shape [T]
+    y64       binary64 output before its final rounding (only if requested)
+    threads   host threads the call used
+    """
+
+    def __init__(self, y, residual, inv, y64, threads):
+        self.y, self.residual, self.inv, self.y64, self.threads = y, residual, inv, y64, threads
+
+
+class Oracle:
+    """ctypes front end of one build of ``rarn_oracle.c``."""
+
+    def __init__(self, lib_path: str):
+        lib = ctypes.CDLL(lib_path)
+        p, i64, i32, f32, c_int = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                   ctypes.c_float, ctypes.c_int)
+        lib.oracle_rms_norm.argtypes = [c_int, i64, i64, p, p, f32, p, p, p, c_int]
+        lib.oracle_fused_add_rms_norm.argtypes = [c_int, i64, i64, p, p, p, f32, p, p, p, p, c_int]
+        lib.oracle_reduce_add_rms_norm.argtypes = [c_int, i64, i64, i32, p, p, p, f32, p, p, p, p,
+                                                   c_int]
+        for f in (lib.oracle_rms_norm, lib.oracle_fused_add_rms_norm,
+                  lib.oracle_reduce_add_rms_norm):
+            f.restype = c_int
+        lib.oracle_decode.argtypes = [c_int, p, p, i64]
+        lib.oracle_decode.restype = None
+        lib.oracle_round.argtypes = [c_int, p, p, i64]
+        lib.oracle_round.restype = None
+        self.lib = lib
+        self.path = lib_path
+
+    @staticmethod
+    def _as_storage(a, dtype):
+        a = np.ascontiguousarray(a)
+        want = STORAGE[dtype]
+        if a.dtype != want:
+            raise TypeError(f"oracle expects {np.dtype(want).name} storage bits for {dtype}, "
+                            f"got {a.dtype}")
+        return a
+
+    def rms_norm(self, x, gamma, eps, dtype, *, want_y64=False, threads=0) -> Result:
+        x = self._as_storage(x, dtype)
+        gamma = self._as_storage(gamma, dtype)
+        T, H = x.shape
+        y = np.empty_like(x)
+        inv = np.empty(T, np.float64)
+        y64 = np.empty((T, H), np.float64) if want_y64 else None
+        n = _check(self.lib.oracle_rms_norm(DTYPES[dtype], T, H, _ptr(x), _ptr(gamma), float(eps),
+                                            _ptr(y), _ptr(inv), _ptr(y64), threads))
+        return Result(y, None, inv, y64, n)
+
+    def fused_add_rms_norm(self, x, residual, gamma, eps, dtype, *, want_y64=False,
+                           threads=0) -> Result:
+        x = self._as_storage(x, dtype)
+        residual = self._as_storage(residual, dtype)
+        gamma = self._as_storage(gamma, dtype)
+        T, H = x.shape
+        y = np.empty_like(x)
+        res_out = np.empty_like(x)
+        inv = np.empty(T, np.float64)
+        y64 = np.empty((T, H), np.float64) if want_y64 else None
+        n = _check(self.lib.oracle_fused_add_rms_norm(
+            DTYPES[dtype], T, H, _ptr(x), _ptr(residual), _ptr(gamma), float(eps), _ptr(res_out),
+            _ptr(y), _ptr(inv), _ptr(y64), threads))
+        return Result(y, res_out, inv, y64, n)
+
+    def reduce_add_rms_norm(self, partials, residual, gamma, eps, dtype, *, want_y64=False,
+                            threads=0) -> Result:
+        partials = self._as_storage(partials, dtype)
+        residual = self._as_storage(residual, dtype)
+        gamma = self._as_storage(gamma, dtype)
+        R, T, H = partials.shape
+        y = np.empty_like(residual)
+        res_out = np.empty_like(residual)
+        inv = np.empty(T, np.float64)
+        y64 = np.empty((T, H), np.float64) if want_y64 else None
+        n = _check(self.lib.oracle_reduce_add_rms_norm(
+            DTYPES[dtype], T, H, R, _ptr(partials), _ptr(residual), _ptr(gamma), float(eps),
+            _ptr(res_out), _ptr(y), _ptr(inv), _ptr(y64), threads))
+        return Result(y, res_out, inv, y64, n)
+
+    def decode(self, bits, dtype) -> np.ndarray:
+        """Storage bits -> binary64 values (the oracle's own decoder)."""
+        bits = self._as_storage(bits, dtype)
+        out = np.empty(bits.shape, np.float64)
+        self.lib.oracle_decode(DTYPES[dtype], _ptr(bits), _ptr(out), bits.size)
+        return out
+
+    def round_to(self, values, dtype) -> np.ndarray:
+        """binary64 values -> storage bits, one round-to-nearest-even."""
+        values = np.ascontiguousarray(values, np.float64)
+        out = np.empty(values.shape, STORAGE[dtype])
+        self.lib.oracle_round(DTYPES[dtype], _ptr(values), _ptr(out), values.size)
+        return out
+
+
+_default: Oracle | None = None
+
+
+def default() -> Oracle:
+    """The oracle built from this directory's source (built on first use)."""
+    global _default
+    if _default is None:
+        _default = Oracle(_build.build())
+    return _default
+
+
+def rms_norm(*a, **k) -> Result:
+    return default().rms_norm(*a, **k)
+
+
+def fused_add_rms_norm(*a, **k) -> Result:
+    return default().fused_add_rms_norm(*a, **k)
+
+
+def reduce_add_rms_norm(*a, **k) -> Result:
+    return default().reduce_add_rms_norm(*a, **k)
+
+
+def decode(*a, **k) -> np.ndarray:
+    return default().decode(*a, **k)
+
+
+def round_to(*a, **k) -> np.ndarray:
+    return default().round_to(*a, **k)
+
+
+def cores() -> int:
+    """Host threads the oracle uses by default."""
+    return os.cpu_count() or 1

@@ -1,0 +1,305 @@
+/*
+ * rarn_oracle.c -- plain CPU oracle for row-wise RMSNorm and its fused
+ * residual-add / reduce + residual-add forms.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker the CUDA library is
+ * compared against.  Only the test suite, the package smoke check and the
+ * benchmark's CPU-baseline leg may load it; the product path never does.  It
+ * shares no code, header, table or helper with the CUDA sources.
+ *
+ * What it computes (per row t of a row-major [T, H] problem):
+ *
+ *   1. h  -- the row that is normalised.
+ *        plain:   h_i = x_i
+ *        fused:   h_i = RN_dt( fl32( x_i + r_i ) )
+ *        reduce:  acc = p0_i; acc = fl32(acc + p1_i); ... ; acc = fl32(acc + p{R-1}_i);
+ *                 acc = fl32(acc + r_i);  h_i = RN_dt(acc)
+ *      "Tokenweave fused-RMSNorm-AR kernel", Code walkthrough: the first
+ *      pass reduces the partial buffers, adds the residual, stores the sum
+ *      back as the new residual and accumulates the squares of that stored
+ *      value.  The pages leave the order of the partial sum to the hardware;
+ *      this oracle fixes it to p0, p1, ..., p{R-1}, then the residual, each
+ *      add in binary32, and rounds once to the storage type.
+ *   2. ss = sum_i h_i^2                     (binary64, index order)
+ *   3. inv = 1 / sqrt(ss / H + eps)         (binary64; eps is the binary32
+ *                                            argument widened)
+ *      "RMSNorm kernel", 1 Background and 2 Analytics & Implementation
+ *      (Abstraction): RMS over the last dimension only, mean of the squares
+ *      plus eps under the root; the tokenweave kernel divides by the full
+ *      hidden size before adding eps.
+ *   4. y_i = RN_dt( (h_i * inv) * gamma_i )  (binary64 product, one rounding)
+ *      "RMSNorm kernel", Abstraction step 2: elementwise x_i * gamma_i / RMS.
+ *
+ * Storage types: binary32 (f32), binary16 (f16), bfloat16 (bf16).  RN_dt is
+ * round-to-nearest-even into the storage type, with IEEE overflow to
+ * infinity and gradual underflow; it is written from the formats'
+ * definitions (precision p, minimum exponent emin, maximum exponent emax).
+ *
+ * Build flags must keep binary32 arithmetic exact IEEE: no -ffast-math, and
+ * -ffp-contract=off (there is no multiply in the binary32 part, but the flag
+ * documents the intent).
+ */
+#define _POSIX_C_SOURCE 200809L
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#include <unistd.h>
+
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2 };
+
+/* ----------------------------------------------------------------------- */
+/* Storage formats                                                          */
+/* ----------------------------------------------------------------------- */
+
+static int elem_size(int dt) { return dt == ORC_F32 ? 4 : 2; }
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double half_bits_to_double(uint16_t b) {
+    int sign = b >> 15;
+    int e = (b >> 10) & 0x1f;
+    int m = b & 0x3ff;
+    double v;
+    if (e == 0x1f) {
+        v = m ? NAN : INFINITY;
+    } else if (e == 0) {
+        v = ldexp((double)m, -24);          /* subnormal: m * 2^-24 */
+    } else {
+        v = ldexp((double)(m + 1024), e - 25); /* (1 + m/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16 is the upper half of a binary32 pattern. */
+static double bf16_bits_to_double(uint16_t b) {
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+}
+
+static double load_elem(int dt, const void *base, int64_t i) {
+    if (dt == ORC_F32) {
+        float f;
+        memcpy(&f, (const char *)base + 4 * i, 4);
+        return (double)f;
+    }
+    uint16_t b = ((const uint16_t *)base)[i];
+    return dt == ORC_F16 ? half_bits_to_double(b) : bf16_bits_to_double(b);
+}
+
+/*
+ * Round v to the nearest value of a binary format with p significand bits,
+ * normal exponents emin..emax, ties to even.  Returns the rounded value as a
+ * double (exact: every such format is a subset of binary64 here).
+ */
+static double round_to_format(double v, int p, int emin, int emax) {
+    if (isnan(v) || isinf(v) || v == 0.0) return v;
+    int e2;
+    frexp(fabs(v), &e2);          /* |v| = m * 2^e2, m in [0.5, 1) */
+    int lead = e2 - 1;            /* exponent of the leading bit */
+    if (lead < emin) lead = emin; /* below the normal range the quantum is fixed */
+    int q = lead - (p - 1);       /* exponent of one unit in the last place */
+    double r = nearbyint(ldexp(v, -q)); /* default mode: nearest, ties to even */
+    double out = ldexp(r, q);
+    double max_finite = ldexp(2.0 - ldexp(1.0, 1 - p), emax);
+    if (fabs(out) > max_finite) return copysign(INFINITY, v);
+    return out;
+}
+
+static double round_dt(int dt, double v) {
+    switch (dt) {
+    case ORC_F32: return round_to_format(v, 24, -126, 127);
+    case ORC_F16: return round_to_format(v, 11, -14, 15);
+    default: return round_to_format(v, 8, -126, 127);
+    }
+}
+
+/* Encode a value that is already exactly representable in dt. */
+static void store_exact(int dt, void *base, int64_t i, double v) {
+    if (dt == ORC_F32) {
+        float f = (float)v;
+        memcpy((char *)base + 4 * i, &f, 4);
+        return;
+    }
+    uint16_t b;
+    if (dt == ORC_BF16) {
+        float f = (float)v; /* exact: v has at most 8 significant bits */
+        uint32_t u;
+        memcpy(&u, &f, 4);
+        b = (uint16_t)(u >> 16);
+        if (isnan(v)) b = 0x7fc0;
+    } else {
+        uint16_t s = signbit(v) ? 0x8000 : 0;
+        double a = fabs(v);
+        if (isnan(v)) {
+            b = 0x7e00;
+        } else if (isinf(a)) {
+            b = s | 0x7c00;
+        } else if (a == 0.0) {
+            b = s;
+        } else {
+            int e2;
+            frexp(a, &e2);
+            int lead = e2 - 1;
+            if (lead >= -14) {
+                int frac = (int)ldexp(a, 10 - lead) - 1024;
+                b = s | (uint16_t)((lead + 15) << 10) | (uint16_t)frac;
+            } else {
+                b = s | (uint16_t)ldexp(a, 24);
+            }
+        }
+    }
+    ((uint16_t *)base)[i] = b;
+}
+
+/* ----------------------------------------------------------------------- */
+/* One row                                                                  */
+/* ----------------------------------------------------------------------- */
+
+typedef struct {
+    int dt;
+    int64_t T, H;
+    int32_t R;                 /* number of partial buffers; 0 = plain */
+    const void *x;             /* plain: x[T,H]; fused/reduce: partials[R,T,H] */
+    const void *residual_in;   /* [T,H] or NULL (plain) */
+    const void *gamma;         /* [H] */
+    float eps;
+    void *residual_out;        /* [T,H] or NULL */
+    void *y;                   /* [T,H] */
+    double *inv_out;           /* [T] or NULL */
+    double *y64_out;           /* [T,H] or NULL: y before the final rounding */
+} job_t;
+
+static void one_row(const job_t *j, int64_t t, double *h) {
+    const int64_t H = j->H;
+    const int64_t row = t * H;
+
+    /* step 1: h */
+    if (j->residual_in == NULL) {
+        for (int64_t i = 0; i < H; ++i) h[i] = load_elem(j->dt, j->x, row + i);
+    } else {
+        const int64_t slice = j->T * H;
+        for (int64_t i = 0; i < H; ++i) {
+            float acc = (float)load_elem(j->dt, j->x, row + i);
+            for (int32_t r = 1; r < j->R; ++r)
+                acc = acc + (float)load_elem(j->dt, j->x, (int64_t)r * slice + row + i);
+            acc = acc + (float)load_elem(j->dt, j->residual_in, row + i);
+            h[i] = round_dt(j->dt, (double)acc);
+        }
+        if (j->residual_out)
+            for (int64_t i = 0; i < H; ++i) store_exact(j->dt, j->residual_out, row + i, h[i]);
+    }
+
+    /* step 2: sum of squares of the (stored) row */
+    double ss = 0.0;
+    for (int64_t i = 0; i < H; ++i) ss += h[i] * h[i];
+
+    /* step 3: reciprocal RMS */
+    double inv = 1.0 / sqrt(ss / (double)H + (double)j->eps);
+    if (j->inv_out) j->inv_out[t] = inv;
+
+    /* step 4: scale, weight, one rounding */
+    for (int64_t i = 0; i < H; ++i) {
+        double v = (h[i] * inv) * load_elem(j->dt, j->gamma, i);
+        if (j->y64_out) j->y64_out[row + i] = v;
+        store_exact(j->dt, j->y, row + i, round_dt(j->dt, v));
+    }
+}
+
+typedef struct {
+    const job_t *job;
+    int64_t t0, t1;
+    int rc;
+} slice_t;
+
+static void *worker(void *arg) {
+    slice_t *s = (slice_t *)arg;
+    double *h = (double *)malloc(sizeof(double) * (size_t)(s->job->H > 0 ? s->job->H : 1));
+    if (!h) {
+        s->rc = -1;
+        return NULL;
+    }
+    for (int64_t t = s->t0; t < s->t1; ++t) one_row(s->job, t, h);
+    free(h);
+    s->rc = 0;
+    return NULL;
+}
+
+/* Runs the rows over nthreads host threads (0 = every online core).
+ * Returns the number of threads used, or a negative value on error. */
+static int run(const job_t *j, int nthreads) {
+    if (j->T < 0 || j->H <= 0 || !j->x || !j->gamma || !j->y) return -2;
+    if (j->T == 0) return 0;
+    if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+    if (nthreads < 1) nthreads = 1;
+    if ((int64_t)nthreads > j->T) nthreads = (int)j->T;
+    pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    slice_t *sl = (slice_t *)calloc((size_t)nthreads, sizeof(slice_t));
+    if (!tid || !sl) {
+        free(tid);
+        free(sl);
+        return -1;
+    }
+    int rc = nthreads;
+    int started = 0;
+    for (int k = 0; k < nthreads; ++k) {
+        sl[k].job = j;
+        sl[k].t0 = j->T * k / nthreads;
+        sl[k].t1 = j->T * (k + 1) / nthreads;
+        sl[k].rc = -1;
+        if (nthreads == 1) {
+            worker(&sl[k]);
+            started = 0;
+        } else if (pthread_create(&tid[k], NULL, worker, &sl[k]) == 0) {
+            ++started;
+        } else {
+            worker(&sl[k]); /* run inline if a thread cannot be created */
+        }
+    }
+    for (int k = 0; k < started; ++k) pthread_join(tid[k], NULL);
+    for (int k = 0; k < nthreads; ++k)
+        if (sl[k].rc != 0) rc = -1;
+    free(tid);
+    free(sl);
+    return rc;
+}
+
+/* ----------------------------------------------------------------------- */
+/* Exported entry points (ctypes)                                           */
+/* ----------------------------------------------------------------------- */
+
+int oracle_rms_norm(int dt, int64_t T, int64_t H, const void *x, const void *gamma, float eps,
+                    void *y, double *inv_out, double *y64_out, int nthreads) {
+    job_t j = {dt, T, H, 0, x, NULL, gamma, eps, NULL, y, inv_out, y64_out};
+    return run(&j, nthreads);
+}
+
+int oracle_fused_add_rms_norm(int dt, int64_t T, int64_t H, const void *x, const void *residual_in,
+                              const void *gamma, float eps, void *residual_out, void *y,
+                              double *inv_out, double *y64_out, int nthreads) {
+    if (!residual_in) return -2;
+    job_t j = {dt, T, H, 1, x, residual_in, gamma, eps, residual_out, y, inv_out, y64_out};
+    return run(&j, nthreads);
+}
+
+int oracle_reduce_add_rms_norm(int dt, int64_t T, int64_t H, int32_t R, const void *partials,
+                               const void *residual_in, const void *gamma, float eps,
+                               void *residual_out, void *y, double *inv_out, double *y64_out,
+                               int nthreads) {
+    if (!residual_in || R < 1) return -2;
+    job_t j = {dt, T, H, R, partials, residual_in, gamma, eps, residual_out, y, inv_out, y64_out};
+    return run(&j, nthreads);
+}
+
+/* Elementwise helpers exposed so the tests can pin the format code alone. */
+void oracle_decode(int dt, const void *src, double *dst, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) dst[i] = load_elem(dt, src, i);
+}
+
+void oracle_round(int dt, const double *src, void *dst, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) store_exact(dt, dst, i, round_dt(dt, src[i]));
+}
+
+int oracle_elem_size(int dt) { return elem_size(dt); }

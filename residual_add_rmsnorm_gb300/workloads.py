@@ -1,0 +1,174 @@
+"""Seeded synthetic inputs for the RMSNorm family.
+
+This module holds only random-number generation and storage-type casts; none
+of the normalisation arithmetic lives here.  It is the one piece shared by the
+tests, the benchmark and the package smoke check: the same seed gives the same
+storage bits on both sides of every comparison.
+
+Recipe (per call, one ``numpy.random.Generator(PCG64(seed))``):
+
+* Normal draws use the Box-Muller transform on binary32 uniforms from that
+  generator: u1, u2 in [0, 1), r = sqrt(-2 log(1 - u1)) (1 - u1 is exact in
+  binary32), z0 = r cos(2 pi u2), z1 = r sin(2 pi u2), interleaved z0, z1.
+  numpy's own normal sampler is an order of magnitude slower at these sizes.
+* Draw order: x (or partials 0..R-1, one [T, H] block each), then residual,
+  then -- for the scaled-token workload -- the per-row log-uniform factors and
+  the outlier channel permutation, then gamma ~ U(0.5, 1.5).
+* Values are formed in binary32 and cast to the storage type with
+  round-to-nearest-even (numpy for f16, torch for bf16).
+* Scaled-token workload: every row t of both x and residual is multiplied by
+  s_t = 10 ** U(-3, 3); ceil(H / 100) channels, chosen by a seeded
+  permutation, are multiplied by 100 in both x and residual.
+
+Arrays hold raw storage bits: ``np.float32`` for f32, ``np.uint16`` for f16 and
+bf16.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+STORAGE = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16}
+ELEM_SIZE = {"f32": 4, "f16": 2, "bf16": 2}
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One problem instance of the RMSNorm family.
+
+    op      'rms_norm' | 'fused_add_rms_norm' | 'reduce_add_rms_norm'
+    R       number of partial buffers (reduce only; 1 for fused, 0 for plain)
+    scaled  per-row log-uniform scale and x100 outlier channels
+    """
+    name: str
+    op: str
+    dtype: str
+    T: int
+    H: int
+    eps: float
+    R: int = 0
+    seed: int = 0
+    partial_std: float = 1.0
+    scaled: bool = False
+    note: str = field(default="", compare=False)
+
+    @property
+    def n_inputs(self) -> int:
+        """Input streams read per element (x or partials, plus residual)."""
+        return {"rms_norm": 1, "fused_add_rms_norm": 2}.get(self.op, self.R + 1)
+
+    @property
+    def n_outputs(self) -> int:
+        """Output streams written per element (y, plus residual)."""
+        return 1 if self.op == "rms_norm" else 2
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes the operation must move at minimum: every input element read
+        once, every output element written once, gamma read once."""
+        s = ELEM_SIZE[self.dtype]
+        return s * self.T * self.H * (self.n_inputs + self.n_outputs) + s * self.H
+
+
+# The five benchmark configurations of the method (the token sweep is five
+# shapes of one configuration).
+CONFIGS = [
+    Workload("plain_f32_T512_H2048", "rms_norm", "f32", 512, 2048, 1e-6),
+    Workload("plain_f16_T512_H1592", "rms_norm", "f16", 512, 1592, 1e-5),
+    Workload("fused_bf16_T4096_H4096", "fused_add_rms_norm", "bf16", 4096, 4096, 1e-6, R=1),
+    Workload("reduce8_bf16_T8192_H8192", "reduce_add_rms_norm", "bf16", 8192, 8192, 1e-6, R=8,
+             partial_std=math.sqrt(1.0 / 8.0)),
+    Workload("fused_scaled_bf16_T1_H5120", "fused_add_rms_norm", "bf16", 1, 5120, 1e-6, R=1,
+             scaled=True),
+    Workload("fused_scaled_bf16_T16_H5120", "fused_add_rms_norm", "bf16", 16, 5120, 1e-6, R=1,
+             scaled=True),
+    Workload("fused_scaled_bf16_T128_H5120", "fused_add_rms_norm", "bf16", 128, 5120, 1e-6, R=1,
+             scaled=True),
+    Workload("fused_scaled_bf16_T32768_H5120", "fused_add_rms_norm", "bf16", 32768, 5120, 1e-6,
+             R=1, scaled=True),
+    Workload("fused_scaled_bf16_T64_H16384", "fused_add_rms_norm", "bf16", 64, 16384, 1e-6, R=1,
+             scaled=True),
+]
+BY_NAME = {w.name: w for w in CONFIGS}
+
+
+def workload(op: str, dtype: str, T: int, H: int, *, R: int | None = None, eps: float = 1e-6,
+             seed: int = 0, scaled: bool = False, partial_std: float = 1.0) -> Workload:
+    """An ad-hoc problem (edge-shape grids in the tests)."""
+    if R is None:
+        R = {"rms_norm": 0, "fused_add_rms_norm": 1}.get(op, 2)
+    return Workload(f"{op}_{dtype}_T{T}_H{H}_R{R}", op, dtype, T, H, eps, R=R, seed=seed,
+                    partial_std=partial_std, scaled=scaled)
+
+
+def _normal_f32(rng: np.random.Generator, n: int) -> np.ndarray:
+    m = (n + 1) // 2
+    u1 = rng.random(m, dtype=np.float32)
+    u2 = rng.random(m, dtype=np.float32)
+    r = np.sqrt(np.float32(-2.0) * np.log(np.float32(1.0) - u1))
+    th = np.float32(2.0 * np.pi) * u2
+    z = np.empty(2 * m, np.float32)
+    z[0::2] = r * np.cos(th)
+    z[1::2] = r * np.sin(th)
+    return z[:n]
+
+
+def to_storage(v: np.ndarray, dtype: str) -> np.ndarray:
+    """binary32 values -> storage bits (round to nearest even)."""
+    v = np.ascontiguousarray(v, np.float32)
+    if dtype == "f32":
+        return v
+    if dtype == "f16":
+        return v.astype(np.float16).view(np.uint16)
+    import torch
+    return torch.from_numpy(v).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def from_storage(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Storage bits -> binary32 values (exact widening)."""
+    if dtype == "f32":
+        return np.asarray(bits, np.float32)
+    if dtype == "f16":
+        return np.asarray(bits, np.uint16).view(np.float16).astype(np.float32)
+    u = np.asarray(bits, np.uint16).astype(np.uint32) << 16
+    return u.view(np.float32)
+
+
+def generate(w: Workload) -> dict:
+    """Inputs of ``w`` as storage bits: keys 'x' (plain, fused), 'partials'
+    (reduce, shape [R, T, H]), 'residual' (fused, reduce) and 'gamma'."""
+    rng = np.random.default_rng(w.seed)
+    T, H = w.T, w.H
+    out = {}
+    if w.op == "reduce_add_rms_norm":
+        parts = np.empty((w.R, T, H), STORAGE[w.dtype])
+        for r in range(w.R):
+            z = _normal_f32(rng, T * H).reshape(T, H)
+            if w.partial_std != 1.0:
+                z *= np.float32(w.partial_std)
+            parts[r] = to_storage(z, w.dtype)
+        out["partials"] = parts
+        first = None
+    else:
+        first = _normal_f32(rng, T * H).reshape(T, H)
+    res = None
+    if w.op != "rms_norm":
+        res = _normal_f32(rng, T * H).reshape(T, H)
+    if w.scaled:
+        s = np.power(10.0, rng.uniform(-3.0, 3.0, size=T)).astype(np.float32)[:, None]
+        k = math.ceil(H / 100)
+        chan = rng.permutation(H)[:k]
+        cs = np.ones(H, np.float32)
+        cs[chan] = 100.0
+        if first is not None:
+            first = first * s * cs
+        if res is not None:
+            res = res * s * cs
+    if first is not None:
+        out["x"] = to_storage(first, w.dtype)
+    if res is not None:
+        out["residual"] = to_storage(res, w.dtype)
+    g = rng.uniform(0.5, 1.5, size=H).astype(np.float32)
+    out["gamma"] = to_storage(g, w.dtype)
+    return out

@@ -1,0 +1,439 @@
+"""Checks that pin the CPU oracle to facts outside itself.
+
+Each ``pin_*`` function takes an oracle instance (``oracle.Oracle``) and raises
+``AssertionError`` on a mismatch.  ``test_oracle_pins.py`` runs them on the
+real oracle; ``test_oracle_mutations.py`` runs them on copies of the oracle
+with a planted mistake and requires that at least one fails.
+
+What the pins rest on (none of it is the oracle's own code):
+  * the storage formats' definitions, through numpy's float16 / float32 casts,
+    torch's bfloat16 decode, and exact rational rounding (``fractions``);
+  * closed forms of the normalisation (constant row, unit weight, scale
+    invariance at eps = 0, one-element rows);
+  * a worked example of the fixed binary32 summation order;
+  * exact integer sums;
+  * brute force on tiny rows in exact rational / 50-digit decimal arithmetic.
+"""
+from __future__ import annotations
+
+import math
+from decimal import Decimal, getcontext
+from fractions import Fraction
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# Storage formats, from the library decoders
+# ---------------------------------------------------------------------------
+
+FORMATS = {  # precision p, emin, emax
+    "f32": (24, -126, 127),
+    "f16": (11, -14, 15),
+    "bf16": (8, -126, 127),
+}
+
+
+def lib_decode(bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Decode storage bits with numpy / torch (not the oracle)."""
+    if dtype == "f32":
+        return np.asarray(bits, np.float32).astype(np.float64)
+    if dtype == "f16":
+        return np.asarray(bits, np.uint16).view(np.float16).astype(np.float64)
+    import torch
+    t = torch.from_numpy(np.asarray(bits, np.uint16).astype(np.int16).copy())
+    return t.view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def rn_exact(v: Fraction, dtype: str) -> float:
+    """Round an exact rational to the storage format: nearest, ties to even,
+    overflow to infinity.  Exact rational arithmetic throughout; Python's
+    ``round`` on a Fraction rounds half to even."""
+    p, emin, emax = FORMATS[dtype]
+    if v == 0:
+        return 0.0
+    a = abs(v)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    if Fraction(2) ** e > a:
+        e -= 1
+    if Fraction(2) ** (e + 1) <= a:
+        e += 1
+    e = max(e, emin)
+    q = e - (p - 1)
+    n = round(a / Fraction(2) ** q)
+    r = Fraction(n) * Fraction(2) ** q
+    max_finite = (2 - Fraction(2) ** (1 - p)) * Fraction(2) ** emax
+    out = math.inf if r > max_finite else float(r)
+    return out if v > 0 else -out
+
+
+def bits_of(values: np.ndarray, dtype: str) -> np.ndarray:
+    """Storage bits of values that are exactly representable (library casts)."""
+    values = np.asarray(values, np.float64)
+    if dtype == "f32":
+        return values.astype(np.float32)
+    if dtype == "f16":
+        return values.astype(np.float16).view(np.uint16)
+    import torch
+    t = torch.from_numpy(values.astype(np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def ulp_dist(a_bits: np.ndarray, b_bits: np.ndarray, dtype: str) -> np.ndarray:
+    """Distance in units in the last place between two arrays of storage bits."""
+    if dtype == "f32":
+        a = np.asarray(a_bits, np.float32).view(np.int32).astype(np.int64)
+        b = np.asarray(b_bits, np.float32).view(np.int32).astype(np.int64)
+        sign = 1 << 31
+    else:
+        a = np.asarray(a_bits, np.uint16).astype(np.int64)
+        b = np.asarray(b_bits, np.uint16).astype(np.int64)
+        sign = 1 << 15
+    a = np.where(a & sign, -(a & (sign - 1)), a & (sign - 1))
+    b = np.where(b & sign, -(b & (sign - 1)), b & (sign - 1))
+    return np.abs(a - b)
+
+
+# ---------------------------------------------------------------------------
+# Pins on the format code
+# ---------------------------------------------------------------------------
+
+def pin_decode_all_patterns(O):
+    """Every f16 / bf16 bit pattern decodes as numpy / torch decode it."""
+    allbits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    for dt in ("f16", "bf16"):
+        got = O.decode(allbits, dt)
+        want = lib_decode(allbits, dt)
+        nan = np.isnan(want)
+        assert np.array_equal(np.isnan(got), nan), dt
+        assert np.array_equal(got[~nan], want[~nan]), dt
+        assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan])), dt
+
+
+def _rounding_probe(dtype, rng, n=20000):
+    """Doubles that stress rounding: random magnitudes across the whole range
+    of the format (subnormals and overflow included) plus exact midpoints."""
+    p, emin, emax = FORMATS[dtype]
+    e = rng.integers(emin - p - 2, emax + 2, size=n)
+    m = rng.random(n) + 1.0
+    v = np.ldexp(m, e) * np.where(rng.random(n) < 0.5, -1.0, 1.0)
+    # exact midpoints between neighbours: (2k + 1) * 2^(q-1)
+    k = rng.integers(1 << (p - 1), 1 << p, size=n // 4)
+    q = rng.integers(emin - (p - 1), emax - (p - 1) + 1, size=n // 4)
+    mids = np.ldexp(2.0 * k + 1.0, q - 1)
+    # midpoints in the subnormal range and at the overflow threshold
+    sub = np.ldexp(2.0 * rng.integers(0, 1 << (p - 1), size=64) + 1.0, emin - (p - 1) - 1)
+    maxf = (2.0 - 2.0 ** (1 - p)) * 2.0 ** emax
+    edge = np.array([maxf, maxf + 2.0 ** (emax - p), maxf + 2.0 ** (emax - p) * 0.999,
+                     np.nextafter(maxf + 2.0 ** (emax - p), 0), 2.0 ** (emin - p),
+                     2.0 ** (emin - p) * 1.0001, 2.0 ** (emin - p) * 0.9999, 0.0, -0.0])
+    return np.concatenate([v, mids, -mids, sub, edge, -edge])
+
+
+def pin_round_matches_library(O):
+    """One rounding double -> f16 / f32 equals numpy's cast (both round once,
+    to nearest, ties to even)."""
+    rng = np.random.default_rng(1)
+    for dt, np_t in (("f16", np.float16), ("f32", np.float32)):
+        v = _rounding_probe(dt, rng)
+        with np.errstate(over="ignore"):
+            want = v.astype(np_t)
+        got = O.round_to(v, dt)
+        if dt == "f16":
+            assert np.array_equal(got, want.view(np.uint16)), dt
+        else:
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), dt
+
+
+def pin_round_bf16_nearest(O):
+    """One rounding double -> bf16 picks the nearest bf16 value, ties to the
+    even pattern, overflow to infinity: brute force over the table of every
+    finite bf16 value, decoded by torch."""
+    allbits = np.arange(0, 0x7F80, dtype=np.uint16)  # +0 .. largest finite
+    table = lib_decode(allbits, "bf16")
+    rng = np.random.default_rng(2)
+    v = _rounding_probe("bf16", rng, n=8000)
+    got = O.round_to(v, "bf16")
+    a = np.abs(v)
+    i = np.clip(np.searchsorted(table, a), 1, len(table) - 1)
+    lo, hi = table[i - 1], table[i]
+    below = a - lo
+    above = hi - a
+    pick = np.where(below < above, i - 1, i)
+    tie = below == above
+    pick = np.where(tie & ((i - 1) % 2 == 0), i - 1, pick)
+    res = allbits[pick].astype(np.uint32)
+    maxf = table[-1]
+    half_ulp = (table[-1] - table[-2]) / 2
+    res = np.where(a > maxf, 0x7F7F, res)               # between max and the midpoint
+    res = np.where(a >= maxf + half_ulp, 0x7F80, res)  # at or past it: infinity
+    res = np.where(np.signbit(v), res | 0x8000, res).astype(np.uint16)
+    assert np.array_equal(got, res)
+
+
+def pin_round_exact_rationals(O):
+    """Hand-checked ties: the exact midpoint between two neighbours goes to
+    the even one."""
+    cases = {
+        # bf16 has 8 significant bits: neighbours of 1 are 1 and 1 + 2^-7
+        "bf16": [(1 + 2.0 ** -8, 1.0), (1 + 3 * 2.0 ** -8, 1 + 2.0 ** -6),
+                 (1 + 2.0 ** -8 + 2.0 ** -30, 1 + 2.0 ** -7)],
+        # f16 has 11 significant bits
+        "f16": [(1 + 2.0 ** -11, 1.0), (1 + 3 * 2.0 ** -11, 1 + 2.0 ** -9),
+                (65520.0, math.inf), (65519.99, 65504.0), (2.0 ** -25, 0.0),
+                (3 * 2.0 ** -26, 2.0 ** -24)],
+        "f32": [(1 + 2.0 ** -24, 1.0), (1 + 3 * 2.0 ** -24, 1 + 2.0 ** -22)],
+    }
+    for dt, pairs in cases.items():
+        v = np.array([a for a, _ in pairs])
+        got = O.decode(O.round_to(v, dt), dt)
+        want = np.array([b for _, b in pairs])
+        assert np.array_equal(got, want), (dt, got, want)
+        for a, b in pairs:
+            assert rn_exact(Fraction(a), dt) == b, (dt, a)
+
+
+# ---------------------------------------------------------------------------
+# Pins on the residual (step 1)
+# ---------------------------------------------------------------------------
+
+def _rand_bits(rng, shape, dtype, scale=1.0):
+    v = rng.standard_normal(shape) * scale
+    return bits_of(v.astype(np.float32).astype(np.float64), dtype)
+
+
+def pin_fused_residual_is_exact_rounded_sum(O):
+    """R = 1: the stored residual is the exact sum x + r rounded once
+    (for f16 / bf16 the binary32 add of two such values never double-rounds)."""
+    rng = np.random.default_rng(3)
+    for dt in ("bf16", "f16", "f32"):
+        T, H = 4, 257
+        x = _rand_bits(rng, (T, H), dt)
+        r = _rand_bits(rng, (T, H), dt, scale=3.0)
+        g = bits_of(np.ones(H), dt)
+        res = O.fused_add_rms_norm(x, r, g, 1e-6, dt)
+        xv, rv = lib_decode(x, dt).ravel(), lib_decode(r, dt).ravel()
+        want = np.array([rn_exact(Fraction(a) + Fraction(b), dt) for a, b in zip(xv, rv)])
+        got = lib_decode(res.residual, dt).ravel()
+        assert np.array_equal(got, want), dt
+
+
+def pin_reduce_order_worked_example(O):
+    """Worked example of the fixed order: partials (2^24, 1, -2^24) and
+    residual 0.  In binary32, 2^24 + 1 rounds back to 2^24 (tie to even), so
+    the sequential sum is exactly 0; the exact sum is 1, and any other order
+    that adds 1 last, or a wider accumulator, gives 1."""
+    for dt in ("bf16", "f32"):  # 2^24 overflows binary16
+        H = 3
+        p = np.stack([bits_of(np.full((1, H), v), dt) for v in (2.0 ** 24, 1.0, -(2.0 ** 24))])
+        r = bits_of(np.zeros((1, H)), dt)
+        g = bits_of(np.ones(H), dt)
+        res = O.reduce_add_rms_norm(p, r, g, 1e-6, dt)
+        assert np.all(lib_decode(res.residual, dt) == 0.0), dt
+    # One final rounding, not one per add: partials (2^11, 1, 1) in f16 and
+    # (2^8, 1, 1) in bf16.  binary32 holds 2^k + 2 exactly and it is
+    # representable in the storage type; rounding after every add would
+    # lose each 1 to a tie-to-even and give 2^k.
+    for dt, big in (("f16", 2048.0), ("bf16", 256.0)):
+        p = np.stack([bits_of(np.full((1, 2), v), dt) for v in (big, 1.0, 1.0)])
+        r = bits_of(np.zeros((1, 2)), dt)
+        res = O.reduce_add_rms_norm(p, r, bits_of(np.ones(2), dt), 1e-6, dt)
+        assert np.all(lib_decode(res.residual, dt) == big + 2.0), dt
+        # and the final rounding itself ties to even: 2^k + 1 -> 2^k
+        p1 = np.stack([bits_of(np.full((1, 2), v), dt) for v in (big, 1.0)])
+        res1 = O.reduce_add_rms_norm(p1, r, bits_of(np.ones(2), dt), 1e-6, dt)
+        assert np.all(lib_decode(res1.residual, dt) == big), dt
+
+
+def pin_reduce_integer_sums(O):
+    """Small integers add exactly in every order: the residual is the plain
+    integer sum of all partials and the residual, per element."""
+    rng = np.random.default_rng(4)
+    for dt in ("bf16", "f16", "f32"):
+        R, T, H = 8, 3, 67
+        pi = rng.integers(-12, 13, size=(R, T, H))
+        ri = rng.integers(-12, 13, size=(T, H))
+        p = bits_of(pi.astype(np.float64), dt).reshape(R, T, H)
+        r = bits_of(ri.astype(np.float64), dt)
+        res = O.reduce_add_rms_norm(p, r, bits_of(np.ones(H), dt), 1e-6, dt)
+        want = (pi.sum(0) + ri).astype(np.float64)
+        assert np.array_equal(lib_decode(res.residual, dt), want), dt
+
+
+def pin_reduce_brute_force_binary32(O):
+    """Tiny random reduce problems: the residual equals the sequential
+    binary32 sum p0 + p1 + ... + p{R-1} + r, each add rounded to binary32 in
+    exact rational arithmetic, then one rounding to the storage type."""
+    rng = np.random.default_rng(5)
+    for dt in ("bf16", "f16", "f32"):
+        for R in (2, 3, 8):
+            T, H = 2, 9
+            scales = rng.choice([1e-3, 1.0, 300.0], size=R)
+            p = np.stack([_rand_bits(rng, (T, H), dt, s) for s in scales])
+            r = _rand_bits(rng, (T, H), dt)
+            res = O.reduce_add_rms_norm(p, r, bits_of(np.ones(H), dt), 1e-6, dt)
+            pv = lib_decode(p, dt)
+            rv = lib_decode(r, dt)
+            want = np.empty((T, H))
+            for t in range(T):
+                for i in range(H):
+                    acc = Fraction(pv[0, t, i])
+                    for k in range(1, R):
+                        acc = Fraction(rn_exact(acc + Fraction(pv[k, t, i]), "f32"))
+                    acc = Fraction(rn_exact(acc + Fraction(rv[t, i]), "f32"))
+                    want[t, i] = rn_exact(acc, dt)
+            assert np.array_equal(lib_decode(res.residual, dt), want), (dt, R)
+
+
+def pin_reduce_special_cases(O):
+    """reduce with partials (x, 0, ..., 0) equals fused(x); reduce with R = 1
+    equals fused; fused with a zero residual equals plain."""
+    rng = np.random.default_rng(6)
+    for dt in ("bf16", "f16", "f32"):
+        T, H = 5, 130
+        x = _rand_bits(rng, (T, H), dt)
+        r = _rand_bits(rng, (T, H), dt)
+        g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+        zero = bits_of(np.zeros((T, H)), dt)
+        f = O.fused_add_rms_norm(x, r, g, 1e-5, dt)
+        red = O.reduce_add_rms_norm(np.stack([x] + [zero] * 3), r, g, 1e-5, dt)
+        red1 = O.reduce_add_rms_norm(x[None], r, g, 1e-5, dt)
+        for other in (red, red1):
+            assert np.array_equal(other.y, f.y), dt
+            assert np.array_equal(other.residual, f.residual), dt
+        plain = O.rms_norm(x, g, 1e-5, dt)
+        fz = O.fused_add_rms_norm(x, zero, g, 1e-5, dt)
+        assert np.array_equal(plain.y, fz.y), dt
+        assert np.array_equal(fz.residual, x), dt
+
+
+# ---------------------------------------------------------------------------
+# Pins on the normalisation (steps 2-4)
+# ---------------------------------------------------------------------------
+
+def _rel(a, b):
+    a = np.asarray(a, np.float64)
+    b = np.asarray(b, np.float64)
+    return np.max(np.abs(a - b) / np.maximum(np.abs(b), 1e-300))
+
+
+def pin_constant_row(O):
+    """A row of constant c gives y_i = c / sqrt(c^2 + eps) * gamma_i."""
+    getcontext().prec = 50
+    for dt in ("f32", "f16", "bf16"):
+        for c, eps in ((3.0, 1e-6), (0.015625, 0.25), (-2.5, 1e-5), (1.0, 1.0), (0.0078125, 0.0)):
+            H = 96
+            x = bits_of(np.full((1, H), c), dt)
+            gv = np.linspace(0.5, 1.5, H)
+            g = bits_of(gv, dt)
+            gd = lib_decode(g, dt)
+            e32 = float(np.float32(eps))
+            res = O.rms_norm(x, g, eps, dt, want_y64=True)
+            k = Decimal(c) / (Decimal(c) * Decimal(c) + Decimal(e32)).sqrt()
+            want = np.array([float(k * Decimal(gi)) for gi in gd])
+            assert _rel(res.y64[0], want) < 1e-14, (dt, c, eps)
+            inv = 1 / (Decimal(c) * Decimal(c) + Decimal(e32)).sqrt()
+            assert abs(res.inv[0] - float(inv)) <= 1e-15 * float(inv), (dt, c, eps)
+
+
+def pin_unit_gamma_rms(O):
+    """With gamma = 1 the output's mean square is ms / (ms + eps), ms being the
+    input's mean square (exact rational)."""
+    rng = np.random.default_rng(7)
+    for dt in ("f32", "f16", "bf16"):
+        for eps in (1e-6, 0.5):
+            T, H = 3, 200
+            x = _rand_bits(rng, (T, H), dt, scale=0.7)
+            g = bits_of(np.ones(H), dt)
+            res = O.rms_norm(x, g, eps, dt, want_y64=True)
+            xv = lib_decode(x, dt)
+            e32 = Fraction(float(np.float32(eps)))
+            for t in range(T):
+                ms = sum(Fraction(v) ** 2 for v in xv[t]) / H
+                want = float(ms / (ms + e32))
+                got = float(np.mean(res.y64[t] ** 2))
+                assert abs(got - want) <= 1e-13 * want, (dt, eps, t)
+
+
+def pin_scale_invariance(O):
+    """eps = 0: scaling the row by a power of two changes nothing; scaling an
+    f32 row by 3 changes y only by binary64 rounding."""
+    rng = np.random.default_rng(8)
+    for dt, k in (("f32", 2.0 ** 10), ("f16", 4.0), ("bf16", 2.0 ** -20), ("bf16", 2.0 ** 30)):
+        T, H = 4, 123
+        xv = lib_decode(_rand_bits(rng, (T, H), dt), dt)
+        x = bits_of(xv, dt)
+        xk = bits_of(xv * k, dt)
+        g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+        a = O.rms_norm(x, g, 0.0, dt, want_y64=True)
+        b = O.rms_norm(xk, g, 0.0, dt, want_y64=True)
+        assert np.array_equal(a.y, b.y), (dt, k)
+        assert np.allclose(a.inv, b.inv * k, rtol=1e-15, atol=0), (dt, k)
+    # values with 8 significant bits, so that 3x is exact in binary32
+    xv = lib_decode(_rand_bits(rng, (2, 50), "bf16"), "bf16")
+    g = bits_of(np.ones(50), "f32")
+    a = O.rms_norm(bits_of(xv, "f32"), g, 0.0, "f32", want_y64=True)
+    b = O.rms_norm(bits_of(xv * 3.0, "f32"), g, 0.0, "f32", want_y64=True)
+    assert _rel(a.y64, b.y64) < 1e-14
+
+
+def pin_single_element_rows(O):
+    """H = 1: y = x / sqrt(x^2 + eps) * gamma."""
+    getcontext().prec = 50
+    rng = np.random.default_rng(9)
+    for dt in ("f32", "f16", "bf16"):
+        x = _rand_bits(rng, (32, 1), dt, scale=2.0)
+        g = bits_of(np.array([1.25]), dt)
+        res = O.rms_norm(x, g, 1e-3, dt, want_y64=True)
+        xv = lib_decode(x, dt)[:, 0]
+        e32 = Decimal(float(np.float32(1e-3)))
+        want = np.array([float(Decimal(v) / (Decimal(v) ** 2 + e32).sqrt() * Decimal(1.25))
+                         for v in xv])
+        assert _rel(res.y64[:, 0], want) < 1e-14, dt
+
+
+def pin_brute_force_tiny(O):
+    """Tiny fused problems against a from-scratch computation: exact rational
+    residual and sum of squares, 50-digit square root, exact rounding of y."""
+    getcontext().prec = 50
+    rng = np.random.default_rng(10)
+    for dt in ("f32", "f16", "bf16"):
+        T, H = 3, 11
+        x = _rand_bits(rng, (T, H), dt)
+        r = _rand_bits(rng, (T, H), dt, scale=0.5)
+        g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+        eps = 1e-2
+        res = O.fused_add_rms_norm(x, r, g, eps, dt, want_y64=True)
+        xv, rv, gv = lib_decode(x, dt), lib_decode(r, dt), lib_decode(g, dt)
+        e32 = Fraction(float(np.float32(eps)))
+        for t in range(T):
+            h = [Fraction(rn_exact(Fraction(xv[t, i]) + Fraction(rv[t, i]), dt)) for i in range(H)]
+            ss = sum(v * v for v in h)
+            m = ss / H + e32
+            inv = 1 / (Decimal(m.numerator) / Decimal(m.denominator)).sqrt()
+            assert abs(res.inv[t] - float(inv)) <= 1e-15 * float(inv), (dt, t)
+            yd = [Decimal(h[i].numerator) / Decimal(h[i].denominator) * inv * Decimal(gv[i])
+                  for i in range(H)]
+            want64 = np.array([float(v) for v in yd])
+            assert _rel(res.y64[t], want64) < 1e-14, (dt, t)
+            # the stored output is the one rounding of that value (away from
+            # exact ties, which random data does not hit)
+            want_bits = np.array([rn_exact(Fraction(v), dt) for v in want64])
+            assert np.array_equal(lib_decode(res.y[t], dt), want_bits), (dt, t)
+
+
+ALL_PINS = [
+    pin_decode_all_patterns,
+    pin_round_matches_library,
+    pin_round_bf16_nearest,
+    pin_round_exact_rationals,
+    pin_fused_residual_is_exact_rounded_sum,
+    pin_reduce_order_worked_example,
+    pin_reduce_integer_sums,
+    pin_reduce_brute_force_binary32,
+    pin_reduce_special_cases,
+    pin_constant_row,
+    pin_unit_gamma_rms,
+    pin_scale_invariance,
+    pin_single_element_rows,
+    pin_brute_force_tiny,
+]

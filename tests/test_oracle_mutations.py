@@ -1,0 +1,78 @@
+"""The pins catch plausible mistakes in the oracle.
+
+Each case copies the oracle's C source, plants one mistake by a textual edit,
+compiles the copy into a temporary directory and runs every pin against it:
+at least one pin must fail.  The real oracle is never modified.  CPU only.
+"""
+import os
+
+import pytest
+
+import oracle
+from oracle import build as obuild
+
+from pins import ALL_PINS
+
+MUTATIONS = {
+    # wrong divisor in the mean of squares
+    "mean_over_H_minus_1": ("ss / (double)H", "ss / (double)(H - 1)"),
+    # eps dropped from under the root
+    "drop_eps": ("ss / (double)H + (double)j->eps", "ss / (double)H"),
+    # eps outside the root
+    "eps_outside_root": ("1.0 / sqrt(ss / (double)H + (double)j->eps)",
+                         "1.0 / (sqrt(ss / (double)H) + (double)j->eps)"),
+    # weight read at the wrong index
+    "gamma_reversed": ("load_elem(j->dt, j->gamma, i)", "load_elem(j->dt, j->gamma, H - 1 - i)"),
+    # reciprocal used the wrong way round
+    "divide_by_inv": ("(h[i] * inv)", "(h[i] / inv)"),
+    # residual not added
+    "drop_residual": ("acc = acc + (float)load_elem(j->dt, j->residual_in, row + i);", ""),
+    # partial sum kept in binary64 instead of binary32
+    "wide_accumulator": ("float acc = (float)load_elem", "double acc = (float)load_elem"),
+    # wrong stride between partial buffers
+    "partial_stride": ("(int64_t)r * slice + row + i", "(int64_t)r * H + row + i"),
+    # first partial skipped
+    "skip_p0": ("float acc = (float)load_elem(j->dt, j->x, row + i);", "float acc = 0.0f;"),
+    # sum of squares from the unrounded sum
+    "unrounded_h": ("h[i] = round_dt(j->dt, (double)acc);", "h[i] = (double)acc;"),
+    # ties away from zero instead of to even
+    "ties_away": ("nearbyint(ldexp(v, -q))", "round(ldexp(v, -q))"),
+    # truncation instead of rounding
+    "truncate": ("nearbyint(ldexp(v, -q))", "trunc(ldexp(v, -q))"),
+    # f16 subnormal scale off by one
+    "f16_subnormal": ("ldexp((double)m, -24)", "ldexp((double)m, -25)"),
+    # f16 exponent bias off by one
+    "f16_bias": ("ldexp((double)(m + 1024), e - 25)", "ldexp((double)(m + 1024), e - 24)"),
+    # bf16 precision wrong
+    "bf16_precision": ("return round_to_format(v, 8, -126, 127);",
+                       "return round_to_format(v, 9, -126, 127);"),
+    # sign of the squares
+    "square_sign": ("ss += h[i] * h[i];", "ss += h[i] * fabs(h[i]);"),
+    # no overflow to infinity
+    "no_overflow": ("if (fabs(out) > max_finite) return copysign(INFINITY, v);", ""),
+}
+
+
+@pytest.fixture(scope="module")
+def src_text():
+    with open(obuild.SRC) as f:
+        return f.read()
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_mutation(name, src_text, tmp_path):
+    old, new = MUTATIONS[name]
+    assert src_text.count(old) >= 1, f"mutation anchor not found: {old!r}"
+    mutated = src_text.replace(old, new)
+    src = os.path.join(tmp_path, "mut.c")
+    with open(src, "w") as f:
+        f.write(mutated)
+    lib = obuild.compile_source(src, os.path.join(tmp_path, "libmut.so"))
+    O = oracle.Oracle(lib)
+    failed = []
+    for pin in ALL_PINS:
+        try:
+            pin(O)
+        except (AssertionError, RuntimeError, ValueError, OverflowError, ZeroDivisionError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught mutation {name}"
