@@ -1,0 +1,466 @@
+#!/usr/bin/env python
+"""Throughput of the GB300 RMSNorm library: achieved HBM GB/s and rows/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step is one call of the whole path -- reduce the R = 8 partial buffers,
+add the residual, write it back, normalise, weight, write y -- over one batch
+of the headline workload (reduce + residual + RMSNorm, bf16 storage,
+partials [8, 8192, 8192], residual [8192, 8192]).  Its 1.3 GB of inputs are
+ten times the L2, so consecutive steps read cold data without a flush.  The
+other configurations of the method are timed as well (cold L2: a 2 x L2
+buffer is written before each launch) and reported under "per_config".
+
+Rank 0 prints one JSON line.  Under torchrun each rank runs its own replica on
+its own GPU (rows are independent, there is no exchange step): weak scaling,
+value = all ranks' bytes / the slowest rank's time.
+
+``--impl reference`` times the CPU oracle (the method's plain definition, in
+C, binary64) on the host cores over bounded row samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+HEADLINE = "reduce8_bf16_T8192_H8192"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--config-reps", type=int, default=30)
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config table")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; barrier and max only)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def dist_init(world, use_cuda):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend="nccl" if use_cuda else "gloo")
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(v: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+                "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 200 ms while the measurement runs."""
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="rarn_clocks_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + ",".join(CLOCK_FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict | None:
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                cols = [c.strip() for c in line.split(",")]
+                if len(cols) != len(CLOCK_FIELDS):
+                    continue
+                try:
+                    sm.append(float(cols[0]))
+                    smax.append(float(cols[1]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, cols[4:]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def to_device(bits, dtype, device):
+    import numpy as np
+    import torch
+    if dtype == "f32":
+        t = torch.from_numpy(np.ascontiguousarray(bits, np.float32))
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16))
+        t = t.view({"f16": torch.float16, "bf16": torch.bfloat16}[dtype])
+    return t.to(device)
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "residual_add_rmsnorm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            v = json.load(f).get("hbm_gbs")
+        if v:
+            return float(v), "measured"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(workload: str, plan_text: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources for this workload and kernel; else None."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            data = json.load(f)
+    except (OSError, ValueError):
+        return None
+    for e in data.get("entries", []):
+        if (e.get("workload") == workload and e.get("source_sha") == kernel_source_sha()
+                and e.get("plan") == plan_text):
+            return e.get("dram_bytes_per_launch")
+    return None
+
+
+def make_call(w, tensors, rarn):
+    dt_eps = w.eps
+    if w.op == "rms_norm":
+        x, g, y = tensors["x"], tensors["gamma"], tensors["y"]
+        return lambda: rarn.rms_norm(x, g, dt_eps, out=y)
+    if w.op == "fused_add_rms_norm":
+        x, r, g, y = tensors["x"], tensors["residual"], tensors["gamma"], tensors["y"]
+        return lambda: rarn.fused_add_rms_norm(x, r, g, dt_eps, out=y)
+    p, r, g, y = tensors["partials"], tensors["residual"], tensors["gamma"], tensors["y"]
+    return lambda: rarn.reduce_add_rms_norm(p, r, g, dt_eps, out=y)
+
+
+def device_tensors(w, data, device):
+    import torch
+    t = {k: to_device(v, w.dtype, device) for k, v in data.items()}
+    ref = t.get("x", t.get("residual"))
+    t["y"] = torch.empty_like(ref)
+    return t
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_call(w, d, threads=0):
+    import oracle
+    if w.op == "rms_norm":
+        return oracle.rms_norm(d["x"], d["gamma"], w.eps, w.dtype, threads=threads)
+    if w.op == "fused_add_rms_norm":
+        return oracle.fused_add_rms_norm(d["x"], d["residual"], d["gamma"], w.eps, w.dtype,
+                                         threads=threads)
+    return oracle.reduce_add_rms_norm(d["partials"], d["residual"], d["gamma"], w.eps, w.dtype,
+                                      threads=threads)
+
+
+def row_bytes(w) -> int:
+    from residual_add_rmsnorm_gb300 import workloads as W
+    return W.ELEM_SIZE[w.dtype] * w.H * (w.n_inputs + w.n_outputs)
+
+
+def cpu_baseline(w, target_s: float) -> dict:
+    """The oracle as it stands on the host cores, on the first rows of the
+    workload, repeated until about target_s seconds of wall time."""
+    from residual_add_rmsnorm_gb300 import workloads as W
+    rows = min(w.T, 256)
+    d = W.generate(w, rows=(0, rows))
+    t0 = time.perf_counter()
+    r = oracle_call(w, d)
+    one = time.perf_counter() - t0
+    reps = max(1, min(200, int(target_s / max(one, 1e-6))))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        r = oracle_call(w, d)
+    el = time.perf_counter() - t0
+    nbytes = rows * row_bytes(w) * reps
+    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": r.threads, "kind": "oracle",
+            "sample": f"rows 0..{rows - 1} of {w.name}, {reps} repetitions, {el:.1f} s",
+            "rows_per_s": rows * reps / el}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    from residual_add_rmsnorm_gb300 import workloads as W
+    w = W.BY_NAME[args.workload]
+    rows = min(w.T, 128)
+    samples = []
+    nblocks = max(1, w.T // rows)
+    cache = {}
+
+    def sample(i):
+        b = (i % min(nblocks, 4)) * rows
+        if b not in cache:
+            cache[b] = W.generate(w, rows=(b, b + rows))
+        return cache[b]
+
+    threads = 0
+    for i in range(args.warmup):
+        oracle_call(w, sample(i))
+    for i in range(args.steps):
+        d = sample(i)
+        t0 = time.perf_counter()
+        r = oracle_call(w, d)
+        samples.append(time.perf_counter() - t0)
+        threads = r.threads
+    el = sum(samples)
+    nbytes = rows * row_bytes(w) * args.steps
+    value = nbytes / el / 1e9
+    line = {
+        "impl": "reference", "metric": "achieved HBM GB/s (algorithmic bytes / time)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "op": w.op, "storage": w.dtype, "T": w.T, "H": w.H,
+                   "R": w.R, "rows_per_step": rows},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{rows} rows of {w.name} per step"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU measurement
+# ---------------------------------------------------------------------------
+
+def time_steps(call, steps, warmup, stream):
+    import torch
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        call()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)  # ms
+
+
+def time_cold(call, reps, flush, stream):
+    """Median / min of single launches, L2 flushed (flush buffer written)
+    before each one."""
+    import torch
+    times = []
+    for _ in range(3):
+        call()
+    for _ in range(reps):
+        flush.add_(1.0)
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        call()
+        e.record(stream)
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    return statistics.median(times), min(times)
+
+
+def e2e_steps(w, data, tensors, call, steps, device, stream):
+    """Host buffers in, host buffers out: every step copies that step's inputs
+    from pinned host memory, runs the call, copies y and the residual back."""
+    import torch
+    hin = {k: to_device(v, w.dtype, "cpu").pin_memory() for k, v in data.items()}
+    outs = ["y"] + (["residual"] if w.op != "rms_norm" else [])
+    hout = {k: torch.empty_like(tensors[k], device="cpu").pin_memory() for k in outs}
+    h2d = sum(v.numel() * v.element_size() for v in hin.values())
+    d2h = sum(v.numel() * v.element_size() for v in hout.values())
+
+    def step():
+        for k, v in hin.items():
+            tensors[k].copy_(v, non_blocking=True)
+        call()
+        for k, v in hout.items():
+            v.copy_(tensors[k], non_blocking=True)
+
+    ms = time_steps(step, steps, 2, stream)
+    return ms, h2d, d2h
+
+
+def main():
+    args = parse_args()
+    rank, local_rank, world = dist_env()
+    if args.impl == "reference":
+        dist_init(world, use_cuda=False)
+        run_reference(args)
+        return
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    dist_init(world, use_cuda=True)
+
+    import residual_add_rmsnorm_gb300 as rarn
+    from residual_add_rmsnorm_gb300 import build as rbuild
+    from residual_add_rmsnorm_gb300 import workloads as W
+    rbuild.build()
+
+    w = W.BY_NAME[args.workload]
+    data = W.generate(w)
+    tensors = device_tensors(w, data, device)
+    call = make_call(w, tensors, rarn)
+    stream = torch.cuda.current_stream(device)
+    R = w.R if w.op == "reduce_add_rms_norm" else 1
+    plan_text = rarn.plan(w.op, w.T, w.H, R, w.dtype)
+
+    props = torch.cuda.get_device_properties(device)
+    gpu_id = str(getattr(props, "uuid", local_rank))
+    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id)
+    ms = time_steps(call, args.steps, args.warmup, stream)
+    clocks = sampler.stop()
+    ms = max_over_ranks(ms, device)
+    alg = w.algorithmic_bytes()
+    per_launch_s = ms / 1e3 / args.steps
+    value = world * alg * args.steps / (ms / 1e3) / 1e9
+    peak, peak_kind = measured_hbm_peak()
+    achieved = alg / per_launch_s / 1e9
+
+    e2e_ms, h2d, d2h = e2e_steps(w, data, tensors, call, args.e2e_steps, device, stream)
+    e2e_ms = max_over_ranks(e2e_ms, device)
+    e2e_value = world * alg * args.e2e_steps / (e2e_ms / 1e3) / 1e9
+    watchdog = rarn.watchdog(clear=True)
+
+    per_config = {}
+    if not args.no_configs:
+        l2 = int(getattr(props, "L2_cache_size", 128 << 20))
+        flush = torch.zeros(2 * l2 // 4, dtype=torch.float32, device=device)
+        del tensors, call
+        torch.cuda.empty_cache()
+        for cw in W.CONFIGS:
+            cd = W.generate(cw)
+            ct = device_tensors(cw, cd, device)
+            cc = make_call(cw, ct, rarn)
+            med, best = time_cold(cc, args.config_reps, flush, stream)
+            cb = cw.algorithmic_bytes()
+            cR = cw.R if cw.op == "reduce_add_rms_norm" else 1
+            per_config[cw.name] = {
+                "us_median": 1e3 * med, "us_min": 1e3 * best,
+                "gbs": cb / (med / 1e3) / 1e9, "rows_per_s": cw.T / (med / 1e3),
+                "frac_of_peak": cb / (med / 1e3) / 1e9 / peak,
+                "algorithmic_bytes": cb,
+                "plan": rarn.plan(cw.op, cw.T, cw.H, cR, cw.dtype)}
+            del ct, cc, cd
+            torch.cuda.empty_cache()
+        if rarn.watchdog(clear=True):
+            watchdog = 1
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": "achieved HBM GB/s (algorithmic bytes / time)",
+        "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "op": w.op, "storage": w.dtype, "T": w.T, "H": w.H,
+                   "R": w.R, "eps": w.eps, "rows_per_s": world * w.T * args.steps / (ms / 1e3),
+                   "l2": "inputs larger than L2 (no flush between steps)",
+                   "parallelism": "replicas" if world > 1 else "single",
+                   "plan": plan_text},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic(w.name, plan_text),
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes_per_launch": alg},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+        "watchdog": watchdog,
+        "per_config": per_config,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

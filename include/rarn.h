@@ -1,0 +1,181 @@
+/*
+ * rarn.h -- C ABI of the GB300 (sm_103a) row-wise RMSNorm library.
+ *
+ * Three operations on row-major [T, H] problems, one row per token:
+ *
+ *   rarn_rms_norm             y = x * rsqrt(mean(x^2) + eps) * gamma
+ *   rarn_fused_add_rms_norm   h = x + residual; residual <- h; y = rmsnorm(h)
+ *   rarn_reduce_add_rms_norm  h = p_0 + ... + p_{R-1} + residual;
+ *                             residual <- h; y = rmsnorm(h)
+ *
+ * Definitions followed (page title, section):
+ *   "RMSNorm kernel", 1 Background and 2 Analytics & Implementation
+ *   (Abstraction): y_i = x_i * gamma_i / RMS(x), RMS taken over the last
+ *   (hidden) dimension only; the shape [..., hidden] is flattened to
+ *   [rows, hidden].
+ *   "Tokenweave fused-RMSNorm-AR kernel", Code walkthrough: the first pass
+ *   reduces the partial-sum buffers, adds the residual, writes the sum back as
+ *   the residual and accumulates the squares of that stored value in fp32; the
+ *   reciprocal RMS is rsqrt(variance / hidden_size + eps); the second pass
+ *   scales by it and by the weight.
+ *
+ * Arithmetic contract:
+ *   - h is summed in binary32 in the fixed order p_0, p_1, ..., p_{R-1}, then
+ *     the residual, and rounded once (nearest-even) to the storage type.  The
+ *     updated residual is that rounded h, bit for bit.
+ *   - The sum of squares of the rounded h is accumulated in binary32; the
+ *     reciprocal RMS is rsqrtf(ss / H + eps).
+ *   - y_i = (h_i * inv) * gamma_i in binary32, rounded once to the storage
+ *     type.  fp32 storage: within 1e-5 relative of the exact value; fp16 and
+ *     bf16: within 2 units in the last place.
+ *   - Results are deterministic: the same inputs give the same bits on every
+ *     call.
+ *   - Limitation: the sum of squares is binary32, so a row whose sum of
+ *     squares exceeds FLT_MAX (|h| around 1e19 and above for H = 4096)
+ *     normalises to zero.
+ *
+ * Common conventions for every compute entry point:
+ *   - Pointers are DEVICE pointers owned by the caller (y, x, partials,
+ *     residual, gamma).  The library allocates no memory and keeps no pointer
+ *     after the call returns.
+ *   - Layout: dense row-major.  x, residual and y are [T, H] with row stride H
+ *     elements; partials is [R, T, H], partial r starting at element r*T*H;
+ *     gamma is [H].  All share one storage type `dt`.  eps is binary32.
+ *   - Alignment: any element-aligned pointer is accepted.  When every pointer
+ *     is 16-byte aligned and H * sizeof(dt) is a multiple of 16 the 128-bit
+ *     vector kernels run; otherwise a scalar kernel does.
+ *   - Aliasing: y may equal x (rms_norm, fused) or partials (reduce: y then
+ *     overwrites partial 0).  Any other overlap between an output (y,
+ *     residual) and any other buffer returns RARN_ERR_ALIAS.
+ *   - Streams: the work is enqueued on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream) on the current device and the call returns
+ *     without synchronising.  Results are ready when the stream reaches that
+ *     point.
+ *   - Errors: argument errors are returned synchronously, before any work is
+ *     enqueued (nothing is written).  T == 0 is a no-op returning RARN_OK.  A
+ *     failed launch returns RARN_ERR_CUDA; rarn_last_cuda_error() then gives
+ *     the CUDA error code.  No C++ exception crosses this interface.
+ */
+#ifndef RARN_H
+#define RARN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rarn_dtype {
+    RARN_F32 = 0,  /* IEEE binary32 */
+    RARN_F16 = 1,  /* IEEE binary16 */
+    RARN_BF16 = 2  /* bfloat16 */
+} rarn_dtype;
+
+typedef enum rarn_status {
+    RARN_OK = 0,
+    RARN_ERR_INVALID_ARG = 1, /* null pointer with T > 0, T < 0, H <= 0, R < 1,
+                                 eps negative or NaN, unknown dtype or op */
+    RARN_ERR_UNSUPPORTED = 2, /* sizes beyond the limits below, or a forced
+                                 kernel path that cannot run this shape */
+    RARN_ERR_ALIAS = 3,       /* outputs overlap inputs other than as allowed */
+    RARN_ERR_CUDA = 4         /* a CUDA runtime call or launch failed */
+} rarn_status;
+
+/* Size limits: 1 <= H <= RARN_MAX_H, 0 <= T <= RARN_MAX_T, 1 <= R <= RARN_MAX_R. */
+#define RARN_MAX_H (1 << 24)
+#define RARN_MAX_T ((int64_t)1 << 40)
+#define RARN_MAX_R 64
+
+/* Operation codes used by the planning query. */
+typedef enum rarn_op {
+    RARN_OP_RMS_NORM = 0,
+    RARN_OP_FUSED_ADD_RMS_NORM = 1,
+    RARN_OP_REDUCE_ADD_RMS_NORM = 2
+} rarn_op;
+
+/* Kernel families.  RARN_PATH_AUTO picks per shape; the others force one
+ * family (for tests and measurements) and return RARN_ERR_UNSUPPORTED from a
+ * compute call whose shape that family cannot run. */
+typedef enum rarn_path {
+    RARN_PATH_AUTO = 0,
+    RARN_PATH_ROWS = 1,    /* a warp or a CTA per row, row held in registers;
+                              a two-pass CTA kernel when the row is too long */
+    RARN_PATH_STREAM = 2,  /* persistent CTAs, one per SM, fed by TMA bulk
+                              copies into a shared-memory pipeline */
+    RARN_PATH_CLUSTER = 3  /* a thread-block cluster per row, sum of squares
+                              combined through distributed shared memory */
+} rarn_path;
+
+/*
+ * y[T,H] = RMSNorm(x[T,H]) * gamma[H].
+ * ("RMSNorm kernel", 1 Background; 2 Abstraction.)
+ * In: x, gamma.  Out: y (may equal x).
+ */
+rarn_status rarn_rms_norm(void *y, const void *x, const void *gamma, int64_t T, int64_t H,
+                          float eps, rarn_dtype dt, void *stream);
+
+/*
+ * h = x + residual (binary32 add, one rounding); residual <- h;
+ * y = RMSNorm(h) * gamma.
+ * ("Tokenweave fused-RMSNorm-AR kernel", Code walkthrough, with one input
+ * buffer in place of the cross-GPU reduction.)
+ * In: x, gamma.  In/out: residual.  Out: y (may equal x, not residual).
+ */
+rarn_status rarn_fused_add_rms_norm(void *y, const void *x, void *residual, const void *gamma,
+                                    int64_t T, int64_t H, float eps, rarn_dtype dt,
+                                    void *stream);
+
+/*
+ * h = ((p_0 + p_1) + ... + p_{R-1}) + residual, each add in binary32, one
+ * rounding; residual <- h; y = RMSNorm(h) * gamma.
+ * ("Tokenweave fused-RMSNorm-AR kernel", Code walkthrough: the reduce of the
+ * partial buffers, here R buffers in this GPU's memory, summed in a fixed
+ * order.)
+ * In: partials [R,T,H], gamma.  In/out: residual.  Out: y (may equal
+ * partials, i.e. overwrite partial 0).
+ */
+rarn_status rarn_reduce_add_rms_norm(void *y, const void *partials, int32_t R, void *residual,
+                                     const void *gamma, int64_t T, int64_t H, float eps,
+                                     rarn_dtype dt, void *stream);
+
+/* Static text for a status code. */
+const char *rarn_status_string(rarn_status s);
+
+/* CUDA error code (cudaError_t as int) of the last RARN_ERR_CUDA returned on
+ * the calling thread; 0 if none. */
+int rarn_last_cuda_error(void);
+
+/* Select the kernel family for later calls from any thread (process-wide).
+ * Returns RARN_ERR_INVALID_ARG for an unknown value. */
+rarn_status rarn_set_path(rarn_path p);
+rarn_path rarn_get_path(void);
+
+/*
+ * Describe the kernel the current path setting would launch for a problem,
+ * as text such as "stream smem=...", without launching anything.
+ * `vec_ok` says whether every pointer is 16-byte aligned; `num_sms` is the
+ * device's SM count (if <= 0 the current device is queried).  Writes a
+ * NUL-terminated string of at most `cap` bytes to `out`.  Pure host logic when
+ * num_sms > 0.
+ */
+rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt, int vec_ok,
+                      int num_sms, char *out, size_t cap);
+
+/*
+ * Watchdog word of the current device.  Kernels that wait on shared-memory
+ * barriers give up after a bounded time, set a bit here and return without
+ * hanging; their outputs are then not valid.  Bit 0: a consumer wait timed
+ * out; bit 1: a producer wait timed out.  Synchronises the device.  If
+ * `clear` is nonzero the word is reset to 0 after reading.
+ */
+rarn_status rarn_watchdog(uint32_t *flags, int clear);
+
+/* ABI version: (major << 16) | minor. */
+int rarn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RARN_H */

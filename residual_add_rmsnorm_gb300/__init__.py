@@ -1,0 +1,217 @@
+"""GB300 (sm_103a) row-wise RMSNorm: plain, fused residual-add, and
+reduce + residual-add.
+
+Thin Python binding over the C ABI in ``include/rarn.h`` (``librarn.so``,
+built in-tree by ``residual_add_rmsnorm_gb300.build``).  This module only
+checks and marshals arguments -- tensors to device pointers, the current CUDA
+stream -- and raises on a non-OK status.  Every step of the computation runs
+in the library's CUDA kernels; there is no CPU or PyTorch fallback: if the
+library is missing or fails to load, every call raises.
+
+    y = rms_norm(x, gamma, eps)                         # x: [..., H]
+    y = fused_add_rms_norm(x, residual, gamma, eps)     # residual updated in place
+    y = reduce_add_rms_norm(partials, residual, gamma, eps)   # partials: [R, ..., H]
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+__all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "RarnError", "library",
+           "set_path", "get_path", "plan", "watchdog", "PATHS", "DTYPE_CODES"]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
+
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
+OP_CODES = {"rms_norm": 0, "fused_add_rms_norm": 1, "reduce_add_rms_norm": 2}
+PATHS = {"auto": 0, "rows": 1, "stream": 2, "cluster": 3}
+STATUS = {0: "RARN_OK", 1: "RARN_ERR_INVALID_ARG", 2: "RARN_ERR_UNSUPPORTED",
+          3: "RARN_ERR_ALIAS", 4: "RARN_ERR_CUDA"}
+
+
+class RarnError(RuntimeError):
+    """A non-OK status from the C ABI."""
+
+    def __init__(self, status: int, what: str, cuda_error: int = 0):
+        self.status = status
+        self.cuda_error = cuda_error
+        msg = f"{what}: {STATUS.get(status, status)}"
+        if status == 4:
+            msg += f" (cudaError {cuda_error})"
+        super().__init__(msg)
+
+
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """The loaded ``librarn.so`` with its argument types declared."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -m residual_add_rmsnorm_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, i32, f32, c_int = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32,
+                                ctypes.c_float, ctypes.c_int)
+    lib.rarn_rms_norm.argtypes = [vp, vp, vp, i64, i64, f32, c_int, vp]
+    lib.rarn_fused_add_rms_norm.argtypes = [vp, vp, vp, vp, i64, i64, f32, c_int, vp]
+    lib.rarn_reduce_add_rms_norm.argtypes = [vp, vp, i32, vp, vp, i64, i64, f32, c_int, vp]
+    for f in (lib.rarn_rms_norm, lib.rarn_fused_add_rms_norm, lib.rarn_reduce_add_rms_norm):
+        f.restype = c_int
+    lib.rarn_status_string.argtypes = [c_int]
+    lib.rarn_status_string.restype = ctypes.c_char_p
+    lib.rarn_last_cuda_error.argtypes = []
+    lib.rarn_last_cuda_error.restype = c_int
+    lib.rarn_set_path.argtypes = [c_int]
+    lib.rarn_set_path.restype = c_int
+    lib.rarn_get_path.argtypes = []
+    lib.rarn_get_path.restype = c_int
+    lib.rarn_plan.argtypes = [c_int, i64, i64, i32, c_int, c_int, c_int, ctypes.c_char_p,
+                              ctypes.c_size_t]
+    lib.rarn_plan.restype = c_int
+    lib.rarn_watchdog.argtypes = [ctypes.POINTER(ctypes.c_uint32), c_int]
+    lib.rarn_watchdog.restype = c_int
+    lib.rarn_version.argtypes = []
+    lib.rarn_version.restype = c_int
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise RarnError(status, what, library().rarn_last_cuda_error() if status == 4 else 0)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    codes = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+    if t.dtype not in codes:
+        raise TypeError(f"unsupported dtype {t.dtype}: expected float32, float16 or bfloat16")
+    return codes[t.dtype]
+
+
+def _check_tensor(name, t, dtype, device):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream(device):
+    import torch
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def rms_norm(x, gamma, eps: float, out=None):
+    """y = x * rsqrt(mean(x^2, -1) + eps) * gamma over the last dimension.
+
+    x: [..., H] CUDA tensor (float32 / float16 / bfloat16, contiguous);
+    gamma: [H].  ``out`` may be given (it may be ``x`` itself).  Runs on the
+    current stream of x's device.
+    """
+    import torch
+    H = x.shape[-1]
+    _check_tensor("x", x, x.dtype, x.device)
+    _check_tensor("gamma", gamma, x.dtype, x.device)
+    if gamma.numel() != H:
+        raise ValueError(f"gamma has {gamma.numel()} elements, expected {H}")
+    y = torch.empty_like(x) if out is None else out
+    _check_tensor("out", y, x.dtype, x.device)
+    if y.shape != x.shape:
+        raise ValueError("out must have the shape of x")
+    T = x.numel() // H if H else 0
+    with torch.cuda.device(x.device):
+        _check(library().rarn_rms_norm(y.data_ptr(), x.data_ptr(), gamma.data_ptr(), T, H,
+                                       float(eps), _dtype_code(x), _stream(x.device)),
+               "rarn_rms_norm")
+    return y
+
+
+def fused_add_rms_norm(x, residual, gamma, eps: float, out=None):
+    """residual <- x + residual (in place); returns RMSNorm(residual) * gamma.
+
+    x, residual: [..., H]; gamma: [H]; all one dtype, contiguous, on one CUDA
+    device.  ``out`` may be ``x``.
+    """
+    import torch
+    H = x.shape[-1]
+    for n, t in (("x", x), ("residual", residual), ("gamma", gamma)):
+        _check_tensor(n, t, x.dtype, x.device)
+    if residual.shape != x.shape:
+        raise ValueError("residual must have the shape of x")
+    if gamma.numel() != H:
+        raise ValueError(f"gamma has {gamma.numel()} elements, expected {H}")
+    y = torch.empty_like(x) if out is None else out
+    _check_tensor("out", y, x.dtype, x.device)
+    if y.shape != x.shape:
+        raise ValueError("out must have the shape of x")
+    T = x.numel() // H if H else 0
+    with torch.cuda.device(x.device):
+        _check(library().rarn_fused_add_rms_norm(
+            y.data_ptr(), x.data_ptr(), residual.data_ptr(), gamma.data_ptr(), T, H, float(eps),
+            _dtype_code(x), _stream(x.device)), "rarn_fused_add_rms_norm")
+    return y
+
+
+def reduce_add_rms_norm(partials, residual, gamma, eps: float, out=None):
+    """residual <- ((p_0 + p_1) + ... + p_{R-1}) + residual (binary32, one
+    rounding, in place); returns RMSNorm(residual) * gamma.
+
+    partials: [R, ..., H]; residual: [..., H]; gamma: [H].  ``out`` may be
+    ``partials[0]``.
+    """
+    import torch
+    R = partials.shape[0]
+    H = residual.shape[-1]
+    for n, t in (("partials", partials), ("residual", residual), ("gamma", gamma)):
+        _check_tensor(n, t, residual.dtype, residual.device)
+    if tuple(partials.shape[1:]) != tuple(residual.shape):
+        raise ValueError("partials must have shape [R, *residual.shape]")
+    if gamma.numel() != H:
+        raise ValueError(f"gamma has {gamma.numel()} elements, expected {H}")
+    y = torch.empty_like(residual) if out is None else out
+    _check_tensor("out", y, residual.dtype, residual.device)
+    if y.shape != residual.shape:
+        raise ValueError("out must have the shape of residual")
+    T = residual.numel() // H if H else 0
+    with torch.cuda.device(residual.device):
+        _check(library().rarn_reduce_add_rms_norm(
+            y.data_ptr(), partials.data_ptr(), R, residual.data_ptr(), gamma.data_ptr(), T, H,
+            float(eps), _dtype_code(residual), _stream(residual.device)),
+            "rarn_reduce_add_rms_norm")
+    return y
+
+
+def set_path(name: str) -> None:
+    """Force a kernel family ('auto', 'rows', 'stream', 'cluster'), process-wide."""
+    _check(library().rarn_set_path(PATHS[name]), "rarn_set_path")
+
+
+def get_path() -> str:
+    code = library().rarn_get_path()
+    return {v: k for k, v in PATHS.items()}[code]
+
+
+def plan(op: str, T: int, H: int, R: int, dtype: str, vec_ok: bool = True,
+         num_sms: int = 0) -> str:
+    """The kernel the current path setting would launch for a problem."""
+    buf = ctypes.create_string_buffer(256)
+    st = library().rarn_plan(OP_CODES[op], T, H, R, DTYPE_CODES[dtype], int(vec_ok), num_sms,
+                             buf, 256)
+    if st not in (0, 2):
+        _check(st, "rarn_plan")
+    return buf.value.decode()
+
+
+def watchdog(clear: bool = True) -> int:
+    """Read (and by default clear) the current device's watchdog word."""
+    v = ctypes.c_uint32(0)
+    _check(library().rarn_watchdog(ctypes.byref(v), int(clear)), "rarn_watchdog")
+    return v.value

@@ -1,0 +1,291 @@
+// api.cu -- the C ABI: argument checks, kernel planning, dispatch by dtype.
+//
+// Every entry point validates its arguments before touching the GPU, picks a
+// kernel family from the shape (or the forced path), and enqueues exactly one
+// kernel launch on the caller's stream.  No memory is allocated.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/rarn.h"
+#include "plan.h"
+
+using namespace rarn;
+
+// Watchdog word: kernels with bounded waits record a timeout here.
+__device__ unsigned int g_rarn_watchdog = 0;
+
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+std::atomic<int> g_path{RARN_PATH_AUTO};
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool ready = false;
+    int num_sms = 0;
+    int max_smem_optin = 0;
+    unsigned int *watchdog = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+rarn_status cuda_fail(cudaError_t e) {
+    t_last_cuda_error = (int)e;
+    return RARN_ERR_CUDA;
+}
+
+// Device properties and the watchdog word's device address, once per device.
+rarn_status device_info(DeviceInfo **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev < 0 || dev >= kMaxDevices) return RARN_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (!d.ready) {
+        int sms = 0, smem = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return cuda_fail(e);
+        if ((e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+            cudaSuccess)
+            return cuda_fail(e);
+        void *wd = nullptr;
+        if ((e = cudaGetSymbolAddress(&wd, g_rarn_watchdog)) != cudaSuccess) return cuda_fail(e);
+        d.num_sms = sms;
+        d.max_smem_optin = smem;
+        d.watchdog = static_cast<unsigned int *>(wd);
+        d.ready = true;
+    }
+    *out = &d;
+    return RARN_OK;
+}
+
+int elem_size(rarn_dtype dt) { return dt == RARN_F32 ? 4 : 2; }
+
+int pow2_at_least(int64_t v) {
+    int p = 1;
+    while (p < v) p <<= 1;
+    return p;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int round_up(int64_t a, int64_t b) { return (int)(ceil_div(a, b) * b); }
+
+// Register-staged kernels: a warp per row for short rows, a CTA per row up to
+// the register budget, two passes beyond it.
+Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
+    Plan pl;
+    pl.vec = vec;
+    const int epv = vec ? 16 / s : 1;
+    const int64_t n = H / epv;  // packs (vec) or elements (scalar) per row
+    const int resident_threads = 2048;
+    if (vec && n <= 128) {
+        pl.kind = KIND_WARP;
+        pl.per_thread = n <= 32 ? 1 : n <= 64 ? 2 : 4;
+        pl.block = 256;
+        const int64_t rows_per_cta = pl.block / 32;
+        pl.grid = (int)std::min<int64_t>(ceil_div(T, rows_per_cta),
+                                          (int64_t)num_sms * (resident_threads / pl.block));
+        return pl;
+    }
+    // values per thread: aim at 256 threads per row, powers of two
+    const int max_pt = vec ? 8 : 16;
+    int pt = std::min(max_pt, pow2_at_least(ceil_div(n, 256)));
+    while (pt < max_pt && ceil_div(n, pt) > rows_max_block(pt * epv)) pt <<= 1;
+    if (ceil_div(n, pt) > rows_max_block(pt * epv)) {
+        pl.kind = KIND_TWO_PASS;
+        pl.per_thread = 1;
+        pl.block = 1024;
+    } else {
+        pl.kind = KIND_CTA;
+        pl.per_thread = pt;
+        pl.block = round_up(ceil_div(n, pt), 32);
+    }
+    pl.grid = (int)std::min<int64_t>(T, (int64_t)num_sms * std::max(1, resident_threads / pl.block));
+    return pl;
+}
+
+Plan make_plan(int op, int64_t T, int64_t H, int R, rarn_dtype dt, bool vec, int num_sms,
+               int path) {
+    (void)R;
+    const int s = elem_size(dt);
+    switch (path) {
+    case RARN_PATH_AUTO:
+    case RARN_PATH_ROWS: return plan_rows(op, T, H, s, vec, num_sms);
+    default: return Plan{};
+    }
+}
+
+const char *kind_name(int k) {
+    switch (k) {
+    case KIND_WARP: return "rows.warp";
+    case KIND_CTA: return "rows.cta";
+    case KIND_TWO_PASS: return "rows.two_pass";
+    case KIND_STREAM: return "stream";
+    case KIND_CLUSTER: return "cluster";
+    default: return "none";
+    }
+}
+
+bool overlaps(const void *a, int64_t na, const void *b, int64_t nb) {
+    const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shared body of the three entry points.
+rarn_status run(int op, void *y, const void *src, int32_t R, void *residual, const void *gamma,
+                int64_t T, int64_t H, float eps, rarn_dtype dt, void *stream) {
+    if (dt != RARN_F32 && dt != RARN_F16 && dt != RARN_BF16) return RARN_ERR_INVALID_ARG;
+    if (T < 0 || H <= 0 || !(eps >= 0.f) || std::isinf(eps)) return RARN_ERR_INVALID_ARG;
+    if (op == OP_REDUCE && R < 1) return RARN_ERR_INVALID_ARG;
+    if (H > RARN_MAX_H || T > RARN_MAX_T || R > RARN_MAX_R) return RARN_ERR_UNSUPPORTED;
+    if (T == 0) return RARN_OK;
+    if (!y || !src || !gamma || (op != OP_PLAIN && !residual)) return RARN_ERR_INVALID_ARG;
+
+    const int s = elem_size(dt);
+    const int64_t row_bytes = H * s;
+    const int64_t mat = T * row_bytes;  // one [T, H] buffer
+    const int nsrc = op == OP_REDUCE ? R : 1;
+    // y may coincide exactly with x / partial 0; nothing else may overlap an output
+    const bool y_is_src = (y == src);
+    if (!y_is_src && overlaps(y, mat, src, mat * nsrc)) return RARN_ERR_ALIAS;
+    if (y_is_src && nsrc > 1 && overlaps(y, mat, static_cast<const char *>(src) + mat,
+                                         mat * (nsrc - 1)))
+        return RARN_ERR_ALIAS;
+    if (overlaps(y, mat, gamma, row_bytes)) return RARN_ERR_ALIAS;
+    if (op != OP_PLAIN) {
+        if (overlaps(residual, mat, y, mat) || overlaps(residual, mat, src, mat * nsrc) ||
+            overlaps(residual, mat, gamma, row_bytes))
+            return RARN_ERR_ALIAS;
+    }
+
+    const bool vec = aligned16(y) && aligned16(src) && aligned16(gamma) &&
+                     (op == OP_PLAIN || aligned16(residual)) && (row_bytes % 16 == 0);
+
+    DeviceInfo *d = nullptr;
+    rarn_status st = device_info(&d);
+    if (st != RARN_OK) return st;
+
+    const Plan pl = make_plan(op, T, H, R, dt, vec, d->num_sms, g_path.load());
+    if (pl.kind == KIND_NONE) return RARN_ERR_UNSUPPORTED;
+
+    Problem p{};
+    p.y = y;
+    p.src = src;
+    p.residual = residual;
+    p.gamma = gamma;
+    p.T = T;
+    p.H = H;
+    p.slice = T * H;
+    p.R = op == OP_PLAIN ? 0 : (op == OP_FUSED ? 1 : R);
+    p.op = op;
+    p.eps = eps;
+    p.watchdog = d->watchdog;
+
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorInvalidValue;
+    switch (pl.kind) {
+    case KIND_WARP:
+    case KIND_CTA:
+    case KIND_TWO_PASS:
+        switch (dt) {
+        case RARN_F32: e = launch_rows<float>(p, pl, cs); break;
+        case RARN_F16: e = launch_rows<__half>(p, pl, cs); break;
+        case RARN_BF16: e = launch_rows<__nv_bfloat16>(p, pl, cs); break;
+        }
+        break;
+    default: return RARN_ERR_UNSUPPORTED;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
+    return RARN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+rarn_status rarn_rms_norm(void *y, const void *x, const void *gamma, int64_t T, int64_t H,
+                          float eps, rarn_dtype dt, void *stream) {
+    return run(OP_PLAIN, y, x, 0, nullptr, gamma, T, H, eps, dt, stream);
+}
+
+rarn_status rarn_fused_add_rms_norm(void *y, const void *x, void *residual, const void *gamma,
+                                    int64_t T, int64_t H, float eps, rarn_dtype dt,
+                                    void *stream) {
+    return run(OP_FUSED, y, x, 1, residual, gamma, T, H, eps, dt, stream);
+}
+
+rarn_status rarn_reduce_add_rms_norm(void *y, const void *partials, int32_t R, void *residual,
+                                     const void *gamma, int64_t T, int64_t H, float eps,
+                                     rarn_dtype dt, void *stream) {
+    return run(OP_REDUCE, y, partials, R, residual, gamma, T, H, eps, dt, stream);
+}
+
+const char *rarn_status_string(rarn_status s) {
+    switch (s) {
+    case RARN_OK: return "ok";
+    case RARN_ERR_INVALID_ARG: return "invalid argument";
+    case RARN_ERR_UNSUPPORTED: return "unsupported size or kernel path";
+    case RARN_ERR_ALIAS: return "output overlaps an input";
+    case RARN_ERR_CUDA: return "CUDA error";
+    default: return "unknown status";
+    }
+}
+
+int rarn_last_cuda_error(void) { return t_last_cuda_error; }
+
+rarn_status rarn_set_path(rarn_path p) {
+    if (p < RARN_PATH_AUTO || p > RARN_PATH_CLUSTER) return RARN_ERR_INVALID_ARG;
+    g_path.store(p);
+    return RARN_OK;
+}
+
+rarn_path rarn_get_path(void) { return static_cast<rarn_path>(g_path.load()); }
+
+rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt, int vec_ok,
+                      int num_sms, char *out, size_t cap) {
+    if (!out || cap == 0) return RARN_ERR_INVALID_ARG;
+    if (op < RARN_OP_RMS_NORM || op > RARN_OP_REDUCE_ADD_RMS_NORM) return RARN_ERR_INVALID_ARG;
+    if (dt != RARN_F32 && dt != RARN_F16 && dt != RARN_BF16) return RARN_ERR_INVALID_ARG;
+    if (T < 0 || H <= 0 || (op == RARN_OP_REDUCE_ADD_RMS_NORM && R < 1))
+        return RARN_ERR_INVALID_ARG;
+    if (num_sms <= 0) {
+        DeviceInfo *d = nullptr;
+        rarn_status st = device_info(&d);
+        if (st != RARN_OK) return st;
+        num_sms = d->num_sms;
+    }
+    const bool vec = vec_ok && (H * elem_size(dt)) % 16 == 0;
+    const Plan pl = make_plan((int)op, T, H, R, dt, vec, num_sms, g_path.load());
+    snprintf(out, cap, "%s %s per_thread=%d block=%d grid=%d cluster=%d smem=%d stages=%d chunk=%d",
+             kind_name(pl.kind), pl.vec ? "vec16" : "scalar", pl.per_thread, pl.block, pl.grid,
+             pl.cluster, pl.smem, pl.stages, pl.chunk);
+    return pl.kind == KIND_NONE ? RARN_ERR_UNSUPPORTED : RARN_OK;
+}
+
+rarn_status rarn_watchdog(uint32_t *flags, int clear) {
+    if (!flags) return RARN_ERR_INVALID_ARG;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e);
+    unsigned int v = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_rarn_watchdog, sizeof(v))) != cudaSuccess)
+        return cuda_fail(e);
+    *flags = v;
+    if (clear) {
+        const unsigned int zero = 0;
+        if ((e = cudaMemcpyToSymbol(g_rarn_watchdog, &zero, sizeof(zero))) != cudaSuccess)
+            return cuda_fail(e);
+    }
+    return RARN_OK;
+}
+
+int rarn_version(void) { return (1 << 16) | 0; }
+
+}  // extern "C"

@@ -1,0 +1,177 @@
+// common.cuh -- problem description and device helpers shared by the kernels.
+//
+// Storage types: float (binary32), __half (binary16), __nv_bfloat16.  Every
+// kernel moves rows in 16-byte vectors ("packs") of EPV elements when the row
+// and every base pointer are 16-byte aligned, and element by element
+// otherwise.  All arithmetic is binary32.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rarn {
+
+enum Op : int { OP_PLAIN = 0, OP_FUSED = 1, OP_REDUCE = 2 };
+
+// One call's arguments, passed to every kernel by value.
+struct Problem {
+    void *y;               // [T, H] output
+    const void *src;       // plain / fused: x [T, H]; reduce: partials [R, T, H]
+    void *residual;        // [T, H] in/out (fused, reduce); unused for plain
+    const void *gamma;     // [H]
+    int64_t T, H;
+    int64_t slice;         // elements between consecutive partial buffers (T * H)
+    int R;                 // partial buffers (reduce), 1 (fused), 0 (plain)
+    int op;                // Op
+    float eps;
+    unsigned int *watchdog;  // device word for bounded-wait failures
+};
+
+// ---------------------------------------------------------------------------
+// Storage-type traits: 16-byte packs <-> binary32, one rounding on the way out
+// ---------------------------------------------------------------------------
+
+template <typename T>
+struct DT;
+
+template <>
+struct DT<float> {
+    static constexpr int EPV = 4;
+    __device__ __forceinline__ static float to_f(float v) { return v; }
+    __device__ __forceinline__ static float from_f(float v) { return v; }
+    __device__ __forceinline__ static void unpack(const uint4 &p, float (&f)[EPV]) {
+        f[0] = __uint_as_float(p.x);
+        f[1] = __uint_as_float(p.y);
+        f[2] = __uint_as_float(p.z);
+        f[3] = __uint_as_float(p.w);
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&f)[EPV]) {
+        return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]),
+                          __float_as_uint(f[3]));
+    }
+    __device__ __forceinline__ static float round(float v) { return v; }
+};
+
+template <>
+struct DT<__half> {
+    static constexpr int EPV = 8;
+    __device__ __forceinline__ static float to_f(__half v) { return __half2float(v); }
+    __device__ __forceinline__ static __half from_f(float v) { return __float2half_rn(v); }
+    __device__ __forceinline__ static float2 w2f(uint32_t w) {
+        __half2 h = *reinterpret_cast<__half2 *>(&w);
+        return __half22float2(h);
+    }
+    __device__ __forceinline__ static uint32_t f2w(float a, float b) {
+        __half2 h = __floats2half2_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ __forceinline__ static void unpack(const uint4 &p, float (&f)[EPV]) {
+        float2 a = w2f(p.x), b = w2f(p.y), c = w2f(p.z), d = w2f(p.w);
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+        f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&f)[EPV]) {
+        return make_uint4(f2w(f[0], f[1]), f2w(f[2], f[3]), f2w(f[4], f[5]), f2w(f[6], f[7]));
+    }
+    __device__ __forceinline__ static float round(float v) {
+        return __half2float(__float2half_rn(v));
+    }
+};
+
+template <>
+struct DT<__nv_bfloat16> {
+    static constexpr int EPV = 8;
+    __device__ __forceinline__ static float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+    __device__ __forceinline__ static __nv_bfloat16 from_f(float v) {
+        return __float2bfloat16_rn(v);
+    }
+    // bf16 -> f32 is exact: the pattern moves to the upper half of the word.
+    __device__ __forceinline__ static float2 w2f(uint32_t w) {
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+    }
+    __device__ __forceinline__ static uint32_t f2w(float a, float b) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ __forceinline__ static void unpack(const uint4 &p, float (&f)[EPV]) {
+        float2 a = w2f(p.x), b = w2f(p.y), c = w2f(p.z), d = w2f(p.w);
+        f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+        f[4] = c.x; f[5] = c.y; f[6] = d.x; f[7] = d.y;
+    }
+    __device__ __forceinline__ static uint4 pack(const float (&f)[EPV]) {
+        return make_uint4(f2w(f[0], f[1]), f2w(f[2], f[3]), f2w(f[4], f[5]), f2w(f[6], f[7]));
+    }
+    __device__ __forceinline__ static float round(float v) {
+        return __bfloat162float(__float2bfloat16_rn(v));
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Global memory access with cache hints (inline PTX)
+// ---------------------------------------------------------------------------
+
+// Streaming load: data read once (x, partials, residual).  Coherent, so it is
+// also correct for buffers this kernel writes (residual, y aliasing x).
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Read-only, reused load (gamma: every row reads it).
+__device__ __forceinline__ uint4 ld_keep(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_global(void *p, const uint4 &v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
+template <typename T>
+__device__ __forceinline__ float ld_elem(const void *base, int64_t i) {
+    return DT<T>::to_f(reinterpret_cast<const T *>(base)[i]);
+}
+
+template <typename T>
+__device__ __forceinline__ void st_elem(void *base, int64_t i, float v) {
+    reinterpret_cast<T *>(base)[i] = DT<T>::from_f(v);
+}
+
+// ---------------------------------------------------------------------------
+// Reductions (xor butterfly within a warp; warp totals combined through
+// shared memory).  "Tokenweave fused-RMSNorm-AR kernel", blockReduceSum, and
+// "Block All Reduce", warp_reduce_sum_f32 / block_all_reduce: the same
+// two-stage scheme.
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v += __shfl_xor_sync(0xffffffffu, v, m);
+    return v;
+}
+
+// Sum of v over the whole CTA, returned to every thread.  `red` holds one
+// float per warp; callers alternate between two such buffers on consecutive
+// rows so that one __syncthreads per row suffices.  Deterministic: fixed
+// order for a fixed block size.
+__device__ __forceinline__ float block_sum(float v, float *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    v = warp_sum(v);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float s = lane < nwarps ? red[lane] : 0.f;
+    return warp_sum(s);
+}
+
+}  // namespace rarn

@@ -1,0 +1,370 @@
+// rows.cuh -- register-staged row kernels: a warp or a CTA per row.
+//
+// Each row is read once from HBM.  The first pass loads the row's input
+// streams (x; or the R partial buffers and the residual), sums them in
+// binary32 in stream order, rounds the sum once to the storage type, writes it
+// back as the residual and keeps it in registers while it accumulates the sum
+// of squares.  After the row reduction the second pass scales the values still
+// held in registers by rsqrt(ss / H + eps) and by gamma and writes y: the
+// normalise pass never goes back to HBM.  ("Tokenweave fused-RMSNorm-AR
+// kernel", Code walkthrough: the same two passes, where the second pass
+// re-reads the residual from global memory; here only the two-pass kernel for
+// rows too long for registers does that.)
+//
+// Rows are spread over a grid that is capped at what the GPU holds at once;
+// each CTA (or warp) walks its rows with a grid stride.
+#pragma once
+
+#include "common.cuh"
+#include "plan.h"
+
+namespace rarn {
+
+// Input streams per element: plain 1 (x); fused 2 (x, residual); reduce R + 1
+// (partials, residual).  Stream s < R is partial s (x for fused); the last
+// stream is the residual.
+__device__ __forceinline__ int n_streams(const Problem &p) {
+    return p.op == OP_PLAIN ? 1 : p.R + 1;
+}
+
+template <typename T>
+__device__ __forceinline__ const T *stream_row(const Problem &p, int s, int64_t row_off) {
+    const bool is_res = (p.op != OP_PLAIN) && (s == p.R);
+    const T *base = is_res ? reinterpret_cast<const T *>(p.residual)
+                           : reinterpret_cast<const T *>(p.src) + (int64_t)s * p.slice;
+    return base + row_off;
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1, 16-byte packs.  Thread owns packs j = j0 + k * js (k < VPT, j < nv).
+// Loads RC streams at a time so that RC * VPT loads are in flight per thread.
+// Returns this thread's share of the sum of squares; hv receives the rounded
+// row values.
+// ---------------------------------------------------------------------------
+template <typename T, int VPT, int OP, int RC>
+__device__ __forceinline__ float pass1_vec(const Problem &p, int64_t t, int j0, int js, int nv,
+                                           uint4 (&hv)[VPT]) {
+    constexpr int EPV = DT<T>::EPV;
+    const int64_t row_off = t * p.H;
+    float ss = 0.f;
+    if (OP == OP_PLAIN) {
+        const T *x = reinterpret_cast<const T *>(p.src) + row_off;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = j0 + k * js;
+            if (j < nv) hv[k] = ld_stream(x + (int64_t)j * EPV);
+        }
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = j0 + k * js;
+            if (j < nv) {
+                float f[EPV];
+                DT<T>::unpack(hv[k], f);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) ss += f[e] * f[e];
+            }
+        }
+        return ss;
+    }
+    const int S = p.R + 1;
+    float acc[VPT][EPV];
+    for (int s0 = 0; s0 < S; s0 += RC) {
+        uint4 buf[RC][VPT];
+#pragma unroll
+        for (int q = 0; q < RC; ++q) {
+            if (s0 + q < S) {
+                const T *base = stream_row<T>(p, s0 + q, row_off);
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int j = j0 + k * js;
+                    if (j < nv) buf[q][k] = ld_stream(base + (int64_t)j * EPV);
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < RC; ++q) {
+            if (s0 + q < S) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int j = j0 + k * js;
+                    if (j < nv) {
+                        float f[EPV];
+                        DT<T>::unpack(buf[q][k], f);
+#pragma unroll
+                        for (int e = 0; e < EPV; ++e)
+                            acc[k][e] = (s0 + q == 0) ? f[e] : acc[k][e] + f[e];
+                    }
+                }
+            }
+        }
+    }
+    T *res = reinterpret_cast<T *>(p.residual) + row_off;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = j0 + k * js;
+        if (j < nv) {
+            hv[k] = DT<T>::pack(acc[k]);  // the one rounding to the storage type
+            st_global(res + (int64_t)j * EPV, hv[k]);
+            float f[EPV];
+            DT<T>::unpack(hv[k], f);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) ss += f[e] * f[e];
+        }
+    }
+    return ss;
+}
+
+// Pass 2, 16-byte packs: y = (h * inv) * gamma, one rounding.
+template <typename T, int VPT>
+__device__ __forceinline__ void pass2_vec(const Problem &p, int64_t t, int j0, int js, int nv,
+                                          const uint4 (&hv)[VPT], float inv) {
+    constexpr int EPV = DT<T>::EPV;
+    const T *g = reinterpret_cast<const T *>(p.gamma);
+    T *y = reinterpret_cast<T *>(p.y) + t * p.H;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = j0 + k * js;
+        if (j < nv) {
+            float h[EPV], w[EPV];
+            DT<T>::unpack(hv[k], h);
+            DT<T>::unpack(ld_keep(g + (int64_t)j * EPV), w);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) h[e] = (h[e] * inv) * w[e];
+            st_global(y + (int64_t)j * EPV, DT<T>::pack(h));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1 / pass 2, single elements (rows or pointers not 16-byte aligned).
+// Thread owns elements i = i0 + k * is (k < NE, i < H); values held as
+// binary32 (already rounded to the storage type).
+// ---------------------------------------------------------------------------
+template <typename T, int NE, int OP, int RC>
+__device__ __forceinline__ float pass1_scalar(const Problem &p, int64_t t, int i0, int is,
+                                              float (&h)[NE]) {
+    const int64_t row_off = t * p.H;
+    const int H = (int)p.H;
+    float ss = 0.f;
+    if (OP == OP_PLAIN) {
+        const T *x = reinterpret_cast<const T *>(p.src) + row_off;
+#pragma unroll
+        for (int k = 0; k < NE; ++k) {
+            const int i = i0 + k * is;
+            h[k] = i < H ? DT<T>::to_f(x[i]) : 0.f;
+            ss += h[k] * h[k];
+        }
+        return ss;
+    }
+    const int S = p.R + 1;
+    for (int s0 = 0; s0 < S; s0 += RC) {
+        float buf[RC][NE];
+#pragma unroll
+        for (int q = 0; q < RC; ++q) {
+            if (s0 + q < S) {
+                const T *base = stream_row<T>(p, s0 + q, row_off);
+#pragma unroll
+                for (int k = 0; k < NE; ++k) {
+                    const int i = i0 + k * is;
+                    buf[q][k] = i < H ? DT<T>::to_f(base[i]) : 0.f;
+                }
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < RC; ++q) {
+            if (s0 + q < S) {
+#pragma unroll
+                for (int k = 0; k < NE; ++k) h[k] = (s0 + q == 0) ? buf[q][k] : h[k] + buf[q][k];
+            }
+        }
+    }
+    T *res = reinterpret_cast<T *>(p.residual) + row_off;
+#pragma unroll
+    for (int k = 0; k < NE; ++k) {
+        const int i = i0 + k * is;
+        if (i < H) {
+            const T r = DT<T>::from_f(h[k]);
+            res[i] = r;
+            h[k] = DT<T>::to_f(r);
+            ss += h[k] * h[k];
+        }
+    }
+    return ss;
+}
+
+template <typename T, int NE>
+__device__ __forceinline__ void pass2_scalar(const Problem &p, int64_t t, int i0, int is,
+                                             const float (&h)[NE], float inv) {
+    const T *g = reinterpret_cast<const T *>(p.gamma);
+    T *y = reinterpret_cast<T *>(p.y) + t * p.H;
+    const int H = (int)p.H;
+#pragma unroll
+    for (int k = 0; k < NE; ++k) {
+        const int i = i0 + k * is;
+        if (i < H) y[i] = DT<T>::from_f((h[k] * inv) * DT<T>::to_f(g[i]));
+    }
+}
+
+template <int OP>
+struct Chunk {  // streams loaded together in pass 1
+    static constexpr int value = OP == OP_REDUCE ? 4 : 2;
+};
+
+// Register budget: F row values per thread (packs x EPV, or elements) caps the
+// CTA size the kernel is compiled for (rows_max_block in plan.h).
+template <typename T, int VPT>
+struct VecBound {
+    static constexpr int value = rows_max_block(VPT * DT<T>::EPV);
+};
+
+// ---------------------------------------------------------------------------
+// Kernels
+// ---------------------------------------------------------------------------
+
+// One CTA per row, packs.
+template <typename T, int VPT, int OP>
+__global__ void __launch_bounds__(VecBound<T, VPT>::value) k_cta_vec(Problem p) {
+    __shared__ float red[2][32];
+    const int nv = (int)(p.H / DT<T>::EPV);
+    int par = 0;
+    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
+        uint4 hv[VPT];
+        const float ss = pass1_vec<T, VPT, OP, Chunk<OP>::value>(p, t, threadIdx.x, blockDim.x,
+                                                                nv, hv);
+        const float tot = block_sum(ss, red[par]);
+        const float inv = rsqrtf(tot / (float)p.H + p.eps);
+        pass2_vec<T, VPT>(p, t, threadIdx.x, blockDim.x, nv, hv, inv);
+    }
+}
+
+// One warp per row, packs; blockDim.x / 32 rows per CTA at a time.
+template <typename T, int VPT, int OP>
+__global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
+    const int nv = (int)(p.H / DT<T>::EPV);
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    const int64_t first = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
+    const int64_t step = (int64_t)gridDim.x * wpb;
+    for (int64_t t = first; t < p.T; t += step) {
+        uint4 hv[VPT];
+        const float ss = pass1_vec<T, VPT, OP, Chunk<OP>::value>(p, t, lane, 32, nv, hv);
+        const float tot = warp_sum(ss);
+        const float inv = rsqrtf(tot / (float)p.H + p.eps);
+        pass2_vec<T, VPT>(p, t, lane, 32, nv, hv, inv);
+    }
+}
+
+// One CTA per row, single elements.
+template <typename T, int NE, int OP>
+__global__ void __launch_bounds__(rows_max_block(NE)) k_cta_scalar(Problem p) {
+    __shared__ float red[2][32];
+    int par = 0;
+    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
+        float h[NE];
+        const float ss =
+            pass1_scalar<T, NE, OP, Chunk<OP>::value>(p, t, threadIdx.x, blockDim.x, h);
+        const float tot = block_sum(ss, red[par]);
+        const float inv = rsqrtf(tot / (float)p.H + p.eps);
+        pass2_scalar<T, NE>(p, t, threadIdx.x, blockDim.x, h, inv);
+    }
+}
+
+// Rows too long for registers: pass 1 walks the row in tiles of blockDim
+// packs (or elements); pass 2 re-reads the stored row (the residual, or x for
+// the plain form) -- each thread re-reads only what it wrote itself.
+template <typename T, int OP, bool VEC>
+__global__ void __launch_bounds__(1024) k_two_pass(Problem p) {
+    __shared__ float red[2][32];
+    constexpr int EPV = VEC ? DT<T>::EPV : 1;
+    const int n = (int)(p.H / EPV);
+    int par = 0;
+    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
+        float ss = 0.f;
+        for (int base = 0; base < n; base += blockDim.x) {
+            if (VEC) {
+                uint4 hv[1];
+                ss += pass1_vec<T, 1, OP, Chunk<OP>::value>(p, t, base + threadIdx.x, 1 << 30,
+                                                           n, hv);
+            } else {
+                float h[1];
+                ss += pass1_scalar<T, 1, OP, Chunk<OP>::value>(p, t, base + threadIdx.x,
+                                                              1 << 30, h);
+            }
+        }
+        const float tot = block_sum(ss, red[par]);
+        const float inv = rsqrtf(tot / (float)p.H + p.eps);
+        const void *stored = OP == OP_PLAIN ? p.src : p.residual;
+        for (int base = 0; base < n; base += blockDim.x) {
+            const int j = base + threadIdx.x;
+            if (j >= n) break;
+            if (VEC) {
+                uint4 hv[1] = {ld_stream(reinterpret_cast<const T *>(stored) + t * p.H +
+                                         (int64_t)j * EPV)};
+                pass2_vec<T, 1>(p, t, j, 1 << 30, n, hv, inv);
+            } else {
+                float h[1] = {ld_elem<T>(stored, t * p.H + j)};
+                pass2_scalar<T, 1>(p, t, j, 1 << 30, h, inv);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Launcher: plan -> template instance
+// ---------------------------------------------------------------------------
+
+template <typename T, int OP>
+static cudaError_t launch_rows_op(const Problem &p, const Plan &pl, cudaStream_t st) {
+    const dim3 g(pl.grid), b(pl.block);
+    switch (pl.kind) {
+    case KIND_WARP:
+        switch (pl.per_thread) {
+        case 1: k_warp_vec<T, 1, OP><<<g, b, 0, st>>>(p); break;
+        case 2: k_warp_vec<T, 2, OP><<<g, b, 0, st>>>(p); break;
+        case 4: k_warp_vec<T, 4, OP><<<g, b, 0, st>>>(p); break;
+        default: return cudaErrorInvalidValue;
+        }
+        break;
+    case KIND_CTA:
+        if (pl.vec) {
+            switch (pl.per_thread) {
+            case 1: k_cta_vec<T, 1, OP><<<g, b, 0, st>>>(p); break;
+            case 2: k_cta_vec<T, 2, OP><<<g, b, 0, st>>>(p); break;
+            case 4: k_cta_vec<T, 4, OP><<<g, b, 0, st>>>(p); break;
+            case 8: k_cta_vec<T, 8, OP><<<g, b, 0, st>>>(p); break;
+            default: return cudaErrorInvalidValue;
+            }
+        } else {
+            switch (pl.per_thread) {
+            case 1: k_cta_scalar<T, 1, OP><<<g, b, 0, st>>>(p); break;
+            case 2: k_cta_scalar<T, 2, OP><<<g, b, 0, st>>>(p); break;
+            case 4: k_cta_scalar<T, 4, OP><<<g, b, 0, st>>>(p); break;
+            case 8: k_cta_scalar<T, 8, OP><<<g, b, 0, st>>>(p); break;
+            case 16: k_cta_scalar<T, 16, OP><<<g, b, 0, st>>>(p); break;
+            default: return cudaErrorInvalidValue;
+            }
+        }
+        break;
+    case KIND_TWO_PASS:
+        if (pl.vec)
+            k_two_pass<T, OP, true><<<g, b, 0, st>>>(p);
+        else
+            k_two_pass<T, OP, false><<<g, b, 0, st>>>(p);
+        break;
+    default:
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_rows(const Problem &p, const Plan &pl, cudaStream_t st) {
+    switch (p.op) {
+    case OP_PLAIN: return launch_rows_op<T, OP_PLAIN>(p, pl, st);
+    case OP_FUSED: return launch_rows_op<T, OP_FUSED>(p, pl, st);
+    case OP_REDUCE: return launch_rows_op<T, OP_REDUCE>(p, pl, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace rarn

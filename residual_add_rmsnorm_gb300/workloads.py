@@ -5,20 +5,25 @@ of the normalisation arithmetic lives here.  It is the one piece shared by the
 tests, the benchmark and the package smoke check: the same seed gives the same
 storage bits on both sides of every comparison.
 
-Recipe (per call, one ``numpy.random.Generator(PCG64(seed))``):
+Recipe (seed s):
 
-* Normal draws use the Box-Muller transform on binary32 uniforms from that
-  generator: u1, u2 in [0, 1), r = sqrt(-2 log(1 - u1)) (1 - u1 is exact in
-  binary32), z0 = r cos(2 pi u2), z1 = r sin(2 pi u2), interleaved z0, z1.
-  numpy's own normal sampler is an order of magnitude slower at these sizes.
-* Draw order: x (or partials 0..R-1, one [T, H] block each), then residual,
-  then -- for the scaled-token workload -- the per-row log-uniform factors and
-  the outlier channel permutation, then gamma ~ U(0.5, 1.5).
+* Each [T, H] input stream is drawn in blocks of CHUNK_ROWS rows; block b of
+  stream k comes from its own ``numpy.random.Generator(PCG64(SeedSequence(
+  [s, k, b])))``, so any row range can be generated on its own and blocks are
+  drawn in parallel threads.  Streams: plain k=0 is x; fused k=0 is x, k=1 the
+  residual; reduce k=0..R-1 are the partials, k=R the residual.
+* Normal draws use the Box-Muller transform on binary32 uniforms: u1, u2 in
+  [0, 1), r = sqrt(-2 log(1 - u1)) (1 - u1 is exact in binary32),
+  z0 = r cos(2 pi u2), z1 = r sin(2 pi u2), interleaved z0, z1 along the row
+  block.
+* gamma ~ U(0.5, 1.5) from SeedSequence([s, GAMMA_KEY]).
 * Values are formed in binary32 and cast to the storage type with
   round-to-nearest-even (numpy for f16, torch for bf16).
 * Scaled-token workload: every row t of both x and residual is multiplied by
-  s_t = 10 ** U(-3, 3); ceil(H / 100) channels, chosen by a seeded
-  permutation, are multiplied by 100 in both x and residual.
+  s_t = 10 ** U(-3, 3) (SeedSequence([s, SCALE_KEY]), T draws); ceil(H / 100)
+  channels, the first ones of a permutation drawn from
+  SeedSequence([s, OUTLIER_KEY]), are multiplied by 100 in x and residual.
+* Reduce partials are N(0, partial_std^2); x and residual are N(0, 1).
 
 Arrays hold raw storage bits: ``np.float32`` for f32, ``np.uint16`` for f16 and
 bf16.
@@ -102,6 +107,14 @@ def workload(op: str, dtype: str, T: int, H: int, *, R: int | None = None, eps: 
                     partial_std=partial_std, scaled=scaled)
 
 
+CHUNK_ROWS = 256
+GAMMA_KEY, SCALE_KEY, OUTLIER_KEY = 1 << 20, (1 << 20) + 1, (1 << 20) + 2
+
+
+def _rng(*key) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(list(key))))
+
+
 def _normal_f32(rng: np.random.Generator, n: int) -> np.ndarray:
     m = (n + 1) // 2
     u1 = rng.random(m, dtype=np.float32)
@@ -135,40 +148,62 @@ def from_storage(bits: np.ndarray, dtype: str) -> np.ndarray:
     return u.view(np.float32)
 
 
-def generate(w: Workload) -> dict:
+def _pool():
+    import concurrent.futures as cf
+    import os
+    return cf.ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1))
+
+
+def generate(w: Workload, rows: tuple[int, int] | None = None) -> dict:
     """Inputs of ``w`` as storage bits: keys 'x' (plain, fused), 'partials'
-    (reduce, shape [R, T, H]), 'residual' (fused, reduce) and 'gamma'."""
-    rng = np.random.default_rng(w.seed)
+    (reduce, shape [R, T', H]), 'residual' (fused, reduce) and 'gamma'.
+
+    ``rows=(a, b)`` generates only rows a..b-1 (T' = b - a); the bits equal
+    those rows of the full problem."""
     T, H = w.T, w.H
-    out = {}
+    a, b = (0, T) if rows is None else rows
+    if not 0 <= a <= b <= T:
+        raise ValueError(f"rows {rows} outside 0..{T}")
+    n = b - a
     if w.op == "reduce_add_rms_norm":
-        parts = np.empty((w.R, T, H), STORAGE[w.dtype])
-        for r in range(w.R):
-            z = _normal_f32(rng, T * H).reshape(T, H)
-            if w.partial_std != 1.0:
-                z *= np.float32(w.partial_std)
-            parts[r] = to_storage(z, w.dtype)
-        out["partials"] = parts
-        first = None
+        nstreams, names = w.R + 1, None
+    elif w.op == "fused_add_rms_norm":
+        nstreams, names = 2, ("x", "residual")
     else:
-        first = _normal_f32(rng, T * H).reshape(T, H)
-    res = None
-    if w.op != "rms_norm":
-        res = _normal_f32(rng, T * H).reshape(T, H)
+        nstreams, names = 1, ("x",)
+    row_scale = col_scale = None
     if w.scaled:
-        s = np.power(10.0, rng.uniform(-3.0, 3.0, size=T)).astype(np.float32)[:, None]
-        k = math.ceil(H / 100)
-        chan = rng.permutation(H)[:k]
-        cs = np.ones(H, np.float32)
-        cs[chan] = 100.0
-        if first is not None:
-            first = first * s * cs
-        if res is not None:
-            res = res * s * cs
-    if first is not None:
-        out["x"] = to_storage(first, w.dtype)
-    if res is not None:
-        out["residual"] = to_storage(res, w.dtype)
-    g = rng.uniform(0.5, 1.5, size=H).astype(np.float32)
+        row_scale = np.power(10.0, _rng(w.seed, SCALE_KEY).uniform(-3.0, 3.0, size=T)).astype(
+            np.float32)
+        col_scale = np.ones(H, np.float32)
+        col_scale[_rng(w.seed, OUTLIER_KEY).permutation(H)[:math.ceil(H / 100)]] = 100.0
+    std = np.float32(w.partial_std)
+    out_arr = np.empty((nstreams, n, H), STORAGE[w.dtype])
+
+    def block(job):
+        k, c = job
+        r0, r1 = c * CHUNK_ROWS, min((c + 1) * CHUNK_ROWS, T)
+        z = _normal_f32(_rng(w.seed, k, c), (r1 - r0) * H).reshape(r1 - r0, H)
+        lo, hi = max(r0, a), min(r1, b)
+        z = z[lo - r0:hi - r0]
+        if w.op == "reduce_add_rms_norm" and k < w.R and w.partial_std != 1.0:
+            z = z * std
+        if row_scale is not None:
+            z = z * row_scale[lo:hi, None] * col_scale[None, :]
+        out_arr[k, lo - a:hi - a] = to_storage(z, w.dtype)
+
+    jobs = [(k, c) for k in range(nstreams)
+            for c in range(a // CHUNK_ROWS, (b + CHUNK_ROWS - 1) // CHUNK_ROWS)]
+    if n > 0:
+        with _pool() as ex:
+            list(ex.map(block, jobs))
+    out = {}
+    if names is None:
+        out["partials"] = out_arr[:w.R]
+        out["residual"] = out_arr[w.R]
+    else:
+        for k, name in enumerate(names):
+            out[name] = out_arr[k]
+    g = _rng(w.seed, GAMMA_KEY).uniform(0.5, 1.5, size=H).astype(np.float32)
     out["gamma"] = to_storage(g, w.dtype)
     return out

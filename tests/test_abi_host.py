@@ -1,0 +1,154 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared
+symbol, rejects bad arguments before touching a GPU, and plans kernels.
+CPU only: no call here launches anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import residual_add_rmsnorm_gb300 as rarn
+from residual_add_rmsnorm_gb300 import build as rbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "rarn.h")
+
+OK, INVALID, UNSUPPORTED, ALIAS, CUDA = 0, 1, 2, 3, 4
+F32, F16, BF16 = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rbuild.build()
+    return rarn.library()
+
+
+def declared_functions():
+    with open(HEADER) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rarn_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version_and_status_strings(lib):
+    assert lib.rarn_version() >> 16 == 1
+    for code in range(5):
+        assert lib.rarn_status_string(code)
+    assert lib.rarn_status_string(99) == b"unknown status"
+
+
+# fake, never dereferenced device addresses: argument checks run before any
+# CUDA call, so these calls never reach the GPU
+A, B, C, D = 1 << 40, 2 << 40, 3 << 40, 4 << 40
+
+
+@pytest.mark.parametrize("args,want", [
+    ((A, B, C, 4, 0, 1e-6, BF16, None), INVALID),        # H = 0
+    ((A, B, C, -1, 8, 1e-6, BF16, None), INVALID),       # T < 0
+    ((A, B, C, 4, 8, -1.0, BF16, None), INVALID),        # eps < 0
+    ((A, B, C, 4, 8, float("nan"), BF16, None), INVALID),
+    ((A, B, C, 4, 8, float("inf"), BF16, None), INVALID),
+    ((A, B, C, 4, 8, 1e-6, 7, None), INVALID),           # dtype
+    ((None, B, C, 4, 8, 1e-6, BF16, None), INVALID),     # null y
+    ((A, None, C, 4, 8, 1e-6, BF16, None), INVALID),     # null x
+    ((A, B, None, 4, 8, 1e-6, BF16, None), INVALID),     # null gamma
+    ((A, B, C, 4, (1 << 24) + 1, 1e-6, BF16, None), UNSUPPORTED),
+    ((A, A + 2, C, 4, 8, 1e-6, BF16, None), ALIAS),      # y overlaps x, not equal
+    ((A, B, A + 16, 4, 8, 1e-6, BF16, None), ALIAS),     # gamma inside y
+    ((None, None, None, 0, 8, 1e-6, BF16, None), OK),    # T = 0 is a no-op
+])
+def test_rms_norm_argument_errors(lib, args, want):
+    assert lib.rarn_rms_norm(*args) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((A, B, None, D, 4, 8, 1e-6, F16, None), INVALID),   # null residual
+    ((A, B, A, D, 4, 8, 1e-6, F16, None), ALIAS),        # residual == y
+    ((A, B, B, D, 4, 8, 1e-6, F16, None), ALIAS),        # residual == x
+    ((A, B, C, C + 8, 4, 8, 1e-6, F16, None), ALIAS),    # gamma inside residual
+    ((A, B, C, D, 0, 8, 1e-6, F16, None), OK),
+])
+def test_fused_argument_errors(lib, args, want):
+    assert lib.rarn_fused_add_rms_norm(*args) == want
+
+
+@pytest.mark.parametrize("args,want", [
+    ((A, B, 0, C, D, 4, 8, 1e-6, F32, None), INVALID),   # R = 0
+    ((A, B, 65, C, D, 4, 8, 1e-6, F32, None), UNSUPPORTED),  # R > max
+    # y == partial 0 is allowed, but y overlapping partial 1 is not
+    ((B + 4 * 8 * 4, B, 2, C, D, 4, 8, 1e-6, F32, None), ALIAS),
+    # residual inside partial 2
+    ((A, B, 3, B + 2 * 4 * 8 * 4, D, 4, 8, 1e-6, F32, None), ALIAS),
+    ((A, B, 8, C, D, 0, 8, 1e-6, F32, None), OK),
+])
+def test_reduce_argument_errors(lib, args, want):
+    assert lib.rarn_reduce_add_rms_norm(*args) == want
+
+
+def test_path_setting(lib):
+    assert rarn.get_path() == "auto"
+    for name in ("rows", "stream", "cluster", "auto"):
+        rarn.set_path(name)
+        assert rarn.get_path() == name
+    assert lib.rarn_set_path(9) == INVALID
+    assert rarn.get_path() == "auto"
+
+
+def test_watchdog_null_pointer(lib):
+    assert lib.rarn_watchdog(None, 0) == INVALID
+
+
+def _plan(op, T, H, R, dt, vec=True):
+    return rarn.plan(op, T, H, R, dt, vec_ok=vec, num_sms=152)
+
+
+def test_plan_rows_kinds():
+    rarn.set_path("rows")
+    try:
+        # short rows: a warp per row
+        assert _plan("rms_norm", 512, 512, 0, "bf16").startswith("rows.warp")
+        assert _plan("rms_norm", 512, 1024, 0, "bf16").startswith("rows.warp")
+        # medium rows: a CTA per row, packs
+        p = _plan("fused_add_rms_norm", 4096, 4096, 1, "bf16")
+        assert p.startswith("rows.cta vec16"), p
+        # H*2 bytes not a multiple of 16: scalar kernel
+        assert "scalar" in _plan("fused_add_rms_norm", 8, 1591, 1, "bf16")
+        # unaligned pointers: scalar kernel
+        assert "scalar" in _plan("fused_add_rms_norm", 8, 4096, 1, "bf16", vec=False)
+        # rows beyond the register budget: two passes
+        assert _plan("fused_add_rms_norm", 8, 1 << 20, 1, "bf16").startswith("rows.two_pass")
+        assert _plan("rms_norm", 8, 20000, 0, "f16", vec=False).startswith("rows.two_pass")
+    finally:
+        rarn.set_path("auto")
+
+
+def test_plan_grid_is_capped_and_covers_small_t():
+    rarn.set_path("rows")
+    try:
+        p = _plan("fused_add_rms_norm", 3, 4096, 1, "bf16")
+        assert "grid=3 " in p, p
+        p = _plan("fused_add_rms_norm", 1 << 20, 4096, 1, "bf16")
+        grid = int(re.search(r"grid=(\d+)", p).group(1))
+        assert grid <= 152 * 8, p
+    finally:
+        rarn.set_path("auto")
+
+
+def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
+    monkeypatch.setattr(rarn, "_lib", None)
+    monkeypatch.setattr(rarn, "LIB_PATH", str(tmp_path / "nope.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        rarn.library()
+
+
+def test_header_declares_three_compute_calls():
+    names = declared_functions()
+    for n in ("rarn_rms_norm", "rarn_fused_add_rms_norm", "rarn_reduce_add_rms_norm"):
+        assert n in names

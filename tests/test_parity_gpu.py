@@ -1,0 +1,248 @@
+"""GPU parity: the CUDA library against the CPU oracle, element by element.
+
+Every configuration of the method at its full size, an edge-shape grid,
+unaligned and in-place buffers, guard bands around the outputs, determinism,
+and the stored golden fixture.  Residual bit-exact; y within 1e-5 relative
+(fp32) or 2 ulps (fp16 / bf16).
+"""
+import functools
+
+import numpy as np
+import pytest
+
+import oracle
+import residual_add_rmsnorm_gb300 as rarn
+from residual_add_rmsnorm_gb300 import workloads as W
+
+from gpu_util import (assert_bits_equal, assert_y_close, check_parity, run_gpu, run_oracle,
+                      to_device, to_host)
+
+pytestmark = pytest.mark.gpu
+
+PATHS = ["auto", "rows", "stream", "cluster"]
+
+
+@pytest.fixture(autouse=True)
+def _reset_path():
+    yield
+    rarn.set_path("auto")
+
+
+def _supported(w, path):
+    """Whether a forced path can run this shape (auto always can)."""
+    rarn.set_path(path)
+    R = w.R if w.op == "reduce_add_rms_norm" else 0
+    text = rarn.plan(w.op, w.T, w.H, max(R, 1), w.dtype)
+    return not text.startswith("none")
+
+
+@functools.lru_cache(maxsize=1)
+def _config_data(name):
+    w = W.BY_NAME[name]
+    d = W.generate(w)
+    return w, d, run_oracle(w, d)
+
+
+CONFIG_CASES = [(w.name, p) for w in W.CONFIGS for p in PATHS]
+
+
+@pytest.mark.parametrize("name,path", CONFIG_CASES, ids=[f"{n}-{p}" for n, p in CONFIG_CASES])
+def test_config_parity(name, path):
+    w, d, ref = _config_data(name)
+    if not _supported(w, path):
+        pytest.skip(f"path {path} does not run {name}")
+    rarn.set_path(path)
+    y, res = run_gpu(w, d)
+    assert_y_close(y, ref.y, w.dtype, f"{name}/{path}")
+    if ref.residual is not None:
+        assert_bits_equal(res, ref.residual, f"{name}/{path} residual")
+
+
+EDGE_H = [1, 7, 8, 9, 31, 33, 127, 1591, 1592, 1593, 4095, 5120, 8191, 16384, 16385]
+EDGE_T = [1, 2, 3, 131]
+
+
+def _edge_cases():
+    cases = []
+    for dt in ("f32", "f16", "bf16"):
+        for H in EDGE_H:
+            for T in EDGE_T:
+                if T == 131 and H > 5120 and dt != "bf16":
+                    continue
+                cases.append(("rms_norm", dt, T, H, 0))
+                cases.append(("fused_add_rms_norm", dt, T, H, 1))
+                for R in ((2, 3, 8) if H <= 1593 else (3,)):
+                    cases.append(("reduce_add_rms_norm", dt, T, H, R))
+    return cases
+
+
+EDGE = _edge_cases()
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_edge_grid(path):
+    """All edge shapes under one forced path (skipping shapes it cannot run)."""
+    ran = 0
+    for op, dt, T, H, R in EDGE:
+        w = W.workload(op, dt, T, H, R=R, eps=1e-5, seed=T * 100003 + H)
+        if not _supported(w, path):
+            continue
+        rarn.set_path(path)
+        check_parity(w, W.generate(w), what=f"{op}/{dt}/T{T}/H{H}/R{R}/{path}")
+        ran += 1
+    if path in ("auto", "rows"):
+        assert ran == len(EDGE)
+    elif ran == 0:
+        pytest.skip(f"path {path} runs none of the edge shapes")
+
+
+@pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm"])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_in_place_output(op, dt):
+    """y may overwrite x (or partial 0)."""
+    for H in (1592, 4096, 5121):
+        w = W.workload(op, dt, 37, H, eps=1e-6, seed=H)
+        check_parity(w, W.generate(w), out_is_input=True, what=f"in-place {op} {dt} H{H}")
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_unaligned_pointers(dt):
+    """Buffers offset by one element from a 16-byte boundary run the scalar
+    kernels and give the same results."""
+    import torch
+    T, H = 19, 1024
+    for op in ("rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm"):
+        w = W.workload(op, dt, T, H, R=3, eps=1e-6, seed=5)
+        d = W.generate(w)
+        ref = run_oracle(w, d)
+
+        def shifted(bits):
+            t = to_device(bits.reshape(-1), dt)
+            buf = torch.empty(t.numel() + 1, dtype=t.dtype, device=t.device)
+            v = buf[1:]
+            v.copy_(t)
+            return v
+
+        g = shifted(d["gamma"])
+        y = shifted(np.zeros((T, H), d["gamma"].dtype)).view(T, H)
+        if op == "rms_norm":
+            rarn.rms_norm(shifted(d["x"]).view(T, H), g, w.eps, out=y)
+            res = None
+        elif op == "fused_add_rms_norm":
+            res = shifted(d["residual"]).view(T, H)
+            rarn.fused_add_rms_norm(shifted(d["x"]).view(T, H), res, g, w.eps, out=y)
+        else:
+            res = shifted(d["residual"]).view(T, H)
+            p = shifted(d["partials"]).view(3, T, H)
+            rarn.reduce_add_rms_norm(p, res, g, w.eps, out=y)
+        torch.cuda.synchronize()
+        assert_y_close(to_host(y, dt), ref.y, dt, f"unaligned {op}")
+        if res is not None:
+            assert_bits_equal(to_host(res, dt), ref.residual, f"unaligned {op} residual")
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_guard_bands(path):
+    """Nothing is written outside y and the residual: 256-byte guards on both
+    sides keep their pattern."""
+    import torch
+    G = 128  # bf16 elements = 256 bytes
+    for op, T, H in (("fused_add_rms_norm", 133, 4096), ("reduce_add_rms_norm", 61, 5120),
+                     ("rms_norm", 300, 1000), ("fused_add_rms_norm", 7, 16385)):
+        w = W.workload(op, "bf16", T, H, R=4, eps=1e-6, seed=9)
+        if not _supported(w, path):
+            continue
+        rarn.set_path(path)
+        d = W.generate(w)
+        ref = run_oracle(w, d)
+
+        def guarded(bits):
+            t = to_device(bits.reshape(-1), "bf16")
+            buf = torch.full((t.numel() + 2 * G,), -7.0, dtype=t.dtype, device=t.device)
+            buf[G:G + t.numel()].copy_(t)
+            return buf
+
+        ybuf = guarded(np.zeros(T * H, np.uint16))
+        y = ybuf[G:G + T * H].view(T, H)
+        g = to_device(d["gamma"], "bf16")
+        rbuf = None
+        if op == "rms_norm":
+            rarn.rms_norm(to_device(d["x"], "bf16"), g, w.eps, out=y)
+        else:
+            rbuf = guarded(d["residual"])
+            res = rbuf[G:G + T * H].view(T, H)
+            if op == "fused_add_rms_norm":
+                rarn.fused_add_rms_norm(to_device(d["x"], "bf16"), res, g, w.eps, out=y)
+            else:
+                rarn.reduce_add_rms_norm(to_device(d["partials"], "bf16"), res, g, w.eps, out=y)
+        torch.cuda.synchronize()
+        for buf in (ybuf, rbuf):
+            if buf is None:
+                continue
+            assert torch.all(buf[:G] == -7.0) and torch.all(buf[G + T * H:] == -7.0), \
+                f"guard overwritten: {op} {path}"
+        assert_y_close(to_host(y, "bf16"), ref.y, "bf16", f"guarded {op}")
+        if rbuf is not None:
+            assert_bits_equal(to_host(rbuf[G:G + T * H], "bf16").reshape(T, H), ref.residual)
+
+
+def test_deterministic_bits():
+    """Two runs on the same inputs give identical bits, every path."""
+    w = W.BY_NAME["fused_bf16_T4096_H4096"]
+    d = W.generate(w)
+    for path in PATHS:
+        if not _supported(w, path):
+            continue
+        rarn.set_path(path)
+        a = run_gpu(w, d)
+        b = run_gpu(w, d)
+        assert_bits_equal(a[0], b[0], f"y {path}")
+        assert_bits_equal(a[1], b[1], f"residual {path}")
+
+
+def test_zero_row_with_zero_eps_gives_nan():
+    """A zero row with eps = 0: inv = +inf and y = 0 * inf = NaN, as in the
+    oracle."""
+    w = W.workload("rms_norm", "f32", 4, 64, eps=0.0)
+    d = W.generate(w)
+    d["x"][2] = 0.0
+    y, _ = run_gpu(w, d)
+    ref = run_oracle(w, d)
+    assert np.all(np.isnan(ref.y[2])) and np.all(np.isnan(y[2]))
+    assert_y_close(y, ref.y, "f32")
+
+
+def test_many_rows_grid_stride():
+    """T far above the grid size: every row is visited exactly once."""
+    for op, dt, T, H in (("rms_norm", "bf16", 200003, 64), ("fused_add_rms_norm", "f16", 50001,
+                                                            1024),
+                         ("reduce_add_rms_norm", "bf16", 20011, 2048)):
+        w = W.workload(op, dt, T, H, R=2, eps=1e-6, seed=3)
+        check_parity(w, W.generate(w), what=f"grid-stride {op}")
+
+
+def test_golden_fixture_on_gpu():
+    """The stored oracle outputs (tests/golden/oracle_small.json)."""
+    from golden_io import cases
+    for c in cases():
+        w = W.workload(c["op"], c["dtype"], c["T"], c["H"], R=c["R"], eps=c["eps"])
+        y, res = run_gpu(w, c["inputs"])
+        assert_y_close(y, c["expected"]["y"], c["dtype"], f"golden {c['op']} {c['dtype']}")
+        if "residual" in c["expected"]:
+            assert_bits_equal(res, c["expected"]["residual"], "golden residual")
+
+
+def test_binding_rejects_bad_tensors():
+    import torch
+    x = torch.zeros(4, 8, device="cuda", dtype=torch.bfloat16)
+    g = torch.ones(8, device="cuda", dtype=torch.float16)
+    with pytest.raises(TypeError):
+        rarn.rms_norm(x, g, 1e-6)
+    with pytest.raises(ValueError):
+        rarn.rms_norm(x.t(), torch.ones(4, device="cuda", dtype=torch.bfloat16), 1e-6)
+    with pytest.raises(rarn.RarnError):
+        rarn.fused_add_rms_norm(x, x, torch.ones(8, device="cuda", dtype=torch.bfloat16), 1e-6)
+
+
+def test_watchdog_clear_after_everything():
+    assert rarn.watchdog(clear=True) == 0
