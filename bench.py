@@ -8,8 +8,9 @@ add the residual, write it back, normalise, weight, write y -- over one batch
 of the headline workload (reduce + residual + RMSNorm, bf16 storage,
 partials [8, 8192, 8192], residual [8192, 8192]).  Its 1.3 GB of inputs are
 ten times the L2, so consecutive steps read cold data without a flush.  The
-other configurations of the method are timed as well (cold L2: a 2 x L2
-buffer is written before each launch) and reported under "per_config".
+other configurations of the method are timed as well and reported under
+"per_config": CUDA-graph replays of launches that cycle through enough input
+copies to cover twice the L2 (no host overhead, cold L2).
 
 Rank 0 prints one JSON line.  Under torchrun each rank runs its own replica on
 its own GPU (rows are independent, there is no exchange step): weak scaling,
@@ -47,7 +48,6 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--e2e-steps", type=int, default=10)
-    ap.add_argument("--config-reps", type=int, default=30)
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -321,23 +321,53 @@ def time_steps(call, steps, warmup, stream):
     return start.elapsed_time(end)  # ms
 
 
-def time_cold(call, reps, flush, stream):
-    """Median / min of single launches, L2 flushed (flush buffer written)
-    before each one."""
+def time_graph(w, data, device, l2_bytes, min_launches=200):
+    """Per-launch device time of one configuration without host overhead and
+    with a cold L2: enough copies of the inputs and outputs to cover 2 x L2
+    are launched round-robin inside one CUDA graph, so no launch finds its
+    data in L2 (unless one copy alone is smaller than L2 and the graph wraps
+    around within it -- the copies are cycled in order, so each is evicted
+    before its next use).  Returns (us per launch, copies, launches)."""
+    import math
+
     import torch
+
+    import residual_add_rmsnorm_gb300 as rarn
+    footprint = w.algorithmic_bytes()
+    copies = max(1, min(64, math.ceil(2 * l2_bytes / footprint)))
+    sets = [device_tensors(w, data, device) for _ in range(copies)]
+    calls = [make_call(w, t, rarn) for t in sets]
+    per_pass = copies
+    passes = max(1, math.ceil(min_launches / per_pass))
+    if footprint * copies * passes > 40e9:  # keep huge configurations short
+        passes = 1
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        for c in calls:
+            c()
+    torch.cuda.current_stream(device).wait_stream(side)
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(passes):
+            for c in calls:
+                c()
+    n = passes * per_pass
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize(device)
     times = []
     for _ in range(3):
-        call()
-    for _ in range(reps):
-        flush.add_(1.0)
         s = torch.cuda.Event(enable_timing=True)
         e = torch.cuda.Event(enable_timing=True)
-        s.record(stream)
-        call()
-        e.record(stream)
+        s.record()
+        graph.replay()
+        e.record()
         e.synchronize()
         times.append(s.elapsed_time(e))
-    return statistics.median(times), min(times)
+    del graph, sets, calls
+    return 1e3 * statistics.median(times) / n, copies, n
 
 
 def e2e_steps(w, data, tensors, call, steps, device, stream):
@@ -410,23 +440,20 @@ def main():
     per_config = {}
     if not args.no_configs:
         l2 = int(getattr(props, "L2_cache_size", 128 << 20))
-        flush = torch.zeros(2 * l2 // 4, dtype=torch.float32, device=device)
         del tensors, call
         torch.cuda.empty_cache()
         for cw in W.CONFIGS:
             cd = W.generate(cw)
-            ct = device_tensors(cw, cd, device)
-            cc = make_call(cw, ct, rarn)
-            med, best = time_cold(cc, args.config_reps, flush, stream)
+            us, copies, n = time_graph(cw, cd, device, l2)
             cb = cw.algorithmic_bytes()
             cR = cw.R if cw.op == "reduce_add_rms_norm" else 1
+            gbs = cb / (us / 1e6) / 1e9
             per_config[cw.name] = {
-                "us_median": 1e3 * med, "us_min": 1e3 * best,
-                "gbs": cb / (med / 1e3) / 1e9, "rows_per_s": cw.T / (med / 1e3),
-                "frac_of_peak": cb / (med / 1e3) / 1e9 / peak,
-                "algorithmic_bytes": cb,
+                "us_per_launch": us, "gbs": gbs, "rows_per_s": cw.T / (us / 1e6),
+                "frac_of_peak": gbs / peak, "algorithmic_bytes": cb,
+                "timing": f"CUDA graph of {n} launches over {copies} input copies (cold L2)",
                 "plan": rarn.plan(cw.op, cw.T, cw.H, cR, cw.dtype)}
-            del ct, cc, cd
+            del cd
             torch.cuda.empty_cache()
         if rarn.watchdog(clear=True):
             watchdog = 1

@@ -7,6 +7,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -110,13 +111,93 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
     return pl;
 }
 
+// Persistent TMA-fed kernel: 16-byte aligned rows whose staged copy fits in
+// shared memory next to at least two pipeline stages.
+constexpr int64_t kStreamMaxRowBytes = 96 * 1024;
+constexpr int kDefaultMaxSmem = 232448;  // opt-in shared memory per CTA on sm_100 / sm_103
+
+Plan plan_stream(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_sms,
+                 int max_smem, int groups) {
+    Plan pl;
+    const int64_t row_bytes = H * s;
+    if (!vec || row_bytes > kStreamMaxRowBytes) return pl;
+    const int ns = op == OP_PLAIN ? 1 : R + 1;
+    // fewer groups when their rings and row copies would not fit
+    for (; groups >= 1; --groups) {
+        int stages = stream::kMaxStages / groups;  // per group
+        while (stages >= 2 &&
+               stream::layout(stages, ns, (int)row_bytes, groups).total > max_smem)
+            --stages;
+        if (stages < 2) continue;
+        pl.kind = KIND_STREAM;
+        pl.vec = true;
+        pl.per_thread = 1;
+        pl.groups = groups;
+        pl.block = stream::threads(groups);
+        pl.grid = (int)std::min<int64_t>(T, num_sms);
+        pl.stages = stages;
+        pl.chunk = stream::kChunkBytes;
+        pl.smem = stream::layout(stages, ns, (int)row_bytes, groups).total;
+        return pl;
+    }
+    return Plan{};
+}
+
+// Cluster per row: the smallest cluster (2, 4, 8 CTAs) whose segments fit the
+// register budget and, where possible, puts a CTA on every SM.
+Plan plan_cluster(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
+    Plan pl;
+    if (!vec) return pl;
+    const int epv = 16 / s;
+    const int64_t n = H / epv;
+    for (int cs = 2; cs <= 8; cs <<= 1) {
+        const int64_t seg = ceil_div(n, cs);
+        int pt = std::min(8, pow2_at_least(ceil_div(seg, 256)));
+        while (pt < 8 && ceil_div(seg, pt) > rows_max_block(pt * epv)) pt <<= 1;
+        if (ceil_div(seg, pt) > rows_max_block(pt * epv)) continue;
+        const bool fills = T * cs >= num_sms;
+        if (!fills && cs < 8) {
+            // a larger cluster spreads the rows over more SMs; keep looking
+            // unless the segments would become tiny
+            if (ceil_div(n, cs * 2) >= 64) continue;
+        }
+        pl.kind = KIND_CLUSTER;
+        pl.vec = true;
+        pl.cluster = cs;
+        pl.per_thread = pt;
+        pl.block = round_up(ceil_div(seg, pt), 32);
+        const int64_t resident = (int64_t)num_sms * std::max(1, 2048 / pl.block) / cs;
+        pl.grid = (int)(std::min<int64_t>(T, std::max<int64_t>(1, resident)) * cs);
+        return pl;
+    }
+    return pl;
+}
+
+// Consumer groups of the stream kernel: RARN_STREAM_GROUPS (1..3) overrides
+// the default for measurements; read on every plan.
+int stream_groups() {
+    const char *v = getenv("RARN_STREAM_GROUPS");
+    if (!v || !*v) return 2;
+    const int g = atoi(v);
+    return g < 1 ? 1 : g > stream::kMaxGroups ? stream::kMaxGroups : g;
+}
+
 Plan make_plan(int op, int64_t T, int64_t H, int R, rarn_dtype dt, bool vec, int num_sms,
-               int path) {
-    (void)R;
+               int max_smem, int path) {
     const int s = elem_size(dt);
     switch (path) {
-    case RARN_PATH_AUTO:
     case RARN_PATH_ROWS: return plan_rows(op, T, H, s, vec, num_sms);
+    case RARN_PATH_STREAM:
+        return plan_stream(op, T, H, R, s, vec, num_sms, max_smem, stream_groups());
+    case RARN_PATH_CLUSTER: return plan_cluster(op, T, H, s, vec, num_sms);
+    case RARN_PATH_AUTO: {
+        Plan r = plan_rows(op, T, H, s, vec, num_sms);
+        if (r.kind == KIND_TWO_PASS && vec) {
+            Plan c = plan_cluster(op, T, H, s, vec, num_sms);
+            if (c.kind != KIND_NONE) return c;
+        }
+        return r;
+    }
     default: return Plan{};
     }
 }
@@ -173,7 +254,7 @@ rarn_status run(int op, void *y, const void *src, int32_t R, void *residual, con
     rarn_status st = device_info(&d);
     if (st != RARN_OK) return st;
 
-    const Plan pl = make_plan(op, T, H, R, dt, vec, d->num_sms, g_path.load());
+    const Plan pl = make_plan(op, T, H, R, dt, vec, d->num_sms, d->max_smem_optin, g_path.load());
     if (pl.kind == KIND_NONE) return RARN_ERR_UNSUPPORTED;
 
     Problem p{};
@@ -199,6 +280,20 @@ rarn_status run(int op, void *y, const void *src, int32_t R, void *residual, con
         case RARN_F32: e = launch_rows<float>(p, pl, cs); break;
         case RARN_F16: e = launch_rows<__half>(p, pl, cs); break;
         case RARN_BF16: e = launch_rows<__nv_bfloat16>(p, pl, cs); break;
+        }
+        break;
+    case KIND_STREAM:
+        switch (dt) {
+        case RARN_F32: e = launch_stream<float>(p, pl, cs); break;
+        case RARN_F16: e = launch_stream<__half>(p, pl, cs); break;
+        case RARN_BF16: e = launch_stream<__nv_bfloat16>(p, pl, cs); break;
+        }
+        break;
+    case KIND_CLUSTER:
+        switch (dt) {
+        case RARN_F32: e = launch_cluster<float>(p, pl, cs); break;
+        case RARN_F16: e = launch_cluster<__half>(p, pl, cs); break;
+        case RARN_BF16: e = launch_cluster<__nv_bfloat16>(p, pl, cs); break;
         }
         break;
     default: return RARN_ERR_UNSUPPORTED;
@@ -256,17 +351,21 @@ rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt
     if (dt != RARN_F32 && dt != RARN_F16 && dt != RARN_BF16) return RARN_ERR_INVALID_ARG;
     if (T < 0 || H <= 0 || (op == RARN_OP_REDUCE_ADD_RMS_NORM && R < 1))
         return RARN_ERR_INVALID_ARG;
+    int max_smem = kDefaultMaxSmem;
     if (num_sms <= 0) {
         DeviceInfo *d = nullptr;
         rarn_status st = device_info(&d);
         if (st != RARN_OK) return st;
         num_sms = d->num_sms;
+        max_smem = d->max_smem_optin;
     }
     const bool vec = vec_ok && (H * elem_size(dt)) % 16 == 0;
-    const Plan pl = make_plan((int)op, T, H, R, dt, vec, num_sms, g_path.load());
-    snprintf(out, cap, "%s %s per_thread=%d block=%d grid=%d cluster=%d smem=%d stages=%d chunk=%d",
+    const Plan pl = make_plan((int)op, T, H, R, dt, vec, num_sms, max_smem, g_path.load());
+    snprintf(out, cap,
+             "%s %s per_thread=%d block=%d grid=%d cluster=%d smem=%d stages=%d chunk=%d "
+             "groups=%d",
              kind_name(pl.kind), pl.vec ? "vec16" : "scalar", pl.per_thread, pl.block, pl.grid,
-             pl.cluster, pl.smem, pl.stages, pl.chunk);
+             pl.cluster, pl.smem, pl.stages, pl.chunk, pl.groups);
     return pl.kind == KIND_NONE ? RARN_ERR_UNSUPPORTED : RARN_OK;
 }
 

@@ -1,0 +1,111 @@
+// cluster.cuh -- a thread-block cluster per row for long rows.
+//
+// The row is cut into CS contiguous segments, one per CTA of a cluster of CS
+// CTAs (2, 4 or 8).  Each CTA runs the register-staged passes of rows.cuh on
+// its segment; the CTAs' partial sums of squares meet through distributed
+// shared memory: each CTA publishes its partial in its own shared memory, a
+// hardware cluster barrier orders the writes, and every CTA reads all CS
+// partials in rank order (the same order in every CTA, so all of them get the
+// same total).  The row is read from HBM once and never re-read, even when it
+// is too long for one CTA's registers, and a short batch of long rows spreads
+// over CS times more SMs.
+#pragma once
+
+#include "rows.cuh"
+
+namespace rarn {
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Hardware cluster barrier: release this thread's prior writes (shared memory
+// included) to the cluster, acquire everyone else's.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Read a float from the same shared-memory variable in CTA `rank` of this
+// cluster.
+__device__ __forceinline__ float ld_peer(const float *local, uint32_t rank) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+template <typename T, int VPT, int OP>
+__global__ void __launch_bounds__(VecBound<T, VPT>::value) k_cluster_vec(Problem p) {
+    __shared__ float red[2][32];
+    __shared__ float part[2];
+    const uint32_t rank = cluster_ctarank(), cs = cluster_nctarank();
+    const int nv = (int)(p.H / DT<T>::EPV);
+    const int seg = (nv + (int)cs - 1) / (int)cs;
+    const int j_begin = (int)rank * seg;
+    const int j_end = min(nv, j_begin + seg);
+    const int64_t first = blockIdx.x / cs, step = gridDim.x / cs;
+    int par = 0;
+    for (int64_t t = first; t < p.T; t += step, par ^= 1) {
+        uint4 hv[VPT];
+        const float ss = pass1_vec<T, VPT, OP, Chunk<OP>::value>(p, t, j_begin + threadIdx.x,
+                                                                blockDim.x, j_end, hv);
+        const float mine = block_sum(ss, red[par]);
+        if (threadIdx.x == 0) part[par] = mine;
+        cluster_sync();
+        float tot = 0.f;
+        for (uint32_t r = 0; r < cs; ++r) tot += ld_peer(&part[par], r);
+        const float inv = rsqrtf(tot / (float)p.H + p.eps);
+        pass2_vec<T, VPT>(p, t, j_begin + threadIdx.x, blockDim.x, j_end, hv, inv);
+    }
+    // no CTA leaves while a peer may still read its partials
+    cluster_sync();
+}
+
+template <typename T, int OP>
+static cudaError_t launch_cluster_op(const Problem &p, const Plan &pl, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(pl.grid);
+    cfg.blockDim = dim3(pl.block);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = pl.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    switch (pl.per_thread) {
+    case 1: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 1, OP>, p);
+    case 2: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 2, OP>, p);
+    case 4: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 4, OP>, p);
+    case 8: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 8, OP>, p);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t launch_cluster(const Problem &p, const Plan &pl, cudaStream_t st) {
+    cudaError_t e;
+    switch (p.op) {
+    case OP_PLAIN: e = launch_cluster_op<T, OP_PLAIN>(p, pl, st); break;
+    case OP_FUSED: e = launch_cluster_op<T, OP_FUSED>(p, pl, st); break;
+    case OP_REDUCE: e = launch_cluster_op<T, OP_REDUCE>(p, pl, st); break;
+    default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace rarn

@@ -28,6 +28,7 @@ struct Plan {
     int cluster = 1;     // CTAs per cluster
     int stages = 0;      // pipeline depth (stream kernel)
     int chunk = 0;       // bytes per stream per pipeline stage (stream kernel)
+    int groups = 1;      // consumer groups (stream kernel)
 };
 
 // Largest CTA the register row kernels are compiled for, by the number of row
@@ -38,7 +39,52 @@ __host__ __device__ constexpr int rows_max_block(int F) {
     return F <= 8 ? 1024 : F <= 16 ? 512 : F <= 32 ? 256 : 128;
 }
 
+// Shape of the TMA-fed persistent kernel (stream.cuh), shared with the planner.
+namespace stream {
+constexpr int kConsumerWarps = 8;                // per consumer group
+constexpr int kConsumers = kConsumerWarps * 32;  // threads per group = packs per chunk
+constexpr int kChunkBytes = kConsumers * 16;     // per stream per stage
+constexpr int kMaxStages = 32;
+constexpr int kMaxGroups = 3;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr unsigned int kWatchConsumer = 1u, kWatchProducer = 2u;
+
+__host__ __device__ constexpr int threads(int groups) { return 32 + groups * kConsumers; }
+
+// Dynamic shared memory layout (all offsets 128-byte aligned), per consumer
+// group g < G its own ring of `stages` stages:
+//   [g * stages * NS * kChunkBytes, ...)   group g's stage ring
+//   G x row copy (H * sizeof(T) bytes each)
+//   control: full[G * stages], empty[G * stages] mbarriers (G * stages <=
+//            kMaxStages), red[G][2][kConsumerWarps] floats, abort word
+struct Layout {
+    int stages, ns, row_bytes, groups;
+    int ring_stride, row_off, row_stride, ctl_off, total;
+};
+
+__host__ __device__ inline int align128(int v) { return (v + 127) & ~127; }
+
+__host__ __device__ inline Layout layout(int stages, int ns, int row_bytes, int groups) {
+    Layout L;
+    L.stages = stages;
+    L.ns = ns;
+    L.row_bytes = row_bytes;
+    L.groups = groups;
+    L.ring_stride = stages * ns * kChunkBytes;
+    L.row_off = align128(groups * L.ring_stride);
+    L.row_stride = align128(row_bytes);
+    L.ctl_off = L.row_off + groups * L.row_stride;
+    L.total = L.ctl_off + 2 * kMaxStages * 8 + groups * 2 * kConsumerWarps * 4 + 16;
+    return L;
+}
+
+}  // namespace stream
+
 template <typename T>
 cudaError_t launch_rows(const Problem &p, const Plan &plan, cudaStream_t stream);
+template <typename T>
+cudaError_t launch_stream(const Problem &p, const Plan &plan, cudaStream_t stream);
+template <typename T>
+cudaError_t launch_cluster(const Problem &p, const Plan &plan, cudaStream_t stream);
 
 }  // namespace rarn

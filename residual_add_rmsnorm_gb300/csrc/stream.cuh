@@ -9,11 +9,14 @@
 // across row boundaries, so HBM reads stay in flight while the consumers
 // reduce and normalise.
 //
-// Warps 1..8 are the consumers (256 threads).  For chunk c of a row, thread j
-// takes pack p = c * 256 + j: it sums the streams' packs in stream order in
+// Warps 1.. are the consumers: G groups of 8 warps (256 threads); group g
+// takes the CTA's rows i = g, g + G, ... so that while one group reduces and
+// normalises its row the next group already consumes the following row's
+// chunks.  For chunk c of a row, thread j of the group takes pack
+// p = c * 256 + j: it sums the streams' packs in stream order in
 // binary32, rounds once, writes the residual pack to global memory, keeps the
 // rounded pack in a shared-memory copy of the row and accumulates its
-// squares.  After the row's last chunk a named barrier combines the consumer
+// squares.  After the row's last chunk a named barrier combines the group's
 // warps' sums; each thread then normalises the packs it staged itself (same
 // p, so no further synchronisation) with gamma and writes y.  HBM is read
 // exactly once per input element.
@@ -29,38 +32,6 @@
 
 namespace rarn {
 namespace stream {
-
-constexpr int kConsumerWarps = 8;
-constexpr int kConsumers = kConsumerWarps * 32;  // packs per chunk
-constexpr int kThreads = kConsumers + 32;        // + producer warp
-constexpr int kChunkBytes = kConsumers * 16;     // per stream per stage
-constexpr int kMaxStages = 32;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr unsigned int kWatchConsumer = 1u, kWatchProducer = 2u;
-
-// Dynamic shared memory layout (all offsets 128-byte aligned):
-//   [0, stages * NS * kChunkBytes)    stage ring
-//   row copy: H * sizeof(T) bytes
-//   control: full[kMaxStages], empty[kMaxStages] mbarriers, red[2][8], abort
-struct Layout {
-    int stages, ns, row_bytes;
-    int ring_off, row_off, ctl_off, total;
-};
-
-__host__ __device__ inline int align128(int v) { return (v + 127) & ~127; }
-
-__host__ __device__ inline Layout layout(int stages, int ns, int row_bytes) {
-    Layout L;
-    L.stages = stages;
-    L.ns = ns;
-    L.row_bytes = row_bytes;
-    L.ring_off = 0;
-    L.row_off = align128(stages * ns * kChunkBytes);
-    L.ctl_off = align128(L.row_off + row_bytes);
-    // 2 * kMaxStages mbarriers (8 B each), 2 x 8 floats, one abort word
-    L.total = L.ctl_off + 2 * kMaxStages * 8 + 2 * kConsumerWarps * 4 + 16;
-    return L;
-}
 
 // ---------------------------------------------------------------------------
 // mbarrier and bulk-copy primitives (inline PTX)
@@ -137,45 +108,53 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
-// Drain wait used by the producer before it exits: bounded, ignores the abort
-// word (copies already issued must land before the CTA's memory goes away).
-__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity, unsigned int *watchdog) {
-    const unsigned long long t0 = global_ns();
+// Drain wait used by the producer before it exits: ignores the abort word
+// (copies already issued must land before the CTA's memory goes away) and
+// gives up at `deadline` (one deadline for the whole drain).
+__device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity,
+                                           unsigned long long deadline, unsigned int *watchdog) {
     while (!mbar_try_wait(bar, parity)) {
-        if (global_ns() - t0 > kWaitLimitNs) {
+        if (global_ns() > deadline) {
             atomicOr(watchdog, kWatchProducer);
-            return;
+            return false;
         }
     }
+    return true;
 }
 
-__device__ __forceinline__ void named_barrier_consumers() {
-    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+// Barrier over one consumer group's 256 threads (ids 1.. ; 0 is __syncthreads).
+__device__ __forceinline__ void named_barrier(int id) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kConsumers) : "memory");
 }
 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
 
-template <typename T, int OP>
-__global__ void __launch_bounds__(kThreads, 1) k_stream(Problem p, int stages) {
+// Row k of this CTA (t = blockIdx.x + k * gridDim.x) goes to consumer group
+// g = k % G and through g's own ring of `stages` stages.  Each ring has one
+// producer and one consumer group taking its fills in the same order, so a
+// parity wait is never more than one phase ahead of its barrier: fill n of a
+// ring lands in stage n % stages during that stage's phase n / stages, and
+// fill n - stages of the same stage was consumed before fill n is waited on.
+template <typename T, int OP, int G>
+__global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages) {
     constexpr int EPV = DT<T>::EPV;
     extern __shared__ __align__(128) unsigned char smem[];
     const int ns = OP == OP_PLAIN ? 1 : p.R + 1;  // input streams
     const int row_bytes = (int)(p.H * (int64_t)sizeof(T));
     const int nv = row_bytes / 16;                // packs per row
     const int nchunks = (nv + kConsumers - 1) / kConsumers;
-    const Layout L = layout(stages, ns, row_bytes);
-    unsigned char *ring = smem + L.ring_off;
-    uint4 *row_copy = reinterpret_cast<uint4 *>(smem + L.row_off);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.ctl_off);
-    uint64_t *empty = full + kMaxStages;
-    float *red = reinterpret_cast<float *>(empty + kMaxStages);  // [2][kConsumerWarps]
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 2 * kConsumerWarps);
+    const Layout L = layout(stages, ns, row_bytes, G);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.ctl_off);   // [G][stages]
+    uint64_t *empty = full + kMaxStages;                                // [G][stages]
+    float *red_all = reinterpret_cast<float *>(empty + kMaxStages);  // [G][2][kConsumerWarps]
+    volatile int *abort_flag =
+        reinterpret_cast<volatile int *>(red_all + G * 2 * kConsumerWarps);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) {
+        for (int s = 0; s < G * stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
             mbar_init(smem_addr(&empty[s]), kConsumerWarps);
         }
@@ -188,21 +167,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(Problem p, int stages) {
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
-        int stage = 0;
-        uint32_t phase = 0;
-        long long issued = 0;
+        int stage[G];
+        uint32_t phase[G];
+        long long issued[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            stage[g] = 0;
+            phase[g] = 0;
+            issued[g] = 0;
+        }
         bool ok = true;
+        int g = 0;
         for (int64_t t = blockIdx.x; t < p.T && ok; t += gridDim.x) {
             const int64_t row_elem = t * p.H;
             for (int c = 0; c < nchunks && ok; ++c) {
                 const int packs = min(kConsumers, nv - c * kConsumers);
                 const uint32_t bytes = (uint32_t)packs * 16u;
-                ok = wait_bounded(smem_addr(&empty[stage]), phase ^ 1u, abort_flag, p.watchdog,
+                const int b = g * stages + stage[g];
+                ok = wait_bounded(smem_addr(&empty[b]), phase[g] ^ 1u, abort_flag, p.watchdog,
                                   kWatchProducer);
                 if (!ok) break;
-                const uint32_t fb = smem_addr(&full[stage]);
+                const uint32_t fb = smem_addr(&full[b]);
                 mbar_arrive_expect_tx(fb, bytes * (uint32_t)ns);
-                const uint32_t dst = smem_addr(ring + (size_t)stage * ns * kChunkBytes);
+                const uint32_t dst = smem_addr(smem + (size_t)g * L.ring_stride +
+                                               (size_t)stage[g] * ns * kChunkBytes);
                 const int64_t off = row_elem + (int64_t)c * kConsumers * EPV;
                 for (int s = 0; s < ns; ++s) {
                     const T *src;
@@ -212,32 +200,46 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(Problem p, int stages) {
                         src = reinterpret_cast<const T *>(p.src) + (int64_t)s * p.slice + off;
                     bulk_g2s(dst + (uint32_t)(s * kChunkBytes), src, bytes, fb);
                 }
-                ++issued;
-                if (++stage == stages) {
-                    stage = 0;
-                    phase ^= 1u;
+                ++issued[g];
+                if (++stage[g] == stages) {
+                    stage[g] = 0;
+                    phase[g] ^= 1u;
                 }
             }
+            if (++g == G) g = 0;
         }
-        // Drain: the last min(stages, issued) fills must land before exit.
-        const long long first = issued > stages ? issued - stages : 0;
-        for (long long f = first; f < issued; ++f)
-            wait_drain(smem_addr(&full[f % stages]), (uint32_t)((f / stages) & 1), p.watchdog);
+        // Drain: in every ring the last min(stages, issued) fills must land
+        // before the CTA exits.
+        const unsigned long long deadline = global_ns() + kWaitLimitNs;
+        for (int r = 0; r < G; ++r) {
+            const long long first = issued[r] > stages ? issued[r] - stages : 0;
+            for (long long f = first; f < issued[r]; ++f)
+                if (!wait_drain(smem_addr(&full[r * stages + (int)(f % stages)]),
+                                (uint32_t)((f / stages) & 1), deadline, p.watchdog))
+                    return;
+        }
         return;
     }
 
     // ---------------------------------------------------------------- consumers
-    const int j = threadIdx.x - 32;  // 0..255
-    const int cw = warp - 1;          // consumer warp 0..7
+    const int g = (warp - 1) / kConsumerWarps;       // consumer group
+    const int cw = (warp - 1) % kConsumerWarps;      // warp within the group
+    const int j = threadIdx.x - 32 - g * kConsumers;  // 0..255 within the group
+    unsigned char *ring = smem + (size_t)g * L.ring_stride;
+    uint64_t *gfull = full + g * stages;
+    uint64_t *gempty = empty + g * stages;
+    uint4 *row_copy = reinterpret_cast<uint4 *>(smem + L.row_off + g * L.row_stride);
+    float *red = red_all + g * 2 * kConsumerWarps;
     const T *gamma = reinterpret_cast<const T *>(p.gamma);
     int stage = 0;
     uint32_t phase = 0;
     int par = 0;
-    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
+    for (int64_t t = blockIdx.x + (int64_t)g * gridDim.x; t < p.T;
+         t += (int64_t)G * gridDim.x, par ^= 1) {
         const int64_t row_elem = t * p.H;
         float ss = 0.f;
         for (int c = 0; c < nchunks; ++c) {
-            const bool ok = wait_bounded(smem_addr(&full[stage]), phase, abort_flag, p.watchdog,
+            const bool ok = wait_bounded(smem_addr(&gfull[stage]), phase, abort_flag, p.watchdog,
                                          kWatchConsumer);
             const int pk = c * kConsumers + j;
             if (ok && pk < nv) {
@@ -250,32 +252,32 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(Problem p, int stages) {
                     DT<T>::unpack(*reinterpret_cast<const uint4 *>(sb), acc);
 #pragma unroll 4
                     for (int s = 1; s < ns; ++s) {
-                        float f[EPV];
-                        DT<T>::unpack(*reinterpret_cast<const uint4 *>(sb + s * kChunkBytes), f);
+                        float f2[EPV];
+                        DT<T>::unpack(*reinterpret_cast<const uint4 *>(sb + s * kChunkBytes), f2);
 #pragma unroll
-                        for (int e = 0; e < EPV; ++e) acc[e] = acc[e] + f[e];
+                        for (int e = 0; e < EPV; ++e) acc[e] = acc[e] + f2[e];
                     }
                     hv = DT<T>::pack(acc);  // the one rounding to the storage type
                     st_global(reinterpret_cast<T *>(p.residual) + row_elem + (int64_t)pk * EPV,
                               hv);
                 }
                 row_copy[pk] = hv;
-                float f[EPV];
-                DT<T>::unpack(hv, f);
+                float h[EPV];
+                DT<T>::unpack(hv, h);
 #pragma unroll
-                for (int e = 0; e < EPV; ++e) ss += f[e] * f[e];
+                for (int e = 0; e < EPV; ++e) ss += h[e] * h[e];
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&empty[stage]));
+            if (lane == 0) mbar_arrive(smem_addr(&gempty[stage]));
             if (++stage == stages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
-        // row sum of squares over the 8 consumer warps
+        // row sum of squares over the group's 8 warps
         ss = warp_sum(ss);
         if (lane == 0) red[par * kConsumerWarps + cw] = ss;
-        named_barrier_consumers();
+        named_barrier(1 + g);
         float tot = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) tot += red[par * kConsumerWarps + w];
@@ -295,32 +297,33 @@ __global__ void __launch_bounds__(kThreads, 1) k_stream(Problem p, int stages) {
 
 }  // namespace stream
 
-template <typename T>
-cudaError_t launch_stream(const Problem &p, const Plan &pl, cudaStream_t st) {
-    const int smem = pl.smem;
-    cudaError_t e;
-    switch (p.op) {
-    case OP_PLAIN:
-        e = cudaFuncSetAttribute(stream::k_stream<T, OP_PLAIN>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        stream::k_stream<T, OP_PLAIN><<<pl.grid, stream::kThreads, smem, st>>>(p, pl.stages);
-        break;
-    case OP_FUSED:
-        e = cudaFuncSetAttribute(stream::k_stream<T, OP_FUSED>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        stream::k_stream<T, OP_FUSED><<<pl.grid, stream::kThreads, smem, st>>>(p, pl.stages);
-        break;
-    case OP_REDUCE:
-        e = cudaFuncSetAttribute(stream::k_stream<T, OP_REDUCE>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        stream::k_stream<T, OP_REDUCE><<<pl.grid, stream::kThreads, smem, st>>>(p, pl.stages);
-        break;
+template <typename T, int OP, int G>
+static cudaError_t launch_stream_g(const Problem &p, const Plan &pl, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(stream::k_stream<T, OP, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
+    if (e != cudaSuccess) return e;
+    stream::k_stream<T, OP, G><<<pl.grid, stream::threads(G), pl.smem, st>>>(p, pl.stages);
+    return cudaGetLastError();
+}
+
+template <typename T, int OP>
+static cudaError_t launch_stream_op(const Problem &p, const Plan &pl, cudaStream_t st) {
+    switch (pl.groups) {
+    case 1: return launch_stream_g<T, OP, 1>(p, pl, st);
+    case 2: return launch_stream_g<T, OP, 2>(p, pl, st);
+    case 3: return launch_stream_g<T, OP, 3>(p, pl, st);
     default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_stream(const Problem &p, const Plan &pl, cudaStream_t st) {
+    switch (p.op) {
+    case OP_PLAIN: return launch_stream_op<T, OP_PLAIN>(p, pl, st);
+    case OP_FUSED: return launch_stream_op<T, OP_FUSED>(p, pl, st);
+    case OP_REDUCE: return launch_stream_op<T, OP_REDUCE>(p, pl, st);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace rarn
