@@ -47,6 +47,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--path", choices=["auto", "rows", "stream", "cluster"], default="auto",
+                    help="kernel family (default: the library's own choice)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -410,6 +412,7 @@ def main():
     from residual_add_rmsnorm_gb300 import workloads as W
     rbuild.build()
 
+    rarn.set_path(args.path)
     w = W.BY_NAME[args.workload]
     data = W.generate(w)
     tensors = device_tensors(w, data, device)
@@ -442,6 +445,7 @@ def main():
         l2 = int(getattr(props, "L2_cache_size", 128 << 20))
         del tensors, call
         torch.cuda.empty_cache()
+        rarn.set_path("auto")
         for cw in W.CONFIGS:
             cd = W.generate(cw)
             us, copies, n = time_graph(cw, cd, device, l2)

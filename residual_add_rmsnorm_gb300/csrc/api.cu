@@ -116,29 +116,41 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
 constexpr int64_t kStreamMaxRowBytes = 96 * 1024;
 constexpr int kDefaultMaxSmem = 232448;  // opt-in shared memory per CTA on sm_100 / sm_103
 
+// Packs per consumer thread per chunk: as large as the row allows (fewer,
+// larger copies per producer iteration) while at least `min_stages` stages
+// fit.  RARN_STREAM_PPT (1, 2, 4) overrides it for measurements.
 Plan plan_stream(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_sms,
                  int max_smem, int groups) {
     Plan pl;
     const int64_t row_bytes = H * s;
     if (!vec || row_bytes > kStreamMaxRowBytes) return pl;
     const int ns = op == OP_PLAIN ? 1 : R + 1;
-    // fewer groups when their rings and row copies would not fit
-    for (; groups >= 1; --groups) {
-        int stages = stream::kMaxStages / groups;  // per group
-        while (stages >= 2 &&
-               stream::layout(stages, ns, (int)row_bytes, groups).total > max_smem)
-            --stages;
-        if (stages < 2) continue;
-        pl.kind = KIND_STREAM;
-        pl.vec = true;
-        pl.per_thread = 1;
-        pl.groups = groups;
-        pl.block = stream::threads(groups);
-        pl.grid = (int)std::min<int64_t>(T, num_sms);
-        pl.stages = stages;
-        pl.chunk = stream::kChunkBytes;
-        pl.smem = stream::layout(stages, ns, (int)row_bytes, groups).total;
-        return pl;
+    const int64_t nv = row_bytes / 16;
+    int ppt = std::min<int64_t>(stream::kMaxPacksPerThread,
+                                pow2_at_least(ceil_div(nv, stream::kConsumers)));
+    if (const char *v = getenv("RARN_STREAM_PPT")) {
+        const int f = atoi(v);
+        if (f == 1 || f == 2 || f == 4) ppt = f;
+    }
+    for (; ppt >= 1; ppt >>= 1) {
+        const int chunk = stream::chunk_bytes(ppt);
+        for (int g = groups; g >= 1; --g) {
+            int stages = stream::kMaxStages / g;  // per group
+            while (stages >= 2 &&
+                   stream::layout(stages, ns, (int)row_bytes, g, chunk).total > max_smem)
+                --stages;
+            if (stages < 2 || (ppt > 1 && stages < 4)) continue;
+            pl.kind = KIND_STREAM;
+            pl.vec = true;
+            pl.per_thread = ppt;
+            pl.groups = g;
+            pl.block = stream::threads(g);
+            pl.grid = (int)std::min<int64_t>(T, num_sms);
+            pl.stages = stages;
+            pl.chunk = chunk;
+            pl.smem = stream::layout(stages, ns, (int)row_bytes, g, chunk).total;
+            return pl;
+        }
     }
     return Plan{};
 }
@@ -173,13 +185,45 @@ Plan plan_cluster(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
     return pl;
 }
 
-// Consumer groups of the stream kernel: RARN_STREAM_GROUPS (1..3) overrides
-// the default for measurements; read on every plan.
-int stream_groups() {
+// Consumer groups of the stream kernel when it is forced: RARN_STREAM_GROUPS
+// (1..2) overrides the default for measurements; read on every plan.
+int stream_groups(int fallback) {
     const char *v = getenv("RARN_STREAM_GROUPS");
-    if (!v || !*v) return 2;
+    if (!v || !*v) return fallback;
     const int g = atoi(v);
     return g < 1 ? 1 : g > stream::kMaxGroups ? stream::kMaxGroups : g;
+}
+
+// The automatic choice, from measurements on GB300 (cold L2, CUDA-graph
+// timing; see the sweep in the design notes):
+//  * enough rows to give every SM several (T >= 2 x #SM) and 16-byte rows:
+//      - reduce (R >= 2): the TMA-fed stream kernel; it keeps R + 1 input
+//        streams in flight without spending registers on them (one consumer
+//        group from R >= 4, two below);
+//      - fused with rows of 16 KB and more: the stream kernel (two groups
+//        below 32 KB rows, one above);
+//      - plain with rows beyond the register kernels (> 16 KB): the stream
+//        kernel;
+//  * otherwise the register kernels: warp per row for short rows, CTA per
+//    row, and a cluster per row where one CTA's registers cannot hold it.
+Plan plan_auto(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_sms, int max_smem) {
+    const int64_t row_bytes = H * s;
+    if (vec && T >= 2 * (int64_t)num_sms) {
+        int groups = 0;
+        if (op == OP_REDUCE && R >= 2) groups = R >= 4 ? 1 : 2;
+        if (op == OP_FUSED && row_bytes >= 16 * 1024) groups = row_bytes >= 32 * 1024 ? 1 : 2;
+        if (op == OP_PLAIN && row_bytes > 16 * 1024) groups = 1;
+        if (groups) {
+            Plan st = plan_stream(op, T, H, R, s, vec, num_sms, max_smem, groups);
+            if (st.kind != KIND_NONE) return st;
+        }
+    }
+    Plan r = plan_rows(op, T, H, s, vec, num_sms);
+    if (r.kind == KIND_TWO_PASS && vec) {
+        Plan c = plan_cluster(op, T, H, s, vec, num_sms);
+        if (c.kind != KIND_NONE) return c;
+    }
+    return r;
 }
 
 Plan make_plan(int op, int64_t T, int64_t H, int R, rarn_dtype dt, bool vec, int num_sms,
@@ -188,16 +232,9 @@ Plan make_plan(int op, int64_t T, int64_t H, int R, rarn_dtype dt, bool vec, int
     switch (path) {
     case RARN_PATH_ROWS: return plan_rows(op, T, H, s, vec, num_sms);
     case RARN_PATH_STREAM:
-        return plan_stream(op, T, H, R, s, vec, num_sms, max_smem, stream_groups());
+        return plan_stream(op, T, H, R, s, vec, num_sms, max_smem, stream_groups(1));
     case RARN_PATH_CLUSTER: return plan_cluster(op, T, H, s, vec, num_sms);
-    case RARN_PATH_AUTO: {
-        Plan r = plan_rows(op, T, H, s, vec, num_sms);
-        if (r.kind == KIND_TWO_PASS && vec) {
-            Plan c = plan_cluster(op, T, H, s, vec, num_sms);
-            if (c.kind != KIND_NONE) return c;
-        }
-        return r;
-    }
+    case RARN_PATH_AUTO: return plan_auto(op, T, H, R, s, vec, num_sms, max_smem);
     default: return Plan{};
     }
 }

@@ -42,35 +42,40 @@ __host__ __device__ constexpr int rows_max_block(int F) {
 // Shape of the TMA-fed persistent kernel (stream.cuh), shared with the planner.
 namespace stream {
 constexpr int kConsumerWarps = 8;                // per consumer group
-constexpr int kConsumers = kConsumerWarps * 32;  // threads per group = packs per chunk
-constexpr int kChunkBytes = kConsumers * 16;     // per stream per stage
+constexpr int kConsumers = kConsumerWarps * 32;  // threads per group
+constexpr int kPackBytes = 16;
 constexpr int kMaxStages = 32;
-constexpr int kMaxGroups = 3;
+constexpr int kMaxGroups = 2;
+constexpr int kMaxPacksPerThread = 4;            // per chunk
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr unsigned int kWatchConsumer = 1u, kWatchProducer = 2u;
 
 __host__ __device__ constexpr int threads(int groups) { return 32 + groups * kConsumers; }
+// Bytes of one stream's chunk when each consumer thread takes `ppt` packs.
+__host__ __device__ constexpr int chunk_bytes(int ppt) { return kConsumers * ppt * kPackBytes; }
 
 // Dynamic shared memory layout (all offsets 128-byte aligned), per consumer
-// group g < G its own ring of `stages` stages:
-//   [g * stages * NS * kChunkBytes, ...)   group g's stage ring
+// group g < G its own ring of `stages` stages of NS chunks:
+//   [g * stages * NS * chunk, ...)   group g's stage ring
 //   G x row copy (H * sizeof(T) bytes each)
 //   control: full[G * stages], empty[G * stages] mbarriers (G * stages <=
 //            kMaxStages), red[G][2][kConsumerWarps] floats, abort word
 struct Layout {
-    int stages, ns, row_bytes, groups;
+    int stages, ns, row_bytes, groups, chunk;
     int ring_stride, row_off, row_stride, ctl_off, total;
 };
 
 __host__ __device__ inline int align128(int v) { return (v + 127) & ~127; }
 
-__host__ __device__ inline Layout layout(int stages, int ns, int row_bytes, int groups) {
+__host__ __device__ inline Layout layout(int stages, int ns, int row_bytes, int groups,
+                                         int chunk) {
     Layout L;
     L.stages = stages;
     L.ns = ns;
     L.row_bytes = row_bytes;
     L.groups = groups;
-    L.ring_stride = stages * ns * kChunkBytes;
+    L.chunk = chunk;
+    L.ring_stride = stages * ns * chunk;
     L.row_off = align128(groups * L.ring_stride);
     L.row_stride = align128(row_bytes);
     L.ctl_off = L.row_off + groups * L.row_stride;

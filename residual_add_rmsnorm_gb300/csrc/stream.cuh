@@ -3,7 +3,7 @@
 // One CTA per SM walks rows t = blockIdx.x, blockIdx.x + gridDim.x, ...
 // Warp 0 is the producer: one elected lane issues cp.async.bulk copies of each
 // row's input streams (x; or the R partials and the residual) in chunks of
-// 256 x 16 bytes per stream into a ring of shared-memory stages, each stage
+// 256 x PPT x 16 bytes per stream into a ring of shared-memory stages, each stage
 // guarded by a "full" mbarrier (completed by the copies' byte count) and an
 // "empty" mbarrier (released by the consumer warps).  The producer runs ahead
 // across row boundaries, so HBM reads stay in flight while the consumers
@@ -137,15 +137,21 @@ __device__ __forceinline__ void named_barrier(int id) {
 // parity wait is never more than one phase ahead of its barrier: fill n of a
 // ring lands in stage n % stages during that stage's phase n / stages, and
 // fill n - stages of the same stage was consumed before fill n is waited on.
-template <typename T, int OP, int G>
+//
+// A chunk is 256 * PPT packs of every input stream; consumer thread j takes
+// packs c * 256 * PPT + m * 256 + j (m < PPT), i.e. over the whole row the
+// packs j, j + 256, j + 512, ... -- the same packs it normalises later.
+template <typename T, int OP, int G, int PPT>
 __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages) {
     constexpr int EPV = DT<T>::EPV;
+    constexpr int CP = kConsumers * PPT;      // packs per chunk
+    constexpr int CB = CP * kPackBytes;       // bytes per stream per chunk
     extern __shared__ __align__(128) unsigned char smem[];
     const int ns = OP == OP_PLAIN ? 1 : p.R + 1;  // input streams
     const int row_bytes = (int)(p.H * (int64_t)sizeof(T));
-    const int nv = row_bytes / 16;                // packs per row
-    const int nchunks = (nv + kConsumers - 1) / kConsumers;
-    const Layout L = layout(stages, ns, row_bytes, G);
+    const int nv = row_bytes / kPackBytes;        // packs per row
+    const int nchunks = (nv + CP - 1) / CP;
+    const Layout L = layout(stages, ns, row_bytes, G, CB);
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.ctl_off);   // [G][stages]
     uint64_t *empty = full + kMaxStages;                                // [G][stages]
     float *red_all = reinterpret_cast<float *>(empty + kMaxStages);  // [G][2][kConsumerWarps]
@@ -167,43 +173,33 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
-        int stage[G];
-        uint32_t phase[G];
-        long long issued[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            stage[g] = 0;
-            phase[g] = 0;
-            issued[g] = 0;
-        }
+        long long issued0 = 0, issued1 = 0;  // fills issued into ring 0 / ring 1
         bool ok = true;
         int g = 0;
         for (int64_t t = blockIdx.x; t < p.T && ok; t += gridDim.x) {
             const int64_t row_elem = t * p.H;
-            for (int c = 0; c < nchunks && ok; ++c) {
-                const int packs = min(kConsumers, nv - c * kConsumers);
-                const uint32_t bytes = (uint32_t)packs * 16u;
-                const int b = g * stages + stage[g];
-                ok = wait_bounded(smem_addr(&empty[b]), phase[g] ^ 1u, abort_flag, p.watchdog,
+            long long &n = g == 0 ? issued0 : issued1;
+            for (int c = 0; c < nchunks && ok; ++c, ++n) {
+                const int packs = min(CP, nv - c * CP);
+                const uint32_t bytes = (uint32_t)packs * kPackBytes;
+                const int st = (int)(n % stages);
+                const uint32_t ph = (uint32_t)((n / stages) & 1);
+                const int b = g * stages + st;
+                ok = wait_bounded(smem_addr(&empty[b]), ph ^ 1u, abort_flag, p.watchdog,
                                   kWatchProducer);
                 if (!ok) break;
                 const uint32_t fb = smem_addr(&full[b]);
                 mbar_arrive_expect_tx(fb, bytes * (uint32_t)ns);
-                const uint32_t dst = smem_addr(smem + (size_t)g * L.ring_stride +
-                                               (size_t)stage[g] * ns * kChunkBytes);
-                const int64_t off = row_elem + (int64_t)c * kConsumers * EPV;
+                const uint32_t dst =
+                    smem_addr(smem + (size_t)g * L.ring_stride + (size_t)st * ns * CB);
+                const int64_t off = row_elem + (int64_t)c * CP * EPV;
                 for (int s = 0; s < ns; ++s) {
                     const T *src;
                     if (OP != OP_PLAIN && s == ns - 1)
                         src = reinterpret_cast<const T *>(p.residual) + off;
                     else
                         src = reinterpret_cast<const T *>(p.src) + (int64_t)s * p.slice + off;
-                    bulk_g2s(dst + (uint32_t)(s * kChunkBytes), src, bytes, fb);
-                }
-                ++issued[g];
-                if (++stage[g] == stages) {
-                    stage[g] = 0;
-                    phase[g] ^= 1u;
+                    bulk_g2s(dst + (uint32_t)(s * CB), src, bytes, fb);
                 }
             }
             if (++g == G) g = 0;
@@ -212,8 +208,9 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
         // before the CTA exits.
         const unsigned long long deadline = global_ns() + kWaitLimitNs;
         for (int r = 0; r < G; ++r) {
-            const long long first = issued[r] > stages ? issued[r] - stages : 0;
-            for (long long f = first; f < issued[r]; ++f)
+            const long long issued = r == 0 ? issued0 : issued1;
+            const long long first = issued > stages ? issued - stages : 0;
+            for (long long f = first; f < issued; ++f)
                 if (!wait_drain(smem_addr(&full[r * stages + (int)(f % stages)]),
                                 (uint32_t)((f / stages) & 1), deadline, p.watchdog))
                     return;
@@ -231,6 +228,7 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
     uint4 *row_copy = reinterpret_cast<uint4 *>(smem + L.row_off + g * L.row_stride);
     float *red = red_all + g * 2 * kConsumerWarps;
     const T *gamma = reinterpret_cast<const T *>(p.gamma);
+    T *residual = reinterpret_cast<T *>(p.residual);
     int stage = 0;
     uint32_t phase = 0;
     int par = 0;
@@ -241,9 +239,13 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
         for (int c = 0; c < nchunks; ++c) {
             const bool ok = wait_bounded(smem_addr(&gfull[stage]), phase, abort_flag, p.watchdog,
                                          kWatchConsumer);
-            const int pk = c * kConsumers + j;
-            if (ok && pk < nv) {
-                const unsigned char *sb = ring + (size_t)stage * ns * kChunkBytes + j * 16;
+            const unsigned char *sbase = ring + (size_t)stage * ns * CB;
+#pragma unroll
+            for (int m = 0; m < PPT; ++m) {
+                const int q = m * kConsumers + j;  // pack within the chunk
+                const int pk = c * CP + q;         // pack within the row
+                if (!ok || pk >= nv) continue;
+                const unsigned char *sb = sbase + q * kPackBytes;
                 uint4 hv;
                 if (OP == OP_PLAIN) {
                     hv = *reinterpret_cast<const uint4 *>(sb);
@@ -253,13 +255,12 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
 #pragma unroll 4
                     for (int s = 1; s < ns; ++s) {
                         float f2[EPV];
-                        DT<T>::unpack(*reinterpret_cast<const uint4 *>(sb + s * kChunkBytes), f2);
+                        DT<T>::unpack(*reinterpret_cast<const uint4 *>(sb + s * CB), f2);
 #pragma unroll
                         for (int e = 0; e < EPV; ++e) acc[e] = acc[e] + f2[e];
                     }
                     hv = DT<T>::pack(acc);  // the one rounding to the storage type
-                    st_global(reinterpret_cast<T *>(p.residual) + row_elem + (int64_t)pk * EPV,
-                              hv);
+                    st_global(residual + row_elem + (int64_t)pk * EPV, hv);
                 }
                 row_copy[pk] = hv;
                 float h[EPV];
@@ -297,13 +298,23 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
 
 }  // namespace stream
 
-template <typename T, int OP, int G>
-static cudaError_t launch_stream_g(const Problem &p, const Plan &pl, cudaStream_t st) {
-    cudaError_t e = cudaFuncSetAttribute(stream::k_stream<T, OP, G>,
+template <typename T, int OP, int G, int PPT>
+static cudaError_t launch_stream_k(const Problem &p, const Plan &pl, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(stream::k_stream<T, OP, G, PPT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
     if (e != cudaSuccess) return e;
-    stream::k_stream<T, OP, G><<<pl.grid, stream::threads(G), pl.smem, st>>>(p, pl.stages);
+    stream::k_stream<T, OP, G, PPT><<<pl.grid, stream::threads(G), pl.smem, st>>>(p, pl.stages);
     return cudaGetLastError();
+}
+
+template <typename T, int OP, int G>
+static cudaError_t launch_stream_g(const Problem &p, const Plan &pl, cudaStream_t st) {
+    switch (pl.per_thread) {
+    case 1: return launch_stream_k<T, OP, G, 1>(p, pl, st);
+    case 2: return launch_stream_k<T, OP, G, 2>(p, pl, st);
+    case 4: return launch_stream_k<T, OP, G, 4>(p, pl, st);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 template <typename T, int OP>
@@ -311,7 +322,6 @@ static cudaError_t launch_stream_op(const Problem &p, const Plan &pl, cudaStream
     switch (pl.groups) {
     case 1: return launch_stream_g<T, OP, 1>(p, pl, st);
     case 2: return launch_stream_g<T, OP, 2>(p, pl, st);
-    case 3: return launch_stream_g<T, OP, 3>(p, pl, st);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -152,3 +152,26 @@ def test_header_declares_three_compute_calls():
     names = declared_functions()
     for n in ("rarn_rms_norm", "rarn_fused_add_rms_norm", "rarn_reduce_add_rms_norm"):
         assert n in names
+
+
+def test_plan_auto_policy():
+    """The automatic choice per shape (152 SMs)."""
+    assert rarn.get_path() == "auto"
+    # R = 8 reduce at full size: the TMA-fed stream kernel, one consumer group
+    p = _plan("reduce_add_rms_norm", 8192, 8192, 8, "bf16")
+    assert p.startswith("stream") and "groups=1" in p, p
+    # R = 2 reduce: stream kernel with two consumer groups
+    p = _plan("reduce_add_rms_norm", 16384, 4096, 2, "bf16")
+    assert p.startswith("stream") and "groups=2" in p, p
+    # fused with 8 KB rows: register kernel; with 16 KB rows: stream
+    assert _plan("fused_add_rms_norm", 4096, 4096, 1, "bf16").startswith("rows.cta")
+    assert _plan("fused_add_rms_norm", 4096, 8192, 1, "bf16").startswith("stream")
+    # few rows: never the persistent kernel
+    assert _plan("reduce_add_rms_norm", 64, 8192, 8, "bf16").startswith("rows")
+    # long rows, few of them: a cluster per row
+    p = _plan("fused_add_rms_norm", 64, 16384, 1, "bf16")
+    assert p.startswith("cluster") and "cluster=4" in p, p
+    # unaligned: scalar register kernels whatever the size
+    assert "scalar" in _plan("reduce_add_rms_norm", 8192, 8192, 8, "bf16", vec=False)
+    # plain: register kernel
+    assert _plan("rms_norm", 16384, 4096, 0, "bf16").startswith("rows.cta")

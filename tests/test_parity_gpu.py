@@ -248,12 +248,15 @@ def test_watchdog_clear_after_everything():
     assert rarn.watchdog(clear=True) == 0
 
 
-@pytest.mark.parametrize("groups", [1, 2, 3])
-def test_stream_consumer_groups(groups, monkeypatch):
-    """The TMA-fed kernel with 1, 2 and 3 consumer groups (rows handed out
-    round-robin), including row counts that are not a multiple of the grid
-    times the group count, and rows of one, several and a partial chunk."""
+@pytest.mark.parametrize("ppt", [1, 2, 4])
+@pytest.mark.parametrize("groups", [1, 2])
+def test_stream_consumer_groups(groups, ppt, monkeypatch):
+    """The TMA-fed kernel with 1 and 2 consumer groups (rows handed out
+    round-robin) and 1, 2, 4 packs per thread per chunk, including row
+    counts that are not a multiple of the grid times the group count, and
+    rows of one, several and a partial chunk."""
     monkeypatch.setenv("RARN_STREAM_GROUPS", str(groups))
+    monkeypatch.setenv("RARN_STREAM_PPT", str(ppt))
     rarn.set_path("stream")
     for op, dt, T, H, R in (("fused_add_rms_norm", "bf16", 1001, 4096, 1),
                             ("reduce_add_rms_norm", "bf16", 777, 2048, 8),
@@ -261,7 +264,7 @@ def test_stream_consumer_groups(groups, monkeypatch):
                             ("rms_norm", "f32", 999, 1592, 0),
                             ("fused_add_rms_norm", "bf16", 157, 32768, 1),
                             ("fused_add_rms_norm", "f32", 5, 200, 1)):
-        w = W.workload(op, dt, T, H, R=R, eps=1e-6, seed=groups)
+        w = W.workload(op, dt, T, H, R=R, eps=1e-6, seed=groups * 10 + ppt)
         plan = rarn.plan(op, T, H, max(R, 1), dt)
         assert plan.startswith("stream"), plan
         check_parity(w, W.generate(w), what=f"stream G{groups} {op} {dt} T{T} H{H}")
