@@ -89,16 +89,22 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
         pl.kind = KIND_WARP;
         pl.per_thread = n <= 32 ? 1 : n <= 64 ? 2 : 4;
         pl.block = 256;
-        const int64_t rows_per_cta = pl.block / 32;
-        pl.grid = (int)std::min<int64_t>(ceil_div(T, rows_per_cta),
-                                          (int64_t)num_sms * (resident_threads / pl.block));
+        // one warp per row; balanced like the CTA grid below
+        const int64_t slots = (int64_t)num_sms * (resident_threads / 32);
+        const int64_t rounds = ceil_div(T, slots);
+        pl.grid = (int)ceil_div(ceil_div(T, rounds), pl.block / 32);
         return pl;
     }
-    // values per thread: aim at 256 threads per row, powers of two
+    // values per thread: aim at 256 threads per row, powers of two, within
+    // the register budget of the kernel compiled for that count
+    auto max_block = [&](int pt, bool pg) {
+        return vec ? rows_max_block(rows_regs_vec(pt, epv, op, pg))
+                   : (pg ? 0 : rows_max_block(rows_regs_scalar(pt, op)));
+    };
     const int max_pt = vec ? 8 : 16;
     int pt = std::min(max_pt, pow2_at_least(ceil_div(n, 256)));
-    while (pt < max_pt && ceil_div(n, pt) > rows_max_block(pt * epv)) pt <<= 1;
-    if (ceil_div(n, pt) > rows_max_block(pt * epv)) {
+    while (pt < max_pt && ceil_div(n, pt) > max_block(pt, false)) pt <<= 1;
+    if (ceil_div(n, pt) > max_block(pt, false)) {
         pl.kind = KIND_TWO_PASS;
         pl.per_thread = 1;
         pl.block = 1024;
@@ -107,7 +113,17 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
         pl.per_thread = pt;
         pl.block = round_up(ceil_div(n, pt), 32);
     }
-    pl.grid = (int)std::min<int64_t>(T, (int64_t)num_sms * std::max(1, resident_threads / pl.block));
+    // Balanced grid: every CTA gets ceil(T / slots) or one fewer rows, so the
+    // last round is not a ragged partial wave (T = 4096 on 1216 slots would
+    // otherwise leave 3 full rounds and a 37 % fourth one).
+    const int64_t slots = (int64_t)num_sms * std::max(1, resident_threads / pl.block);
+    const int64_t rounds = ceil_div(T, slots);
+    pl.grid = (int)ceil_div(T, rounds);
+    // Gamma in registers when every CTA has a single row (latency-bound: the
+    // gamma load then overlaps the row's loads instead of following the row
+    // reduction) and the kernel's register budget allows it.
+    pl.prefetch_gamma =
+        pl.kind == KIND_CTA && pl.vec && rounds == 1 && pl.block <= max_block(pl.per_thread, true);
     return pl;
 }
 
@@ -164,9 +180,12 @@ Plan plan_cluster(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
     const int64_t n = H / epv;
     for (int cs = 2; cs <= 8; cs <<= 1) {
         const int64_t seg = ceil_div(n, cs);
+        auto max_block = [&](int p, bool pg) {
+            return rows_max_block(rows_regs_vec(p, epv, op, pg));
+        };
         int pt = std::min(8, pow2_at_least(ceil_div(seg, 256)));
-        while (pt < 8 && ceil_div(seg, pt) > rows_max_block(pt * epv)) pt <<= 1;
-        if (ceil_div(seg, pt) > rows_max_block(pt * epv)) continue;
+        while (pt < 8 && ceil_div(seg, pt) > max_block(pt, false)) pt <<= 1;
+        if (ceil_div(seg, pt) > max_block(pt, false)) continue;
         const bool fills = T * cs >= num_sms;
         if (!fills && cs < 8) {
             // a larger cluster spreads the rows over more SMs; keep looking
@@ -178,8 +197,11 @@ Plan plan_cluster(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
         pl.cluster = cs;
         pl.per_thread = pt;
         pl.block = round_up(ceil_div(seg, pt), 32);
-        const int64_t resident = (int64_t)num_sms * std::max(1, 2048 / pl.block) / cs;
-        pl.grid = (int)(std::min<int64_t>(T, std::max<int64_t>(1, resident)) * cs);
+        const int64_t resident =
+            std::max<int64_t>(1, (int64_t)num_sms * std::max(1, 2048 / pl.block) / cs);
+        const int64_t rounds = ceil_div(T, resident);
+        pl.grid = (int)(ceil_div(T, rounds) * cs);
+        pl.prefetch_gamma = rounds == 1 && pl.block <= max_block(pt, true);
         return pl;
     }
     return pl;
@@ -400,9 +422,9 @@ rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt
     const Plan pl = make_plan((int)op, T, H, R, dt, vec, num_sms, max_smem, g_path.load());
     snprintf(out, cap,
              "%s %s per_thread=%d block=%d grid=%d cluster=%d smem=%d stages=%d chunk=%d "
-             "groups=%d",
+             "groups=%d gamma_regs=%d",
              kind_name(pl.kind), pl.vec ? "vec16" : "scalar", pl.per_thread, pl.block, pl.grid,
-             pl.cluster, pl.smem, pl.stages, pl.chunk, pl.groups);
+             pl.cluster, pl.smem, pl.stages, pl.chunk, pl.groups, (int)pl.prefetch_gamma);
     return pl.kind == KIND_NONE ? RARN_ERR_UNSUPPORTED : RARN_OK;
 }
 

@@ -45,8 +45,8 @@ __device__ __forceinline__ float ld_peer(const float *local, uint32_t rank) {
     return v;
 }
 
-template <typename T, int VPT, int OP>
-__global__ void __launch_bounds__(VecBound<T, VPT>::value) k_cluster_vec(Problem p) {
+template <typename T, int VPT, int OP, bool PG>
+__global__ void __launch_bounds__(VecBound<T, VPT, OP, PG>::value) k_cluster_vec(Problem p) {
     __shared__ float red[2][32];
     __shared__ float part[2];
     const uint32_t rank = cluster_ctarank(), cs = cluster_nctarank();
@@ -55,6 +55,8 @@ __global__ void __launch_bounds__(VecBound<T, VPT>::value) k_cluster_vec(Problem
     const int j_begin = (int)rank * seg;
     const int j_end = min(nv, j_begin + seg);
     const int64_t first = blockIdx.x / cs, step = gridDim.x / cs;
+    uint4 gv[VPT];  // PG: this thread's gamma packs, the same for every row
+    if (PG) load_gamma_vec<T, VPT>(p, j_begin + threadIdx.x, blockDim.x, j_end, gv);
     int par = 0;
     for (int64_t t = first; t < p.T; t += step, par ^= 1) {
         uint4 hv[VPT];
@@ -66,7 +68,7 @@ __global__ void __launch_bounds__(VecBound<T, VPT>::value) k_cluster_vec(Problem
         float tot = 0.f;
         for (uint32_t r = 0; r < cs; ++r) tot += ld_peer(&part[par], r);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_vec<T, VPT>(p, t, j_begin + threadIdx.x, blockDim.x, j_end, hv, inv);
+        pass2_vec<T, VPT, PG>(p, t, j_begin + threadIdx.x, blockDim.x, j_end, hv, inv, gv);
     }
     // no CTA leaves while a peer may still read its partials
     cluster_sync();
@@ -86,11 +88,20 @@ static cudaError_t launch_cluster_op(const Problem &p, const Plan &pl, cudaStrea
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (pl.prefetch_gamma) {
+        switch (pl.per_thread) {
+        case 1: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 1, OP, true>, p);
+        case 2: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 2, OP, true>, p);
+        case 4: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 4, OP, true>, p);
+        case 8: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 8, OP, true>, p);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (pl.per_thread) {
-    case 1: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 1, OP>, p);
-    case 2: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 2, OP>, p);
-    case 4: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 4, OP>, p);
-    case 8: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 8, OP>, p);
+    case 1: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 1, OP, false>, p);
+    case 2: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 2, OP, false>, p);
+    case 4: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 4, OP, false>, p);
+    case 8: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 8, OP, false>, p);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -29,14 +29,29 @@ struct Plan {
     int stages = 0;      // pipeline depth (stream kernel)
     int chunk = 0;       // bytes per stream per pipeline stage (stream kernel)
     int groups = 1;      // consumer groups (stream kernel)
+    bool prefetch_gamma = false;  // CTA register kernel keeps gamma in registers
 };
 
-// Largest CTA the register row kernels are compiled for, by the number of row
-// values F each thread holds (16-byte packs x elements per pack, or single
-// elements).  Keeps the pass-1 accumulators, load buffers and the staged row
-// in registers without spilling.
-__host__ __device__ constexpr int rows_max_block(int F) {
-    return F <= 8 ? 1024 : F <= 16 ? 512 : F <= 32 ? 256 : 128;
+// Register budget of the register-staged row kernels.  A thread holding P
+// 16-byte packs of the row keeps, per pack: the load buffers of `rc` streams
+// loaded together (4 registers each), the binary32 accumulators (EPV), the
+// rounded row (4) and, if gamma is held in registers, gamma (4); about 32
+// more for addresses and loop state.  Single-element kernels hold one value
+// per stream buffer, accumulator and row copy.  The CTA size a kernel is
+// compiled for follows from 64 K registers per SM (and at most 255 per
+// thread); 0 means the combination is not built.
+__host__ __device__ constexpr int rows_loads_together(int op) { return op == 2 ? 4 : op == 1 ? 2 : 1; }
+
+__host__ __device__ constexpr int rows_regs_vec(int P, int epv, int op, bool gamma_regs) {
+    return P * (4 * rows_loads_together(op) + epv + 4 + (gamma_regs ? 4 : 0)) + 32;
+}
+
+__host__ __device__ constexpr int rows_regs_scalar(int NE, int op) {
+    return NE * (rows_loads_together(op) + 2) + 32;
+}
+
+__host__ __device__ constexpr int rows_max_block(int regs) {
+    return regs <= 64 ? 1024 : regs <= 128 ? 512 : regs <= 256 ? 256 : 0;
 }
 
 // Shape of the TMA-fed persistent kernel (stream.cuh), shared with the planner.

@@ -114,10 +114,28 @@ __device__ __forceinline__ float pass1_vec(const Problem &p, int64_t t, int j0, 
     return ss;
 }
 
-// Pass 2, 16-byte packs: y = (h * inv) * gamma, one rounding.
+// This thread's gamma packs.  A thread owns the same packs of every row, so
+// kernels that keep gamma in registers load it once, before their first row:
+// its latency then overlaps the first row's loads instead of following the
+// row reduction.
 template <typename T, int VPT>
+__device__ __forceinline__ void load_gamma_vec(const Problem &p, int j0, int js, int nv,
+                                               uint4 (&gv)[VPT]) {
+    constexpr int EPV = DT<T>::EPV;
+    const T *g = reinterpret_cast<const T *>(p.gamma);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = j0 + k * js;
+        if (j < nv) gv[k] = ld_keep(g + (int64_t)j * EPV);
+    }
+}
+
+// Pass 2, 16-byte packs: y = (h * inv) * gamma, one rounding.  With PG the
+// gamma packs come from registers (gv), otherwise from memory (L1 / L2).
+template <typename T, int VPT, bool PG = false>
 __device__ __forceinline__ void pass2_vec(const Problem &p, int64_t t, int j0, int js, int nv,
-                                          const uint4 (&hv)[VPT], float inv) {
+                                          const uint4 (&hv)[VPT], float inv,
+                                          const uint4 *gv = nullptr) {
     constexpr int EPV = DT<T>::EPV;
     const T *g = reinterpret_cast<const T *>(p.gamma);
     T *y = reinterpret_cast<T *>(p.y) + t * p.H;
@@ -127,7 +145,7 @@ __device__ __forceinline__ void pass2_vec(const Problem &p, int64_t t, int j0, i
         if (j < nv) {
             float h[EPV], w[EPV];
             DT<T>::unpack(hv[k], h);
-            DT<T>::unpack(ld_keep(g + (int64_t)j * EPV), w);
+            DT<T>::unpack(PG ? gv[k] : ld_keep(g + (int64_t)j * EPV), w);
 #pragma unroll
             for (int e = 0; e < EPV; ++e) h[e] = (h[e] * inv) * w[e];
             st_global(y + (int64_t)j * EPV, DT<T>::pack(h));
@@ -210,22 +228,31 @@ struct Chunk {  // streams loaded together in pass 1
     static constexpr int value = OP == OP_REDUCE ? 4 : 2;
 };
 
-// Register budget: F row values per thread (packs x EPV, or elements) caps the
-// CTA size the kernel is compiled for (rows_max_block in plan.h).
-template <typename T, int VPT>
+// CTA size each register-staged kernel is compiled for (plan.h budget); a
+// combination over budget is compiled for 128 threads and never planned.
+template <typename T, int VPT, int OP, bool PG = false>
 struct VecBound {
-    static constexpr int value = rows_max_block(VPT * DT<T>::EPV);
+    static constexpr int b = rows_max_block(rows_regs_vec(VPT, DT<T>::EPV, OP, PG));
+    static constexpr int value = b > 0 ? b : 128;
+};
+
+template <int NE, int OP>
+struct ScalarBound {
+    static constexpr int b = rows_max_block(rows_regs_scalar(NE, OP));
+    static constexpr int value = b > 0 ? b : 128;
 };
 
 // ---------------------------------------------------------------------------
 // Kernels
 // ---------------------------------------------------------------------------
 
-// One CTA per row, packs.
-template <typename T, int VPT, int OP>
-__global__ void __launch_bounds__(VecBound<T, VPT>::value) k_cta_vec(Problem p) {
+// One CTA per row, packs.  PG: gamma held in registers for all rows.
+template <typename T, int VPT, int OP, bool PG>
+__global__ void __launch_bounds__(VecBound<T, VPT, OP, PG>::value) k_cta_vec(Problem p) {
     __shared__ float red[2][32];
     const int nv = (int)(p.H / DT<T>::EPV);
+    uint4 gv[VPT];
+    if (PG) load_gamma_vec<T, VPT>(p, threadIdx.x, blockDim.x, nv, gv);
     int par = 0;
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
         uint4 hv[VPT];
@@ -233,11 +260,12 @@ __global__ void __launch_bounds__(VecBound<T, VPT>::value) k_cta_vec(Problem p) 
                                                                 nv, hv);
         const float tot = block_sum(ss, red[par]);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_vec<T, VPT>(p, t, threadIdx.x, blockDim.x, nv, hv, inv);
+        pass2_vec<T, VPT, PG>(p, t, threadIdx.x, blockDim.x, nv, hv, inv, gv);
     }
 }
 
-// One warp per row, packs; blockDim.x / 32 rows per CTA at a time.
+// One warp per row, packs; blockDim.x / 32 rows per CTA at a time.  Gamma is
+// held in registers (at most 4 packs per lane).
 template <typename T, int VPT, int OP>
 __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
     const int nv = (int)(p.H / DT<T>::EPV);
@@ -245,18 +273,20 @@ __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
     const int wpb = blockDim.x >> 5;
     const int64_t first = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     const int64_t step = (int64_t)gridDim.x * wpb;
+    uint4 gv[VPT];
+    load_gamma_vec<T, VPT>(p, lane, 32, nv, gv);
     for (int64_t t = first; t < p.T; t += step) {
         uint4 hv[VPT];
         const float ss = pass1_vec<T, VPT, OP, Chunk<OP>::value>(p, t, lane, 32, nv, hv);
         const float tot = warp_sum(ss);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_vec<T, VPT>(p, t, lane, 32, nv, hv, inv);
+        pass2_vec<T, VPT, true>(p, t, lane, 32, nv, hv, inv, gv);
     }
 }
 
 // One CTA per row, single elements.
 template <typename T, int NE, int OP>
-__global__ void __launch_bounds__(rows_max_block(NE)) k_cta_scalar(Problem p) {
+__global__ void __launch_bounds__(ScalarBound<NE, OP>::value) k_cta_scalar(Problem p) {
     __shared__ float red[2][32];
     int par = 0;
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
@@ -327,12 +357,22 @@ static cudaError_t launch_rows_op(const Problem &p, const Plan &pl, cudaStream_t
         break;
     case KIND_CTA:
         if (pl.vec) {
-            switch (pl.per_thread) {
-            case 1: k_cta_vec<T, 1, OP><<<g, b, 0, st>>>(p); break;
-            case 2: k_cta_vec<T, 2, OP><<<g, b, 0, st>>>(p); break;
-            case 4: k_cta_vec<T, 4, OP><<<g, b, 0, st>>>(p); break;
-            case 8: k_cta_vec<T, 8, OP><<<g, b, 0, st>>>(p); break;
-            default: return cudaErrorInvalidValue;
+            if (pl.prefetch_gamma) {
+                switch (pl.per_thread) {
+                case 1: k_cta_vec<T, 1, OP, true><<<g, b, 0, st>>>(p); break;
+                case 2: k_cta_vec<T, 2, OP, true><<<g, b, 0, st>>>(p); break;
+                case 4: k_cta_vec<T, 4, OP, true><<<g, b, 0, st>>>(p); break;
+                case 8: k_cta_vec<T, 8, OP, true><<<g, b, 0, st>>>(p); break;
+                default: return cudaErrorInvalidValue;
+                }
+            } else {
+                switch (pl.per_thread) {
+                case 1: k_cta_vec<T, 1, OP, false><<<g, b, 0, st>>>(p); break;
+                case 2: k_cta_vec<T, 2, OP, false><<<g, b, 0, st>>>(p); break;
+                case 4: k_cta_vec<T, 4, OP, false><<<g, b, 0, st>>>(p); break;
+                case 8: k_cta_vec<T, 8, OP, false><<<g, b, 0, st>>>(p); break;
+                default: return cudaErrorInvalidValue;
+                }
             }
         } else {
             switch (pl.per_thread) {

@@ -168,9 +168,17 @@ def test_plan_auto_policy():
     assert _plan("fused_add_rms_norm", 4096, 8192, 1, "bf16").startswith("stream")
     # few rows: never the persistent kernel
     assert _plan("reduce_add_rms_norm", 64, 8192, 8, "bf16").startswith("rows")
-    # long rows, few of them: a cluster per row
+    # 32 KB rows, few of them: one CTA per row still holds the row (8 packs
+    # per thread); 64 KB rows need a cluster per row
     p = _plan("fused_add_rms_norm", 64, 16384, 1, "bf16")
-    assert p.startswith("cluster") and "cluster=4" in p, p
+    assert p.startswith("rows.cta") and "per_thread=8" in p, p
+    p = _plan("fused_add_rms_norm", 64, 32768, 1, "bf16")
+    assert p.startswith("cluster"), p
+    # a single wave keeps gamma in registers; many rounds read it from L1
+    assert "gamma_regs=1" in _plan("fused_add_rms_norm", 16, 5120, 1, "bf16")
+    assert "gamma_regs=0" in _plan("fused_add_rms_norm", 32768, 5120, 1, "bf16")
+    # balanced grid: 4096 rows on 1216 slots -> 4 rounds of 1024 CTAs
+    assert "grid=1024 " in _plan("fused_add_rms_norm", 4096, 4096, 1, "bf16")
     # unaligned: scalar register kernels whatever the size
     assert "scalar" in _plan("reduce_add_rms_norm", 8192, 8192, 8, "bf16", vec=False)
     # plain: register kernel
