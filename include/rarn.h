@@ -36,8 +36,9 @@
  *
  * Common conventions for every compute entry point:
  *   - Pointers are DEVICE pointers owned by the caller (y, x, partials,
- *     residual, gamma).  The library allocates no memory and keeps no pointer
- *     after the call returns.
+ *     residual, gamma); the *_host forms below take pinned host pointers
+ *     instead.  The library allocates no memory and keeps no pointer after
+ *     the call returns.
  *   - Layout: dense row-major.  x, residual and y are [T, H] with row stride H
  *     elements; partials is [R, T, H], partial r starting at element r*T*H;
  *     gamma is [H].  All share one storage type `dt`.  eps is binary32.
@@ -139,6 +140,34 @@ rarn_status rarn_reduce_add_rms_norm(void *y, const void *partials, int32_t R, v
                                      const void *gamma, int64_t T, int64_t H, float eps,
                                      rarn_dtype dt, void *stream);
 
+/*
+ * Host-buffer forms of the three operations: the same arguments, layout,
+ * aliasing and stream rules, but every buffer (y, x / partials, residual,
+ * gamma) is PINNED HOST memory that the current device can address:
+ * allocated with cudaHostAlloc / cudaMallocHost, or registered with
+ * cudaHostRegister and mapped.  The kernels read the inputs and write the
+ * outputs through that mapping, so the host<->device transfer happens inside
+ * the one kernel launch (over NVLink-C2C on Grace systems) and no device
+ * memory is needed.  The first and last byte of every buffer are checked
+ * with cudaPointerGetAttributes before anything is enqueued: pinned host
+ * memory is accepted; pageable host memory only where the device reads it
+ * through the host's page tables (rarn_host_access() == 2, e.g. Grace);
+ * device or managed memory, or pageable memory elsewhere, returns
+ * RARN_ERR_INVALID_ARG.  As with the device forms, the caller guarantees
+ * that each buffer really spans its full size.  Results are in
+ * host memory once the stream reaches the call.  These forms have no
+ * counterpart on the pages: they are how a caller with data in host memory
+ * runs the path without staging copies.
+ */
+rarn_status rarn_rms_norm_host(void *y, const void *x, const void *gamma, int64_t T, int64_t H,
+                               float eps, rarn_dtype dt, void *stream);
+rarn_status rarn_fused_add_rms_norm_host(void *y, const void *x, void *residual,
+                                         const void *gamma, int64_t T, int64_t H, float eps,
+                                         rarn_dtype dt, void *stream);
+rarn_status rarn_reduce_add_rms_norm_host(void *y, const void *partials, int32_t R,
+                                          void *residual, const void *gamma, int64_t T,
+                                          int64_t H, float eps, rarn_dtype dt, void *stream);
+
 /* Static text for a status code. */
 const char *rarn_status_string(rarn_status s);
 
@@ -170,6 +199,12 @@ rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt
  * `clear` is nonzero the word is reset to 0 after reading.
  */
 rarn_status rarn_watchdog(uint32_t *flags, int clear);
+
+/* Which host memory the *_host entry points can use on the current device:
+ * 2 = any host memory, pageable included (the device reaches it through the
+ * host's page tables, e.g. Grace with NVLink-C2C); 1 = pinned, mapped host
+ * memory only; 0 = none; -1 = the query failed (no device). */
+int rarn_host_access(void);
 
 /* ABI version: (major << 16) | minor. */
 int rarn_version(void);

@@ -17,7 +17,8 @@ from __future__ import annotations
 import ctypes
 import os
 
-__all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "RarnError", "library",
+__all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_host",
+           "fused_add_rms_norm_host", "reduce_add_rms_norm_host", "RarnError", "library",
            "set_path", "get_path", "plan", "watchdog", "PATHS", "DTYPE_CODES"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -59,7 +60,12 @@ def library() -> ctypes.CDLL:
     lib.rarn_rms_norm.argtypes = [vp, vp, vp, i64, i64, f32, c_int, vp]
     lib.rarn_fused_add_rms_norm.argtypes = [vp, vp, vp, vp, i64, i64, f32, c_int, vp]
     lib.rarn_reduce_add_rms_norm.argtypes = [vp, vp, i32, vp, vp, i64, i64, f32, c_int, vp]
-    for f in (lib.rarn_rms_norm, lib.rarn_fused_add_rms_norm, lib.rarn_reduce_add_rms_norm):
+    lib.rarn_rms_norm_host.argtypes = [vp, vp, vp, i64, i64, f32, c_int, vp]
+    lib.rarn_fused_add_rms_norm_host.argtypes = [vp, vp, vp, vp, i64, i64, f32, c_int, vp]
+    lib.rarn_reduce_add_rms_norm_host.argtypes = [vp, vp, i32, vp, vp, i64, i64, f32, c_int, vp]
+    for f in (lib.rarn_rms_norm, lib.rarn_fused_add_rms_norm, lib.rarn_reduce_add_rms_norm,
+              lib.rarn_rms_norm_host, lib.rarn_fused_add_rms_norm_host,
+              lib.rarn_reduce_add_rms_norm_host):
         f.restype = c_int
     lib.rarn_status_string.argtypes = [c_int]
     lib.rarn_status_string.restype = ctypes.c_char_p
@@ -76,6 +82,8 @@ def library() -> ctypes.CDLL:
     lib.rarn_watchdog.restype = c_int
     lib.rarn_version.argtypes = []
     lib.rarn_version.restype = c_int
+    lib.rarn_host_access.argtypes = []
+    lib.rarn_host_access.restype = c_int
     _lib = lib
     return lib
 
@@ -186,6 +194,80 @@ def reduce_add_rms_norm(partials, residual, gamma, eps: float, out=None):
             y.data_ptr(), partials.data_ptr(), R, residual.data_ptr(), gamma.data_ptr(), T, H,
             float(eps), _dtype_code(residual), _stream(residual.device)),
             "rarn_reduce_add_rms_norm")
+    return y
+
+
+def _check_host(name, t, dtype):
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a pinned host tensor")
+    if not t.is_pinned():
+        raise ValueError(f"{name} must be pinned (torch.Tensor.pin_memory())")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _host_call(fn, what, device):
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        _check(fn(_stream(dev)), what)
+
+
+def rms_norm_host(x, gamma, eps: float, out=None, device=None):
+    """rms_norm on pinned host tensors: the kernel on ``device`` (default:
+    the current one) reads x and gamma and writes y through their device
+    mapping; y is in host memory once that device's current stream reaches
+    the call."""
+    import torch
+    H = x.shape[-1]
+    for n, t in (("x", x), ("gamma", gamma)):
+        _check_host(n, t, x.dtype)
+    y = torch.empty_like(x).pin_memory() if out is None else out
+    _check_host("out", y, x.dtype)
+    if y.shape != x.shape or gamma.numel() != H:
+        raise ValueError("shape mismatch")
+    T = x.numel() // H if H else 0
+    _host_call(lambda st: library().rarn_rms_norm_host(
+        y.data_ptr(), x.data_ptr(), gamma.data_ptr(), T, H, float(eps), _dtype_code(x), st),
+        "rarn_rms_norm_host", device)
+    return y
+
+
+def fused_add_rms_norm_host(x, residual, gamma, eps: float, out=None, device=None):
+    """fused_add_rms_norm on pinned host tensors (see rms_norm_host)."""
+    import torch
+    H = x.shape[-1]
+    for n, t in (("x", x), ("residual", residual), ("gamma", gamma)):
+        _check_host(n, t, x.dtype)
+    y = torch.empty_like(x).pin_memory() if out is None else out
+    _check_host("out", y, x.dtype)
+    if y.shape != x.shape or residual.shape != x.shape or gamma.numel() != H:
+        raise ValueError("shape mismatch")
+    T = x.numel() // H if H else 0
+    _host_call(lambda st: library().rarn_fused_add_rms_norm_host(
+        y.data_ptr(), x.data_ptr(), residual.data_ptr(), gamma.data_ptr(), T, H, float(eps),
+        _dtype_code(x), st), "rarn_fused_add_rms_norm_host", device)
+    return y
+
+
+def reduce_add_rms_norm_host(partials, residual, gamma, eps: float, out=None, device=None):
+    """reduce_add_rms_norm on pinned host tensors (see rms_norm_host)."""
+    import torch
+    R = partials.shape[0]
+    H = residual.shape[-1]
+    for n, t in (("partials", partials), ("residual", residual), ("gamma", gamma)):
+        _check_host(n, t, residual.dtype)
+    y = torch.empty_like(residual).pin_memory() if out is None else out
+    _check_host("out", y, residual.dtype)
+    if tuple(partials.shape[1:]) != tuple(residual.shape) or y.shape != residual.shape or \
+            gamma.numel() != H:
+        raise ValueError("shape mismatch")
+    T = residual.numel() // H if H else 0
+    _host_call(lambda st: library().rarn_reduce_add_rms_norm_host(
+        y.data_ptr(), partials.data_ptr(), R, residual.data_ptr(), gamma.data_ptr(), T, H,
+        float(eps), _dtype_code(residual), st), "rarn_reduce_add_rms_norm_host", device)
     return y
 
 

@@ -280,8 +280,39 @@ bool overlaps(const void *a, int64_t na, const void *b, int64_t nb) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Shared body of the three entry points.
+// Device view of a range of host memory for the *_host entry points.
+// Pinned host memory (cudaMemoryTypeHost, first and last byte, one
+// contiguous mapping) is used through its device pointer; pageable memory
+// (unregistered) only where the device reads it through the host's page
+// tables, at the same address.  Device and managed memory are refused, and so
+// is pageable memory elsewhere: RARN_ERR_INVALID_ARG, nothing launched.
+rarn_status host_view(const void *p, int64_t bytes, bool pageable_ok, void **view) {
+    const char *first = static_cast<const char *>(p);
+    const char *last = first + (bytes - 1);
+    cudaPointerAttributes a{}, b{};
+    if (cudaPointerGetAttributes(&a, first) != cudaSuccess ||
+        cudaPointerGetAttributes(&b, last) != cudaSuccess) {
+        cudaGetLastError();  // not a sticky error: clear it
+        return RARN_ERR_INVALID_ARG;
+    }
+    if (a.type == cudaMemoryTypeHost && b.type == cudaMemoryTypeHost && a.devicePointer &&
+        b.devicePointer &&
+        static_cast<const char *>(b.devicePointer) - static_cast<const char *>(a.devicePointer) ==
+            bytes - 1) {
+        *view = a.devicePointer;
+        return RARN_OK;
+    }
+    if (pageable_ok && a.type == cudaMemoryTypeUnregistered &&
+        b.type == cudaMemoryTypeUnregistered) {
+        *view = const_cast<char *>(first);
+        return RARN_OK;
+    }
+    return RARN_ERR_INVALID_ARG;
+}
+
 rarn_status run(int op, void *y, const void *src, int32_t R, void *residual, const void *gamma,
-                int64_t T, int64_t H, float eps, rarn_dtype dt, void *stream) {
+                int64_t T, int64_t H, float eps, rarn_dtype dt, void *stream,
+                bool host_buffers = false) {
     if (dt != RARN_F32 && dt != RARN_F16 && dt != RARN_BF16) return RARN_ERR_INVALID_ARG;
     if (T < 0 || H <= 0 || !(eps >= 0.f) || std::isinf(eps)) return RARN_ERR_INVALID_ARG;
     if (op == OP_REDUCE && R < 1) return RARN_ERR_INVALID_ARG;
@@ -306,14 +337,43 @@ rarn_status run(int op, void *y, const void *src, int32_t R, void *residual, con
             return RARN_ERR_ALIAS;
     }
 
-    const bool vec = aligned16(y) && aligned16(src) && aligned16(gamma) &&
-                     (op == OP_PLAIN || aligned16(residual)) && (row_bytes % 16 == 0);
-
     DeviceInfo *d = nullptr;
     rarn_status st = device_info(&d);
     if (st != RARN_OK) return st;
 
-    const Plan pl = make_plan(op, T, H, R, dt, vec, d->num_sms, d->max_smem_optin, g_path.load());
+    if (host_buffers) {
+        // Every buffer lives in host memory; the kernels read and write it
+        // through its device mapping (over NVLink-C2C on Grace systems), so
+        // the transfers happen inside the kernel.
+        int pageable = 0;
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccessUsesHostPageTables,
+                                   dev) != cudaSuccess)
+            pageable = 0;
+        void *vy, *vs, *vg, *vr = nullptr;
+        if ((st = host_view(y, mat, pageable, &vy)) != RARN_OK) return st;
+        if ((st = host_view(src, mat * nsrc, pageable, &vs)) != RARN_OK) return st;
+        if ((st = host_view(gamma, row_bytes, pageable, &vg)) != RARN_OK) return st;
+        if (op != OP_PLAIN && (st = host_view(residual, mat, pageable, &vr)) != RARN_OK) return st;
+        y = vy;
+        src = vs;
+        gamma = vg;
+        residual = vr;
+    }
+
+    const bool vec = aligned16(y) && aligned16(src) && aligned16(gamma) &&
+                     (op == OP_PLAIN || aligned16(residual)) && (row_bytes % 16 == 0);
+
+    // Host-resident data: the register kernels keep more requests in flight
+    // over the host link than the single-producer stream kernel (measured).
+    const int path = host_buffers && g_path.load() == RARN_PATH_AUTO ? RARN_PATH_ROWS
+                                                                     : g_path.load();
+    Plan pl = make_plan(op, T, H, R, dt, vec, d->num_sms, d->max_smem_optin, path);
+    if (host_buffers && path == RARN_PATH_ROWS && pl.kind == KIND_TWO_PASS && vec) {
+        const Plan c = plan_cluster(op, T, H, elem_size(dt), vec, d->num_sms);
+        if (c.kind != KIND_NONE) pl = c;
+    }
     if (pl.kind == KIND_NONE) return RARN_ERR_UNSUPPORTED;
 
     Problem p{};
@@ -382,6 +442,23 @@ rarn_status rarn_reduce_add_rms_norm(void *y, const void *partials, int32_t R, v
     return run(OP_REDUCE, y, partials, R, residual, gamma, T, H, eps, dt, stream);
 }
 
+rarn_status rarn_rms_norm_host(void *y, const void *x, const void *gamma, int64_t T, int64_t H,
+                               float eps, rarn_dtype dt, void *stream) {
+    return run(OP_PLAIN, y, x, 0, nullptr, gamma, T, H, eps, dt, stream, true);
+}
+
+rarn_status rarn_fused_add_rms_norm_host(void *y, const void *x, void *residual,
+                                         const void *gamma, int64_t T, int64_t H, float eps,
+                                         rarn_dtype dt, void *stream) {
+    return run(OP_FUSED, y, x, 1, residual, gamma, T, H, eps, dt, stream, true);
+}
+
+rarn_status rarn_reduce_add_rms_norm_host(void *y, const void *partials, int32_t R,
+                                          void *residual, const void *gamma, int64_t T,
+                                          int64_t H, float eps, rarn_dtype dt, void *stream) {
+    return run(OP_REDUCE, y, partials, R, residual, gamma, T, H, eps, dt, stream, true);
+}
+
 const char *rarn_status_string(rarn_status s) {
     switch (s) {
     case RARN_OK: return "ok";
@@ -442,6 +519,16 @@ rarn_status rarn_watchdog(uint32_t *flags, int clear) {
             return cuda_fail(e);
     }
     return RARN_OK;
+}
+
+int rarn_host_access(void) {
+    int dev = 0, pageable = 0, mapped = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&mapped, cudaDevAttrCanMapHostMemory, dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&pageable, cudaDevAttrPageableMemoryAccessUsesHostPageTables,
+                               dev) != cudaSuccess)
+        return -1;
+    return pageable ? 2 : (mapped ? 1 : 0);
 }
 
 int rarn_version(void) { return (1 << 16) | 0; }

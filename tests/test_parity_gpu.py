@@ -268,3 +268,73 @@ def test_stream_consumer_groups(groups, ppt, monkeypatch):
         plan = rarn.plan(op, T, H, max(R, 1), dt)
         assert plan.startswith("stream"), plan
         check_parity(w, W.generate(w), what=f"stream G{groups} {op} {dt} T{T} H{H}")
+
+
+def _pinned(bits, dt):
+    import torch
+    if dt == "f32":
+        t = torch.from_numpy(np.ascontiguousarray(bits, np.float32))
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(bits, np.uint16).view(np.int16))
+        t = t.view({"f16": torch.float16, "bf16": torch.bfloat16}[dt])
+    return t.pin_memory()
+
+
+@pytest.mark.parametrize("op", ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm"])
+def test_host_buffers(op):
+    """The *_host entry points on pinned host memory: the kernels read and
+    write the host buffers through their device mapping; same results."""
+    import torch
+    for dt, T, H in (("bf16", 300, 4096), ("f32", 7, 1593), ("f16", 129, 8192),
+                     ("bf16", 3, 40000)):
+        w = W.workload(op, dt, T, H, R=3, eps=1e-6, seed=T + H)
+        d = W.generate(w)
+        ref = run_oracle(w, d)
+        g = _pinned(d["gamma"], dt)
+        if op == "rms_norm":
+            y = rarn.rms_norm_host(_pinned(d["x"], dt), g, w.eps)
+            res = None
+        elif op == "fused_add_rms_norm":
+            res = _pinned(d["residual"], dt)
+            y = rarn.fused_add_rms_norm_host(_pinned(d["x"], dt), res, g, w.eps)
+        else:
+            res = _pinned(d["residual"], dt)
+            y = rarn.reduce_add_rms_norm_host(_pinned(d["partials"], dt), res, g, w.eps)
+        torch.cuda.synchronize()
+        assert_y_close(to_host(y, dt), ref.y, dt, f"host {op} {dt} T{T} H{H}")
+        if res is not None:
+            assert_bits_equal(to_host(res, dt), ref.residual, f"host {op} residual")
+
+
+def test_host_buffers_memory_kinds():
+    """Pageable host memory is used where the device reads it through the
+    host's page tables (rarn_host_access() == 2, e.g. Grace) and refused
+    otherwise; device memory is always refused; nothing is launched on a
+    refusal (the output keeps its contents)."""
+    import ctypes
+
+    import torch
+    lib = rarn.library()
+    access = lib.rarn_host_access()
+    assert access in (1, 2)
+    x = torch.full((4, 64), 2.0, dtype=torch.bfloat16)    # pageable
+    g = torch.ones(64, dtype=torch.bfloat16).pin_memory()
+    y = torch.zeros(4, 64, dtype=torch.bfloat16).pin_memory()
+    st = lib.rarn_rms_norm_host(y.data_ptr(), x.data_ptr(), g.data_ptr(), 4, 64, 1e-6, 2,
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    if access == 2:
+        assert st == 0
+        assert torch.allclose(y.float(), torch.ones(4, 64), rtol=0, atol=1e-2)
+    else:
+        assert st == 1  # RARN_ERR_INVALID_ARG
+    xd = torch.zeros(4, 64, dtype=torch.bfloat16, device="cuda")
+    y.fill_(5.0)
+    st = lib.rarn_rms_norm_host(y.data_ptr(), xd.data_ptr(), g.data_ptr(), 4, 64, 1e-6, 2,
+                                ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert st == 1
+    assert torch.all(y == 5.0)
+    with pytest.raises(ValueError):
+        rarn.rms_norm_host(x, g, 1e-6)  # the binding asks for pinned tensors
+    torch.cuda.synchronize()
