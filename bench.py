@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--path", choices=["auto", "rows", "stream", "cluster"], default="auto",
                     help="kernel family (default: the library's own choice)")
+    ap.add_argument("--no-pdl", action="store_true",
+                    help="launch without programmatic dependent launch")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-configs", action="store_true", help="skip the per-config table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -159,14 +161,16 @@ def to_device(bits, dtype, device):
     return t.to(device)
 
 
-def kernel_source_sha() -> str:
+def kernel_source_sha(files=None) -> str:
+    """sha256 over the named kernel source files (default: all of csrc/)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "residual_add_rmsnorm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(csrc, name), "rb") as f:
-                h.update(name.encode())
-                h.update(f.read())
+    names = sorted(files) if files else sorted(
+        n for n in os.listdir(csrc) if n.endswith((".cu", ".cuh", ".h")))
+    for name in names:
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
     return h.hexdigest()
 
 
@@ -183,15 +187,16 @@ def measured_hbm_peak():
 
 def ncu_traffic(workload: str, plan_text: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources for this workload and kernel; else None."""
+    on the current sources of that kernel (the files listed in the entry) for
+    this workload and plan; else None."""
     try:
         with open(TRAFFIC_FILE) as f:
             data = json.load(f)
     except (OSError, ValueError):
         return None
     for e in data.get("entries", []):
-        if (e.get("workload") == workload and e.get("source_sha") == kernel_source_sha()
-                and e.get("plan") == plan_text):
+        if (e.get("workload") == workload and e.get("plan") == plan_text
+                and e.get("source_sha") == kernel_source_sha(e.get("source_files"))):
             return e.get("dram_bytes_per_launch")
     return None
 
@@ -417,6 +422,7 @@ def main():
     rbuild.build()
 
     rarn.set_path(args.path)
+    rarn.set_pdl(not args.no_pdl)
     w = W.BY_NAME[args.workload]
     data = W.generate(w)
     tensors = device_tensors(w, data, device)
@@ -481,7 +487,7 @@ def main():
                    "R": w.R, "eps": w.eps, "rows_per_s": world * w.T * args.steps / (ms / 1e3),
                    "l2": "inputs larger than L2 (no flush between steps)",
                    "parallelism": "replicas" if world > 1 else "single",
-                   "plan": plan_text},
+                   "plan": plan_text, "pdl": not args.no_pdl},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": ncu_traffic(w.name, plan_text),
                      "peak_source": f"{peak_kind} hbm_gbs",

@@ -181,6 +181,30 @@ rarn_status rarn_set_path(rarn_path p);
 rarn_path rarn_get_path(void);
 
 /*
+ * Programmatic dependent launch (process-wide, on by default).  When on,
+ * every launch carries the programmatic-serialization attribute: the kernel
+ * may be scheduled while the previous kernel on the stream is still running
+ * and waits (griddepcontrol.wait) for it to finish before it touches global
+ * memory, and it lets the next such kernel launch once each of its CTAs has
+ * started its last row.  Results are the same either way; only launch gaps
+ * differ.
+ */
+rarn_status rarn_set_pdl(int enable);
+int rarn_get_pdl(void);
+
+/*
+ * Test hook for the watchdog: in the next launch of the stream kernel (on any
+ * thread) CTA 0 expects 16 bytes more for fill number `fill` (0-based, in issue
+ * order) than its copies bring, so that fill never completes; every
+ * shared-memory barrier wait of that launch is bounded by
+ * `wait_limit_ns` (1 ns .. 2 s).  The waits on that fill run out: the kernel
+ * sets the watchdog word and returns with its outputs invalid, and the
+ * context stays usable.  Returns RARN_ERR_INVALID_ARG for a negative fill or a
+ * limit out of range.  Not for production use.
+ */
+rarn_status rarn_test_stall(long long fill, unsigned long long wait_limit_ns);
+
+/*
  * Describe the kernel the current path setting would launch for a problem,
  * as text such as "stream smem=...", without launching anything.
  * `vec_ok` says whether every pointer is 16-byte aligned; `num_sms` is the

@@ -19,7 +19,8 @@ import os
 
 __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_host",
            "fused_add_rms_norm_host", "reduce_add_rms_norm_host", "RarnError", "library",
-           "set_path", "get_path", "plan", "watchdog", "PATHS", "DTYPE_CODES"]
+           "set_path", "get_path", "set_pdl", "get_pdl", "plan", "watchdog", "PATHS",
+           "DTYPE_CODES"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
@@ -84,6 +85,12 @@ def library() -> ctypes.CDLL:
     lib.rarn_version.restype = c_int
     lib.rarn_host_access.argtypes = []
     lib.rarn_host_access.restype = c_int
+    lib.rarn_set_pdl.argtypes = [c_int]
+    lib.rarn_set_pdl.restype = c_int
+    lib.rarn_get_pdl.argtypes = []
+    lib.rarn_get_pdl.restype = c_int
+    lib.rarn_test_stall.argtypes = [ctypes.c_longlong, ctypes.c_ulonglong]
+    lib.rarn_test_stall.restype = c_int
     _lib = lib
     return lib
 
@@ -274,6 +281,15 @@ def reduce_add_rms_norm_host(partials, residual, gamma, eps: float, out=None, de
 def set_path(name: str) -> None:
     """Force a kernel family ('auto', 'rows', 'stream', 'cluster'), process-wide."""
     _check(library().rarn_set_path(PATHS[name]), "rarn_set_path")
+
+
+def set_pdl(enable: bool) -> None:
+    """Programmatic dependent launch for every later launch (process-wide)."""
+    _check(library().rarn_set_pdl(int(bool(enable))), "rarn_set_pdl")
+
+
+def get_pdl() -> bool:
+    return bool(library().rarn_get_pdl())
 
 
 def get_path() -> str:

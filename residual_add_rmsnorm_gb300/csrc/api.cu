@@ -23,6 +23,10 @@ namespace {
 
 thread_local int t_last_cuda_error = 0;
 std::atomic<int> g_path{RARN_PATH_AUTO};
+std::atomic<int> g_pdl{1};
+// test hook (rarn_test_stall): consumed by the next stream-kernel launch
+std::atomic<long long> g_stall_fill{-1};
+std::atomic<unsigned long long> g_stall_limit_ns{0};
 
 constexpr int kMaxDevices = 64;
 
@@ -388,6 +392,16 @@ rarn_status run(int op, void *y, const void *src, int32_t R, void *residual, con
     p.op = op;
     p.eps = eps;
     p.watchdog = d->watchdog;
+    p.wait_limit_ns = stream::kWaitLimitNs;
+    p.stall_fill = -1;
+    if (pl.kind == KIND_STREAM) {
+        const long long f = g_stall_fill.exchange(-1);
+        if (f >= 0) {
+            p.stall_fill = f;
+            p.wait_limit_ns = g_stall_limit_ns.load();
+        }
+    }
+    pl.pdl = g_pdl.load() != 0;
 
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorInvalidValue;
@@ -479,6 +493,21 @@ rarn_status rarn_set_path(rarn_path p) {
 }
 
 rarn_path rarn_get_path(void) { return static_cast<rarn_path>(g_path.load()); }
+
+rarn_status rarn_set_pdl(int enable) {
+    g_pdl.store(enable ? 1 : 0);
+    return RARN_OK;
+}
+
+int rarn_get_pdl(void) { return g_pdl.load(); }
+
+rarn_status rarn_test_stall(long long fill, unsigned long long wait_limit_ns) {
+    if (fill < 0 || wait_limit_ns == 0 || wait_limit_ns > stream::kWaitLimitNs)
+        return RARN_ERR_INVALID_ARG;
+    g_stall_limit_ns.store(wait_limit_ns);
+    g_stall_fill.store(fill);
+    return RARN_OK;
+}
 
 rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt, int vec_ok,
                       int num_sms, char *out, size_t cap) {

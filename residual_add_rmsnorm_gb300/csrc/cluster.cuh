@@ -55,10 +55,12 @@ __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG>::value) k_cluster_vec
     const int j_begin = (int)rank * seg;
     const int j_end = min(nv, j_begin + seg);
     const int64_t first = blockIdx.x / cs, step = gridDim.x / cs;
+    grid_dependency_wait();
     uint4 gv[VPT];  // PG: this thread's gamma packs, the same for every row
     if (PG) load_gamma_vec<T, VPT>(p, j_begin + threadIdx.x, blockDim.x, j_end, gv);
     int par = 0;
     for (int64_t t = first; t < p.T; t += step, par ^= 1) {
+        if (t + step >= p.T) grid_launch_dependents();
         uint4 hv[VPT];
         const float ss = pass1_vec<T, VPT, OP, Chunk<OP>::value>(p, t, j_begin + threadIdx.x,
                                                                 blockDim.x, j_end, hv);
@@ -76,32 +78,24 @@ __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG>::value) k_cluster_vec
 
 template <typename T, int OP>
 static cudaError_t launch_cluster_op(const Problem &p, const Plan &pl, cudaStream_t st) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(pl.grid);
-    cfg.blockDim = dim3(pl.block);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = pl.cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    const dim3 g(pl.grid), b(pl.block);
+    auto go = [&](auto kernel) {
+        return launch_kernel(kernel, g, b, 0, st, pl.pdl, pl.cluster, p);
+    };
     if (pl.prefetch_gamma) {
         switch (pl.per_thread) {
-        case 1: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 1, OP, true>, p);
-        case 2: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 2, OP, true>, p);
-        case 4: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 4, OP, true>, p);
-        case 8: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 8, OP, true>, p);
+        case 1: return go(k_cluster_vec<T, 1, OP, true>);
+        case 2: return go(k_cluster_vec<T, 2, OP, true>);
+        case 4: return go(k_cluster_vec<T, 4, OP, true>);
+        case 8: return go(k_cluster_vec<T, 8, OP, true>);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (pl.per_thread) {
-    case 1: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 1, OP, false>, p);
-    case 2: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 2, OP, false>, p);
-    case 4: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 4, OP, false>, p);
-    case 8: return cudaLaunchKernelEx(&cfg, k_cluster_vec<T, 8, OP, false>, p);
+    case 1: return go(k_cluster_vec<T, 1, OP, false>);
+    case 2: return go(k_cluster_vec<T, 2, OP, false>);
+    case 4: return go(k_cluster_vec<T, 4, OP, false>);
+    case 8: return go(k_cluster_vec<T, 8, OP, false>);
     default: return cudaErrorInvalidValue;
     }
 }

@@ -27,7 +27,54 @@ struct Problem {
     int op;                // Op
     float eps;
     unsigned int *watchdog;  // device word for bounded-wait failures
+    unsigned long long wait_limit_ns;  // bound on every shared-memory barrier wait
+    long long stall_fill;    // test hook: in CTA 0 of the stream kernel this fill never
+                             // completes (-1: never), so that its consumers' wait runs out
 };
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel waits for the grids it depends
+// on before its first global memory access (a no-op when it was launched
+// without the programmatic-serialization attribute), and lets its dependents
+// launch once each CTA has started its last row, so that their launch
+// overlaps this grid's tail.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Host: launch with the programmatic-serialization attribute (pdl) and an
+// optional cluster shape.
+template <typename... K, typename... A>
+inline cudaError_t launch_kernel(void (*kernel)(K...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, bool pdl, int cluster, A &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<A &&>(args)...);
+}
 
 // ---------------------------------------------------------------------------
 // Storage-type traits: 16-byte packs <-> binary32, one rounding on the way out

@@ -30,6 +30,7 @@ struct Plan {
     int chunk = 0;       // bytes per stream per pipeline stage (stream kernel)
     int groups = 1;      // consumer groups (stream kernel)
     bool prefetch_gamma = false;  // CTA register kernel keeps gamma in registers
+    bool pdl = false;    // programmatic dependent launch
 };
 
 // Register budget of the register-staged row kernels.  A thread holding P

@@ -251,10 +251,12 @@ template <typename T, int VPT, int OP, bool PG>
 __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG>::value) k_cta_vec(Problem p) {
     __shared__ float red[2][32];
     const int nv = (int)(p.H / DT<T>::EPV);
+    grid_dependency_wait();
     uint4 gv[VPT];
     if (PG) load_gamma_vec<T, VPT>(p, threadIdx.x, blockDim.x, nv, gv);
     int par = 0;
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
+        if (t + gridDim.x >= p.T) grid_launch_dependents();
         uint4 hv[VPT];
         const float ss = pass1_vec<T, VPT, OP, Chunk<OP>::value>(p, t, threadIdx.x, blockDim.x,
                                                                 nv, hv);
@@ -273,9 +275,11 @@ __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
     const int wpb = blockDim.x >> 5;
     const int64_t first = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     const int64_t step = (int64_t)gridDim.x * wpb;
+    grid_dependency_wait();
     uint4 gv[VPT];
     load_gamma_vec<T, VPT>(p, lane, 32, nv, gv);
     for (int64_t t = first; t < p.T; t += step) {
+        if (t + step >= p.T) grid_launch_dependents();
         uint4 hv[VPT];
         const float ss = pass1_vec<T, VPT, OP, Chunk<OP>::value>(p, t, lane, 32, nv, hv);
         const float tot = warp_sum(ss);
@@ -288,8 +292,10 @@ __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
 template <typename T, int NE, int OP>
 __global__ void __launch_bounds__(ScalarBound<NE, OP>::value) k_cta_scalar(Problem p) {
     __shared__ float red[2][32];
+    grid_dependency_wait();
     int par = 0;
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
+        if (t + gridDim.x >= p.T) grid_launch_dependents();
         float h[NE];
         const float ss =
             pass1_scalar<T, NE, OP, Chunk<OP>::value>(p, t, threadIdx.x, blockDim.x, h);
@@ -307,8 +313,10 @@ __global__ void __launch_bounds__(1024) k_two_pass(Problem p) {
     __shared__ float red[2][32];
     constexpr int EPV = VEC ? DT<T>::EPV : 1;
     const int n = (int)(p.H / EPV);
+    grid_dependency_wait();
     int par = 0;
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
+        if (t + gridDim.x >= p.T) grid_launch_dependents();
         float ss = 0.f;
         for (int base = 0; base < n; base += blockDim.x) {
             if (VEC) {
@@ -346,65 +354,59 @@ __global__ void __launch_bounds__(1024) k_two_pass(Problem p) {
 template <typename T, int OP>
 static cudaError_t launch_rows_op(const Problem &p, const Plan &pl, cudaStream_t st) {
     const dim3 g(pl.grid), b(pl.block);
+    auto go = [&](auto kernel) { return launch_kernel(kernel, g, b, 0, st, pl.pdl, 1, p); };
     switch (pl.kind) {
     case KIND_WARP:
         switch (pl.per_thread) {
-        case 1: k_warp_vec<T, 1, OP><<<g, b, 0, st>>>(p); break;
-        case 2: k_warp_vec<T, 2, OP><<<g, b, 0, st>>>(p); break;
-        case 4: k_warp_vec<T, 4, OP><<<g, b, 0, st>>>(p); break;
+        case 1: return go(k_warp_vec<T, 1, OP>);
+        case 2: return go(k_warp_vec<T, 2, OP>);
+        case 4: return go(k_warp_vec<T, 4, OP>);
         default: return cudaErrorInvalidValue;
         }
-        break;
     case KIND_CTA:
-        if (pl.vec) {
-            if (pl.prefetch_gamma) {
-                switch (pl.per_thread) {
-                case 1: k_cta_vec<T, 1, OP, true><<<g, b, 0, st>>>(p); break;
-                case 2: k_cta_vec<T, 2, OP, true><<<g, b, 0, st>>>(p); break;
-                case 4: k_cta_vec<T, 4, OP, true><<<g, b, 0, st>>>(p); break;
-                case 8: k_cta_vec<T, 8, OP, true><<<g, b, 0, st>>>(p); break;
-                default: return cudaErrorInvalidValue;
-                }
-            } else {
-                switch (pl.per_thread) {
-                case 1: k_cta_vec<T, 1, OP, false><<<g, b, 0, st>>>(p); break;
-                case 2: k_cta_vec<T, 2, OP, false><<<g, b, 0, st>>>(p); break;
-                case 4: k_cta_vec<T, 4, OP, false><<<g, b, 0, st>>>(p); break;
-                case 8: k_cta_vec<T, 8, OP, false><<<g, b, 0, st>>>(p); break;
-                default: return cudaErrorInvalidValue;
-                }
-            }
-        } else {
+        if (pl.vec && pl.prefetch_gamma) {
             switch (pl.per_thread) {
-            case 1: k_cta_scalar<T, 1, OP><<<g, b, 0, st>>>(p); break;
-            case 2: k_cta_scalar<T, 2, OP><<<g, b, 0, st>>>(p); break;
-            case 4: k_cta_scalar<T, 4, OP><<<g, b, 0, st>>>(p); break;
-            case 8: k_cta_scalar<T, 8, OP><<<g, b, 0, st>>>(p); break;
-            case 16: k_cta_scalar<T, 16, OP><<<g, b, 0, st>>>(p); break;
+            case 1: return go(k_cta_vec<T, 1, OP, true>);
+            case 2: return go(k_cta_vec<T, 2, OP, true>);
+            case 4: return go(k_cta_vec<T, 4, OP, true>);
+            case 8: return go(k_cta_vec<T, 8, OP, true>);
             default: return cudaErrorInvalidValue;
             }
         }
-        break;
+        if (pl.vec) {
+            switch (pl.per_thread) {
+            case 1: return go(k_cta_vec<T, 1, OP, false>);
+            case 2: return go(k_cta_vec<T, 2, OP, false>);
+            case 4: return go(k_cta_vec<T, 4, OP, false>);
+            case 8: return go(k_cta_vec<T, 8, OP, false>);
+            default: return cudaErrorInvalidValue;
+            }
+        }
+        switch (pl.per_thread) {
+        case 1: return go(k_cta_scalar<T, 1, OP>);
+        case 2: return go(k_cta_scalar<T, 2, OP>);
+        case 4: return go(k_cta_scalar<T, 4, OP>);
+        case 8: return go(k_cta_scalar<T, 8, OP>);
+        case 16: return go(k_cta_scalar<T, 16, OP>);
+        default: return cudaErrorInvalidValue;
+        }
     case KIND_TWO_PASS:
-        if (pl.vec)
-            k_two_pass<T, OP, true><<<g, b, 0, st>>>(p);
-        else
-            k_two_pass<T, OP, false><<<g, b, 0, st>>>(p);
-        break;
+        return pl.vec ? go(k_two_pass<T, OP, true>) : go(k_two_pass<T, OP, false>);
     default:
         return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t launch_rows(const Problem &p, const Plan &pl, cudaStream_t st) {
+    cudaError_t e;
     switch (p.op) {
-    case OP_PLAIN: return launch_rows_op<T, OP_PLAIN>(p, pl, st);
-    case OP_FUSED: return launch_rows_op<T, OP_FUSED>(p, pl, st);
-    case OP_REDUCE: return launch_rows_op<T, OP_REDUCE>(p, pl, st);
+    case OP_PLAIN: e = launch_rows_op<T, OP_PLAIN>(p, pl, st); break;
+    case OP_FUSED: e = launch_rows_op<T, OP_FUSED>(p, pl, st); break;
+    case OP_REDUCE: e = launch_rows_op<T, OP_REDUCE>(p, pl, st); break;
     default: return cudaErrorInvalidValue;
     }
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace rarn

@@ -24,7 +24,8 @@
 // Every wait is bounded (see wait_bounded): on a timeout the kernel records a
 // bit in the watchdog word, stops issuing copies, drains the copies already
 // issued and returns.  Consumer warps keep executing the same named barriers
-// so that none is left waiting.
+// so that none is left waiting, and release only stages whose fills they saw
+// complete.
 #pragma once
 
 #include "common.cuh"
@@ -85,12 +86,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
 }
 
 // Wait for the phase of `bar` with parity `parity`.  Gives up after
-// kWaitLimitNs (or at once if another thread already gave up): sets the
-// block's abort word and the watchdog bit, returns false.
+// `limit_ns` (or at once if another thread of the CTA already gave up): sets
+// the CTA's abort word and the watchdog bit, returns false.
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
                                              volatile int *abort_flag, unsigned int *watchdog,
-                                             unsigned int bit) {
+                                             unsigned int bit, unsigned long long limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
     unsigned long long t0 = 0;
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -99,7 +101,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
             const unsigned long long now = global_ns();
             if (t0 == 0) {
                 t0 = now;
-            } else if (now - t0 > kWaitLimitNs) {
+            } else if (now - t0 > limit_ns) {
                 *abort_flag = 1;
                 atomicOr(watchdog, bit);
                 return false;
@@ -159,6 +161,7 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
         reinterpret_cast<volatile int *>(red_all + G * 2 * kConsumerWarps);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    grid_dependency_wait();
     if (threadIdx.x == 0) {
         for (int s = 0; s < G * stages; ++s) {
             mbar_init(smem_addr(&full[s]), 1);
@@ -174,6 +177,7 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
         // ------------------------------------------------------------ producer
         if (lane != 0) return;
         long long issued0 = 0, issued1 = 0;  // fills issued into ring 0 / ring 1
+        const long long stall_at = blockIdx.x == 0 ? p.stall_fill : -1;
         bool ok = true;
         int g = 0;
         for (int64_t t = blockIdx.x; t < p.T && ok; t += gridDim.x) {
@@ -186,10 +190,13 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
                 const uint32_t ph = (uint32_t)((n / stages) & 1);
                 const int b = g * stages + st;
                 ok = wait_bounded(smem_addr(&empty[b]), ph ^ 1u, abort_flag, p.watchdog,
-                                  kWatchProducer);
+                                  kWatchProducer, p.wait_limit_ns);
                 if (!ok) break;
                 const uint32_t fb = smem_addr(&full[b]);
-                mbar_arrive_expect_tx(fb, bytes * (uint32_t)ns);
+                // test hook: expect 16 bytes more than the copies bring, so that
+                // this fill never completes and its consumers' wait runs out
+                const uint32_t extra = issued0 + issued1 == stall_at ? 16u : 0u;
+                mbar_arrive_expect_tx(fb, bytes * (uint32_t)ns + extra);
                 const uint32_t dst =
                     smem_addr(smem + (size_t)g * L.ring_stride + (size_t)st * ns * CB);
                 const int64_t off = row_elem + (int64_t)c * CP * EPV;
@@ -204,16 +211,17 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
             }
             if (++g == G) g = 0;
         }
+        grid_launch_dependents();
         // Drain: in every ring the last min(stages, issued) fills must land
-        // before the CTA exits.
-        const unsigned long long deadline = global_ns() + kWaitLimitNs;
+        // before the CTA exits (one deadline for all of them; after it, each
+        // remaining fill is still checked once).
+        const unsigned long long deadline = global_ns() + p.wait_limit_ns;
         for (int r = 0; r < G; ++r) {
             const long long issued = r == 0 ? issued0 : issued1;
             const long long first = issued > stages ? issued - stages : 0;
             for (long long f = first; f < issued; ++f)
-                if (!wait_drain(smem_addr(&full[r * stages + (int)(f % stages)]),
-                                (uint32_t)((f / stages) & 1), deadline, p.watchdog))
-                    return;
+                wait_drain(smem_addr(&full[r * stages + (int)(f % stages)]),
+                           (uint32_t)((f / stages) & 1), deadline, p.watchdog);
         }
         return;
     }
@@ -236,9 +244,10 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
          t += (int64_t)G * gridDim.x, par ^= 1) {
         const int64_t row_elem = t * p.H;
         float ss = 0.f;
+        if (t + (int64_t)G * gridDim.x >= p.T) grid_launch_dependents();
         for (int c = 0; c < nchunks; ++c) {
             const bool ok = wait_bounded(smem_addr(&gfull[stage]), phase, abort_flag, p.watchdog,
-                                         kWatchConsumer);
+                                         kWatchConsumer, p.wait_limit_ns);
             const unsigned char *sbase = ring + (size_t)stage * ns * CB;
 #pragma unroll
             for (int m = 0; m < PPT; ++m) {
@@ -269,7 +278,11 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
                 for (int e = 0; e < EPV; ++e) ss += h[e] * h[e];
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_addr(&gempty[stage]));
+            // Release the stage only if this warp saw its fill complete: after
+            // an abort, a stage whose fill never completed stays held, so the
+            // producer can never re-arm a full barrier inside an unfinished
+            // phase (its own bounded wait then ends it).
+            if (lane == 0 && ok) mbar_arrive(smem_addr(&gempty[stage]));
             if (++stage == stages) {
                 stage = 0;
                 phase ^= 1u;
@@ -303,8 +316,9 @@ static cudaError_t launch_stream_k(const Problem &p, const Plan &pl, cudaStream_
     cudaError_t e = cudaFuncSetAttribute(stream::k_stream<T, OP, G, PPT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem);
     if (e != cudaSuccess) return e;
-    stream::k_stream<T, OP, G, PPT><<<pl.grid, stream::threads(G), pl.smem, st>>>(p, pl.stages);
-    return cudaGetLastError();
+    e = launch_kernel(stream::k_stream<T, OP, G, PPT>, dim3(pl.grid), dim3(stream::threads(G)),
+                      pl.smem, st, pl.pdl, 1, p, pl.stages);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <typename T, int OP, int G>

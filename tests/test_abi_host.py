@@ -183,3 +183,14 @@ def test_plan_auto_policy():
     assert "scalar" in _plan("reduce_add_rms_norm", 8192, 8192, 8, "bf16", vec=False)
     # plain: register kernel
     assert _plan("rms_norm", 16384, 4096, 0, "bf16").startswith("rows.cta")
+
+
+def test_pdl_setting_and_stall_hook_arguments(lib):
+    assert rarn.get_pdl() is True  # on by default
+    rarn.set_pdl(False)
+    assert rarn.get_pdl() is False
+    rarn.set_pdl(True)
+    assert rarn.get_pdl() is True
+    assert lib.rarn_test_stall(-1, 1000) == INVALID
+    assert lib.rarn_test_stall(0, 0) == INVALID
+    assert lib.rarn_test_stall(0, 3_000_000_000) == INVALID

@@ -338,3 +338,40 @@ def test_host_buffers_memory_kinds():
     with pytest.raises(ValueError):
         rarn.rms_norm_host(x, g, 1e-6)  # the binding asks for pinned tensors
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("pdl", [False, True])
+def test_chained_launches(pdl):
+    """Three launches in a row on one stream, each reading what the previous
+    one wrote (y becomes the next x; the residual carries over), with and
+    without programmatic dependent launch: each step matches the oracle run
+    on that step's actual inputs (the GPU's y of the step before)."""
+    import torch
+    rarn.set_pdl(pdl)
+    try:
+        for path, T, H in (("auto", 4096, 4096), ("stream", 2000, 8192), ("rows", 3, 5120),
+                           ("cluster", 64, 32768)):
+            w = W.workload("fused_add_rms_norm", "bf16", T, H, eps=1e-6, seed=T)
+            if not _supported(w, path):
+                continue
+            rarn.set_path(path)
+            d = W.generate(w)
+            x = to_device(d["x"], "bf16")
+            res = to_device(d["residual"], "bf16")
+            g = to_device(d["gamma"], "bf16")
+            bufs = [torch.empty_like(x) for _ in range(3)]
+            cur = x
+            for b in bufs:
+                rarn.fused_add_rms_norm(cur, res, g, w.eps, out=b)
+                cur = b
+            torch.cuda.synchronize()
+            xs, rs = d["x"], d["residual"]
+            for k in range(3):
+                ref = oracle.fused_add_rms_norm(xs, rs, d["gamma"], w.eps, "bf16")
+                yk = to_host(bufs[k], "bf16")
+                assert_y_close(yk, ref.y, "bf16", f"chain step {k} {path} pdl={pdl}")
+                xs, rs = yk, ref.residual
+            assert_bits_equal(to_host(res, "bf16"), rs, f"chain residual {path} pdl={pdl}")
+    finally:
+        rarn.set_pdl(True)
+        rarn.set_path("auto")
