@@ -107,6 +107,10 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
     };
     const int max_pt = vec ? 8 : 16;
     int pt = std::min(max_pt, pow2_at_least(ceil_div(n, 256)));
+    if (const char *v = getenv("RARN_ROWS_PT")) {  // measurements only
+        const int f = atoi(v);
+        if (f >= 1 && f <= max_pt && (f & (f - 1)) == 0) pt = f;
+    }
     while (pt < max_pt && ceil_div(n, pt) > max_block(pt, false)) pt <<= 1;
     if (ceil_div(n, pt) > max_block(pt, false)) {
         pl.kind = KIND_TWO_PASS;
@@ -128,6 +132,17 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
     // reduction) and the kernel's register budget allows it.
     pl.prefetch_gamma =
         pl.kind == KIND_CTA && pl.vec && rounds == 1 && pl.block <= max_block(pl.per_thread, true);
+    // Software pipelining across rows (plain / fused): worth it when every
+    // CTA has several rows; it holds a second set of load buffers.
+    if (pl.kind == KIND_CTA && pl.vec && op != OP_REDUCE && rounds >= 2) {
+        const int streams = op == OP_PLAIN ? 1 : 2;
+        const int pipe_max =
+            rows_max_block(rows_regs_vec(pl.per_thread, epv, op, false) + pl.per_thread * 4 * streams);
+        pl.pipe = pl.block <= pipe_max;
+        if (const char *v = getenv("RARN_ROWS_PIPE")) {  // measurements only
+            if (*v == '0') pl.pipe = false;
+        }
+    }
     return pl;
 }
 
@@ -528,9 +543,10 @@ rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt
     const Plan pl = make_plan((int)op, T, H, R, dt, vec, num_sms, max_smem, g_path.load());
     snprintf(out, cap,
              "%s %s per_thread=%d block=%d grid=%d cluster=%d smem=%d stages=%d chunk=%d "
-             "groups=%d gamma_regs=%d",
+             "groups=%d gamma_regs=%d pipe=%d",
              kind_name(pl.kind), pl.vec ? "vec16" : "scalar", pl.per_thread, pl.block, pl.grid,
-             pl.cluster, pl.smem, pl.stages, pl.chunk, pl.groups, (int)pl.prefetch_gamma);
+             pl.cluster, pl.smem, pl.stages, pl.chunk, pl.groups, (int)pl.prefetch_gamma,
+             (int)pl.pipe);
     return pl.kind == KIND_NONE ? RARN_ERR_UNSUPPORTED : RARN_OK;
 }
 

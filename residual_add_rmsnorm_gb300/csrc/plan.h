@@ -31,6 +31,7 @@ struct Plan {
     int groups = 1;      // consumer groups (stream kernel)
     bool prefetch_gamma = false;  // CTA register kernel keeps gamma in registers
     bool pdl = false;    // programmatic dependent launch
+    bool pipe = false;   // CTA register kernel loads the next row before finishing this one
 };
 
 // Register budget of the register-staged row kernels.  A thread holding P

@@ -266,6 +266,98 @@ __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG>::value) k_cta_vec(Pro
     }
 }
 
+// One CTA per row, packs, software-pipelined across rows (plain and fused
+// forms: one or two input streams).  Before a CTA reduces and writes row t it
+// issues the loads of its next row into a second register buffer, so the
+// SM keeps reads in flight through the row reduction and the y stores instead
+// of draining between rows.
+template <typename T, int VPT, int OP>
+struct RowLoads {
+    static constexpr int S = OP == OP_PLAIN ? 1 : 2;  // x (, residual)
+    uint4 v[S][VPT];
+};
+
+template <typename T, int VPT, int OP>
+__device__ __forceinline__ void issue_row_loads(const Problem &p, int64_t t, int j0, int js,
+                                                int nv, RowLoads<T, VPT, OP> &b) {
+    constexpr int EPV = DT<T>::EPV;
+    const int64_t row_off = t * p.H;
+#pragma unroll
+    for (int s = 0; s < RowLoads<T, VPT, OP>::S; ++s) {
+        const T *base = s == 0 ? reinterpret_cast<const T *>(p.src) + row_off
+                               : reinterpret_cast<const T *>(p.residual) + row_off;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = j0 + k * js;
+            if (j < nv) b.v[s][k] = ld_stream(base + (int64_t)j * EPV);
+        }
+    }
+}
+
+// h from the loaded packs (fused: x + residual in binary32, one rounding,
+// residual written back); returns this thread's share of the sum of squares.
+template <typename T, int VPT, int OP>
+__device__ __forceinline__ float consume_row_loads(const Problem &p, int64_t t, int j0, int js,
+                                                   int nv, const RowLoads<T, VPT, OP> &b,
+                                                   uint4 (&hv)[VPT]) {
+    constexpr int EPV = DT<T>::EPV;
+    T *res = reinterpret_cast<T *>(p.residual) + t * p.H;
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = j0 + k * js;
+        if (j < nv) {
+            float h[EPV];
+            DT<T>::unpack(b.v[0][k], h);
+            if (OP == OP_FUSED) {
+                float r[EPV];
+                DT<T>::unpack(b.v[1][k], r);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) h[e] = h[e] + r[e];
+                hv[k] = DT<T>::pack(h);  // the one rounding to the storage type
+                st_global(res + (int64_t)j * EPV, hv[k]);
+                DT<T>::unpack(hv[k], h);
+            } else {
+                hv[k] = b.v[0][k];
+            }
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) ss += h[e] * h[e];
+        }
+    }
+    return ss;
+}
+
+template <typename T, int VPT, int OP>
+struct PipeBound {
+    static constexpr int b = rows_max_block(rows_regs_vec(VPT, DT<T>::EPV, OP, false) +
+                                            VPT * 4 * RowLoads<T, VPT, OP>::S);
+    static constexpr int value = b > 0 ? b : 128;
+};
+
+template <typename T, int VPT, int OP>
+__global__ void __launch_bounds__(PipeBound<T, VPT, OP>::value) k_cta_pipe(Problem p) {
+    __shared__ float red[2][32];
+    const int nv = (int)(p.H / DT<T>::EPV);
+    grid_dependency_wait();
+    RowLoads<T, VPT, OP> next;
+    int64_t t = blockIdx.x;
+    if (t < p.T) issue_row_loads<T, VPT, OP>(p, t, threadIdx.x, blockDim.x, nv, next);
+    int par = 0;
+    for (; t < p.T; t += gridDim.x, par ^= 1) {
+        const RowLoads<T, VPT, OP> cur = next;
+        if (t + gridDim.x < p.T) {
+            issue_row_loads<T, VPT, OP>(p, t + gridDim.x, threadIdx.x, blockDim.x, nv, next);
+        } else {
+            grid_launch_dependents();
+        }
+        uint4 hv[VPT];
+        const float ss = consume_row_loads<T, VPT, OP>(p, t, threadIdx.x, blockDim.x, nv, cur, hv);
+        const float tot = block_sum(ss, red[par]);
+        const float inv = rsqrtf(tot / (float)p.H + p.eps);
+        pass2_vec<T, VPT, false>(p, t, threadIdx.x, blockDim.x, nv, hv, inv);
+    }
+}
+
 // One warp per row, packs; blockDim.x / 32 rows per CTA at a time.  Gamma is
 // held in registers (at most 4 packs per lane).
 template <typename T, int VPT, int OP>
@@ -364,6 +456,15 @@ static cudaError_t launch_rows_op(const Problem &p, const Plan &pl, cudaStream_t
         default: return cudaErrorInvalidValue;
         }
     case KIND_CTA:
+        if (pl.vec && pl.pipe && OP != OP_REDUCE) {
+            switch (pl.per_thread) {
+            case 1: return go(k_cta_pipe<T, 1, OP == OP_REDUCE ? OP_FUSED : OP>);
+            case 2: return go(k_cta_pipe<T, 2, OP == OP_REDUCE ? OP_FUSED : OP>);
+            case 4: return go(k_cta_pipe<T, 4, OP == OP_REDUCE ? OP_FUSED : OP>);
+            case 8: return go(k_cta_pipe<T, 8, OP == OP_REDUCE ? OP_FUSED : OP>);
+            default: return cudaErrorInvalidValue;
+            }
+        }
         if (pl.vec && pl.prefetch_gamma) {
             switch (pl.per_thread) {
             case 1: return go(k_cta_vec<T, 1, OP, true>);

@@ -375,3 +375,18 @@ def test_chained_launches(pdl):
     finally:
         rarn.set_pdl(True)
         rarn.set_path("auto")
+
+
+def test_pipelined_rows_kernel():
+    """The software-pipelined CTA kernel (next row's loads issued before the
+    current row is reduced and written): several rows per CTA, ragged row
+    counts, and y written over x in place."""
+    for op, dt, T, H, inplace in (("fused_add_rms_norm", "bf16", 5003, 2048, False),
+                                  ("rms_norm", "f32", 3001, 4096, False),
+                                  ("fused_add_rms_norm", "f16", 7777, 1600, True),
+                                  ("rms_norm", "bf16", 9000, 3000, True),
+                                  ("fused_add_rms_norm", "bf16", 40000, 5120, False)):
+        w = W.workload(op, dt, T, H, eps=1e-6, seed=T)
+        plan = rarn.plan(op, T, H, 1, dt)
+        assert "pipe=1" in plan, plan
+        check_parity(w, W.generate(w), out_is_input=inplace, what=f"pipe {op} {dt} T{T} H{H}")
