@@ -151,9 +151,9 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
 constexpr int64_t kStreamMaxRowBytes = 96 * 1024;
 constexpr int kDefaultMaxSmem = 232448;  // opt-in shared memory per CTA on sm_100 / sm_103
 
-// Packs per consumer thread per chunk: as large as the row allows (fewer,
-// larger copies per producer iteration) while at least `min_stages` stages
-// fit.  RARN_STREAM_PPT (1, 2, 4) overrides it for measurements.
+// Packs per consumer thread per chunk: up to two (fewer, larger copies per
+// producer iteration) while at least 4 stages fit.  RARN_STREAM_PPT (1, 2, 4)
+// overrides it for measurements.
 Plan plan_stream(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_sms,
                  int max_smem, int groups) {
     Plan pl;
@@ -161,8 +161,8 @@ Plan plan_stream(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_s
     if (!vec || row_bytes > kStreamMaxRowBytes) return pl;
     const int ns = op == OP_PLAIN ? 1 : R + 1;
     const int64_t nv = row_bytes / 16;
-    int ppt = std::min<int64_t>(stream::kMaxPacksPerThread,
-                                pow2_at_least(ceil_div(nv, stream::kConsumers)));
+    // two packs per thread measured best or equal everywhere (4 only for tests)
+    int ppt = std::min<int64_t>(2, pow2_at_least(ceil_div(nv, stream::kConsumers)));
     if (const char *v = getenv("RARN_STREAM_PPT")) {
         const int f = atoi(v);
         if (f == 1 || f == 2 || f == 4) ppt = f;
@@ -236,31 +236,29 @@ int stream_groups(int fallback) {
 }
 
 // The automatic choice, from measurements on GB300 (cold L2, CUDA-graph
-// timing; see the sweep in the design notes):
+// timing over rotating input copies):
 //  * enough rows to give every SM several (T >= 2 x #SM) and 16-byte rows:
 //      - reduce (R >= 2): the TMA-fed stream kernel; it keeps R + 1 input
 //        streams in flight without spending registers on them (one consumer
 //        group from R >= 4, two below);
-//      - fused with rows of 16 KB and more: the stream kernel (two groups
-//        below 32 KB rows, one above);
-//      - plain with rows beyond the register kernels (> 16 KB): the stream
-//        kernel;
-//  * otherwise the register kernels: warp per row for short rows, CTA per
-//    row, and a cluster per row where one CTA's registers cannot hold it.
+//      - plain / fused rows too long for one CTA's registers (> 2048
+//        packs): the stream kernel instead of the two-pass kernel;
+//      - otherwise the software-pipelined register kernel, which beats the
+//        stream kernel for one or two input streams up to 32 KB rows;
+//  * few rows: the register kernels, with a cluster per row where one CTA's
+//    registers cannot hold the row.
 Plan plan_auto(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_sms, int max_smem) {
-    const int64_t row_bytes = H * s;
-    if (vec && T >= 2 * (int64_t)num_sms) {
-        int groups = 0;
-        if (op == OP_REDUCE && R >= 2) groups = R >= 4 ? 1 : 2;
-        if (op == OP_FUSED && row_bytes >= 16 * 1024) groups = row_bytes >= 32 * 1024 ? 1 : 2;
-        if (op == OP_PLAIN && row_bytes > 16 * 1024) groups = 1;
-        if (groups) {
-            Plan st = plan_stream(op, T, H, R, s, vec, num_sms, max_smem, groups);
-            if (st.kind != KIND_NONE) return st;
-        }
+    const bool many = vec && T >= 2 * (int64_t)num_sms;
+    if (many && op == OP_REDUCE && R >= 2) {
+        Plan st = plan_stream(op, T, H, R, s, vec, num_sms, max_smem, R >= 4 ? 1 : 2);
+        if (st.kind != KIND_NONE) return st;
     }
     Plan r = plan_rows(op, T, H, s, vec, num_sms);
     if (r.kind == KIND_TWO_PASS && vec) {
+        if (many) {
+            Plan st = plan_stream(op, T, H, R, s, vec, num_sms, max_smem, op == OP_PLAIN ? 2 : 1);
+            if (st.kind != KIND_NONE) return st;
+        }
         Plan c = plan_cluster(op, T, H, s, vec, num_sms);
         if (c.kind != KIND_NONE) return c;
     }

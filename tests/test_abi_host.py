@@ -163,9 +163,14 @@ def test_plan_auto_policy():
     # R = 2 reduce: stream kernel with two consumer groups
     p = _plan("reduce_add_rms_norm", 16384, 4096, 2, "bf16")
     assert p.startswith("stream") and "groups=2" in p, p
-    # fused with 8 KB rows: register kernel; with 16 KB rows: stream
-    assert _plan("fused_add_rms_norm", 4096, 4096, 1, "bf16").startswith("rows.cta")
-    assert _plan("fused_add_rms_norm", 4096, 8192, 1, "bf16").startswith("stream")
+    # fused / plain rows that fit one CTA's registers: the pipelined register
+    # kernel; longer rows: the stream kernel
+    for H in (4096, 8192, 16384):
+        p = _plan("fused_add_rms_norm", 4096, H, 1, "bf16")
+        assert p.startswith("rows.cta") and "pipe=1" in p, p
+    assert _plan("fused_add_rms_norm", 4096, 32768, 1, "bf16").startswith("stream")
+    p = _plan("rms_norm", 4096, 20000, 0, "bf16")
+    assert p.startswith("stream") and "groups=2" in p, p
     # few rows: never the persistent kernel
     assert _plan("reduce_add_rms_norm", 64, 8192, 8, "bf16").startswith("rows")
     # 32 KB rows, few of them: one CTA per row still holds the row (8 packs
