@@ -72,6 +72,9 @@ class Oracle:
         for f in (lib.oracle_rms_norm, lib.oracle_fused_add_rms_norm,
                   lib.oracle_reduce_add_rms_norm):
             f.restype = c_int
+        lib.oracle_rows_ex.argtypes = [c_int, c_int, i64, i64, i32, p, i64, i64, p, p, i64, p, f32,
+                                       p, i64, p, p, c_int]
+        lib.oracle_rows_ex.restype = c_int
         lib.oracle_decode.argtypes = [c_int, p, p, i64]
         lib.oracle_decode.restype = None
         lib.oracle_round.argtypes = [c_int, p, p, i64]
@@ -129,6 +132,28 @@ class Oracle:
             _ptr(res_out), _ptr(y), _ptr(inv), _ptr(y64), threads))
         return Result(y, res_out, inv, y64, n)
 
+    def rows_ex(self, dtype, rdtype, T, H, R, x, ldx, slice_, residual, ldr, gamma, eps, y, ldy,
+                *, want_y64=False, threads=0) -> Result:
+        """General form: x (R = 0 or 1) or the R partials live in the flat
+        storage array ``x`` with row stride ``ldx`` and ``slice_`` elements
+        between partials; ``residual`` (storage type ``rdtype``, row stride
+        ``ldr``) is updated IN PLACE; ``y`` (row stride ``ldy``) receives the
+        first H elements of each row.  R = 0 is plain RMSNorm."""
+        x = self._as_storage(x, dtype)
+        gamma = self._as_storage(gamma, dtype)
+        if not (y.flags.c_contiguous and y.dtype == STORAGE[dtype]):
+            raise TypeError("y must be contiguous storage of the x dtype")
+        if residual is not None and not (residual.flags.c_contiguous and
+                                         residual.dtype == STORAGE[rdtype]):
+            raise TypeError("residual must be contiguous storage of its dtype")
+        inv = np.empty(T, np.float64)
+        y64 = np.empty((T, H), np.float64) if want_y64 else None
+        n = _check(self.lib.oracle_rows_ex(
+            DTYPES[dtype], DTYPES[rdtype], T, H, R, _ptr(x), ldx, slice_, _ptr(residual),
+            _ptr(residual), ldr, _ptr(gamma), float(eps), _ptr(y), ldy, _ptr(inv), _ptr(y64),
+            threads))
+        return Result(y, residual, inv, y64, n)
+
     def decode(self, bits, dtype) -> np.ndarray:
         """Storage bits -> binary64 values (the oracle's own decoder)."""
         bits = self._as_storage(bits, dtype)
@@ -165,6 +190,10 @@ def fused_add_rms_norm(*a, **k) -> Result:
 
 def reduce_add_rms_norm(*a, **k) -> Result:
     return default().reduce_add_rms_norm(*a, **k)
+
+
+def rows_ex(*a, **k) -> Result:
+    return default().rows_ex(*a, **k)
 
 
 def decode(*a, **k) -> np.ndarray:

@@ -159,37 +159,43 @@ static void store_exact(int dt, void *base, int64_t i, double v) {
 /* ----------------------------------------------------------------------- */
 
 typedef struct {
-    int dt;
+    int dt;                    /* storage type of x / partials, gamma and y */
+    int rdt;                   /* storage type of the residual (in and out) */
     int64_t T, H;
     int32_t R;                 /* number of partial buffers; 0 = plain */
-    const void *x;             /* plain: x[T,H]; fused/reduce: partials[R,T,H] */
-    const void *residual_in;   /* [T,H] or NULL (plain) */
+    const void *x;             /* plain: x; fused/reduce: partials (R buffers) */
+    int64_t ldx;               /* elements between rows of x / of each partial */
+    int64_t slice;             /* elements between partial buffers */
+    const void *residual_in;   /* or NULL (plain) */
+    int64_t ldr;               /* elements between rows of the residual (in and out) */
     const void *gamma;         /* [H] */
     float eps;
-    void *residual_out;        /* [T,H] or NULL */
-    void *y;                   /* [T,H] */
+    void *residual_out;        /* or NULL */
+    void *y;
+    int64_t ldy;               /* elements between rows of y */
     double *inv_out;           /* [T] or NULL */
-    double *y64_out;           /* [T,H] or NULL: y before the final rounding */
+    double *y64_out;           /* [T, H] dense or NULL: y before the final rounding */
 } job_t;
 
 static void one_row(const job_t *j, int64_t t, double *h) {
     const int64_t H = j->H;
-    const int64_t row = t * H;
+    const int64_t xrow = t * j->ldx;
+    const int64_t rrow = t * j->ldr;
+    const int64_t yrow = t * j->ldy;
 
     /* step 1: h */
     if (j->residual_in == NULL) {
-        for (int64_t i = 0; i < H; ++i) h[i] = load_elem(j->dt, j->x, row + i);
+        for (int64_t i = 0; i < H; ++i) h[i] = load_elem(j->dt, j->x, xrow + i);
     } else {
-        const int64_t slice = j->T * H;
         for (int64_t i = 0; i < H; ++i) {
-            float acc = (float)load_elem(j->dt, j->x, row + i);
+            float acc = (float)load_elem(j->dt, j->x, xrow + i);
             for (int32_t r = 1; r < j->R; ++r)
-                acc = acc + (float)load_elem(j->dt, j->x, (int64_t)r * slice + row + i);
-            acc = acc + (float)load_elem(j->dt, j->residual_in, row + i);
-            h[i] = round_dt(j->dt, (double)acc);
+                acc = acc + (float)load_elem(j->dt, j->x, (int64_t)r * j->slice + xrow + i);
+            acc = acc + (float)load_elem(j->rdt, j->residual_in, rrow + i);
+            h[i] = round_dt(j->rdt, (double)acc);
         }
         if (j->residual_out)
-            for (int64_t i = 0; i < H; ++i) store_exact(j->dt, j->residual_out, row + i, h[i]);
+            for (int64_t i = 0; i < H; ++i) store_exact(j->rdt, j->residual_out, rrow + i, h[i]);
     }
 
     /* step 2: sum of squares of the (stored) row */
@@ -203,8 +209,8 @@ static void one_row(const job_t *j, int64_t t, double *h) {
     /* step 4: scale, weight, one rounding */
     for (int64_t i = 0; i < H; ++i) {
         double v = (h[i] * inv) * load_elem(j->dt, j->gamma, i);
-        if (j->y64_out) j->y64_out[row + i] = v;
-        store_exact(j->dt, j->y, row + i, round_dt(j->dt, v));
+        if (j->y64_out) j->y64_out[t * H + i] = v;
+        store_exact(j->dt, j->y, yrow + i, round_dt(j->dt, v));
     }
 }
 
@@ -272,7 +278,7 @@ static int run(const job_t *j, int nthreads) {
 
 int oracle_rms_norm(int dt, int64_t T, int64_t H, const void *x, const void *gamma, float eps,
                     void *y, double *inv_out, double *y64_out, int nthreads) {
-    job_t j = {dt, T, H, 0, x, NULL, gamma, eps, NULL, y, inv_out, y64_out};
+    job_t j = {dt, dt, T, H, 0, x, H, T * H, NULL, H, gamma, eps, NULL, y, H, inv_out, y64_out};
     return run(&j, nthreads);
 }
 
@@ -280,7 +286,8 @@ int oracle_fused_add_rms_norm(int dt, int64_t T, int64_t H, const void *x, const
                               const void *gamma, float eps, void *residual_out, void *y,
                               double *inv_out, double *y64_out, int nthreads) {
     if (!residual_in) return -2;
-    job_t j = {dt, T, H, 1, x, residual_in, gamma, eps, residual_out, y, inv_out, y64_out};
+    job_t j = {dt, dt, T, H, 1, x, H, T * H, residual_in, H, gamma, eps, residual_out, y, H,
+               inv_out, y64_out};
     return run(&j, nthreads);
 }
 
@@ -289,7 +296,27 @@ int oracle_reduce_add_rms_norm(int dt, int64_t T, int64_t H, int32_t R, const vo
                                void *residual_out, void *y, double *inv_out, double *y64_out,
                                int nthreads) {
     if (!residual_in || R < 1) return -2;
-    job_t j = {dt, T, H, R, partials, residual_in, gamma, eps, residual_out, y, inv_out, y64_out};
+    job_t j = {dt, dt, T, H, R, partials, H, T * H, residual_in, H, gamma, eps, residual_out, y, H,
+               inv_out, y64_out};
+    return run(&j, nthreads);
+}
+
+/*
+ * General form: every buffer has its own row stride (in elements, >= H), the
+ * partial buffers are `slice` elements apart, and the residual has its own
+ * storage type `rdt` (the sum is rounded once to rdt, which is the identity
+ * for binary32).  R = 0: plain (residual ignored); R >= 1: partials (x for
+ * R = 1) plus residual.  The residual is updated in place (residual_out may
+ * equal residual_in).  Only the first H elements of each row of y and of the
+ * residual are written.
+ */
+int oracle_rows_ex(int dt, int rdt, int64_t T, int64_t H, int32_t R, const void *x, int64_t ldx,
+                   int64_t slice, const void *residual_in, void *residual_out, int64_t ldr,
+                   const void *gamma, float eps, void *y, int64_t ldy, double *inv_out,
+                   double *y64_out, int nthreads) {
+    if (R < 0 || ldx < H || ldy < H || (R >= 1 && (!residual_in || ldr < H))) return -2;
+    job_t j = {dt, rdt, T, H, R, x, ldx, slice, R >= 1 ? residual_in : NULL, ldr, gamma, eps,
+               R >= 1 ? residual_out : NULL, y, ldy, inv_out, y64_out};
     return run(&j, nthreads);
 }
 

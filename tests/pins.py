@@ -421,6 +421,118 @@ def pin_brute_force_tiny(O):
             assert np.array_equal(lib_decode(res.y[t], dt), want_bits), (dt, t)
 
 
+# ---------------------------------------------------------------------------
+# Pins on the general form: row strides and an fp32 residual
+# ---------------------------------------------------------------------------
+
+GARBAGE = {"f32": np.float32(-1234.5), "f16": np.uint16(0x7BFF), "bf16": np.uint16(0x4B4B)}
+
+
+def _strided(dense, ld, dtype, extra=0):
+    """Copy [T, H] storage into a flat buffer with row stride ld, the padding
+    (and `extra` trailing elements) filled with a garbage pattern."""
+    T, H = dense.shape
+    buf = np.full(T * ld + extra, GARBAGE[dtype], dtype=dense.dtype)
+    view = buf[:T * ld].reshape(T, ld)
+    view[:, :H] = dense
+    return buf
+
+
+def _rows(buf, T, ld, H):
+    return buf[:T * ld].reshape(T, ld)[:, :H]
+
+
+def pin_strided_equals_dense(O):
+    """Rows with a stride larger than H (padding holding garbage) give the
+    dense results, and nothing outside the first H elements of each row of y
+    or of the residual is written."""
+    rng = np.random.default_rng(11)
+    for dt in ("f32", "bf16", "f16"):
+        for R in (0, 1, 3):
+            T, H, ldx, ldr, ldy = 5, 37, 45, 41, 50
+            n = max(R, 1)
+            parts = np.stack([_rand_bits(rng, (T, H), dt) for _ in range(n)])
+            res = _rand_bits(rng, (T, H), dt)
+            g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+            slice_ = T * ldx + 3
+            X = np.concatenate([_strided(parts[r], ldx, dt, extra=3) for r in range(n)])
+            Rb = _strided(res, ldr, dt)
+            Y = np.full(T * ldy, GARBAGE[dt], dtype=parts.dtype)
+            r_ex = O.rows_ex(dt, dt, T, H, R, X, ldx, slice_, Rb if R else None, ldr, g, 1e-5,
+                             Y, ldy)
+            if R == 0:
+                want = O.rms_norm(parts[0], g, 1e-5, dt)
+            elif R == 1:
+                want = O.fused_add_rms_norm(parts[0], res, g, 1e-5, dt)
+            else:
+                want = O.reduce_add_rms_norm(parts, res, g, 1e-5, dt)
+            assert np.array_equal(_rows(Y, T, ldy, H), want.y), (dt, R)
+            pad_y = Y[:T * ldy].reshape(T, ldy)[:, H:]
+            assert np.array_equal(pad_y, np.full_like(pad_y, GARBAGE[dt])), (dt, R)
+            if R:
+                assert np.array_equal(_rows(Rb, T, ldr, H), want.residual), (dt, R)
+                pad_r = Rb.reshape(T, ldr)[:, H:]
+                assert np.array_equal(pad_r, np.full_like(pad_r, GARBAGE[dt])), (dt, R)
+
+
+def pin_fp32_residual_sum(O):
+    """An fp32 residual with 16-bit inputs: the stored residual is the binary32
+    sequential sum itself, with no rounding to 16 bits (exact rational
+    emulation of every add), and inv / y64 follow from that binary32 row."""
+    getcontext().prec = 50
+    rng = np.random.default_rng(12)
+    for dt in ("bf16", "f16"):
+        for R in (1, 3):
+            T, H = 3, 17
+            parts = np.stack([_rand_bits(rng, (T, H), dt) for _ in range(R)])
+            res = (rng.standard_normal((T, H)) * 0.37).astype(np.float32)  # not 16-bit values
+            g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+            X = parts.reshape(-1).copy()
+            Rb = res.reshape(-1).copy()
+            Y = np.zeros(T * H, parts.dtype)
+            out = O.rows_ex(dt, "f32", T, H, R, X, H, T * H, Rb, H, g, 1e-3, Y, H, want_y64=True)
+            pv = lib_decode(parts, dt)
+            gv = lib_decode(g, dt)
+            e32 = Fraction(float(np.float32(1e-3)))
+            for t in range(T):
+                h = []
+                for i in range(H):
+                    acc = Fraction(pv[0, t, i])
+                    for k in range(1, R):
+                        acc = Fraction(rn_exact(acc + Fraction(pv[k, t, i]), "f32"))
+                    acc = Fraction(rn_exact(acc + Fraction(float(res[t, i])), "f32"))
+                    h.append(acc)
+                got = out.residual.reshape(T, H)[t].astype(np.float64)
+                assert np.array_equal(got, np.array([float(v) for v in h])), (dt, R, t)
+                m = sum(v * v for v in h) / H + e32
+                inv = 1 / (Decimal(m.numerator) / Decimal(m.denominator)).sqrt()
+                assert abs(out.inv[t] - float(inv)) <= 1e-15 * float(inv), (dt, R, t)
+                want = np.array([float(Decimal(v.numerator) / Decimal(v.denominator) * inv *
+                                       Decimal(gv[i])) for i, v in enumerate(h)])
+                assert _rel(out.y64[t], want) < 1e-14, (dt, R, t)
+
+
+def pin_fp32_residual_matches_16bit_when_exact(O):
+    """Integer data whose sums stay exactly representable in 16 bits: an fp32
+    residual and a 16-bit residual give identical y and identical residual
+    values."""
+    rng = np.random.default_rng(13)
+    for dt in ("bf16", "f16"):
+        R, T, H = 4, 3, 29
+        pi = rng.integers(-8, 9, size=(R, T, H)).astype(np.float64)
+        ri = rng.integers(-8, 9, size=(T, H)).astype(np.float64)
+        parts = bits_of(pi, dt).reshape(R, T, H)
+        g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+        same = O.reduce_add_rms_norm(parts, bits_of(ri, dt), g, 1e-6, dt)
+        Rb = ri.astype(np.float32).reshape(-1).copy()
+        Y = np.zeros(T * H, parts.dtype)
+        mixed = O.rows_ex(dt, "f32", T, H, R, parts.reshape(-1).copy(), H, T * H, Rb, H, g, 1e-6,
+                          Y, H)
+        assert np.array_equal(mixed.y.reshape(T, H), same.y), dt
+        assert np.array_equal(mixed.residual.reshape(T, H).astype(np.float64),
+                              lib_decode(same.residual, dt)), dt
+
+
 ALL_PINS = [
     pin_decode_all_patterns,
     pin_round_matches_library,
@@ -436,4 +548,7 @@ ALL_PINS = [
     pin_scale_invariance,
     pin_single_element_rows,
     pin_brute_force_tiny,
+    pin_strided_equals_dense,
+    pin_fp32_residual_sum,
+    pin_fp32_residual_matches_16bit_when_exact,
 ]

@@ -26,15 +26,23 @@ MUTATIONS = {
     # reciprocal used the wrong way round
     "divide_by_inv": ("(h[i] * inv)", "(h[i] / inv)"),
     # residual not added
-    "drop_residual": ("acc = acc + (float)load_elem(j->dt, j->residual_in, row + i);", ""),
+    "drop_residual": ("acc = acc + (float)load_elem(j->rdt, j->residual_in, rrow + i);", ""),
     # partial sum kept in binary64 instead of binary32
     "wide_accumulator": ("float acc = (float)load_elem", "double acc = (float)load_elem"),
     # wrong stride between partial buffers
-    "partial_stride": ("(int64_t)r * slice + row + i", "(int64_t)r * H + row + i"),
+    "partial_stride": ("(int64_t)r * j->slice + xrow + i", "(int64_t)r * j->H + xrow + i"),
     # first partial skipped
-    "skip_p0": ("float acc = (float)load_elem(j->dt, j->x, row + i);", "float acc = 0.0f;"),
+    "skip_p0": ("float acc = (float)load_elem(j->dt, j->x, xrow + i);", "float acc = 0.0f;"),
     # sum of squares from the unrounded sum
-    "unrounded_h": ("h[i] = round_dt(j->dt, (double)acc);", "h[i] = (double)acc;"),
+    "unrounded_h": ("h[i] = round_dt(j->rdt, (double)acc);", "h[i] = (double)acc;"),
+    # residual decoded / rounded with the type of x instead of its own
+    "residual_decoded_as_x": ("load_elem(j->rdt, j->residual_in", "load_elem(j->dt, j->residual_in"),
+    "residual_rounded_as_x": ("h[i] = round_dt(j->rdt, (double)acc);",
+                              "h[i] = round_dt(j->dt, (double)acc);"),
+    # row strides ignored
+    "x_stride": ("const int64_t xrow = t * j->ldx;", "const int64_t xrow = t * j->H;"),
+    "residual_stride": ("const int64_t rrow = t * j->ldr;", "const int64_t rrow = t * j->H;"),
+    "y_stride": ("const int64_t yrow = t * j->ldy;", "const int64_t yrow = t * j->H;"),
     # ties away from zero instead of to even
     "ties_away": ("nearbyint(ldexp(v, -q))", "round(ldexp(v, -q))"),
     # truncation instead of rounding
