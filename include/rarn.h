@@ -168,6 +168,46 @@ rarn_status rarn_reduce_add_rms_norm_host(void *y, const void *partials, int32_t
                                           void *residual, const void *gamma, int64_t T,
                                           int64_t H, float eps, rarn_dtype dt, void *stream);
 
+/*
+ * General forms: per-buffer row strides and an fp32 residual stream.
+ *
+ * A rarn_rows names a [T, H] matrix inside a larger allocation: row t starts
+ * at element t * row_stride of `data` (row_stride >= H, in elements of
+ * `dtype`); only the first H elements of each row are read or written.
+ * Partials are R such matrices `partial_stride` elements apart (from the
+ * start of one to the start of the next).  gamma is [H] of the inputs' type.
+ *
+ * Storage types: y, x / partials and gamma share one type; the residual has
+ * either that type or RARN_F32 with 16-bit inputs (the sum of the partials and
+ * the residual is then kept in binary32 with no rounding, and y is rounded
+ * once to the 16-bit type).  Other combinations return RARN_ERR_UNSUPPORTED.
+ *
+ * Aliasing is judged on the row spans ((T - 1) * row_stride + H elements):
+ * y may equal x / partial 0 exactly (same data and row stride); any other
+ * overlap of an output with another buffer returns RARN_ERR_ALIAS, even where
+ * the rows themselves would interleave without touching.  The 16-byte kernels
+ * run when every base pointer is 16-byte aligned and every row stride and the
+ * partial stride are multiples of 16 bytes.  Everything else is as for the
+ * dense forms above; those are these forms with every row stride H and the
+ * partials T * H apart.  ("RMSNorm kernel", 1 Background: the norm runs over
+ * the last dimension of [..., hidden]; a row stride lets that last dimension
+ * be a slice of a wider one.)
+ */
+typedef struct rarn_rows {
+    void *data;
+    int64_t row_stride;
+    rarn_dtype dtype;
+} rarn_rows;
+
+rarn_status rarn_rms_norm_ex(rarn_rows y, rarn_rows x, const void *gamma, int64_t T, int64_t H,
+                             float eps, void *stream);
+rarn_status rarn_fused_add_rms_norm_ex(rarn_rows y, rarn_rows x, rarn_rows residual,
+                                       const void *gamma, int64_t T, int64_t H, float eps,
+                                       void *stream);
+rarn_status rarn_reduce_add_rms_norm_ex(rarn_rows y, rarn_rows partials, int64_t partial_stride,
+                                        int32_t R, rarn_rows residual, const void *gamma,
+                                        int64_t T, int64_t H, float eps, void *stream);
+
 /* Static text for a status code. */
 const char *rarn_status_string(rarn_status s);
 
@@ -214,6 +254,10 @@ rarn_status rarn_test_stall(long long fill, unsigned long long wait_limit_ns);
  */
 rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt, int vec_ok,
                       int num_sms, char *out, size_t cap);
+
+/* rarn_plan for a residual of storage type `rdt` (see the general forms). */
+rarn_status rarn_plan_ex(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt,
+                         rarn_dtype rdt, int vec_ok, int num_sms, char *out, size_t cap);
 
 /*
  * Watchdog word of the current device.  Kernels that wait on shared-memory

@@ -20,7 +20,7 @@ import os
 __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_host",
            "fused_add_rms_norm_host", "reduce_add_rms_norm_host", "RarnError", "library",
            "set_path", "get_path", "set_pdl", "get_pdl", "plan", "watchdog", "PATHS",
-           "DTYPE_CODES"]
+           "DTYPE_CODES", "rms_norm_ex", "fused_add_rms_norm_ex", "reduce_add_rms_norm_ex"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
@@ -42,6 +42,12 @@ class RarnError(RuntimeError):
         if status == 4:
             msg += f" (cudaError {cuda_error})"
         super().__init__(msg)
+
+
+class Rows(ctypes.Structure):
+    """``rarn_rows``: data pointer, row stride in elements, storage type."""
+    _fields_ = [("data", ctypes.c_void_p), ("row_stride", ctypes.c_int64),
+                ("dtype", ctypes.c_int)]
 
 
 _lib = None
@@ -85,6 +91,16 @@ def library() -> ctypes.CDLL:
     lib.rarn_version.restype = c_int
     lib.rarn_host_access.argtypes = []
     lib.rarn_host_access.restype = c_int
+    lib.rarn_rms_norm_ex.argtypes = [Rows, Rows, vp, i64, i64, f32, vp]
+    lib.rarn_fused_add_rms_norm_ex.argtypes = [Rows, Rows, Rows, vp, i64, i64, f32, vp]
+    lib.rarn_reduce_add_rms_norm_ex.argtypes = [Rows, Rows, i64, i32, Rows, vp, i64, i64, f32,
+                                                vp]
+    for f in (lib.rarn_rms_norm_ex, lib.rarn_fused_add_rms_norm_ex,
+              lib.rarn_reduce_add_rms_norm_ex):
+        f.restype = c_int
+    lib.rarn_plan_ex.argtypes = [c_int, i64, i64, i32, c_int, c_int, c_int, c_int,
+                                 ctypes.c_char_p, ctypes.c_size_t]
+    lib.rarn_plan_ex.restype = c_int
     lib.rarn_set_pdl.argtypes = [c_int]
     lib.rarn_set_pdl.restype = c_int
     lib.rarn_get_pdl.argtypes = []
@@ -283,6 +299,68 @@ def set_path(name: str) -> None:
     _check(library().rarn_set_path(PATHS[name]), "rarn_set_path")
 
 
+def _rows(name, t, device):
+    """A 2-D CUDA tensor with unit element stride as a rarn_rows."""
+    if not t.is_cuda or t.device != device:
+        raise ValueError(f"{name} must be a CUDA tensor on {device}")
+    if t.dim() != 2 or t.stride(1) != 1 or t.stride(0) < t.shape[1]:
+        raise ValueError(f"{name} must be 2-D with unit stride along rows and a row stride "
+                         f">= its row length")
+    return Rows(t.data_ptr(), t.stride(0), _dtype_code(t))
+
+
+def rms_norm_ex(x, gamma, eps: float, out):
+    """rms_norm on row-strided 2-D views: x [T, H] and out [T, H] may be
+    slices of wider tensors (unit stride within a row, any row stride >= H)."""
+    import torch
+    T, H = x.shape
+    _check_tensor("gamma", gamma, x.dtype, x.device)
+    if gamma.numel() != H or tuple(out.shape) != (T, H):
+        raise ValueError("shape mismatch")
+    with torch.cuda.device(x.device):
+        _check(library().rarn_rms_norm_ex(_rows("out", out, x.device), _rows("x", x, x.device),
+                                          gamma.data_ptr(), T, H, float(eps), _stream(x.device)),
+               "rarn_rms_norm_ex")
+    return out
+
+
+def fused_add_rms_norm_ex(x, residual, gamma, eps: float, out):
+    """fused_add_rms_norm on row-strided 2-D views; the residual may be
+    float32 with float16 / bfloat16 x, gamma and out (an fp32 residual
+    stream: the sum is kept in binary32)."""
+    import torch
+    T, H = x.shape
+    _check_tensor("gamma", gamma, x.dtype, x.device)
+    if gamma.numel() != H or tuple(out.shape) != (T, H) or tuple(residual.shape) != (T, H):
+        raise ValueError("shape mismatch")
+    with torch.cuda.device(x.device):
+        _check(library().rarn_fused_add_rms_norm_ex(
+            _rows("out", out, x.device), _rows("x", x, x.device),
+            _rows("residual", residual, x.device), gamma.data_ptr(), T, H, float(eps),
+            _stream(x.device)), "rarn_fused_add_rms_norm_ex")
+    return out
+
+
+def reduce_add_rms_norm_ex(partials, residual, gamma, eps: float, out):
+    """reduce_add_rms_norm on strided views: partials [R, T, H] with unit
+    stride within a row and any row / partial strides; residual and out are
+    row-strided 2-D views; the residual may be float32 with 16-bit partials."""
+    import torch
+    R, T, H = partials.shape
+    dev = partials.device
+    if not partials.is_cuda or partials.stride(2) != 1 or partials.stride(1) < H:
+        raise ValueError("partials must be [R, T, H] with unit stride within a row")
+    _check_tensor("gamma", gamma, partials.dtype, dev)
+    if gamma.numel() != H or tuple(out.shape) != (T, H) or tuple(residual.shape) != (T, H):
+        raise ValueError("shape mismatch")
+    pr = Rows(partials.data_ptr(), partials.stride(1), _dtype_code(partials))
+    with torch.cuda.device(dev):
+        _check(library().rarn_reduce_add_rms_norm_ex(
+            _rows("out", out, dev), pr, partials.stride(0), R, _rows("residual", residual, dev),
+            gamma.data_ptr(), T, H, float(eps), _stream(dev)), "rarn_reduce_add_rms_norm_ex")
+    return out
+
+
 def set_pdl(enable: bool) -> None:
     """Programmatic dependent launch for every later launch (process-wide)."""
     _check(library().rarn_set_pdl(int(bool(enable))), "rarn_set_pdl")
@@ -298,11 +376,12 @@ def get_path() -> str:
 
 
 def plan(op: str, T: int, H: int, R: int, dtype: str, vec_ok: bool = True,
-         num_sms: int = 0) -> str:
-    """The kernel the current path setting would launch for a problem."""
+         num_sms: int = 0, rdtype: str | None = None) -> str:
+    """The kernel the current path setting would launch for a problem
+    (``rdtype``: the residual's storage type, default ``dtype``)."""
     buf = ctypes.create_string_buffer(256)
-    st = library().rarn_plan(OP_CODES[op], T, H, R, DTYPE_CODES[dtype], int(vec_ok), num_sms,
-                             buf, 256)
+    st = library().rarn_plan_ex(OP_CODES[op], T, H, R, DTYPE_CODES[dtype],
+                                DTYPE_CODES[rdtype or dtype], int(vec_ok), num_sms, buf, 256)
     if st not in (0, 2):
         _check(st, "rarn_plan")
     return buf.value.decode()

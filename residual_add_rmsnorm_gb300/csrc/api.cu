@@ -83,7 +83,9 @@ int round_up(int64_t a, int64_t b) { return (int)(ceil_div(a, b) * b); }
 
 // Register-staged kernels: a warp per row for short rows, a CTA per row up to
 // the register budget, two passes beyond it.
-Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
+// rn: residual words per pack (1, or 2 for a binary32 residual with 16-bit
+// inputs).
+Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms, int rn = 1) {
     Plan pl;
     pl.vec = vec;
     const int epv = vec ? 16 / s : 1;
@@ -102,7 +104,7 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
     // values per thread: aim at 256 threads per row, powers of two, within
     // the register budget of the kernel compiled for that count
     auto max_block = [&](int pt, bool pg) {
-        return vec ? rows_max_block(rows_regs_vec(pt, epv, op, pg))
+        return vec ? rows_max_block(rows_regs_vec(pt, epv, op, pg, rn))
                    : (pg ? 0 : rows_max_block(rows_regs_scalar(pt, op)));
     };
     const int max_pt = vec ? 8 : 16;
@@ -135,9 +137,9 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
     // Software pipelining across rows (plain / fused): worth it when every
     // CTA has several rows; it holds a second set of load buffers.
     if (pl.kind == KIND_CTA && pl.vec && op != OP_REDUCE && rounds >= 2) {
-        const int streams = op == OP_PLAIN ? 1 : 2;
-        const int pipe_max =
-            rows_max_block(rows_regs_vec(pl.per_thread, epv, op, false) + pl.per_thread * 4 * streams);
+        const int streams = op == OP_PLAIN ? 1 : 1 + rn;
+        const int pipe_max = rows_max_block(rows_regs_vec(pl.per_thread, epv, op, false, rn) +
+                                            pl.per_thread * 4 * streams);
         pl.pipe = pl.block <= pipe_max;
         if (const char *v = getenv("RARN_ROWS_PIPE")) {  // measurements only
             if (*v == '0') pl.pipe = false;
@@ -192,7 +194,7 @@ Plan plan_stream(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_s
 
 // Cluster per row: the smallest cluster (2, 4, 8 CTAs) whose segments fit the
 // register budget and, where possible, puts a CTA on every SM.
-Plan plan_cluster(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
+Plan plan_cluster(int op, int64_t T, int64_t H, int s, bool vec, int num_sms, int rn = 1) {
     Plan pl;
     if (!vec) return pl;
     const int epv = 16 / s;
@@ -200,7 +202,7 @@ Plan plan_cluster(int op, int64_t T, int64_t H, int s, bool vec, int num_sms) {
     for (int cs = 2; cs <= 8; cs <<= 1) {
         const int64_t seg = ceil_div(n, cs);
         auto max_block = [&](int p, bool pg) {
-            return rows_max_block(rows_regs_vec(p, epv, op, pg));
+            return rows_max_block(rows_regs_vec(p, epv, op, pg, rn));
         };
         int pt = std::min(8, pow2_at_least(ceil_div(seg, 256)));
         while (pt < 8 && ceil_div(seg, pt) > max_block(pt, false)) pt <<= 1;
@@ -247,33 +249,37 @@ int stream_groups(int fallback) {
 //        stream kernel for one or two input streams up to 32 KB rows;
 //  * few rows: the register kernels, with a cluster per row where one CTA's
 //    registers cannot hold the row.
-Plan plan_auto(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_sms, int max_smem) {
-    const bool many = vec && T >= 2 * (int64_t)num_sms;
+Plan plan_auto(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_sms, int max_smem,
+               int rn) {
+    const bool many = vec && T >= 2 * (int64_t)num_sms && rn == 1;  // stream: same types only
     if (many && op == OP_REDUCE && R >= 2) {
         Plan st = plan_stream(op, T, H, R, s, vec, num_sms, max_smem, R >= 4 ? 1 : 2);
         if (st.kind != KIND_NONE) return st;
     }
-    Plan r = plan_rows(op, T, H, s, vec, num_sms);
+    Plan r = plan_rows(op, T, H, s, vec, num_sms, rn);
     if (r.kind == KIND_TWO_PASS && vec) {
         if (many) {
             Plan st = plan_stream(op, T, H, R, s, vec, num_sms, max_smem, op == OP_PLAIN ? 2 : 1);
             if (st.kind != KIND_NONE) return st;
         }
-        Plan c = plan_cluster(op, T, H, s, vec, num_sms);
+        Plan c = plan_cluster(op, T, H, s, vec, num_sms, rn);
         if (c.kind != KIND_NONE) return c;
     }
     return r;
 }
 
+// rn: residual words per pack (2 for a binary32 residual with 16-bit
+// inputs: register and cluster kernels only).
 Plan make_plan(int op, int64_t T, int64_t H, int R, rarn_dtype dt, bool vec, int num_sms,
-               int max_smem, int path) {
+               int max_smem, int path, int rn = 1) {
     const int s = elem_size(dt);
     switch (path) {
-    case RARN_PATH_ROWS: return plan_rows(op, T, H, s, vec, num_sms);
+    case RARN_PATH_ROWS: return plan_rows(op, T, H, s, vec, num_sms, rn);
     case RARN_PATH_STREAM:
+        if (rn != 1) return Plan{};
         return plan_stream(op, T, H, R, s, vec, num_sms, max_smem, stream_groups(1));
-    case RARN_PATH_CLUSTER: return plan_cluster(op, T, H, s, vec, num_sms);
-    case RARN_PATH_AUTO: return plan_auto(op, T, H, R, s, vec, num_sms, max_smem);
+    case RARN_PATH_CLUSTER: return plan_cluster(op, T, H, s, vec, num_sms, rn);
+    case RARN_PATH_AUTO: return plan_auto(op, T, H, R, s, vec, num_sms, max_smem, rn);
     default: return Plan{};
     }
 }
@@ -327,30 +333,67 @@ rarn_status host_view(const void *p, int64_t bytes, bool pageable_ok, void **vie
     return RARN_ERR_INVALID_ARG;
 }
 
-rarn_status run(int op, void *y, const void *src, int32_t R, void *residual, const void *gamma,
-                int64_t T, int64_t H, float eps, rarn_dtype dt, void *stream,
-                bool host_buffers = false) {
-    if (dt != RARN_F32 && dt != RARN_F16 && dt != RARN_BF16) return RARN_ERR_INVALID_ARG;
-    if (T < 0 || H <= 0 || !(eps >= 0.f) || std::isinf(eps)) return RARN_ERR_INVALID_ARG;
-    if (op == OP_REDUCE && R < 1) return RARN_ERR_INVALID_ARG;
-    if (H > RARN_MAX_H || T > RARN_MAX_T || R > RARN_MAX_R) return RARN_ERR_UNSUPPORTED;
-    if (T == 0) return RARN_OK;
-    if (!y || !src || !gamma || (op != OP_PLAIN && !residual)) return RARN_ERR_INVALID_ARG;
+// One call, in its most general form.
+struct Call {
+    int op = OP_PLAIN;
+    void *y = nullptr;
+    int64_t ldy = 0;
+    const void *src = nullptr;  // x, or partial 0
+    int64_t ldx = 0;
+    int64_t slice = 0;          // elements between partials
+    int32_t R = 0;
+    void *residual = nullptr;
+    int64_t ldr = 0;
+    const void *gamma = nullptr;
+    int64_t T = 0, H = 0;
+    float eps = 0.f;
+    rarn_dtype dt = RARN_F32;   // x / partials, gamma, y
+    rarn_dtype rdt = RARN_F32;  // residual
+    void *stream = nullptr;
+    bool host_buffers = false;
+};
 
-    const int s = elem_size(dt);
-    const int64_t row_bytes = H * s;
-    const int64_t mat = T * row_bytes;  // one [T, H] buffer
-    const int nsrc = op == OP_REDUCE ? R : 1;
-    // y may coincide exactly with x / partial 0; nothing else may overlap an output
-    const bool y_is_src = (y == src);
-    if (!y_is_src && overlaps(y, mat, src, mat * nsrc)) return RARN_ERR_ALIAS;
-    if (y_is_src && nsrc > 1 && overlaps(y, mat, static_cast<const char *>(src) + mat,
-                                         mat * (nsrc - 1)))
+bool dtype_ok(rarn_dtype d) { return d == RARN_F32 || d == RARN_F16 || d == RARN_BF16; }
+
+// Bytes spanned by T rows of H elements with row stride ld.
+int64_t span_bytes(int64_t T, int64_t H, int64_t ld, int s) { return ((T - 1) * ld + H) * s; }
+
+rarn_status run_ex(Call c) {
+    const int op = c.op;
+    if (!dtype_ok(c.dt) || !dtype_ok(c.rdt)) return RARN_ERR_INVALID_ARG;
+    if (c.T < 0 || c.H <= 0 || !(c.eps >= 0.f) || std::isinf(c.eps)) return RARN_ERR_INVALID_ARG;
+    if (op == OP_REDUCE && c.R < 1) return RARN_ERR_INVALID_ARG;
+    if (c.H > RARN_MAX_H || c.T > RARN_MAX_T || c.R > RARN_MAX_R) return RARN_ERR_UNSUPPORTED;
+    if (c.ldx < c.H || c.ldy < c.H || (op != OP_PLAIN && c.ldr < c.H) || c.slice < 0)
+        return RARN_ERR_INVALID_ARG;
+    if (c.T == 0) return RARN_OK;
+    if (!c.y || !c.src || !c.gamma || (op != OP_PLAIN && !c.residual)) return RARN_ERR_INVALID_ARG;
+    // storage types: all one type, or a binary32 residual with 16-bit inputs
+    const bool mixed = op != OP_PLAIN && c.rdt != c.dt;
+    if (mixed && !(c.rdt == RARN_F32 && (c.dt == RARN_F16 || c.dt == RARN_BF16)))
+        return RARN_ERR_UNSUPPORTED;
+    if (op == OP_PLAIN) c.rdt = c.dt;
+
+    const int s = elem_size(c.dt), rs = elem_size(c.rdt);
+    const int64_t row_bytes = c.H * s;
+    const int nsrc = op == OP_REDUCE ? c.R : 1;
+    const int64_t ybytes = span_bytes(c.T, c.H, c.ldy, s);
+    const int64_t xbytes = span_bytes(c.T, c.H, c.ldx, s);
+    const int64_t srcbytes = (int64_t)(nsrc - 1) * c.slice * s + xbytes;
+    const int64_t rbytes = op != OP_PLAIN ? span_bytes(c.T, c.H, c.ldr, rs) : 0;
+    // y may coincide exactly with x / partial 0 (same row stride); nothing
+    // else may overlap an output (overlaps are judged on the row spans)
+    const bool y_is_src = c.y == c.src && c.ldy == c.ldx;
+    if (!y_is_src && overlaps(c.y, ybytes, c.src, srcbytes)) return RARN_ERR_ALIAS;
+    if (y_is_src && nsrc > 1 &&
+        overlaps(c.y, ybytes, static_cast<const char *>(c.src) + c.slice * s,
+                 srcbytes - c.slice * s))
         return RARN_ERR_ALIAS;
-    if (overlaps(y, mat, gamma, row_bytes)) return RARN_ERR_ALIAS;
+    if (overlaps(c.y, ybytes, c.gamma, row_bytes)) return RARN_ERR_ALIAS;
     if (op != OP_PLAIN) {
-        if (overlaps(residual, mat, y, mat) || overlaps(residual, mat, src, mat * nsrc) ||
-            overlaps(residual, mat, gamma, row_bytes))
+        if (overlaps(c.residual, rbytes, c.y, ybytes) ||
+            overlaps(c.residual, rbytes, c.src, srcbytes) ||
+            overlaps(c.residual, rbytes, c.gamma, row_bytes))
             return RARN_ERR_ALIAS;
     }
 
@@ -358,7 +401,7 @@ rarn_status run(int op, void *y, const void *src, int32_t R, void *residual, con
     rarn_status st = device_info(&d);
     if (st != RARN_OK) return st;
 
-    if (host_buffers) {
+    if (c.host_buffers) {
         // Every buffer lives in host memory; the kernels read and write it
         // through its device mapping (over NVLink-C2C on Grace systems), so
         // the transfers happen inside the kernel.
@@ -369,41 +412,48 @@ rarn_status run(int op, void *y, const void *src, int32_t R, void *residual, con
                                    dev) != cudaSuccess)
             pageable = 0;
         void *vy, *vs, *vg, *vr = nullptr;
-        if ((st = host_view(y, mat, pageable, &vy)) != RARN_OK) return st;
-        if ((st = host_view(src, mat * nsrc, pageable, &vs)) != RARN_OK) return st;
-        if ((st = host_view(gamma, row_bytes, pageable, &vg)) != RARN_OK) return st;
-        if (op != OP_PLAIN && (st = host_view(residual, mat, pageable, &vr)) != RARN_OK) return st;
-        y = vy;
-        src = vs;
-        gamma = vg;
-        residual = vr;
+        if ((st = host_view(c.y, ybytes, pageable, &vy)) != RARN_OK) return st;
+        if ((st = host_view(c.src, srcbytes, pageable, &vs)) != RARN_OK) return st;
+        if ((st = host_view(c.gamma, row_bytes, pageable, &vg)) != RARN_OK) return st;
+        if (op != OP_PLAIN && (st = host_view(c.residual, rbytes, pageable, &vr)) != RARN_OK)
+            return st;
+        c.y = vy;
+        c.src = vs;
+        c.gamma = vg;
+        c.residual = vr;
     }
 
-    const bool vec = aligned16(y) && aligned16(src) && aligned16(gamma) &&
-                     (op == OP_PLAIN || aligned16(residual)) && (row_bytes % 16 == 0);
+    const bool vec = aligned16(c.y) && aligned16(c.src) && aligned16(c.gamma) &&
+                     (c.ldx * s) % 16 == 0 && (c.ldy * s) % 16 == 0 && row_bytes % 16 == 0 &&
+                     (nsrc == 1 || (c.slice * s) % 16 == 0) &&
+                     (op == OP_PLAIN || (aligned16(c.residual) && (c.ldr * rs) % 16 == 0));
+    const int rn = mixed ? 2 : 1;
 
     // Host-resident data: the register kernels keep more requests in flight
     // over the host link than the single-producer stream kernel (measured).
-    const int path = host_buffers && g_path.load() == RARN_PATH_AUTO ? RARN_PATH_ROWS
-                                                                     : g_path.load();
-    Plan pl = make_plan(op, T, H, R, dt, vec, d->num_sms, d->max_smem_optin, path);
-    if (host_buffers && path == RARN_PATH_ROWS && pl.kind == KIND_TWO_PASS && vec) {
-        const Plan c = plan_cluster(op, T, H, elem_size(dt), vec, d->num_sms);
-        if (c.kind != KIND_NONE) pl = c;
+    const int path = c.host_buffers && g_path.load() == RARN_PATH_AUTO ? RARN_PATH_ROWS
+                                                                       : g_path.load();
+    Plan pl = make_plan(op, c.T, c.H, c.R, c.dt, vec, d->num_sms, d->max_smem_optin, path, rn);
+    if (c.host_buffers && path == RARN_PATH_ROWS && pl.kind == KIND_TWO_PASS && vec) {
+        const Plan cl = plan_cluster(op, c.T, c.H, s, vec, d->num_sms, rn);
+        if (cl.kind != KIND_NONE) pl = cl;
     }
     if (pl.kind == KIND_NONE) return RARN_ERR_UNSUPPORTED;
 
     Problem p{};
-    p.y = y;
-    p.src = src;
-    p.residual = residual;
-    p.gamma = gamma;
-    p.T = T;
-    p.H = H;
-    p.slice = T * H;
-    p.R = op == OP_PLAIN ? 0 : (op == OP_FUSED ? 1 : R);
+    p.y = c.y;
+    p.src = c.src;
+    p.residual = c.residual;
+    p.gamma = c.gamma;
+    p.T = c.T;
+    p.H = c.H;
+    p.ldx = c.ldx;
+    p.ldr = op != OP_PLAIN ? c.ldr : c.H;
+    p.ldy = c.ldy;
+    p.slice = c.slice;
+    p.R = op == OP_PLAIN ? 0 : (op == OP_FUSED ? 1 : c.R);
     p.op = op;
-    p.eps = eps;
+    p.eps = c.eps;
     p.watchdog = d->watchdog;
     p.wait_limit_ns = stream::kWaitLimitNs;
     p.stall_fill = -1;
@@ -416,36 +466,64 @@ rarn_status run(int op, void *y, const void *src, int32_t R, void *residual, con
     }
     pl.pdl = g_pdl.load() != 0;
 
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaStream_t cs = static_cast<cudaStream_t>(c.stream);
     cudaError_t e = cudaErrorInvalidValue;
+    const int key = (int)c.dt * 4 + (int)c.rdt;  // (inputs, residual) storage types
+    const int F32F32 = RARN_F32 * 4 + RARN_F32, F16F16 = RARN_F16 * 4 + RARN_F16,
+              BF16BF16 = RARN_BF16 * 4 + RARN_BF16, F16F32 = RARN_F16 * 4 + RARN_F32,
+              BF16F32 = RARN_BF16 * 4 + RARN_F32;
     switch (pl.kind) {
     case KIND_WARP:
     case KIND_CTA:
     case KIND_TWO_PASS:
-        switch (dt) {
-        case RARN_F32: e = launch_rows<float>(p, pl, cs); break;
-        case RARN_F16: e = launch_rows<__half>(p, pl, cs); break;
-        case RARN_BF16: e = launch_rows<__nv_bfloat16>(p, pl, cs); break;
-        }
+        if (key == F32F32) e = launch_rows<float, float>(p, pl, cs);
+        else if (key == F16F16) e = launch_rows<__half, __half>(p, pl, cs);
+        else if (key == BF16BF16) e = launch_rows<__nv_bfloat16, __nv_bfloat16>(p, pl, cs);
+        else if (key == F16F32) e = launch_rows<__half, float>(p, pl, cs);
+        else if (key == BF16F32) e = launch_rows<__nv_bfloat16, float>(p, pl, cs);
         break;
     case KIND_STREAM:
-        switch (dt) {
-        case RARN_F32: e = launch_stream<float>(p, pl, cs); break;
-        case RARN_F16: e = launch_stream<__half>(p, pl, cs); break;
-        case RARN_BF16: e = launch_stream<__nv_bfloat16>(p, pl, cs); break;
-        }
+        if (key == F32F32) e = launch_stream<float>(p, pl, cs);
+        else if (key == F16F16) e = launch_stream<__half>(p, pl, cs);
+        else if (key == BF16BF16) e = launch_stream<__nv_bfloat16>(p, pl, cs);
+        else return RARN_ERR_UNSUPPORTED;
         break;
     case KIND_CLUSTER:
-        switch (dt) {
-        case RARN_F32: e = launch_cluster<float>(p, pl, cs); break;
-        case RARN_F16: e = launch_cluster<__half>(p, pl, cs); break;
-        case RARN_BF16: e = launch_cluster<__nv_bfloat16>(p, pl, cs); break;
-        }
+        if (key == F32F32) e = launch_cluster<float, float>(p, pl, cs);
+        else if (key == F16F16) e = launch_cluster<__half, __half>(p, pl, cs);
+        else if (key == BF16BF16) e = launch_cluster<__nv_bfloat16, __nv_bfloat16>(p, pl, cs);
+        else if (key == F16F32) e = launch_cluster<__half, float>(p, pl, cs);
+        else if (key == BF16F32) e = launch_cluster<__nv_bfloat16, float>(p, pl, cs);
         break;
     default: return RARN_ERR_UNSUPPORTED;
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return RARN_OK;
+}
+
+// Dense row-major form of one call: every row stride H, partials T * H apart.
+rarn_status run(int op, void *y, const void *src, int32_t R, void *residual, const void *gamma,
+                int64_t T, int64_t H, float eps, rarn_dtype dt, void *stream,
+                bool host_buffers = false) {
+    Call c;
+    c.op = op;
+    c.y = y;
+    c.ldy = H;
+    c.src = src;
+    c.ldx = H;
+    c.slice = T * H;
+    c.R = R;
+    c.residual = residual;
+    c.ldr = H;
+    c.gamma = gamma;
+    c.T = T;
+    c.H = H;
+    c.eps = eps;
+    c.dt = dt;
+    c.rdt = dt;
+    c.stream = stream;
+    c.host_buffers = host_buffers;
+    return run_ex(c);
 }
 
 }  // namespace
@@ -486,6 +564,71 @@ rarn_status rarn_reduce_add_rms_norm_host(void *y, const void *partials, int32_t
     return run(OP_REDUCE, y, partials, R, residual, gamma, T, H, eps, dt, stream, true);
 }
 
+rarn_status rarn_rms_norm_ex(rarn_rows y, rarn_rows x, const void *gamma, int64_t T, int64_t H,
+                             float eps, void *stream) {
+    if (y.dtype != x.dtype) return RARN_ERR_UNSUPPORTED;
+    Call c;
+    c.op = OP_PLAIN;
+    c.y = y.data;
+    c.ldy = y.row_stride;
+    c.src = x.data;
+    c.ldx = x.row_stride;
+    c.gamma = gamma;
+    c.T = T;
+    c.H = H;
+    c.eps = eps;
+    c.dt = c.rdt = x.dtype;
+    c.stream = stream;
+    return run_ex(c);
+}
+
+rarn_status rarn_fused_add_rms_norm_ex(rarn_rows y, rarn_rows x, rarn_rows residual,
+                                       const void *gamma, int64_t T, int64_t H, float eps,
+                                       void *stream) {
+    if (y.dtype != x.dtype) return RARN_ERR_UNSUPPORTED;
+    Call c;
+    c.op = OP_FUSED;
+    c.y = y.data;
+    c.ldy = y.row_stride;
+    c.src = x.data;
+    c.ldx = x.row_stride;
+    c.R = 1;
+    c.residual = residual.data;
+    c.ldr = residual.row_stride;
+    c.gamma = gamma;
+    c.T = T;
+    c.H = H;
+    c.eps = eps;
+    c.dt = x.dtype;
+    c.rdt = residual.dtype;
+    c.stream = stream;
+    return run_ex(c);
+}
+
+rarn_status rarn_reduce_add_rms_norm_ex(rarn_rows y, rarn_rows partials, int64_t partial_stride,
+                                        int32_t R, rarn_rows residual, const void *gamma,
+                                        int64_t T, int64_t H, float eps, void *stream) {
+    if (y.dtype != partials.dtype) return RARN_ERR_UNSUPPORTED;
+    Call c;
+    c.op = OP_REDUCE;
+    c.y = y.data;
+    c.ldy = y.row_stride;
+    c.src = partials.data;
+    c.ldx = partials.row_stride;
+    c.slice = partial_stride;
+    c.R = R;
+    c.residual = residual.data;
+    c.ldr = residual.row_stride;
+    c.gamma = gamma;
+    c.T = T;
+    c.H = H;
+    c.eps = eps;
+    c.dt = partials.dtype;
+    c.rdt = residual.dtype;
+    c.stream = stream;
+    return run_ex(c);
+}
+
 const char *rarn_status_string(rarn_status s) {
     switch (s) {
     case RARN_OK: return "ok";
@@ -524,11 +667,21 @@ rarn_status rarn_test_stall(long long fill, unsigned long long wait_limit_ns) {
 
 rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt, int vec_ok,
                       int num_sms, char *out, size_t cap) {
+    return rarn_plan_ex(op, T, H, R, dt, dt, vec_ok, num_sms, out, cap);
+}
+
+rarn_status rarn_plan_ex(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt,
+                         rarn_dtype rdt, int vec_ok, int num_sms, char *out, size_t cap) {
     if (!out || cap == 0) return RARN_ERR_INVALID_ARG;
     if (op < RARN_OP_RMS_NORM || op > RARN_OP_REDUCE_ADD_RMS_NORM) return RARN_ERR_INVALID_ARG;
-    if (dt != RARN_F32 && dt != RARN_F16 && dt != RARN_BF16) return RARN_ERR_INVALID_ARG;
+    if (!dtype_ok(dt) || !dtype_ok(rdt)) return RARN_ERR_INVALID_ARG;
     if (T < 0 || H <= 0 || (op == RARN_OP_REDUCE_ADD_RMS_NORM && R < 1))
         return RARN_ERR_INVALID_ARG;
+    const bool mixed = op != RARN_OP_RMS_NORM && rdt != dt;
+    if (mixed && !(rdt == RARN_F32 && (dt == RARN_F16 || dt == RARN_BF16))) {
+        snprintf(out, cap, "none: unsupported storage types");
+        return RARN_ERR_UNSUPPORTED;
+    }
     int max_smem = kDefaultMaxSmem;
     if (num_sms <= 0) {
         DeviceInfo *d = nullptr;
@@ -538,7 +691,8 @@ rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt
         max_smem = d->max_smem_optin;
     }
     const bool vec = vec_ok && (H * elem_size(dt)) % 16 == 0;
-    const Plan pl = make_plan((int)op, T, H, R, dt, vec, num_sms, max_smem, g_path.load());
+    const Plan pl =
+        make_plan((int)op, T, H, R, dt, vec, num_sms, max_smem, g_path.load(), mixed ? 2 : 1);
     snprintf(out, cap,
              "%s %s per_thread=%d block=%d grid=%d cluster=%d smem=%d stages=%d chunk=%d "
              "groups=%d gamma_regs=%d pipe=%d",

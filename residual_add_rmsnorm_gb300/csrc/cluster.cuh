@@ -45,8 +45,8 @@ __device__ __forceinline__ float ld_peer(const float *local, uint32_t rank) {
     return v;
 }
 
-template <typename T, int VPT, int OP, bool PG>
-__global__ void __launch_bounds__(VecBound<T, VPT, OP, PG>::value) k_cluster_vec(Problem p) {
+template <typename T, int VPT, int OP, bool PG, typename TR>
+__global__ void __launch_bounds__(VecBound<T, VPT, OP, PG, TR>::value, 1) k_cluster_vec(Problem p) {
     __shared__ float red[2][32];
     __shared__ float part[2];
     const uint32_t rank = cluster_ctarank(), cs = cluster_nctarank();
@@ -61,22 +61,22 @@ __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG>::value) k_cluster_vec
     int par = 0;
     for (int64_t t = first; t < p.T; t += step, par ^= 1) {
         if (t + step >= p.T) grid_launch_dependents();
-        uint4 hv[VPT];
-        const float ss = pass1_vec<T, VPT, OP, Chunk<OP>::value>(p, t, j_begin + threadIdx.x,
-                                                                blockDim.x, j_end, hv);
+        uint4 hv[VPT][Res<T, TR>::N];
+        const float ss =
+            pass1_vec<T, VPT, OP, TR>(p, t, j_begin + threadIdx.x, blockDim.x, j_end, hv);
         const float mine = block_sum(ss, red[par]);
         if (threadIdx.x == 0) part[par] = mine;
         cluster_sync();
         float tot = 0.f;
         for (uint32_t r = 0; r < cs; ++r) tot += ld_peer(&part[par], r);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_vec<T, VPT, PG>(p, t, j_begin + threadIdx.x, blockDim.x, j_end, hv, inv, gv);
+        pass2_vec<T, VPT, TR, PG>(p, t, j_begin + threadIdx.x, blockDim.x, j_end, hv, inv, gv);
     }
     // no CTA leaves while a peer may still read its partials
     cluster_sync();
 }
 
-template <typename T, int OP>
+template <typename T, int OP, typename TR>
 static cudaError_t launch_cluster_op(const Problem &p, const Plan &pl, cudaStream_t st) {
     const dim3 g(pl.grid), b(pl.block);
     auto go = [&](auto kernel) {
@@ -84,29 +84,35 @@ static cudaError_t launch_cluster_op(const Problem &p, const Plan &pl, cudaStrea
     };
     if (pl.prefetch_gamma) {
         switch (pl.per_thread) {
-        case 1: return go(k_cluster_vec<T, 1, OP, true>);
-        case 2: return go(k_cluster_vec<T, 2, OP, true>);
-        case 4: return go(k_cluster_vec<T, 4, OP, true>);
-        case 8: return go(k_cluster_vec<T, 8, OP, true>);
+        case 1: return go(k_cluster_vec<T, 1, OP, true, TR>);
+        case 2: return go(k_cluster_vec<T, 2, OP, true, TR>);
+        case 4: return go(k_cluster_vec<T, 4, OP, true, TR>);
+        case 8: return go(k_cluster_vec<T, 8, OP, true, TR>);
         default: return cudaErrorInvalidValue;
         }
     }
     switch (pl.per_thread) {
-    case 1: return go(k_cluster_vec<T, 1, OP, false>);
-    case 2: return go(k_cluster_vec<T, 2, OP, false>);
-    case 4: return go(k_cluster_vec<T, 4, OP, false>);
-    case 8: return go(k_cluster_vec<T, 8, OP, false>);
+    case 1: return go(k_cluster_vec<T, 1, OP, false, TR>);
+    case 2: return go(k_cluster_vec<T, 2, OP, false, TR>);
+    case 4: return go(k_cluster_vec<T, 4, OP, false, TR>);
+    case 8: return go(k_cluster_vec<T, 8, OP, false, TR>);
     default: return cudaErrorInvalidValue;
     }
 }
 
-template <typename T>
+template <typename T, typename TR>
 cudaError_t launch_cluster(const Problem &p, const Plan &pl, cudaStream_t st) {
     cudaError_t e;
     switch (p.op) {
-    case OP_PLAIN: e = launch_cluster_op<T, OP_PLAIN>(p, pl, st); break;
-    case OP_FUSED: e = launch_cluster_op<T, OP_FUSED>(p, pl, st); break;
-    case OP_REDUCE: e = launch_cluster_op<T, OP_REDUCE>(p, pl, st); break;
+    case OP_PLAIN:
+        if constexpr (!std::is_same<T, TR>::value) {
+            return cudaErrorInvalidValue;
+        } else {
+            e = launch_cluster_op<T, OP_PLAIN, T>(p, pl, st);
+        }
+        break;
+    case OP_FUSED: e = launch_cluster_op<T, OP_FUSED, TR>(p, pl, st); break;
+    case OP_REDUCE: e = launch_cluster_op<T, OP_REDUCE, TR>(p, pl, st); break;
     default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;

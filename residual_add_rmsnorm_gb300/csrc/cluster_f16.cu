@@ -2,5 +2,5 @@
 #include "cluster.cuh"
 
 namespace rarn {
-template cudaError_t launch_cluster<__half>(const Problem &, const Plan &, cudaStream_t);
+template cudaError_t launch_cluster<__half, __half>(const Problem &, const Plan &, cudaStream_t);
 }  // namespace rarn

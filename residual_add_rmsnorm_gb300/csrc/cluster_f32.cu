@@ -2,5 +2,5 @@
 #include "cluster.cuh"
 
 namespace rarn {
-template cudaError_t launch_cluster<float>(const Problem &, const Plan &, cudaStream_t);
+template cudaError_t launch_cluster<float, float>(const Problem &, const Plan &, cudaStream_t);
 }  // namespace rarn

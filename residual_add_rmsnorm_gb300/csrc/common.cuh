@@ -15,14 +15,18 @@ namespace rarn {
 
 enum Op : int { OP_PLAIN = 0, OP_FUSED = 1, OP_REDUCE = 2 };
 
-// One call's arguments, passed to every kernel by value.
+// One call's arguments, passed to every kernel by value.  Strides are in
+// elements of each buffer's own storage type.
 struct Problem {
     void *y;               // [T, H] output
     const void *src;       // plain / fused: x [T, H]; reduce: partials [R, T, H]
     void *residual;        // [T, H] in/out (fused, reduce); unused for plain
     const void *gamma;     // [H]
     int64_t T, H;
-    int64_t slice;         // elements between consecutive partial buffers (T * H)
+    int64_t ldx;           // elements between rows of x / of each partial
+    int64_t ldr;           // elements between rows of the residual
+    int64_t ldy;           // elements between rows of y
+    int64_t slice;         // elements between consecutive partial buffers
     int R;                 // partial buffers (reduce), 1 (fused), 0 (plain)
     int op;                // Op
     float eps;

@@ -35,21 +35,26 @@ struct Plan {
 };
 
 // Register budget of the register-staged row kernels.  A thread holding P
-// 16-byte packs of the row keeps, per pack: the load buffers of `rc` streams
-// loaded together (4 registers each), the binary32 accumulators (EPV), the
-// rounded row (4) and, if gamma is held in registers, gamma (4); about 32
-// more for addresses and loop state.  Single-element kernels hold one value
-// per stream buffer, accumulator and row copy.  The CTA size a kernel is
-// compiled for follows from 64 K registers per SM (and at most 255 per
-// thread); 0 means the combination is not built.
-__host__ __device__ constexpr int rows_loads_together(int op) { return op == 2 ? 4 : op == 1 ? 2 : 1; }
+// 16-byte packs of the row keeps, per pack: the load buffers of the streams
+// loaded together (4 registers each; a binary32 residual with 16-bit inputs
+// takes rn = 2 words per pack), the binary32 accumulators (EPV), the staged
+// row (4 * rn) and, if gamma is held in registers, gamma (4); about 32 more
+// for addresses and loop state.  Single-element kernels hold per element one
+// value per stream buffer, the residual, the accumulator and the row copy,
+// plus its address arithmetic (6 registers measured).  The CTA size a kernel is compiled
+// for follows from 64 K registers per SM (and at most 255 per thread); 0 means
+// the combination is not built.
+__host__ __device__ constexpr int rows_loads_together(int op, int rn) {
+    return op == 2 ? (rn == 1 ? 4 : 4 + rn) : op == 1 ? 1 + rn : 1;
+}
 
-__host__ __device__ constexpr int rows_regs_vec(int P, int epv, int op, bool gamma_regs) {
-    return P * (4 * rows_loads_together(op) + epv + 4 + (gamma_regs ? 4 : 0)) + 32;
+__host__ __device__ constexpr int rows_regs_vec(int P, int epv, int op, bool gamma_regs,
+                                                int rn = 1) {
+    return P * (4 * rows_loads_together(op, rn) + epv + 4 * rn + (gamma_regs ? 4 : 0)) + 32;
 }
 
 __host__ __device__ constexpr int rows_regs_scalar(int NE, int op) {
-    return NE * (rows_loads_together(op) + 2) + 32;
+    return NE * (rows_loads_together(op, 1) + 6) + 32;
 }
 
 __host__ __device__ constexpr int rows_max_block(int regs) {
@@ -102,11 +107,13 @@ __host__ __device__ inline Layout layout(int stages, int ns, int row_bytes, int 
 
 }  // namespace stream
 
-template <typename T>
+// Per-storage-type launchers.  TR is the residual's type: T, or binary32 with
+// a 16-bit T (register and cluster kernels only).
+template <typename T, typename TR>
 cudaError_t launch_rows(const Problem &p, const Plan &plan, cudaStream_t stream);
 template <typename T>
 cudaError_t launch_stream(const Problem &p, const Plan &plan, cudaStream_t stream);
-template <typename T>
+template <typename T, typename TR>
 cudaError_t launch_cluster(const Problem &p, const Plan &plan, cudaStream_t stream);
 
 }  // namespace rarn

@@ -2,116 +2,217 @@
 //
 // Each row is read once from HBM.  The first pass loads the row's input
 // streams (x; or the R partial buffers and the residual), sums them in
-// binary32 in stream order, rounds the sum once to the storage type, writes it
-// back as the residual and keeps it in registers while it accumulates the sum
-// of squares.  After the row reduction the second pass scales the values still
-// held in registers by rsqrt(ss / H + eps) and by gamma and writes y: the
-// normalise pass never goes back to HBM.  ("Tokenweave fused-RMSNorm-AR
-// kernel", Code walkthrough: the same two passes, where the second pass
-// re-reads the residual from global memory; here only the two-pass kernel for
-// rows too long for registers does that.)
+// binary32 in stream order, rounds the sum once to the residual's storage
+// type, writes it back as the residual and keeps it in registers while it
+// accumulates the sum of squares.  After the row reduction the second pass
+// scales the values still held in registers by rsqrt(ss / H + eps) and by
+// gamma and writes y: the normalise pass never goes back to HBM.
+// ("Tokenweave fused-RMSNorm-AR kernel", Code walkthrough: the same two
+// passes, where the second pass re-reads the residual from global memory;
+// here only the two-pass kernel for rows too long for registers does that.)
+//
+// T is the storage type of x / partials, gamma and y; TR that of the residual:
+// either T, or binary32 with a 16-bit T (an fp32 residual stream), in which
+// case the sum is kept in binary32 without rounding and staged as such.
+// Every buffer has its own row stride (Problem::ldx, ldr, ldy).
 //
 // Rows are spread over a grid that is capped at what the GPU holds at once;
 // each CTA (or warp) walks its rows with a grid stride.
 #pragma once
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "plan.h"
 
 namespace rarn {
 
-// Input streams per element: plain 1 (x); fused 2 (x, residual); reduce R + 1
-// (partials, residual).  Stream s < R is partial s (x for fused); the last
-// stream is the residual.
-__device__ __forceinline__ int n_streams(const Problem &p) {
-    return p.op == OP_PLAIN ? 1 : p.R + 1;
-}
+// ---------------------------------------------------------------------------
+// Residual storage for one pack of T (EPV elements): N 16-byte words.
+// ---------------------------------------------------------------------------
+template <typename T, typename TR>
+struct Res {
+    static constexpr int EPV = DT<T>::EPV;
+    static constexpr bool SAME = std::is_same<T, TR>::value;
+    static_assert(SAME || std::is_same<TR, float>::value, "residual: T or binary32");
+    static constexpr int N = SAME ? 1 : (EPV * 4) / 16;  // 16-byte words per pack
+    static constexpr int EPW = 16 / (int)sizeof(TR);     // residual elements per word
 
-template <typename T>
-__device__ __forceinline__ const T *stream_row(const Problem &p, int s, int64_t row_off) {
-    const bool is_res = (p.op != OP_PLAIN) && (s == p.R);
-    const T *base = is_res ? reinterpret_cast<const T *>(p.residual)
-                           : reinterpret_cast<const T *>(p.src) + (int64_t)s * p.slice;
-    return base + row_off;
-}
+    __device__ __forceinline__ static void to_f(const uint4 (&v)[N], float (&f)[EPV]) {
+        if constexpr (SAME) {
+            DT<T>::unpack(v[0], f);
+        } else {
+#pragma unroll
+            for (int q = 0; q < N; ++q) {
+                f[4 * q + 0] = __uint_as_float(v[q].x);
+                f[4 * q + 1] = __uint_as_float(v[q].y);
+                f[4 * q + 2] = __uint_as_float(v[q].z);
+                f[4 * q + 3] = __uint_as_float(v[q].w);
+            }
+        }
+    }
+    // The one rounding of the sum to the residual's storage type (none for
+    // binary32).
+    __device__ __forceinline__ static void from_f(const float (&f)[EPV], uint4 (&v)[N]) {
+        if constexpr (SAME) {
+            v[0] = DT<T>::pack(f);
+        } else {
+#pragma unroll
+            for (int q = 0; q < N; ++q)
+                v[q] = make_uint4(__float_as_uint(f[4 * q + 0]), __float_as_uint(f[4 * q + 1]),
+                                  __float_as_uint(f[4 * q + 2]), __float_as_uint(f[4 * q + 3]));
+        }
+    }
+};
+
+template <int OP>
+struct Chunk {  // streams loaded together in pass 1 (same-type residual)
+    static constexpr int value = OP == OP_REDUCE ? 4 : 2;
+};
 
 // ---------------------------------------------------------------------------
 // Pass 1, 16-byte packs.  Thread owns packs j = j0 + k * js (k < VPT, j < nv).
-// Loads RC streams at a time so that RC * VPT loads are in flight per thread.
-// Returns this thread's share of the sum of squares; hv receives the rounded
-// row values.
+// Returns this thread's share of the sum of squares; hv receives the row
+// values as stored in the residual (or x for the plain form).
 // ---------------------------------------------------------------------------
-template <typename T, int VPT, int OP, int RC>
+template <typename T, int VPT, int OP, typename TR>
 __device__ __forceinline__ float pass1_vec(const Problem &p, int64_t t, int j0, int js, int nv,
-                                           uint4 (&hv)[VPT]) {
+                                           uint4 (&hv)[VPT][Res<T, TR>::N]) {
+    using RS = Res<T, TR>;
     constexpr int EPV = DT<T>::EPV;
-    const int64_t row_off = t * p.H;
+    constexpr int RC = Chunk<OP>::value;
+    const int64_t xo = t * p.ldx;
     float ss = 0.f;
-    if (OP == OP_PLAIN) {
-        const T *x = reinterpret_cast<const T *>(p.src) + row_off;
+    if constexpr (OP == OP_PLAIN) {
+        const T *x = reinterpret_cast<const T *>(p.src) + xo;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int j = j0 + k * js;
-            if (j < nv) hv[k] = ld_stream(x + (int64_t)j * EPV);
+            if (j < nv) hv[k][0] = ld_stream(x + (int64_t)j * EPV);
         }
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int j = j0 + k * js;
             if (j < nv) {
                 float f[EPV];
-                DT<T>::unpack(hv[k], f);
+                DT<T>::unpack(hv[k][0], f);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) ss += f[e] * f[e];
+            }
+        }
+        return ss;
+    } else {
+        TR *res = reinterpret_cast<TR *>(p.residual) + t * p.ldr;
+        float acc[VPT][EPV];
+        if constexpr (RS::SAME) {
+            // streams 0..R-1 are the partials (x for fused), stream R the
+            // residual; RC streams are loaded together
+            const int S = p.R + 1;
+            for (int s0 = 0; s0 < S; s0 += RC) {
+                uint4 buf[RC][VPT];
+#pragma unroll
+                for (int q = 0; q < RC; ++q) {
+                    if (s0 + q < S) {
+                        const T *base =
+                            s0 + q == p.R
+                                ? reinterpret_cast<const T *>(res)
+                                : reinterpret_cast<const T *>(p.src) + (int64_t)(s0 + q) * p.slice +
+                                      xo;
+#pragma unroll
+                        for (int k = 0; k < VPT; ++k) {
+                            const int j = j0 + k * js;
+                            if (j < nv) buf[q][k] = ld_stream(base + (int64_t)j * EPV);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < RC; ++q) {
+                    if (s0 + q < S) {
+#pragma unroll
+                        for (int k = 0; k < VPT; ++k) {
+                            const int j = j0 + k * js;
+                            if (j < nv) {
+                                float f[EPV];
+                                DT<T>::unpack(buf[q][k], f);
+#pragma unroll
+                                for (int e = 0; e < EPV; ++e)
+                                    acc[k][e] = (s0 + q == 0) ? f[e] : acc[k][e] + f[e];
+                            }
+                        }
+                    }
+                }
+            }
+        } else {
+            // binary32 residual: its words are loaded first and added last
+            uint4 rv[VPT][RS::N];
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int j = j0 + k * js;
+                if (j < nv) {
+#pragma unroll
+                    for (int q = 0; q < RS::N; ++q)
+                        rv[k][q] = ld_stream(res + (int64_t)j * EPV + q * RS::EPW);
+                }
+            }
+            constexpr int PC = RC > 2 ? RC : 1;  // partials loaded together
+            for (int s0 = 0; s0 < p.R; s0 += PC) {
+                uint4 buf[PC][VPT];
+#pragma unroll
+                for (int q = 0; q < PC; ++q) {
+                    if (s0 + q < p.R) {
+                        const T *base =
+                            reinterpret_cast<const T *>(p.src) + (int64_t)(s0 + q) * p.slice + xo;
+#pragma unroll
+                        for (int k = 0; k < VPT; ++k) {
+                            const int j = j0 + k * js;
+                            if (j < nv) buf[q][k] = ld_stream(base + (int64_t)j * EPV);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int q = 0; q < PC; ++q) {
+                    if (s0 + q < p.R) {
+#pragma unroll
+                        for (int k = 0; k < VPT; ++k) {
+                            const int j = j0 + k * js;
+                            if (j < nv) {
+                                float f[EPV];
+                                DT<T>::unpack(buf[q][k], f);
+#pragma unroll
+                                for (int e = 0; e < EPV; ++e)
+                                    acc[k][e] = (s0 + q == 0) ? f[e] : acc[k][e] + f[e];
+                            }
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int j = j0 + k * js;
+                if (j < nv) {
+                    float f[EPV];
+                    RS::to_f(rv[k], f);
+#pragma unroll
+                    for (int e = 0; e < EPV; ++e) acc[k][e] = acc[k][e] + f[e];
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = j0 + k * js;
+            if (j < nv) {
+                RS::from_f(acc[k], hv[k]);  // the one rounding to the residual's type
+#pragma unroll
+                for (int q = 0; q < RS::N; ++q)
+                    st_global(res + (int64_t)j * EPV + q * RS::EPW, hv[k][q]);
+                float f[EPV];
+                RS::to_f(hv[k], f);
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) ss += f[e] * f[e];
             }
         }
         return ss;
     }
-    const int S = p.R + 1;
-    float acc[VPT][EPV];
-    for (int s0 = 0; s0 < S; s0 += RC) {
-        uint4 buf[RC][VPT];
-#pragma unroll
-        for (int q = 0; q < RC; ++q) {
-            if (s0 + q < S) {
-                const T *base = stream_row<T>(p, s0 + q, row_off);
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) {
-                    const int j = j0 + k * js;
-                    if (j < nv) buf[q][k] = ld_stream(base + (int64_t)j * EPV);
-                }
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < RC; ++q) {
-            if (s0 + q < S) {
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) {
-                    const int j = j0 + k * js;
-                    if (j < nv) {
-                        float f[EPV];
-                        DT<T>::unpack(buf[q][k], f);
-#pragma unroll
-                        for (int e = 0; e < EPV; ++e)
-                            acc[k][e] = (s0 + q == 0) ? f[e] : acc[k][e] + f[e];
-                    }
-                }
-            }
-        }
-    }
-    T *res = reinterpret_cast<T *>(p.residual) + row_off;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int j = j0 + k * js;
-        if (j < nv) {
-            hv[k] = DT<T>::pack(acc[k]);  // the one rounding to the storage type
-            st_global(res + (int64_t)j * EPV, hv[k]);
-            float f[EPV];
-            DT<T>::unpack(hv[k], f);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) ss += f[e] * f[e];
-        }
-    }
-    return ss;
 }
 
 // This thread's gamma packs.  A thread owns the same packs of every row, so
@@ -132,19 +233,19 @@ __device__ __forceinline__ void load_gamma_vec(const Problem &p, int j0, int js,
 
 // Pass 2, 16-byte packs: y = (h * inv) * gamma, one rounding.  With PG the
 // gamma packs come from registers (gv), otherwise from memory (L1 / L2).
-template <typename T, int VPT, bool PG = false>
+template <typename T, int VPT, typename TR, bool PG = false>
 __device__ __forceinline__ void pass2_vec(const Problem &p, int64_t t, int j0, int js, int nv,
-                                          const uint4 (&hv)[VPT], float inv,
+                                          const uint4 (&hv)[VPT][Res<T, TR>::N], float inv,
                                           const uint4 *gv = nullptr) {
     constexpr int EPV = DT<T>::EPV;
     const T *g = reinterpret_cast<const T *>(p.gamma);
-    T *y = reinterpret_cast<T *>(p.y) + t * p.H;
+    T *y = reinterpret_cast<T *>(p.y) + t * p.ldy;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int j = j0 + k * js;
         if (j < nv) {
             float h[EPV], w[EPV];
-            DT<T>::unpack(hv[k], h);
+            Res<T, TR>::to_f(hv[k], h);
             DT<T>::unpack(PG ? gv[k] : ld_keep(g + (int64_t)j * EPV), w);
 #pragma unroll
             for (int e = 0; e < EPV; ++e) h[e] = (h[e] * inv) * w[e];
@@ -156,16 +257,17 @@ __device__ __forceinline__ void pass2_vec(const Problem &p, int64_t t, int j0, i
 // ---------------------------------------------------------------------------
 // Pass 1 / pass 2, single elements (rows or pointers not 16-byte aligned).
 // Thread owns elements i = i0 + k * is (k < NE, i < H); values held as
-// binary32 (already rounded to the storage type).
+// binary32 (already rounded to the residual's storage type).
 // ---------------------------------------------------------------------------
-template <typename T, int NE, int OP, int RC>
+template <typename T, int NE, int OP, typename TR>
 __device__ __forceinline__ float pass1_scalar(const Problem &p, int64_t t, int i0, int is,
                                               float (&h)[NE]) {
-    const int64_t row_off = t * p.H;
+    constexpr int RC = Chunk<OP>::value;
+    const int64_t xo = t * p.ldx;
     const int H = (int)p.H;
     float ss = 0.f;
-    if (OP == OP_PLAIN) {
-        const T *x = reinterpret_cast<const T *>(p.src) + row_off;
+    if constexpr (OP == OP_PLAIN) {
+        const T *x = reinterpret_cast<const T *>(p.src) + xo;
 #pragma unroll
         for (int k = 0; k < NE; ++k) {
             const int i = i0 + k * is;
@@ -173,48 +275,56 @@ __device__ __forceinline__ float pass1_scalar(const Problem &p, int64_t t, int i
             ss += h[k] * h[k];
         }
         return ss;
-    }
-    const int S = p.R + 1;
-    for (int s0 = 0; s0 < S; s0 += RC) {
-        float buf[RC][NE];
+    } else {
+        TR *res = reinterpret_cast<TR *>(p.residual) + t * p.ldr;
+        float rv[NE];
 #pragma unroll
-        for (int q = 0; q < RC; ++q) {
-            if (s0 + q < S) {
-                const T *base = stream_row<T>(p, s0 + q, row_off);
+        for (int k = 0; k < NE; ++k) {
+            const int i = i0 + k * is;
+            rv[k] = i < H ? DT<TR>::to_f(res[i]) : 0.f;
+        }
+        for (int s0 = 0; s0 < p.R; s0 += RC) {
+            float buf[RC][NE];
 #pragma unroll
-                for (int k = 0; k < NE; ++k) {
-                    const int i = i0 + k * is;
-                    buf[q][k] = i < H ? DT<T>::to_f(base[i]) : 0.f;
+            for (int q = 0; q < RC; ++q) {
+                if (s0 + q < p.R) {
+                    const T *base =
+                        reinterpret_cast<const T *>(p.src) + (int64_t)(s0 + q) * p.slice + xo;
+#pragma unroll
+                    for (int k = 0; k < NE; ++k) {
+                        const int i = i0 + k * is;
+                        buf[q][k] = i < H ? DT<T>::to_f(base[i]) : 0.f;
+                    }
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < RC; ++q) {
+                if (s0 + q < p.R) {
+#pragma unroll
+                    for (int k = 0; k < NE; ++k)
+                        h[k] = (s0 + q == 0) ? buf[q][k] : h[k] + buf[q][k];
                 }
             }
         }
 #pragma unroll
-        for (int q = 0; q < RC; ++q) {
-            if (s0 + q < S) {
-#pragma unroll
-                for (int k = 0; k < NE; ++k) h[k] = (s0 + q == 0) ? buf[q][k] : h[k] + buf[q][k];
+        for (int k = 0; k < NE; ++k) {
+            const int i = i0 + k * is;
+            if (i < H) {
+                const TR r = DT<TR>::from_f(h[k] + rv[k]);  // one rounding to TR
+                res[i] = r;
+                h[k] = DT<TR>::to_f(r);
+                ss += h[k] * h[k];
             }
         }
+        return ss;
     }
-    T *res = reinterpret_cast<T *>(p.residual) + row_off;
-#pragma unroll
-    for (int k = 0; k < NE; ++k) {
-        const int i = i0 + k * is;
-        if (i < H) {
-            const T r = DT<T>::from_f(h[k]);
-            res[i] = r;
-            h[k] = DT<T>::to_f(r);
-            ss += h[k] * h[k];
-        }
-    }
-    return ss;
 }
 
 template <typename T, int NE>
 __device__ __forceinline__ void pass2_scalar(const Problem &p, int64_t t, int i0, int is,
                                              const float (&h)[NE], float inv) {
     const T *g = reinterpret_cast<const T *>(p.gamma);
-    T *y = reinterpret_cast<T *>(p.y) + t * p.H;
+    T *y = reinterpret_cast<T *>(p.y) + t * p.ldy;
     const int H = (int)p.H;
 #pragma unroll
     for (int k = 0; k < NE; ++k) {
@@ -223,16 +333,12 @@ __device__ __forceinline__ void pass2_scalar(const Problem &p, int64_t t, int i0
     }
 }
 
-template <int OP>
-struct Chunk {  // streams loaded together in pass 1
-    static constexpr int value = OP == OP_REDUCE ? 4 : 2;
-};
-
 // CTA size each register-staged kernel is compiled for (plan.h budget); a
 // combination over budget is compiled for 128 threads and never planned.
-template <typename T, int VPT, int OP, bool PG = false>
+template <typename T, int VPT, int OP, bool PG, typename TR>
 struct VecBound {
-    static constexpr int b = rows_max_block(rows_regs_vec(VPT, DT<T>::EPV, OP, PG));
+    static constexpr int b =
+        rows_max_block(rows_regs_vec(VPT, DT<T>::EPV, OP, PG, Res<T, TR>::N));
     static constexpr int value = b > 0 ? b : 128;
 };
 
@@ -247,8 +353,8 @@ struct ScalarBound {
 // ---------------------------------------------------------------------------
 
 // One CTA per row, packs.  PG: gamma held in registers for all rows.
-template <typename T, int VPT, int OP, bool PG>
-__global__ void __launch_bounds__(VecBound<T, VPT, OP, PG>::value) k_cta_vec(Problem p) {
+template <typename T, int VPT, int OP, bool PG, typename TR>
+__global__ void __launch_bounds__(VecBound<T, VPT, OP, PG, TR>::value) k_cta_vec(Problem p) {
     __shared__ float red[2][32];
     const int nv = (int)(p.H / DT<T>::EPV);
     grid_dependency_wait();
@@ -257,68 +363,74 @@ __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG>::value) k_cta_vec(Pro
     int par = 0;
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
         if (t + gridDim.x >= p.T) grid_launch_dependents();
-        uint4 hv[VPT];
-        const float ss = pass1_vec<T, VPT, OP, Chunk<OP>::value>(p, t, threadIdx.x, blockDim.x,
-                                                                nv, hv);
+        uint4 hv[VPT][Res<T, TR>::N];
+        const float ss = pass1_vec<T, VPT, OP, TR>(p, t, threadIdx.x, blockDim.x, nv, hv);
         const float tot = block_sum(ss, red[par]);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_vec<T, VPT, PG>(p, t, threadIdx.x, blockDim.x, nv, hv, inv, gv);
+        pass2_vec<T, VPT, TR, PG>(p, t, threadIdx.x, blockDim.x, nv, hv, inv, gv);
     }
 }
 
 // One CTA per row, packs, software-pipelined across rows (plain and fused
-// forms: one or two input streams).  Before a CTA reduces and writes row t it
-// issues the loads of its next row into a second register buffer, so the
-// SM keeps reads in flight through the row reduction and the y stores instead
-// of draining between rows.
-template <typename T, int VPT, int OP>
+// forms: one input stream plus the residual).  Before a CTA reduces and
+// writes row t it issues the loads of its next row into a second register
+// buffer, so the SM keeps reads in flight through the row reduction and the
+// y stores instead of draining between rows.
+template <typename T, int VPT, int OP, typename TR>
 struct RowLoads {
-    static constexpr int S = OP == OP_PLAIN ? 1 : 2;  // x (, residual)
-    uint4 v[S][VPT];
+    static constexpr int RN = OP == OP_PLAIN ? 0 : Res<T, TR>::N;  // residual words per pack
+    uint4 x[VPT];
+    uint4 r[VPT][RN > 0 ? RN : 1];
 };
 
-template <typename T, int VPT, int OP>
+template <typename T, int VPT, int OP, typename TR>
 __device__ __forceinline__ void issue_row_loads(const Problem &p, int64_t t, int j0, int js,
-                                                int nv, RowLoads<T, VPT, OP> &b) {
+                                                int nv, RowLoads<T, VPT, OP, TR> &b) {
     constexpr int EPV = DT<T>::EPV;
-    const int64_t row_off = t * p.H;
+    constexpr int RN = RowLoads<T, VPT, OP, TR>::RN;
+    const T *x = reinterpret_cast<const T *>(p.src) + t * p.ldx;
+    const TR *res = reinterpret_cast<const TR *>(p.residual) + t * p.ldr;
 #pragma unroll
-    for (int s = 0; s < RowLoads<T, VPT, OP>::S; ++s) {
-        const T *base = s == 0 ? reinterpret_cast<const T *>(p.src) + row_off
-                               : reinterpret_cast<const T *>(p.residual) + row_off;
+    for (int k = 0; k < VPT; ++k) {
+        const int j = j0 + k * js;
+        if (j < nv) {
+            b.x[k] = ld_stream(x + (int64_t)j * EPV);
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int j = j0 + k * js;
-            if (j < nv) b.v[s][k] = ld_stream(base + (int64_t)j * EPV);
+            for (int q = 0; q < RN; ++q)
+                b.r[k][q] = ld_stream(res + (int64_t)j * EPV + q * Res<T, TR>::EPW);
         }
     }
 }
 
-// h from the loaded packs (fused: x + residual in binary32, one rounding,
-// residual written back); returns this thread's share of the sum of squares.
-template <typename T, int VPT, int OP>
+// h from the loaded packs (fused: x + residual in binary32, one rounding to
+// the residual's type, residual written back); returns this thread's share of
+// the sum of squares.
+template <typename T, int VPT, int OP, typename TR>
 __device__ __forceinline__ float consume_row_loads(const Problem &p, int64_t t, int j0, int js,
-                                                   int nv, const RowLoads<T, VPT, OP> &b,
-                                                   uint4 (&hv)[VPT]) {
+                                                   int nv, const RowLoads<T, VPT, OP, TR> &b,
+                                                   uint4 (&hv)[VPT][Res<T, TR>::N]) {
+    using RS = Res<T, TR>;
     constexpr int EPV = DT<T>::EPV;
-    T *res = reinterpret_cast<T *>(p.residual) + t * p.H;
+    TR *res = reinterpret_cast<TR *>(p.residual) + t * p.ldr;
     float ss = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int j = j0 + k * js;
         if (j < nv) {
             float h[EPV];
-            DT<T>::unpack(b.v[0][k], h);
-            if (OP == OP_FUSED) {
+            DT<T>::unpack(b.x[k], h);
+            if constexpr (OP == OP_FUSED) {
                 float r[EPV];
-                DT<T>::unpack(b.v[1][k], r);
+                RS::to_f(b.r[k], r);
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) h[e] = h[e] + r[e];
-                hv[k] = DT<T>::pack(h);  // the one rounding to the storage type
-                st_global(res + (int64_t)j * EPV, hv[k]);
-                DT<T>::unpack(hv[k], h);
+                RS::from_f(h, hv[k]);  // the one rounding to the residual's type
+#pragma unroll
+                for (int q = 0; q < RS::N; ++q)
+                    st_global(res + (int64_t)j * EPV + q * RS::EPW, hv[k][q]);
+                RS::to_f(hv[k], h);
             } else {
-                hv[k] = b.v[0][k];
+                hv[k][0] = b.x[k];
             }
 #pragma unroll
             for (int e = 0; e < EPV; ++e) ss += h[e] * h[e];
@@ -327,40 +439,42 @@ __device__ __forceinline__ float consume_row_loads(const Problem &p, int64_t t, 
     return ss;
 }
 
-template <typename T, int VPT, int OP>
+template <typename T, int VPT, int OP, typename TR>
 struct PipeBound {
-    static constexpr int b = rows_max_block(rows_regs_vec(VPT, DT<T>::EPV, OP, false) +
-                                            VPT * 4 * RowLoads<T, VPT, OP>::S);
+    static constexpr int streams = 1 + RowLoads<T, VPT, OP, TR>::RN;
+    static constexpr int b = rows_max_block(
+        rows_regs_vec(VPT, DT<T>::EPV, OP, false, Res<T, TR>::N) + VPT * 4 * streams);
     static constexpr int value = b > 0 ? b : 128;
 };
 
-template <typename T, int VPT, int OP>
-__global__ void __launch_bounds__(PipeBound<T, VPT, OP>::value) k_cta_pipe(Problem p) {
+template <typename T, int VPT, int OP, typename TR>
+__global__ void __launch_bounds__(PipeBound<T, VPT, OP, TR>::value) k_cta_pipe(Problem p) {
     __shared__ float red[2][32];
     const int nv = (int)(p.H / DT<T>::EPV);
     grid_dependency_wait();
-    RowLoads<T, VPT, OP> next;
+    RowLoads<T, VPT, OP, TR> next;
     int64_t t = blockIdx.x;
-    if (t < p.T) issue_row_loads<T, VPT, OP>(p, t, threadIdx.x, blockDim.x, nv, next);
+    if (t < p.T) issue_row_loads<T, VPT, OP, TR>(p, t, threadIdx.x, blockDim.x, nv, next);
     int par = 0;
     for (; t < p.T; t += gridDim.x, par ^= 1) {
-        const RowLoads<T, VPT, OP> cur = next;
+        const RowLoads<T, VPT, OP, TR> cur = next;
         if (t + gridDim.x < p.T) {
-            issue_row_loads<T, VPT, OP>(p, t + gridDim.x, threadIdx.x, blockDim.x, nv, next);
+            issue_row_loads<T, VPT, OP, TR>(p, t + gridDim.x, threadIdx.x, blockDim.x, nv, next);
         } else {
             grid_launch_dependents();
         }
-        uint4 hv[VPT];
-        const float ss = consume_row_loads<T, VPT, OP>(p, t, threadIdx.x, blockDim.x, nv, cur, hv);
+        uint4 hv[VPT][Res<T, TR>::N];
+        const float ss =
+            consume_row_loads<T, VPT, OP, TR>(p, t, threadIdx.x, blockDim.x, nv, cur, hv);
         const float tot = block_sum(ss, red[par]);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_vec<T, VPT, false>(p, t, threadIdx.x, blockDim.x, nv, hv, inv);
+        pass2_vec<T, VPT, TR, false>(p, t, threadIdx.x, blockDim.x, nv, hv, inv);
     }
 }
 
 // One warp per row, packs; blockDim.x / 32 rows per CTA at a time.  Gamma is
 // held in registers (at most 4 packs per lane).
-template <typename T, int VPT, int OP>
+template <typename T, int VPT, int OP, typename TR>
 __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
     const int nv = (int)(p.H / DT<T>::EPV);
     const int lane = threadIdx.x & 31;
@@ -372,25 +486,24 @@ __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
     load_gamma_vec<T, VPT>(p, lane, 32, nv, gv);
     for (int64_t t = first; t < p.T; t += step) {
         if (t + step >= p.T) grid_launch_dependents();
-        uint4 hv[VPT];
-        const float ss = pass1_vec<T, VPT, OP, Chunk<OP>::value>(p, t, lane, 32, nv, hv);
+        uint4 hv[VPT][Res<T, TR>::N];
+        const float ss = pass1_vec<T, VPT, OP, TR>(p, t, lane, 32, nv, hv);
         const float tot = warp_sum(ss);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_vec<T, VPT, true>(p, t, lane, 32, nv, hv, inv, gv);
+        pass2_vec<T, VPT, TR, true>(p, t, lane, 32, nv, hv, inv, gv);
     }
 }
 
 // One CTA per row, single elements.
-template <typename T, int NE, int OP>
-__global__ void __launch_bounds__(ScalarBound<NE, OP>::value) k_cta_scalar(Problem p) {
+template <typename T, int NE, int OP, typename TR>
+__global__ void __launch_bounds__(ScalarBound<NE, OP>::value, 1) k_cta_scalar(Problem p) {
     __shared__ float red[2][32];
     grid_dependency_wait();
     int par = 0;
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
         if (t + gridDim.x >= p.T) grid_launch_dependents();
         float h[NE];
-        const float ss =
-            pass1_scalar<T, NE, OP, Chunk<OP>::value>(p, t, threadIdx.x, blockDim.x, h);
+        const float ss = pass1_scalar<T, NE, OP, TR>(p, t, threadIdx.x, blockDim.x, h);
         const float tot = block_sum(ss, red[par]);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
         pass2_scalar<T, NE>(p, t, threadIdx.x, blockDim.x, h, inv);
@@ -400,8 +513,9 @@ __global__ void __launch_bounds__(ScalarBound<NE, OP>::value) k_cta_scalar(Probl
 // Rows too long for registers: pass 1 walks the row in tiles of blockDim
 // packs (or elements); pass 2 re-reads the stored row (the residual, or x for
 // the plain form) -- each thread re-reads only what it wrote itself.
-template <typename T, int OP, bool VEC>
+template <typename T, int OP, bool VEC, typename TR>
 __global__ void __launch_bounds__(1024) k_two_pass(Problem p) {
+    using RS = Res<T, TR>;
     __shared__ float red[2][32];
     constexpr int EPV = VEC ? DT<T>::EPV : 1;
     const int n = (int)(p.H / EPV);
@@ -411,28 +525,34 @@ __global__ void __launch_bounds__(1024) k_two_pass(Problem p) {
         if (t + gridDim.x >= p.T) grid_launch_dependents();
         float ss = 0.f;
         for (int base = 0; base < n; base += blockDim.x) {
-            if (VEC) {
-                uint4 hv[1];
-                ss += pass1_vec<T, 1, OP, Chunk<OP>::value>(p, t, base + threadIdx.x, 1 << 30,
-                                                           n, hv);
+            if constexpr (VEC) {
+                uint4 hv[1][RS::N];
+                ss += pass1_vec<T, 1, OP, TR>(p, t, base + threadIdx.x, 1 << 30, n, hv);
             } else {
                 float h[1];
-                ss += pass1_scalar<T, 1, OP, Chunk<OP>::value>(p, t, base + threadIdx.x,
-                                                              1 << 30, h);
+                ss += pass1_scalar<T, 1, OP, TR>(p, t, base + threadIdx.x, 1 << 30, h);
             }
         }
         const float tot = block_sum(ss, red[par]);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        const void *stored = OP == OP_PLAIN ? p.src : p.residual;
         for (int base = 0; base < n; base += blockDim.x) {
             const int j = base + threadIdx.x;
             if (j >= n) break;
-            if (VEC) {
-                uint4 hv[1] = {ld_stream(reinterpret_cast<const T *>(stored) + t * p.H +
-                                         (int64_t)j * EPV)};
-                pass2_vec<T, 1>(p, t, j, 1 << 30, n, hv, inv);
+            if constexpr (VEC) {
+                uint4 hv[1][RS::N];
+                if constexpr (OP == OP_PLAIN) {
+                    hv[0][0] = ld_stream(reinterpret_cast<const T *>(p.src) + t * p.ldx +
+                                         (int64_t)j * EPV);
+                } else {
+                    const TR *res = reinterpret_cast<const TR *>(p.residual) + t * p.ldr;
+#pragma unroll
+                    for (int q = 0; q < RS::N; ++q)
+                        hv[0][q] = ld_stream(res + (int64_t)j * EPV + q * RS::EPW);
+                }
+                pass2_vec<T, 1, TR>(p, t, j, 1 << 30, n, hv, inv);
             } else {
-                float h[1] = {ld_elem<T>(stored, t * p.H + j)};
+                float h[1] = {OP == OP_PLAIN ? ld_elem<T>(p.src, t * p.ldx + j)
+                                             : ld_elem<TR>(p.residual, t * p.ldr + j)};
                 pass2_scalar<T, 1>(p, t, j, 1 << 30, h, inv);
             }
         }
@@ -443,68 +563,78 @@ __global__ void __launch_bounds__(1024) k_two_pass(Problem p) {
 // Launcher: plan -> template instance
 // ---------------------------------------------------------------------------
 
-template <typename T, int OP>
+template <typename T, int OP, typename TR>
 static cudaError_t launch_rows_op(const Problem &p, const Plan &pl, cudaStream_t st) {
     const dim3 g(pl.grid), b(pl.block);
     auto go = [&](auto kernel) { return launch_kernel(kernel, g, b, 0, st, pl.pdl, 1, p); };
     switch (pl.kind) {
     case KIND_WARP:
         switch (pl.per_thread) {
-        case 1: return go(k_warp_vec<T, 1, OP>);
-        case 2: return go(k_warp_vec<T, 2, OP>);
-        case 4: return go(k_warp_vec<T, 4, OP>);
+        case 1: return go(k_warp_vec<T, 1, OP, TR>);
+        case 2: return go(k_warp_vec<T, 2, OP, TR>);
+        case 4: return go(k_warp_vec<T, 4, OP, TR>);
         default: return cudaErrorInvalidValue;
         }
     case KIND_CTA:
-        if (pl.vec && pl.pipe && OP != OP_REDUCE) {
-            switch (pl.per_thread) {
-            case 1: return go(k_cta_pipe<T, 1, OP == OP_REDUCE ? OP_FUSED : OP>);
-            case 2: return go(k_cta_pipe<T, 2, OP == OP_REDUCE ? OP_FUSED : OP>);
-            case 4: return go(k_cta_pipe<T, 4, OP == OP_REDUCE ? OP_FUSED : OP>);
-            case 8: return go(k_cta_pipe<T, 8, OP == OP_REDUCE ? OP_FUSED : OP>);
-            default: return cudaErrorInvalidValue;
+        if constexpr (OP != OP_REDUCE) {
+            if (pl.vec && pl.pipe) {
+                switch (pl.per_thread) {
+                case 1: return go(k_cta_pipe<T, 1, OP, TR>);
+                case 2: return go(k_cta_pipe<T, 2, OP, TR>);
+                case 4: return go(k_cta_pipe<T, 4, OP, TR>);
+                case 8: return go(k_cta_pipe<T, 8, OP, TR>);
+                default: return cudaErrorInvalidValue;
+                }
             }
         }
         if (pl.vec && pl.prefetch_gamma) {
             switch (pl.per_thread) {
-            case 1: return go(k_cta_vec<T, 1, OP, true>);
-            case 2: return go(k_cta_vec<T, 2, OP, true>);
-            case 4: return go(k_cta_vec<T, 4, OP, true>);
-            case 8: return go(k_cta_vec<T, 8, OP, true>);
+            case 1: return go(k_cta_vec<T, 1, OP, true, TR>);
+            case 2: return go(k_cta_vec<T, 2, OP, true, TR>);
+            case 4: return go(k_cta_vec<T, 4, OP, true, TR>);
+            case 8: return go(k_cta_vec<T, 8, OP, true, TR>);
             default: return cudaErrorInvalidValue;
             }
         }
         if (pl.vec) {
             switch (pl.per_thread) {
-            case 1: return go(k_cta_vec<T, 1, OP, false>);
-            case 2: return go(k_cta_vec<T, 2, OP, false>);
-            case 4: return go(k_cta_vec<T, 4, OP, false>);
-            case 8: return go(k_cta_vec<T, 8, OP, false>);
+            case 1: return go(k_cta_vec<T, 1, OP, false, TR>);
+            case 2: return go(k_cta_vec<T, 2, OP, false, TR>);
+            case 4: return go(k_cta_vec<T, 4, OP, false, TR>);
+            case 8: return go(k_cta_vec<T, 8, OP, false, TR>);
             default: return cudaErrorInvalidValue;
             }
         }
         switch (pl.per_thread) {
-        case 1: return go(k_cta_scalar<T, 1, OP>);
-        case 2: return go(k_cta_scalar<T, 2, OP>);
-        case 4: return go(k_cta_scalar<T, 4, OP>);
-        case 8: return go(k_cta_scalar<T, 8, OP>);
-        case 16: return go(k_cta_scalar<T, 16, OP>);
+        case 1: return go(k_cta_scalar<T, 1, OP, TR>);
+        case 2: return go(k_cta_scalar<T, 2, OP, TR>);
+        case 4: return go(k_cta_scalar<T, 4, OP, TR>);
+        case 8: return go(k_cta_scalar<T, 8, OP, TR>);
+        case 16: return go(k_cta_scalar<T, 16, OP, TR>);
         default: return cudaErrorInvalidValue;
         }
     case KIND_TWO_PASS:
-        return pl.vec ? go(k_two_pass<T, OP, true>) : go(k_two_pass<T, OP, false>);
+        return pl.vec ? go(k_two_pass<T, OP, true, TR>) : go(k_two_pass<T, OP, false, TR>);
     default:
         return cudaErrorInvalidValue;
     }
 }
 
-template <typename T>
+// TR = T: every form.  TR = float with a 16-bit T: the fused and reduce forms
+// (the plain form has no residual).
+template <typename T, typename TR>
 cudaError_t launch_rows(const Problem &p, const Plan &pl, cudaStream_t st) {
     cudaError_t e;
     switch (p.op) {
-    case OP_PLAIN: e = launch_rows_op<T, OP_PLAIN>(p, pl, st); break;
-    case OP_FUSED: e = launch_rows_op<T, OP_FUSED>(p, pl, st); break;
-    case OP_REDUCE: e = launch_rows_op<T, OP_REDUCE>(p, pl, st); break;
+    case OP_PLAIN:
+        if constexpr (!std::is_same<T, TR>::value) {
+            return cudaErrorInvalidValue;
+        } else {
+            e = launch_rows_op<T, OP_PLAIN, T>(p, pl, st);
+        }
+        break;
+    case OP_FUSED: e = launch_rows_op<T, OP_FUSED, TR>(p, pl, st); break;
+    case OP_REDUCE: e = launch_rows_op<T, OP_REDUCE, TR>(p, pl, st); break;
     default: return cudaErrorInvalidValue;
     }
     return e != cudaSuccess ? e : cudaGetLastError();

@@ -2,5 +2,5 @@
 #include "rows.cuh"
 
 namespace rarn {
-template cudaError_t launch_rows<__half>(const Problem &, const Plan &, cudaStream_t);
+template cudaError_t launch_rows<__half, __half>(const Problem &, const Plan &, cudaStream_t);
 }  // namespace rarn

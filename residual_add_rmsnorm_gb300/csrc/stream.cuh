@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
         bool ok = true;
         int g = 0;
         for (int64_t t = blockIdx.x; t < p.T && ok; t += gridDim.x) {
-            const int64_t row_elem = t * p.H;
+            const int64_t xrow = t * p.ldx, rrow = t * p.ldr;
             long long &n = g == 0 ? issued0 : issued1;
             for (int c = 0; c < nchunks && ok; ++c, ++n) {
                 const int packs = min(CP, nv - c * CP);
@@ -199,13 +199,14 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
                 mbar_arrive_expect_tx(fb, bytes * (uint32_t)ns + extra);
                 const uint32_t dst =
                     smem_addr(smem + (size_t)g * L.ring_stride + (size_t)st * ns * CB);
-                const int64_t off = row_elem + (int64_t)c * CP * EPV;
+                const int64_t off = (int64_t)c * CP * EPV;
                 for (int s = 0; s < ns; ++s) {
                     const T *src;
                     if (OP != OP_PLAIN && s == ns - 1)
-                        src = reinterpret_cast<const T *>(p.residual) + off;
+                        src = reinterpret_cast<const T *>(p.residual) + rrow + off;
                     else
-                        src = reinterpret_cast<const T *>(p.src) + (int64_t)s * p.slice + off;
+                        src = reinterpret_cast<const T *>(p.src) + (int64_t)s * p.slice + xrow +
+                              off;
                     bulk_g2s(dst + (uint32_t)(s * CB), src, bytes, fb);
                 }
             }
@@ -242,7 +243,6 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
     int par = 0;
     for (int64_t t = blockIdx.x + (int64_t)g * gridDim.x; t < p.T;
          t += (int64_t)G * gridDim.x, par ^= 1) {
-        const int64_t row_elem = t * p.H;
         float ss = 0.f;
         if (t + (int64_t)G * gridDim.x >= p.T) grid_launch_dependents();
         for (int c = 0; c < nchunks; ++c) {
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
                         for (int e = 0; e < EPV; ++e) acc[e] = acc[e] + f2[e];
                     }
                     hv = DT<T>::pack(acc);  // the one rounding to the storage type
-                    st_global(residual + row_elem + (int64_t)pk * EPV, hv);
+                    st_global(residual + t * p.ldr + (int64_t)pk * EPV, hv);
                 }
                 row_copy[pk] = hv;
                 float h[EPV];
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
         for (int w = 0; w < kConsumerWarps; ++w) tot += red[par * kConsumerWarps + w];
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
         if (*abort_flag) continue;
-        T *y = reinterpret_cast<T *>(p.y) + row_elem;
+        T *y = reinterpret_cast<T *>(p.y) + t * p.ldy;
         for (int pk = j; pk < nv; pk += kConsumers) {
             float h[EPV], w[EPV];
             DT<T>::unpack(row_copy[pk], h);

@@ -24,6 +24,8 @@ Recipe (seed s):
   channels, the first ones of a permutation drawn from
   SeedSequence([s, OUTLIER_KEY]), are multiplied by 100 in x and residual.
 * Reduce partials are N(0, partial_std^2); x and residual are N(0, 1).
+* A binary32 residual (``rdtype="f32"``) keeps the binary32 draws of its
+  stream without rounding to the inputs' type.
 
 Arrays hold raw storage bits: ``np.float32`` for f32, ``np.uint16`` for f16 and
 bf16.
@@ -57,7 +59,17 @@ class Workload:
     seed: int = 0
     partial_std: float = 1.0
     scaled: bool = False
+    rdtype: str = ""   # residual storage type ("": the inputs' type)
+    ld: int = 0        # row stride of x / partials, residual and y (0: H)
     note: str = field(default="", compare=False)
+
+    @property
+    def res_dtype(self) -> str:
+        return self.rdtype or self.dtype
+
+    @property
+    def row_stride(self) -> int:
+        return self.ld or self.H
 
     @property
     def n_inputs(self) -> int:
@@ -71,9 +83,14 @@ class Workload:
 
     def algorithmic_bytes(self) -> int:
         """Bytes the operation must move at minimum: every input element read
-        once, every output element written once, gamma read once."""
+        once, every output element written once, gamma read once (the
+        residual counted in its own storage type)."""
         s = ELEM_SIZE[self.dtype]
-        return s * self.T * self.H * (self.n_inputs + self.n_outputs) + s * self.H
+        if self.op == "rms_norm":
+            return s * self.T * self.H * 2 + s * self.H
+        rs = ELEM_SIZE[self.res_dtype]
+        n_x = self.n_inputs - 1  # partials (or x)
+        return self.T * self.H * (s * (n_x + 1) + rs * 2) + s * self.H
 
 
 # The five benchmark configurations of the method (the token sweep is five
@@ -95,16 +112,28 @@ CONFIGS = [
     Workload("fused_scaled_bf16_T64_H16384", "fused_add_rms_norm", "bf16", 64, 16384, 1e-6, R=1,
              scaled=True),
 ]
-BY_NAME = {w.name: w for w in CONFIGS}
+# The widened rows: a row-strided plain norm (the first H = 512 of 576
+# columns, as a latent slice inside a wider projection output) and a fused
+# norm with a binary32 residual stream and bf16 inputs / output.
+EXTENDED = [
+    Workload("plain_strided_bf16_T32768_H512_ld576", "rms_norm", "bf16", 32768, 512, 1e-6,
+             ld=576),
+    Workload("fused_r32_bf16_T32768_H5120", "fused_add_rms_norm", "bf16", 32768, 5120, 1e-6,
+             R=1, rdtype="f32"),
+]
+BY_NAME = {w.name: w for w in CONFIGS + EXTENDED}
 
 
 def workload(op: str, dtype: str, T: int, H: int, *, R: int | None = None, eps: float = 1e-6,
-             seed: int = 0, scaled: bool = False, partial_std: float = 1.0) -> Workload:
+             seed: int = 0, scaled: bool = False, partial_std: float = 1.0, rdtype: str = "",
+             ld: int = 0) -> Workload:
     """An ad-hoc problem (edge-shape grids in the tests)."""
     if R is None:
         R = {"rms_norm": 0, "fused_add_rms_norm": 1}.get(op, 2)
-    return Workload(f"{op}_{dtype}_T{T}_H{H}_R{R}", op, dtype, T, H, eps, R=R, seed=seed,
-                    partial_std=partial_std, scaled=scaled)
+    name = f"{op}_{dtype}_T{T}_H{H}_R{R}" + (f"_r{rdtype}" if rdtype else "") + \
+        (f"_ld{ld}" if ld else "")
+    return Workload(name, op, dtype, T, H, eps, R=R, seed=seed, partial_std=partial_std,
+                    scaled=scaled, rdtype=rdtype, ld=ld)
 
 
 CHUNK_ROWS = 256
@@ -204,6 +233,24 @@ def generate(w: Workload, rows: tuple[int, int] | None = None) -> dict:
     else:
         for k, name in enumerate(names):
             out[name] = out_arr[k]
+    if w.op != "rms_norm" and w.res_dtype != w.dtype:
+        # the residual keeps its binary32 draws (stream R of the same blocks)
+        k_res = w.R if w.op == "reduce_add_rms_norm" else 1
+        res32 = np.empty((n, H), np.float32)
+
+        def rblock(c):
+            r0, r1 = c * CHUNK_ROWS, min((c + 1) * CHUNK_ROWS, T)
+            z = _normal_f32(_rng(w.seed, k_res, c), (r1 - r0) * H).reshape(r1 - r0, H)
+            lo, hi = max(r0, a), min(r1, b)
+            z = z[lo - r0:hi - r0]
+            if row_scale is not None:
+                z = z * row_scale[lo:hi, None] * col_scale[None, :]
+            res32[lo - a:hi - a] = z
+
+        if n > 0:
+            with _pool() as ex:
+                list(ex.map(rblock, range(a // CHUNK_ROWS, (b + CHUNK_ROWS - 1) // CHUNK_ROWS)))
+        out["residual"] = to_storage(res32, w.res_dtype)
     g = _rng(w.seed, GAMMA_KEY).uniform(0.5, 1.5, size=H).astype(np.float32)
     out["gamma"] = to_storage(g, w.dtype)
     return out

@@ -199,3 +199,51 @@ def test_pdl_setting_and_stall_hook_arguments(lib):
     assert lib.rarn_test_stall(-1, 1000) == INVALID
     assert lib.rarn_test_stall(0, 0) == INVALID
     assert lib.rarn_test_stall(0, 3_000_000_000) == INVALID
+
+
+def _rows(ptr, ld, dt):
+    return rarn.Rows(ptr, ld, dt)
+
+
+def test_general_forms_argument_errors(lib):
+    """General forms: storage-type combinations, strides and aliasing are
+    checked before any CUDA call."""
+    H, T = 64, 4
+    # residual f16 with bf16 inputs: not a supported combination
+    st = lib.rarn_fused_add_rms_norm_ex(_rows(A, H, BF16), _rows(B, H, BF16), _rows(C, H, F16), D,
+                                        T, H, 1e-6, None)
+    assert st == UNSUPPORTED
+    # fp32 inputs with a 16-bit residual: not supported either
+    st = lib.rarn_fused_add_rms_norm_ex(_rows(A, H, F32), _rows(B, H, F32), _rows(C, H, BF16), D,
+                                        T, H, 1e-6, None)
+    assert st == UNSUPPORTED
+    # y of another type than x
+    assert lib.rarn_rms_norm_ex(_rows(A, H, F16), _rows(B, H, BF16), D, T, H, 1e-6,
+                                None) == UNSUPPORTED
+    # row stride below H
+    assert lib.rarn_rms_norm_ex(_rows(A, H, BF16), _rows(B, H - 1, BF16), D, T, H, 1e-6,
+                                None) == INVALID
+    # y interleaved with x inside one allocation: spans overlap -> refused
+    assert lib.rarn_rms_norm_ex(_rows(A + 2 * H, 2 * H, BF16), _rows(A, 2 * H, BF16), D, T, H,
+                                1e-6, None) == ALIAS
+    # in place with the same stride is allowed (fails later only for lack of a GPU)
+    st = lib.rarn_rms_norm_ex(_rows(A, 2 * H, BF16), _rows(A, 2 * H, BF16), D, T, H, 1e-6, None)
+    assert st not in (INVALID, ALIAS, UNSUPPORTED)
+    # residual inside the span of partial 1 (partials 10 000 elements apart)
+    st = lib.rarn_reduce_add_rms_norm_ex(_rows(A, H, BF16), _rows(B, H, BF16), 10000, 2,
+                                         _rows(B + 2 * 10000 + 8, H, F32), D, T, H, 1e-6, None)
+    assert st == ALIAS
+    # T = 0 is a no-op whatever the pointers
+    assert lib.rarn_rms_norm_ex(_rows(None, H, BF16), _rows(None, H, BF16), None, 0, H, 1e-6,
+                                None) == OK
+
+
+def test_plan_fp32_residual():
+    p = rarn.plan("fused_add_rms_norm", 32768, 5120, 1, "bf16", num_sms=152, rdtype="f32")
+    assert p.startswith("rows.cta") and "pipe=1" in p, p
+    # the stream kernel is for one storage type only: a long fp32-residual row
+    # with many rows goes to the two-pass / cluster kernels
+    p = rarn.plan("fused_add_rms_norm", 4096, 40000, 1, "bf16", num_sms=152, rdtype="f32")
+    assert not p.startswith("stream"), p
+    assert rarn.plan("fused_add_rms_norm", 8, 4096, 1, "f32", num_sms=152, rdtype="bf16") \
+        .startswith("none")
