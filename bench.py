@@ -202,22 +202,51 @@ def ncu_traffic(workload: str, plan_text: str):
 
 
 def make_call(w, tensors, rarn):
-    dt_eps = w.eps
+    """The public call for workload w on device tensors: the dense entry
+    points, or the general ones for row-strided layouts / a binary32
+    residual."""
+    eps = w.eps
+    general = w.row_stride != w.H or w.res_dtype != w.dtype
     if w.op == "rms_norm":
         x, g, y = tensors["x"], tensors["gamma"], tensors["y"]
-        return lambda: rarn.rms_norm(x, g, dt_eps, out=y)
+        if general:
+            return lambda: rarn.rms_norm_ex(x, g, eps, out=y)
+        return lambda: rarn.rms_norm(x, g, eps, out=y)
     if w.op == "fused_add_rms_norm":
         x, r, g, y = tensors["x"], tensors["residual"], tensors["gamma"], tensors["y"]
-        return lambda: rarn.fused_add_rms_norm(x, r, g, dt_eps, out=y)
+        if general:
+            return lambda: rarn.fused_add_rms_norm_ex(x, r, g, eps, out=y)
+        return lambda: rarn.fused_add_rms_norm(x, r, g, eps, out=y)
     p, r, g, y = tensors["partials"], tensors["residual"], tensors["gamma"], tensors["y"]
-    return lambda: rarn.reduce_add_rms_norm(p, r, g, dt_eps, out=y)
+    if general:
+        return lambda: rarn.reduce_add_rms_norm_ex(p, r, g, eps, out=y)
+    return lambda: rarn.reduce_add_rms_norm(p, r, g, eps, out=y)
 
 
 def device_tensors(w, data, device):
+    """Inputs and an output buffer on the device; with a row stride, each
+    [T, H] operand is a view into a [T, row_stride] allocation."""
     import torch
-    t = {k: to_device(v, w.dtype, device) for k, v in data.items()}
+    ld = w.row_stride
+    t = {}
+    for k, v in data.items():
+        dt = w.res_dtype if k == "residual" else w.dtype
+        dense = to_device(v, dt, device)
+        if ld != w.H and k != "gamma":
+            shape = dense.shape[:-1] + (ld,)
+            full = torch.empty(shape, dtype=dense.dtype, device=device)
+            view = full[..., :w.H]
+            view.copy_(dense)
+            t[k] = view
+        else:
+            t[k] = dense
     ref = t.get("x", t.get("residual"))
-    t["y"] = torch.empty_like(ref)
+    if ld != w.H:
+        t["y"] = torch.empty((w.T, ld), dtype=to_device(data["gamma"], w.dtype, device).dtype,
+                             device=device)[:, :w.H]
+    else:
+        t["y"] = torch.empty(ref.shape, dtype=to_device(data["gamma"], w.dtype, device).dtype,
+                             device=device)
     return t
 
 
@@ -456,17 +485,18 @@ def main():
         del tensors, call
         torch.cuda.empty_cache()
         rarn.set_path("auto")
-        for cw in W.CONFIGS:
+        for cw in W.CONFIGS + W.EXTENDED:
             cd = W.generate(cw)
             us, copies, n = time_graph(cw, cd, device, l2)
             cb = cw.algorithmic_bytes()
             cR = cw.R if cw.op == "reduce_add_rms_norm" else 1
             gbs = cb / (us / 1e6) / 1e9
             per_config[cw.name] = {
+                "kind": "widened" if cw in W.EXTENDED else "config",
                 "us_per_launch": us, "gbs": gbs, "rows_per_s": cw.T / (us / 1e6),
                 "frac_of_peak": gbs / peak, "algorithmic_bytes": cb,
                 "timing": f"CUDA graph of {n} launches over {copies} input copies (cold L2)",
-                "plan": rarn.plan(cw.op, cw.T, cw.H, cR, cw.dtype)}
+                "plan": rarn.plan(cw.op, cw.T, cw.H, cR, cw.dtype, rdtype=cw.res_dtype)}
             del cd
             torch.cuda.empty_cache()
         if rarn.watchdog(clear=True):

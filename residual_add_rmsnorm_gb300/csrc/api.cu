@@ -99,6 +99,11 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms, int r
         const int64_t slots = (int64_t)num_sms * (resident_threads / 32);
         const int64_t rounds = ceil_div(T, slots);
         pl.grid = (int)ceil_div(ceil_div(T, rounds), pl.block / 32);
+        // pipelined across rows (plain / fused) when every warp has several
+        pl.pipe = op != OP_REDUCE && rounds >= 2;
+        if (const char *v = getenv("RARN_ROWS_PIPE")) {  // measurements only
+            if (*v == '0') pl.pipe = false;
+        }
         return pl;
     }
     // values per thread: aim at 256 threads per row, powers of two, within
@@ -108,7 +113,11 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms, int r
                    : (pg ? 0 : rows_max_block(rows_regs_scalar(pt, op)));
     };
     const int max_pt = vec ? 8 : 16;
-    int pt = std::min(max_pt, pow2_at_least(ceil_div(n, 256)));
+    // a binary32 residual doubles the registers per pack of a reduce row:
+    // spread it over twice the threads (measured: 293 vs 366 us at R = 8,
+    // [8192, 8192])
+    const int target = (op == OP_REDUCE && rn == 2) ? 512 : 256;
+    int pt = std::min(max_pt, pow2_at_least(ceil_div(n, target)));
     if (const char *v = getenv("RARN_ROWS_PT")) {  // measurements only
         const int f = atoi(v);
         if (f >= 1 && f <= max_pt && (f & (f - 1)) == 0) pt = f;

@@ -494,6 +494,36 @@ __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
     }
 }
 
+// One warp per row, pipelined like k_cta_pipe (plain and fused): the next
+// row's loads are in flight while this row is reduced and written.
+template <typename T, int VPT, int OP, typename TR>
+__global__ void __launch_bounds__(256) k_warp_pipe(Problem p) {
+    const int nv = (int)(p.H / DT<T>::EPV);
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    const int64_t first = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
+    const int64_t step = (int64_t)gridDim.x * wpb;
+    grid_dependency_wait();
+    uint4 gv[VPT];
+    load_gamma_vec<T, VPT>(p, lane, 32, nv, gv);
+    RowLoads<T, VPT, OP, TR> next;
+    int64_t t = first;
+    if (t < p.T) issue_row_loads<T, VPT, OP, TR>(p, t, lane, 32, nv, next);
+    for (; t < p.T; t += step) {
+        const RowLoads<T, VPT, OP, TR> cur = next;
+        if (t + step < p.T) {
+            issue_row_loads<T, VPT, OP, TR>(p, t + step, lane, 32, nv, next);
+        } else {
+            grid_launch_dependents();
+        }
+        uint4 hv[VPT][Res<T, TR>::N];
+        const float ss = consume_row_loads<T, VPT, OP, TR>(p, t, lane, 32, nv, cur, hv);
+        const float tot = warp_sum(ss);
+        const float inv = rsqrtf(tot / (float)p.H + p.eps);
+        pass2_vec<T, VPT, TR, true>(p, t, lane, 32, nv, hv, inv, gv);
+    }
+}
+
 // One CTA per row, single elements.
 template <typename T, int NE, int OP, typename TR>
 __global__ void __launch_bounds__(ScalarBound<NE, OP>::value, 1) k_cta_scalar(Problem p) {
@@ -569,6 +599,16 @@ static cudaError_t launch_rows_op(const Problem &p, const Plan &pl, cudaStream_t
     auto go = [&](auto kernel) { return launch_kernel(kernel, g, b, 0, st, pl.pdl, 1, p); };
     switch (pl.kind) {
     case KIND_WARP:
+        if constexpr (OP != OP_REDUCE) {
+            if (pl.pipe) {
+                switch (pl.per_thread) {
+                case 1: return go(k_warp_pipe<T, 1, OP, TR>);
+                case 2: return go(k_warp_pipe<T, 2, OP, TR>);
+                case 4: return go(k_warp_pipe<T, 4, OP, TR>);
+                default: return cudaErrorInvalidValue;
+                }
+            }
+        }
         switch (pl.per_thread) {
         case 1: return go(k_warp_vec<T, 1, OP, TR>);
         case 2: return go(k_warp_vec<T, 2, OP, TR>);

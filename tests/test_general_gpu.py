@@ -173,3 +173,9 @@ def test_extended_workloads(name):
     """The widened rows' benchmark workloads at full size."""
     w = W.BY_NAME[name]
     _check(w, W.generate(w), w.row_stride, w.row_stride, w.row_stride, 0, name)
+
+
+def test_fp32_residual_pipelined_warp():
+    w = W.workload("fused_add_rms_norm", "bf16", 30000, 256, eps=1e-6, seed=5, rdtype="f32")
+    assert "pipe=1" in rarn.plan(w.op, w.T, w.H, 1, "bf16", rdtype="f32")
+    _check(w, W.generate(w), 256, 256, 256, 0, "fp32 residual warp pipe")

@@ -390,3 +390,16 @@ def test_pipelined_rows_kernel():
         plan = rarn.plan(op, T, H, 1, dt)
         assert "pipe=1" in plan, plan
         check_parity(w, W.generate(w), out_is_input=inplace, what=f"pipe {op} {dt} T{T} H{H}")
+
+
+def test_pipelined_warp_kernel():
+    """The pipelined warp-per-row kernel: short rows, several rows per warp,
+    ragged row counts, in place."""
+    for op, dt, T, H, inplace in (("rms_norm", "f32", 20011, 96, False),
+                                  ("fused_add_rms_norm", "bf16", 30001, 1024, True),
+                                  ("rms_norm", "f16", 25000, 512, True),
+                                  ("fused_add_rms_norm", "f16", 10999, 8, False)):
+        w = W.workload(op, dt, T, H, eps=1e-6, seed=T)
+        plan = rarn.plan(op, T, H, 1, dt)
+        assert plan.startswith("rows.warp") and "pipe=1" in plan, plan
+        check_parity(w, W.generate(w), out_is_input=inplace, what=f"warp pipe {op} {dt} T{T}")
