@@ -18,6 +18,10 @@ Sources followed (by page title and section):
     squares of that stored value, rsqrt(variance / hidden_size + eps), then
     scale by the reciprocal RMS and the weight.
 
+The 8-bit output (``rows_fp8``) follows "Block All Reduce", FP8 section: e4m3
+and e5m2 codes, converted with saturation to the largest finite value; the
+scale is a given per-tensor value or max |v| / maxf per row.
+
 Every function here is pinned by ``tests/test_oracle_pins.py`` against values
 fixed by the formats' definitions, closed forms and exact rational arithmetic.
 """
@@ -32,6 +36,8 @@ from . import build as _build
 
 DTYPES = {"f32": 0, "f16": 1, "bf16": 2}
 STORAGE = {"f32": np.float32, "f16": np.uint16, "bf16": np.uint16}
+FP8 = {"e4m3": 0, "e5m2": 1}
+QMODES = {"tensor": 0, "row": 1}
 
 
 def _ptr(a):
@@ -75,6 +81,13 @@ class Oracle:
         lib.oracle_rows_ex.argtypes = [c_int, c_int, i64, i64, i32, p, i64, i64, p, p, i64, p, f32,
                                        p, i64, p, p, c_int]
         lib.oracle_rows_ex.restype = c_int
+        lib.oracle_rows_fp8.argtypes = [c_int, c_int, i64, i64, i32, p, i64, i64, p, i64, p, f32,
+                                        c_int, f32, p, i64, p, p]
+        lib.oracle_rows_fp8.restype = c_int
+        lib.oracle_decode_fp8.argtypes = [c_int, p, p, i64]
+        lib.oracle_decode_fp8.restype = c_int
+        lib.oracle_round_fp8.argtypes = [c_int, p, p, i64]
+        lib.oracle_round_fp8.restype = c_int
         lib.oracle_decode.argtypes = [c_int, p, p, i64]
         lib.oracle_decode.restype = None
         lib.oracle_round.argtypes = [c_int, p, p, i64]
@@ -154,6 +167,44 @@ class Oracle:
             threads))
         return Result(y, residual, inv, y64, n)
 
+    def rows_fp8(self, dtype, fmt, T, H, R, x, ldx, slice_, residual, ldr, gamma, eps, mode,
+                 scale=1.0, ldq=None, *, fill=0, want_u64=False):
+        """8-bit output (``fmt`` "e4m3" / "e5m2").  x (R = 0 or 1) or the R
+        partials live in the flat storage array ``x`` (row stride ``ldx``,
+        ``slice_`` elements between partials); ``residual`` (row stride
+        ``ldr``) is updated IN PLACE.  ``mode`` "tensor" divides by the given
+        ``scale``, "row" by max|v| / maxf per row.  Returns (codes [T, ldq]
+        uint8 with the padding left at ``fill``, row scales [T] float32 (row
+        mode), u64 [T, H] or None)."""
+        x = self._as_storage(x, dtype)
+        gamma = self._as_storage(gamma, dtype)
+        if residual is not None and not (residual.flags.c_contiguous and
+                                         residual.dtype == STORAGE[dtype]):
+            raise TypeError("residual must be contiguous storage of the x dtype")
+        ldq = ldq or H
+        codes = np.full(T * ldq, fill, np.uint8)
+        rs = np.zeros(T, np.float32)
+        u64 = np.empty((T, H), np.float64) if want_u64 else None
+        _check(self.lib.oracle_rows_fp8(DTYPES[dtype], FP8[fmt], T, H, R, _ptr(x), ldx, slice_,
+                                        _ptr(residual), ldr, _ptr(gamma), float(eps),
+                                        QMODES[mode], float(scale), _ptr(codes), ldq, _ptr(rs),
+                                        _ptr(u64)))
+        return codes.reshape(T, ldq), rs, u64
+
+    def decode_fp8(self, codes, fmt) -> np.ndarray:
+        """8-bit codes -> binary64 values (the oracle's own decoder)."""
+        codes = np.ascontiguousarray(codes, np.uint8)
+        out = np.empty(codes.shape, np.float64)
+        _check(self.lib.oracle_decode_fp8(FP8[fmt], _ptr(codes), _ptr(out), codes.size))
+        return out
+
+    def round_fp8(self, values, fmt) -> np.ndarray:
+        """binary64 values -> 8-bit codes, nearest-even with saturation."""
+        values = np.ascontiguousarray(values, np.float64)
+        out = np.empty(values.shape, np.uint8)
+        _check(self.lib.oracle_round_fp8(FP8[fmt], _ptr(values), _ptr(out), values.size))
+        return out
+
     def decode(self, bits, dtype) -> np.ndarray:
         """Storage bits -> binary64 values (the oracle's own decoder)."""
         bits = self._as_storage(bits, dtype)
@@ -194,6 +245,10 @@ def reduce_add_rms_norm(*a, **k) -> Result:
 
 def rows_ex(*a, **k) -> Result:
     return default().rows_ex(*a, **k)
+
+
+def rows_fp8(*a, **k):
+    return default().rows_fp8(*a, **k)
 
 
 def decode(*a, **k) -> np.ndarray:

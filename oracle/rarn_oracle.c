@@ -35,6 +35,15 @@
  * infinity and gradual underflow; it is written from the formats'
  * definitions (precision p, minimum exponent emin, maximum exponent emax).
  *
+ * 8-bit output (oracle_rows_fp8): steps 1-3, then v_i = (h_i * inv) * gamma_i
+ * in binary64 and the code q_i = FP8( v_i / s ), FP8 being nearest-even
+ * rounding to e4m3 or e5m2 with saturation to the largest finite value
+ * ("Block All Reduce", FP8 section: both formats, saturating conversion).
+ * s is a given per-tensor binary32 scale, or per row max_i |v_i| / maxf, so
+ * that the row's largest magnitude maps to the format's largest value.  The
+ * pages give no formula for the scale; this is the plainest reading of a
+ * per-row (dynamic) scale.
+ *
  * Build flags must keep binary32 arithmetic exact IEEE: no -ffast-math, and
  * -ffp-contract=off (there is no multiply in the binary32 part, but the flag
  * documents the intent).
@@ -318,6 +327,144 @@ int oracle_rows_ex(int dt, int rdt, int64_t T, int64_t H, int32_t R, const void 
     job_t j = {dt, rdt, T, H, R, x, ldx, slice, R >= 1 ? residual_in : NULL, ldr, gamma, eps,
                R >= 1 ? residual_out : NULL, y, ldy, inv_out, y64_out};
     return run(&j, nthreads);
+}
+
+/* ----------------------------------------------------------------------- */
+/* fp8 output                                                               */
+/* ----------------------------------------------------------------------- */
+
+/* The two 8-bit formats ("Block All Reduce", FP8 section: e4m3 and e5m2,
+ * converted with saturation to the largest finite value):
+ *   e4m3: 1 sign, 4 exponent bits (bias 7), 3 fraction bits; no infinity;
+ *         S.1111.111 is NaN, so the largest finite value is 448 (S.1111.110);
+ *   e5m2: 1 sign, 5 exponent bits (bias 15), 2 fraction bits; IEEE-style
+ *         infinities and NaNs; largest finite value 57344.
+ * Both have gradual underflow (subnormal step 2^(emin - mbits)). */
+typedef struct {
+    int p, emin, emax, mbits, bias;
+    double maxf;
+} fp8_format;
+
+static const fp8_format FP8[2] = {
+    {4, -6, 8, 3, 7, 448.0},      /* e4m3 */
+    {3, -14, 15, 2, 15, 57344.0}, /* e5m2 */
+};
+
+/* Round to nearest, ties to even, saturating: a value whose rounding would
+ * exceed the largest finite value in magnitude gives +-maxf. */
+static double round_fp8_sat(const fp8_format *f, double v) {
+    if (isnan(v)) return v;
+    double r = round_to_format(v, f->p, f->emin, f->emax);
+    if (isinf(r) || fabs(r) > f->maxf) r = copysign(f->maxf, v);
+    return r;
+}
+
+/* Code of a value that is exactly representable (finite or NaN). */
+static uint8_t encode_fp8(const fp8_format *f, double v) {
+    if (isnan(v)) return 0x7f;
+    uint8_t s = signbit(v) ? 0x80 : 0;
+    double a = fabs(v);
+    if (a == 0.0) return s;
+    int e2;
+    frexp(a, &e2);
+    int lead = e2 - 1;
+    if (lead >= f->emin) {
+        int frac = (int)ldexp(a, f->mbits - lead) - (1 << f->mbits);
+        return (uint8_t)(s | ((lead + f->bias) << f->mbits) | frac);
+    }
+    return (uint8_t)(s | (int)ldexp(a, f->mbits - f->emin)); /* subnormal */
+}
+
+static double decode_fp8(const fp8_format *f, uint8_t b) {
+    int sign = b >> 7, e = (b & 0x7f) >> f->mbits, m = b & ((1 << f->mbits) - 1);
+    int emax_field = (1 << (7 - f->mbits)) - 1;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, f->emin - f->mbits);
+    else if (f->mbits == 3 && e == emax_field && m == 7)
+        v = NAN;
+    else if (f->mbits == 2 && e == emax_field)
+        v = m == 0 ? INFINITY : NAN;
+    else
+        v = ldexp((double)(m + (1 << f->mbits)), e - f->bias - f->mbits);
+    return sign ? -v : v;
+}
+
+/*
+ * The three operations with an 8-bit output.  h, inv and v_i = (h_i * inv) *
+ * gamma_i as in one_row (binary64); then the code q_i = fp8(v_i / s):
+ *   mode 0 (per tensor): s = the binary32 `scale` argument;
+ *   mode 1 (per row):    s = max_i |v_i| / maxf (binary64; s = 1 for a row
+ *                        of zeros), reported in row_scales_out[t] rounded to
+ *                        binary32.
+ * R = 0 plain, R >= 1 partials + residual (residual in the inputs' type,
+ * updated in place).  codes: T rows of ldq bytes.  u64_out (optional, dense
+ * [T, H]): v_i / s before the rounding.
+ */
+int oracle_rows_fp8(int dt, int fmt, int64_t T, int64_t H, int32_t R, const void *x, int64_t ldx,
+                    int64_t slice, void *residual, int64_t ldr, const void *gamma, float eps,
+                    int mode, float scale, uint8_t *codes, int64_t ldq, float *row_scales_out,
+                    double *u64_out) {
+    if (T < 0 || H <= 0 || ldx < H || ldq < H || (R >= 1 && (!residual || ldr < H)) ||
+        (mode != 0 && mode != 1) || (fmt != 0 && fmt != 1) || !codes)
+        return -2;
+    const fp8_format *f = &FP8[fmt];
+    double *h = (double *)malloc(sizeof(double) * (size_t)H);
+    double *v = (double *)malloc(sizeof(double) * (size_t)H);
+    if (!h || !v) {
+        free(h);
+        free(v);
+        return -1;
+    }
+    for (int64_t t = 0; t < T; ++t) {
+        /* h, inv: the same steps as one_row */
+        const int64_t xrow = t * ldx, rrow = t * ldr;
+        if (R == 0) {
+            for (int64_t i = 0; i < H; ++i) h[i] = load_elem(dt, x, xrow + i);
+        } else {
+            for (int64_t i = 0; i < H; ++i) {
+                float acc = (float)load_elem(dt, x, xrow + i);
+                for (int32_t r = 1; r < R; ++r)
+                    acc = acc + (float)load_elem(dt, x, (int64_t)r * slice + xrow + i);
+                acc = acc + (float)load_elem(dt, residual, rrow + i);
+                h[i] = round_dt(dt, (double)acc);
+            }
+            for (int64_t i = 0; i < H; ++i) store_exact(dt, residual, rrow + i, h[i]);
+        }
+        double ss = 0.0;
+        for (int64_t i = 0; i < H; ++i) ss += h[i] * h[i];
+        const double inv = 1.0 / sqrt(ss / (double)H + (double)eps);
+        double amax = 0.0;
+        for (int64_t i = 0; i < H; ++i) {
+            v[i] = (h[i] * inv) * load_elem(dt, gamma, i);
+            if (fabs(v[i]) > amax) amax = fabs(v[i]);
+        }
+        double s = (double)scale;
+        if (mode == 1) {
+            s = amax > 0.0 ? amax / f->maxf : 1.0;
+            if (row_scales_out) row_scales_out[t] = (float)s;
+        }
+        for (int64_t i = 0; i < H; ++i) {
+            const double u = v[i] / s;
+            if (u64_out) u64_out[t * H + i] = u;
+            codes[t * ldq + i] = encode_fp8(f, round_fp8_sat(f, u));
+        }
+    }
+    free(h);
+    free(v);
+    return 1;
+}
+
+int oracle_decode_fp8(int fmt, const uint8_t *src, double *dst, int64_t n) {
+    if (fmt != 0 && fmt != 1) return -2;
+    for (int64_t i = 0; i < n; ++i) dst[i] = decode_fp8(&FP8[fmt], src[i]);
+    return 1;
+}
+
+int oracle_round_fp8(int fmt, const double *src, uint8_t *dst, int64_t n) {
+    if (fmt != 0 && fmt != 1) return -2;
+    for (int64_t i = 0; i < n; ++i) dst[i] = encode_fp8(&FP8[fmt], round_fp8_sat(&FP8[fmt], src[i]));
+    return 1;
 }
 
 /* Elementwise helpers exposed so the tests can pin the format code alone. */

@@ -12,7 +12,9 @@ What the pins rest on (none of it is the oracle's own code):
     invariance at eps = 0, one-element rows);
   * a worked example of the fixed binary32 summation order;
   * exact integer sums;
-  * brute force on tiny rows in exact rational / 50-digit decimal arithmetic.
+  * brute force on tiny rows in exact rational / 50-digit decimal arithmetic;
+  * for the 8-bit output, torch's float8 decoders and casts and a brute-force
+    nearest search over the code table.
 """
 from __future__ import annotations
 
@@ -533,6 +535,185 @@ def pin_fp32_residual_matches_16bit_when_exact(O):
                               lib_decode(same.residual, dt)), dt
 
 
+# ---------------------------------------------------------------------------
+# Pins on the 8-bit output (e4m3 / e5m2 codes with a per-tensor or per-row
+# scale)
+# ---------------------------------------------------------------------------
+
+FP8_MAX = {"e4m3": 448.0, "e5m2": 57344.0}
+
+
+def lib_decode_fp8(codes, fmt: str) -> np.ndarray:
+    """Decode 8-bit codes with torch's float8 types (not the oracle)."""
+    import torch
+    td = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+    c = torch.from_numpy(np.ascontiguousarray(codes, np.uint8).copy())
+    return c.view(td).to(torch.float64).numpy()
+
+
+def _fp8_table(fmt):
+    """Values and codes of the non-negative finite codes, ascending."""
+    codes = np.arange(128, dtype=np.uint8)
+    vals = lib_decode_fp8(codes, fmt)
+    ok = np.isfinite(vals)
+    return vals[ok], codes[ok]
+
+
+def fp8_nearest(u, fmt: str) -> np.ndarray:
+    """Brute force: the code of the finite value nearest to each u (exact
+    rational distances, ties to the even code), so values beyond the largest
+    finite value saturate to it; the sign bit is u's."""
+    vals, codes = _fp8_table(fmt)
+    u = np.asarray(u, np.float64)
+    out = np.empty(u.size, np.uint8)
+    for n, x in enumerate(u.ravel()):
+        a = abs(float(x))
+        k = int(np.searchsorted(vals, a))
+        if k >= len(vals):
+            c = codes[-1]
+        elif vals[k] == a or k == 0:
+            c = codes[k]
+        else:
+            fa = Fraction(a)
+            dl, dh = fa - Fraction(vals[k - 1]), Fraction(vals[k]) - fa
+            c = codes[k - 1] if dl < dh or (dl == dh and codes[k - 1] % 2 == 0) else codes[k]
+        out[n] = c | (0x80 if np.signbit(x) else 0)
+    return out.reshape(u.shape)
+
+
+def pin_fp8_decode_all_codes(O):
+    """Every code of both formats decodes as torch's float8 types decode it."""
+    codes = np.arange(256, dtype=np.uint8)
+    for fmt in ("e4m3", "e5m2"):
+        a = O.decode_fp8(codes, fmt)
+        b = lib_decode_fp8(codes, fmt)
+        assert np.array_equal(np.isnan(a), np.isnan(b)), fmt
+        ok = ~np.isnan(b)
+        assert np.array_equal(a[ok], b[ok]), fmt
+
+
+def _fp8_probe(fmt, rng):
+    vals, _ = _fp8_table(fmt)
+    mid = (vals[1:] + vals[:-1]) / 2  # exact in binary64
+    top = FP8_MAX[fmt]
+    step = vals[-1] - vals[-2]
+    probe = [mid, np.nextafter(mid, 0), np.nextafter(mid, np.inf), vals,
+             np.exp2(rng.uniform(np.log2(vals[1]) - 2, np.log2(top) + 1, 3000)),
+             np.array([0.0, vals[1] / 2, vals[1] / 4, top + step / 2, top + step,
+                       top * 1.01, top * 4, 1e30])]
+    p = np.concatenate(probe)
+    return np.concatenate([p, -p])
+
+
+def pin_fp8_round_nearest(O):
+    """Rounding to 8 bits is nearest-even with saturation (brute force over the
+    code table), and agrees with torch's float32 -> float8 cast inside the
+    finite range."""
+    import torch
+    rng = np.random.default_rng(21)
+    for fmt in ("e4m3", "e5m2"):
+        p = _fp8_probe(fmt, rng)
+        got = O.round_fp8(p, fmt)
+        assert np.array_equal(got, fp8_nearest(p, fmt)), fmt
+        td = torch.float8_e4m3fn if fmt == "e4m3" else torch.float8_e5m2
+        p32 = p[np.abs(p) <= FP8_MAX[fmt]].astype(np.float32)
+        lib = torch.from_numpy(p32).to(td).view(torch.uint8).numpy()
+        assert np.array_equal(O.round_fp8(p32.astype(np.float64), fmt), lib), fmt
+
+
+def pin_fp8_tensor_scale_closed_form(O):
+    """A constant row c with weights gamma_i and a per-tensor scale s:
+    u_i = c / sqrt(c^2 + eps) * gamma_i / s (50-digit decimal), and each code
+    is the nearest-even 8-bit value of u_i."""
+    getcontext().prec = 50
+    for dt in ("f32", "bf16", "f16"):
+        for fmt, s in (("e4m3", 0.0078125), ("e4m3", 0.3), ("e5m2", 2.0 ** -10)):
+            T, H, c, eps = 2, 64, 1.5, 1e-3
+            x = bits_of(np.full((T, H), c), dt)
+            gd = lib_decode(bits_of(np.linspace(-2.0, 2.0, H), dt), dt)
+            g = bits_of(gd, dt)
+            codes, _, u = O.rows_fp8(dt, fmt, T, H, 0, x.reshape(-1), H, T * H, None, H, g,
+                                     eps, "tensor", s, want_u64=True)
+            e32 = Decimal(float(np.float32(eps)))
+            s32 = Decimal(float(np.float32(s)))
+            k = Decimal(c) / (Decimal(c) * Decimal(c) + e32).sqrt()
+            want = np.array([float(k * Decimal(gi) / s32) for gi in gd])
+            for t in range(T):
+                assert _rel(u[t], want) < 1e-14, (dt, fmt, s)
+            assert np.array_equal(codes, fp8_nearest(u, fmt)), (dt, fmt, s)
+
+
+def pin_fp8_row_scale(O):
+    """Per-row scale: s_t = max_i |v_i| / maxf with v the normalised row of the
+    16-bit-output path (whose pins fix it), u = v / s_t, codes nearest-even of
+    u; the largest element becomes +-maxf; a row of zeros has s = 1 and zero
+    codes; the residual is the one of the 16-bit-output path."""
+    rng = np.random.default_rng(22)
+    for dt in ("f32", "bf16", "f16"):
+        for R in (0, 1, 3):
+            T, H = 5, 77
+            n = max(R, 1)
+            parts = np.stack([_rand_bits(rng, (T, H), dt) for _ in range(n)])
+            parts[:, 2] = bits_of(np.zeros((n, H)), dt)
+            res = _rand_bits(rng, (T, H), dt)
+            if R:
+                res[2] = bits_of(np.zeros(H), dt)
+            g = bits_of(rng.uniform(-1.5, 1.5, H), dt)
+            if R == 0:
+                ref = O.rms_norm(parts[0], g, 1e-5, dt, want_y64=True)
+            elif R == 1:
+                ref = O.fused_add_rms_norm(parts[0], res, g, 1e-5, dt, want_y64=True)
+            else:
+                ref = O.reduce_add_rms_norm(parts, res, g, 1e-5, dt, want_y64=True)
+            for fmt in ("e4m3", "e5m2"):
+                rb = res.reshape(-1).copy() if R else None
+                codes, rs, u = O.rows_fp8(dt, fmt, T, H, R, parts.reshape(-1).copy(), H, T * H,
+                                          rb, H, g, 1e-5, "row", want_u64=True)
+                amax = np.max(np.abs(ref.y64), axis=1)
+                s = np.where(amax > 0, amax / FP8_MAX[fmt], 1.0)
+                assert np.array_equal(rs, s.astype(np.float32)), (dt, R, fmt)
+                assert _rel(u, ref.y64 / s[:, None]) < 1e-15, (dt, R, fmt)
+                assert np.array_equal(codes, fp8_nearest(u, fmt)), (dt, R, fmt)
+                vals = lib_decode_fp8(codes, fmt)
+                top = np.max(np.abs(vals), axis=1)
+                assert np.array_equal(top[amax > 0], np.full((amax > 0).sum(), FP8_MAX[fmt]))
+                assert rs[2] == 1.0 and np.all(vals[2] == 0), (dt, R, fmt)
+                if R:
+                    assert np.array_equal(rb.reshape(T, H), ref.residual), (dt, R, fmt)
+
+
+def pin_fp8_strides(O):
+    """Strided inputs and a code row stride larger than H: the dense result in
+    the first H bytes of each row, the padding untouched."""
+    rng = np.random.default_rng(23)
+    for dt in ("bf16", "f32"):
+        for R in (0, 1, 3):
+            T, H, ldx, ldr, ldq = 4, 45, 51, 47, 64
+            n = max(R, 1)
+            parts = np.stack([_rand_bits(rng, (T, H), dt) for _ in range(n)])
+            res = _rand_bits(rng, (T, H), dt)
+            g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+            slice_ = T * ldx + 5
+            X = np.concatenate([_strided(parts[r], ldx, dt, extra=5) for r in range(n)])
+            Rs = _strided(res, ldr, dt) if R else None
+            Rd = res.reshape(-1).copy() if R else None
+            for mode in ("tensor", "row"):
+                a = O.rows_fp8(dt, "e4m3", T, H, R, X, ldx, slice_, Rs, ldr, g, 1e-5, mode, 0.05,
+                               ldq, fill=0x5A)
+                b = O.rows_fp8(dt, "e4m3", T, H, R, parts.reshape(-1).copy(), H, T * H, Rd, H, g,
+                               1e-5, mode, 0.05)
+                assert np.array_equal(a[0][:, :H], b[0]), (dt, R, mode)
+                assert np.all(a[0][:, H:] == 0x5A), (dt, R, mode)
+                assert np.array_equal(a[1], b[1]), (dt, R, mode)
+                if R:
+                    assert np.array_equal(_rows(Rs, T, ldr, H), Rd.reshape(T, H)), (dt, R, mode)
+                    pad = Rs.reshape(T, ldr)[:, H:]
+                    assert np.array_equal(pad, np.full_like(pad, GARBAGE[dt])), (dt, R, mode)
+                    # second call on updated residuals: restore for the next mode
+                    Rs = _strided(res, ldr, dt)
+                    Rd = res.reshape(-1).copy()
+
+
 ALL_PINS = [
     pin_decode_all_patterns,
     pin_round_matches_library,
@@ -551,4 +732,9 @@ ALL_PINS = [
     pin_strided_equals_dense,
     pin_fp32_residual_sum,
     pin_fp32_residual_matches_16bit_when_exact,
+    pin_fp8_decode_all_codes,
+    pin_fp8_round_nearest,
+    pin_fp8_tensor_scale_closed_form,
+    pin_fp8_row_scale,
+    pin_fp8_strides,
 ]

@@ -58,6 +58,30 @@ MUTATIONS = {
     "square_sign": ("ss += h[i] * h[i];", "ss += h[i] * fabs(h[i]);"),
     # no overflow to infinity
     "no_overflow": ("if (fabs(out) > max_finite) return copysign(INFINITY, v);", ""),
+    # 8-bit output: no saturation (the largest code pattern instead)
+    "fp8_no_saturation": ("r = copysign(f->maxf, v);", "r = NAN;"),
+    # e4m3 with one significant bit too many / an exponent range off by one
+    "e4m3_precision": ("{4, -6, 8, 3, 7, 448.0}", "{5, -6, 8, 3, 7, 448.0}"),
+    "e4m3_emin": ("{4, -6, 8, 3, 7, 448.0}", "{4, -7, 8, 3, 7, 448.0}"),
+    "e5m2_max": ("{3, -14, 15, 2, 15, 57344.0}", "{3, -14, 15, 2, 15, 61440.0}"),
+    # exponent bias off by one in the encoder / decoder
+    "fp8_encode_bias": ("((lead + f->bias) << f->mbits)", "((lead + f->bias + 1) << f->mbits)"),
+    "fp8_decode_subnormal": ("ldexp((double)m, f->emin - f->mbits)",
+                             "ldexp((double)m, f->emin - f->mbits - 1)"),
+    # scale applied the wrong way round / per-row divisor wrong
+    "fp8_scale_multiplied": ("const double u = v[i] / s;", "const double u = v[i] * s;"),
+    "fp8_row_divisor": ("s = amax > 0.0 ? amax / f->maxf : 1.0;",
+                        "s = amax > 0.0 ? amax / 256.0 : 1.0;"),
+    "fp8_zero_row_scale": ("s = amax > 0.0 ? amax / f->maxf : 1.0;",
+                           "s = amax > 0.0 ? amax / f->maxf : 0.0;"),
+    # signed maximum instead of the maximum magnitude
+    "fp8_signed_amax": ("if (fabs(v[i]) > amax) amax = fabs(v[i]);", "if (v[i] > amax) amax = v[i];"),
+    # residual not written back / code rows not strided
+    "fp8_residual_not_stored": (
+        "for (int64_t i = 0; i < H; ++i) store_exact(dt, residual, rrow + i, h[i]);", ""),
+    "fp8_code_stride": ("codes[t * ldq + i]", "codes[t * H + i]"),
+    # gamma dropped from the 8-bit path
+    "fp8_no_gamma": ("v[i] = (h[i] * inv) * load_elem(dt, gamma, i);", "v[i] = h[i] * inv;"),
 }
 
 
