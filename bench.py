@@ -207,6 +207,17 @@ def make_call(w, tensors, rarn):
     residual."""
     eps = w.eps
     general = w.row_stride != w.H or w.res_dtype != w.dtype
+    if w.qfmt:  # 8-bit output: codes in y, scale in "scale"
+        y, sc, g, f, m = tensors["y"], tensors["scale"], tensors["gamma"], w.qfmt, w.qmode
+        if w.op == "rms_norm":
+            x = tensors["x"]
+            return lambda: rarn.rms_norm_fp8(x, g, eps, y, sc, f, m)
+        r = tensors["residual"]
+        if w.op == "fused_add_rms_norm":
+            x = tensors["x"]
+            return lambda: rarn.fused_add_rms_norm_fp8(x, r, g, eps, y, sc, f, m)
+        p = tensors["partials"]
+        return lambda: rarn.reduce_add_rms_norm_fp8(p, r, g, eps, y, sc, f, m)
     if w.op == "rms_norm":
         x, g, y = tensors["x"], tensors["gamma"], tensors["y"]
         if general:
@@ -241,7 +252,12 @@ def device_tensors(w, data, device):
         else:
             t[k] = dense
     ref = t.get("x", t.get("residual"))
-    if ld != w.H:
+    if w.qfmt:
+        t["y"] = torch.empty((w.T, ld), dtype=torch.uint8, device=device)[:, :w.H]
+        t["scale"] = (torch.full((1,), w.qscale, dtype=torch.float32, device=device)
+                      if w.qmode == "tensor" else
+                      torch.empty(w.T, dtype=torch.float32, device=device))
+    elif ld != w.H:
         t["y"] = torch.empty((w.T, ld), dtype=to_device(data["gamma"], w.dtype, device).dtype,
                              device=device)[:, :w.H]
     else:
@@ -496,7 +512,8 @@ def main():
                 "us_per_launch": us, "gbs": gbs, "rows_per_s": cw.T / (us / 1e6),
                 "frac_of_peak": gbs / peak, "algorithmic_bytes": cb,
                 "timing": f"CUDA graph of {n} launches over {copies} input copies (cold L2)",
-                "plan": rarn.plan(cw.op, cw.T, cw.H, cR, cw.dtype, rdtype=cw.res_dtype)}
+                "plan": (rarn.plan_fp8(cw.op, cw.T, cw.H, cR, cw.dtype) if cw.qfmt else
+                         rarn.plan(cw.op, cw.T, cw.H, cR, cw.dtype, rdtype=cw.res_dtype))}
             del cd
             torch.cuda.empty_cache()
         if rarn.watchdog(clear=True):

@@ -208,6 +208,55 @@ rarn_status rarn_reduce_add_rms_norm_ex(rarn_rows y, rarn_rows partials, int64_t
                                         int32_t R, rarn_rows residual, const void *gamma,
                                         int64_t T, int64_t H, float eps, void *stream);
 
+/*
+ * 8-bit output forms: the general forms above with y replaced by a matrix of
+ * one-byte codes in e4m3 or e5m2 and a scale ("Block All Reduce", FP8
+ * section: both formats, converted with saturation to the largest finite
+ * value).  For each row, with h, inv and v_i = (h_i * inv) * gamma_i computed
+ * as for the 16-bit output (binary32), the code is u_i = v_i / s rounded to
+ * nearest even and saturated to +-maxf (448 for e4m3, 57344 for e5m2):
+ *   RARN_SCALE_TENSOR: s = scale[0], a binary32 value the kernel reads
+ *                      (in device memory, so an earlier kernel may write it);
+ *                      u_i = v_i * (1 / s);
+ *   RARN_SCALE_ROW:    s = max_i |v_i| / maxf, written to scale[t] (T binary32
+ *                      values); u_i = (v_i * (1 / max|v|)) * maxf, so the
+ *                      row's largest magnitude maps to maxf; a row of zeros
+ *                      gets s = 1 and zero codes.
+ * Dequantised, code value * s approximates v.  Row t of the codes starts at
+ * byte t * row_stride of `data` (row_stride >= H); only the first H bytes of
+ * each row are written.  The residual (fused / reduce) has the inputs'
+ * storage type and is updated as in the other forms.
+ *
+ * Errors: a NULL descriptor or scale, an unknown format or mode:
+ * RARN_ERR_INVALID_ARG; a residual of another type than the inputs, or the
+ * stream / cluster path forced (the 8-bit output is built for the register
+ * row kernels only): RARN_ERR_UNSUPPORTED; the codes or a written scale
+ * overlapping any other buffer, or a read scale overlapping an output:
+ * RARN_ERR_ALIAS.  Everything else as for the general forms.  The packed
+ * kernels need, besides the inputs' 16-byte conditions, codes aligned to and
+ * a row stride a multiple of 16 / sizeof(input element) bytes.
+ */
+typedef enum rarn_fp8_format { RARN_E4M3 = 0, RARN_E5M2 = 1 } rarn_fp8_format;
+typedef enum rarn_scale_mode { RARN_SCALE_TENSOR = 0, RARN_SCALE_ROW = 1 } rarn_scale_mode;
+
+typedef struct rarn_fp8_rows {
+    void *data;                 /* codes: T rows of H bytes, device memory */
+    int64_t row_stride;         /* bytes between rows, >= H */
+    rarn_fp8_format format;
+    rarn_scale_mode scale_mode;
+    float *scale;               /* device memory: 1 value (read) or T values (written) */
+} rarn_fp8_rows;
+
+rarn_status rarn_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows x, const void *gamma, int64_t T,
+                              int64_t H, float eps, void *stream);
+rarn_status rarn_fused_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows x, rarn_rows residual,
+                                        const void *gamma, int64_t T, int64_t H, float eps,
+                                        void *stream);
+rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows partials,
+                                         int64_t partial_stride, int32_t R, rarn_rows residual,
+                                         const void *gamma, int64_t T, int64_t H, float eps,
+                                         void *stream);
+
 /* Static text for a status code. */
 const char *rarn_status_string(rarn_status s);
 
@@ -258,6 +307,10 @@ rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt
 /* rarn_plan for a residual of storage type `rdt` (see the general forms). */
 rarn_status rarn_plan_ex(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt,
                          rarn_dtype rdt, int vec_ok, int num_sms, char *out, size_t cap);
+
+/* rarn_plan for the 8-bit output forms (residual of the inputs' type). */
+rarn_status rarn_plan_fp8(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt, int vec_ok,
+                          int num_sms, char *out, size_t cap);
 
 /*
  * Watchdog word of the current device.  Kernels that wait on shared-memory

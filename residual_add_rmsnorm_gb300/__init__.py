@@ -11,6 +11,12 @@ library is missing or fails to load, every call raises.
     y = rms_norm(x, gamma, eps)                         # x: [..., H]
     y = fused_add_rms_norm(x, residual, gamma, eps)     # residual updated in place
     y = reduce_add_rms_norm(partials, residual, gamma, eps)   # partials: [R, ..., H]
+
+8-bit output (e4m3 / e5m2 codes with a per-tensor or per-row scale):
+
+    rms_norm_fp8(x, gamma, eps, out, scale, fmt="e4m3", scale_mode="tensor")
+    fused_add_rms_norm_fp8(x, residual, gamma, eps, out, scale, ...)
+    reduce_add_rms_norm_fp8(partials, residual, gamma, eps, out, scale, ...)
 """
 from __future__ import annotations
 
@@ -20,7 +26,9 @@ import os
 __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_host",
            "fused_add_rms_norm_host", "reduce_add_rms_norm_host", "RarnError", "library",
            "set_path", "get_path", "set_pdl", "get_pdl", "plan", "watchdog", "PATHS",
-           "DTYPE_CODES", "rms_norm_ex", "fused_add_rms_norm_ex", "reduce_add_rms_norm_ex"]
+           "DTYPE_CODES", "rms_norm_ex", "fused_add_rms_norm_ex", "reduce_add_rms_norm_ex",
+           "rms_norm_fp8", "fused_add_rms_norm_fp8", "reduce_add_rms_norm_fp8", "plan_fp8",
+           "FP8_FORMATS", "SCALE_MODES"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
@@ -28,6 +36,8 @@ LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
 DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
 OP_CODES = {"rms_norm": 0, "fused_add_rms_norm": 1, "reduce_add_rms_norm": 2}
 PATHS = {"auto": 0, "rows": 1, "stream": 2, "cluster": 3}
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
+SCALE_MODES = {"tensor": 0, "row": 1}
 STATUS = {0: "RARN_OK", 1: "RARN_ERR_INVALID_ARG", 2: "RARN_ERR_UNSUPPORTED",
           3: "RARN_ERR_ALIAS", 4: "RARN_ERR_CUDA"}
 
@@ -48,6 +58,14 @@ class Rows(ctypes.Structure):
     """``rarn_rows``: data pointer, row stride in elements, storage type."""
     _fields_ = [("data", ctypes.c_void_p), ("row_stride", ctypes.c_int64),
                 ("dtype", ctypes.c_int)]
+
+
+class Fp8Rows(ctypes.Structure):
+    """``rarn_fp8_rows``: code matrix (row stride in bytes), format, scale
+    mode and the scale's device pointer."""
+    _fields_ = [("data", ctypes.c_void_p), ("row_stride", ctypes.c_int64),
+                ("format", ctypes.c_int), ("scale_mode", ctypes.c_int),
+                ("scale", ctypes.c_void_p)]
 
 
 _lib = None
@@ -101,6 +119,16 @@ def library() -> ctypes.CDLL:
     lib.rarn_plan_ex.argtypes = [c_int, i64, i64, i32, c_int, c_int, c_int, c_int,
                                  ctypes.c_char_p, ctypes.c_size_t]
     lib.rarn_plan_ex.restype = c_int
+    fp = ctypes.POINTER(Fp8Rows)
+    lib.rarn_rms_norm_fp8.argtypes = [fp, Rows, vp, i64, i64, f32, vp]
+    lib.rarn_fused_add_rms_norm_fp8.argtypes = [fp, Rows, Rows, vp, i64, i64, f32, vp]
+    lib.rarn_reduce_add_rms_norm_fp8.argtypes = [fp, Rows, i64, i32, Rows, vp, i64, i64, f32, vp]
+    for f in (lib.rarn_rms_norm_fp8, lib.rarn_fused_add_rms_norm_fp8,
+              lib.rarn_reduce_add_rms_norm_fp8):
+        f.restype = c_int
+    lib.rarn_plan_fp8.argtypes = [c_int, i64, i64, i32, c_int, c_int, c_int, ctypes.c_char_p,
+                                  ctypes.c_size_t]
+    lib.rarn_plan_fp8.restype = c_int
     lib.rarn_set_pdl.argtypes = [c_int]
     lib.rarn_set_pdl.restype = c_int
     lib.rarn_get_pdl.argtypes = []
@@ -359,6 +387,97 @@ def reduce_add_rms_norm_ex(partials, residual, gamma, eps: float, out):
             _rows("out", out, dev), pr, partials.stride(0), R, _rows("residual", residual, dev),
             gamma.data_ptr(), T, H, float(eps), _stream(dev)), "rarn_reduce_add_rms_norm_ex")
     return out
+
+
+def _fp8_out(out, scale, fmt, scale_mode, T, H, device):
+    """The rarn_fp8_rows of an 8-bit output: ``out`` is a 2-D [T, H] view
+    (unit stride within a row) of uint8 or a torch float8 type (whose format
+    must then match ``fmt``); ``scale`` a float32 CUDA tensor of 1 (per
+    tensor) or T (per row, contiguous) values."""
+    import torch
+    f8 = {torch.float8_e4m3fn: "e4m3", torch.float8_e5m2: "e5m2"}
+    if out.dtype in f8:
+        if f8[out.dtype] != fmt:
+            raise ValueError(f"out is {out.dtype} but fmt is {fmt}")
+    elif out.dtype != torch.uint8:
+        raise TypeError("out must be uint8 or a float8 tensor")
+    if not out.is_cuda or out.device != device:
+        raise ValueError(f"out must be a CUDA tensor on {device}")
+    if tuple(out.shape) != (T, H) or out.stride(1) != 1 or (T > 1 and out.stride(0) < H):
+        raise ValueError("out must be [T, H] with unit stride within a row")
+    n = 1 if scale_mode == "tensor" else T
+    if (not scale.is_cuda or scale.device != device or scale.dtype != torch.float32 or
+            scale.numel() != n or (n > 1 and scale.stride(0) != 1)):
+        raise ValueError(f"scale must be a contiguous float32 CUDA tensor of {n} values")
+    return Fp8Rows(out.data_ptr(), out.stride(0) if T > 1 else H, FP8_FORMATS[fmt],
+                   SCALE_MODES[scale_mode], scale.data_ptr())
+
+
+def rms_norm_fp8(x, gamma, eps: float, out, scale, fmt: str = "e4m3",
+                 scale_mode: str = "tensor"):
+    """RMSNorm with an 8-bit output: out[t, i] = code of v / s, v = x_i /
+    RMS(x) * gamma_i, s = scale[0] (per tensor) or max|v| / maxf written to
+    scale[t] (per row).  x: 2-D row-strided view."""
+    import torch
+    T, H = x.shape
+    _check_tensor("gamma", gamma, x.dtype, x.device)
+    if gamma.numel() != H:
+        raise ValueError("shape mismatch")
+    d = _fp8_out(out, scale, fmt, scale_mode, T, H, x.device)
+    with torch.cuda.device(x.device):
+        _check(library().rarn_rms_norm_fp8(ctypes.byref(d), _rows("x", x, x.device),
+                                           gamma.data_ptr(), T, H, float(eps),
+                                           _stream(x.device)), "rarn_rms_norm_fp8")
+    return out
+
+
+def fused_add_rms_norm_fp8(x, residual, gamma, eps: float, out, scale, fmt: str = "e4m3",
+                           scale_mode: str = "tensor"):
+    """fused_add_rms_norm with an 8-bit output (residual updated in place, of
+    x's type)."""
+    import torch
+    T, H = x.shape
+    _check_tensor("gamma", gamma, x.dtype, x.device)
+    if gamma.numel() != H or tuple(residual.shape) != (T, H):
+        raise ValueError("shape mismatch")
+    d = _fp8_out(out, scale, fmt, scale_mode, T, H, x.device)
+    with torch.cuda.device(x.device):
+        _check(library().rarn_fused_add_rms_norm_fp8(
+            ctypes.byref(d), _rows("x", x, x.device), _rows("residual", residual, x.device),
+            gamma.data_ptr(), T, H, float(eps), _stream(x.device)), "rarn_fused_add_rms_norm_fp8")
+    return out
+
+
+def reduce_add_rms_norm_fp8(partials, residual, gamma, eps: float, out, scale,
+                            fmt: str = "e4m3", scale_mode: str = "tensor"):
+    """reduce_add_rms_norm with an 8-bit output: partials [R, T, H] with unit
+    stride within a row (any row / partial strides)."""
+    import torch
+    R, T, H = partials.shape
+    dev = partials.device
+    if not partials.is_cuda or partials.stride(2) != 1 or partials.stride(1) < H:
+        raise ValueError("partials must be [R, T, H] with unit stride within a row")
+    _check_tensor("gamma", gamma, partials.dtype, dev)
+    if gamma.numel() != H or tuple(residual.shape) != (T, H):
+        raise ValueError("shape mismatch")
+    d = _fp8_out(out, scale, fmt, scale_mode, T, H, dev)
+    pr = Rows(partials.data_ptr(), partials.stride(1), _dtype_code(partials))
+    with torch.cuda.device(dev):
+        _check(library().rarn_reduce_add_rms_norm_fp8(
+            ctypes.byref(d), pr, partials.stride(0), R, _rows("residual", residual, dev),
+            gamma.data_ptr(), T, H, float(eps), _stream(dev)), "rarn_reduce_add_rms_norm_fp8")
+    return out
+
+
+def plan_fp8(op: str, T: int, H: int, R: int, dtype: str, vec_ok: bool = True,
+             num_sms: int = 0) -> str:
+    """The kernel the current path setting would launch for an 8-bit output."""
+    buf = ctypes.create_string_buffer(256)
+    st = library().rarn_plan_fp8(OP_CODES[op], T, H, R, DTYPE_CODES[dtype], int(vec_ok),
+                                 num_sms, buf, 256)
+    if st not in (0, 2):
+        _check(st, "rarn_plan_fp8")
+    return buf.value.decode()
 
 
 def set_pdl(enable: bool) -> None:

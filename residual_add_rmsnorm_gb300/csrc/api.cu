@@ -278,10 +278,15 @@ Plan plan_auto(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_sms
 }
 
 // rn: residual words per pack (2 for a binary32 residual with 16-bit
-// inputs: register and cluster kernels only).
+// inputs: register and cluster kernels only).  q8: 8-bit output, built for
+// the register row kernels only (warp, CTA, pipelined, two-pass).
 Plan make_plan(int op, int64_t T, int64_t H, int R, rarn_dtype dt, bool vec, int num_sms,
-               int max_smem, int path, int rn = 1) {
+               int max_smem, int path, int rn = 1, bool q8 = false) {
     const int s = elem_size(dt);
+    if (q8) {
+        if (rn != 1 || (path != RARN_PATH_AUTO && path != RARN_PATH_ROWS)) return Plan{};
+        return plan_rows(op, T, H, s, vec, num_sms, 1);
+    }
     switch (path) {
     case RARN_PATH_ROWS: return plan_rows(op, T, H, s, vec, num_sms, rn);
     case RARN_PATH_STREAM:
@@ -360,6 +365,11 @@ struct Call {
     rarn_dtype rdt = RARN_F32;  // residual
     void *stream = nullptr;
     bool host_buffers = false;
+    // 8-bit output: y holds codes (ldy in bytes)
+    bool q8 = false;
+    int qfmt = 0;
+    int qmode = 0;
+    float *qscale = nullptr;
 };
 
 bool dtype_ok(rarn_dtype d) { return d == RARN_F32 || d == RARN_F16 || d == RARN_BF16; }
@@ -382,17 +392,26 @@ rarn_status run_ex(Call c) {
     if (mixed && !(c.rdt == RARN_F32 && (c.dt == RARN_F16 || c.dt == RARN_BF16)))
         return RARN_ERR_UNSUPPORTED;
     if (op == OP_PLAIN) c.rdt = c.dt;
+    if (c.q8) {
+        if ((c.qfmt != Q_E4M3 && c.qfmt != Q_E5M2) || (c.qmode != Q_TENSOR && c.qmode != Q_ROW) ||
+            !c.qscale || c.host_buffers)
+            return RARN_ERR_INVALID_ARG;
+        if (mixed) return RARN_ERR_UNSUPPORTED;
+        const int path = g_path.load();
+        if (path == RARN_PATH_STREAM || path == RARN_PATH_CLUSTER) return RARN_ERR_UNSUPPORTED;
+    }
 
     const int s = elem_size(c.dt), rs = elem_size(c.rdt);
+    const int ys = c.q8 ? 1 : s;  // bytes per element of y
     const int64_t row_bytes = c.H * s;
     const int nsrc = op == OP_REDUCE ? c.R : 1;
-    const int64_t ybytes = span_bytes(c.T, c.H, c.ldy, s);
+    const int64_t ybytes = span_bytes(c.T, c.H, c.ldy, ys);
     const int64_t xbytes = span_bytes(c.T, c.H, c.ldx, s);
     const int64_t srcbytes = (int64_t)(nsrc - 1) * c.slice * s + xbytes;
     const int64_t rbytes = op != OP_PLAIN ? span_bytes(c.T, c.H, c.ldr, rs) : 0;
     // y may coincide exactly with x / partial 0 (same row stride); nothing
     // else may overlap an output (overlaps are judged on the row spans)
-    const bool y_is_src = c.y == c.src && c.ldy == c.ldx;
+    const bool y_is_src = !c.q8 && c.y == c.src && c.ldy == c.ldx;
     if (!y_is_src && overlaps(c.y, ybytes, c.src, srcbytes)) return RARN_ERR_ALIAS;
     if (y_is_src && nsrc > 1 &&
         overlaps(c.y, ybytes, static_cast<const char *>(c.src) + c.slice * s,
@@ -403,6 +422,17 @@ rarn_status run_ex(Call c) {
         if (overlaps(c.residual, rbytes, c.y, ybytes) ||
             overlaps(c.residual, rbytes, c.src, srcbytes) ||
             overlaps(c.residual, rbytes, c.gamma, row_bytes))
+            return RARN_ERR_ALIAS;
+    }
+    if (c.q8) {
+        // the scale (one value read, or T values written) overlaps no output,
+        // and a written scale no input either
+        const int64_t qbytes = c.qmode == Q_ROW ? c.T * 4 : 4;
+        if (overlaps(c.qscale, qbytes, c.y, ybytes) ||
+            (op != OP_PLAIN && overlaps(c.qscale, qbytes, c.residual, rbytes)))
+            return RARN_ERR_ALIAS;
+        if (c.qmode == Q_ROW && (overlaps(c.qscale, qbytes, c.src, srcbytes) ||
+                                 overlaps(c.qscale, qbytes, c.gamma, row_bytes)))
             return RARN_ERR_ALIAS;
     }
 
@@ -432,8 +462,11 @@ rarn_status run_ex(Call c) {
         c.residual = vr;
     }
 
-    const bool vec = aligned16(c.y) && aligned16(c.src) && aligned16(c.gamma) &&
-                     (c.ldx * s) % 16 == 0 && (c.ldy * s) % 16 == 0 && row_bytes % 16 == 0 &&
+    // 16-byte packs: one pack of EPV = 16 / s inputs gives EPV bytes of codes
+    const int yalign = c.q8 ? 16 / s : 16;
+    const bool y_ok = reinterpret_cast<uintptr_t>(c.y) % yalign == 0 && (c.ldy * ys) % yalign == 0;
+    const bool vec = y_ok && aligned16(c.src) && aligned16(c.gamma) &&
+                     (c.ldx * s) % 16 == 0 && row_bytes % 16 == 0 &&
                      (nsrc == 1 || (c.slice * s) % 16 == 0) &&
                      (op == OP_PLAIN || (aligned16(c.residual) && (c.ldr * rs) % 16 == 0));
     const int rn = mixed ? 2 : 1;
@@ -442,7 +475,8 @@ rarn_status run_ex(Call c) {
     // over the host link than the single-producer stream kernel (measured).
     const int path = c.host_buffers && g_path.load() == RARN_PATH_AUTO ? RARN_PATH_ROWS
                                                                        : g_path.load();
-    Plan pl = make_plan(op, c.T, c.H, c.R, c.dt, vec, d->num_sms, d->max_smem_optin, path, rn);
+    Plan pl =
+        make_plan(op, c.T, c.H, c.R, c.dt, vec, d->num_sms, d->max_smem_optin, path, rn, c.q8);
     if (c.host_buffers && path == RARN_PATH_ROWS && pl.kind == KIND_TWO_PASS && vec) {
         const Plan cl = plan_cluster(op, c.T, c.H, s, vec, d->num_sms, rn);
         if (cl.kind != KIND_NONE) pl = cl;
@@ -466,6 +500,9 @@ rarn_status run_ex(Call c) {
     p.watchdog = d->watchdog;
     p.wait_limit_ns = stream::kWaitLimitNs;
     p.stall_fill = -1;
+    p.qscale = c.qscale;
+    p.qfmt = c.qfmt;
+    p.qmode = c.qmode;
     if (pl.kind == KIND_STREAM) {
         const long long f = g_stall_fill.exchange(-1);
         if (f >= 0) {
@@ -481,7 +518,15 @@ rarn_status run_ex(Call c) {
     const int F32F32 = RARN_F32 * 4 + RARN_F32, F16F16 = RARN_F16 * 4 + RARN_F16,
               BF16BF16 = RARN_BF16 * 4 + RARN_BF16, F16F32 = RARN_F16 * 4 + RARN_F32,
               BF16F32 = RARN_BF16 * 4 + RARN_F32;
-    switch (pl.kind) {
+    switch (c.q8 ? -pl.kind : pl.kind) {
+    case -KIND_WARP:
+    case -KIND_CTA:
+    case -KIND_TWO_PASS:
+        if (key == F32F32) e = launch_rows_q8<float>(p, pl, cs);
+        else if (key == F16F16) e = launch_rows_q8<__half>(p, pl, cs);
+        else if (key == BF16BF16) e = launch_rows_q8<__nv_bfloat16>(p, pl, cs);
+        else return RARN_ERR_UNSUPPORTED;
+        break;
     case KIND_WARP:
     case KIND_CTA:
     case KIND_TWO_PASS:
@@ -638,6 +683,78 @@ rarn_status rarn_reduce_add_rms_norm_ex(rarn_rows y, rarn_rows partials, int64_t
     return run_ex(c);
 }
 
+// 8-bit output forms: the general forms with y replaced by a code matrix.
+static bool fp8_desc(const rarn_fp8_rows *y, Call &c) {
+    if (!y) return false;
+    c.q8 = true;
+    c.y = y->data;
+    c.ldy = y->row_stride;
+    c.qfmt = (int)y->format;
+    c.qmode = (int)y->scale_mode;
+    c.qscale = y->scale;
+    return true;
+}
+
+rarn_status rarn_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows x, const void *gamma, int64_t T,
+                              int64_t H, float eps, void *stream) {
+    Call c;
+    if (!fp8_desc(y, c)) return RARN_ERR_INVALID_ARG;
+    c.op = OP_PLAIN;
+    c.src = x.data;
+    c.ldx = x.row_stride;
+    c.gamma = gamma;
+    c.T = T;
+    c.H = H;
+    c.eps = eps;
+    c.dt = c.rdt = x.dtype;
+    c.stream = stream;
+    return run_ex(c);
+}
+
+rarn_status rarn_fused_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows x, rarn_rows residual,
+                                        const void *gamma, int64_t T, int64_t H, float eps,
+                                        void *stream) {
+    Call c;
+    if (!fp8_desc(y, c)) return RARN_ERR_INVALID_ARG;
+    c.op = OP_FUSED;
+    c.src = x.data;
+    c.ldx = x.row_stride;
+    c.R = 1;
+    c.residual = residual.data;
+    c.ldr = residual.row_stride;
+    c.gamma = gamma;
+    c.T = T;
+    c.H = H;
+    c.eps = eps;
+    c.dt = x.dtype;
+    c.rdt = residual.dtype;
+    c.stream = stream;
+    return run_ex(c);
+}
+
+rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows partials,
+                                         int64_t partial_stride, int32_t R, rarn_rows residual,
+                                         const void *gamma, int64_t T, int64_t H, float eps,
+                                         void *stream) {
+    Call c;
+    if (!fp8_desc(y, c)) return RARN_ERR_INVALID_ARG;
+    c.op = OP_REDUCE;
+    c.src = partials.data;
+    c.ldx = partials.row_stride;
+    c.slice = partial_stride;
+    c.R = R;
+    c.residual = residual.data;
+    c.ldr = residual.row_stride;
+    c.gamma = gamma;
+    c.T = T;
+    c.H = H;
+    c.eps = eps;
+    c.dt = partials.dtype;
+    c.rdt = residual.dtype;
+    c.stream = stream;
+    return run_ex(c);
+}
+
 const char *rarn_status_string(rarn_status s) {
     switch (s) {
     case RARN_OK: return "ok";
@@ -679,15 +796,16 @@ rarn_status rarn_plan(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt
     return rarn_plan_ex(op, T, H, R, dt, dt, vec_ok, num_sms, out, cap);
 }
 
-rarn_status rarn_plan_ex(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt,
-                         rarn_dtype rdt, int vec_ok, int num_sms, char *out, size_t cap) {
+static rarn_status plan_text(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt,
+                             rarn_dtype rdt, int vec_ok, int num_sms, char *out, size_t cap,
+                             bool q8) {
     if (!out || cap == 0) return RARN_ERR_INVALID_ARG;
     if (op < RARN_OP_RMS_NORM || op > RARN_OP_REDUCE_ADD_RMS_NORM) return RARN_ERR_INVALID_ARG;
     if (!dtype_ok(dt) || !dtype_ok(rdt)) return RARN_ERR_INVALID_ARG;
     if (T < 0 || H <= 0 || (op == RARN_OP_REDUCE_ADD_RMS_NORM && R < 1))
         return RARN_ERR_INVALID_ARG;
     const bool mixed = op != RARN_OP_RMS_NORM && rdt != dt;
-    if (mixed && !(rdt == RARN_F32 && (dt == RARN_F16 || dt == RARN_BF16))) {
+    if (mixed && (q8 || !(rdt == RARN_F32 && (dt == RARN_F16 || dt == RARN_BF16)))) {
         snprintf(out, cap, "none: unsupported storage types");
         return RARN_ERR_UNSUPPORTED;
     }
@@ -700,8 +818,8 @@ rarn_status rarn_plan_ex(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype
         max_smem = d->max_smem_optin;
     }
     const bool vec = vec_ok && (H * elem_size(dt)) % 16 == 0;
-    const Plan pl =
-        make_plan((int)op, T, H, R, dt, vec, num_sms, max_smem, g_path.load(), mixed ? 2 : 1);
+    const Plan pl = make_plan((int)op, T, H, R, dt, vec, num_sms, max_smem, g_path.load(),
+                              mixed ? 2 : 1, q8);
     snprintf(out, cap,
              "%s %s per_thread=%d block=%d grid=%d cluster=%d smem=%d stages=%d chunk=%d "
              "groups=%d gamma_regs=%d pipe=%d",
@@ -709,6 +827,16 @@ rarn_status rarn_plan_ex(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype
              pl.cluster, pl.smem, pl.stages, pl.chunk, pl.groups, (int)pl.prefetch_gamma,
              (int)pl.pipe);
     return pl.kind == KIND_NONE ? RARN_ERR_UNSUPPORTED : RARN_OK;
+}
+
+rarn_status rarn_plan_ex(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt,
+                         rarn_dtype rdt, int vec_ok, int num_sms, char *out, size_t cap) {
+    return plan_text(op, T, H, R, dt, rdt, vec_ok, num_sms, out, cap, false);
+}
+
+rarn_status rarn_plan_fp8(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtype dt, int vec_ok,
+                          int num_sms, char *out, size_t cap) {
+    return plan_text(op, T, H, R, dt, dt, vec_ok, num_sms, out, cap, true);
 }
 
 rarn_status rarn_watchdog(uint32_t *flags, int clear) {
@@ -737,6 +865,6 @@ int rarn_host_access(void) {
     return pageable ? 2 : (mapped ? 1 : 0);
 }
 
-int rarn_version(void) { return (1 << 16) | 0; }
+int rarn_version(void) { return (1 << 16) | 1; }
 
 }  // extern "C"

@@ -8,12 +8,17 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace rarn {
 
 enum Op : int { OP_PLAIN = 0, OP_FUSED = 1, OP_REDUCE = 2 };
+
+// 8-bit output: code format and where its scale comes from.
+enum QFormat : int { Q_E4M3 = 0, Q_E5M2 = 1 };
+enum QMode : int { Q_TENSOR = 0, Q_ROW = 1 };
 
 // One call's arguments, passed to every kernel by value.  Strides are in
 // elements of each buffer's own storage type.
@@ -34,6 +39,10 @@ struct Problem {
     unsigned long long wait_limit_ns;  // bound on every shared-memory barrier wait
     long long stall_fill;    // test hook: in CTA 0 of the stream kernel this fill never
                              // completes (-1: never), so that its consumers' wait runs out
+    // 8-bit output (kernels built for it): y holds one-byte codes, ldy in bytes
+    float *qscale;           // Q_TENSOR: the one scale (read); Q_ROW: [T] scales (written)
+    int qfmt;                // QFormat
+    int qmode;               // QMode
 };
 
 // ---------------------------------------------------------------------------
@@ -211,6 +220,12 @@ __device__ __forceinline__ float warp_sum(float v) {
     return v;
 }
 
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int m = 16; m > 0; m >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, m));
+    return v;
+}
+
 // Sum of v over the whole CTA, returned to every thread.  `red` holds one
 // float per warp; callers alternate between two such buffers on consecutive
 // rows so that one __syncthreads per row suffices.  Deterministic: fixed
@@ -223,6 +238,73 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
     __syncthreads();
     float s = lane < nwarps ? red[lane] : 0.f;
     return warp_sum(s);
+}
+
+// Maximum of v over the whole CTA, returned to every thread (same scheme and
+// buffer discipline as block_sum).
+__device__ __forceinline__ float block_max(float v, float *red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = (blockDim.x + 31) >> 5;
+    v = warp_max(v);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float s = lane < nwarps ? red[lane] : 0.f;
+    return warp_max(s);
+}
+
+// ---------------------------------------------------------------------------
+// 8-bit output.  A value v becomes the code of u = (v * m1) * m2, rounded to
+// nearest even and saturated to the format's largest finite value:
+//   per tensor: m1 = 1 / scale, m2 = 1;
+//   per row:    m1 = 1 / max|v|, m2 = maxf (448 for e4m3, 57344 for e5m2), so
+//               the row's largest magnitude maps to maxf; the row's scale
+//               max|v| / maxf is written out (1 and m1 = m2 = 1 for a row of
+//               zeros).
+// ("Block All Reduce", FP8 section: e4m3 and e5m2 codes, converted with
+// saturation to the largest finite value.)
+// ---------------------------------------------------------------------------
+struct QMul {
+    float m1, m2;
+};
+
+__device__ __forceinline__ float q_maxf(int fmt) { return fmt == Q_E5M2 ? 57344.f : 448.f; }
+
+// Per-tensor multipliers; the scale is read after the grid dependency wait.
+__device__ __forceinline__ QMul quant_tensor(const Problem &p) {
+    return p.qmode == Q_TENSOR ? QMul{1.f / *p.qscale, 1.f} : QMul{1.f, 1.f};
+}
+
+// Per-row multipliers from the row's reduced max|v|; `writer` stores the scale.
+// A subnormal max|v| is scaled by 2^24 first (exact), so that its reciprocal
+// stays finite.
+__device__ __forceinline__ QMul quant_row(const Problem &p, int64_t t, float amax, bool writer) {
+    const float maxf = q_maxf(p.qfmt);
+    if (writer) p.qscale[t] = amax > 0.f ? amax / maxf : 1.f;
+    if (!(amax > 0.f)) return QMul{1.f, 1.f};
+    const float k = amax < 1.17549435e-38f ? 16777216.f : 1.f;
+    return QMul{1.f / (amax * k), maxf * k};
+}
+
+__device__ __forceinline__ uint32_t fp8x2(float a, float b, int fmt) {
+    return __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE,
+                                    fmt == Q_E5M2 ? __NV_E5M2 : __NV_E4M3);
+}
+
+__device__ __forceinline__ uint8_t fp8x1(float a, int fmt) {
+    return __nv_cvt_float_to_fp8(a, __NV_SATFINITE, fmt == Q_E5M2 ? __NV_E5M2 : __NV_E4M3);
+}
+
+// Store the codes of N = 4 or 8 values (element 0 at the lowest address).
+template <int N>
+__device__ __forceinline__ void st_codes(uint8_t *dst, const float (&u)[N], int fmt) {
+    static_assert(N == 4 || N == 8, "4 or 8 codes per store");
+    const uint32_t w0 = fp8x2(u[0], u[1], fmt) | (fp8x2(u[2], u[3], fmt) << 16);
+    if constexpr (N == 4) {
+        asm volatile("st.global.u32 [%0], %1;" ::"l"(dst), "r"(w0) : "memory");
+    } else {
+        const uint32_t w1 = fp8x2(u[4], u[5], fmt) | (fp8x2(u[6], u[7], fmt) << 16);
+        asm volatile("st.global.v2.u32 [%0], {%1,%2};" ::"l"(dst), "r"(w0), "r"(w1) : "memory");
+    }
 }
 
 }  // namespace rarn

@@ -111,6 +111,9 @@ __host__ __device__ inline Layout layout(int stages, int ns, int row_bytes, int 
 // a 16-bit T (register and cluster kernels only).
 template <typename T, typename TR>
 cudaError_t launch_rows(const Problem &p, const Plan &plan, cudaStream_t stream);
+// Register row kernels with an 8-bit output (residual of type T).
+template <typename T>
+cudaError_t launch_rows_q8(const Problem &p, const Plan &plan, cudaStream_t stream);
 template <typename T>
 cudaError_t launch_stream(const Problem &p, const Plan &plan, cudaStream_t stream);
 template <typename T, typename TR>

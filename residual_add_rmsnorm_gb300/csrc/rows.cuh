@@ -233,13 +233,14 @@ __device__ __forceinline__ void load_gamma_vec(const Problem &p, int j0, int js,
 
 // Pass 2, 16-byte packs: y = (h * inv) * gamma, one rounding.  With PG the
 // gamma packs come from registers (gv), otherwise from memory (L1 / L2).
-template <typename T, int VPT, typename TR, bool PG = false>
+// Q8: y holds 8-bit codes of ((h * inv) * gamma * m1) * m2 instead (EPV bytes
+// per pack).
+template <typename T, int VPT, typename TR, bool PG = false, bool Q8 = false>
 __device__ __forceinline__ void pass2_vec(const Problem &p, int64_t t, int j0, int js, int nv,
                                           const uint4 (&hv)[VPT][Res<T, TR>::N], float inv,
-                                          const uint4 *gv = nullptr) {
+                                          const uint4 *gv = nullptr, QMul qm = QMul{1.f, 1.f}) {
     constexpr int EPV = DT<T>::EPV;
     const T *g = reinterpret_cast<const T *>(p.gamma);
-    T *y = reinterpret_cast<T *>(p.y) + t * p.ldy;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int j = j0 + k * js;
@@ -249,9 +250,40 @@ __device__ __forceinline__ void pass2_vec(const Problem &p, int64_t t, int j0, i
             DT<T>::unpack(PG ? gv[k] : ld_keep(g + (int64_t)j * EPV), w);
 #pragma unroll
             for (int e = 0; e < EPV; ++e) h[e] = (h[e] * inv) * w[e];
-            st_global(y + (int64_t)j * EPV, DT<T>::pack(h));
+            if constexpr (Q8) {
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) h[e] = (h[e] * qm.m1) * qm.m2;
+                st_codes<EPV>(reinterpret_cast<uint8_t *>(p.y) + t * p.ldy + (int64_t)j * EPV, h,
+                              p.qfmt);
+            } else {
+                st_global(reinterpret_cast<T *>(p.y) + t * p.ldy + (int64_t)j * EPV,
+                          DT<T>::pack(h));
+            }
         }
     }
+}
+
+// Per-row scale: this thread's max |(h * inv) * gamma| over its packs -- the
+// same products pass2_vec converts.
+template <typename T, int VPT, typename TR, bool PG>
+__device__ __forceinline__ float amax_vec(const Problem &p, int j0, int js, int nv,
+                                          const uint4 (&hv)[VPT][Res<T, TR>::N], float inv,
+                                          const uint4 *gv) {
+    constexpr int EPV = DT<T>::EPV;
+    const T *g = reinterpret_cast<const T *>(p.gamma);
+    float m = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = j0 + k * js;
+        if (j < nv) {
+            float h[EPV], w[EPV];
+            Res<T, TR>::to_f(hv[k], h);
+            DT<T>::unpack(PG ? gv[k] : ld_keep(g + (int64_t)j * EPV), w);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) m = fmaxf(m, fabsf((h[e] * inv) * w[e]));
+        }
+    }
+    return m;
 }
 
 // ---------------------------------------------------------------------------
@@ -320,17 +352,38 @@ __device__ __forceinline__ float pass1_scalar(const Problem &p, int64_t t, int i
     }
 }
 
-template <typename T, int NE>
+template <typename T, int NE, bool Q8 = false>
 __device__ __forceinline__ void pass2_scalar(const Problem &p, int64_t t, int i0, int is,
-                                             const float (&h)[NE], float inv) {
+                                             const float (&h)[NE], float inv,
+                                             QMul qm = QMul{1.f, 1.f}) {
     const T *g = reinterpret_cast<const T *>(p.gamma);
-    T *y = reinterpret_cast<T *>(p.y) + t * p.ldy;
     const int H = (int)p.H;
 #pragma unroll
     for (int k = 0; k < NE; ++k) {
         const int i = i0 + k * is;
-        if (i < H) y[i] = DT<T>::from_f((h[k] * inv) * DT<T>::to_f(g[i]));
+        if (i < H) {
+            const float v = (h[k] * inv) * DT<T>::to_f(g[i]);
+            if constexpr (Q8)
+                reinterpret_cast<uint8_t *>(p.y)[t * p.ldy + i] =
+                    fp8x1((v * qm.m1) * qm.m2, p.qfmt);
+            else
+                reinterpret_cast<T *>(p.y)[t * p.ldy + i] = DT<T>::from_f(v);
+        }
     }
+}
+
+template <typename T, int NE>
+__device__ __forceinline__ float amax_scalar(const Problem &p, int i0, int is,
+                                             const float (&h)[NE], float inv) {
+    const T *g = reinterpret_cast<const T *>(p.gamma);
+    const int H = (int)p.H;
+    float m = 0.f;
+#pragma unroll
+    for (int k = 0; k < NE; ++k) {
+        const int i = i0 + k * is;
+        if (i < H) m = fmaxf(m, fabsf((h[k] * inv) * DT<T>::to_f(g[i])));
+    }
+    return m;
 }
 
 // CTA size each register-staged kernel is compiled for (plan.h budget); a
@@ -352,12 +405,16 @@ struct ScalarBound {
 // Kernels
 // ---------------------------------------------------------------------------
 
-// One CTA per row, packs.  PG: gamma held in registers for all rows.
-template <typename T, int VPT, int OP, bool PG, typename TR>
+// One CTA per row, packs.  PG: gamma held in registers for all rows.  Q8:
+// 8-bit output; a per-row scale takes a second CTA reduction (max |v|).
+template <typename T, int VPT, int OP, bool PG, typename TR, bool Q8>
 __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG, TR>::value) k_cta_vec(Problem p) {
     __shared__ float red[2][32];
+    __shared__ float redm[Q8 ? 64 : 1];
     const int nv = (int)(p.H / DT<T>::EPV);
     grid_dependency_wait();
+    QMul qm{1.f, 1.f};
+    if constexpr (Q8) qm = quant_tensor(p);
     uint4 gv[VPT];
     if (PG) load_gamma_vec<T, VPT>(p, threadIdx.x, blockDim.x, nv, gv);
     int par = 0;
@@ -367,7 +424,13 @@ __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG, TR>::value) k_cta_vec
         const float ss = pass1_vec<T, VPT, OP, TR>(p, t, threadIdx.x, blockDim.x, nv, hv);
         const float tot = block_sum(ss, red[par]);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_vec<T, VPT, TR, PG>(p, t, threadIdx.x, blockDim.x, nv, hv, inv, gv);
+        if constexpr (Q8) {
+            if (p.qmode == Q_ROW) {
+                const float a = amax_vec<T, VPT, TR, PG>(p, threadIdx.x, blockDim.x, nv, hv, inv, gv);
+                qm = quant_row(p, t, block_max(a, redm + 32 * par), threadIdx.x == 0);
+            }
+        }
+        pass2_vec<T, VPT, TR, PG, Q8>(p, t, threadIdx.x, blockDim.x, nv, hv, inv, gv, qm);
     }
 }
 
@@ -447,11 +510,14 @@ struct PipeBound {
     static constexpr int value = b > 0 ? b : 128;
 };
 
-template <typename T, int VPT, int OP, typename TR>
+template <typename T, int VPT, int OP, typename TR, bool Q8>
 __global__ void __launch_bounds__(PipeBound<T, VPT, OP, TR>::value) k_cta_pipe(Problem p) {
     __shared__ float red[2][32];
+    __shared__ float redm[Q8 ? 64 : 1];
     const int nv = (int)(p.H / DT<T>::EPV);
     grid_dependency_wait();
+    QMul qm{1.f, 1.f};
+    if constexpr (Q8) qm = quant_tensor(p);
     RowLoads<T, VPT, OP, TR> next;
     int64_t t = blockIdx.x;
     if (t < p.T) issue_row_loads<T, VPT, OP, TR>(p, t, threadIdx.x, blockDim.x, nv, next);
@@ -468,13 +534,20 @@ __global__ void __launch_bounds__(PipeBound<T, VPT, OP, TR>::value) k_cta_pipe(P
             consume_row_loads<T, VPT, OP, TR>(p, t, threadIdx.x, blockDim.x, nv, cur, hv);
         const float tot = block_sum(ss, red[par]);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_vec<T, VPT, TR, false>(p, t, threadIdx.x, blockDim.x, nv, hv, inv);
+        if constexpr (Q8) {
+            if (p.qmode == Q_ROW) {
+                const float a =
+                    amax_vec<T, VPT, TR, false>(p, threadIdx.x, blockDim.x, nv, hv, inv, nullptr);
+                qm = quant_row(p, t, block_max(a, redm + 32 * par), threadIdx.x == 0);
+            }
+        }
+        pass2_vec<T, VPT, TR, false, Q8>(p, t, threadIdx.x, blockDim.x, nv, hv, inv, nullptr, qm);
     }
 }
 
 // One warp per row, packs; blockDim.x / 32 rows per CTA at a time.  Gamma is
 // held in registers (at most 4 packs per lane).
-template <typename T, int VPT, int OP, typename TR>
+template <typename T, int VPT, int OP, typename TR, bool Q8>
 __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
     const int nv = (int)(p.H / DT<T>::EPV);
     const int lane = threadIdx.x & 31;
@@ -482,6 +555,8 @@ __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
     const int64_t first = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     const int64_t step = (int64_t)gridDim.x * wpb;
     grid_dependency_wait();
+    QMul qm{1.f, 1.f};
+    if constexpr (Q8) qm = quant_tensor(p);
     uint4 gv[VPT];
     load_gamma_vec<T, VPT>(p, lane, 32, nv, gv);
     for (int64_t t = first; t < p.T; t += step) {
@@ -490,13 +565,18 @@ __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
         const float ss = pass1_vec<T, VPT, OP, TR>(p, t, lane, 32, nv, hv);
         const float tot = warp_sum(ss);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_vec<T, VPT, TR, true>(p, t, lane, 32, nv, hv, inv, gv);
+        if constexpr (Q8) {
+            if (p.qmode == Q_ROW)
+                qm = quant_row(p, t, warp_max(amax_vec<T, VPT, TR, true>(p, lane, 32, nv, hv, inv, gv)),
+                               lane == 0);
+        }
+        pass2_vec<T, VPT, TR, true, Q8>(p, t, lane, 32, nv, hv, inv, gv, qm);
     }
 }
 
 // One warp per row, pipelined like k_cta_pipe (plain and fused): the next
 // row's loads are in flight while this row is reduced and written.
-template <typename T, int VPT, int OP, typename TR>
+template <typename T, int VPT, int OP, typename TR, bool Q8>
 __global__ void __launch_bounds__(256) k_warp_pipe(Problem p) {
     const int nv = (int)(p.H / DT<T>::EPV);
     const int lane = threadIdx.x & 31;
@@ -504,6 +584,8 @@ __global__ void __launch_bounds__(256) k_warp_pipe(Problem p) {
     const int64_t first = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     const int64_t step = (int64_t)gridDim.x * wpb;
     grid_dependency_wait();
+    QMul qm{1.f, 1.f};
+    if constexpr (Q8) qm = quant_tensor(p);
     uint4 gv[VPT];
     load_gamma_vec<T, VPT>(p, lane, 32, nv, gv);
     RowLoads<T, VPT, OP, TR> next;
@@ -520,15 +602,23 @@ __global__ void __launch_bounds__(256) k_warp_pipe(Problem p) {
         const float ss = consume_row_loads<T, VPT, OP, TR>(p, t, lane, 32, nv, cur, hv);
         const float tot = warp_sum(ss);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_vec<T, VPT, TR, true>(p, t, lane, 32, nv, hv, inv, gv);
+        if constexpr (Q8) {
+            if (p.qmode == Q_ROW)
+                qm = quant_row(p, t, warp_max(amax_vec<T, VPT, TR, true>(p, lane, 32, nv, hv, inv, gv)),
+                               lane == 0);
+        }
+        pass2_vec<T, VPT, TR, true, Q8>(p, t, lane, 32, nv, hv, inv, gv, qm);
     }
 }
 
 // One CTA per row, single elements.
-template <typename T, int NE, int OP, typename TR>
+template <typename T, int NE, int OP, typename TR, bool Q8>
 __global__ void __launch_bounds__(ScalarBound<NE, OP>::value, 1) k_cta_scalar(Problem p) {
     __shared__ float red[2][32];
+    __shared__ float redm[Q8 ? 64 : 1];
     grid_dependency_wait();
+    QMul qm{1.f, 1.f};
+    if constexpr (Q8) qm = quant_tensor(p);
     int par = 0;
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
         if (t + gridDim.x >= p.T) grid_launch_dependents();
@@ -536,20 +626,50 @@ __global__ void __launch_bounds__(ScalarBound<NE, OP>::value, 1) k_cta_scalar(Pr
         const float ss = pass1_scalar<T, NE, OP, TR>(p, t, threadIdx.x, blockDim.x, h);
         const float tot = block_sum(ss, red[par]);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        pass2_scalar<T, NE>(p, t, threadIdx.x, blockDim.x, h, inv);
+        if constexpr (Q8) {
+            if (p.qmode == Q_ROW) {
+                const float a = amax_scalar<T, NE>(p, threadIdx.x, blockDim.x, h, inv);
+                qm = quant_row(p, t, block_max(a, redm + 32 * par), threadIdx.x == 0);
+            }
+        }
+        pass2_scalar<T, NE, Q8>(p, t, threadIdx.x, blockDim.x, h, inv, qm);
     }
+}
+
+// The stored row (the residual, or x for the plain form): pack or element j.
+template <typename T, int OP, typename TR>
+__device__ __forceinline__ void reload_vec(const Problem &p, int64_t t, int j,
+                                           uint4 (&hv)[1][Res<T, TR>::N]) {
+    using RS = Res<T, TR>;
+    constexpr int EPV = DT<T>::EPV;
+    if constexpr (OP == OP_PLAIN) {
+        hv[0][0] = ld_stream(reinterpret_cast<const T *>(p.src) + t * p.ldx + (int64_t)j * EPV);
+    } else {
+        const TR *res = reinterpret_cast<const TR *>(p.residual) + t * p.ldr;
+#pragma unroll
+        for (int q = 0; q < RS::N; ++q) hv[0][q] = ld_stream(res + (int64_t)j * EPV + q * RS::EPW);
+    }
+}
+
+template <typename T, int OP, typename TR>
+__device__ __forceinline__ float reload_scalar(const Problem &p, int64_t t, int j) {
+    return OP == OP_PLAIN ? ld_elem<T>(p.src, t * p.ldx + j) : ld_elem<TR>(p.residual, t * p.ldr + j);
 }
 
 // Rows too long for registers: pass 1 walks the row in tiles of blockDim
 // packs (or elements); pass 2 re-reads the stored row (the residual, or x for
-// the plain form) -- each thread re-reads only what it wrote itself.
-template <typename T, int OP, bool VEC, typename TR>
+// the plain form) -- each thread re-reads only what it wrote itself.  With a
+// per-row 8-bit scale a middle pass re-reads it once more for max |v|.
+template <typename T, int OP, bool VEC, typename TR, bool Q8>
 __global__ void __launch_bounds__(1024) k_two_pass(Problem p) {
     using RS = Res<T, TR>;
     __shared__ float red[2][32];
+    __shared__ float redm[Q8 ? 64 : 1];
     constexpr int EPV = VEC ? DT<T>::EPV : 1;
     const int n = (int)(p.H / EPV);
     grid_dependency_wait();
+    QMul qm{1.f, 1.f};
+    if constexpr (Q8) qm = quant_tensor(p);
     int par = 0;
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
         if (t + gridDim.x >= p.T) grid_launch_dependents();
@@ -565,25 +685,34 @@ __global__ void __launch_bounds__(1024) k_two_pass(Problem p) {
         }
         const float tot = block_sum(ss, red[par]);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
+        if constexpr (Q8) {
+            if (p.qmode == Q_ROW) {
+                float a = 0.f;
+                for (int base = 0; base < n; base += blockDim.x) {
+                    const int j = base + threadIdx.x;
+                    if (j >= n) break;
+                    if constexpr (VEC) {
+                        uint4 hv[1][RS::N];
+                        reload_vec<T, OP, TR>(p, t, j, hv);
+                        a = fmaxf(a, amax_vec<T, 1, TR, false>(p, j, 1 << 30, n, hv, inv, nullptr));
+                    } else {
+                        const float h[1] = {reload_scalar<T, OP, TR>(p, t, j)};
+                        a = fmaxf(a, amax_scalar<T, 1>(p, j, 1 << 30, h, inv));
+                    }
+                }
+                qm = quant_row(p, t, block_max(a, redm + 32 * par), threadIdx.x == 0);
+            }
+        }
         for (int base = 0; base < n; base += blockDim.x) {
             const int j = base + threadIdx.x;
             if (j >= n) break;
             if constexpr (VEC) {
                 uint4 hv[1][RS::N];
-                if constexpr (OP == OP_PLAIN) {
-                    hv[0][0] = ld_stream(reinterpret_cast<const T *>(p.src) + t * p.ldx +
-                                         (int64_t)j * EPV);
-                } else {
-                    const TR *res = reinterpret_cast<const TR *>(p.residual) + t * p.ldr;
-#pragma unroll
-                    for (int q = 0; q < RS::N; ++q)
-                        hv[0][q] = ld_stream(res + (int64_t)j * EPV + q * RS::EPW);
-                }
-                pass2_vec<T, 1, TR>(p, t, j, 1 << 30, n, hv, inv);
+                reload_vec<T, OP, TR>(p, t, j, hv);
+                pass2_vec<T, 1, TR, false, Q8>(p, t, j, 1 << 30, n, hv, inv, nullptr, qm);
             } else {
-                float h[1] = {OP == OP_PLAIN ? ld_elem<T>(p.src, t * p.ldx + j)
-                                             : ld_elem<TR>(p.residual, t * p.ldr + j)};
-                pass2_scalar<T, 1>(p, t, j, 1 << 30, h, inv);
+                const float h[1] = {reload_scalar<T, OP, TR>(p, t, j)};
+                pass2_scalar<T, 1, Q8>(p, t, j, 1 << 30, h, inv, qm);
             }
         }
     }
@@ -593,7 +722,7 @@ __global__ void __launch_bounds__(1024) k_two_pass(Problem p) {
 // Launcher: plan -> template instance
 // ---------------------------------------------------------------------------
 
-template <typename T, int OP, typename TR>
+template <typename T, int OP, typename TR, bool Q8>
 static cudaError_t launch_rows_op(const Problem &p, const Plan &pl, cudaStream_t st) {
     const dim3 g(pl.grid), b(pl.block);
     auto go = [&](auto kernel) { return launch_kernel(kernel, g, b, 0, st, pl.pdl, 1, p); };
@@ -602,59 +731,59 @@ static cudaError_t launch_rows_op(const Problem &p, const Plan &pl, cudaStream_t
         if constexpr (OP != OP_REDUCE) {
             if (pl.pipe) {
                 switch (pl.per_thread) {
-                case 1: return go(k_warp_pipe<T, 1, OP, TR>);
-                case 2: return go(k_warp_pipe<T, 2, OP, TR>);
-                case 4: return go(k_warp_pipe<T, 4, OP, TR>);
+                case 1: return go(k_warp_pipe<T, 1, OP, TR, Q8>);
+                case 2: return go(k_warp_pipe<T, 2, OP, TR, Q8>);
+                case 4: return go(k_warp_pipe<T, 4, OP, TR, Q8>);
                 default: return cudaErrorInvalidValue;
                 }
             }
         }
         switch (pl.per_thread) {
-        case 1: return go(k_warp_vec<T, 1, OP, TR>);
-        case 2: return go(k_warp_vec<T, 2, OP, TR>);
-        case 4: return go(k_warp_vec<T, 4, OP, TR>);
+        case 1: return go(k_warp_vec<T, 1, OP, TR, Q8>);
+        case 2: return go(k_warp_vec<T, 2, OP, TR, Q8>);
+        case 4: return go(k_warp_vec<T, 4, OP, TR, Q8>);
         default: return cudaErrorInvalidValue;
         }
     case KIND_CTA:
         if constexpr (OP != OP_REDUCE) {
             if (pl.vec && pl.pipe) {
                 switch (pl.per_thread) {
-                case 1: return go(k_cta_pipe<T, 1, OP, TR>);
-                case 2: return go(k_cta_pipe<T, 2, OP, TR>);
-                case 4: return go(k_cta_pipe<T, 4, OP, TR>);
-                case 8: return go(k_cta_pipe<T, 8, OP, TR>);
+                case 1: return go(k_cta_pipe<T, 1, OP, TR, Q8>);
+                case 2: return go(k_cta_pipe<T, 2, OP, TR, Q8>);
+                case 4: return go(k_cta_pipe<T, 4, OP, TR, Q8>);
+                case 8: return go(k_cta_pipe<T, 8, OP, TR, Q8>);
                 default: return cudaErrorInvalidValue;
                 }
             }
         }
         if (pl.vec && pl.prefetch_gamma) {
             switch (pl.per_thread) {
-            case 1: return go(k_cta_vec<T, 1, OP, true, TR>);
-            case 2: return go(k_cta_vec<T, 2, OP, true, TR>);
-            case 4: return go(k_cta_vec<T, 4, OP, true, TR>);
-            case 8: return go(k_cta_vec<T, 8, OP, true, TR>);
+            case 1: return go(k_cta_vec<T, 1, OP, true, TR, Q8>);
+            case 2: return go(k_cta_vec<T, 2, OP, true, TR, Q8>);
+            case 4: return go(k_cta_vec<T, 4, OP, true, TR, Q8>);
+            case 8: return go(k_cta_vec<T, 8, OP, true, TR, Q8>);
             default: return cudaErrorInvalidValue;
             }
         }
         if (pl.vec) {
             switch (pl.per_thread) {
-            case 1: return go(k_cta_vec<T, 1, OP, false, TR>);
-            case 2: return go(k_cta_vec<T, 2, OP, false, TR>);
-            case 4: return go(k_cta_vec<T, 4, OP, false, TR>);
-            case 8: return go(k_cta_vec<T, 8, OP, false, TR>);
+            case 1: return go(k_cta_vec<T, 1, OP, false, TR, Q8>);
+            case 2: return go(k_cta_vec<T, 2, OP, false, TR, Q8>);
+            case 4: return go(k_cta_vec<T, 4, OP, false, TR, Q8>);
+            case 8: return go(k_cta_vec<T, 8, OP, false, TR, Q8>);
             default: return cudaErrorInvalidValue;
             }
         }
         switch (pl.per_thread) {
-        case 1: return go(k_cta_scalar<T, 1, OP, TR>);
-        case 2: return go(k_cta_scalar<T, 2, OP, TR>);
-        case 4: return go(k_cta_scalar<T, 4, OP, TR>);
-        case 8: return go(k_cta_scalar<T, 8, OP, TR>);
-        case 16: return go(k_cta_scalar<T, 16, OP, TR>);
+        case 1: return go(k_cta_scalar<T, 1, OP, TR, Q8>);
+        case 2: return go(k_cta_scalar<T, 2, OP, TR, Q8>);
+        case 4: return go(k_cta_scalar<T, 4, OP, TR, Q8>);
+        case 8: return go(k_cta_scalar<T, 8, OP, TR, Q8>);
+        case 16: return go(k_cta_scalar<T, 16, OP, TR, Q8>);
         default: return cudaErrorInvalidValue;
         }
     case KIND_TWO_PASS:
-        return pl.vec ? go(k_two_pass<T, OP, true, TR>) : go(k_two_pass<T, OP, false, TR>);
+        return pl.vec ? go(k_two_pass<T, OP, true, TR, Q8>) : go(k_two_pass<T, OP, false, TR, Q8>);
     default:
         return cudaErrorInvalidValue;
     }
@@ -670,11 +799,25 @@ cudaError_t launch_rows(const Problem &p, const Plan &pl, cudaStream_t st) {
         if constexpr (!std::is_same<T, TR>::value) {
             return cudaErrorInvalidValue;
         } else {
-            e = launch_rows_op<T, OP_PLAIN, T>(p, pl, st);
+            e = launch_rows_op<T, OP_PLAIN, T, false>(p, pl, st);
         }
         break;
-    case OP_FUSED: e = launch_rows_op<T, OP_FUSED, TR>(p, pl, st); break;
-    case OP_REDUCE: e = launch_rows_op<T, OP_REDUCE, TR>(p, pl, st); break;
+    case OP_FUSED: e = launch_rows_op<T, OP_FUSED, TR, false>(p, pl, st); break;
+    case OP_REDUCE: e = launch_rows_op<T, OP_REDUCE, TR, false>(p, pl, st); break;
+    default: return cudaErrorInvalidValue;
+    }
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// 8-bit output (codes in p.y, scale in p.qscale): every form, residual of
+// type T.
+template <typename T>
+cudaError_t launch_rows_q8(const Problem &p, const Plan &pl, cudaStream_t st) {
+    cudaError_t e;
+    switch (p.op) {
+    case OP_PLAIN: e = launch_rows_op<T, OP_PLAIN, T, true>(p, pl, st); break;
+    case OP_FUSED: e = launch_rows_op<T, OP_FUSED, T, true>(p, pl, st); break;
+    case OP_REDUCE: e = launch_rows_op<T, OP_REDUCE, T, true>(p, pl, st); break;
     default: return cudaErrorInvalidValue;
     }
     return e != cudaSuccess ? e : cudaGetLastError();

@@ -61,6 +61,9 @@ class Workload:
     scaled: bool = False
     rdtype: str = ""   # residual storage type ("": the inputs' type)
     ld: int = 0        # row stride of x / partials, residual and y (0: H)
+    qfmt: str = ""     # 8-bit output: "e4m3" | "e5m2" ("": y in the inputs' type)
+    qmode: str = ""    # 8-bit output scale: "tensor" (given) | "row" (computed per row)
+    qscale: float = 1.0  # the per-tensor scale
     note: str = field(default="", compare=False)
 
     @property
@@ -84,13 +87,16 @@ class Workload:
     def algorithmic_bytes(self) -> int:
         """Bytes the operation must move at minimum: every input element read
         once, every output element written once, gamma read once (the
-        residual counted in its own storage type)."""
+        residual counted in its own storage type; an 8-bit y as one byte per
+        element plus its scales)."""
         s = ELEM_SIZE[self.dtype]
+        ys = 1 if self.qfmt else s
+        scales = (4 * self.T if self.qmode == "row" else 4) if self.qfmt else 0
         if self.op == "rms_norm":
-            return s * self.T * self.H * 2 + s * self.H
+            return self.T * self.H * (s + ys) + s * self.H + scales
         rs = ELEM_SIZE[self.res_dtype]
         n_x = self.n_inputs - 1  # partials (or x)
-        return self.T * self.H * (s * (n_x + 1) + rs * 2) + s * self.H
+        return self.T * self.H * (s * n_x + rs * 2 + ys) + s * self.H + scales
 
 
 # The five benchmark configurations of the method (the token sweep is five
@@ -113,13 +119,19 @@ CONFIGS = [
              scaled=True),
 ]
 # The widened rows: a row-strided plain norm (the first H = 512 of 576
-# columns, as a latent slice inside a wider projection output) and a fused
-# norm with a binary32 residual stream and bf16 inputs / output.
+# columns, as a latent slice inside a wider projection output), a fused
+# norm with a binary32 residual stream and bf16 inputs / output, and the fused
+# norm with an e4m3 output under a per-row (dynamic) or a per-tensor (static)
+# scale.
 EXTENDED = [
     Workload("plain_strided_bf16_T32768_H512_ld576", "rms_norm", "bf16", 32768, 512, 1e-6,
              ld=576),
     Workload("fused_r32_bf16_T32768_H5120", "fused_add_rms_norm", "bf16", 32768, 5120, 1e-6,
              R=1, rdtype="f32"),
+    Workload("fused_e4m3row_bf16_T32768_H5120", "fused_add_rms_norm", "bf16", 32768, 5120, 1e-6,
+             R=1, qfmt="e4m3", qmode="row"),
+    Workload("fused_e4m3_bf16_T32768_H5120", "fused_add_rms_norm", "bf16", 32768, 5120, 1e-6,
+             R=1, qfmt="e4m3", qmode="tensor", qscale=0.02),
 ]
 BY_NAME = {w.name: w for w in CONFIGS + EXTENDED}
 

@@ -106,3 +106,37 @@ def check_parity(w, d, *, out_is_input=False, what=""):
     if ref.residual is not None:
         assert_bits_equal(res, ref.residual, (what or w.name) + " residual")
     return y, res
+
+
+# 8-bit codes: the kernel computes v in binary32, the oracle in binary64, so
+# a code may differ only where the oracle's exact u = v / s lies within
+# Q_MID_REL of the midpoint between two adjacent codes' values, and then by
+# one step.  (Binary32 error of v: the sum of squares over <= 2^17 terms with
+# per-thread runs of <= 64 and a <= 10-level tree, rsqrtf, two products and
+# the scale multiply: well below 8e-6 relative.)
+Q_MID_REL = 8e-6
+Q_SCALE_REL = 4e-6
+
+
+def assert_codes_close(got: np.ndarray, want: np.ndarray, u64: np.ndarray, fmt: str, what=""):
+    got = np.asarray(got, np.uint8)
+    want = np.asarray(want, np.uint8)
+    diff = got != want
+    if not diff.any():
+        return
+    g = got[diff].astype(np.int64)
+    w = want[diff].astype(np.int64)
+    gv = oracle.default().decode_fp8(got[diff], fmt)
+    wv = oracle.default().decode_fp8(want[diff], fmt)
+    adjacent = ((g & 0x80) == (w & 0x80)) & (np.abs((g & 0x7F) - (w & 0x7F)) == 1)
+    mid = (gv + wv) / 2
+    near = np.abs(u64[diff] - mid) <= Q_MID_REL * np.abs(mid)
+    bad = ~(adjacent & near)
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {diff.size} codes differ beyond a "
+                           f"midpoint tie, e.g. got {g[bad][:4]} want {w[bad][:4]} "
+                           f"u {u64[diff][bad][:4]}")
+
+
+def assert_scales_close(got: np.ndarray, want: np.ndarray, what=""):
+    rel = np.abs(got.astype(np.float64) - want) / np.abs(want.astype(np.float64))
+    assert float(rel.max(initial=0.0)) <= Q_SCALE_REL, f"{what}: scale rel err {rel.max():.3e}"

@@ -247,3 +247,68 @@ def test_plan_fp32_residual():
     assert not p.startswith("stream"), p
     assert rarn.plan("fused_add_rms_norm", 8, 4096, 1, "f32", num_sms=152, rdtype="bf16") \
         .startswith("none")
+
+
+def _fp8(ptr, ld, fmt=0, mode=0, scale=C + (1 << 30)):
+    return ctypes.byref(rarn.Fp8Rows(ptr, ld, fmt, mode, scale))
+
+
+def test_fp8_forms_argument_errors(lib):
+    """8-bit output forms: descriptor, storage types and aliasing are checked
+    before any CUDA call."""
+    H, T = 64, 4
+    x = _rows(B, H, BF16)
+    assert lib.rarn_rms_norm_fp8(None, x, D, T, H, 1e-6, None) == INVALID
+    assert lib.rarn_rms_norm_fp8(_fp8(A, H, fmt=2), x, D, T, H, 1e-6, None) == INVALID
+    assert lib.rarn_rms_norm_fp8(_fp8(A, H, mode=2), x, D, T, H, 1e-6, None) == INVALID
+    assert lib.rarn_rms_norm_fp8(_fp8(A, H, scale=None), x, D, T, H, 1e-6, None) == INVALID
+    assert lib.rarn_rms_norm_fp8(_fp8(A, H - 1), x, D, T, H, 1e-6, None) == INVALID
+    # an fp32 residual with 16-bit inputs is not built for the 8-bit output
+    st = lib.rarn_fused_add_rms_norm_fp8(_fp8(A, H), x, _rows(C, H, F32), D, T, H, 1e-6, None)
+    assert st == UNSUPPORTED
+    # codes over x; per-row scales inside x; per-tensor scale inside the codes
+    assert lib.rarn_rms_norm_fp8(_fp8(B + 8, H), x, D, T, H, 1e-6, None) == ALIAS
+    assert lib.rarn_rms_norm_fp8(_fp8(A, H, mode=1, scale=B + 16), x, D, T, H, 1e-6,
+                                 None) == ALIAS
+    assert lib.rarn_rms_norm_fp8(_fp8(A, H, mode=0, scale=A + 4), x, D, T, H, 1e-6,
+                                 None) == ALIAS
+    # a per-tensor scale may sit inside an input (it is only read) ...
+    st = lib.rarn_rms_norm_fp8(_fp8(A, H, mode=0, scale=B + 16), x, D, T, H, 1e-6, None)
+    assert st not in (INVALID, ALIAS, UNSUPPORTED)
+    # ... but not inside the residual, which is written
+    st = lib.rarn_fused_add_rms_norm_fp8(_fp8(A, H, mode=0, scale=C + 8), x, _rows(C, H, BF16),
+                                         D, T, H, 1e-6, None)
+    assert st == ALIAS
+    # the codes span T rows of row_stride bytes: a scale right after it is fine
+    st = lib.rarn_rms_norm_fp8(_fp8(A, 2 * H, mode=1, scale=A + 3 * 2 * H + H), x, D, T, H,
+                               1e-6, None)
+    assert st not in (INVALID, ALIAS, UNSUPPORTED)
+    # the stream and cluster kernels have no 8-bit output
+    for path in ("stream", "cluster"):
+        rarn.set_path(path)
+        try:
+            assert lib.rarn_reduce_add_rms_norm_fp8(_fp8(A, H), x, T * H, 2, _rows(C, H, BF16), D,
+                                                    T, H, 1e-6, None) == UNSUPPORTED
+        finally:
+            rarn.set_path("auto")
+    assert lib.rarn_rms_norm_fp8(_fp8(None, H), _rows(None, H, BF16), None, 0, H, 1e-6,
+                                 None) == OK
+
+
+def test_plan_fp8():
+    """The 8-bit output runs on the register row kernels for every shape."""
+    cases = [("rms_norm", 30000, 512, 0, "warp", "pipe=1"),
+             ("fused_add_rms_norm", 32768, 5120, 1, "rows.cta", "pipe=1"),
+             ("fused_add_rms_norm", 16, 5120, 1, "rows.cta", "gamma_regs=1"),
+             ("reduce_add_rms_norm", 8192, 8192, 8, "rows.cta", "vec16"),
+             ("rms_norm", 4, 100000, 0, "rows.two_pass", "vec16")]
+    for op, T, H, R, kind, flag in cases:
+        p = rarn.plan_fp8(op, T, H, R, "bf16", num_sms=152)
+        assert kind in p and flag in p, (op, T, H, p)
+    assert "scalar" in rarn.plan_fp8("rms_norm", 64, 1000, 0, "bf16", vec_ok=False, num_sms=152)
+    rarn.set_path("stream")
+    try:
+        assert rarn.plan_fp8("reduce_add_rms_norm", 8192, 8192, 8, "bf16",
+                             num_sms=152).startswith("none")
+    finally:
+        rarn.set_path("auto")
