@@ -221,7 +221,9 @@ rarn_status rarn_reduce_add_rms_norm_ex(rarn_rows y, rarn_rows partials, int64_t
  *   RARN_SCALE_ROW:    s = max_i |v_i| / maxf, written to scale[t] (T binary32
  *                      values); u_i = (v_i * (1 / max|v|)) * maxf, so the
  *                      row's largest magnitude maps to maxf; a row of zeros
- *                      gets s = 1 and zero codes.
+ *                      gets s = 1 and zero codes.  max|v| is computed as
+ *                      inv * max_i |h_i * gamma_i| (inv > 0), which equals it
+ *                      up to binary32 rounding and joins the row reduction.
  * Dequantised, code value * s approximates v.  Row t of the codes starts at
  * byte t * row_stride of `data` (row_stride >= H); only the first H bytes of
  * each row are written.  The residual (fused / reduce) has the inputs'

@@ -240,16 +240,18 @@ __device__ __forceinline__ float block_sum(float v, float *red) {
     return warp_sum(s);
 }
 
-// Maximum of v over the whole CTA, returned to every thread (same scheme and
-// buffer discipline as block_sum).
-__device__ __forceinline__ float block_max(float v, float *red) {
+// Sum of s and maximum of m over the whole CTA in one pass through shared
+// memory (one barrier), returned to every thread; the sum in the same order
+// as block_sum.
+__device__ __forceinline__ float2 block_sum_max(float s, float m, float2 *red) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int nwarps = (blockDim.x + 31) >> 5;
-    v = warp_max(v);
-    if (lane == 0) red[warp] = v;
+    s = warp_sum(s);
+    m = warp_max(m);
+    if (lane == 0) red[warp] = make_float2(s, m);
     __syncthreads();
-    float s = lane < nwarps ? red[lane] : 0.f;
-    return warp_max(s);
+    const float2 v = lane < nwarps ? red[lane] : make_float2(0.f, 0.f);
+    return make_float2(warp_sum(v.x), warp_max(v.y));
 }
 
 // ---------------------------------------------------------------------------
@@ -259,7 +261,8 @@ __device__ __forceinline__ float block_max(float v, float *red) {
 //   per row:    m1 = 1 / max|v|, m2 = maxf (448 for e4m3, 57344 for e5m2), so
 //               the row's largest magnitude maps to maxf; the row's scale
 //               max|v| / maxf is written out (1 and m1 = m2 = 1 for a row of
-//               zeros).
+//               zeros).  Since inv > 0, max|v| is taken as inv * max|h * gamma|,
+//               so the maximum joins the sum of squares in one row reduction.
 // ("Block All Reduce", FP8 section: e4m3 and e5m2 codes, converted with
 // saturation to the largest finite value.)
 // ---------------------------------------------------------------------------

@@ -263,11 +263,11 @@ __device__ __forceinline__ void pass2_vec(const Problem &p, int64_t t, int j0, i
     }
 }
 
-// Per-row scale: this thread's max |(h * inv) * gamma| over its packs -- the
-// same products pass2_vec converts.
+// Per-row scale: this thread's max |h * gamma| over its packs (times inv > 0
+// after the row reduction, the row's max |v|).
 template <typename T, int VPT, typename TR, bool PG>
 __device__ __forceinline__ float amax_vec(const Problem &p, int j0, int js, int nv,
-                                          const uint4 (&hv)[VPT][Res<T, TR>::N], float inv,
+                                          const uint4 (&hv)[VPT][Res<T, TR>::N],
                                           const uint4 *gv) {
     constexpr int EPV = DT<T>::EPV;
     const T *g = reinterpret_cast<const T *>(p.gamma);
@@ -280,7 +280,7 @@ __device__ __forceinline__ float amax_vec(const Problem &p, int j0, int js, int 
             Res<T, TR>::to_f(hv[k], h);
             DT<T>::unpack(PG ? gv[k] : ld_keep(g + (int64_t)j * EPV), w);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) m = fmaxf(m, fabsf((h[e] * inv) * w[e]));
+            for (int e = 0; e < EPV; ++e) m = fmaxf(m, fabsf(h[e] * w[e]));
         }
     }
     return m;
@@ -374,16 +374,45 @@ __device__ __forceinline__ void pass2_scalar(const Problem &p, int64_t t, int i0
 
 template <typename T, int NE>
 __device__ __forceinline__ float amax_scalar(const Problem &p, int i0, int is,
-                                             const float (&h)[NE], float inv) {
+                                             const float (&h)[NE]) {
     const T *g = reinterpret_cast<const T *>(p.gamma);
     const int H = (int)p.H;
     float m = 0.f;
 #pragma unroll
     for (int k = 0; k < NE; ++k) {
         const int i = i0 + k * is;
-        if (i < H) m = fmaxf(m, fabsf((h[k] * inv) * DT<T>::to_f(g[i])));
+        if (i < H) m = fmaxf(m, fabsf(h[k] * DT<T>::to_f(g[i])));
     }
     return m;
+}
+
+// The row's reciprocal RMS from this thread's share ss of the sum of squares
+// (CTA-wide).  With a per-row 8-bit scale, am is this thread's share of
+// max |h * gamma|: it is reduced in the same pass (one barrier) and qm
+// receives the row's multipliers.  red / red2 alternate between rows.
+template <bool Q8>
+__device__ __forceinline__ float row_inv_cta(const Problem &p, int64_t t, float ss, float am,
+                                             float *red, float2 *red2, QMul &qm) {
+    if constexpr (Q8) {
+        if (p.qmode == Q_ROW) {
+            const float2 r = block_sum_max(ss, am, red2);
+            const float inv = rsqrtf(r.x / (float)p.H + p.eps);
+            qm = quant_row(p, t, r.y * inv, threadIdx.x == 0);
+            return inv;
+        }
+    }
+    return rsqrtf(block_sum(ss, red) / (float)p.H + p.eps);
+}
+
+// The same for a warp per row.
+template <bool Q8>
+__device__ __forceinline__ float row_inv_warp(const Problem &p, int64_t t, float ss, float am,
+                                              QMul &qm) {
+    const float inv = rsqrtf(warp_sum(ss) / (float)p.H + p.eps);
+    if constexpr (Q8) {
+        if (p.qmode == Q_ROW) qm = quant_row(p, t, warp_max(am) * inv, (threadIdx.x & 31) == 0);
+    }
+    return inv;
 }
 
 // CTA size each register-staged kernel is compiled for (plan.h budget); a
@@ -410,11 +439,12 @@ struct ScalarBound {
 template <typename T, int VPT, int OP, bool PG, typename TR, bool Q8>
 __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG, TR>::value) k_cta_vec(Problem p) {
     __shared__ float red[2][32];
-    __shared__ float redm[Q8 ? 64 : 1];
+    __shared__ float2 red2[Q8 ? 64 : 1];
     const int nv = (int)(p.H / DT<T>::EPV);
     grid_dependency_wait();
     QMul qm{1.f, 1.f};
     if constexpr (Q8) qm = quant_tensor(p);
+    const bool qrow = Q8 && p.qmode == Q_ROW;
     uint4 gv[VPT];
     if (PG) load_gamma_vec<T, VPT>(p, threadIdx.x, blockDim.x, nv, gv);
     int par = 0;
@@ -422,14 +452,9 @@ __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG, TR>::value) k_cta_vec
         if (t + gridDim.x >= p.T) grid_launch_dependents();
         uint4 hv[VPT][Res<T, TR>::N];
         const float ss = pass1_vec<T, VPT, OP, TR>(p, t, threadIdx.x, blockDim.x, nv, hv);
-        const float tot = block_sum(ss, red[par]);
-        const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        if constexpr (Q8) {
-            if (p.qmode == Q_ROW) {
-                const float a = amax_vec<T, VPT, TR, PG>(p, threadIdx.x, blockDim.x, nv, hv, inv, gv);
-                qm = quant_row(p, t, block_max(a, redm + 32 * par), threadIdx.x == 0);
-            }
-        }
+        const float am =
+            qrow ? amax_vec<T, VPT, TR, PG>(p, threadIdx.x, blockDim.x, nv, hv, gv) : 0.f;
+        const float inv = row_inv_cta<Q8>(p, t, ss, am, red[par], red2 + 32 * par, qm);
         pass2_vec<T, VPT, TR, PG, Q8>(p, t, threadIdx.x, blockDim.x, nv, hv, inv, gv, qm);
     }
 }
@@ -513,11 +538,12 @@ struct PipeBound {
 template <typename T, int VPT, int OP, typename TR, bool Q8>
 __global__ void __launch_bounds__(PipeBound<T, VPT, OP, TR>::value) k_cta_pipe(Problem p) {
     __shared__ float red[2][32];
-    __shared__ float redm[Q8 ? 64 : 1];
+    __shared__ float2 red2[Q8 ? 64 : 1];
     const int nv = (int)(p.H / DT<T>::EPV);
     grid_dependency_wait();
     QMul qm{1.f, 1.f};
     if constexpr (Q8) qm = quant_tensor(p);
+    const bool qrow = Q8 && p.qmode == Q_ROW;
     RowLoads<T, VPT, OP, TR> next;
     int64_t t = blockIdx.x;
     if (t < p.T) issue_row_loads<T, VPT, OP, TR>(p, t, threadIdx.x, blockDim.x, nv, next);
@@ -532,15 +558,9 @@ __global__ void __launch_bounds__(PipeBound<T, VPT, OP, TR>::value) k_cta_pipe(P
         uint4 hv[VPT][Res<T, TR>::N];
         const float ss =
             consume_row_loads<T, VPT, OP, TR>(p, t, threadIdx.x, blockDim.x, nv, cur, hv);
-        const float tot = block_sum(ss, red[par]);
-        const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        if constexpr (Q8) {
-            if (p.qmode == Q_ROW) {
-                const float a =
-                    amax_vec<T, VPT, TR, false>(p, threadIdx.x, blockDim.x, nv, hv, inv, nullptr);
-                qm = quant_row(p, t, block_max(a, redm + 32 * par), threadIdx.x == 0);
-            }
-        }
+        const float am =
+            qrow ? amax_vec<T, VPT, TR, false>(p, threadIdx.x, blockDim.x, nv, hv, nullptr) : 0.f;
+        const float inv = row_inv_cta<Q8>(p, t, ss, am, red[par], red2 + 32 * par, qm);
         pass2_vec<T, VPT, TR, false, Q8>(p, t, threadIdx.x, blockDim.x, nv, hv, inv, nullptr, qm);
     }
 }
@@ -557,19 +577,15 @@ __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
     grid_dependency_wait();
     QMul qm{1.f, 1.f};
     if constexpr (Q8) qm = quant_tensor(p);
+    const bool qrow = Q8 && p.qmode == Q_ROW;
     uint4 gv[VPT];
     load_gamma_vec<T, VPT>(p, lane, 32, nv, gv);
     for (int64_t t = first; t < p.T; t += step) {
         if (t + step >= p.T) grid_launch_dependents();
         uint4 hv[VPT][Res<T, TR>::N];
         const float ss = pass1_vec<T, VPT, OP, TR>(p, t, lane, 32, nv, hv);
-        const float tot = warp_sum(ss);
-        const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        if constexpr (Q8) {
-            if (p.qmode == Q_ROW)
-                qm = quant_row(p, t, warp_max(amax_vec<T, VPT, TR, true>(p, lane, 32, nv, hv, inv, gv)),
-                               lane == 0);
-        }
+        const float am = qrow ? amax_vec<T, VPT, TR, true>(p, lane, 32, nv, hv, gv) : 0.f;
+        const float inv = row_inv_warp<Q8>(p, t, ss, am, qm);
         pass2_vec<T, VPT, TR, true, Q8>(p, t, lane, 32, nv, hv, inv, gv, qm);
     }
 }
@@ -586,6 +602,7 @@ __global__ void __launch_bounds__(256) k_warp_pipe(Problem p) {
     grid_dependency_wait();
     QMul qm{1.f, 1.f};
     if constexpr (Q8) qm = quant_tensor(p);
+    const bool qrow = Q8 && p.qmode == Q_ROW;
     uint4 gv[VPT];
     load_gamma_vec<T, VPT>(p, lane, 32, nv, gv);
     RowLoads<T, VPT, OP, TR> next;
@@ -600,13 +617,8 @@ __global__ void __launch_bounds__(256) k_warp_pipe(Problem p) {
         }
         uint4 hv[VPT][Res<T, TR>::N];
         const float ss = consume_row_loads<T, VPT, OP, TR>(p, t, lane, 32, nv, cur, hv);
-        const float tot = warp_sum(ss);
-        const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        if constexpr (Q8) {
-            if (p.qmode == Q_ROW)
-                qm = quant_row(p, t, warp_max(amax_vec<T, VPT, TR, true>(p, lane, 32, nv, hv, inv, gv)),
-                               lane == 0);
-        }
+        const float am = qrow ? amax_vec<T, VPT, TR, true>(p, lane, 32, nv, hv, gv) : 0.f;
+        const float inv = row_inv_warp<Q8>(p, t, ss, am, qm);
         pass2_vec<T, VPT, TR, true, Q8>(p, t, lane, 32, nv, hv, inv, gv, qm);
     }
 }
@@ -615,23 +627,18 @@ __global__ void __launch_bounds__(256) k_warp_pipe(Problem p) {
 template <typename T, int NE, int OP, typename TR, bool Q8>
 __global__ void __launch_bounds__(ScalarBound<NE, OP>::value, 1) k_cta_scalar(Problem p) {
     __shared__ float red[2][32];
-    __shared__ float redm[Q8 ? 64 : 1];
+    __shared__ float2 red2[Q8 ? 64 : 1];
     grid_dependency_wait();
     QMul qm{1.f, 1.f};
     if constexpr (Q8) qm = quant_tensor(p);
+    const bool qrow = Q8 && p.qmode == Q_ROW;
     int par = 0;
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
         if (t + gridDim.x >= p.T) grid_launch_dependents();
         float h[NE];
         const float ss = pass1_scalar<T, NE, OP, TR>(p, t, threadIdx.x, blockDim.x, h);
-        const float tot = block_sum(ss, red[par]);
-        const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        if constexpr (Q8) {
-            if (p.qmode == Q_ROW) {
-                const float a = amax_scalar<T, NE>(p, threadIdx.x, blockDim.x, h, inv);
-                qm = quant_row(p, t, block_max(a, redm + 32 * par), threadIdx.x == 0);
-            }
-        }
+        const float am = qrow ? amax_scalar<T, NE>(p, threadIdx.x, blockDim.x, h) : 0.f;
+        const float inv = row_inv_cta<Q8>(p, t, ss, am, red[par], red2 + 32 * par, qm);
         pass2_scalar<T, NE, Q8>(p, t, threadIdx.x, blockDim.x, h, inv, qm);
     }
 }
@@ -658,51 +665,36 @@ __device__ __forceinline__ float reload_scalar(const Problem &p, int64_t t, int 
 
 // Rows too long for registers: pass 1 walks the row in tiles of blockDim
 // packs (or elements); pass 2 re-reads the stored row (the residual, or x for
-// the plain form) -- each thread re-reads only what it wrote itself.  With a
-// per-row 8-bit scale a middle pass re-reads it once more for max |v|.
+// the plain form) -- each thread re-reads only what it wrote itself.  A
+// per-row 8-bit scale takes max |h * gamma| in pass 1.
 template <typename T, int OP, bool VEC, typename TR, bool Q8>
 __global__ void __launch_bounds__(1024) k_two_pass(Problem p) {
     using RS = Res<T, TR>;
     __shared__ float red[2][32];
-    __shared__ float redm[Q8 ? 64 : 1];
+    __shared__ float2 red2[Q8 ? 64 : 1];
     constexpr int EPV = VEC ? DT<T>::EPV : 1;
     const int n = (int)(p.H / EPV);
     grid_dependency_wait();
     QMul qm{1.f, 1.f};
     if constexpr (Q8) qm = quant_tensor(p);
+    const bool qrow = Q8 && p.qmode == Q_ROW;
     int par = 0;
     for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
         if (t + gridDim.x >= p.T) grid_launch_dependents();
-        float ss = 0.f;
+        float ss = 0.f, am = 0.f;
         for (int base = 0; base < n; base += blockDim.x) {
+            const int j = base + threadIdx.x;
             if constexpr (VEC) {
                 uint4 hv[1][RS::N];
-                ss += pass1_vec<T, 1, OP, TR>(p, t, base + threadIdx.x, 1 << 30, n, hv);
+                ss += pass1_vec<T, 1, OP, TR>(p, t, j, 1 << 30, n, hv);
+                if (qrow) am = fmaxf(am, amax_vec<T, 1, TR, false>(p, j, 1 << 30, n, hv, nullptr));
             } else {
                 float h[1];
-                ss += pass1_scalar<T, 1, OP, TR>(p, t, base + threadIdx.x, 1 << 30, h);
+                ss += pass1_scalar<T, 1, OP, TR>(p, t, j, 1 << 30, h);
+                if (qrow) am = fmaxf(am, amax_scalar<T, 1>(p, j, 1 << 30, h));
             }
         }
-        const float tot = block_sum(ss, red[par]);
-        const float inv = rsqrtf(tot / (float)p.H + p.eps);
-        if constexpr (Q8) {
-            if (p.qmode == Q_ROW) {
-                float a = 0.f;
-                for (int base = 0; base < n; base += blockDim.x) {
-                    const int j = base + threadIdx.x;
-                    if (j >= n) break;
-                    if constexpr (VEC) {
-                        uint4 hv[1][RS::N];
-                        reload_vec<T, OP, TR>(p, t, j, hv);
-                        a = fmaxf(a, amax_vec<T, 1, TR, false>(p, j, 1 << 30, n, hv, inv, nullptr));
-                    } else {
-                        const float h[1] = {reload_scalar<T, OP, TR>(p, t, j)};
-                        a = fmaxf(a, amax_scalar<T, 1>(p, j, 1 << 30, h, inv));
-                    }
-                }
-                qm = quant_row(p, t, block_max(a, redm + 32 * par), threadIdx.x == 0);
-            }
-        }
+        const float inv = row_inv_cta<Q8>(p, t, ss, am, red[par], red2 + 32 * par, qm);
         for (int base = 0; base < n; base += blockDim.x) {
             const int j = base + threadIdx.x;
             if (j >= n) break;
