@@ -40,13 +40,21 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_HBM_GBS = 6800.0
 
 
+def _configs():
+    from residual_add_rmsnorm_gb300 import workloads as W
+    return W.CONFIGS + W.EXTENDED
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--workload", default=HEADLINE,
+                    choices=[w.name for w in _configs()],
+                    help="the timed configuration; a widened workload (row strides, fp32 "
+                         "residual, 8-bit output) has no host-buffer (e2e) or CPU leg")
     ap.add_argument("--path", choices=["auto", "rows", "stream", "cluster"], default="auto",
                     help="kernel family (default: the library's own choice)")
     ap.add_argument("--no-pdl", action="store_true",
@@ -201,6 +209,18 @@ def ncu_traffic(workload: str, plan_text: str):
     return None
 
 
+E2E_HOW = ("host-buffer entry point: the kernel reads the inputs from and writes the outputs "
+           "to pinned host memory (no staging copies)")
+
+
+def plan_of(w, rarn) -> str:
+    """The library's plan text for workload w (auto path unless forced)."""
+    R = w.R if w.op == "reduce_add_rms_norm" else 1
+    if w.qfmt:
+        return rarn.plan_fp8(w.op, w.T, w.H, R, w.dtype)
+    return rarn.plan(w.op, w.T, w.H, R, w.dtype, rdtype=w.res_dtype)
+
+
 def make_call(w, tensors, rarn):
     """The public call for workload w on device tensors: the dense entry
     points, or the general ones for row-strided layouts / a binary32
@@ -312,6 +332,8 @@ def run_reference(args):
         return
     from residual_add_rmsnorm_gb300 import workloads as W
     w = W.BY_NAME[args.workload]
+    if w not in W.CONFIGS:
+        raise SystemExit("the reference arm times the method's configurations only")
     rows = min(w.T, 128)
     samples = []
     nblocks = max(1, w.T // rows)
@@ -391,8 +413,8 @@ def time_graph(w, data, device, l2_bytes, min_launches=200):
     calls = [make_call(w, t, rarn) for t in sets]
     per_pass = copies
     passes = max(1, math.ceil(min_launches / per_pass))
-    if footprint * copies * passes > 40e9:  # keep huge configurations short
-        passes = 1
+    # keep huge configurations short: at most ~40 GB of traffic per replay
+    passes = max(1, min(passes, int(40e9 // (footprint * copies))))
     side = torch.cuda.Stream(device)
     side.wait_stream(torch.cuda.current_stream(device))
     with torch.cuda.stream(side):
@@ -473,8 +495,8 @@ def main():
     tensors = device_tensors(w, data, device)
     call = make_call(w, tensors, rarn)
     stream = torch.cuda.current_stream(device)
-    R = w.R if w.op == "reduce_add_rms_norm" else 1
-    plan_text = rarn.plan(w.op, w.T, w.H, R, w.dtype)
+    plan_text = plan_of(w, rarn)
+    dense = w in W.CONFIGS  # the forms the host-buffer entry points and the oracle leg cover
 
     props = torch.cuda.get_device_properties(device)
     gpu_id = str(getattr(props, "uuid", local_rank))
@@ -490,9 +512,14 @@ def main():
     peak, peak_kind = measured_hbm_peak()
     achieved = alg / per_launch_s / 1e9
 
-    e2e_ms, h2d, d2h = e2e_steps(w, data, args.e2e_steps, device, stream)
-    e2e_ms = max_over_ranks(e2e_ms, device)
-    e2e_value = world * alg * args.e2e_steps / (e2e_ms / 1e3) / 1e9
+    e2e = {"value": None, "unit": "GB/s",
+           "note": "no host-buffer entry point for this form (dense forms only)"}
+    if dense:
+        e2e_ms, h2d, d2h = e2e_steps(w, data, args.e2e_steps, device, stream)
+        e2e_ms = max_over_ranks(e2e_ms, device)
+        e2e = {"value": world * alg * args.e2e_steps / (e2e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+               "how": E2E_HOW}
     watchdog = rarn.watchdog(clear=True)
 
     per_config = {}
@@ -505,22 +532,20 @@ def main():
             cd = W.generate(cw)
             us, copies, n = time_graph(cw, cd, device, l2)
             cb = cw.algorithmic_bytes()
-            cR = cw.R if cw.op == "reduce_add_rms_norm" else 1
             gbs = cb / (us / 1e6) / 1e9
             per_config[cw.name] = {
                 "kind": "widened" if cw in W.EXTENDED else "config",
                 "us_per_launch": us, "gbs": gbs, "rows_per_s": cw.T / (us / 1e6),
                 "frac_of_peak": gbs / peak, "algorithmic_bytes": cb,
                 "timing": f"CUDA graph of {n} launches over {copies} input copies (cold L2)",
-                "plan": (rarn.plan_fp8(cw.op, cw.T, cw.H, cR, cw.dtype) if cw.qfmt else
-                         rarn.plan(cw.op, cw.T, cw.H, cR, cw.dtype, rdtype=cw.res_dtype))}
+                "plan": plan_of(cw, rarn)}
             del cd
             torch.cuda.empty_cache()
         if rarn.watchdog(clear=True):
             watchdog = 1
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and dense:
         cpu = cpu_baseline(w, args.cpu_seconds)
 
     if rank != 0:
@@ -540,10 +565,7 @@ def main():
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "algorithmic_bytes_per_launch": alg},
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-                "how": "host-buffer entry point: the kernel reads the inputs from and writes "
-                       "the outputs to pinned host memory (no staging copies)"},
+        "e2e": e2e,
         "clocks": clocks,
         "gpu_launches": args.steps,
         "watchdog": watchdog,

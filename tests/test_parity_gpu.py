@@ -385,7 +385,8 @@ def test_pipelined_rows_kernel():
                                   ("rms_norm", "f32", 3001, 4096, False),
                                   ("fused_add_rms_norm", "f16", 7777, 1600, True),
                                   ("rms_norm", "bf16", 9000, 3000, True),
-                                  ("fused_add_rms_norm", "bf16", 40000, 5120, False)):
+                                  ("fused_add_rms_norm", "bf16", 40000, 5120, False),
+                                  ("fused_add_rms_norm", "bf16", 4099, 16384, False)):
         w = W.workload(op, dt, T, H, eps=1e-6, seed=T)
         plan = rarn.plan(op, T, H, 1, dt)
         assert "pipe=1" in plan, plan
