@@ -88,6 +88,9 @@ class Oracle:
         lib.oracle_decode_fp8.restype = c_int
         lib.oracle_round_fp8.argtypes = [c_int, p, p, i64]
         lib.oracle_round_fp8.restype = c_int
+        lib.oracle_gemm_add_rms_norm.argtypes = [c_int, i64, i64, i64, p, i64, p, i64, p, i64, p,
+                                                 f32, p, i64, p, p, p, c_int]
+        lib.oracle_gemm_add_rms_norm.restype = c_int
         lib.oracle_decode.argtypes = [c_int, p, p, i64]
         lib.oracle_decode.restype = None
         lib.oracle_round.argtypes = [c_int, p, p, i64]
@@ -205,6 +208,30 @@ class Oracle:
         _check(self.lib.oracle_round_fp8(FP8[fmt], _ptr(values), _ptr(out), values.size))
         return out
 
+    def gemm_add_rms_norm(self, dtype, A, W, residual, gamma, eps, T, H, K, lda=None, ldw=None,
+                          ldr=None, ldy=None, *, want_p64=False, threads=0):
+        """GEMM producer + fused residual-add RMSNorm: P = A W^T (A: T rows of
+        lda, W: H rows of ldw, flat storage arrays), h = RN(P + residual),
+        residual updated IN PLACE (T rows of ldr), y returned as T rows of
+        ldy.  Returns a Result with y, residual, inv, and (want_p64) the
+        attributes p64 (P) and abs64 (sum |A W|), both [T, H]."""
+        lda, ldw, ldr, ldy = lda or K, ldw or K, ldr or H, ldy or H
+        A = self._as_storage(A, dtype)
+        W = self._as_storage(W, dtype)
+        gamma = self._as_storage(gamma, dtype)
+        if not (residual.flags.c_contiguous and residual.dtype == STORAGE[dtype]):
+            raise TypeError("residual must be contiguous storage of the dtype")
+        y = np.zeros(T * ldy, STORAGE[dtype])
+        inv = np.empty(T, np.float64)
+        p64 = np.empty((T, H), np.float64) if want_p64 else None
+        a64 = np.empty((T, H), np.float64) if want_p64 else None
+        n = _check(self.lib.oracle_gemm_add_rms_norm(
+            DTYPES[dtype], T, H, K, _ptr(A), lda, _ptr(W), ldw, _ptr(residual), ldr, _ptr(gamma),
+            float(eps), _ptr(y), ldy, _ptr(p64), _ptr(a64), _ptr(inv), threads))
+        r = Result(y, residual, inv, None, n)
+        r.p64, r.abs64 = p64, a64
+        return r
+
     def decode(self, bits, dtype) -> np.ndarray:
         """Storage bits -> binary64 values (the oracle's own decoder)."""
         bits = self._as_storage(bits, dtype)
@@ -249,6 +276,10 @@ def rows_ex(*a, **k) -> Result:
 
 def rows_fp8(*a, **k):
     return default().rows_fp8(*a, **k)
+
+
+def gemm_add_rms_norm(*a, **k) -> Result:
+    return default().gemm_add_rms_norm(*a, **k)
 
 
 def decode(*a, **k) -> np.ndarray:

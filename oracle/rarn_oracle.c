@@ -223,62 +223,74 @@ static void one_row(const job_t *j, int64_t t, double *h) {
     }
 }
 
+/* Rows are independent: a row function is run over row ranges in host
+ * threads, each with its own scratch of `scratch` doubles. */
+typedef void (*row_fn)(const void *ctx, int64_t t, double *scratch);
+
 typedef struct {
-    const job_t *job;
-    int64_t t0, t1;
+    const void *ctx;
+    row_fn fn;
+    int64_t t0, t1, scratch;
     int rc;
 } slice_t;
 
 static void *worker(void *arg) {
     slice_t *s = (slice_t *)arg;
-    double *h = (double *)malloc(sizeof(double) * (size_t)(s->job->H > 0 ? s->job->H : 1));
+    double *h = (double *)malloc(sizeof(double) * (size_t)(s->scratch > 0 ? s->scratch : 1));
     if (!h) {
         s->rc = -1;
         return NULL;
     }
-    for (int64_t t = s->t0; t < s->t1; ++t) one_row(s->job, t, h);
+    for (int64_t t = s->t0; t < s->t1; ++t) s->fn(s->ctx, t, h);
     free(h);
     s->rc = 0;
     return NULL;
 }
 
-/* Runs the rows over nthreads host threads (0 = every online core).
+/* Runs rows 0..T-1 over nthreads host threads (0 = every online core).
  * Returns the number of threads used, or a negative value on error. */
-static int run(const job_t *j, int nthreads) {
-    if (j->T < 0 || j->H <= 0 || !j->x || !j->gamma || !j->y) return -2;
-    if (j->T == 0) return 0;
+static int run_rows(const void *ctx, row_fn fn, int64_t T, int64_t scratch, int nthreads) {
+    if (T == 0) return 0;
     if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
     if (nthreads < 1) nthreads = 1;
-    if ((int64_t)nthreads > j->T) nthreads = (int)j->T;
+    if ((int64_t)nthreads > T) nthreads = (int)T;
     pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+    char *made = (char *)calloc((size_t)nthreads, 1);
     slice_t *sl = (slice_t *)calloc((size_t)nthreads, sizeof(slice_t));
-    if (!tid || !sl) {
+    if (!tid || !made || !sl) {
         free(tid);
+        free(made);
         free(sl);
         return -1;
     }
     int rc = nthreads;
-    int started = 0;
     for (int k = 0; k < nthreads; ++k) {
-        sl[k].job = j;
-        sl[k].t0 = j->T * k / nthreads;
-        sl[k].t1 = j->T * (k + 1) / nthreads;
+        sl[k].ctx = ctx;
+        sl[k].fn = fn;
+        sl[k].t0 = T * k / nthreads;
+        sl[k].t1 = T * (k + 1) / nthreads;
+        sl[k].scratch = scratch;
         sl[k].rc = -1;
-        if (nthreads == 1) {
-            worker(&sl[k]);
-            started = 0;
-        } else if (pthread_create(&tid[k], NULL, worker, &sl[k]) == 0) {
-            ++started;
-        } else {
-            worker(&sl[k]); /* run inline if a thread cannot be created */
-        }
+        if (nthreads > 1 && pthread_create(&tid[k], NULL, worker, &sl[k]) == 0)
+            made[k] = 1;
+        else
+            worker(&sl[k]); /* one thread, or a thread could not be created: inline */
     }
-    for (int k = 0; k < started; ++k) pthread_join(tid[k], NULL);
+    for (int k = 0; k < nthreads; ++k)
+        if (made[k]) pthread_join(tid[k], NULL);
     for (int k = 0; k < nthreads; ++k)
         if (sl[k].rc != 0) rc = -1;
     free(tid);
+    free(made);
     free(sl);
     return rc;
+}
+
+static void job_row(const void *ctx, int64_t t, double *h) { one_row((const job_t *)ctx, t, h); }
+
+static int run(const job_t *j, int nthreads) {
+    if (j->T < 0 || j->H <= 0 || !j->x || !j->gamma || !j->y) return -2;
+    return run_rows(j, job_row, j->T, j->H, nthreads);
 }
 
 /* ----------------------------------------------------------------------- */
@@ -465,6 +477,94 @@ int oracle_round_fp8(int fmt, const double *src, uint8_t *dst, int64_t n) {
     if (fmt != 0 && fmt != 1) return -2;
     for (int64_t i = 0; i < n; ++i) dst[i] = encode_fp8(&FP8[fmt], round_fp8_sat(&FP8[fmt], src[i]));
     return 1;
+}
+
+/* ----------------------------------------------------------------------- */
+/* GEMM producer with the fused residual-add RMSNorm as its epilogue        */
+/* ----------------------------------------------------------------------- */
+
+/*
+ * The partial that the fused form adds to the residual is produced by a
+ * matrix product: P = A W^T, A [T, K] (activations), W [H, K] (a linear
+ * layer's weight, output features by input features).  Per row t:
+ *
+ *   0. P_ti = sum_k A_tk W_ik: every product is exact in binary64 (at most
+ *      48 significant bits), summed with Neumaier's compensated summation,
+ *      so P_ti is the exact sum to within one binary64 rounding;
+ *   1. h_ti = RN_dt(P_ti + r_ti): the epilogue adds the residual to the
+ *      accumulator and rounds once to the storage type (the partial is
+ *      never rounded on its own); residual <- h;
+ *   2-4. as in one_row: ss, inv = 1 / sqrt(ss / H + eps), y = RN_dt((h inv) gamma).
+ *
+ * ("Tokenweave fused-RMSNorm-AR kernel", Code walkthrough, for steps 1-4;
+ * "sm80 GEMM + ReduceScatter", the flux epilogue: the GEMM's epilogue
+ * consumes the accumulator tile before anything is written.)
+ *
+ * Also reported per element: P (p64_out) and S = sum_k |A_tk W_ik|
+ * (abs64_out), the scale of the rounding error any binary32 accumulation of
+ * the same products can make.
+ */
+typedef struct {
+    int dt;
+    int64_t T, H, K;
+    const void *A;
+    int64_t lda;
+    const double *W64; /* W decoded, [H, K] dense */
+    void *residual;    /* [T] rows of ldr, type dt, updated in place */
+    int64_t ldr;
+    const void *gamma;
+    float eps;
+    void *y;
+    int64_t ldy;
+    double *p64_out, *abs64_out, *inv_out;
+} gemm_job_t;
+
+static void gemm_row(const void *ctx, int64_t t, double *scratch) {
+    const gemm_job_t *g = (const gemm_job_t *)ctx;
+    const int64_t H = g->H, K = g->K;
+    double *h = scratch, *arow = scratch + H;
+    for (int64_t k = 0; k < K; ++k) arow[k] = load_elem(g->dt, g->A, t * g->lda + k);
+    for (int64_t i = 0; i < H; ++i) {
+        const double *wrow = g->W64 + i * K;
+        double s = 0.0, c = 0.0, a = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double prod = arow[k] * wrow[k];
+            const double u = s + prod;
+            c += fabs(s) >= fabs(prod) ? (s - u) + prod : (prod - u) + s;
+            s = u;
+            a += fabs(prod);
+        }
+        const double P = s + c;
+        if (g->p64_out) g->p64_out[t * H + i] = P;
+        if (g->abs64_out) g->abs64_out[t * H + i] = a;
+        h[i] = round_dt(g->dt, P + load_elem(g->dt, g->residual, t * g->ldr + i));
+    }
+    for (int64_t i = 0; i < H; ++i) store_exact(g->dt, g->residual, t * g->ldr + i, h[i]);
+    double ss = 0.0;
+    for (int64_t i = 0; i < H; ++i) ss += h[i] * h[i];
+    const double inv = 1.0 / sqrt(ss / (double)H + (double)g->eps);
+    if (g->inv_out) g->inv_out[t] = inv;
+    for (int64_t i = 0; i < H; ++i)
+        store_exact(g->dt, g->y, t * g->ldy + i,
+                    round_dt(g->dt, (h[i] * inv) * load_elem(g->dt, g->gamma, i)));
+}
+
+int oracle_gemm_add_rms_norm(int dt, int64_t T, int64_t H, int64_t K, const void *A, int64_t lda,
+                             const void *W, int64_t ldw, void *residual, int64_t ldr,
+                             const void *gamma, float eps, void *y, int64_t ldy, double *p64_out,
+                             double *abs64_out, double *inv_out, int nthreads) {
+    if (T < 0 || H <= 0 || K <= 0 || lda < K || ldw < K || ldr < H || ldy < H || !A || !W ||
+        !residual || !gamma || !y)
+        return -2;
+    double *W64 = (double *)malloc(sizeof(double) * (size_t)(H * K));
+    if (!W64) return -1;
+    for (int64_t i = 0; i < H; ++i)
+        for (int64_t k = 0; k < K; ++k) W64[i * K + k] = load_elem(dt, W, i * ldw + k);
+    gemm_job_t g = {dt, T, H, K, A, lda, W64, residual, ldr, gamma, eps, y, ldy,
+                    p64_out, abs64_out, inv_out};
+    const int rc = run_rows(&g, gemm_row, T, H + K, nthreads);
+    free(W64);
+    return rc;
 }
 
 /* Elementwise helpers exposed so the tests can pin the format code alone. */

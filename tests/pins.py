@@ -14,7 +14,10 @@ What the pins rest on (none of it is the oracle's own code):
   * exact integer sums;
   * brute force on tiny rows in exact rational / 50-digit decimal arithmetic;
   * for the 8-bit output, torch's float8 decoders and casts and a brute-force
-    nearest search over the code table.
+    nearest search over the code table;
+  * for the GEMM producer, numpy's binary64 matrix product, the identity
+    weight (reduces to the fused form), a constructed single-rounding case and
+    exact rational brute force.
 """
 from __future__ import annotations
 
@@ -714,6 +717,118 @@ def pin_fp8_strides(O):
                     Rd = res.reshape(-1).copy()
 
 
+# ---------------------------------------------------------------------------
+# Pins on the GEMM producer with the fused epilogue
+# ---------------------------------------------------------------------------
+
+def _gemm(O, dt, A, W, r, g, eps, lda=None, ldw=None, ldr=None, ldy=None, T=None, H=None,
+          K=None):
+    T = T or A.shape[0]
+    H = H or W.shape[0]
+    K = K or A.shape[-1]
+    return O.gemm_add_rms_norm(dt, A.reshape(-1), W.reshape(-1), r, g, eps, T, H, K, lda, ldw,
+                               ldr, ldy, want_p64=True)
+
+
+def pin_gemm_product_library(O):
+    """P and sum |A W| against numpy's binary64 matrix product of the
+    library-decoded operands, with magnitudes spread over 2^+-20 so that the
+    sums are not all exact."""
+    rng = np.random.default_rng(31)
+    for dt in ("bf16", "f16", "f32"):
+        T, H, K = 5, 7, 300
+        av = rng.standard_normal((T, K)) * np.exp2(rng.integers(-20, 21, (T, K)) * (dt != "f16"))
+        wv = rng.standard_normal((H, K)) * 0.1
+        A, W = bits_of(av, dt), bits_of(wv, dt)
+        r = bits_of(rng.standard_normal((T, H)), dt).reshape(-1).copy()
+        res = _gemm(O, dt, A, W, r, bits_of(np.ones(H), dt), 1e-6)
+        ad, wd = lib_decode(A, dt), lib_decode(W, dt)
+        P = ad @ wd.T
+        S = np.abs(ad) @ np.abs(wd).T
+        tol = 4 * K * 2.0 ** -53
+        assert np.all(np.abs(res.p64 - P) <= tol * S), dt
+        assert np.all(np.abs(res.abs64 - S) <= tol * S), dt
+
+
+def pin_gemm_identity_is_fused(O):
+    """W = I (H = K): P = A exactly, and the GEMM form equals the fused form
+    with x = A bit for bit (y, residual; the fused form's binary32 sum of two
+    storage values rounds like the exact sum)."""
+    rng = np.random.default_rng(32)
+    for dt in ("bf16", "f16", "f32"):
+        T, H = 6, 96
+        A = _rand_bits(rng, (T, H), dt)
+        r = _rand_bits(rng, (T, H), dt)
+        g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+        W = bits_of(np.eye(H), dt)
+        got = _gemm(O, dt, A, W, r.reshape(-1).copy(), g, 1e-5)
+        want = O.fused_add_rms_norm(A, r, g, 1e-5, dt)
+        assert np.array_equal(got.y.reshape(T, H), want.y), dt
+        assert np.array_equal(got.residual.reshape(T, H), want.residual), dt
+
+
+def pin_gemm_one_rounding(O):
+    """The residual is the exact P + r rounded once: with A = [1, 1],
+    W = [1, 3 * 2^-10], r = 2^-8 (bf16), P + r = 1 + 7 * 2^-10 rounds to
+    1 + 2^-7, whereas rounding P first (to 1) would give the tie 1 + 2^-8 and
+    round it to 1."""
+    A = bits_of(np.array([[1.0, 1.0]]), "bf16")
+    W = bits_of(np.array([[1.0, 3 * 2.0 ** -10]]), "bf16")
+    r = bits_of(np.array([2.0 ** -8]), "bf16").copy()
+    got = _gemm(O, "bf16", A, W, r, bits_of(np.array([1.0]), "bf16"), 1e-6)
+    assert lib_decode(got.residual, "bf16")[0] == 1 + 2.0 ** -7
+    assert got.p64[0, 0] == 1 + 3 * 2.0 ** -10
+
+
+def pin_gemm_brute_force_tiny(O):
+    """Tiny problems from scratch: exact rational P and residual rounding,
+    exact sum of squares, 50-digit root, exact rounding of y."""
+    getcontext().prec = 50
+    rng = np.random.default_rng(33)
+    for dt in ("bf16", "f16", "f32"):
+        T, H, K = 3, 9, 11
+        A = _rand_bits(rng, (T, K), dt)
+        W = _rand_bits(rng, (H, K), dt, scale=0.3)
+        r = _rand_bits(rng, (T, H), dt)
+        g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+        got = _gemm(O, dt, A, W, r.reshape(-1).copy(), g, 1e-2)
+        ad, wd, rd, gd = (lib_decode(A, dt), lib_decode(W, dt), lib_decode(r, dt),
+                          lib_decode(g, dt))
+        e32 = Fraction(float(np.float32(1e-2)))
+        for t in range(T):
+            P = [sum(Fraction(ad[t, k]) * Fraction(wd[i, k]) for k in range(K)) for i in range(H)]
+            h = [Fraction(rn_exact(P[i] + Fraction(rd[t, i]), dt)) for i in range(H)]
+            got_h = lib_decode(got.residual.reshape(T, H)[t], dt)
+            assert np.array_equal(got_h, np.array([float(v) for v in h])), (dt, t)
+            m = sum(v * v for v in h) / H + e32
+            inv = 1 / (Decimal(m.numerator) / Decimal(m.denominator)).sqrt()
+            assert abs(got.inv[t] - float(inv)) <= 1e-15 * float(inv), (dt, t)
+            want = [rn_exact(Fraction(Decimal(v.numerator) / Decimal(v.denominator) * inv *
+                                      Decimal(gd[i])), dt) for i, v in enumerate(h)]
+            assert np.array_equal(lib_decode(got.y.reshape(T, H)[t], dt), np.array(want)), (dt, t)
+
+
+def pin_gemm_strides(O):
+    """Row strides for A, W, the residual and y (padding holding garbage):
+    the dense results, the padding of the residual untouched."""
+    rng = np.random.default_rng(34)
+    for dt in ("bf16", "f32"):
+        T, H, K = 4, 10, 24
+        lda, ldw, ldr, ldy = 30, 27, 13, 16
+        A = _rand_bits(rng, (T, K), dt)
+        W = _rand_bits(rng, (H, K), dt, scale=0.2)
+        r = _rand_bits(rng, (T, H), dt)
+        g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+        dense = _gemm(O, dt, A, W, r.reshape(-1).copy(), g, 1e-5)
+        Rs = _strided(r, ldr, dt)
+        got = O.gemm_add_rms_norm(dt, _strided(A, lda, dt), _strided(W, ldw, dt), Rs, g, 1e-5,
+                                  T, H, K, lda, ldw, ldr, ldy)
+        assert np.array_equal(got.y.reshape(T, ldy)[:, :H], dense.y.reshape(T, H)), dt
+        assert np.array_equal(_rows(Rs, T, ldr, H), dense.residual.reshape(T, H)), dt
+        pad = Rs.reshape(T, ldr)[:, H:]
+        assert np.array_equal(pad, np.full_like(pad, GARBAGE[dt])), dt
+
+
 ALL_PINS = [
     pin_decode_all_patterns,
     pin_round_matches_library,
@@ -737,4 +852,9 @@ ALL_PINS = [
     pin_fp8_tensor_scale_closed_form,
     pin_fp8_row_scale,
     pin_fp8_strides,
+    pin_gemm_product_library,
+    pin_gemm_identity_is_fused,
+    pin_gemm_one_rounding,
+    pin_gemm_brute_force_tiny,
+    pin_gemm_strides,
 ]

@@ -82,6 +82,27 @@ MUTATIONS = {
     "fp8_code_stride": ("codes[t * ldq + i]", "codes[t * H + i]"),
     # gamma dropped from the 8-bit path
     "fp8_no_gamma": ("v[i] = (h[i] * inv) * load_elem(dt, gamma, i);", "v[i] = h[i] * inv;"),
+    # GEMM producer: strides ignored, a product dropped, |.| dropped
+    "gemm_w_stride": ("W64[i * K + k] = load_elem(dt, W, i * ldw + k);",
+                      "W64[i * K + k] = load_elem(dt, W, i * K + k);"),
+    "gemm_a_stride": ("arow[k] = load_elem(g->dt, g->A, t * g->lda + k);",
+                      "arow[k] = load_elem(g->dt, g->A, t * g->K + k);"),
+    "gemm_drop_last_k": ("for (int64_t k = 0; k < K; ++k) {\n            const double prod",
+                         "for (int64_t k = 0; k < K - 1; ++k) {\n            const double prod"),
+    "gemm_abs_signed": ("a += fabs(prod);", "a += prod;"),
+    # the partial rounded on its own first / residual not added or not stored
+    "gemm_round_partial_first": (
+        "h[i] = round_dt(g->dt, P + load_elem(g->dt, g->residual, t * g->ldr + i));",
+        "h[i] = round_dt(g->dt, round_dt(g->dt, P) + load_elem(g->dt, g->residual, "
+        "t * g->ldr + i));"),
+    "gemm_no_residual": (
+        "h[i] = round_dt(g->dt, P + load_elem(g->dt, g->residual, t * g->ldr + i));",
+        "h[i] = round_dt(g->dt, P);"),
+    "gemm_residual_not_stored": (
+        "for (int64_t i = 0; i < H; ++i) store_exact(g->dt, g->residual, t * g->ldr + i, h[i]);",
+        ""),
+    "gemm_gamma_index": ("round_dt(g->dt, (h[i] * inv) * load_elem(g->dt, g->gamma, i))",
+                         "round_dt(g->dt, (h[i] * inv) * load_elem(g->dt, g->gamma, 0))"),
 }
 
 
