@@ -259,6 +259,37 @@ rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows parti
                                          const void *gamma, int64_t T, int64_t H, float eps,
                                          void *stream);
 
+/*
+ * GEMM producer with the fused residual-add RMSNorm as its epilogue: the
+ * partial that the fused form adds to the residual is the product of the
+ * activations A [T, K] and a linear layer's weight W [H, K]:
+ *   P = A W^T                      (binary32 accumulation on the tensor cores)
+ *   h = RN(P + residual)           residual <- h (the accumulator plus the
+ *                                  residual, rounded once; P is never written)
+ *   y = RN((h * inv) * gamma),     inv = rsqrt(mean(h^2) + eps)
+ * ("sm80 GEMM + ReduceScatter": the flux epilogue consumes the accumulator
+ * tile before anything is written; "Tokenweave fused-RMSNorm-AR kernel",
+ * Code walkthrough: the norm steps.)
+ *
+ * Matrices are rarn_rows (row-major, row_stride in elements), all of one
+ * 16-bit type (RARN_BF16 or RARN_F16; RARN_F32 returns UNSUPPORTED); gamma is
+ * [H] of that type.  Bases 16-byte aligned and row strides multiples of 8
+ * elements, else RARN_ERR_UNSUPPORTED.  H must be a multiple of 512 up to
+ * 8192, or of 256 up to 4096 (a thread-block cluster spans each row); T and K
+ * are free (partial tiles read zeros).  The outputs (y, residual) overlap
+ * nothing else (RARN_ERR_ALIAS).  Accuracy: P is a binary32 accumulation, so
+ * h may differ from the exact rounding of P + residual by one unit in the
+ * last place where that exact value lies within the accumulation error of a
+ * rounding boundary.  One kernel launch (tcgen05 tensor cores, TMA, a cluster
+ * of H / 512 or H / 256 CTAs per 128 rows), no memory allocated.
+ */
+rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_rows residual,
+                                   const void *gamma, int64_t T, int64_t H, int64_t K, float eps,
+                                   void *stream);
+
+/* Describe the GEMM kernel's tiling for a problem (pure host logic). */
+rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, char *out, size_t cap);
+
 /* Static text for a status code. */
 const char *rarn_status_string(rarn_status s);
 

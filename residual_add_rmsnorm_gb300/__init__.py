@@ -28,7 +28,7 @@ __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_ho
            "set_path", "get_path", "set_pdl", "get_pdl", "plan", "watchdog", "PATHS",
            "DTYPE_CODES", "rms_norm_ex", "fused_add_rms_norm_ex", "reduce_add_rms_norm_ex",
            "rms_norm_fp8", "fused_add_rms_norm_fp8", "reduce_add_rms_norm_fp8", "plan_fp8",
-           "FP8_FORMATS", "SCALE_MODES"]
+           "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
@@ -129,6 +129,10 @@ def library() -> ctypes.CDLL:
     lib.rarn_plan_fp8.argtypes = [c_int, i64, i64, i32, c_int, c_int, c_int, ctypes.c_char_p,
                                   ctypes.c_size_t]
     lib.rarn_plan_fp8.restype = c_int
+    lib.rarn_gemm_add_rms_norm.argtypes = [Rows, Rows, Rows, Rows, vp, i64, i64, i64, f32, vp]
+    lib.rarn_gemm_add_rms_norm.restype = c_int
+    lib.rarn_plan_gemm.argtypes = [i64, i64, i64, c_int, ctypes.c_char_p, ctypes.c_size_t]
+    lib.rarn_plan_gemm.restype = c_int
     lib.rarn_set_pdl.argtypes = [c_int]
     lib.rarn_set_pdl.restype = c_int
     lib.rarn_get_pdl.argtypes = []
@@ -477,6 +481,37 @@ def plan_fp8(op: str, T: int, H: int, R: int, dtype: str, vec_ok: bool = True,
                                  num_sms, buf, 256)
     if st not in (0, 2):
         _check(st, "rarn_plan_fp8")
+    return buf.value.decode()
+
+
+def gemm_add_rms_norm(a, w, residual, gamma, eps: float, out=None):
+    """The fused form whose partial is a matrix product: P = a @ w.T
+    (a [T, K], w [H, K], bfloat16 or float16; 2-D views with unit stride
+    within a row), residual [T, H] <- RN(P + residual) in place,
+    y = RMSNorm(residual) * gamma into ``out`` (allocated if None)."""
+    import torch
+    T, K = a.shape
+    H = w.shape[0]
+    dev = a.device
+    if tuple(w.shape) != (H, K) or tuple(residual.shape) != (T, H) or gamma.numel() != H:
+        raise ValueError("shape mismatch")
+    _check_tensor("gamma", gamma, a.dtype, dev)
+    if out is None:
+        out = torch.empty(T, H, dtype=a.dtype, device=dev)
+    with torch.cuda.device(dev):
+        _check(library().rarn_gemm_add_rms_norm(
+            _rows("out", out, dev), _rows("a", a, dev), _rows("w", w, dev),
+            _rows("residual", residual, dev), gamma.data_ptr(), T, H, K, float(eps),
+            _stream(dev)), "rarn_gemm_add_rms_norm")
+    return out
+
+
+def plan_gemm(T: int, H: int, K: int, dtype: str = "bf16") -> str:
+    """The GEMM kernel's tiling for a problem (host logic only)."""
+    buf = ctypes.create_string_buffer(256)
+    st = library().rarn_plan_gemm(T, H, K, DTYPE_CODES[dtype], buf, 256)
+    if st not in (0, 2):
+        _check(st, "rarn_plan_gemm")
     return buf.value.decode()
 
 

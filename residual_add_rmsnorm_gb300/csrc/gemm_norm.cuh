@@ -1,0 +1,448 @@
+// gemm_norm.cuh -- a GEMM whose epilogue is the fused residual-add RMSNorm.
+//
+//   P = A W^T          A [T, K] activations, W [H, K] a linear layer's weight
+//   h = RN(P + r)      residual <- h   (the accumulator plus the residual, one rounding)
+//   y = RN((h * inv) * gamma),  inv = rsqrt(mean(h^2) + eps)
+//
+// The partial P is never written: the epilogue consumes the accumulator tile
+// where the matrix unit left it ("sm80 GEMM + ReduceScatter", the flux
+// epilogue, consumes the accumulator tile before anything is written;
+// "Tokenweave fused-RMSNorm-AR kernel", Code walkthrough, for the norm steps).
+//
+// Blackwell mapping (sm_103a):
+//   * one CTA computes a [128 x NS] tile of P (NS = 256 or 512 columns), the
+//     accumulator in tensor memory (TMEM: 128 lanes = rows, NS columns of
+//     binary32);
+//   * a cluster of C = H / NS CTAs covers whole rows: the row's sum of squares
+//     is exchanged through distributed shared memory, so no CTA re-reads
+//     anything from HBM and no global scratch is used;
+//   * operands arrive by TMA (cp.async.bulk.tensor, 2-D tiles, BK-element K
+//     slabs in the BK * 2-byte swizzle) into an S-stage ring; one thread
+//     issues tcgen05.mma (kind::f16, M = 128, N = 256, K = 16) and commits
+//     each stage back to the producer;
+//   * 4 warps: warp 0 lane 0 produces, warp 1 lane 0 issues the MMAs, then
+//     all 128 threads run the epilogue, thread i owning row i of the tile
+//     (TMEM lane i): tcgen05.ld 32 columns at a time, add the residual, round,
+//     store the residual, keep h in TMEM (tcgen05.st) for the second pass.
+//
+// Every mbarrier wait is bounded (global timer); a wait that runs out sets the
+// watchdog word and the CTA's abort flag, the CTA drains what it issued (also
+// bounded), passes the same cluster barriers as its peers, frees its tensor
+// memory and returns with its outputs invalid.
+#pragma once
+
+#include <cuda.h>  // CUtensorMap (type only; the map is encoded on the host)
+
+#include <type_traits>
+
+#include "common.cuh"
+#include "plan.h"
+
+namespace rarn {
+namespace gemm {
+
+constexpr int kBM = 128;       // tile rows = TMEM lanes
+constexpr int kMmaN = 256;     // N of one tcgen05.mma
+constexpr int kMmaK = 16;      // K of one tcgen05.mma (16-bit inputs)
+constexpr int kThreads = 128;  // 4 warps
+constexpr unsigned int kWatchGemm = 4u;  // watchdog bit
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+// Shared-memory layout of one CTA (dynamic, 1024-byte aligned base).
+struct Layout {
+    int a_bytes, b_bytes, stage_bytes, ctl_off, total;
+};
+
+__host__ __device__ constexpr Layout layout(int stages, int ns, int bk) {
+    Layout L{};
+    L.a_bytes = kBM * bk * 2;
+    L.b_bytes = ns * bk * 2;
+    L.stage_bytes = L.a_bytes + L.b_bytes;
+    L.ctl_off = stages * L.stage_bytes;
+    // full[S], empty[S], accum (8 B each), tmem slot, abort word, red[128]
+    L.total = L.ctl_off + (2 * stages + 1) * 8 + 8 + kBM * 4 + 1024;  // + alignment slack
+    return L;
+}
+
+struct Params {
+    void *y;
+    void *residual;
+    const void *gamma;
+    int64_t T, H, K;
+    int64_t ldr, ldy;  // elements
+    float eps;
+    int ns;            // columns per CTA
+    int stages;
+    int kblocks;       // ceil(K / BK)
+    unsigned int *watchdog;
+    unsigned long long wait_limit_ns;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long now_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait on a phase of `bar`.  Gives up when the CTA's abort word is
+// set (unless `ignore_abort`) or after `limit_ns`: then sets the abort word
+// and the watchdog bit and returns false.
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           unsigned int *watchdog, unsigned long long limit_ns,
+                                           bool ignore_abort = false) {
+    if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0 = 0;
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 127u) == 0) {
+            if (!ignore_abort && *abort_flag) return false;
+            const unsigned long long t = now_ns();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > limit_ns) {
+                *abort_flag = 1;
+                atomicOr(watchdog, kWatchGemm);
+                return false;
+            }
+        }
+    }
+}
+
+// 2-D TMA tile load into shared memory, completion on `bar` (byte count).
+// c0 is the innermost (K) coordinate: a multiple of BK, so c0 * 2 bytes is a
+// multiple of 16.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int c0, int c1,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile whose rows are
+// BK * 2 = 128 (or 64) bytes, swizzled in 8-row atoms by the TMA
+// (128-byte / 64-byte swizzle): start address, stride between 8-row groups
+// (8 rows x row bytes), descriptor version 1, swizzle mode.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, int row_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(1) << 16;  // leading byte offset: unused for swizzled K-major
+    d |= static_cast<uint64_t>((8 * row_bytes) >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(row_bytes == 128 ? 2 : 4) << 61;  // 128B / 64B swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: binary32 accumulator, A and B of the same
+// 16-bit type (bf16: 1, f16: 0), both K-major, M = 128, N = 256.
+template <typename T>
+__host__ __device__ constexpr uint32_t instr_desc() {
+    constexpr uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+    return (1u << 4)                   // D: f32
+           | (ab << 7) | (ab << 10)    // A, B type
+           | (0u << 15) | (0u << 16)   // K-major A, B
+           | ((uint32_t)(kMmaN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma this thread issued so far completes.
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+        : "memory");
+}
+
+// 32 lanes x 32 columns of 32-bit TMEM (this warp's lane quarter).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_barrier() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float ld_peer_f32(uint32_t local_saddr, uint32_t rank) {
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// The kernel.  Grid: C x ceil(T / 128) CTAs in clusters of C (C = H / NS);
+// CTA rank c of a cluster owns columns [c * NS, (c + 1) * NS).
+// ---------------------------------------------------------------------------
+template <typename T, int BK>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_norm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
+                Params p) {
+    static_assert(BK == 64 || BK == 32, "K slab of 128 or 64 bytes");
+    constexpr int kRowBytes = BK * 2;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzle atoms
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int S = p.stages, NS = p.ns;
+    const Layout L = layout(S, NS, BK);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.ctl_off);
+    uint64_t *empty = full + S;
+    uint64_t *accum = empty + S;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *red = reinterpret_cast<float *>(tmem_slot + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t crank = cluster_rank();
+    const int C = (int)(p.H / NS);
+    const int64_t m0 = (int64_t)(blockIdx.x / C) * kBM;
+    const int n0 = (int)crank * NS;
+    const uint32_t ncols = NS;  // TMEM columns (power of two >= 32)
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(accum), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(ncols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    grid_dependency_wait();  // A, W and the residual may come from the previous kernel
+
+    const uint32_t idesc = instr_desc<T>();
+    const int KB = p.kblocks;
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer ----
+        int issued = 0;
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % S;
+            if (kb >= S &&
+                !wait_phase(smem_u32(&empty[s]), ((kb / S) - 1) & 1, abort_flag, p.watchdog,
+                            p.wait_limit_ns))
+                break;
+            const uint32_t fb = smem_u32(&full[s]);
+            mbar_arrive_expect_tx(fb, L.stage_bytes);
+            const uint32_t sa = smem_u32(smem + s * L.stage_bytes);
+            const uint32_t sb = sa + L.a_bytes;
+            tma_load_2d(sa, &map_a, kb * BK, (int)m0, fb);
+            for (int h = 0; h < NS / kMmaN; ++h)
+                tma_load_2d(sb + h * kMmaN * kRowBytes, &map_w, kb * BK, n0 + h * kMmaN, fb);
+            issued = kb + 1;
+        }
+        // Drain: every fill issued must land before this CTA's memory goes
+        // away (bounded; only matters after an abort).
+        if (*abort_flag) {
+            const unsigned long long limit = p.wait_limit_ns;
+            for (int kb = issued - S > 0 ? issued - S : 0; kb < issued; ++kb)
+                wait_phase(smem_u32(&full[kb % S]), (kb / S) & 1, abort_flag, p.watchdog, limit,
+                           true);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer ----
+        int done = 0;
+        for (int kb = 0; kb < KB; ++kb) {
+            const int s = kb % S;
+            if (!wait_phase(smem_u32(&full[s]), (kb / S) & 1, abort_flag, p.watchdog,
+                            p.wait_limit_ns))
+                break;
+            tmem_fence_after();
+            const uint32_t sa = smem_u32(smem + s * L.stage_bytes);
+            const uint32_t sb = sa + L.a_bytes;
+#pragma unroll
+            for (int kk = 0; kk < BK / kMmaK; ++kk) {
+                const uint64_t ad = smem_desc(sa + kk * kMmaK * 2, kRowBytes);
+                for (int h = 0; h < NS / kMmaN; ++h) {
+                    const uint64_t bd = smem_desc(sb + h * kMmaN * kRowBytes + kk * kMmaK * 2,
+                                                  kRowBytes);
+                    mma_f16(tmem + h * kMmaN, ad, bd, idesc, (kb | kk) != 0);
+                }
+            }
+            mma_commit(smem_u32(&empty[s]));  // frees the stage once these MMAs are done
+            done = kb + 1;
+        }
+        mma_commit(smem_u32(accum));  // arrives once every MMA issued has completed
+        (void)done;
+    }
+    __syncwarp();
+
+    // ---- epilogue: all 128 threads, thread i = row m0 + i ----
+    const bool ok = wait_phase(smem_u32(accum), 0, abort_flag, p.watchdog, p.wait_limit_ns, true);
+    tmem_fence_after();
+    grid_launch_dependents();
+    const int r = threadIdx.x;
+    const int64_t t = m0 + r;
+    const bool row_ok = ok && !*abort_flag && t < p.T;
+    const uint32_t tbase = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    T *res = reinterpret_cast<T *>(p.residual) + t * p.ldr + n0;
+    float ss = 0.f;
+    for (int c = 0; c < NS; c += 32) {
+        float v[32];
+        tmem_ld32(tbase + c, v);
+        if (row_ok) {
+            float rv[32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float f[8];
+                DT<T>::unpack(ld_stream(res + c + 8 * q), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) rv[8 * q + e] = f[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                v[e] = DT<T>::round(v[e] + rv[e]);  // h: one rounding of acc + residual
+                ss += v[e] * v[e];
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = v[8 * q + e];
+                st_global(res + c + 8 * q, DT<T>::pack(f));
+            }
+        }
+        tmem_st32(tbase + c, v);  // h, for the second pass
+    }
+    tmem_wait_st();
+    red[r] = ss;
+    cluster_barrier();  // every CTA of the cluster has published its partial sums
+    float tot = 0.f;
+    for (int q = 0; q < C; ++q) tot += ld_peer_f32(smem_u32(&red[r]), (uint32_t)q);
+    const float inv = rsqrtf(tot / (float)p.H + p.eps);
+    const T *g = reinterpret_cast<const T *>(p.gamma) + n0;
+    T *y = reinterpret_cast<T *>(p.y) + t * p.ldy + n0;
+    for (int c = 0; c < NS; c += 32) {
+        float v[32];
+        tmem_ld32(tbase + c, v);
+        if (row_ok) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float w[8], f[8];
+                DT<T>::unpack(ld_keep(g + c + 8 * q), w);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = (v[8 * q + e] * inv) * w[e];
+                st_global(y + c + 8 * q, DT<T>::pack(f));
+            }
+        }
+    }
+    tmem_fence_before();
+    cluster_barrier();  // peers are done reading this CTA's partial sums
+    tmem_fence_after();
+    if (warp == 0) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(ncols)
+                     : "memory");
+    }
+}
+
+}  // namespace gemm
+
+}  // namespace rarn

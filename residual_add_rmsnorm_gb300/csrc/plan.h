@@ -119,4 +119,61 @@ cudaError_t launch_stream(const Problem &p, const Plan &plan, cudaStream_t strea
 template <typename T, typename TR>
 cudaError_t launch_cluster(const Problem &p, const Plan &plan, cudaStream_t stream);
 
+// GEMM producer with the fused residual-add RMSNorm epilogue (gemm_norm.cuh).
+struct GemmCall {
+    const void *a;
+    int64_t lda;
+    const void *w;
+    int64_t ldw;
+    void *residual;
+    int64_t ldr;
+    void *y;
+    int64_t ldy;
+    const void *gamma;
+    int64_t T, H, K;
+    float eps;
+    int ns, stages, bk;  // columns per CTA, ring stages, K slab (elements)
+    bool pdl;
+    unsigned int *watchdog;
+};
+
+template <typename T>
+cudaError_t launch_gemm_norm(const GemmCall &c, cudaStream_t stream);
+
+// Clusters of `cluster` CTAs of the GEMM kernel that can be resident at once
+// (0 if the shape cannot be scheduled).
+template <typename T>
+int gemm_norm_max_clusters(int cluster, int ns, int stages, int bk);
+
+// Tile plan of the GEMM kernel: columns per CTA (a cluster spans H), K slab
+// and ring depth within the shared memory of one SM.  ns = 0: unsupported H.
+struct GemmPlan {
+    int ns = 0, cluster = 0, bk = 0, stages = 0, smem = 0;
+    int64_t grid = 0;
+};
+
+inline GemmPlan plan_gemm(int64_t T, int64_t H, int bk_override = 0) {
+    GemmPlan g;
+    constexpr int kMaxCluster = 16, kSmem = 227 * 1024;
+    if (H % 512 == 0 && H / 512 <= kMaxCluster) {
+        g.ns = 512;
+        g.bk = 32;
+    } else if (H % 256 == 0 && H / 256 <= kMaxCluster) {
+        g.ns = 256;
+        g.bk = 64;
+    } else {
+        return g;
+    }
+    if (bk_override == 32 || bk_override == 64) g.bk = bk_override;
+    g.cluster = (int)(H / g.ns);
+    const int stage = (128 + g.ns) * g.bk * 2;
+    const int fixed = 2048 + 1024;  // barriers, partial sums, alignment slack
+    g.stages = (kSmem - fixed) / stage;
+    if (g.stages > 8) g.stages = 8;
+    if (g.stages < 2) return GemmPlan{};
+    g.smem = g.stages * stage + fixed;
+    g.grid = ((T + 127) / 128) * g.cluster;
+    return g;
+}
+
 }  // namespace rarn

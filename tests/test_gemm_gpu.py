@@ -1,0 +1,205 @@
+"""GPU parity of the GEMM producer with the fused residual-add RMSNorm
+epilogue (tcgen05 tensor cores, TMA, a cluster per row block) against the CPU
+oracle.
+
+Bar.  The kernel accumulates P = A W^T in binary32 on the tensor cores; the
+oracle has P exactly.  So the updated residual h must be a correct rounding
+of some value within the accumulation error of P + r: RN(P + r - B) <= h <=
+RN(P + r + B), with B = (ceil(K / 16) + 8) * 2^-23 * sum_k |A_tk W_ik| plus
+one binary32 rounding of the sum -- a binary32 accumulation in 16-element
+chunks.  Away from cancellation that is h = RN(P + r) or its neighbour at a
+near-tie.  y must be within 2 units in the last place of the oracle's y plus
+the residual's own distance at that element (y is computed from h)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import residual_add_rmsnorm_gb300 as rarn
+from residual_add_rmsnorm_gb300 import workloads as W
+
+from gpu_util import to_device, to_host
+from pins import lib_decode, ulp_dist
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _reset():
+    yield
+    rarn.set_pdl(True)
+
+
+def gemm_inputs(T, H, K, dt, seed):
+    """A ~ N(0, 1), W ~ N(0, 1 / K) (so P ~ N(0, 1)), residual ~ N(0, 1),
+    gamma ~ U(0.5, 1.5), as storage bits."""
+    rng = np.random.default_rng(seed)
+    A = W.to_storage(rng.standard_normal((T, K)).astype(np.float32), dt)
+    Wt = W.to_storage((rng.standard_normal((H, K)) / math.sqrt(K)).astype(np.float32), dt)
+    R = W.to_storage(rng.standard_normal((T, H)).astype(np.float32), dt)
+    G = W.to_storage(rng.uniform(0.5, 1.5, H).astype(np.float32), dt)
+    return A, Wt, R, G
+
+
+def ulp_of(v, dt):
+    """Unit in the last place of the storage-format values v (binary64)."""
+    p, emin = {"bf16": (8, -126), "f16": (11, -14), "f32": (24, -126)}[dt]
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(np.where(a > 0, e, emin), emin)
+    return np.exp2(e - (p - 1))
+
+
+def check_gemm(ref, K, y, res, dt, what, rows=None):
+    """ref: oracle Result (residual, y, p64, abs64) for the rows checked."""
+    T, H = ref.p64.shape
+    r_in = ref.r_in
+    exact = ref.p64 + r_in
+    B = (math.ceil(K / 16) + 8) * 2.0 ** -23 * ref.abs64
+    B = B + 2.0 ** -24 * (np.abs(exact) + B)
+    O = oracle.default()
+    lo = lib_decode(O.round_to(exact - B, dt), dt)
+    hi = lib_decode(O.round_to(exact + B, dt), dt)
+    h = lib_decode(res, dt).reshape(T, H)
+    outside = (h < lo) | (h > hi)
+    assert not outside.any(), (f"{what}: {int(outside.sum())} residual elements outside the "
+                               f"accumulation bound, e.g. {np.argwhere(outside)[:3].tolist()}")
+    # y = RN((h inv) gamma): the GPU's h may differ from the oracle's by the
+    # amount allowed above; that difference scales by inv |gamma| into y, on
+    # top of two units in the last place of y (two roundings, inv's binary32
+    # evaluation)
+    h_o = lib_decode(ref.residual, dt).reshape(T, H)
+    y_o = lib_decode(ref.y, dt).reshape(T, H)
+    y_g = lib_decode(y, dt).reshape(T, H)
+    allow = 2 * ulp_of(y_o, dt) + np.abs(h - h_o) * ref.inv[:, None] * np.abs(ref.gamma) * 1.01
+    over = np.abs(y_g - y_o) > allow
+    assert not over.any(), (f"{what}: {int(over.sum())} y elements beyond 2 ulps plus the "
+                            f"residual's difference, e.g. {np.argwhere(over)[:3].tolist()}")
+
+
+def run_case(T, H, K, dt="bf16", seed=0, lda=None, ldw=None, ldr=None, ldy=None, eps=1e-6,
+             sample_rows=None):
+    import torch
+    lda, ldw, ldr, ldy = lda or K, ldw or K, ldr or H, ldy or H
+    A, Wt, R, G = gemm_inputs(T, H, K, dt, seed)
+
+    def strided(bits, rows, cols, ld):
+        full = torch.zeros(rows, ld, dtype=to_device(bits[:1], dt).dtype, device="cuda")
+        full[:, :cols] = to_device(bits, dt)
+        return full, full[:, :cols]
+
+    _, a = strided(A, T, K, lda)
+    _, w = strided(Wt, H, K, ldw)
+    rfull, r = strided(R, T, H, ldr)
+    yfull, y = strided(np.zeros((T, H), R.dtype), T, H, ldy)
+    g = to_device(G, dt)
+    plan = rarn.plan_gemm(T, H, K, dt)
+    try:
+        rarn.gemm_add_rms_norm(a, w, r, g, eps, out=y)
+    except rarn.RarnError as e:
+        if e.status == 2 and "cluster=1" not in plan and int(plan.split("cluster=")[1].split()[0]) > 8:
+            pytest.skip(f"clusters larger than 8 cannot be scheduled here ({plan})")
+        raise
+    torch.cuda.synchronize()
+    assert rarn.watchdog(clear=True) == 0
+    rows = np.arange(T) if sample_rows is None else sample_rows
+    As = np.ascontiguousarray(A[rows])
+    Rs = np.ascontiguousarray(R[rows]).reshape(-1).copy()
+    ref = oracle.gemm_add_rms_norm(dt, As.reshape(-1), Wt.reshape(-1), Rs, G, eps, len(rows), H,
+                                   K, want_p64=True)
+    ref.residual = ref.residual.reshape(len(rows), H)
+    ref.y = ref.y.reshape(len(rows), H)
+    ref.r_in = lib_decode(R[rows], dt)
+    ref.gamma = lib_decode(G, dt)
+    res_h = to_host(r.contiguous(), dt)[rows]
+    y_h = to_host(y.contiguous(), dt)[rows]
+    check_gemm(ref, K, y_h, res_h, dt, f"gemm {dt} T{T} H{H} K{K} ({plan})")
+    # padding of the strided outputs untouched
+    if ldr > H:
+        assert torch.all(rfull[:, H:] == 0)
+    if ldy > H:
+        assert torch.all(yfull[:, H:] == 0)
+    return plan
+
+
+@pytest.mark.parametrize("T,H,K", [
+    (128, 512, 64),      # one CTA, one cluster of 1, two K slabs
+    (200, 1024, 200),    # ragged rows and K, a cluster of 2, the ring wraps
+    (256, 4096, 1024),   # a cluster of 8 (512 columns per CTA)
+    (300, 768, 512),     # 256 columns per CTA, a cluster of 3, 64-element K slabs
+    (1, 2048, 4096),     # one row (decode), long K
+    (77, 8192, 256),     # a cluster of 16 (non-portable size)
+    (130, 5120, 320),    # a cluster of 10
+])
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_gemm_parity(T, H, K, dt):
+    plan = run_case(T, H, K, dt, seed=T + H + K)
+    assert plan.startswith("gemm.tcgen05"), plan
+
+
+@pytest.mark.parametrize("bk", ["32", "64"])
+def test_gemm_k_slab_widths(bk, monkeypatch):
+    """Both operand layouts (64-byte and 128-byte swizzled K slabs)."""
+    monkeypatch.setenv("RARN_GEMM_BK", bk)
+    for T, H, K in ((256, 1024, 448), (64, 512, 1000)):
+        plan = run_case(T, H, K, "bf16", seed=K)
+        assert f"bk={bk}" in plan, plan
+
+
+def test_gemm_strides():
+    """Row strides for every matrix; padding of the outputs untouched."""
+    run_case(150, 1024, 136, "bf16", seed=5, lda=200, ldw=144, ldr=1096, ldy=1032)
+
+
+@pytest.mark.parametrize("pdl", [True, False])
+def test_gemm_chained_with_norm_kernels(pdl):
+    """A chain on one stream: GEMM + norm, the fused norm kernel on its
+    output, the GEMM again -- the residual carries over; PDL on and off."""
+    import torch
+    rarn.set_pdl(pdl)
+    T, H, K = 512, 2048, 512
+    A, Wt, R, G = gemm_inputs(T, H, K, "bf16", 11)
+    a, w, r, g = (to_device(A, "bf16"), to_device(Wt, "bf16"), to_device(R, "bf16"),
+                  to_device(G, "bf16"))
+    y = rarn.gemm_add_rms_norm(a, w, r, g, 1e-6)
+    rarn.fused_add_rms_norm(y, r, g, 1e-6)   # residual += y
+    y2 = rarn.gemm_add_rms_norm(a, w, r, g, 1e-6)
+    torch.cuda.synchronize()
+    # replay on the host side with the oracle, step by step, from the GPU's
+    # inputs only (no GPU value feeds the oracle)
+    res = R.reshape(-1).copy()
+    o1 = oracle.gemm_add_rms_norm("bf16", A.reshape(-1), Wt.reshape(-1), res, G, 1e-6, T, H, K)
+    o2 = oracle.fused_add_rms_norm(o1.y.reshape(T, H), o1.residual.reshape(T, H), G, 1e-6,
+                                   "bf16")
+    res2 = o2.residual.reshape(-1).copy()
+    o3 = oracle.gemm_add_rms_norm("bf16", A.reshape(-1), Wt.reshape(-1), res2, G, 1e-6, T, H, K)
+    # the chain amplifies near-tie roundings only slightly: compare in ulps
+    d_r = ulp_dist(to_host(r, "bf16").reshape(-1), o3.residual, "bf16")
+    d_y = ulp_dist(to_host(y2, "bf16").reshape(-1), o3.y, "bf16")
+    assert np.percentile(d_r, 99.9) <= 1 and np.percentile(d_y, 99.9) <= 2
+    assert np.mean(d_r == 0) > 0.999 and np.mean(d_y <= 1) > 0.999
+
+
+def test_gemm_full_size_sampled():
+    """The benchmark shape (T = K = H = 4096, bf16) in its launch
+    configuration; the oracle checks 64 sampled rows."""
+    rows = np.linspace(0, 4095, 64).astype(int)
+    plan = run_case(4096, 4096, 4096, "bf16", seed=4096, sample_rows=rows)
+    assert "cluster=8" in plan, plan
+
+
+def test_gemm_rejects():
+    import torch
+    a = torch.zeros(8, 64, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(300, 64, dtype=torch.bfloat16, device="cuda")
+    r = torch.zeros(8, 300, dtype=torch.bfloat16, device="cuda")
+    g = torch.zeros(300, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(rarn.RarnError):  # H = 300: no cluster tiling
+        rarn.gemm_add_rms_norm(a, w, r, g, 1e-6)
+    a32 = torch.zeros(8, 64, dtype=torch.float32, device="cuda")
+    w32 = torch.zeros(512, 64, dtype=torch.float32, device="cuda")
+    r32 = torch.zeros(8, 512, dtype=torch.float32, device="cuda")
+    g32 = torch.zeros(512, dtype=torch.float32, device="cuda")
+    with pytest.raises(rarn.RarnError):  # f32: no tensor path
+        rarn.gemm_add_rms_norm(a32, w32, r32, g32, 1e-6)
