@@ -38,6 +38,7 @@ HEADLINE = "reduce8_bf16_T8192_H8192"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 def _configs():
@@ -444,6 +445,70 @@ def time_graph(w, data, device, l2_bytes, min_launches=200):
     return 1e3 * statistics.median(times) / n, copies, n
 
 
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s measured on this machine's GPUs (burst: a kernel timed
+    alone), else the fallback."""
+    try:
+        with open(PEAKS_FILE) as f:
+            v = json.load(f).get("bf16_tflops")
+        if v:
+            return float(v), "measured bf16_tflops (burst)"
+    except (OSError, ValueError):
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def _graph_us(fn, launches=10, reps=3):
+    """Per-launch device time of fn() replayed in a CUDA graph (best of reps)."""
+    import torch
+    for _ in range(2):
+        fn()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(launches):
+            fn()
+    graph.replay()
+    torch.cuda.synchronize()
+    best = None
+    for _ in range(reps):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        graph.replay()
+        e.record()
+        e.synchronize()
+        t = 1e3 * s.elapsed_time(e) / launches
+        best = t if best is None else min(best, t)
+    return best
+
+
+def time_gemm(gw, device, rarn):
+    """The GEMM-producer form: one tcgen05 kernel (matrix product, residual
+    add, RMSNorm) timed against the unfused sequence the same library offers
+    a user (cuBLAS product through torch.matmul, then the fused norm kernel);
+    TFLOP/s of the 2 T H K product against the measured tensor peak."""
+    import torch
+    from residual_add_rmsnorm_gb300 import workloads as W
+    d = W.generate_gemm(gw)
+    a, w, r, g = (to_device(d[k], gw.dtype, device) for k in ("a", "w", "residual", "gamma"))
+    y = torch.empty_like(r)
+    part = torch.empty_like(r)
+    us = _graph_us(lambda: rarn.gemm_add_rms_norm(a, w, r, g, gw.eps, out=y))
+    us_mm = _graph_us(lambda: torch.matmul(a, w.t(), out=part))
+    us_unfused = _graph_us(lambda: (torch.matmul(a, w.t(), out=part),
+                                    rarn.fused_add_rms_norm(part, r, g, gw.eps, out=y)))
+    peak, kind = measured_tensor_peak()
+    tflops = gw.flops() / (us / 1e6) / 1e12
+    return {"kind": "widened (GEMM producer)", "us_per_launch": us, "tflops": tflops,
+            "frac_of_tensor_peak": tflops / peak, "tensor_peak": peak, "peak_source": kind,
+            "gbs_algorithmic": gw.algorithmic_bytes() / (us / 1e6) / 1e9,
+            "unfused_us": us_unfused, "cublas_matmul_us": us_mm,
+            "timing": "CUDA graph of 10 launches, best of 3 (operands L2-resident after the "
+                      "first launch)",
+            "plan": rarn.plan_gemm(gw.T, gw.H, gw.K, gw.dtype)}
+
+
 def e2e_steps(w, data, steps, device, stream):
     """End to end through the public host-buffer API: the inputs start in
     pinned host memory and the outputs end there.  Each step is one call of
@@ -541,6 +606,8 @@ def main():
                 "plan": plan_of(cw, rarn)}
             del cd
             torch.cuda.empty_cache()
+        for gw in W.GEMM_CONFIGS:
+            per_config[gw.name] = time_gemm(gw, device, rarn)
         if rarn.watchdog(clear=True):
             watchdog = 1
 

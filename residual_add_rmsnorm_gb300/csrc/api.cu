@@ -772,9 +772,10 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     if (!y.data || !a.data || !w.data || !residual.data || !gamma) return RARN_ERR_INVALID_ARG;
     if (dt == RARN_F32) return RARN_ERR_UNSUPPORTED;  // the tensor path takes 16-bit operands
     if (T > (int64_t(1) << 31) - 128 || K > (int64_t(1) << 31) - 64) return RARN_ERR_UNSUPPORTED;
-    int bk_env = 0;
-    if (const char *v = getenv("RARN_GEMM_BK")) bk_env = atoi(v);  // measurements only
-    const GemmPlan gp = plan_gemm(T, H, bk_env);
+    int bk_env = 0, ns_env = 0;  // measurements only
+    if (const char *v = getenv("RARN_GEMM_BK")) bk_env = atoi(v);
+    if (const char *v = getenv("RARN_GEMM_NS")) ns_env = atoi(v);
+    const GemmPlan gp = plan_gemm(T, H, bk_env, ns_env);
     if (gp.ns == 0) return RARN_ERR_UNSUPPORTED;
     auto al16 = [](const void *ptr, int64_t ld) {
         return aligned16(ptr) && (ld * 2) % 16 == 0;
@@ -828,9 +829,10 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
 rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, char *out, size_t cap) {
     if (!out || cap == 0) return RARN_ERR_INVALID_ARG;
     if (!dtype_ok(dt) || T < 0 || H <= 0 || K <= 0) return RARN_ERR_INVALID_ARG;
-    int bk_env = 0;
+    int bk_env = 0, ns_env = 0;
     if (const char *v = getenv("RARN_GEMM_BK")) bk_env = atoi(v);
-    const GemmPlan gp = dt == RARN_F32 ? GemmPlan{} : plan_gemm(T, H, bk_env);
+    if (const char *v = getenv("RARN_GEMM_NS")) ns_env = atoi(v);
+    const GemmPlan gp = dt == RARN_F32 ? GemmPlan{} : plan_gemm(T, H, bk_env, ns_env);
     if (gp.ns == 0) {
         snprintf(out, cap, "none: unsupported shape or type");
         return RARN_ERR_UNSUPPORTED;

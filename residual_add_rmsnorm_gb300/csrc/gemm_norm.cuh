@@ -22,8 +22,13 @@
 //     each stage back to the producer;
 //   * 4 warps: warp 0 lane 0 produces, warp 1 lane 0 issues the MMAs, then
 //     all 128 threads run the epilogue, thread i owning row i of the tile
-//     (TMEM lane i): tcgen05.ld 32 columns at a time, add the residual, round,
-//     store the residual, keep h in TMEM (tcgen05.st) for the second pass.
+//     (TMEM lane i).  The operand ring is free once the MMAs are done, so it
+//     stages the epilogue: the residual tile arrives by TMA in [128 x 32]
+//     chunks (64-byte rows, 64-byte swizzle: a thread's 16-byte accesses to its
+//     own row are free of bank conflicts); each thread adds its accumulator
+//     row (tcgen05.ld), rounds, writes h back into the chunk and keeps it in
+//     TMEM (tcgen05.st); the chunk goes back to the residual by a TMA store.
+//     The second pass writes y through the same chunks.
 //
 // Every mbarrier wait is bounded (global timer); a wait that runs out sets the
 // watchdog word and the CTA's abort flag, the CTA drains what it issued (also
@@ -47,6 +52,9 @@ constexpr int kMmaK = 16;      // K of one tcgen05.mma (16-bit inputs)
 constexpr int kThreads = 128;  // 4 warps
 constexpr unsigned int kWatchGemm = 4u;  // watchdog bit
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+constexpr int kChunkCols = 32;                      // epilogue chunk: 128 rows x 32 columns
+constexpr int kChunkBytes = kBM * kChunkCols * 2;   // 8 KB
+constexpr int kMaxChunks = 16;                      // 512 columns per CTA
 
 // Shared-memory layout of one CTA (dynamic, 1024-byte aligned base).
 struct Layout {
@@ -59,8 +67,9 @@ __host__ __device__ constexpr Layout layout(int stages, int ns, int bk) {
     L.b_bytes = ns * bk * 2;
     L.stage_bytes = L.a_bytes + L.b_bytes;
     L.ctl_off = stages * L.stage_bytes;
-    // full[S], empty[S], accum (8 B each), tmem slot, abort word, red[128]
-    L.total = L.ctl_off + (2 * stages + 1) * 8 + 8 + kBM * 4 + 1024;  // + alignment slack
+    // full[S], empty[S], accum, chunk[16] (8 B each), tmem slot, abort word,
+    // red[128]
+    L.total = L.ctl_off + (2 * stages + 1 + kMaxChunks) * 8 + 8 + kBM * 4 + 1024;  // + slack
     return L;
 }
 
@@ -149,6 +158,54 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
         : "memory");
+}
+
+// 2-D TMA tile store from shared memory (bulk group); rows and columns
+// outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int c0, int c1, uint32_t src) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(c0), "r"(c1), "r"(src)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// This thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// This thread's bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Make this thread's shared-memory writes visible to the TMA (async proxy).
+__device__ __forceinline__ void fence_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4 &v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Barrier over the CTA's 128 threads (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void epi_barrier() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
 }
 
 __device__ __forceinline__ void tmem_fence_before() {
@@ -271,6 +328,7 @@ __device__ __forceinline__ float ld_peer_f32(uint32_t local_saddr, uint32_t rank
 template <typename T, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_norm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
+                const __grid_constant__ CUtensorMap map_r, const __grid_constant__ CUtensorMap map_y,
                 Params p) {
     static_assert(BK == 64 || BK == 32, "K slab of 128 or 64 bytes");
     constexpr int kRowBytes = BK * 2;
@@ -283,7 +341,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.ctl_off);
     uint64_t *empty = full + S;
     uint64_t *accum = empty + S;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1);
+    uint64_t *chunk_bar = accum + 1;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(chunk_bar + kMaxChunks);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *red = reinterpret_cast<float *>(tmem_slot + 2);
 
@@ -300,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&empty[s]), 1);
         }
         mbar_init(smem_u32(accum), 1);
+        for (int c = 0; c < kMaxChunks; ++c) mbar_init(smem_u32(&chunk_bar[c]), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -375,41 +435,54 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
 
     // ---- epilogue: all 128 threads, thread i = row m0 + i ----
-    const bool ok = wait_phase(smem_u32(accum), 0, abort_flag, p.watchdog, p.wait_limit_ns, true);
+    wait_phase(smem_u32(accum), 0, abort_flag, p.watchdog, p.wait_limit_ns, true);
     tmem_fence_after();
+    __syncthreads();
+    const bool ok = !*abort_flag;  // the same snapshot in every thread
     grid_launch_dependents();
     const int r = threadIdx.x;
-    const int64_t t = m0 + r;
-    const bool row_ok = ok && !*abort_flag && t < p.T;
     const uint32_t tbase = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    T *res = reinterpret_cast<T *>(p.residual) + t * p.ldr + n0;
-    float ss = 0.f;
-    for (int c = 0; c < NS; c += 32) {
-        float v[32];
-        tmem_ld32(tbase + c, v);
-        if (row_ok) {
-            float rv[32];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float f[8];
-                DT<T>::unpack(ld_stream(res + c + 8 * q), f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) rv[8 * q + e] = f[e];
-            }
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                v[e] = DT<T>::round(v[e] + rv[e]);  // h: one rounding of acc + residual
-                ss += v[e] * v[e];
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float f[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = v[8 * q + e];
-                st_global(res + c + 8 * q, DT<T>::pack(f));
-            }
+    const int nchunks = NS / kChunkCols;
+    const uint32_t ring = smem_u32(smem);  // every MMA has completed: the ring is free
+    // byte offset of 16-byte piece q of row r within a chunk (64-byte swizzle:
+    // the piece index is XORed with bits 1-2 of the row)
+    const uint32_t row_off = static_cast<uint32_t>(r) * 64u;
+    const uint32_t swz = (static_cast<uint32_t>(r) >> 1) & 3u;
+    if (ok && threadIdx.x == 0) {
+        for (int c = 0; c < nchunks; ++c) {
+            const uint32_t cb = smem_u32(&chunk_bar[c]);
+            mbar_arrive_expect_tx(cb, kChunkBytes);
+            tma_load_2d(ring + c * kChunkBytes, &map_r, n0 + c * kChunkCols, (int)m0, cb);
         }
-        tmem_st32(tbase + c, v);  // h, for the second pass
+    }
+    float ss = 0.f;
+    for (int c = 0; c < nchunks; ++c) {
+        float v[32];
+        tmem_ld32(tbase + c * kChunkCols, v);
+        const uint32_t ca = ring + c * kChunkBytes + row_off;
+        if (ok) {
+            wait_phase(smem_u32(&chunk_bar[c]), 0, abort_flag, p.watchdog, p.wait_limit_ns, true);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float f[8];
+                const uint32_t a = ca + ((q ^ swz) << 4);
+                DT<T>::unpack(lds128(a), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    f[e] = DT<T>::round(v[8 * q + e] + f[e]);  // h: one rounding of acc + r
+                    ss += f[e] * f[e];
+                    v[8 * q + e] = f[e];
+                }
+                sts128(a, DT<T>::pack(f));
+            }
+            fence_async_shared();
+        }
+        tmem_st32(tbase + c * kChunkCols, v);  // h, for the second pass
+        epi_barrier();
+        if (ok && threadIdx.x == 0) {
+            tma_store_2d(&map_r, n0 + c * kChunkCols, (int)m0, ring + c * kChunkBytes);
+            bulk_commit();
+        }
     }
     tmem_wait_st();
     red[r] = ss;
@@ -417,20 +490,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     float tot = 0.f;
     for (int q = 0; q < C; ++q) tot += ld_peer_f32(smem_u32(&red[r]), (uint32_t)q);
     const float inv = rsqrtf(tot / (float)p.H + p.eps);
+    if (threadIdx.x == 0) bulk_wait_read_all();  // the chunks are free again
+    epi_barrier();
     const T *g = reinterpret_cast<const T *>(p.gamma) + n0;
-    T *y = reinterpret_cast<T *>(p.y) + t * p.ldy + n0;
-    for (int c = 0; c < NS; c += 32) {
+    for (int c = 0; c < nchunks; ++c) {
         float v[32];
-        tmem_ld32(tbase + c, v);
-        if (row_ok) {
+        tmem_ld32(tbase + c * kChunkCols, v);
+        const uint32_t ca = ring + c * kChunkBytes + row_off;
+        if (ok) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float w[8], f[8];
-                DT<T>::unpack(ld_keep(g + c + 8 * q), w);
+                DT<T>::unpack(ld_keep(g + c * kChunkCols + 8 * q), w);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) f[e] = (v[8 * q + e] * inv) * w[e];
-                st_global(y + c + 8 * q, DT<T>::pack(f));
+                sts128(ca + ((q ^ swz) << 4), DT<T>::pack(f));
             }
+            fence_async_shared();
+        }
+        epi_barrier();
+        if (ok && threadIdx.x == 0) {
+            tma_store_2d(&map_y, n0 + c * kChunkCols, (int)m0, ring + c * kChunkBytes);
+            bulk_commit();
+        }
+    }
+    if (threadIdx.x == 0) {
+        bulk_wait_all();  // the stores have completed before this CTA's memory goes away
+        if (*abort_flag) {  // loads issued after an abort elsewhere must still land (bounded)
+            for (int c = 0; ok && c < nchunks; ++c)
+                wait_phase(smem_u32(&chunk_bar[c]), 0, abort_flag, p.watchdog, p.wait_limit_ns,
+                           true);
         }
     }
     tmem_fence_before();

@@ -48,9 +48,14 @@ template <typename T, int BK>
 static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     using namespace gemm;
     const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
-    CUtensorMap ma, mw;
+    CUtensorMap ma, mw, mr, my;
     if (!encode_map(&ma, c.a, c.T, c.K, c.lda, kBM, BK, bf16) ||
-        !encode_map(&mw, c.w, c.H, c.K, c.ldw, kMmaN, BK, bf16))
+        !encode_map(&mw, c.w, c.H, c.K, c.ldw, kMmaN, BK, bf16) ||
+        !encode_map(&mr, c.residual, c.T, c.H, c.ldr, kBM, kChunkCols, bf16) ||
+        !encode_map(&my, c.y, c.T, c.H, c.ldy, kBM, kChunkCols, bf16))
+        return cudaErrorInvalidValue;
+    // the epilogue stages the residual / y tile in the operand ring
+    if (c.stages * layout(c.stages, c.ns, BK).stage_bytes < (c.ns / kChunkCols) * kChunkBytes)
         return cudaErrorInvalidValue;
     Params p{};
     p.y = c.y;
@@ -78,7 +83,7 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
         return e;
     const int64_t mblocks = (c.T + kBM - 1) / kBM;
     return launch_kernel(kernel, dim3(static_cast<unsigned>(mblocks * C)), dim3(kThreads),
-                         static_cast<size_t>(smem), st, c.pdl, C, ma, mw, p);
+                         static_cast<size_t>(smem), st, c.pdl, C, ma, mw, mr, my, p);
 }
 
 template <typename T>

@@ -152,10 +152,13 @@ struct GemmPlan {
     int64_t grid = 0;
 };
 
-inline GemmPlan plan_gemm(int64_t T, int64_t H, int bk_override = 0) {
+inline GemmPlan plan_gemm(int64_t T, int64_t H, int bk_override = 0, int ns_override = 0) {
     GemmPlan g;
     constexpr int kMaxCluster = 16, kSmem = 227 * 1024;
-    if (H % 512 == 0 && H / 512 <= kMaxCluster) {
+    if (ns_override == 256 && H % 256 == 0 && H / 256 <= kMaxCluster) {
+        g.ns = 256;
+        g.bk = 64;
+    } else if (H % 512 == 0 && H / 512 <= kMaxCluster) {
         g.ns = 512;
         g.bk = 32;
     } else if (H % 256 == 0 && H / 256 <= kMaxCluster) {

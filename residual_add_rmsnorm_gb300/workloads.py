@@ -26,6 +26,9 @@ Recipe (seed s):
 * Reduce partials are N(0, partial_std^2); x and residual are N(0, 1).
 * A binary32 residual (``rdtype="f32"``) keeps the binary32 draws of its
   stream without rounding to the inputs' type.
+* GEMM-producer workloads (``GemmWorkload``): A [T, K] ~ N(0, 1) (stream 0,
+  blocks of CHUNK_ROWS rows), W [H, K] ~ N(0, 1 / K) (stream 1), residual
+  [T, H] ~ N(0, 1) (stream 2), gamma as above; so P = A W^T ~ N(0, 1).
 
 Arrays hold raw storage bits: ``np.float32`` for f32, ``np.uint16`` for f16 and
 bf16.
@@ -134,6 +137,62 @@ EXTENDED = [
              R=1, qfmt="e4m3", qmode="tensor", qscale=0.02),
 ]
 BY_NAME = {w.name: w for w in CONFIGS + EXTENDED}
+
+
+@dataclass(frozen=True)
+class GemmWorkload:
+    """The fused form whose partial is a matrix product: A [T, K] times a
+    linear layer's weight W [H, K] (transposed), plus the residual, RMSNorm."""
+    name: str
+    dtype: str
+    T: int
+    H: int
+    K: int
+    eps: float
+    seed: int = 0
+
+    def flops(self) -> int:
+        return 2 * self.T * self.H * self.K
+
+    def algorithmic_bytes(self) -> int:
+        """A and W read once, the residual read and written, y written, gamma."""
+        s = ELEM_SIZE[self.dtype]
+        return s * (self.T * self.K + self.H * self.K + 3 * self.T * self.H + self.H)
+
+
+# The GEMM-producer workload: the fused form's [4096, 4096] shape (C3) with
+# its partial produced by a 4096 x 4096 projection.
+GEMM_CONFIGS = [GemmWorkload("gemm_fused_bf16_T4096_K4096_H4096", "bf16", 4096, 4096, 4096, 1e-6)]
+
+
+def generate_gemm(w: GemmWorkload, rows: tuple[int, int] | None = None) -> dict:
+    """Inputs of a GEMM workload as storage bits: 'a' [T', K], 'w' [H, K],
+    'residual' [T', H], 'gamma' [H]; ``rows`` as for ``generate``."""
+    T, H, K = w.T, w.H, w.K
+    a, b = (0, T) if rows is None else rows
+    if not 0 <= a <= b <= T:
+        raise ValueError(f"rows {rows} outside 0..{T}")
+
+    def draw(stream, nrows, ncols, lo, hi, scale):
+        out = np.empty((hi - lo, ncols), STORAGE[w.dtype])
+
+        def block(c):
+            r0, r1 = c * CHUNK_ROWS, min((c + 1) * CHUNK_ROWS, nrows)
+            z = _normal_f32(_rng(w.seed, stream, c), (r1 - r0) * ncols).reshape(r1 - r0, ncols)
+            l2, h2 = max(r0, lo), min(r1, hi)
+            z = z[l2 - r0:h2 - r0]
+            if scale != 1.0:
+                z = z * np.float32(scale)
+            out[l2 - lo:h2 - lo] = to_storage(z, w.dtype)
+
+        if hi > lo:
+            with _pool() as ex:
+                list(ex.map(block, range(lo // CHUNK_ROWS, (hi + CHUNK_ROWS - 1) // CHUNK_ROWS)))
+        return out
+
+    g = _rng(w.seed, GAMMA_KEY).uniform(0.5, 1.5, size=H).astype(np.float32)
+    return {"a": draw(0, T, K, a, b, 1.0), "w": draw(1, H, K, 0, H, 1.0 / math.sqrt(K)),
+            "residual": draw(2, T, H, a, b, 1.0), "gamma": to_storage(g, w.dtype)}
 
 
 def workload(op: str, dtype: str, T: int, H: int, *, R: int | None = None, eps: float = 1e-6,
