@@ -271,23 +271,34 @@ rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows parti
  * tile before anything is written; "Tokenweave fused-RMSNorm-AR kernel",
  * Code walkthrough: the norm steps.)
  *
+ * Two kernels on `stream`: the tcgen05 GEMM whose epilogue writes h and, per
+ * row and column tile, the partial sum of squares of h into `workspace`; then
+ * a norm kernel that sums each row's partials in tile order and writes y.
+ * `workspace` is caller-owned device memory of at least
+ * rarn_gemm_workspace_bytes(T, H) bytes (4-byte aligned); its contents are
+ * scratch and need no initialisation.
+ *
  * Matrices are rarn_rows (row-major, row_stride in elements), all of one
  * 16-bit type (RARN_BF16 or RARN_F16; RARN_F32 returns UNSUPPORTED); gamma is
  * [H] of that type.  Bases 16-byte aligned and row strides multiples of 8
  * elements, else RARN_ERR_UNSUPPORTED.  H must be a multiple of 512 up to
- * 8192, or of 256 up to 4096 (a thread-block cluster spans each row); T and K
- * are free (partial tiles read zeros).  The outputs (y, residual) overlap
- * nothing else (RARN_ERR_ALIAS).  Accuracy: P is a binary32 accumulation, so
- * h may differ from the exact rounding of P + residual by one unit in the
- * last place where that exact value lies within the accumulation error of a
- * rounding boundary.  One kernel launch (tcgen05 tensor cores, TMA, a cluster
- * of H / 512 or H / 256 CTAs per 128 rows), no memory allocated.
+ * 16384, or of 256 up to 8192 (else UNSUPPORTED); T and K are free (partial
+ * tiles read zeros).  A
+ * missing or short workspace returns RARN_ERR_INVALID_ARG; outputs (y, the
+ * residual, the workspace) overlapping anything else return RARN_ERR_ALIAS.
+ * Accuracy: P is a binary32 accumulation, so h may differ from the exact
+ * rounding of P + residual by one unit in the last place where that exact
+ * value lies within the accumulation error of a rounding boundary.
  */
 rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_rows residual,
                                    const void *gamma, int64_t T, int64_t H, int64_t K, float eps,
-                                   void *stream);
+                                   void *workspace, size_t workspace_bytes, void *stream);
 
-/* Describe the GEMM kernel's tiling for a problem (pure host logic). */
+/* Workspace bytes rarn_gemm_add_rms_norm needs for T rows of H (-1 if H is
+ * not supported). */
+int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H);
+
+/* Describe the GEMM kernels' tiling for a problem (pure host logic). */
 rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, char *out, size_t cap);
 
 /* Static text for a status code. */

@@ -28,7 +28,8 @@ __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_ho
            "set_path", "get_path", "set_pdl", "get_pdl", "plan", "watchdog", "PATHS",
            "DTYPE_CODES", "rms_norm_ex", "fused_add_rms_norm_ex", "reduce_add_rms_norm_ex",
            "rms_norm_fp8", "fused_add_rms_norm_fp8", "reduce_add_rms_norm_fp8", "plan_fp8",
-           "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm"]
+           "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm",
+           "gemm_workspace_bytes"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
@@ -129,8 +130,11 @@ def library() -> ctypes.CDLL:
     lib.rarn_plan_fp8.argtypes = [c_int, i64, i64, i32, c_int, c_int, c_int, ctypes.c_char_p,
                                   ctypes.c_size_t]
     lib.rarn_plan_fp8.restype = c_int
-    lib.rarn_gemm_add_rms_norm.argtypes = [Rows, Rows, Rows, Rows, vp, i64, i64, i64, f32, vp]
+    lib.rarn_gemm_add_rms_norm.argtypes = [Rows, Rows, Rows, Rows, vp, i64, i64, i64, f32, vp,
+                                           ctypes.c_size_t, vp]
     lib.rarn_gemm_add_rms_norm.restype = c_int
+    lib.rarn_gemm_workspace_bytes.argtypes = [i64, i64]
+    lib.rarn_gemm_workspace_bytes.restype = i64
     lib.rarn_plan_gemm.argtypes = [i64, i64, i64, c_int, ctypes.c_char_p, ctypes.c_size_t]
     lib.rarn_plan_gemm.restype = c_int
     lib.rarn_set_pdl.argtypes = [c_int]
@@ -484,11 +488,18 @@ def plan_fp8(op: str, T: int, H: int, R: int, dtype: str, vec_ok: bool = True,
     return buf.value.decode()
 
 
-def gemm_add_rms_norm(a, w, residual, gamma, eps: float, out=None):
+def gemm_workspace_bytes(T: int, H: int) -> int:
+    """Workspace bytes the GEMM form needs for T rows of H (-1: H unsupported)."""
+    return int(library().rarn_gemm_workspace_bytes(T, H))
+
+
+def gemm_add_rms_norm(a, w, residual, gamma, eps: float, out=None, workspace=None):
     """The fused form whose partial is a matrix product: P = a @ w.T
     (a [T, K], w [H, K], bfloat16 or float16; 2-D views with unit stride
     within a row), residual [T, H] <- RN(P + residual) in place,
-    y = RMSNorm(residual) * gamma into ``out`` (allocated if None)."""
+    y = RMSNorm(residual) * gamma into ``out`` (allocated if None).
+    ``workspace``: a CUDA tensor of at least gemm_workspace_bytes(T, H) bytes
+    (allocated if None)."""
     import torch
     T, K = a.shape
     H = w.shape[0]
@@ -498,10 +509,16 @@ def gemm_add_rms_norm(a, w, residual, gamma, eps: float, out=None):
     _check_tensor("gamma", gamma, a.dtype, dev)
     if out is None:
         out = torch.empty(T, H, dtype=a.dtype, device=dev)
+    if workspace is None:
+        n = max(gemm_workspace_bytes(T, H), 4)
+        workspace = torch.empty((n + 3) // 4, dtype=torch.float32, device=dev)
+    if not workspace.is_cuda or workspace.device != dev:
+        raise ValueError(f"workspace must be a CUDA tensor on {dev}")
     with torch.cuda.device(dev):
         _check(library().rarn_gemm_add_rms_norm(
             _rows("out", out, dev), _rows("a", a, dev), _rows("w", w, dev),
             _rows("residual", residual, dev), gamma.data_ptr(), T, H, K, float(eps),
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
             _stream(dev)), "rarn_gemm_add_rms_norm")
     return out
 

@@ -755,50 +755,64 @@ rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows parti
     return run_ex(c);
 }
 
-// GEMM producer + fused residual-add RMSNorm: every matrix
-// 16-bit, one type; 16-byte aligned bases and row strides.
+// GEMM producer + fused residual-add RMSNorm: every matrix 16-bit, one type;
+// 16-byte aligned bases and row strides; the caller's workspace holds the
+// column tiles' partial sums of squares.
+static GemmPlan gemm_plan_env(int64_t T, int64_t H) {
+    int bk = 0, ns = 0, ctas = 0;  // measurements only
+    if (const char *v = getenv("RARN_GEMM_BK")) bk = atoi(v);
+    if (const char *v = getenv("RARN_GEMM_NS")) ns = atoi(v);
+    if (const char *v = getenv("RARN_GEMM_CTAS")) ctas = atoi(v);
+    return plan_gemm(T, H, bk, ns, ctas);
+}
+
+int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H) {
+    if (T < 0 || H <= 0) return -1;
+    const GemmPlan gp = gemm_plan_env(T, H);
+    return gp.ns == 0 ? -1 : T * gp.tiles_n * 4;
+}
+
 rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_rows residual,
                                    const void *gamma, int64_t T, int64_t H, int64_t K, float eps,
-                                   void *stream) {
+                                   void *workspace, size_t workspace_bytes, void *stream) {
     const rarn_dtype dt = a.dtype;
-    if (!dtype_ok(dt) || w.dtype != dt || y.dtype != dt || residual.dtype != dt)
-        return dtype_ok(dt) && dtype_ok(w.dtype) && dtype_ok(y.dtype) && dtype_ok(residual.dtype)
-                   ? RARN_ERR_UNSUPPORTED
-                   : RARN_ERR_INVALID_ARG;
+    if (!dtype_ok(dt) || !dtype_ok(w.dtype) || !dtype_ok(y.dtype) || !dtype_ok(residual.dtype))
+        return RARN_ERR_INVALID_ARG;
+    if (w.dtype != dt || y.dtype != dt || residual.dtype != dt) return RARN_ERR_UNSUPPORTED;
     if (T < 0 || H <= 0 || K <= 0 || !(eps >= 0.f) || std::isinf(eps)) return RARN_ERR_INVALID_ARG;
     if (a.row_stride < K || w.row_stride < K || residual.row_stride < H || y.row_stride < H)
         return RARN_ERR_INVALID_ARG;
     if (T == 0) return RARN_OK;
-    if (!y.data || !a.data || !w.data || !residual.data || !gamma) return RARN_ERR_INVALID_ARG;
+    if (!y.data || !a.data || !w.data || !residual.data || !gamma || !workspace)
+        return RARN_ERR_INVALID_ARG;
     if (dt == RARN_F32) return RARN_ERR_UNSUPPORTED;  // the tensor path takes 16-bit operands
     if (T > (int64_t(1) << 31) - 128 || K > (int64_t(1) << 31) - 64) return RARN_ERR_UNSUPPORTED;
-    int bk_env = 0, ns_env = 0;  // measurements only
-    if (const char *v = getenv("RARN_GEMM_BK")) bk_env = atoi(v);
-    if (const char *v = getenv("RARN_GEMM_NS")) ns_env = atoi(v);
-    const GemmPlan gp = plan_gemm(T, H, bk_env, ns_env);
+    const GemmPlan gp = gemm_plan_env(T, H);
     if (gp.ns == 0) return RARN_ERR_UNSUPPORTED;
-    auto al16 = [](const void *ptr, int64_t ld) {
-        return aligned16(ptr) && (ld * 2) % 16 == 0;
-    };
+    const int64_t ws = T * gp.tiles_n * 4;
+    if ((int64_t)workspace_bytes < ws || (reinterpret_cast<uintptr_t>(workspace) & 3u))
+        return RARN_ERR_INVALID_ARG;
+    auto al16 = [](const void *ptr, int64_t ld) { return aligned16(ptr) && (ld * 2) % 16 == 0; };
     if (!al16(a.data, a.row_stride) || !al16(w.data, w.row_stride) ||
         !al16(residual.data, residual.row_stride) || !al16(y.data, y.row_stride) ||
         !aligned16(gamma))
         return RARN_ERR_UNSUPPORTED;
     const int64_t yb = span_bytes(T, H, y.row_stride, 2), rb = span_bytes(T, H, residual.row_stride, 2);
     const int64_t ab = span_bytes(T, K, a.row_stride, 2), wb = span_bytes(H, K, w.row_stride, 2);
-    if (overlaps(y.data, yb, residual.data, rb) || overlaps(y.data, yb, a.data, ab) ||
-        overlaps(y.data, yb, w.data, wb) || overlaps(y.data, yb, gamma, H * 2) ||
-        overlaps(residual.data, rb, a.data, ab) || overlaps(residual.data, rb, w.data, wb) ||
-        overlaps(residual.data, rb, gamma, H * 2))
-        return RARN_ERR_ALIAS;
+    const void *outs[3] = {y.data, residual.data, workspace};
+    const int64_t outb[3] = {yb, rb, ws};
+    const void *ins[3] = {a.data, w.data, gamma};
+    const int64_t inb[3] = {ab, wb, H * 2};
+    for (int i = 0; i < 3; ++i) {
+        for (int j = 0; j < 3; ++j)
+            if (overlaps(outs[i], outb[i], ins[j], inb[j])) return RARN_ERR_ALIAS;
+        for (int j = i + 1; j < 3; ++j)
+            if (overlaps(outs[i], outb[i], outs[j], outb[j])) return RARN_ERR_ALIAS;
+    }
 
     DeviceInfo *d = nullptr;
     rarn_status st = device_info(&d);
     if (st != RARN_OK) return st;
-    const int resident = dt == RARN_BF16
-                             ? gemm_norm_max_clusters<__nv_bfloat16>(gp.cluster, gp.ns, gp.stages, gp.bk)
-                             : gemm_norm_max_clusters<__half>(gp.cluster, gp.ns, gp.stages, gp.bk);
-    if (resident < 1) return RARN_ERR_UNSUPPORTED;
 
     GemmCall c{};
     c.a = a.data;
@@ -817,6 +831,8 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     c.ns = gp.ns;
     c.stages = gp.stages;
     c.bk = gp.bk;
+    c.workspace = static_cast<float *>(workspace);
+    c.num_sms = d->num_sms;
     c.pdl = g_pdl.load() != 0;
     c.watchdog = d->watchdog;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -829,18 +845,15 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
 rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, char *out, size_t cap) {
     if (!out || cap == 0) return RARN_ERR_INVALID_ARG;
     if (!dtype_ok(dt) || T < 0 || H <= 0 || K <= 0) return RARN_ERR_INVALID_ARG;
-    int bk_env = 0, ns_env = 0;
-    if (const char *v = getenv("RARN_GEMM_BK")) bk_env = atoi(v);
-    if (const char *v = getenv("RARN_GEMM_NS")) ns_env = atoi(v);
-    const GemmPlan gp = dt == RARN_F32 ? GemmPlan{} : plan_gemm(T, H, bk_env, ns_env);
+    const GemmPlan gp = dt == RARN_F32 ? GemmPlan{} : gemm_plan_env(T, H);
     if (gp.ns == 0) {
         snprintf(out, cap, "none: unsupported shape or type");
         return RARN_ERR_UNSUPPORTED;
     }
     snprintf(out, cap,
-             "gemm.tcgen05 cols_per_cta=%d cluster=%d bk=%d stages=%d smem=%d grid=%lld "
-             "kblocks=%lld",
-             gp.ns, gp.cluster, gp.bk, gp.stages, gp.smem, (long long)gp.grid,
+             "gemm.tcgen05 cols_per_cta=%d col_tiles=%d bk=%d stages=%d smem=%d grid=%lld "
+             "kblocks=%lld + norm",
+             gp.ns, gp.tiles_n, gp.bk, gp.stages, gp.smem, (long long)gp.grid,
              (long long)((K + gp.bk - 1) / gp.bk));
     return RARN_OK;
 }

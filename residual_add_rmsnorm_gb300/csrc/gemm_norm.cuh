@@ -9,31 +9,31 @@
 // epilogue, consumes the accumulator tile before anything is written;
 // "Tokenweave fused-RMSNorm-AR kernel", Code walkthrough, for the norm steps).
 //
-// Blackwell mapping (sm_103a):
-//   * one CTA computes a [128 x NS] tile of P (NS = 256 or 512 columns), the
-//     accumulator in tensor memory (TMEM: 128 lanes = rows, NS columns of
-//     binary32);
-//   * a cluster of C = H / NS CTAs covers whole rows: the row's sum of squares
-//     is exchanged through distributed shared memory, so no CTA re-reads
-//     anything from HBM and no global scratch is used;
-//   * operands arrive by TMA (cp.async.bulk.tensor, 2-D tiles, BK-element K
-//     slabs in the BK * 2-byte swizzle) into an S-stage ring; one thread
-//     issues tcgen05.mma (kind::f16, M = 128, N = 256, K = 16) and commits
-//     each stage back to the producer;
-//   * 4 warps: warp 0 lane 0 produces, warp 1 lane 0 issues the MMAs, then
-//     all 128 threads run the epilogue, thread i owning row i of the tile
-//     (TMEM lane i).  The operand ring is free once the MMAs are done, so it
-//     stages the epilogue: the residual tile arrives by TMA in [128 x 32]
-//     chunks (64-byte rows, 64-byte swizzle: a thread's 16-byte accesses to its
-//     own row are free of bank conflicts); each thread adds its accumulator
-//     row (tcgen05.ld), rounds, writes h back into the chunk and keeps it in
-//     TMEM (tcgen05.st); the chunk goes back to the residual by a TMA store.
-//     The second pass writes y through the same chunks.
+// Blackwell mapping (sm_103a), two kernels on one stream:
+//   1. k_gemm_res: one CTA per [128 x NS] tile of P (NS = 256 or 512
+//      columns), the accumulator in tensor memory (TMEM: 128 lanes = rows, NS
+//      columns of binary32).  Operands arrive by TMA (cp.async.bulk.tensor,
+//      2-D tiles, BK-element K slabs in the BK * 2-byte swizzle) into an
+//      S-stage ring; one thread issues tcgen05.mma (kind::f16, M = 128,
+//      N = 256, K = 16) and commits each stage back to the producer.  4 warps:
+//      warp 0 lane 0 produces, warp 1 lane 0 issues the MMAs, then all 128
+//      threads run the epilogue, thread i owning row i of the tile (TMEM lane
+//      i).  The operand ring is free once the MMAs are done, so it stages the
+//      epilogue: the residual tile arrives by TMA in [128 x 32] chunks
+//      (64-byte rows, 64-byte swizzle: a thread's 16-byte accesses to its own
+//      row are free of bank conflicts); each thread adds its accumulator row
+//      (tcgen05.ld), rounds once, writes h back into the chunk, which a TMA
+//      store returns to the residual; the tile's partial sum of squares of
+//      each row goes to a workspace slot [row][tile column] (no atomics).
+//      Tiles are independent: no cluster, every SM takes tiles.
+//   2. k_norm_ss: per row, the H / NS partial sums in tile order (fixed:
+//      deterministic), inv, and y = RN((h * inv) * gamma) from the stored
+//      residual (16-byte packs, a CTA per row).  Launched with programmatic
+//      dependent launch: it waits for kernel 1 to complete.
 //
 // Every mbarrier wait is bounded (global timer); a wait that runs out sets the
 // watchdog word and the CTA's abort flag, the CTA drains what it issued (also
-// bounded), passes the same cluster barriers as its peers, frees its tensor
-// memory and returns with its outputs invalid.
+// bounded), frees its tensor memory and returns with its outputs invalid.
 #pragma once
 
 #include <cuda.h>  // CUtensorMap (type only; the map is encoded on the host)
@@ -67,24 +67,31 @@ __host__ __device__ constexpr Layout layout(int stages, int ns, int bk) {
     L.b_bytes = ns * bk * 2;
     L.stage_bytes = L.a_bytes + L.b_bytes;
     L.ctl_off = stages * L.stage_bytes;
-    // full[S], empty[S], accum, chunk[16] (8 B each), tmem slot, abort word,
-    // red[128]
-    L.total = L.ctl_off + (2 * stages + 1 + kMaxChunks) * 8 + 8 + kBM * 4 + 1024;  // + slack
+    // full[S], empty[S], accum, chunk[16] (8 B each), tmem slot, abort word
+    L.total = L.ctl_off + (2 * stages + 1 + kMaxChunks) * 8 + 8 + 1024;  // + alignment slack
     return L;
 }
 
 struct Params {
-    void *y;
-    void *residual;
-    const void *gamma;
+    float *ss;         // workspace [T][C]: per row, each column tile's sum of squares of h
     int64_t T, H, K;
-    int64_t ldr, ldy;  // elements
-    float eps;
     int ns;            // columns per CTA
+    int C;             // column tiles (H / ns)
     int stages;
     int kblocks;       // ceil(K / BK)
     unsigned int *watchdog;
     unsigned long long wait_limit_ns;
+};
+
+// Kernel 2 arguments.
+struct NormParams {
+    void *y;
+    const void *h;     // the updated residual
+    const void *gamma;
+    const float *ss;   // [T][C]
+    int64_t T, H, ldh, ldy;
+    int C;
+    float eps;
 };
 
 // ---------------------------------------------------------------------------
@@ -279,57 +286,14 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_wait_st() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ void cluster_barrier() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n"
-                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ float ld_peer_f32(uint32_t local_saddr, uint32_t rank) {
-    uint32_t remote;
-    float v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_saddr), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
-}
-
 // ---------------------------------------------------------------------------
-// The kernel.  Grid: C x ceil(T / 128) CTAs in clusters of C (C = H / NS);
-// CTA rank c of a cluster owns columns [c * NS, (c + 1) * NS).
+// Kernel 1.  Grid: C x ceil(T / 128) CTAs (C = H / NS column tiles); CTA b
+// owns rows [128 (b / C), +128) and columns [NS (b % C), +NS).
 // ---------------------------------------------------------------------------
 template <typename T, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_gemm_norm(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
-                const __grid_constant__ CUtensorMap map_r, const __grid_constant__ CUtensorMap map_y,
-                Params p) {
+    k_gemm_res(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
+               const __grid_constant__ CUtensorMap map_r, Params p) {
     static_assert(BK == 64 || BK == 32, "K slab of 128 or 64 bytes");
     constexpr int kRowBytes = BK * 2;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -344,13 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *chunk_bar = accum + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(chunk_bar + kMaxChunks);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    float *red = reinterpret_cast<float *>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t crank = cluster_rank();
-    const int C = (int)(p.H / NS);
+    const int C = p.C;
+    const int ntile = (int)(blockIdx.x % C);  // consecutive CTAs share the A tile (L2)
     const int64_t m0 = (int64_t)(blockIdx.x / C) * kBM;
-    const int n0 = (int)crank * NS;
+    const int n0 = ntile * NS;
     const uint32_t ncols = NS;  // TMEM columns (power of two >= 32)
 
     if (threadIdx.x == 0) {
@@ -471,49 +434,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int e = 0; e < 8; ++e) {
                     f[e] = DT<T>::round(v[8 * q + e] + f[e]);  // h: one rounding of acc + r
                     ss += f[e] * f[e];
-                    v[8 * q + e] = f[e];
                 }
                 sts128(a, DT<T>::pack(f));
             }
             fence_async_shared();
         }
-        tmem_st32(tbase + c * kChunkCols, v);  // h, for the second pass
         epi_barrier();
         if (ok && threadIdx.x == 0) {
             tma_store_2d(&map_r, n0 + c * kChunkCols, (int)m0, ring + c * kChunkBytes);
             bulk_commit();
         }
     }
-    tmem_wait_st();
-    red[r] = ss;
-    cluster_barrier();  // every CTA of the cluster has published its partial sums
-    float tot = 0.f;
-    for (int q = 0; q < C; ++q) tot += ld_peer_f32(smem_u32(&red[r]), (uint32_t)q);
-    const float inv = rsqrtf(tot / (float)p.H + p.eps);
-    if (threadIdx.x == 0) bulk_wait_read_all();  // the chunks are free again
-    epi_barrier();
-    const T *g = reinterpret_cast<const T *>(p.gamma) + n0;
-    for (int c = 0; c < nchunks; ++c) {
-        float v[32];
-        tmem_ld32(tbase + c * kChunkCols, v);
-        const uint32_t ca = ring + c * kChunkBytes + row_off;
-        if (ok) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float w[8], f[8];
-                DT<T>::unpack(ld_keep(g + c * kChunkCols + 8 * q), w);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = (v[8 * q + e] * inv) * w[e];
-                sts128(ca + ((q ^ swz) << 4), DT<T>::pack(f));
-            }
-            fence_async_shared();
-        }
-        epi_barrier();
-        if (ok && threadIdx.x == 0) {
-            tma_store_2d(&map_y, n0 + c * kChunkCols, (int)m0, ring + c * kChunkBytes);
-            bulk_commit();
-        }
-    }
+    if (ok && m0 + r < p.T) p.ss[(m0 + r) * C + ntile] = ss;
     if (threadIdx.x == 0) {
         bulk_wait_all();  // the stores have completed before this CTA's memory goes away
         if (*abort_flag) {  // loads issued after an abort elsewhere must still land (bounded)
@@ -523,12 +455,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     }
     tmem_fence_before();
-    cluster_barrier();  // peers are done reading this CTA's partial sums
+    __syncthreads();
     tmem_fence_after();
     if (warp == 0) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                      "r"(ncols)
                      : "memory");
+    }
+}
+
+// Kernel 2: y from the stored h and the tiles' partial sums.  A CTA per row
+// (grid-stride), VPT 16-byte packs per thread.
+template <typename T, int VPT>
+__global__ void __launch_bounds__(256) k_norm_ss(NormParams p) {
+    __shared__ float inv_s;
+    constexpr int EPV = DT<T>::EPV;
+    const int nv = (int)(p.H / EPV);
+    grid_dependency_wait();  // kernel 1's stores are visible
+    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
+        if (t + gridDim.x >= p.T) grid_launch_dependents();
+        uint4 hv[VPT], gv[VPT];
+        const T *h = reinterpret_cast<const T *>(p.h) + t * p.ldh;
+        const T *g = reinterpret_cast<const T *>(p.gamma);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = threadIdx.x + k * blockDim.x;
+            if (j < nv) {
+                hv[k] = ld_stream(h + (int64_t)j * EPV);
+                gv[k] = ld_keep(g + (int64_t)j * EPV);
+            }
+        }
+        if (threadIdx.x == 0) {
+            float tot = 0.f;
+            for (int q = 0; q < p.C; ++q) tot += p.ss[t * p.C + q];  // tile order
+            inv_s = rsqrtf(tot / (float)p.H + p.eps);
+        }
+        __syncthreads();
+        const float inv = inv_s;
+        T *y = reinterpret_cast<T *>(p.y) + t * p.ldy;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int j = threadIdx.x + k * blockDim.x;
+            if (j < nv) {
+                float f[EPV], w[EPV];
+                DT<T>::unpack(hv[k], f);
+                DT<T>::unpack(gv[k], w);
+#pragma unroll
+                for (int e = 0; e < EPV; ++e) f[e] = (f[e] * inv) * w[e];
+                st_global(y + (int64_t)j * EPV, DT<T>::pack(f));
+            }
+        }
+        __syncthreads();  // inv_s is rewritten for the next row
     }
 }
 

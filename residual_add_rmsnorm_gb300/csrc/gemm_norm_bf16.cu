@@ -3,5 +3,4 @@
 
 namespace rarn {
 template cudaError_t launch_gemm_norm<__nv_bfloat16>(const GemmCall &, cudaStream_t);
-template int gemm_norm_max_clusters<__nv_bfloat16>(int, int, int, int);
 }  // namespace rarn

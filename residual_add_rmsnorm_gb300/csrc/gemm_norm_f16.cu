@@ -3,5 +3,4 @@
 
 namespace rarn {
 template cudaError_t launch_gemm_norm<__half>(const GemmCall &, cudaStream_t);
-template int gemm_norm_max_clusters<__half>(int, int, int, int);
 }  // namespace rarn

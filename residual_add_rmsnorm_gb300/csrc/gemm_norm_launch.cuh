@@ -1,10 +1,11 @@
-// gemm_norm_launch.cuh -- host side of the GEMM + fused RMSNorm kernel:
+// gemm_norm_launch.cuh -- host side of the GEMM + fused RMSNorm kernels:
 // tensor-map encoding (through the driver entry point, so the library needs
-// no link-time dependency on the driver library) and the cluster launch.
+// no link-time dependency on the driver library) and the two launches.
 #pragma once
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "gemm_norm.cuh"
@@ -48,42 +49,55 @@ template <typename T, int BK>
 static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     using namespace gemm;
     const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
-    CUtensorMap ma, mw, mr, my;
+    CUtensorMap ma, mw, mr;
     if (!encode_map(&ma, c.a, c.T, c.K, c.lda, kBM, BK, bf16) ||
         !encode_map(&mw, c.w, c.H, c.K, c.ldw, kMmaN, BK, bf16) ||
-        !encode_map(&mr, c.residual, c.T, c.H, c.ldr, kBM, kChunkCols, bf16) ||
-        !encode_map(&my, c.y, c.T, c.H, c.ldy, kBM, kChunkCols, bf16))
+        !encode_map(&mr, c.residual, c.T, c.H, c.ldr, kBM, kChunkCols, bf16))
         return cudaErrorInvalidValue;
-    // the epilogue stages the residual / y tile in the operand ring
+    // the epilogue stages the residual tile in the operand ring
     if (c.stages * layout(c.stages, c.ns, BK).stage_bytes < (c.ns / kChunkCols) * kChunkBytes)
         return cudaErrorInvalidValue;
     Params p{};
-    p.y = c.y;
-    p.residual = c.residual;
-    p.gamma = c.gamma;
+    p.ss = c.workspace;
     p.T = c.T;
     p.H = c.H;
     p.K = c.K;
-    p.ldr = c.ldr;
-    p.ldy = c.ldy;
-    p.eps = c.eps;
     p.ns = c.ns;
+    p.C = static_cast<int>(c.H / c.ns);
     p.stages = c.stages;
     p.kblocks = static_cast<int>((c.K + BK - 1) / BK);
     p.watchdog = c.watchdog;
     p.wait_limit_ns = kWaitLimitNs;
-    const int C = static_cast<int>(c.H / c.ns);
     const int smem = layout(c.stages, c.ns, BK).total;
-    auto kernel = k_gemm_norm<T, BK>;
+    auto kernel = k_gemm_res<T, BK>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    if (C > 8 &&
-        (e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) !=
-            cudaSuccess)
-        return e;
     const int64_t mblocks = (c.T + kBM - 1) / kBM;
-    return launch_kernel(kernel, dim3(static_cast<unsigned>(mblocks * C)), dim3(kThreads),
-                         static_cast<size_t>(smem), st, c.pdl, C, ma, mw, mr, my, p);
+    e = launch_kernel(kernel, dim3(static_cast<unsigned>(mblocks * p.C)), dim3(kThreads),
+                      static_cast<size_t>(smem), st, c.pdl, 1, ma, mw, mr, p);
+    if (e != cudaSuccess) return e;
+
+    NormParams q{};
+    q.y = c.y;
+    q.h = c.residual;
+    q.gamma = c.gamma;
+    q.ss = c.workspace;
+    q.T = c.T;
+    q.H = c.H;
+    q.ldh = c.ldr;
+    q.ldy = c.ldy;
+    q.C = p.C;
+    q.eps = c.eps;
+    const int nv = static_cast<int>(c.H / DT<T>::EPV);
+    const int vpt = nv <= 256 ? 1 : nv <= 512 ? 2 : nv <= 1024 ? 4 : 8;
+    const dim3 g2(static_cast<unsigned>(std::min<int64_t>(c.T, (int64_t)c.num_sms * 8)));
+    const dim3 b2(static_cast<unsigned>(((nv + vpt - 1) / vpt + 31) / 32 * 32));
+    switch (vpt) {
+    case 1: return launch_kernel(k_norm_ss<T, 1>, g2, b2, 0, st, c.pdl, 1, q);
+    case 2: return launch_kernel(k_norm_ss<T, 2>, g2, b2, 0, st, c.pdl, 1, q);
+    case 4: return launch_kernel(k_norm_ss<T, 4>, g2, b2, 0, st, c.pdl, 1, q);
+    default: return launch_kernel(k_norm_ss<T, 8>, g2, b2, 0, st, c.pdl, 1, q);
+    }
 }
 
 template <typename T>
@@ -91,43 +105,6 @@ cudaError_t launch_gemm_norm(const GemmCall &c, cudaStream_t st) {
     if (c.T == 0) return cudaSuccess;
     const cudaError_t e = c.bk == 64 ? launch_gemm_bk<T, 64>(c, st) : launch_gemm_bk<T, 32>(c, st);
     return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-template <typename T, int BK>
-static int max_clusters_bk(int cluster, int ns, int stages) {
-    using namespace gemm;
-    auto kernel = k_gemm_norm<T, BK>;
-    const int smem = layout(stages, ns, BK).total;
-    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-        return 0;
-    if (cluster > 8 &&
-        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
-            cudaSuccess)
-        return 0;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(cluster));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = cluster;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
-        cudaGetLastError();
-        return 0;
-    }
-    return n;
-}
-
-template <typename T>
-int gemm_norm_max_clusters(int cluster, int ns, int stages, int bk) {
-    return bk == 64 ? max_clusters_bk<T, 64>(cluster, ns, stages)
-                    : max_clusters_bk<T, 32>(cluster, ns, stages);
 }
 
 }  // namespace rarn

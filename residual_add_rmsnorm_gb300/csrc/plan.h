@@ -133,6 +133,8 @@ struct GemmCall {
     int64_t T, H, K;
     float eps;
     int ns, stages, bk;  // columns per CTA, ring stages, K slab (elements)
+    float *workspace;    // [T][H / ns] partial sums of squares
+    int num_sms;
     bool pdl;
     unsigned int *watchdog;
 };
@@ -140,43 +142,57 @@ struct GemmCall {
 template <typename T>
 cudaError_t launch_gemm_norm(const GemmCall &c, cudaStream_t stream);
 
-// Clusters of `cluster` CTAs of the GEMM kernel that can be resident at once
-// (0 if the shape cannot be scheduled).
-template <typename T>
-int gemm_norm_max_clusters(int cluster, int ns, int stages, int bk);
-
-// Tile plan of the GEMM kernel: columns per CTA (a cluster spans H), K slab
-// and ring depth within the shared memory of one SM.  ns = 0: unsupported H.
+// Tile plan of the GEMM kernel: columns per CTA, K slab and ring depth within
+// the shared memory given to one CTA (one or two CTAs per SM).  ns = 0:
+// unsupported H.
 struct GemmPlan {
-    int ns = 0, cluster = 0, bk = 0, stages = 0, smem = 0;
+    int ns = 0, tiles_n = 0, bk = 0, stages = 0, smem = 0;
     int64_t grid = 0;
 };
 
-inline GemmPlan plan_gemm(int64_t T, int64_t H, int bk_override = 0, int ns_override = 0) {
+constexpr int kGemmMaxTilesN = 32;
+
+// Measured on GB300 (T = K = H = 4096, bf16): 256 columns per CTA with
+// 128-byte K slabs and two CTAs per SM (one CTA's epilogue overlaps the
+// other's main loop) 124.5 us; 512 columns, one CTA per SM, 147 us.  Rows
+// wider than 32 tiles of 256 use 512-column tiles.
+inline GemmPlan plan_gemm(int64_t T, int64_t H, int bk_override = 0, int ns_override = 0,
+                          int ctas_override = 0) {
     GemmPlan g;
-    constexpr int kMaxCluster = 16, kSmem = 227 * 1024;
-    if (ns_override == 256 && H % 256 == 0 && H / 256 <= kMaxCluster) {
+    const bool fit256 = H % 256 == 0 && H / 256 <= kGemmMaxTilesN;
+    const bool fit512 = H % 512 == 0 && H / 512 <= kGemmMaxTilesN;
+    int ctas;
+    if (fit256 && ns_override != 512) {
         g.ns = 256;
         g.bk = 64;
-    } else if (H % 512 == 0 && H / 512 <= kMaxCluster) {
+        ctas = 2;
+    } else if (fit512) {
         g.ns = 512;
         g.bk = 32;
-    } else if (H % 256 == 0 && H / 256 <= kMaxCluster) {
-        g.ns = 256;
-        g.bk = 64;
+        ctas = 1;
     } else {
         return g;
     }
     if (bk_override == 32 || bk_override == 64) g.bk = bk_override;
-    g.cluster = (int)(H / g.ns);
+    if (ctas_override == 1 || ctas_override == 2) ctas = ctas_override;
+    const int smem_budget = ctas == 2 ? 113 * 1024 : 227 * 1024;
+    g.tiles_n = (int)(H / g.ns);
     const int stage = (128 + g.ns) * g.bk * 2;
-    const int fixed = 2048 + 1024;  // barriers, partial sums, alignment slack
-    g.stages = (kSmem - fixed) / stage;
+    const int fixed = 1024 + 1024;  // barriers, alignment slack
+    g.stages = (smem_budget - fixed) / stage;
     if (g.stages > 8) g.stages = 8;
-    if (g.stages < 2) return GemmPlan{};
+    // the epilogue stages the residual tile ([128 x ns] 16-bit) in the ring
+    if (g.stages < 2 || g.stages * stage < 128 * g.ns * 2) return GemmPlan{};
     g.smem = g.stages * stage + fixed;
-    g.grid = ((T + 127) / 128) * g.cluster;
+    g.grid = ((T + 127) / 128) * g.tiles_n;
     return g;
+}
+
+// Workspace of the GEMM form: one binary32 per row and column tile (-1: H
+// not supported).
+inline int64_t gemm_workspace_bytes(int64_t T, int64_t H) {
+    const GemmPlan g = plan_gemm(T, H);
+    return g.ns == 0 ? -1 : T * g.tiles_n * 4;
 }
 
 }  // namespace rarn

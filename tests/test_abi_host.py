@@ -315,37 +315,51 @@ def test_plan_fp8():
 
 
 def test_gemm_form_argument_errors(lib):
-    """GEMM-producer form: types, shapes, alignment and aliasing are checked
-    before any CUDA call."""
+    """GEMM-producer form: types, shapes, workspace, alignment and aliasing
+    are checked before any CUDA call."""
     T, H, K = 16, 1024, 256
     y, a, w, r = _rows(A, H, BF16), _rows(B, K, BF16), _rows(C, K, BF16), _rows(D, H, BF16)
     g = D + (1 << 30)
+    ws, wsb = D + (2 << 30), 1 << 20
     f = lib.rarn_gemm_add_rms_norm
-    assert f(y, a, _rows(C, K, F16), r, g, T, H, K, 1e-6, None) == UNSUPPORTED  # mixed types
-    assert f(y, a, w, r, g, T, H, K, -1.0, None) == INVALID                     # eps
-    assert f(y, a, w, r, g, T, H, 0, 1e-6, None) == INVALID                     # K = 0
-    assert f(y, _rows(B, K - 1, BF16), w, r, g, T, H, K, 1e-6, None) == INVALID  # row stride
-    assert f(y, a, w, r, None, T, H, K, 1e-6, None) == INVALID                  # null gamma
-    assert f(_rows(A, 300, BF16), a, _rows(C, K, BF16), _rows(D, 300, BF16), g, T, 300, K, 1e-6,
-             None) == UNSUPPORTED                                                # H = 300
-    assert f(_rows(A, H, F32), _rows(B, K, F32), _rows(C, K, F32), _rows(D, H, F32), g, T, H, K,
-             1e-6, None) == UNSUPPORTED                                          # no f32 path
-    assert f(y, _rows(B + 2, K, BF16), w, r, g, T, H, K, 1e-6, None) == UNSUPPORTED  # alignment
-    assert f(y, _rows(B, K + 4, BF16), w, r, g, T, H, K, 1e-6, None) == UNSUPPORTED  # stride
-    assert f(_rows(D, H, BF16), a, w, r, g, T, H, K, 1e-6, None) == ALIAS       # y == residual
-    assert f(y, a, w, _rows(C + 64, H, BF16), g, T, H, K, 1e-6, None) == ALIAS  # residual over w
-    assert f(_rows(None, H, BF16), _rows(None, K, BF16), _rows(None, K, BF16),
-             _rows(None, H, BF16), None, 0, H, K, 1e-6, None) == OK             # T = 0
+
+    def call(*args, wsp=ws, wsn=wsb):
+        return f(*args, wsp, wsn, None)
+
+    assert call(y, a, _rows(C, K, F16), r, g, T, H, K, 1e-6) == UNSUPPORTED  # mixed types
+    assert call(y, a, w, r, g, T, H, K, -1.0) == INVALID                     # eps
+    assert call(y, a, w, r, g, T, H, 0, 1e-6) == INVALID                     # K = 0
+    assert call(y, _rows(B, K - 1, BF16), w, r, g, T, H, K, 1e-6) == INVALID  # row stride
+    assert call(y, a, w, r, None, T, H, K, 1e-6) == INVALID                  # null gamma
+    assert call(y, a, w, r, g, T, H, K, 1e-6, wsp=None) == INVALID           # no workspace
+    need = lib.rarn_gemm_workspace_bytes(T, H)
+    assert need == T * (H // 256) * 4
+    assert call(y, a, w, r, g, T, H, K, 1e-6, wsn=need - 4) == INVALID      # short workspace
+    assert call(_rows(A, 300, BF16), a, _rows(C, K, BF16), _rows(D, 300, BF16), g, T, 300, K,
+                1e-6) == UNSUPPORTED                                         # H = 300
+    assert call(_rows(A, H, F32), _rows(B, K, F32), _rows(C, K, F32), _rows(D, H, F32), g, T, H,
+                K, 1e-6) == UNSUPPORTED                                      # no f32 path
+    assert call(y, _rows(B + 2, K, BF16), w, r, g, T, H, K, 1e-6) == UNSUPPORTED  # alignment
+    assert call(y, _rows(B, K + 4, BF16), w, r, g, T, H, K, 1e-6) == UNSUPPORTED  # stride
+    assert call(_rows(D, H, BF16), a, w, r, g, T, H, K, 1e-6) == ALIAS       # y == residual
+    assert call(y, a, w, _rows(C + 64, H, BF16), g, T, H, K, 1e-6) == ALIAS  # residual over w
+    assert call(y, a, w, r, g, T, H, K, 1e-6, wsp=A + 64) == ALIAS          # workspace over y
+    assert call(_rows(None, H, BF16), _rows(None, K, BF16), _rows(None, K, BF16),
+                _rows(None, H, BF16), None, 0, H, K, 1e-6, wsp=None) == OK  # T = 0
 
 
 def test_plan_gemm():
-    """Columns per CTA and cluster size from H; the K slab and ring depth
-    fill one SM's shared memory."""
+    """Columns per CTA from H; the K slab and ring depth fill one SM's shared
+    memory; the workspace holds one float per row and column tile."""
     p = rarn.plan_gemm(4096, 4096, 4096)
-    assert "cols_per_cta=512 cluster=8" in p and "grid=256" in p and "kblocks=128" in p, p
+    assert "cols_per_cta=256 col_tiles=16 bk=64 stages=2" in p and "grid=512" in p, p
+    assert "kblocks=64" in p, p
     p = rarn.plan_gemm(100, 768, 1000)
-    assert "cols_per_cta=256 cluster=3" in p and "stages=4" in p and "grid=3" in p, p
-    assert "cluster=16" in rarn.plan_gemm(8, 8192, 64)
+    assert "cols_per_cta=256 col_tiles=3" in p and "stages=2" in p and "grid=3" in p, p
+    p = rarn.plan_gemm(8, 16384, 64)   # beyond 32 tiles of 256: 512-column tiles
+    assert "cols_per_cta=512 col_tiles=32 bk=32 stages=5" in p, p
     assert rarn.plan_gemm(8, 300, 64).startswith("none")
-    assert rarn.plan_gemm(8, 8704, 64).startswith("none")   # 17 x 512: beyond 16 CTAs
+    assert rarn.plan_gemm(8, 16896, 64).startswith("none")   # 33 x 512: beyond 32 tiles
     assert rarn.plan_gemm(8, 4096, 64, "f32").startswith("none")
+    assert rarn.gemm_workspace_bytes(4096, 4096) == 4096 * 16 * 4
+    assert rarn.gemm_workspace_bytes(7, 300) == -1
