@@ -294,6 +294,20 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
                                    const void *gamma, int64_t T, int64_t H, int64_t K, float eps,
                                    void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * rarn_gemm_add_rms_norm without a workspace argument: allocates nothing and
+ * takes no caller memory; the partial sums live in a 4 MB scratch array that
+ * the library reserves in device memory when it is loaded (found at the first
+ * call on each device), and problems with more rows than it holds run as
+ * several launch pairs on `stream`.  The paper has no counterpart.  Because
+ * every call on a device shares that scratch, calls must be ordered (one
+ * stream, or streams synchronised with each other); results are bit-identical
+ * to the workspace form.  Errors as for rarn_gemm_add_rms_norm.
+ */
+rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w,
+                                           rarn_rows residual, const void *gamma, int64_t T,
+                                           int64_t H, int64_t K, float eps, void *stream);
+
 /* Workspace bytes rarn_gemm_add_rms_norm needs for T rows of H (-1 if H is
  * not supported). */
 int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H);

@@ -29,7 +29,7 @@ __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_ho
            "DTYPE_CODES", "rms_norm_ex", "fused_add_rms_norm_ex", "reduce_add_rms_norm_ex",
            "rms_norm_fp8", "fused_add_rms_norm_fp8", "reduce_add_rms_norm_fp8", "plan_fp8",
            "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm",
-           "gemm_workspace_bytes"]
+           "gemm_workspace_bytes", "gemm_add_rms_norm_noalloc"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
@@ -133,6 +133,9 @@ def library() -> ctypes.CDLL:
     lib.rarn_gemm_add_rms_norm.argtypes = [Rows, Rows, Rows, Rows, vp, i64, i64, i64, f32, vp,
                                            ctypes.c_size_t, vp]
     lib.rarn_gemm_add_rms_norm.restype = c_int
+    lib.rarn_gemm_add_rms_norm_noalloc.argtypes = [Rows, Rows, Rows, Rows, vp, i64, i64, i64,
+                                                   f32, vp]
+    lib.rarn_gemm_add_rms_norm_noalloc.restype = c_int
     lib.rarn_gemm_workspace_bytes.argtypes = [i64, i64]
     lib.rarn_gemm_workspace_bytes.restype = i64
     lib.rarn_plan_gemm.argtypes = [i64, i64, i64, c_int, ctypes.c_char_p, ctypes.c_size_t]
@@ -520,6 +523,26 @@ def gemm_add_rms_norm(a, w, residual, gamma, eps: float, out=None, workspace=Non
             _rows("residual", residual, dev), gamma.data_ptr(), T, H, K, float(eps),
             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
             _stream(dev)), "rarn_gemm_add_rms_norm")
+    return out
+
+
+def gemm_add_rms_norm_noalloc(a, w, residual, gamma, eps: float, out=None):
+    """gemm_add_rms_norm through the entry point that takes no workspace (the
+    library's own static scratch; calls on a device must be ordered)."""
+    import torch
+    T, K = a.shape
+    H = w.shape[0]
+    dev = a.device
+    if tuple(w.shape) != (H, K) or tuple(residual.shape) != (T, H) or gamma.numel() != H:
+        raise ValueError("shape mismatch")
+    _check_tensor("gamma", gamma, a.dtype, dev)
+    if out is None:
+        out = torch.empty(T, H, dtype=a.dtype, device=dev)
+    with torch.cuda.device(dev):
+        _check(library().rarn_gemm_add_rms_norm_noalloc(
+            _rows("out", out, dev), _rows("a", a, dev), _rows("w", w, dev),
+            _rows("residual", residual, dev), gamma.data_ptr(), T, H, K, float(eps),
+            _stream(dev)), "rarn_gemm_add_rms_norm_noalloc")
     return out
 
 

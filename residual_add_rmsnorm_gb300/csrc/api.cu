@@ -19,6 +19,11 @@ using namespace rarn;
 // Watchdog word: kernels with bounded waits record a timeout here.
 __device__ unsigned int g_rarn_watchdog = 0;
 
+// Scratch of the workspace-free GEMM entry point (rarn_gemm_add_rms_norm_noalloc):
+// 4 MB reserved with the module, so that entry point allocates nothing.
+constexpr int64_t kGemmScratchFloats = int64_t(1) << 20;
+static __device__ __align__(256) float g_rarn_gemm_scratch[kGemmScratchFloats];
+
 namespace {
 
 thread_local int t_last_cuda_error = 0;
@@ -35,6 +40,7 @@ struct DeviceInfo {
     int num_sms = 0;
     int max_smem_optin = 0;
     unsigned int *watchdog = nullptr;
+    float *gemm_scratch = nullptr;  // looked up at first use on this device
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
@@ -67,6 +73,22 @@ rarn_status device_info(DeviceInfo **out) {
         d.ready = true;
     }
     *out = &d;
+    return RARN_OK;
+}
+
+// The static GEMM scratch's device address on the current device.
+rarn_status gemm_scratch(float **out) {
+    DeviceInfo *d = nullptr;
+    rarn_status st = device_info(&d);
+    if (st != RARN_OK) return st;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!d->gemm_scratch) {
+        void *p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_rarn_gemm_scratch);
+        if (e != cudaSuccess) return cuda_fail(e);
+        d->gemm_scratch = static_cast<float *>(p);
+    }
+    *out = d->gemm_scratch;
     return RARN_OK;
 }
 
@@ -839,6 +861,34 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     const cudaError_t e = dt == RARN_BF16 ? launch_gemm_norm<__nv_bfloat16>(c, cs)
                                           : launch_gemm_norm<__half>(c, cs);
     if (e != cudaSuccess) return cuda_fail(e);
+    return RARN_OK;
+}
+
+rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w,
+                                           rarn_rows residual, const void *gamma, int64_t T,
+                                           int64_t H, int64_t K, float eps, void *stream) {
+    if (T <= 0 || H <= 0) {  // argument errors and the empty call, as the workspace form
+        return rarn_gemm_add_rms_norm(y, a, w, residual, gamma, T, H, K, eps, nullptr, 0,
+                                      stream);
+    }
+    const GemmPlan gp = gemm_plan_env(T, H);
+    if (gp.ns == 0) return RARN_ERR_UNSUPPORTED;
+    float *scratch = nullptr;
+    rarn_status st = gemm_scratch(&scratch);
+    if (st != RARN_OK) return st;
+    // rows per launch pair that the scratch holds; later chunks reuse it in
+    // stream order
+    const int64_t chunk = kGemmScratchFloats / gp.tiles_n;
+    for (int64_t t0 = 0; t0 < T; t0 += chunk) {
+        const int64_t rows = std::min(chunk, T - t0);
+        auto shift = [t0](rarn_rows m) {
+            if (m.data) m.data = static_cast<char *>(m.data) + t0 * m.row_stride * 2;
+            return m;
+        };
+        st = rarn_gemm_add_rms_norm(shift(y), shift(a), w, shift(residual), gamma, rows, H, K,
+                                    eps, scratch, kGemmScratchFloats * 4, stream);
+        if (st != RARN_OK) return st;
+    }
     return RARN_OK;
 }
 

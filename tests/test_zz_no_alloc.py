@@ -1,0 +1,34 @@
+"""The GEMM form's workspace-free entry point against the workspace one:
+the same inputs through both, the workspace-free one called twice in a row
+(its static scratch reused), every output bit-identical.  Collected last."""
+import pytest
+
+import residual_add_rmsnorm_gb300 as rarn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("T,H,K", [
+    (300, 1024, 512),
+    (4096, 4096, 1024),
+    (40000, 8192, 64),   # 32 column tiles: more rows than the scratch holds (two launch pairs)
+])
+def test_noalloc_matches_workspace_entry_two_calls(T, H, K):
+    import torch
+    gen = torch.Generator(device="cuda").manual_seed(T + H + K)
+    a = torch.randn(T, K, device="cuda", generator=gen).to(torch.bfloat16)
+    w = (torch.randn(H, K, device="cuda", generator=gen) / K ** 0.5).to(torch.bfloat16)
+    r0 = torch.randn(T, H, device="cuda", generator=gen).to(torch.bfloat16)
+    g = (torch.rand(H, device="cuda", generator=gen) + 0.5).to(torch.bfloat16)
+    r_ws = r0.clone()
+    y_ws = rarn.gemm_add_rms_norm(a, w, r_ws, g, 1e-6)
+    outs = []
+    for _ in range(2):
+        r_na = r0.clone()
+        y_na = rarn.gemm_add_rms_norm_noalloc(a, w, r_na, g, 1e-6)
+        outs.append((y_na, r_na))
+    torch.cuda.synchronize()
+    assert rarn.watchdog(clear=True) == 0
+    for y_na, r_na in outs:
+        assert torch.equal(y_na, y_ws)
+        assert torch.equal(r_na, r_ws)
