@@ -43,7 +43,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 def _configs():
     from residual_add_rmsnorm_gb300 import workloads as W
-    return W.CONFIGS + W.EXTENDED
+    return W.CONFIGS + W.EXTENDED + W.GEMM_CONFIGS
 
 
 def parse_args():
@@ -332,8 +332,8 @@ def run_reference(args):
     if rank != 0:
         return
     from residual_add_rmsnorm_gb300 import workloads as W
-    w = W.BY_NAME[args.workload]
-    if w not in W.CONFIGS:
+    w = W.BY_NAME.get(args.workload)
+    if w is None or w not in W.CONFIGS:
         raise SystemExit("the reference arm times the method's configurations only")
     rows = min(w.T, 128)
     samples = []
@@ -534,6 +534,53 @@ def e2e_steps(w, data, steps, device, stream):
     return ms, h2d, d2h
 
 
+def main_gemm(args, gw, device, rank, world):
+    """The GEMM-producer form as the timed step: one call = the tcgen05 GEMM
+    with the residual add and the norm (two kernels).  TFLOP/s of the 2 T H K
+    product; inputs resident in HBM; no host-buffer or CPU leg."""
+    import torch
+
+    import residual_add_rmsnorm_gb300 as rarn
+    from residual_add_rmsnorm_gb300 import workloads as W
+    d = W.generate_gemm(gw)
+    a, w, r, g = (to_device(d[k], gw.dtype, device) for k in ("a", "w", "residual", "gamma"))
+    y = torch.empty_like(r)
+    ws = torch.empty(max(rarn.gemm_workspace_bytes(gw.T, gw.H), 4) // 4, dtype=torch.float32,
+                     device=device)
+    call = lambda: rarn.gemm_add_rms_norm(a, w, r, g, gw.eps, out=y, workspace=ws)
+    stream = torch.cuda.current_stream(device)
+    props = torch.cuda.get_device_properties(device)
+    gpu_id = str(getattr(props, "uuid", 0))
+    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id)
+    ms = time_steps(call, args.steps, args.warmup, stream)
+    clocks = sampler.stop()
+    ms = max_over_ranks(ms, device)
+    peak, kind = measured_tensor_peak()
+    tflops = world * gw.flops() * args.steps / (ms / 1e3) / 1e12
+    if rank != 0:
+        return
+    line = {
+        "metric": "achieved TFLOP/s of the product (2 T H K / time)", "value": tflops,
+        "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": gw.dtype, "data": "synthetic",
+        "config": {"workload": gw.name, "T": gw.T, "H": gw.H, "K": gw.K,
+                   "plan": rarn.plan_gemm(gw.T, gw.H, gw.K, gw.dtype),
+                   "l2": "operands L2-resident after the first step (64 MB)",
+                   "pdl": not args.no_pdl},
+        "roofline": {"bound": "tensor", "achieved": tflops / world, "peak": peak,
+                     "unit": "TFLOP/s", "frac": tflops / world / peak, "traffic": None,
+                     "peak_source": kind},
+        "cpu_baseline": None,
+        "e2e": {"value": None, "unit": "TFLOP/s",
+                "note": "no host-buffer entry point for the GEMM form"},
+        "clocks": clocks, "gpu_launches": 2 * args.steps, "watchdog": rarn.watchdog(clear=True),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     rank, local_rank, world = dist_env()
@@ -555,6 +602,10 @@ def main():
 
     rarn.set_path(args.path)
     rarn.set_pdl(not args.no_pdl)
+    gemm = {gw.name: gw for gw in W.GEMM_CONFIGS}
+    if args.workload in gemm:
+        main_gemm(args, gemm[args.workload], device, rank, world)
+        return
     w = W.BY_NAME[args.workload]
     data = W.generate(w)
     tensors = device_tensors(w, data, device)

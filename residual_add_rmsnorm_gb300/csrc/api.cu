@@ -780,17 +780,18 @@ rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows parti
 // GEMM producer + fused residual-add RMSNorm: every matrix 16-bit, one type;
 // 16-byte aligned bases and row strides; the caller's workspace holds the
 // column tiles' partial sums of squares.
-static GemmPlan gemm_plan_env(int64_t T, int64_t H) {
-    int bk = 0, ns = 0, ctas = 0;  // measurements only
+static GemmPlan gemm_plan_env(int64_t T, int64_t H, int64_t K, int num_sms = 152) {
+    int bk = 0, ns = 0, ctas = 0, persist = -1;  // measurements only
     if (const char *v = getenv("RARN_GEMM_BK")) bk = atoi(v);
     if (const char *v = getenv("RARN_GEMM_NS")) ns = atoi(v);
     if (const char *v = getenv("RARN_GEMM_CTAS")) ctas = atoi(v);
-    return plan_gemm(T, H, bk, ns, ctas);
+    if (const char *v = getenv("RARN_GEMM_PERSIST")) persist = atoi(v);
+    return plan_gemm(T, H, K, bk, ns, ctas, persist, num_sms);
 }
 
 int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H) {
     if (T < 0 || H <= 0) return -1;
-    const GemmPlan gp = gemm_plan_env(T, H);
+    const GemmPlan gp = gemm_plan_env(T, H, 0);
     return gp.ns == 0 ? -1 : T * gp.tiles_n * 4;
 }
 
@@ -809,7 +810,7 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
         return RARN_ERR_INVALID_ARG;
     if (dt == RARN_F32) return RARN_ERR_UNSUPPORTED;  // the tensor path takes 16-bit operands
     if (T > (int64_t(1) << 31) - 128 || K > (int64_t(1) << 31) - 64) return RARN_ERR_UNSUPPORTED;
-    const GemmPlan gp = gemm_plan_env(T, H);
+    const GemmPlan gp = gemm_plan_env(T, H, K);
     if (gp.ns == 0) return RARN_ERR_UNSUPPORTED;
     const int64_t ws = T * gp.tiles_n * 4;
     if ((int64_t)workspace_bytes < ws || (reinterpret_cast<uintptr_t>(workspace) & 3u))
@@ -855,6 +856,7 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     c.bk = gp.bk;
     c.workspace = static_cast<float *>(workspace);
     c.num_sms = d->num_sms;
+    c.persistent = gp.persistent;
     c.pdl = g_pdl.load() != 0;
     c.watchdog = d->watchdog;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -871,7 +873,7 @@ rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w
         return rarn_gemm_add_rms_norm(y, a, w, residual, gamma, T, H, K, eps, nullptr, 0,
                                       stream);
     }
-    const GemmPlan gp = gemm_plan_env(T, H);
+    const GemmPlan gp = gemm_plan_env(T, H, K);
     if (gp.ns == 0) return RARN_ERR_UNSUPPORTED;
     float *scratch = nullptr;
     rarn_status st = gemm_scratch(&scratch);
@@ -895,16 +897,16 @@ rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w
 rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, char *out, size_t cap) {
     if (!out || cap == 0) return RARN_ERR_INVALID_ARG;
     if (!dtype_ok(dt) || T < 0 || H <= 0 || K <= 0) return RARN_ERR_INVALID_ARG;
-    const GemmPlan gp = dt == RARN_F32 ? GemmPlan{} : gemm_plan_env(T, H);
+    const GemmPlan gp = dt == RARN_F32 ? GemmPlan{} : gemm_plan_env(T, H, K);
     if (gp.ns == 0) {
         snprintf(out, cap, "none: unsupported shape or type");
         return RARN_ERR_UNSUPPORTED;
     }
     snprintf(out, cap,
              "gemm.tcgen05 cols_per_cta=%d col_tiles=%d bk=%d stages=%d smem=%d grid=%lld "
-             "kblocks=%lld + norm",
+             "kblocks=%lld persistent=%d + norm",
              gp.ns, gp.tiles_n, gp.bk, gp.stages, gp.smem, (long long)gp.grid,
-             (long long)((K + gp.bk - 1) / gp.bk));
+             (long long)((K + gp.bk - 1) / gp.bk), (int)gp.persistent);
     return RARN_OK;
 }
 

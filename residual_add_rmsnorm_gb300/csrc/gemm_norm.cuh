@@ -106,6 +106,10 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
                  : "memory");
@@ -464,6 +468,232 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Kernel 1, persistent and warp-specialised (256-column tiles): one CTA per
+// SM walks tiles b, b + G, ... (G = grid size).  Warp 0 lane 0 feeds a
+// 4-stage ring of [128 + 256] x 64 operand slabs by TMA; warp 1 lane 0
+// issues the MMAs into one of two TMEM accumulators (2 x 256 columns) while
+// warps 2-9 drain the other: the next tile's main loop overlaps this tile's
+// epilogue, and the whole shared memory serves the operand ring.  Epilogue
+// warp w reads TMEM lane quarter w % 4 and half (w - 2) / 4 of the tile's
+// columns; it reads the residual and writes h with 16-byte accesses of each
+// thread's own row, the next chunk's residual in flight while this chunk is
+// added.
+// ---------------------------------------------------------------------------
+constexpr int kWsStages = 4;
+constexpr int kWsEpiWarps = 8;
+
+// Barrier over the persistent kernel's 8 epilogue warps (id 2).
+__device__ __forceinline__ void epi_barrier_ws() {
+    asm volatile("bar.sync 2, %0;" ::"n"(32 * kWsEpiWarps) : "memory");
+}
+constexpr int kWsThreads = 64 + 32 * kWsEpiWarps;
+
+struct WsLayout {
+    static constexpr int a_bytes = kBM * 64 * 2;                 // 16 KB
+    static constexpr int b_bytes = kMmaN * 64 * 2;               // 32 KB
+    static constexpr int stage_bytes = a_bytes + b_bytes;        // 48 KB
+    static constexpr int ctl_off = kWsStages * stage_bytes;
+    // full[S], empty[S], tfull[2], tempty[2], mma_done, tmem slot, abort
+    // word, the epilogue's half-row sums
+    static constexpr int total =
+        ctl_off + (2 * kWsStages + 5) * 8 + 8 + kWsEpiWarps * 32 * 4 + 16 + 1024;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kWsThreads, 1)
+    k_gemm_res_ws(const __grid_constant__ CUtensorMap map_a,
+                  const __grid_constant__ CUtensorMap map_w, void *residual, int64_t ldr,
+                  Params p) {
+    constexpr int S = kWsStages;
+    constexpr int NS = kMmaN;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + WsLayout::ctl_off);
+    uint64_t *empty = full + S;
+    uint64_t *tfull = empty + S;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *mma_done = tempty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(mma_done + 1);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    float *half_ss = reinterpret_cast<float *>(tmem_slot + 2);  // [8 warps][32]
+    volatile int *tile_ok = reinterpret_cast<volatile int *>(half_ss + kWsEpiWarps * 32);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int C = p.C;
+    const int64_t mtiles = (p.T + kBM - 1) / kBM;
+    const int64_t ntiles = mtiles * C;
+    const int KB = p.kblocks;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull[a]), 1);
+            mbar_init(smem_u32(&tempty[a]), 32 * kWsEpiWarps);  // every epilogue thread
+        }
+        mbar_init(smem_u32(mma_done), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    grid_dependency_wait();  // A, W and the residual may come from the previous kernel
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer ----
+            int64_t kit = 0;  // k-slabs issued so far (all tiles)
+            bool stop = false;
+            for (int64_t tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x) {
+                const int m0 = (int)((tile / C) * kBM);
+                const int n0 = (int)((tile % C) * NS);
+                for (int kb = 0; kb < KB; ++kb, ++kit) {
+                    const int s = (int)(kit % S);
+                    if (kit >= S && !wait_phase(smem_u32(&empty[s]), (uint32_t)((kit / S - 1) & 1),
+                                                abort_flag, p.watchdog, p.wait_limit_ns)) {
+                        stop = true;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_arrive_expect_tx(fb, WsLayout::stage_bytes);
+                    const uint32_t sa = smem_u32(smem + s * WsLayout::stage_bytes);
+                    tma_load_2d(sa, &map_a, kb * 64, m0, fb);
+                    tma_load_2d(sa + WsLayout::a_bytes, &map_w, kb * 64, n0, fb);
+                }
+            }
+            if (*abort_flag) {  // issued fills land before the CTA's memory goes away
+                for (int64_t k = kit - S > 0 ? kit - S : 0; k < kit; ++k)
+                    wait_phase(smem_u32(&full[k % S]), (uint32_t)((k / S) & 1), abort_flag,
+                               p.watchdog, p.wait_limit_ns, true);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---- MMA issuer ----
+            const uint32_t idesc = instr_desc<T>();
+            int64_t kit = 0;
+            int it = 0;
+            bool stop = false;
+            for (int64_t tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x, ++it) {
+                const int acc = it & 1;
+                if (it >= 2 && !wait_phase(smem_u32(&tempty[acc]), (uint32_t)(((it >> 1) - 1) & 1),
+                                           abort_flag, p.watchdog, p.wait_limit_ns))
+                    break;
+                tmem_fence_after();
+                const uint32_t d = tmem + acc * NS;
+                for (int kb = 0; kb < KB; ++kb, ++kit) {
+                    const int s = (int)(kit % S);
+                    if (!wait_phase(smem_u32(&full[s]), (uint32_t)((kit / S) & 1), abort_flag,
+                                    p.watchdog, p.wait_limit_ns)) {
+                        stop = true;
+                        break;
+                    }
+                    tmem_fence_after();
+                    const uint32_t sa = smem_u32(smem + s * WsLayout::stage_bytes);
+                    const uint32_t sb = sa + WsLayout::a_bytes;
+#pragma unroll
+                    for (int kk = 0; kk < 64 / kMmaK; ++kk)
+                        mma_f16(d, smem_desc(sa + kk * kMmaK * 2, 128),
+                                smem_desc(sb + kk * kMmaK * 2, 128), idesc, (kb | kk) != 0);
+                    mma_commit(smem_u32(&empty[s]));
+                }
+                if (!stop) mma_commit(smem_u32(&tfull[acc]));
+            }
+            // every MMA issued has completed before tensor memory is freed
+            mma_commit(smem_u32(mma_done));
+            wait_phase(smem_u32(mma_done), 0, abort_flag, p.watchdog, p.wait_limit_ns, true);
+        }
+        __syncwarp();
+    } else {
+        // ---- epilogue: warps 2-9, TMEM lane quarter warp % 4, column half ----
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int c0 = ((warp - 2) >> 2) * (NS / 2);
+        int it = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+            const int acc = it & 1;
+            // one thread waits (bounded) and the 8 warps leave together, so
+            // none is left at the epilogue barrier
+            if (warp == 2 && lane == 0)
+                *tile_ok = wait_phase(smem_u32(&tfull[acc]), (uint32_t)((it >> 1) & 1), abort_flag,
+                                      p.watchdog, p.wait_limit_ns)
+                               ? 1
+                               : 0;
+            epi_barrier_ws();
+            if (!*tile_ok) break;
+            tmem_fence_after();
+            if (tile + gridDim.x >= ntiles) grid_launch_dependents();
+            const int64_t m0 = (tile / C) * kBM;
+            const int ntile = (int)(tile % C);
+            const int64_t t = m0 + row;
+            const bool live = t < p.T;
+            T *res = reinterpret_cast<T *>(residual) + (live ? t : 0) * ldr + ntile * NS + c0;
+            const uint32_t taddr =
+                tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * NS + c0;
+            uint4 cur[4], nxt[4];
+            if (live) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) cur[q] = ld_stream(res + 8 * q);
+            }
+            float ss = 0.f;
+            for (int c = 0; c < NS / 2; c += 32) {
+                if (live && c + 32 < NS / 2) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) nxt[q] = ld_stream(res + c + 32 + 8 * q);
+                }
+                float v[32];
+                tmem_ld32(taddr + c, v);
+                if (live) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float f[8];
+                        DT<T>::unpack(cur[q], f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            f[e] = DT<T>::round(v[8 * q + e] + f[e]);  // h: one rounding
+                            ss += f[e] * f[e];
+                        }
+                        st_global(res + c + 8 * q, DT<T>::pack(f));
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
+                }
+            }
+            tmem_fence_before();
+            mbar_arrive(smem_u32(&tempty[acc]));  // the accumulator is free again
+            // the two column halves' sums meet in shared memory, added in
+            // column order (first half, then second)
+            half_ss[(warp - 2) * 32 + lane] = ss;
+            epi_barrier_ws();
+            if (c0 == 0 && live && !*abort_flag)
+                p.ss[t * C + ntile] = ss + half_ss[(warp + 2) * 32 + lane];
+            epi_barrier_ws();
+        }
+    }
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
+                     : "memory");
+    }
+}
+
 // Kernel 2: y from the stored h and the tiles' partial sums.  A CTA per row
 // (grid-stride), VPT 16-byte packs per thread.
 template <typename T, int VPT>
@@ -485,10 +715,14 @@ __global__ void __launch_bounds__(256) k_norm_ss(NormParams p) {
                 gv[k] = ld_keep(g + (int64_t)j * EPV);
             }
         }
-        if (threadIdx.x == 0) {
+        if (threadIdx.x < 32) {
+            // lane q loads tile q's partial (all in flight at once); lane 0
+            // adds them in tile order (C <= 32)
+            const int lane = threadIdx.x;
+            const float part = lane < p.C ? p.ss[t * p.C + lane] : 0.f;
             float tot = 0.f;
-            for (int q = 0; q < p.C; ++q) tot += p.ss[t * p.C + q];  // tile order
-            inv_s = rsqrtf(tot / (float)p.H + p.eps);
+            for (int q = 0; q < p.C; ++q) tot += __shfl_sync(0xffffffffu, part, q);
+            if (lane == 0) inv_s = rsqrtf(tot / (float)p.H + p.eps);
         }
         __syncthreads();
         const float inv = inv_s;

@@ -54,8 +54,9 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
         !encode_map(&mw, c.w, c.H, c.K, c.ldw, kMmaN, BK, bf16) ||
         !encode_map(&mr, c.residual, c.T, c.H, c.ldr, kBM, kChunkCols, bf16))
         return cudaErrorInvalidValue;
-    // the epilogue stages the residual tile in the operand ring
-    if (c.stages * layout(c.stages, c.ns, BK).stage_bytes < (c.ns / kChunkCols) * kChunkBytes)
+    // the non-persistent kernel's epilogue stages the residual tile in the ring
+    if (!c.persistent &&
+        c.stages * layout(c.stages, c.ns, BK).stage_bytes < (c.ns / kChunkCols) * kChunkBytes)
         return cudaErrorInvalidValue;
     Params p{};
     p.ss = c.workspace;
@@ -68,13 +69,25 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     p.kblocks = static_cast<int>((c.K + BK - 1) / BK);
     p.watchdog = c.watchdog;
     p.wait_limit_ns = kWaitLimitNs;
-    const int smem = layout(c.stages, c.ns, BK).total;
-    auto kernel = k_gemm_res<T, BK>;
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
     const int64_t mblocks = (c.T + kBM - 1) / kBM;
-    e = launch_kernel(kernel, dim3(static_cast<unsigned>(mblocks * p.C)), dim3(kThreads),
-                      static_cast<size_t>(smem), st, c.pdl, 1, ma, mw, mr, p);
+    cudaError_t e;
+    if (c.persistent && BK == 64 && c.ns == kMmaN) {
+        auto kernel = k_gemm_res_ws<T>;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 WsLayout::total);
+        if (e != cudaSuccess) return e;
+        const int64_t grid = std::min<int64_t>(mblocks * p.C, c.num_sms);
+        e = launch_kernel(kernel, dim3(static_cast<unsigned>(grid)), dim3(kWsThreads),
+                          static_cast<size_t>(WsLayout::total), st, c.pdl, 1, ma, mw, c.residual,
+                          c.ldr, p);
+    } else {
+        const int smem = layout(c.stages, c.ns, BK).total;
+        auto kernel = k_gemm_res<T, BK>;
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        e = launch_kernel(kernel, dim3(static_cast<unsigned>(mblocks * p.C)), dim3(kThreads),
+                          static_cast<size_t>(smem), st, c.pdl, 1, ma, mw, mr, p);
+    }
     if (e != cudaSuccess) return e;
 
     NormParams q{};

@@ -351,13 +351,13 @@ def test_gemm_form_argument_errors(lib):
 def test_plan_gemm():
     """Columns per CTA from H; the K slab and ring depth fill one SM's shared
     memory; the workspace holds one float per row and column tile."""
-    p = rarn.plan_gemm(4096, 4096, 4096)
-    assert "cols_per_cta=256 col_tiles=16 bk=64 stages=2" in p and "grid=512" in p, p
-    assert "kblocks=64" in p, p
+    p = rarn.plan_gemm(4096, 4096, 4096)   # persistent: one CTA per SM walks 512 tiles
+    assert "cols_per_cta=256 col_tiles=16 bk=64 stages=4" in p and "grid=152" in p, p
+    assert "kblocks=64 persistent=1" in p, p
     p = rarn.plan_gemm(100, 768, 1000)
-    assert "cols_per_cta=256 col_tiles=3" in p and "stages=2" in p and "grid=3" in p, p
+    assert "cols_per_cta=256 col_tiles=3" in p and "persistent=1" in p and "grid=3" in p, p
     p = rarn.plan_gemm(8, 16384, 64)   # beyond 32 tiles of 256: 512-column tiles
-    assert "cols_per_cta=512 col_tiles=32 bk=32 stages=5" in p, p
+    assert "cols_per_cta=512 col_tiles=32 bk=32 stages=5" in p and "persistent=0" in p, p
     assert rarn.plan_gemm(8, 300, 64).startswith("none")
     assert rarn.plan_gemm(8, 16896, 64).startswith("none")   # 33 x 512: beyond 32 tiles
     assert rarn.plan_gemm(8, 4096, 64, "f32").startswith("none")

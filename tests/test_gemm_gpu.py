@@ -132,20 +132,24 @@ def run_case(T, H, K, dt="bf16", seed=0, lda=None, ldw=None, ldr=None, ldy=None,
 def test_gemm_parity(T, H, K, dt):
     plan = run_case(T, H, K, dt, seed=T + H + K)
     assert plan.startswith("gemm.tcgen05"), plan
+    assert ("persistent=1" in plan) == (H <= 8192 and K >= 512), plan
 
 
-@pytest.mark.parametrize("ns,bk,ctas", [("256", "32", "2"), ("256", "64", "1"),
-                                        ("512", "32", "1"), ("512", "64", "1")])
+@pytest.mark.parametrize("ns,bk,ctas", [("256", "32", "2"), ("256", "64", "2"),
+                                        ("256", "64", "1"), ("512", "32", "1"),
+                                        ("512", "64", "1")])
 def test_gemm_tilings(ns, bk, ctas, monkeypatch):
-    """Every tiling the planner can choose (measurement switches): 256 / 512
-    columns per CTA, 64-byte and 128-byte swizzled K slabs, one or two CTAs
-    per SM."""
+    """The non-persistent kernel in every tiling the planner can choose
+    (measurement switches): 256 / 512 columns per CTA, 64-byte and 128-byte
+    swizzled K slabs, one or two CTAs per SM.  (The default, persistent kernel
+    runs in every other test.)"""
     monkeypatch.setenv("RARN_GEMM_NS", ns)
     monkeypatch.setenv("RARN_GEMM_BK", bk)
     monkeypatch.setenv("RARN_GEMM_CTAS", ctas)
     for T, H, K in ((256, 1024, 448), (64, 512, 1000), (300, 2048, 2048)):
         plan = run_case(T, H, K, "bf16", seed=K)
         assert f"cols_per_cta={ns}" in plan and f"bk={bk}" in plan, plan
+        assert "persistent=0" in plan, plan
 
 
 def test_gemm_strides():
