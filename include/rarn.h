@@ -340,14 +340,15 @@ rarn_status rarn_set_pdl(int enable);
 int rarn_get_pdl(void);
 
 /*
- * Test hook for the watchdog: in the next launch of the stream kernel (on any
- * thread) CTA 0 expects 16 bytes more for fill number `fill` (0-based, in issue
- * order) than its copies bring, so that fill never completes; every
- * shared-memory barrier wait of that launch is bounded by
- * `wait_limit_ns` (1 ns .. 2 s).  The waits on that fill run out: the kernel
- * sets the watchdog word and returns with its outputs invalid, and the
- * context stays usable.  Returns RARN_ERR_INVALID_ARG for a negative fill or a
- * limit out of range.  Not for production use.
+ * Test hook for the watchdog: in the next launch (on any thread) of the
+ * stream kernel or of the GEMM form, CTA 0 expects 16 bytes more for pipeline
+ * fill number `fill` (0-based, in issue order) than its copies bring, so that
+ * fill never completes; every shared-memory barrier wait of that launch is
+ * bounded by `wait_limit_ns` (1 ns .. 2 s).  The waits on that fill run out:
+ * the kernel sets the watchdog word (bit 0 / 1: stream consumer / producer;
+ * bit 2: GEMM kernel) and returns with its outputs invalid, and the context
+ * stays usable.  Returns RARN_ERR_INVALID_ARG for a negative fill or a limit
+ * out of range.  Not for production use.
  */
 rarn_status rarn_test_stall(long long fill, unsigned long long wait_limit_ns);
 
@@ -373,8 +374,9 @@ rarn_status rarn_plan_fp8(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtyp
 /*
  * Watchdog word of the current device.  Kernels that wait on shared-memory
  * barriers give up after a bounded time, set a bit here and return without
- * hanging; their outputs are then not valid.  Bit 0: a consumer wait timed
- * out; bit 1: a producer wait timed out.  Synchronises the device.  If
+ * hanging; their outputs are then not valid.  Bit 0: a stream-kernel consumer
+ * wait timed out; bit 1: a stream-kernel producer wait; bit 2: a wait in a
+ * GEMM-form kernel.  Synchronises the device.  If
  * `clear` is nonzero the word is reset to 0 after reading.
  */
 rarn_status rarn_watchdog(uint32_t *flags, int clear);

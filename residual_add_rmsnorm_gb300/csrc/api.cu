@@ -29,7 +29,8 @@ namespace {
 thread_local int t_last_cuda_error = 0;
 std::atomic<int> g_path{RARN_PATH_AUTO};
 std::atomic<int> g_pdl{1};
-// test hook (rarn_test_stall): consumed by the next stream-kernel launch
+// test hook (rarn_test_stall): consumed by the next launch of the stream
+// kernel or of the GEMM form
 std::atomic<long long> g_stall_fill{-1};
 std::atomic<unsigned long long> g_stall_limit_ns{0};
 
@@ -857,6 +858,15 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     c.workspace = static_cast<float *>(workspace);
     c.num_sms = d->num_sms;
     c.persistent = gp.persistent;
+    c.wait_limit_ns = 2000000000ull;
+    c.stall_fill = -1;
+    {
+        const long long f = g_stall_fill.exchange(-1);
+        if (f >= 0) {
+            c.stall_fill = f;
+            c.wait_limit_ns = g_stall_limit_ns.load();
+        }
+    }
     c.pdl = g_pdl.load() != 0;
     c.watchdog = d->watchdog;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);

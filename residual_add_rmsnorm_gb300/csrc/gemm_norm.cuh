@@ -81,6 +81,8 @@ struct Params {
     int kblocks;       // ceil(K / BK)
     unsigned int *watchdog;
     unsigned long long wait_limit_ns;
+    long long stall_fill;  // test hook: in CTA 0 this ring fill (0-based, in issue order)
+                           // expects 16 bytes more than it brings, so it never completes
 };
 
 // Kernel 2 arguments.
@@ -347,9 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const uint32_t idesc = instr_desc<T>();
     const int KB = p.kblocks;
+    int issued = 0;  // producer: fills issued
     if (warp == 0 && lane == 0) {
         // ---- TMA producer ----
-        int issued = 0;
         for (int kb = 0; kb < KB; ++kb) {
             const int s = kb % S;
             if (kb >= S &&
@@ -357,21 +359,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                             p.wait_limit_ns))
                 break;
             const uint32_t fb = smem_u32(&full[s]);
-            mbar_arrive_expect_tx(fb, L.stage_bytes);
+            mbar_arrive_expect_tx(fb, L.stage_bytes + (blockIdx.x == 0 && kb == p.stall_fill ? 16u : 0u));
             const uint32_t sa = smem_u32(smem + s * L.stage_bytes);
             const uint32_t sb = sa + L.a_bytes;
             tma_load_2d(sa, &map_a, kb * BK, (int)m0, fb);
             for (int h = 0; h < NS / kMmaN; ++h)
                 tma_load_2d(sb + h * kMmaN * kRowBytes, &map_w, kb * BK, n0 + h * kMmaN, fb);
             issued = kb + 1;
-        }
-        // Drain: every fill issued must land before this CTA's memory goes
-        // away (bounded; only matters after an abort).
-        if (*abort_flag) {
-            const unsigned long long limit = p.wait_limit_ns;
-            for (int kb = issued - S > 0 ? issued - S : 0; kb < issued; ++kb)
-                wait_phase(smem_u32(&full[kb % S]), (kb / S) & 1, abort_flag, p.watchdog, limit,
-                           true);
         }
     } else if (warp == 1 && lane == 0) {
         // ---- MMA issuer ----
@@ -452,7 +446,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && m0 + r < p.T) p.ss[(m0 + r) * C + ntile] = ss;
     if (threadIdx.x == 0) {
         bulk_wait_all();  // the stores have completed before this CTA's memory goes away
-        if (*abort_flag) {  // loads issued after an abort elsewhere must still land (bounded)
+        if (*abort_flag) {
+            // after an abort anywhere in the CTA, the operand fills and the
+            // residual chunks issued land before its memory goes away (bounded)
+            for (int kb = issued - S > 0 ? issued - S : 0; kb < issued; ++kb)
+                wait_phase(smem_u32(&full[kb % S]), (kb / S) & 1, abort_flag, p.watchdog,
+                           p.wait_limit_ns, true);
             for (int c = 0; ok && c < nchunks; ++c)
                 wait_phase(smem_u32(&chunk_bar[c]), 0, abort_flag, p.watchdog, p.wait_limit_ns,
                            true);
@@ -553,10 +552,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const uint32_t tmem = *tmem_slot;
     grid_dependency_wait();  // A, W and the residual may come from the previous kernel
 
+    int64_t kit = 0;  // producer: k-slabs issued so far (all tiles)
     if (warp == 0) {
         if (lane == 0) {
             // ---- TMA producer ----
-            int64_t kit = 0;  // k-slabs issued so far (all tiles)
             bool stop = false;
             for (int64_t tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x) {
                 const int m0 = (int)((tile / C) * kBM);
@@ -569,16 +568,12 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                         break;
                     }
                     const uint32_t fb = smem_u32(&full[s]);
-                    mbar_arrive_expect_tx(fb, WsLayout::stage_bytes);
+                    mbar_arrive_expect_tx(
+                        fb, WsLayout::stage_bytes + (blockIdx.x == 0 && kit == p.stall_fill ? 16u : 0u));
                     const uint32_t sa = smem_u32(smem + s * WsLayout::stage_bytes);
                     tma_load_2d(sa, &map_a, kb * 64, m0, fb);
                     tma_load_2d(sa + WsLayout::a_bytes, &map_w, kb * 64, n0, fb);
                 }
-            }
-            if (*abort_flag) {  // issued fills land before the CTA's memory goes away
-                for (int64_t k = kit - S > 0 ? kit - S : 0; k < kit; ++k)
-                    wait_phase(smem_u32(&full[k % S]), (uint32_t)((k / S) & 1), abort_flag,
-                               p.watchdog, p.wait_limit_ns, true);
             }
         }
         __syncwarp();
@@ -686,6 +681,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
     }
     tmem_fence_before();
+    __syncthreads();
+    // after an abort anywhere in the CTA, the fills the producer issued land
+    // before the CTA's memory goes away (bounded)
+    if (warp == 0 && lane == 0 && *abort_flag) {
+        for (int64_t k = kit - S > 0 ? kit - S : 0; k < kit; ++k)
+            wait_phase(smem_u32(&full[k % S]), (uint32_t)((k / S) & 1), abort_flag, p.watchdog,
+                       p.wait_limit_ns, true);
+    }
     __syncthreads();
     tmem_fence_after();
     if (warp == 1) {

@@ -68,7 +68,8 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     p.stages = c.stages;
     p.kblocks = static_cast<int>((c.K + BK - 1) / BK);
     p.watchdog = c.watchdog;
-    p.wait_limit_ns = kWaitLimitNs;
+    p.wait_limit_ns = c.wait_limit_ns;
+    p.stall_fill = c.stall_fill;
     const int64_t mblocks = (c.T + kBM - 1) / kBM;
     cudaError_t e;
     if (c.persistent && BK == 64 && c.ns == kMmaN) {

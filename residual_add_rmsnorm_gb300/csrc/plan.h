@@ -139,6 +139,8 @@ struct GemmCall {
     bool persistent;     // the warp-specialised persistent kernel (256-column tiles)
     bool pdl;
     unsigned int *watchdog;
+    unsigned long long wait_limit_ns;  // bound on every shared-memory barrier wait
+    long long stall_fill;              // test hook (-1: off)
 };
 
 template <typename T>

@@ -34,3 +34,36 @@ def test_wait_runs_out_and_is_reported(fill):
     # the context is still usable and the next launch is correct
     check_parity(w, d, what="after a watchdog timeout")
     assert rarn.watchdog(clear=True) == 0
+
+
+@pytest.mark.parametrize("K,fill", [(1024, 0), (1024, 9), (256, 0), (256, 2)])
+def test_gemm_wait_runs_out_and_is_reported(K, fill):
+    """The GEMM form (persistent kernel for K = 1024, two-CTA kernel for
+    K = 256): one ring fill of CTA 0 never completes; every role's wait gives
+    up within the limit, the CTA drains what it issued and frees its tensor
+    memory, the watchdog bit is set, and the next call is correct."""
+    import torch
+    T, H = 1000, 2048
+    gen = torch.Generator(device="cuda").manual_seed(K + fill)
+    a = torch.randn(T, K, device="cuda", generator=gen).to(torch.bfloat16)
+    w = (torch.randn(H, K, device="cuda", generator=gen) / K ** 0.5).to(torch.bfloat16)
+    r0 = torch.randn(T, H, device="cuda", generator=gen).to(torch.bfloat16)
+    g = (torch.rand(H, device="cuda", generator=gen) + 0.5).to(torch.bfloat16)
+    r_ref = r0.clone()
+    y_ref = rarn.gemm_add_rms_norm(a, w, r_ref, g, 1e-6)
+    torch.cuda.synchronize()
+    assert rarn.watchdog(clear=True) == 0
+    lib = rarn.library()
+    assert lib.rarn_test_stall(fill, 20_000_000) == 0  # 20 ms bound
+    r_bad = r0.clone()
+    rarn.gemm_add_rms_norm(a, w, r_bad, g, 1e-6)  # outputs not valid; the call must return
+    torch.cuda.synchronize()
+    flags = rarn.watchdog(clear=True)
+    assert flags & 4, f"GEMM timeout not reported (flags={flags})"
+    # the context is still usable and the next call is correct (bit-identical
+    # to the clean run: deterministic kernels)
+    r_again = r0.clone()
+    y_again = rarn.gemm_add_rms_norm(a, w, r_again, g, 1e-6)
+    torch.cuda.synchronize()
+    assert rarn.watchdog(clear=True) == 0
+    assert torch.equal(y_again, y_ref) and torch.equal(r_again, r_ref)
