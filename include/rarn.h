@@ -308,8 +308,9 @@ rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w
                                            rarn_rows residual, const void *gamma, int64_t T,
                                            int64_t H, int64_t K, float eps, void *stream);
 
-/* Workspace bytes rarn_gemm_add_rms_norm needs for T rows of H (-1 if H is
- * not supported). */
+/* Workspace bytes rarn_gemm_add_rms_norm needs for T rows of H: 4 T times the
+ * number of column tiles (H / 256, or H / 512 beyond 8192; -1 if H is not
+ * supported). */
 int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H);
 
 /* Describe the GEMM kernels' tiling for a problem (pure host logic). */

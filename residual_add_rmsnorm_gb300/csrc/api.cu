@@ -792,8 +792,7 @@ static GemmPlan gemm_plan_env(int64_t T, int64_t H, int64_t K, int num_sms = 152
 
 int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H) {
     if (T < 0 || H <= 0) return -1;
-    const GemmPlan gp = gemm_plan_env(T, H, 0);
-    return gp.ns == 0 ? -1 : T * gp.tiles_n * 4;
+    return gemm_workspace_bytes(T, H);
 }
 
 rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_rows residual,

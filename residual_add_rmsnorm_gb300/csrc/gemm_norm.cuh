@@ -244,14 +244,15 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, int row_bytes) {
 }
 
 // Instruction descriptor, kind::f16: binary32 accumulator, A and B of the same
-// 16-bit type (bf16: 1, f16: 0), both K-major, M = 128, N = 256.
-template <typename T>
+// 16-bit type (bf16: 1, f16: 0), both K-major, M = 128, N = N_ (default 256).
+template <typename T, int N_ = kMmaN>
 __host__ __device__ constexpr uint32_t instr_desc() {
+    static_assert(N_ % 16 == 0 && N_ >= 16 && N_ <= 256, "M = 128 takes N = 16 .. 256");
     constexpr uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
     return (1u << 4)                   // D: f32
            | (ab << 7) | (ab << 10)    // A, B type
            | (0u << 15) | (0u << 16)   // K-major A, B
-           | ((uint32_t)(kMmaN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+           | ((uint32_t)(N_ >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
 }
 
 __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
@@ -468,10 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Kernel 1, persistent and warp-specialised (256-column tiles): one CTA per
-// SM walks tiles b, b + G, ... (G = grid size).  Warp 0 lane 0 feeds a
-// 4-stage ring of [128 + 256] x 64 operand slabs by TMA; warp 1 lane 0
-// issues the MMAs into one of two TMEM accumulators (2 x 256 columns) while
+// Kernel 1, persistent and warp-specialised (NT = 256- or 128-column tiles):
+// one CTA per SM walks tiles b, b + G, ... (G = grid size).  Warp 0 lane 0
+// feeds a ring of [128 + NT] x 64 operand slabs by TMA (4 stages for NT = 256,
+// 6 for 128); warp 1 lane 0 issues the MMAs into one of two TMEM accumulators
+// (2 x NT columns) while
 // warps 2-9 drain the other: the next tile's main loop overlaps this tile's
 // epilogue, and the whole shared memory serves the operand ring.  Epilogue
 // warp w reads TMEM lane quarter w % 4 and half (w - 2) / 4 of the tile's
@@ -479,7 +481,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // thread's own row, the next chunk's residual in flight while this chunk is
 // added.
 // ---------------------------------------------------------------------------
-constexpr int kWsStages = 4;
 constexpr int kWsEpiWarps = 8;
 
 // Barrier over the persistent kernel's 8 epilogue warps (id 2).
@@ -488,24 +489,27 @@ __device__ __forceinline__ void epi_barrier_ws() {
 }
 constexpr int kWsThreads = 64 + 32 * kWsEpiWarps;
 
+template <int NT>
 struct WsLayout {
+    static constexpr int stages = NT == 256 ? 4 : 6;
     static constexpr int a_bytes = kBM * 64 * 2;                 // 16 KB
-    static constexpr int b_bytes = kMmaN * 64 * 2;               // 32 KB
-    static constexpr int stage_bytes = a_bytes + b_bytes;        // 48 KB
-    static constexpr int ctl_off = kWsStages * stage_bytes;
+    static constexpr int b_bytes = NT * 64 * 2;                  // 32 / 16 KB
+    static constexpr int stage_bytes = a_bytes + b_bytes;        // 48 / 32 KB
+    static constexpr int ctl_off = stages * stage_bytes;
     // full[S], empty[S], tfull[2], tempty[2], mma_done, tmem slot, abort
     // word, the epilogue's half-row sums
     static constexpr int total =
-        ctl_off + (2 * kWsStages + 5) * 8 + 8 + kWsEpiWarps * 32 * 4 + 16 + 1024;
+        ctl_off + (2 * stages + 5) * 8 + 8 + kWsEpiWarps * 32 * 4 + 16 + 1024;
 };
 
-template <typename T>
+template <typename T, int NT>
 __global__ void __launch_bounds__(kWsThreads, 1)
     k_gemm_res_ws(const __grid_constant__ CUtensorMap map_a,
                   const __grid_constant__ CUtensorMap map_w, void *residual, int64_t ldr,
                   Params p) {
-    constexpr int S = kWsStages;
-    constexpr int NS = kMmaN;
+    using WsLayout = rarn::gemm::WsLayout<NT>;
+    constexpr int S = WsLayout::stages;
+    constexpr int NS = NT;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -580,7 +584,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ---- MMA issuer ----
-            const uint32_t idesc = instr_desc<T>();
+            const uint32_t idesc = instr_desc<T, NT>();
             int64_t kit = 0;
             int it = 0;
             bool stop = false;

@@ -72,15 +72,17 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     p.stall_fill = c.stall_fill;
     const int64_t mblocks = (c.T + kBM - 1) / kBM;
     cudaError_t e;
-    if (c.persistent && BK == 64 && c.ns == kMmaN) {
-        auto kernel = k_gemm_res_ws<T>;
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 WsLayout::total);
-        if (e != cudaSuccess) return e;
+    if (c.persistent && BK == 64 && c.ns == 256) {
         const int64_t grid = std::min<int64_t>(mblocks * p.C, c.num_sms);
-        e = launch_kernel(kernel, dim3(static_cast<unsigned>(grid)), dim3(kWsThreads),
-                          static_cast<size_t>(WsLayout::total), st, c.pdl, 1, ma, mw, c.residual,
-                          c.ldr, p);
+        auto go = [&](auto kernel, int smem_bytes) {
+            cudaError_t r = cudaFuncSetAttribute(
+                kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+            if (r != cudaSuccess) return r;
+            return launch_kernel(kernel, dim3(static_cast<unsigned>(grid)), dim3(kWsThreads),
+                                 static_cast<size_t>(smem_bytes), st, c.pdl, 1, ma, mw,
+                                 c.residual, c.ldr, p);
+        };
+        e = go(k_gemm_res_ws<T, 256>, WsLayout<256>::total);
     } else {
         const int smem = layout(c.stages, c.ns, BK).total;
         auto kernel = k_gemm_res<T, BK>;

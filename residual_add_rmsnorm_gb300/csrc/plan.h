@@ -207,8 +207,8 @@ inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
     return g;
 }
 
-// Workspace of the GEMM form: one binary32 per row and column tile (-1: H
-// not supported).
+// Workspace of the GEMM form: one binary32 per row and column tile (the
+// column tiling depends on H only; -1: H not supported).
 inline int64_t gemm_workspace_bytes(int64_t T, int64_t H) {
     const GemmPlan g = plan_gemm(T, H, 0);
     return g.ns == 0 ? -1 : T * g.tiles_n * 4;
