@@ -79,23 +79,34 @@ __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG, TR>::value, 1) k_clus
 template <typename T, int OP, typename TR>
 static cudaError_t launch_cluster_op(const Problem &p, const Plan &pl, cudaStream_t st) {
     const dim3 g(pl.grid), b(pl.block);
-    auto go = [&](auto kernel) {
-        return launch_kernel(kernel, g, b, 0, st, pl.pdl, pl.cluster, p);
+    // combinations over the register budget are never planned: not built
+    auto go = [&](auto vpt, auto pg) {
+        constexpr int V = decltype(vpt)::value;
+        constexpr bool G = decltype(pg)::value;
+        if constexpr (VecBound<T, V, OP, G, TR>::b > 0)
+            return launch_kernel(k_cluster_vec<T, V, OP, G, TR>, g, b, 0, st, pl.pdl, pl.cluster,
+                                 p);
+        else
+            return cudaErrorInvalidValue;
     };
+    using V1 = std::integral_constant<int, 1>;
+    using V2 = std::integral_constant<int, 2>;
+    using V4 = std::integral_constant<int, 4>;
+    using V8 = std::integral_constant<int, 8>;
     if (pl.prefetch_gamma) {
         switch (pl.per_thread) {
-        case 1: return go(k_cluster_vec<T, 1, OP, true, TR>);
-        case 2: return go(k_cluster_vec<T, 2, OP, true, TR>);
-        case 4: return go(k_cluster_vec<T, 4, OP, true, TR>);
-        case 8: return go(k_cluster_vec<T, 8, OP, true, TR>);
+        case 1: return go(V1{}, std::true_type{});
+        case 2: return go(V2{}, std::true_type{});
+        case 4: return go(V4{}, std::true_type{});
+        case 8: return go(V8{}, std::true_type{});
         default: return cudaErrorInvalidValue;
         }
     }
     switch (pl.per_thread) {
-    case 1: return go(k_cluster_vec<T, 1, OP, false, TR>);
-    case 2: return go(k_cluster_vec<T, 2, OP, false, TR>);
-    case 4: return go(k_cluster_vec<T, 4, OP, false, TR>);
-    case 8: return go(k_cluster_vec<T, 8, OP, false, TR>);
+    case 1: return go(V1{}, std::false_type{});
+    case 2: return go(V2{}, std::false_type{});
+    case 4: return go(V4{}, std::false_type{});
+    case 8: return go(V8{}, std::false_type{});
     default: return cudaErrorInvalidValue;
     }
 }

@@ -718,6 +718,28 @@ template <typename T, int OP, typename TR, bool Q8>
 static cudaError_t launch_rows_op(const Problem &p, const Plan &pl, cudaStream_t st) {
     const dim3 g(pl.grid), b(pl.block);
     auto go = [&](auto kernel) { return launch_kernel(kernel, g, b, 0, st, pl.pdl, 1, p); };
+    // combinations over the register budget are never planned: not built
+    auto go_vec = [&](auto vpt, auto pg) {
+        constexpr int V = decltype(vpt)::value;
+        constexpr bool G = decltype(pg)::value;
+        if constexpr (VecBound<T, V, OP, G, TR>::b > 0)
+            return go(k_cta_vec<T, V, OP, G, TR, Q8>);
+        else
+            return cudaErrorInvalidValue;
+    };
+    auto go_pipe = [&](auto vpt) {
+        constexpr int V = decltype(vpt)::value;
+        if constexpr (PipeBound<T, V, OP, TR>::b > 0)
+            return go(k_cta_pipe<T, V, OP, TR, Q8>);
+        else
+            return cudaErrorInvalidValue;
+    };
+    using V1 = std::integral_constant<int, 1>;
+    using V2 = std::integral_constant<int, 2>;
+    using V4 = std::integral_constant<int, 4>;
+    using V8 = std::integral_constant<int, 8>;
+    using PGt = std::true_type;
+    using PGf = std::false_type;
     switch (pl.kind) {
     case KIND_WARP:
         if constexpr (OP != OP_REDUCE) {
@@ -740,29 +762,29 @@ static cudaError_t launch_rows_op(const Problem &p, const Plan &pl, cudaStream_t
         if constexpr (OP != OP_REDUCE) {
             if (pl.vec && pl.pipe) {
                 switch (pl.per_thread) {
-                case 1: return go(k_cta_pipe<T, 1, OP, TR, Q8>);
-                case 2: return go(k_cta_pipe<T, 2, OP, TR, Q8>);
-                case 4: return go(k_cta_pipe<T, 4, OP, TR, Q8>);
-                case 8: return go(k_cta_pipe<T, 8, OP, TR, Q8>);
+                case 1: return go_pipe(V1{});
+                case 2: return go_pipe(V2{});
+                case 4: return go_pipe(V4{});
+                case 8: return go_pipe(V8{});
                 default: return cudaErrorInvalidValue;
                 }
             }
         }
         if (pl.vec && pl.prefetch_gamma) {
             switch (pl.per_thread) {
-            case 1: return go(k_cta_vec<T, 1, OP, true, TR, Q8>);
-            case 2: return go(k_cta_vec<T, 2, OP, true, TR, Q8>);
-            case 4: return go(k_cta_vec<T, 4, OP, true, TR, Q8>);
-            case 8: return go(k_cta_vec<T, 8, OP, true, TR, Q8>);
+            case 1: return go_vec(V1{}, PGt{});
+            case 2: return go_vec(V2{}, PGt{});
+            case 4: return go_vec(V4{}, PGt{});
+            case 8: return go_vec(V8{}, PGt{});
             default: return cudaErrorInvalidValue;
             }
         }
         if (pl.vec) {
             switch (pl.per_thread) {
-            case 1: return go(k_cta_vec<T, 1, OP, false, TR, Q8>);
-            case 2: return go(k_cta_vec<T, 2, OP, false, TR, Q8>);
-            case 4: return go(k_cta_vec<T, 4, OP, false, TR, Q8>);
-            case 8: return go(k_cta_vec<T, 8, OP, false, TR, Q8>);
+            case 1: return go_vec(V1{}, PGf{});
+            case 2: return go_vec(V2{}, PGf{});
+            case 4: return go_vec(V4{}, PGf{});
+            case 8: return go_vec(V8{}, PGf{});
             default: return cudaErrorInvalidValue;
             }
         }
