@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "../../include/rarn.h"
+#include "gemm_plan.h"
 #include "plan.h"
 
 using namespace rarn;

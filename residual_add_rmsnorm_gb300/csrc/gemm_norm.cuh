@@ -41,7 +41,7 @@
 #include <type_traits>
 
 #include "common.cuh"
-#include "plan.h"
+#include "gemm_plan.h"
 
 namespace rarn {
 namespace gemm {

@@ -1,0 +1,106 @@
+// gemm_plan.h -- the GEMM form's call description, tile planner and the
+// launcher the C ABI dispatches to.  Host-side declarations only.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+namespace rarn {
+
+// GEMM producer with the fused residual-add RMSNorm epilogue (gemm_norm.cuh).
+struct GemmCall {
+    const void *a;
+    int64_t lda;
+    const void *w;
+    int64_t ldw;
+    void *residual;
+    int64_t ldr;
+    void *y;
+    int64_t ldy;
+    const void *gamma;
+    int64_t T, H, K;
+    float eps;
+    int ns, stages, bk;  // columns per CTA, ring stages, K slab (elements)
+    float *workspace;    // [T][H / ns] partial sums of squares
+    int num_sms;
+    bool persistent;     // the warp-specialised persistent kernel (256-column tiles)
+    bool pdl;
+    unsigned int *watchdog;
+    unsigned long long wait_limit_ns;  // bound on every shared-memory barrier wait
+    long long stall_fill;              // test hook (-1: off)
+};
+
+template <typename T>
+cudaError_t launch_gemm_norm(const GemmCall &c, cudaStream_t stream);
+
+// Tile plan of the GEMM kernel: columns per CTA, K slab and ring depth within
+// the shared memory given to one CTA (one or two CTAs per SM).  ns = 0:
+// unsupported H.
+struct GemmPlan {
+    int ns = 0, tiles_n = 0, bk = 0, stages = 0, smem = 0;
+    int64_t grid = 0;
+    bool persistent = false;
+};
+
+constexpr int kGemmMaxTilesN = 32;
+
+// Measured on GB300 (T = K = H = 4096, bf16): 256 columns per CTA with
+// 128-byte K slabs and two CTAs per SM (one CTA's epilogue overlaps the
+// other's main loop) 124.5 us; 512 columns, one CTA per SM, 147 us.  Rows
+// wider than 32 tiles of 256 use 512-column tiles.
+inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
+                          int ns_override = 0, int ctas_override = 0, int persist_override = -1,
+                          int num_sms = 152) {
+    GemmPlan g;
+    const bool fit256 = H % 256 == 0 && H / 256 <= kGemmMaxTilesN;
+    const bool fit512 = H % 512 == 0 && H / 512 <= kGemmMaxTilesN;
+    int ctas;
+    if (fit256 && ns_override != 512) {
+        g.ns = 256;
+        g.bk = 64;
+        ctas = 2;
+    } else if (fit512) {
+        g.ns = 512;
+        g.bk = 32;
+        ctas = 1;
+    } else {
+        return g;
+    }
+    if (bk_override == 32 || bk_override == 64) g.bk = bk_override;
+    if (ctas_override == 1 || ctas_override == 2) ctas = ctas_override;
+    const int smem_budget = ctas == 2 ? 113 * 1024 : 227 * 1024;
+    g.tiles_n = (int)(H / g.ns);
+    const int stage = (128 + g.ns) * g.bk * 2;
+    const int fixed = 1024 + 1024;  // barriers, alignment slack
+    g.stages = (smem_budget - fixed) / stage;
+    if (g.stages > 8) g.stages = 8;
+    // the epilogue stages the residual tile ([128 x ns] 16-bit) in the ring
+    if (g.stages < 2 || g.stages * stage < 128 * g.ns * 2) return GemmPlan{};
+    g.smem = g.stages * stage + fixed;
+    g.grid = ((T + 127) / 128) * g.tiles_n;
+    // 256-column tiles with 128-byte K slabs run persistent and
+    // warp-specialised by default (one CTA per SM, 4 stages, two
+    // accumulators: the main loop hides the epilogue), except for short K,
+    // where there is little main loop to hide it behind and the two-CTA
+    // kernel's TMA-staged epilogue is faster (K = 64: 26 vs 39 us at T = H =
+    // 4096)
+    g.persistent = g.ns == 256 && g.bk == 64 && ctas_override == 0 &&
+                   (persist_override == 1 || (persist_override != 0 && K >= 512));
+    if (g.persistent) {
+        g.stages = 4;
+        g.smem = 4 * stage + 1024 + 1024;
+        g.grid = std::min<int64_t>(g.grid, num_sms);
+    }
+    return g;
+}
+
+// Workspace of the GEMM form: one binary32 per row and column tile (the
+// column tiling depends on H only; -1: H not supported).
+inline int64_t gemm_workspace_bytes(int64_t T, int64_t H) {
+    const GemmPlan g = plan_gemm(T, H, 0);
+    return g.ns == 0 ? -1 : T * g.tiles_n * 4;
+}
+
+}  // namespace rarn
