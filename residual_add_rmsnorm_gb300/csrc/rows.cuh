@@ -544,9 +544,13 @@ __global__ void __launch_bounds__(PipeBound<T, VPT, OP, TR>::value) k_cta_pipe(P
     QMul qm{1.f, 1.f};
     if constexpr (Q8) qm = quant_tensor(p);
     const bool qrow = Q8 && p.qmode == Q_ROW;
-    // 8-bit output: gamma in registers (the row maximum and pass 2 both use it)
+    // gamma in registers (with an 8-bit output the row maximum uses it too),
+    // up to 4 packs per thread with a residual of type T (measured: C3
+    // 21.84 -> 21.64 us; with a binary32 residual the extra registers cost a
+    // CTA per SM: 302 -> 352 us, so not there)
+    constexpr bool PGP = Q8 || (VPT <= 4 && std::is_same<T, TR>::value);
     uint4 gv[VPT];
-    if constexpr (Q8) load_gamma_vec<T, VPT>(p, threadIdx.x, blockDim.x, nv, gv);
+    if constexpr (PGP) load_gamma_vec<T, VPT>(p, threadIdx.x, blockDim.x, nv, gv);
     RowLoads<T, VPT, OP, TR> next;
     int64_t t = blockIdx.x;
     if (t < p.T) issue_row_loads<T, VPT, OP, TR>(p, t, threadIdx.x, blockDim.x, nv, next);
@@ -562,9 +566,9 @@ __global__ void __launch_bounds__(PipeBound<T, VPT, OP, TR>::value) k_cta_pipe(P
         const float ss =
             consume_row_loads<T, VPT, OP, TR>(p, t, threadIdx.x, blockDim.x, nv, cur, hv);
         const float am =
-            qrow ? amax_vec<T, VPT, TR, Q8>(p, threadIdx.x, blockDim.x, nv, hv, gv) : 0.f;
+            qrow ? amax_vec<T, VPT, TR, PGP>(p, threadIdx.x, blockDim.x, nv, hv, gv) : 0.f;
         const float inv = row_inv_cta<Q8>(p, t, ss, am, red[par], red2 + 32 * par, qm);
-        pass2_vec<T, VPT, TR, Q8, Q8>(p, t, threadIdx.x, blockDim.x, nv, hv, inv, gv, qm);
+        pass2_vec<T, VPT, TR, PGP, Q8>(p, t, threadIdx.x, blockDim.x, nv, hv, inv, gv, qm);
     }
 }
 
