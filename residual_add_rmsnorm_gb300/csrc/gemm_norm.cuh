@@ -489,12 +489,14 @@ __device__ __forceinline__ void epi_barrier_ws() {
 }
 constexpr int kWsThreads = 64 + 32 * kWsEpiWarps;
 
-template <int NT>
+template <int NT, int BK = 64>
 struct WsLayout {
-    static constexpr int stages = NT == 256 ? 4 : 6;
-    static constexpr int a_bytes = kBM * 64 * 2;                 // 16 KB
-    static constexpr int b_bytes = NT * 64 * 2;                  // 32 / 16 KB
-    static constexpr int stage_bytes = a_bytes + b_bytes;        // 48 / 32 KB
+    static constexpr int a_bytes = kBM * BK * 2;                 // 16 KB (BK = 64)
+    static constexpr int b_bytes = NT * BK * 2;                  // 32 KB (NT = 256, BK = 64)
+    static constexpr int stage_bytes = a_bytes + b_bytes;        // 48 KB
+    // as many stages as fit next to 3 KB of barriers and slack (at most 9)
+    static constexpr int stages =
+        (227 * 1024 - 3 * 1024) / stage_bytes > 9 ? 9 : (227 * 1024 - 3 * 1024) / stage_bytes;
     static constexpr int ctl_off = stages * stage_bytes;
     // full[S], empty[S], tfull[2], tempty[2], mma_done, tmem slot, abort
     // word, the epilogue's half-row sums
@@ -502,12 +504,13 @@ struct WsLayout {
         ctl_off + (2 * stages + 5) * 8 + 8 + kWsEpiWarps * 32 * 4 + 16 + 1024;
 };
 
-template <typename T, int NT>
+template <typename T, int NT, int BK>
 __global__ void __launch_bounds__(kWsThreads, 1)
     k_gemm_res_ws(const __grid_constant__ CUtensorMap map_a,
                   const __grid_constant__ CUtensorMap map_w, void *residual, int64_t ldr,
                   Params p) {
-    using WsLayout = rarn::gemm::WsLayout<NT>;
+    static_assert(BK == 64 || BK == 32, "K slab of 128 or 64 bytes");
+    using WsLayout = rarn::gemm::WsLayout<NT, BK>;
     constexpr int S = WsLayout::stages;
     constexpr int NS = NT;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -575,8 +578,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     mbar_arrive_expect_tx(
                         fb, WsLayout::stage_bytes + (blockIdx.x == 0 && kit == p.stall_fill ? 16u : 0u));
                     const uint32_t sa = smem_u32(smem + s * WsLayout::stage_bytes);
-                    tma_load_2d(sa, &map_a, kb * 64, m0, fb);
-                    tma_load_2d(sa + WsLayout::a_bytes, &map_w, kb * 64, n0, fb);
+                    tma_load_2d(sa, &map_a, kb * BK, m0, fb);
+                    tma_load_2d(sa + WsLayout::a_bytes, &map_w, kb * BK, n0, fb);
                 }
             }
         }
@@ -606,9 +609,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     const uint32_t sa = smem_u32(smem + s * WsLayout::stage_bytes);
                     const uint32_t sb = sa + WsLayout::a_bytes;
 #pragma unroll
-                    for (int kk = 0; kk < 64 / kMmaK; ++kk)
-                        mma_f16(d, smem_desc(sa + kk * kMmaK * 2, 128),
-                                smem_desc(sb + kk * kMmaK * 2, 128), idesc, (kb | kk) != 0);
+                    for (int kk = 0; kk < BK / kMmaK; ++kk)
+                        mma_f16(d, smem_desc(sa + kk * kMmaK * 2, BK * 2),
+                                smem_desc(sb + kk * kMmaK * 2, BK * 2), idesc, (kb | kk) != 0);
                     mma_commit(smem_u32(&empty[s]));
                 }
                 if (!stop) mma_commit(smem_u32(&tfull[acc]));

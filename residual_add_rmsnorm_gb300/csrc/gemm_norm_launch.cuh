@@ -71,25 +71,28 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     p.wait_limit_ns = c.wait_limit_ns;
     p.stall_fill = c.stall_fill;
     const int64_t mblocks = (c.T + kBM - 1) / kBM;
-    cudaError_t e;
-    if (c.persistent && BK == 64 && c.ns == 256) {
-        const int64_t grid = std::min<int64_t>(mblocks * p.C, c.num_sms);
-        auto go = [&](auto kernel, int smem_bytes) {
-            cudaError_t r = cudaFuncSetAttribute(
-                kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
-            if (r != cudaSuccess) return r;
-            return launch_kernel(kernel, dim3(static_cast<unsigned>(grid)), dim3(kWsThreads),
-                                 static_cast<size_t>(smem_bytes), st, c.pdl, 1, ma, mw,
-                                 c.residual, c.ldr, p);
-        };
-        e = go(k_gemm_res_ws<T, 256>, WsLayout<256>::total);
-    } else {
+    cudaError_t e = cudaErrorInvalidValue;
+    bool launched = false;
+    if constexpr (BK == 64) {  // the persistent kernel takes 128-byte K slabs only
+        if (c.persistent && c.ns == 256) {
+            const int64_t grid = std::min<int64_t>(mblocks * p.C, c.num_sms);
+            auto kernel = k_gemm_res_ws<T, 256, BK>;
+            constexpr int smem = WsLayout<256, BK>::total;
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e == cudaSuccess)
+                e = launch_kernel(kernel, dim3(static_cast<unsigned>(grid)), dim3(kWsThreads),
+                                  static_cast<size_t>(smem), st, c.pdl, 1, ma, mw, c.residual,
+                                  c.ldr, p);
+            launched = true;
+        }
+    }
+    if (!launched) {
         const int smem = layout(c.stages, c.ns, BK).total;
         auto kernel = k_gemm_res<T, BK>;
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        e = launch_kernel(kernel, dim3(static_cast<unsigned>(mblocks * p.C)), dim3(kThreads),
-                          static_cast<size_t>(smem), st, c.pdl, 1, ma, mw, mr, p);
+        if (e == cudaSuccess)
+            e = launch_kernel(kernel, dim3(static_cast<unsigned>(mblocks * p.C)), dim3(kThreads),
+                              static_cast<size_t>(smem), st, c.pdl, 1, ma, mw, mr, p);
     }
     if (e != cudaSuccess) return e;
 

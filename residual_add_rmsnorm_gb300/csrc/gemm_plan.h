@@ -89,8 +89,8 @@ inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
     g.persistent = g.ns == 256 && g.bk == 64 && ctas_override == 0 &&
                    (persist_override == 1 || (persist_override != 0 && K >= 512));
     if (g.persistent) {
-        g.stages = 4;
-        g.smem = 4 * stage + 1024 + 1024;
+        g.stages = std::min(9, (227 * 1024 - 3 * 1024) / stage);
+        g.smem = g.stages * stage + 3 * 1024;
         g.grid = std::min<int64_t>(g.grid, num_sms);
     }
     return g;
