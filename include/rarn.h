@@ -295,14 +295,37 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
                                    void *workspace, size_t workspace_bytes, void *stream);
 
 /*
- * rarn_gemm_add_rms_norm without a workspace argument: allocates nothing and
- * takes no caller memory; the partial sums live in a 4 MB scratch array that
- * the library reserves in device memory when it is loaded (found at the first
- * call on each device), and problems with more rows than it holds run as
- * several launch pairs on `stream`.  The paper has no counterpart.  Because
- * every call on a device shares that scratch, calls must be ordered (one
- * stream, or streams synchronised with each other); results are bit-identical
- * to the workspace form.  Errors as for rarn_gemm_add_rms_norm.
+ * rarn_gemm_add_rms_norm for callers that cannot allocate device memory: it
+ * takes no workspace argument and calls no cudaMalloc, cudaFree or other
+ * allocating routine.  Such callers include plug-ins inside a host program
+ * that owns every byte of device memory and hands out no allocator, runtimes
+ * that plan all memory before they start serving and forbid allocation
+ * afterwards, and latency-critical code that cannot afford the implicit
+ * device synchronisation of cudaMalloc / cudaFree.  The paper has no
+ * counterpart.
+ *
+ * Scratch: the per-row partial sums of squares live in a file-scope device
+ * array of 2^20 binary32 values (4 MiB, 256-byte aligned) that the library
+ * reserves on every GPU it is loaded on and keeps until the process exits.
+ * A launch pair holds T times the column-tile count (H / 256, or H / 512
+ * beyond 8192) of those values, so a call with more rows than the array
+ * holds (32768 rows at the widest tiling) runs as several launch pairs on
+ * `stream`, one after another.  Every value is written before it is read, so
+ * nothing needs clearing between calls.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the array's device address with cudaGetSymbolAddress and keeps it; make
+ * that first call before any stream capture begins.  A failed look-up
+ * returns RARN_ERR_CUDA.
+ *
+ * Ordering: every call on a device shares the one array, which keeps the
+ * last call's contents.  Calls that overlap on the GPU (different streams
+ * with no ordering between them) race on it and give wrong results; issue
+ * them on one stream or synchronise the streams.
+ *
+ * Arguments, results (bit-identical to the workspace form) and other errors
+ * as for rarn_gemm_add_rms_norm; H beyond the supported tilings returns
+ * RARN_ERR_UNSUPPORTED.
  */
 rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w,
                                            rarn_rows residual, const void *gamma, int64_t T,

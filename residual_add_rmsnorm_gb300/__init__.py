@@ -527,8 +527,17 @@ def gemm_add_rms_norm(a, w, residual, gamma, eps: float, out=None, workspace=Non
 
 
 def gemm_add_rms_norm_noalloc(a, w, residual, gamma, eps: float, out=None):
-    """gemm_add_rms_norm through the entry point that takes no workspace (the
-    library's own static scratch; calls on a device must be ordered)."""
+    """gemm_add_rms_norm through the entry point that allocates nothing.
+
+    For callers that cannot allocate device memory (a plug-in whose host
+    program owns all device memory, a runtime that forbids allocation once it
+    serves, code that cannot take cudaMalloc's implicit synchronisation): the
+    partial sums live in a 4 MiB array the library reserves on each GPU when
+    it is loaded.  The first call on a device looks up that array's address;
+    make it before any stream capture.  Calls on one device share the array,
+    so calls that overlap on the GPU race: keep them on one stream or
+    synchronise the streams.  ``out`` is allocated here only when not given;
+    pass it to keep the whole call allocation-free."""
     import torch
     T, K = a.shape
     H = w.shape[0]

@@ -21,7 +21,9 @@ using namespace rarn;
 __device__ unsigned int g_rarn_watchdog = 0;
 
 // Scratch of the workspace-free GEMM entry point (rarn_gemm_add_rms_norm_noalloc):
-// 4 MB reserved with the module, so that entry point allocates nothing.
+// 4 MB reserved with the module, so that entry point allocates nothing.  In
+// host code this name is only a stand-in: the device address comes from
+// cudaGetSymbolAddress (gemm_scratch below), once per device.
 constexpr int64_t kGemmScratchFloats = int64_t(1) << 20;
 static __device__ __align__(256) float g_rarn_gemm_scratch[kGemmScratchFloats];
 

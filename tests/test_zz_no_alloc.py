@@ -1,6 +1,14 @@
-"""The GEMM form's workspace-free entry point against the workspace one:
-the same inputs through both, the workspace-free one called twice in a row
-(its static scratch reused), every output bit-identical.  Collected last."""
+"""The GEMM form's allocation-free entry point against the workspace one.
+
+Callers that cannot allocate device memory (plug-ins whose host program owns
+all of it, runtimes that forbid allocation once serving, latency-critical
+code that cannot take cudaMalloc's implicit synchronisation) use
+rarn_gemm_add_rms_norm_noalloc, which keeps its partial sums in an array the
+library reserves on the GPU.  The same inputs go through both entry points;
+the allocation-free one is called twice in a row, so the second call runs on
+the scratch the first one left behind; every output must be bit-identical to
+the workspace form's.  The file is collected last so that a run stopping at
+the first failure has already run every other test."""
 import pytest
 
 import residual_add_rmsnorm_gb300 as rarn
