@@ -271,12 +271,16 @@ rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows parti
  * tile before anything is written; "Tokenweave fused-RMSNorm-AR kernel",
  * Code walkthrough: the norm steps.)
  *
- * Two kernels on `stream`: the tcgen05 GEMM whose epilogue writes h and, per
- * row and column tile, the partial sum of squares of h into `workspace`; then
- * a norm kernel that sums each row's partials in tile order and writes y.
- * `workspace` is caller-owned device memory of at least
- * rarn_gemm_workspace_bytes(T, H) bytes (4-byte aligned); its contents are
- * scratch and need no initialisation.
+ * Kernels on `stream`: the tcgen05 GEMM whose epilogue writes h and, per row
+ * and column tile, the partial sum of squares of h into `workspace`.  With
+ * K >= 512 (the persistent kernels) the same epilogue then waits for the
+ * other column tiles of its 128-row block (a counter per block in the
+ * workspace, zeroed by a one-CTA kernel launched just before), sums each
+ * row's partials in tile order and writes y; otherwise a norm kernel does
+ * that last step.  Both orders give identical bits.  `workspace` is
+ * caller-owned device memory of at least rarn_gemm_workspace_bytes(T, H)
+ * bytes (4-byte aligned); its contents are scratch and need no
+ * initialisation.
  *
  * Matrices are rarn_rows (row-major, row_stride in elements), all of one
  * 16-bit type (RARN_BF16 or RARN_F16; RARN_F32 returns UNSUPPORTED); gamma is
@@ -331,9 +335,10 @@ rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w
                                            rarn_rows residual, const void *gamma, int64_t T,
                                            int64_t H, int64_t K, float eps, void *stream);
 
-/* Workspace bytes rarn_gemm_add_rms_norm needs for T rows of H: 4 T times the
- * number of column tiles (H / 256, or H / 512 beyond 8192; -1 if H is not
- * supported). */
+/* Workspace bytes rarn_gemm_add_rms_norm needs for T rows of H: one binary32
+ * per row and column tile (H / 256 tiles, or H / 512 beyond 8192), rounded up
+ * to 16 bytes, then one 32-bit counter per 128-row block; -1 if H is not
+ * supported. */
 int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H);
 
 /* Describe the GEMM kernels' tiling for a problem (pure host logic). */

@@ -83,6 +83,16 @@ struct Params {
     unsigned long long wait_limit_ns;
     long long stall_fill;  // test hook: in CTA 0 this ring fill (0-based, in issue order)
                            // expects 16 bytes more than it brings, so it never completes
+    // The norm in the persistent kernels' epilogue: a tile publishes its rows'
+    // partial sums by adding 1 to its 128-row block's counter; once the
+    // counter reaches C every tile of the block scales the h it still holds
+    // by inv and gamma and writes y.  counters == nullptr: the norm kernel
+    // writes y instead.
+    unsigned int *counters;  // [ceil(T / 128)], zero when the kernel starts
+    void *y;
+    int64_t ldy;
+    const void *gamma;
+    float eps;
 };
 
 // Kernel 2 arguments.
@@ -131,6 +141,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// The same with acquire semantics at cluster scope: for a barrier that
+// threads of the peer CTA arrive on (release at cluster scope).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 __device__ __forceinline__ unsigned long long now_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -140,13 +166,18 @@ __device__ __forceinline__ unsigned long long now_ns() {
 // Bounded wait on a phase of `bar`.  Gives up when the CTA's abort word is
 // set (unless `ignore_abort`) or after `limit_ns`: then sets the abort word
 // and the watchdog bit and returns false.
+// kCluster: acquire at cluster scope (arrivals from the peer CTA).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                            unsigned int *watchdog, unsigned long long limit_ns,
                                            bool ignore_abort = false) {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto try_wait = [&] {
+        return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
+    if (try_wait()) return true;
     unsigned long long t0 = 0;
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (try_wait()) return true;
         if ((i & 127u) == 0) {
             if (!ignore_abort && *abort_flag) return false;
             const unsigned long long t = now_ns();
@@ -161,6 +192,35 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
     }
 }
 
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Bounded wait until *cnt >= target (other CTAs' tiles published); gives up
+// like wait_phase.
+__device__ __forceinline__ bool wait_count(const unsigned int *cnt, unsigned int target,
+                                           volatile int *abort_flag, unsigned int *watchdog,
+                                           unsigned long long limit_ns) {
+    unsigned long long t0 = 0;
+    for (uint32_t i = 0;; ++i) {
+        if (ld_acquire_u32(cnt) >= target) return true;
+        if ((i & 15u) == 15u) {
+            if (*abort_flag) return false;
+            const unsigned long long t = now_ns();
+            if (t0 == 0) {
+                t0 = t;
+            } else if (t - t0 > limit_ns) {
+                *abort_flag = 1;
+                atomicOr(watchdog, kWatchGemm);
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+}
+
 // 2-D TMA tile load into shared memory, completion on `bar` (byte count).
 // c0 is the innermost (K) coordinate: a multiple of BK, so c0 * 2 bytes is a
 // multiple of 16.
@@ -170,6 +230,46 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+        : "memory");
+}
+
+// 32-byte global accesses (one full sector per thread): a thread of the
+// persistent kernels' epilogue owns one row, so its accesses are the only
+// ones to that row's sectors in a warp-wide instruction.
+struct Pack32 {
+    uint4 a, b;
+};
+
+__device__ __forceinline__ Pack32 ld_stream32(const void *p) {
+    Pack32 v;
+    asm volatile("ld.global.cs.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(v.a.x), "=r"(v.a.y), "=r"(v.a.z), "=r"(v.a.w), "=r"(v.b.x), "=r"(v.b.y),
+                   "=r"(v.b.z), "=r"(v.b.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_global32(void *p, const uint4 &a, const uint4 &b) {
+    asm volatile("st.global.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(a.x), "r"(a.y),
+                 "r"(a.z), "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+                 : "memory");
+}
+
+// L2 policy that keeps lines resident in preference to others (the GEMM's
+// operands, re-read by every tile of a row or column of tiles).
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_2d with an L2 cache policy.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap *map, int c0,
+                                                 int c1, uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(pol)
         : "memory");
 }
 
@@ -292,6 +392,89 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+
+// One thread's share of a persistent kernel's epilogue for one tile: the
+// NC accumulator columns at TMEM address `taddr` plus the residual row
+// segment `rv` (prefetched), rounded once to h, stored back over the
+// residual at `res`; returns the sum of squares of h in column order.
+// Wide: 32-byte accesses (residual rows 32-byte aligned), else 16-byte.
+template <typename T, int NC, bool Wide>
+struct EpiRow {
+    static constexpr int kPacks = Wide ? NC / 16 : NC / 8;
+    using Pk = typename std::conditional<Wide, Pack32, uint4>::type;
+    Pk rv[kPacks];
+
+    __device__ __forceinline__ void load(const T *res) {
+#pragma unroll
+        for (int q = 0; q < kPacks; ++q) {
+            if constexpr (Wide)
+                rv[q] = ld_stream32(res + 16 * q);
+            else
+                rv[q] = ld_stream(res + 8 * q);
+        }
+    }
+
+    __device__ __forceinline__ float run(uint32_t taddr, T *res, bool live) {
+        float ss = 0.f;
+#pragma unroll
+        for (int c = 0; c < NC; c += 32) {
+            float v[32];
+            tmem_ld32(taddr + c, v);
+            if (live) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {  // 8 columns each, in column order
+                    uint4 r;
+                    if constexpr (Wide)
+                        r = (q & 1) ? rv[c / 16 + q / 2].b : rv[c / 16 + q / 2].a;
+                    else
+                        r = rv[c / 8 + q];
+                    float f[8];
+                    DT<T>::unpack(r, f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        f[e] = DT<T>::round(v[8 * q + e] + f[e]);  // h: one rounding
+                        ss += f[e] * f[e];
+                    }
+                    if constexpr (Wide) {
+                        if (q & 1)
+                            rv[c / 16 + q / 2].b = DT<T>::pack(f);
+                        else
+                            rv[c / 16 + q / 2].a = DT<T>::pack(f);
+                    } else {
+                        rv[c / 8 + q] = DT<T>::pack(f);
+                        st_global(res + c + 8 * q, rv[c / 8 + q]);
+                    }
+                }
+                if constexpr (Wide) {
+                    st_global32(res + c, rv[c / 16].a, rv[c / 16].b);
+                    st_global32(res + c + 16, rv[c / 16 + 1].a, rv[c / 16 + 1].b);
+                }
+            }
+        }
+        return ss;
+    }
+
+    // After run(): y = RN((h * inv) * gamma) for the same columns.
+    __device__ __forceinline__ static uint4 scale(const uint4 &h, float inv, const T *g) {
+        float f[8], w[8];
+        DT<T>::unpack(h, f);
+        DT<T>::unpack(ld_keep(g), w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = (f[e] * inv) * w[e];
+        return DT<T>::pack(f);
+    }
+
+    __device__ __forceinline__ void store_y(float inv, const T *g, T *y) const {
+#pragma unroll
+        for (int q = 0; q < kPacks; ++q) {
+            if constexpr (Wide)
+                st_global32(y + 16 * q, scale(rv[q].a, inv, g + 16 * q),
+                            scale(rv[q].b, inv, g + 16 * q + 8));
+            else
+                st_global(y + 8 * q, scale(rv[q], inv, g + 8 * q));
+        }
+    }
+};
 
 // ---------------------------------------------------------------------------
 // Kernel 1.  Grid: C x ceil(T / 128) CTAs (C = H / NS column tiles); CTA b
@@ -504,7 +687,7 @@ struct WsLayout {
         ctl_off + (2 * stages + 5) * 8 + 8 + kWsEpiWarps * 32 * 4 + 16 + 1024;
 };
 
-template <typename T, int NT, int BK>
+template <typename T, int NT, int BK, bool Wide>
 __global__ void __launch_bounds__(kWsThreads, 1)
     k_gemm_res_ws(const __grid_constant__ CUtensorMap map_a,
                   const __grid_constant__ CUtensorMap map_w, void *residual, int64_t ldr,
@@ -525,6 +708,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     float *half_ss = reinterpret_cast<float *>(tmem_slot + 2);  // [8 warps][32]
     volatile int *tile_ok = reinterpret_cast<volatile int *>(half_ss + kWsEpiWarps * 32);
+    volatile int *norm_ok = tile_ok + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int C = p.C;
@@ -563,23 +747,33 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ---- TMA producer ----
+            // ring position kept incrementally (stage s, round parity ph): the
+            // issuing threads' instruction latency is on the critical path
             bool stop = false;
+            uint32_t s = 0, ph = 0;
+            const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty), ring0 = smem_u32(smem);
+            // the operands stay in L2 ahead of the residual and h streams
+            const uint64_t pol = l2_evict_last_policy();
             for (int64_t tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x) {
                 const int m0 = (int)((tile / C) * kBM);
                 const int n0 = (int)((tile % C) * NS);
                 for (int kb = 0; kb < KB; ++kb, ++kit) {
-                    const int s = (int)(kit % S);
-                    if (kit >= S && !wait_phase(smem_u32(&empty[s]), (uint32_t)((kit / S - 1) & 1),
-                                                abort_flag, p.watchdog, p.wait_limit_ns)) {
+                    // fill kit of round r waits for the release of round r - 1
+                    if (kit >= S && !wait_phase(empty0 + 8 * s, ph ^ 1u, abort_flag, p.watchdog,
+                                                p.wait_limit_ns)) {
                         stop = true;
                         break;
                     }
-                    const uint32_t fb = smem_u32(&full[s]);
+                    const uint32_t fb = full0 + 8 * s;
                     mbar_arrive_expect_tx(
                         fb, WsLayout::stage_bytes + (blockIdx.x == 0 && kit == p.stall_fill ? 16u : 0u));
-                    const uint32_t sa = smem_u32(smem + s * WsLayout::stage_bytes);
-                    tma_load_2d(sa, &map_a, kb * BK, m0, fb);
-                    tma_load_2d(sa + WsLayout::a_bytes, &map_w, kb * BK, n0, fb);
+                    const uint32_t sa = ring0 + s * WsLayout::stage_bytes;
+                    tma_load_2d_hint(sa, &map_a, kb * BK, m0, fb, pol);
+                    tma_load_2d_hint(sa + WsLayout::a_bytes, &map_w, kb * BK, n0, fb, pol);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
         }
@@ -588,7 +782,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         if (lane == 0) {
             // ---- MMA issuer ----
             const uint32_t idesc = instr_desc<T, NT>();
-            int64_t kit = 0;
+            // descriptors of stage 0, advanced by adds (start address in
+            // 16-byte units: a stage is stage_bytes / 16, a K step 2)
+            const uint64_t adesc0 = smem_desc(smem_u32(smem), BK * 2);
+            const uint64_t bdesc0 = smem_desc(smem_u32(smem) + WsLayout::a_bytes, BK * 2);
+            constexpr uint32_t kStageDesc = WsLayout::stage_bytes >> 4;
+            const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
+            uint32_t s = 0, ph = 0;
             int it = 0;
             bool stop = false;
             for (int64_t tile = blockIdx.x; tile < ntiles && !stop; tile += gridDim.x, ++it) {
@@ -598,21 +798,22 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     break;
                 tmem_fence_after();
                 const uint32_t d = tmem + acc * NS;
-                for (int kb = 0; kb < KB; ++kb, ++kit) {
-                    const int s = (int)(kit % S);
-                    if (!wait_phase(smem_u32(&full[s]), (uint32_t)((kit / S) & 1), abort_flag,
-                                    p.watchdog, p.wait_limit_ns)) {
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase(full0 + 8 * s, ph, abort_flag, p.watchdog, p.wait_limit_ns)) {
                         stop = true;
                         break;
                     }
                     tmem_fence_after();
-                    const uint32_t sa = smem_u32(smem + s * WsLayout::stage_bytes);
-                    const uint32_t sb = sa + WsLayout::a_bytes;
+                    const uint64_t ad = adesc0 + s * kStageDesc, bd = bdesc0 + s * kStageDesc;
+                    mma_f16(d, ad, bd, idesc, kb != 0);
 #pragma unroll
-                    for (int kk = 0; kk < BK / kMmaK; ++kk)
-                        mma_f16(d, smem_desc(sa + kk * kMmaK * 2, BK * 2),
-                                smem_desc(sb + kk * kMmaK * 2, BK * 2), idesc, (kb | kk) != 0);
-                    mma_commit(smem_u32(&empty[s]));
+                    for (int kk = 1; kk < BK / kMmaK; ++kk)
+                        mma_f16(d, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
+                    mma_commit(empty0 + 8 * s);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
                 if (!stop) mma_commit(smem_u32(&tfull[acc]));
             }
@@ -629,6 +830,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         int it = 0;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
             const int acc = it & 1;
+            const int64_t m0 = (tile / C) * kBM;
+            const int ntile = (int)(tile % C);
+            const int64_t t = m0 + row;
+            const bool live = t < p.T;
+            T *res = reinterpret_cast<T *>(residual) + (live ? t : 0) * ldr + ntile * NS + c0;
+            // this thread's residual columns are loaded before the wait for
+            // the accumulator, so they arrive while the tile's MMAs run
+            EpiRow<T, NS / 2, Wide> er;
+            if (live) er.load(res);
             // one thread waits (bounded) and the 8 warps leave together, so
             // none is left at the epilogue barrier
             if (warp == 2 && lane == 0)
@@ -640,42 +850,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (!*tile_ok) break;
             tmem_fence_after();
             if (tile + gridDim.x >= ntiles) grid_launch_dependents();
-            const int64_t m0 = (tile / C) * kBM;
-            const int ntile = (int)(tile % C);
-            const int64_t t = m0 + row;
-            const bool live = t < p.T;
-            T *res = reinterpret_cast<T *>(residual) + (live ? t : 0) * ldr + ntile * NS + c0;
             const uint32_t taddr =
                 tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * NS + c0;
-            uint4 cur[4], nxt[4];
-            if (live) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) cur[q] = ld_stream(res + 8 * q);
-            }
-            float ss = 0.f;
-            for (int c = 0; c < NS / 2; c += 32) {
-                if (live && c + 32 < NS / 2) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) nxt[q] = ld_stream(res + c + 32 + 8 * q);
-                }
-                float v[32];
-                tmem_ld32(taddr + c, v);
-                if (live) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float f[8];
-                        DT<T>::unpack(cur[q], f);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            f[e] = DT<T>::round(v[8 * q + e] + f[e]);  // h: one rounding
-                            ss += f[e] * f[e];
-                        }
-                        st_global(res + c + 8 * q, DT<T>::pack(f));
-                    }
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) cur[q] = nxt[q];
-                }
-            }
+            const float ss = er.run(taddr, res, live);
             tmem_fence_before();
             mbar_arrive(smem_u32(&tempty[acc]));  // the accumulator is free again
             // the two column halves' sums meet in shared memory, added in
@@ -685,6 +862,30 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (c0 == 0 && live && !*abort_flag)
                 p.ss[t * C + ntile] = ss + half_ss[(warp + 2) * 32 + lane];
             epi_barrier_ws();
+            if (p.counters) {
+                // publish this tile's partials, then wait (bounded) for the
+                // other column tiles of the 128-row block
+                unsigned int *cnt = p.counters + (m0 / kBM);
+                if (warp == 2 && lane == 0) {
+                    __threadfence();
+                    atomicAdd(cnt, 1u);
+                    *norm_ok = wait_count(cnt, (unsigned int)C, abort_flag, p.watchdog,
+                                          p.wait_limit_ns)
+                                   ? 1
+                                   : 0;
+                }
+                epi_barrier_ws();
+                if (!*norm_ok) break;
+                if (live) {
+                    // the row's partials in tile order (read past L1: other SMs wrote them)
+                    const float *sr = p.ss + t * C;
+                    float tot = 0.f;
+                    for (int q = 0; q < C; ++q) tot += __ldcg(sr + q);
+                    const float inv = rsqrtf(tot / (float)p.H + p.eps);
+                    er.store_y(inv, reinterpret_cast<const T *>(p.gamma) + ntile * NS + c0,
+                               reinterpret_cast<T *>(p.y) + t * p.ldy + ntile * NS + c0);
+                }
+            }
         }
     }
     tmem_fence_before();
@@ -704,52 +905,415 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     }
 }
 
-// Kernel 2: y from the stored h and the tiles' partial sums.  A CTA per row
-// (grid-stride), VPT 16-byte packs per thread.
-template <typename T, int VPT>
-__global__ void __launch_bounds__(256) k_norm_ss(NormParams p) {
-    __shared__ float inv_s;
-    constexpr int EPV = DT<T>::EPV;
-    const int nv = (int)(p.H / EPV);
-    grid_dependency_wait();  // kernel 1's stores are visible
-    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x) {
-        if (t + gridDim.x >= p.T) grid_launch_dependents();
-        uint4 hv[VPT], gv[VPT];
-        const T *h = reinterpret_cast<const T *>(p.h) + t * p.ldh;
-        const T *g = reinterpret_cast<const T *>(p.gamma);
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int j = threadIdx.x + k * blockDim.x;
-            if (j < nv) {
-                hv[k] = ld_stream(h + (int64_t)j * EPV);
-                gv[k] = ld_keep(g + (int64_t)j * EPV);
+// ---------------------------------------------------------------------------
+// Kernel 1, persistent, two SMs per tile (a cluster of two CTAs, tcgen05
+// cta_group::2).  The pair computes a [256 x 256] tile of P with M = 256,
+// N = 256 MMAs issued by the even CTA (the leader): each CTA stages its own
+// 128 rows of A and its own 128 of the tile's 256 columns of W, and the
+// matrix unit of each SM reads the A rows of its own CTA and both CTAs'
+// halves of W, accumulating its 128 rows x 256 columns in its own tensor
+// memory.  Per SM that halves the W bytes written into and read out of
+// shared memory (and fetched from L2) against the one-SM kernel above, where
+// a 128 x 256 x 64 slab moves 48 KB through shared memory per 128 x 256 x 64
+// of work; here it is 32 KB.
+//
+// Signalling: both CTAs' TMA fills complete on the leader's full barrier
+// (cta_group::2 copies may signal the peer's barrier); the leader arms it
+// with both halves' bytes.  The leader's MMA commits arrive on the empty
+// barrier of both CTAs (multicast), and on both CTAs' accumulator-full
+// barrier; every epilogue thread of both CTAs arrives on the leader's
+// accumulator-empty barrier.  The epilogue is the one-SM persistent
+// kernel's, on the CTA's own 128 rows.
+// ---------------------------------------------------------------------------
+constexpr int kPairBM = 2 * kBM;  // rows of a pair tile
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Shared::cluster address of the variable at shared::cta address `a` in the
+// cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t a, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+
+// Every thread of both CTAs (release / acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                     cluster_addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t cluster_addr) {
+    uint32_t v;
+    asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+
+// 2-D TMA tile load into this CTA's shared memory whose completion is
+// signalled on `bar`, a shared::cluster address in either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int c0,
+                                                 int c1, uint32_t bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".cta_group::2.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar), "l"(pol)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_f16_pair(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive on the barrier at shared::cta offset `bar` in every CTA of `mask`
+// once all pair MMAs this thread issued so far complete.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar),
+        "h"(mask)
+        : "memory");
+}
+
+// Instruction descriptor of the pair MMA: as instr_desc, M = 256.
+template <typename T>
+__host__ __device__ constexpr uint32_t instr_desc_pair() {
+    constexpr uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(kMmaN >> 3) << 17) |
+           ((uint32_t)(kPairBM >> 4) << 24);
+}
+
+template <int BK = 64>
+struct PairLayout {
+    static constexpr int a_bytes = kBM * BK * 2;           // 16 KB: this CTA's 128 rows of A
+    static constexpr int b_bytes = (kMmaN / 2) * BK * 2;   // 16 KB: its 128 columns of W
+    static constexpr int stage_bytes = a_bytes + b_bytes;  // 32 KB
+    static constexpr int stages =
+        (227 * 1024 - 3 * 1024) / stage_bytes > 8 ? 8 : (227 * 1024 - 3 * 1024) / stage_bytes;
+    static constexpr int ctl_off = stages * stage_bytes;
+    // full[S], empty[S], tfull[2], tempty[2], mma_done (8 B each); tmem slot,
+    // abort word, the peer's fill count, tile_ok, norm_ok; the epilogue's
+    // half-row sums
+    static constexpr int words_off = ctl_off + (2 * stages + 5) * 8;
+    static constexpr int half_off = words_off + 32;
+    static constexpr int total = half_off + kWsEpiWarps * 32 * 4 + 1024;
+    static_assert(total <= 227 * 1024, "one CTA per SM");
+};
+
+template <typename T, int BK, bool Wide>
+__global__ void __launch_bounds__(kWsThreads, 1)
+    k_gemm_res_pair(const __grid_constant__ CUtensorMap map_a,
+                    const __grid_constant__ CUtensorMap map_w, void *residual, int64_t ldr,
+                    Params p) {
+    static_assert(BK == 64, "K slab of 128 bytes");
+    using Lay = PairLayout<BK>;
+    constexpr int S = Lay::stages;
+    constexpr int NS = kMmaN;  // columns of a tile
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Lay::ctl_off);
+    uint64_t *empty = full + S;
+    uint64_t *tfull = empty + S;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *mma_done = tempty + 2;
+    uint32_t *words = reinterpret_cast<uint32_t *>(smem + Lay::words_off);
+    uint32_t *tmem_slot = words;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(words + 1);
+    volatile uint32_t *peer_kit = words + 2;  // leader: fills the peer issued (set at the end)
+    volatile int *tile_ok = reinterpret_cast<volatile int *>(words + 3);
+    volatile int *norm_ok = reinterpret_cast<volatile int *>(words + 4);
+    float *half_ss = reinterpret_cast<float *>(smem + Lay::half_off);  // [8 warps][32]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();  // 0: leader (issues the MMAs)
+    const int C = p.C;
+    const int64_t mtiles = (p.T + kPairBM - 1) / kPairBM;
+    const int64_t ntiles = mtiles * C;
+    const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+    const int KB = p.kblocks;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);   // the leader's producer arms it
+            mbar_init(smem_u32(&empty[s]), 1);  // the leader's MMA commit
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull[a]), 1);
+            mbar_init(smem_u32(&tempty[a]), 2 * 32 * kWsEpiWarps);  // both CTAs' epilogues
+        }
+        mbar_init(smem_u32(mma_done), 1);
+        *abort_flag = 0;
+        *peer_kit = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {  // one warp of each CTA allocates, together, the same columns in both
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(512)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tmem_fence_before();
+    cluster_sync();  // barriers initialised and tensor memory allocated in both CTAs
+    tmem_fence_after();
+    // a pair allocation takes the same columns in both CTAs: both use the
+    // address the leader's allocation reported
+    const uint32_t tmem = ld_cluster_u32(map_to_rank(smem_u32(tmem_slot), 0));
+    grid_dependency_wait();  // A, W and the residual may come from the previous kernel
+
+    int64_t kit = 0;  // producer: k-slabs issued so far (all tiles)
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---- TMA producer (both CTAs) ----
+            bool stop = false;
+            uint32_t s = 0, ph = 0;
+            const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty), ring0 = smem_u32(smem);
+            const uint32_t lead_full0 = map_to_rank(full0, 0);
+            const uint64_t pol = l2_evict_last_policy();
+            for (int64_t tile = pair; tile < ntiles && !stop; tile += npairs) {
+                const int m0 = (int)((tile / C) * kPairBM + rank * kBM);
+                const int n0 = (int)((tile % C) * NS + rank * (NS / 2));
+                for (int kb = 0; kb < KB; ++kb, ++kit) {
+                    if (kit >= S && !wait_phase(empty0 + 8 * s, ph ^ 1u, abort_flag, p.watchdog,
+                                                p.wait_limit_ns)) {
+                        stop = true;
+                        break;
+                    }
+                    if (rank == 0)
+                        mbar_arrive_expect_tx(
+                            full0 + 8 * s, 2 * Lay::stage_bytes +
+                                               (blockIdx.x == 0 && kit == p.stall_fill ? 16u : 0u));
+                    const uint32_t lead_fb = lead_full0 + 8 * s;
+                    const uint32_t sa = ring0 + s * Lay::stage_bytes;
+                    tma_load_2d_pair(sa, &map_a, kb * BK, m0, lead_fb, pol);
+                    tma_load_2d_pair(sa + Lay::a_bytes, &map_w, kb * BK, n0, lead_fb, pol);
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
             }
         }
-        if (threadIdx.x < 32) {
-            // lane q loads tile q's partial (all in flight at once); lane 0
-            // adds them in tile order (C <= 32)
-            const int lane = threadIdx.x;
-            const float part = lane < p.C ? p.ss[t * p.C + lane] : 0.f;
-            float tot = 0.f;
-            for (int q = 0; q < p.C; ++q) tot += __shfl_sync(0xffffffffu, part, q);
-            if (lane == 0) inv_s = rsqrtf(tot / (float)p.H + p.eps);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ---- MMA issuer (leader only) ----
+            const uint32_t idesc = instr_desc_pair<T>();
+            const uint64_t adesc0 = smem_desc(smem_u32(smem), BK * 2);
+            const uint64_t bdesc0 = smem_desc(smem_u32(smem) + Lay::a_bytes, BK * 2);
+            constexpr uint32_t kStageDesc = Lay::stage_bytes >> 4;
+            const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty);
+            uint32_t s = 0, ph = 0;
+            int it = 0;
+            bool stop = false;
+            for (int64_t tile = pair; tile < ntiles && !stop; tile += npairs, ++it) {
+                const int acc = it & 1;
+                if (it >= 2 &&
+                    !wait_phase<true>(smem_u32(&tempty[acc]), (uint32_t)(((it >> 1) - 1) & 1),
+                                      abort_flag, p.watchdog, p.wait_limit_ns))
+                    break;
+                tmem_fence_after();
+                const uint32_t d = tmem + acc * NS;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_phase(full0 + 8 * s, ph, abort_flag, p.watchdog, p.wait_limit_ns)) {
+                        stop = true;
+                        break;
+                    }
+                    tmem_fence_after();
+                    const uint64_t ad = adesc0 + s * kStageDesc, bd = bdesc0 + s * kStageDesc;
+                    mma_f16_pair(d, ad, bd, idesc, kb != 0);
+#pragma unroll
+                    for (int kk = 1; kk < BK / kMmaK; ++kk)
+                        mma_f16_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
+                    mma_commit_pair(empty0 + 8 * s, 3);  // frees the stage in both CTAs
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+                if (!stop) mma_commit_pair(smem_u32(&tfull[acc]), 3);
+            }
+            // every MMA issued has completed before tensor memory is freed
+            mma_commit_pair(smem_u32(mma_done), 1);
+            wait_phase(smem_u32(mma_done), 0, abort_flag, p.watchdog, p.wait_limit_ns, true);
         }
-        __syncthreads();
-        const float inv = inv_s;
+        __syncwarp();
+    } else {
+        // ---- epilogue: warps 2-9 of both CTAs, each on its CTA's 128 rows ----
+        const int quarter = warp & 3;
+        const int row = quarter * 32 + lane;
+        const int c0 = ((warp - 2) >> 2) * (NS / 2);
+        int it = 0;
+        for (int64_t tile = pair; tile < ntiles; tile += npairs, ++it) {
+            const int acc = it & 1;
+            const int64_t m0 = (tile / C) * kPairBM + rank * kBM;
+            const int ntile = (int)(tile % C);
+            const int64_t t = m0 + row;
+            const bool live = t < p.T;
+            T *res = reinterpret_cast<T *>(residual) + (live ? t : 0) * ldr + ntile * NS + c0;
+            // this thread's residual columns are loaded before the wait for
+            // the accumulator, so they arrive while the tile's MMAs run
+            EpiRow<T, NS / 2, Wide> er;
+            if (live) er.load(res);
+            // one thread waits (bounded) and the 8 warps leave together
+            if (warp == 2 && lane == 0)
+                *tile_ok = wait_phase(smem_u32(&tfull[acc]), (uint32_t)((it >> 1) & 1), abort_flag,
+                                      p.watchdog, p.wait_limit_ns)
+                               ? 1
+                               : 0;
+            epi_barrier_ws();
+            if (!*tile_ok) break;
+            tmem_fence_after();
+            if (tile + npairs >= ntiles) grid_launch_dependents();
+            const uint32_t taddr =
+                tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * NS + c0;
+            const float ss = er.run(taddr, res, live);
+            tmem_fence_before();
+            // this CTA's half of the accumulator is read: tell the leader
+            mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
+            half_ss[(warp - 2) * 32 + lane] = ss;
+            epi_barrier_ws();
+            if (c0 == 0 && live && !*abort_flag)
+                p.ss[t * C + ntile] = ss + half_ss[(warp + 2) * 32 + lane];
+            epi_barrier_ws();
+            if (p.counters) {
+                // publish this tile's partials, then wait (bounded) for the
+                // other column tiles of the 128-row block
+                unsigned int *cnt = p.counters + (m0 / kBM);
+                if (warp == 2 && lane == 0) {
+                    __threadfence();
+                    atomicAdd(cnt, 1u);
+                    *norm_ok = wait_count(cnt, (unsigned int)C, abort_flag, p.watchdog,
+                                          p.wait_limit_ns)
+                                   ? 1
+                                   : 0;
+                }
+                epi_barrier_ws();
+                if (!*norm_ok) break;
+                if (live) {
+                    // the row's partials in tile order (read past L1: other SMs wrote them)
+                    const float *sr = p.ss + t * C;
+                    float tot = 0.f;
+                    for (int q = 0; q < C; ++q) tot += __ldcg(sr + q);
+                    const float inv = rsqrtf(tot / (float)p.H + p.eps);
+                    er.store_y(inv, reinterpret_cast<const T *>(p.gamma) + ntile * NS + c0,
+                               reinterpret_cast<T *>(p.y) + t * p.ldy + ntile * NS + c0);
+                }
+            }
+        }
+    }
+    tmem_fence_before();
+    __syncthreads();
+    // the peer's fill count reaches the leader before the cluster barrier
+    if (warp == 0 && lane == 0 && rank == 1)
+        st_cluster_u32(map_to_rank(smem_u32((const void *)peer_kit), 0), (uint32_t)kit);
+    cluster_sync();
+    // After an abort anywhere in the pair, every fill either CTA issued lands
+    // before shared memory goes away: the leader's full barriers count both
+    // halves, so the leader waits (bounded) on each fill still open, arming
+    // with the peer's bytes any fill its own producer never reached.  Without
+    // an abort every fill was consumed by a completed MMA and nothing waits.
+    if (warp == 0 && lane == 0 && rank == 0) {
+        const int64_t kp = *peer_kit;
+        const int64_t kmax = kit > kp ? kit : kp;
+        for (int64_t k = kmax - S > 0 ? kmax - S : 0; k < kmax; ++k) {
+            const int s = (int)(k % S);
+            if (k >= kit) mbar_arrive_expect_tx(smem_u32(&full[s]), Lay::stage_bytes);
+            wait_phase(smem_u32(&full[s]), (uint32_t)((k / S) & 1), abort_flag, p.watchdog,
+                       p.wait_limit_ns, true);
+        }
+    }
+    tmem_fence_before();
+    cluster_sync();
+    tmem_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
+                     : "memory");
+    }
+}
+
+// Zeroes the row-block counters of the norm in the persistent kernels'
+// epilogue, after the previous kernel on the stream (which may be the previous
+// call's GEMM, still counting) has finished.
+static __global__ void __launch_bounds__(256) k_zero_counters(unsigned int *cnt, int64_t n) {
+    grid_dependency_wait();
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) cnt[i] = 0u;
+    grid_launch_dependents();
+}
+
+// Kernel 2: y from the stored h and the tiles' partial sums.  A warp per
+// (row, slice of up to 32 * VPT 16-byte packs): it loads its slice of h and
+// the row's column-tile partials at once, forms inv from the partials summed
+// in tile order (the same value in every slice of the row) and writes its
+// slice of y.  No barrier: every warp works alone, grid-stride over items.
+constexpr int kNormVPT = 4;
+constexpr int kNormThreads = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(kNormThreads) k_norm_ss(NormParams p) {
+    constexpr int EPV = DT<T>::EPV;
+    constexpr int SLICE = 32 * kNormVPT;  // packs per item
+    const int nv = (int)(p.H / EPV);
+    const int slices = (nv + SLICE - 1) / SLICE;
+    const int64_t items = p.T * slices;
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * kNormThreads) >> 5;
+    const T *g = reinterpret_cast<const T *>(p.gamma);
+    grid_dependency_wait();  // kernel 1's stores are visible
+    for (int64_t item = ((int64_t)blockIdx.x * kNormThreads + threadIdx.x) >> 5; item < items;
+         item += nwarps) {
+        if (item + nwarps >= items) grid_launch_dependents();
+        const int64_t t = item / slices;
+        const int j0 = (int)(item % slices) * SLICE;
+        const T *h = reinterpret_cast<const T *>(p.h) + t * p.ldh;
+        uint4 hv[kNormVPT];
+#pragma unroll
+        for (int k = 0; k < kNormVPT; ++k) {
+            const int j = j0 + lane + 32 * k;
+            if (j < nv) hv[k] = ld_stream(h + (int64_t)j * EPV);
+        }
+        // lane q holds tile q's partial (C <= 32); every lane adds them in
+        // tile order
+        const float part = lane < p.C ? p.ss[t * p.C + lane] : 0.f;
+        float tot = 0.f;
+        for (int q = 0; q < p.C; ++q) tot += __shfl_sync(0xffffffffu, part, q);
+        const float inv = rsqrtf(tot / (float)p.H + p.eps);
         T *y = reinterpret_cast<T *>(p.y) + t * p.ldy;
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int j = threadIdx.x + k * blockDim.x;
+        for (int k = 0; k < kNormVPT; ++k) {
+            const int j = j0 + lane + 32 * k;
             if (j < nv) {
                 float f[EPV], w[EPV];
                 DT<T>::unpack(hv[k], f);
-                DT<T>::unpack(gv[k], w);
+                DT<T>::unpack(ld_keep(g + (int64_t)j * EPV), w);
 #pragma unroll
                 for (int e = 0; e < EPV; ++e) f[e] = (f[e] * inv) * w[e];
                 st_global(y + (int64_t)j * EPV, DT<T>::pack(f));
             }
         }
-        __syncthreads();  // inv_s is rewritten for the next row
     }
 }
 

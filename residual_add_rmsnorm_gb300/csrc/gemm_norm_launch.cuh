@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "gemm_norm.cuh"
@@ -45,6 +46,40 @@ inline bool encode_map(CUtensorMap *map, const void *base, int64_t rows, int64_t
     return r == CUDA_SUCCESS;
 }
 
+// Clusters of two CTAs of the pair kernel that can be resident at once on the
+// current device (SM pairs that share a cluster domain), once per device.
+template <typename T>
+static int pair_clusters(int num_sms) {
+    constexpr int kDevs = 64;
+    static std::atomic<int> cache[kDevs];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return num_sms / 2;
+    int n = cache[dev].load();
+    if (n > 0) return n;
+    auto kernel = gemm::k_gemm_res_pair<T, 64, false>;
+    constexpr int smem = gemm::PairLayout<64>::total;
+    n = num_sms / 2;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+        cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(num_sms & ~1));
+        cfg.blockDim = dim3(gemm::kWsThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int q = 0;
+        if (cudaOccupancyMaxActiveClusters(&q, kernel, &cfg) == cudaSuccess && q > 0) n = q;
+    }
+    (void)cudaGetLastError();
+    cache[dev].store(n);
+    return n;
+}
+
 template <typename T, int BK>
 static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     using namespace gemm;
@@ -71,12 +106,50 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     p.wait_limit_ns = c.wait_limit_ns;
     p.stall_fill = c.stall_fill;
     const int64_t mblocks = (c.T + kBM - 1) / kBM;
+    // y in the persistent kernels' epilogue: the row-block counters follow the
+    // partial sums in the workspace and start each call at zero
+    // (walkers: CTAs, or pairs, of the persistent grid; a tile waits only on
+    // later tiles of its row block, which at least tiles_n walkers reach first)
+    const int64_t walkers =
+        c.pair ? std::min<int64_t>(((c.T + kPairBM - 1) / kPairBM) * p.C, pair_clusters<T>(c.num_sms))
+               : std::min<int64_t>(mblocks * p.C, c.num_sms);
+    const bool fused = c.fuse_norm && c.persistent && BK == 64 && c.ns == 256 && walkers >= p.C;
+    p.counters = nullptr;
+    if (fused) {
+        p.counters = reinterpret_cast<unsigned int *>(c.workspace +
+                                                      gemm_counters_offset(c.T, p.C));
+        p.y = c.y;
+        p.ldy = c.ldy;
+        p.gamma = c.gamma;
+        p.eps = c.eps;
+        const cudaError_t ez = launch_kernel(k_zero_counters, dim3(1), dim3(256), 0, st, c.pdl, 1,
+                                             p.counters, mblocks);
+        if (ez != cudaSuccess) return ez;
+    }
     cudaError_t e = cudaErrorInvalidValue;
     bool launched = false;
-    if constexpr (BK == 64) {  // the persistent kernel takes 128-byte K slabs only
-        if (c.persistent && c.ns == 256) {
+    // the persistent kernels' epilogue moves whole 32-byte sectors when every
+    // residual row starts on one
+    const bool wide = (reinterpret_cast<uintptr_t>(c.residual) & 31u) == 0 && c.ldr % 16 == 0 &&
+                      (reinterpret_cast<uintptr_t>(c.y) & 31u) == 0 && c.ldy % 16 == 0;
+    if constexpr (BK == 64) {  // the persistent kernels take 128-byte K slabs only
+        if (c.persistent && c.ns == 256 && c.pair) {
+            CUtensorMap mw2;  // each CTA of a pair stages 128 of the tile's 256 W rows
+            if (!encode_map(&mw2, c.w, c.H, c.K, c.ldw, kMmaN / 2, BK, bf16))
+                return cudaErrorInvalidValue;
+            const int64_t ptiles = ((c.T + kPairBM - 1) / kPairBM) * p.C;
+            const int64_t grid = 2 * std::min<int64_t>(ptiles, pair_clusters<T>(c.num_sms));
+            auto kernel = wide ? k_gemm_res_pair<T, BK, true> : k_gemm_res_pair<T, BK, false>;
+            constexpr int smem = PairLayout<BK>::total;
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e == cudaSuccess)
+                e = launch_kernel(kernel, dim3(static_cast<unsigned>(grid)), dim3(kWsThreads),
+                                  static_cast<size_t>(smem), st, c.pdl, 2, ma, mw2, c.residual,
+                                  c.ldr, p);
+            launched = true;
+        } else if (c.persistent && c.ns == 256) {
             const int64_t grid = std::min<int64_t>(mblocks * p.C, c.num_sms);
-            auto kernel = k_gemm_res_ws<T, 256, BK>;
+            auto kernel = wide ? k_gemm_res_ws<T, 256, BK, true> : k_gemm_res_ws<T, 256, BK, false>;
             constexpr int smem = WsLayout<256, BK>::total;
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e == cudaSuccess)
@@ -95,6 +168,7 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
                               static_cast<size_t>(smem), st, c.pdl, 1, ma, mw, mr, p);
     }
     if (e != cudaSuccess) return e;
+    if (fused) return cudaSuccess;
 
     NormParams q{};
     q.y = c.y;
@@ -107,16 +181,12 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     q.ldy = c.ldy;
     q.C = p.C;
     q.eps = c.eps;
-    const int nv = static_cast<int>(c.H / DT<T>::EPV);
-    const int vpt = nv <= 256 ? 1 : nv <= 512 ? 2 : nv <= 1024 ? 4 : 8;
-    const dim3 g2(static_cast<unsigned>(std::min<int64_t>(c.T, (int64_t)c.num_sms * 8)));
-    const dim3 b2(static_cast<unsigned>(((nv + vpt - 1) / vpt + 31) / 32 * 32));
-    switch (vpt) {
-    case 1: return launch_kernel(k_norm_ss<T, 1>, g2, b2, 0, st, c.pdl, 1, q);
-    case 2: return launch_kernel(k_norm_ss<T, 2>, g2, b2, 0, st, c.pdl, 1, q);
-    case 4: return launch_kernel(k_norm_ss<T, 4>, g2, b2, 0, st, c.pdl, 1, q);
-    default: return launch_kernel(k_norm_ss<T, 8>, g2, b2, 0, st, c.pdl, 1, q);
-    }
+    const int64_t slices = (c.H / DT<T>::EPV + 32 * kNormVPT - 1) / (32 * kNormVPT);
+    const int64_t warps = c.T * slices;
+    const int64_t ctas = std::min<int64_t>((warps + kNormThreads / 32 - 1) / (kNormThreads / 32),
+                                           (int64_t)c.num_sms * 8);
+    return launch_kernel(k_norm_ss<T>, dim3(static_cast<unsigned>(ctas)), dim3(kNormThreads), 0, st,
+                         c.pdl, 1, q);
 }
 
 template <typename T>

@@ -23,9 +23,11 @@ struct GemmCall {
     int64_t T, H, K;
     float eps;
     int ns, stages, bk;  // columns per CTA, ring stages, K slab (elements)
-    float *workspace;    // [T][H / ns] partial sums of squares
+    float *workspace;    // [T][H / ns] partial sums of squares, then the row-block counters
     int num_sms;
     bool persistent;     // the warp-specialised persistent kernel (256-column tiles)
+    bool pair;           // ... on SM pairs: 256 x 256 tiles, cta_group::2 MMAs
+    bool fuse_norm;      // the persistent kernel writes y (no norm kernel)
     bool pdl;
     unsigned int *watchdog;
     unsigned long long wait_limit_ns;  // bound on every shared-memory barrier wait
@@ -42,6 +44,8 @@ struct GemmPlan {
     int ns = 0, tiles_n = 0, bk = 0, stages = 0, smem = 0;
     int64_t grid = 0;
     bool persistent = false;
+    bool pair = false;
+    bool fuse_norm = false;
 };
 
 constexpr int kGemmMaxTilesN = 32;
@@ -52,7 +56,7 @@ constexpr int kGemmMaxTilesN = 32;
 // wider than 32 tiles of 256 use 512-column tiles.
 inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
                           int ns_override = 0, int ctas_override = 0, int persist_override = -1,
-                          int num_sms = 152) {
+                          int num_sms = 152, int pair_override = -1, int fuse_override = -1) {
     GemmPlan g;
     const bool fit256 = H % 256 == 0 && H / 256 <= kGemmMaxTilesN;
     const bool fit512 = H % 512 == 0 && H / 512 <= kGemmMaxTilesN;
@@ -92,15 +96,37 @@ inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
         g.stages = std::min(9, (227 * 1024 - 3 * 1024) / stage);
         g.smem = g.stages * stage + 3 * 1024;
         g.grid = std::min<int64_t>(g.grid, num_sms);
+        // SM pairs (256-row tiles, each CTA staging half of the W slab) once
+        // there is more than one 128-row block
+        g.pair = pair_override == 1 || (pair_override != 0 && T > 128);
+        if (g.pair) {
+            const int half = (128 + g.ns / 2) * g.bk * 2;
+            g.stages = std::min(8, (227 * 1024 - 3 * 1024) / half);
+            g.smem = g.stages * half + 3 * 1024;
+            g.grid = 2 * std::min<int64_t>(((T + 255) / 256) * g.tiles_n, num_sms / 2);
+        }
+        // y in the epilogue: a tile waits for the other column tiles of its
+        // row block, which tiles walked in row-major order by at least
+        // tiles_n CTAs (or pairs) always reach without waiting on it
+        g.fuse_norm = fuse_override != 0 && g.grid / (g.pair ? 2 : 1) >= g.tiles_n;
     }
     return g;
 }
 
 // Workspace of the GEMM form: one binary32 per row and column tile (the
-// column tiling depends on H only; -1: H not supported).
+// column tiling depends on H only), then, 16-byte aligned, one 32-bit counter
+// per 128-row block (-1: H not supported).
+inline int64_t gemm_counters_offset(int64_t T, int tiles_n) {  // in floats
+    return (T * tiles_n + 3) / 4 * 4;
+}
+
+inline int64_t gemm_workspace_bytes_for(int64_t T, int tiles_n) {
+    return (gemm_counters_offset(T, tiles_n) + (T + 127) / 128) * 4;
+}
+
 inline int64_t gemm_workspace_bytes(int64_t T, int64_t H) {
     const GemmPlan g = plan_gemm(T, H, 0);
-    return g.ns == 0 ? -1 : T * g.tiles_n * 4;
+    return g.ns == 0 ? -1 : gemm_workspace_bytes_for(T, g.tiles_n);
 }
 
 }  // namespace rarn

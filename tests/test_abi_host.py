@@ -333,7 +333,7 @@ def test_gemm_form_argument_errors(lib):
     assert call(y, a, w, r, None, T, H, K, 1e-6) == INVALID                  # null gamma
     assert call(y, a, w, r, g, T, H, K, 1e-6, wsp=None) == INVALID           # no workspace
     need = lib.rarn_gemm_workspace_bytes(T, H)
-    assert need == T * (H // 256) * 4
+    assert need == (T * (H // 256) + 1) * 4   # partial sums, then one row-block counter
     assert call(y, a, w, r, g, T, H, K, 1e-6, wsn=need - 4) == INVALID      # short workspace
     assert call(_rows(A, 300, BF16), a, _rows(C, K, BF16), _rows(D, 300, BF16), g, T, 300, K,
                 1e-6) == UNSUPPORTED                                         # H = 300
@@ -348,18 +348,30 @@ def test_gemm_form_argument_errors(lib):
                 _rows(None, H, BF16), None, 0, H, K, 1e-6, wsp=None) == OK  # T = 0
 
 
-def test_plan_gemm():
+def test_plan_gemm(monkeypatch):
     """Columns per CTA from H; the K slab and ring depth fill one SM's shared
     memory; the workspace holds one float per row and column tile."""
-    p = rarn.plan_gemm(4096, 4096, 4096)   # persistent: one CTA per SM walks 512 tiles
+    # persistent on SM pairs: 76 two-CTA clusters walk 256 tiles of 256 x 256,
+    # each CTA staging 32 KB per K slab
+    p = rarn.plan_gemm(4096, 4096, 4096)
+    assert "cols_per_cta=256 col_tiles=16 bk=64 stages=7" in p and "grid=152" in p, p
+    assert "kblocks=64 persistent=1 pair=1" in p, p
+    p = rarn.plan_gemm(300, 512, 4096)     # 2 x 2 pair tiles: 4 clusters
+    assert "grid=8 " in p and "pair=1" in p, p
+    monkeypatch.setenv("RARN_GEMM_PAIR", "0")  # one CTA per SM walks 512 tiles of 128 x 256
+    p = rarn.plan_gemm(4096, 4096, 4096)
     assert "cols_per_cta=256 col_tiles=16 bk=64 stages=4" in p and "grid=152" in p, p
-    assert "kblocks=64 persistent=1" in p, p
-    p = rarn.plan_gemm(100, 768, 1000)
+    assert "kblocks=64 persistent=1 pair=0" in p, p
+    monkeypatch.delenv("RARN_GEMM_PAIR")
+    p = rarn.plan_gemm(100, 768, 1000)     # one 128-row block: no pair
     assert "cols_per_cta=256 col_tiles=3" in p and "persistent=1" in p and "grid=3" in p, p
+    assert "pair=0" in p, p
     p = rarn.plan_gemm(8, 16384, 64)   # beyond 32 tiles of 256: 512-column tiles
     assert "cols_per_cta=512 col_tiles=32 bk=32 stages=5" in p and "persistent=0" in p, p
     assert rarn.plan_gemm(8, 300, 64).startswith("none")
     assert rarn.plan_gemm(8, 16896, 64).startswith("none")   # 33 x 512: beyond 32 tiles
     assert rarn.plan_gemm(8, 4096, 64, "f32").startswith("none")
-    assert rarn.gemm_workspace_bytes(4096, 4096) == 4096 * 16 * 4
+    # partial sums [T][tiles], then one counter per 128-row block (16-byte aligned)
+    assert rarn.gemm_workspace_bytes(4096, 4096) == (4096 * 16 + 32) * 4
+    assert rarn.gemm_workspace_bytes(1, 768) == (4 + 1) * 4
     assert rarn.gemm_workspace_bytes(7, 300) == -1

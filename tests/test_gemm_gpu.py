@@ -133,6 +133,7 @@ def test_gemm_parity(T, H, K, dt):
     plan = run_case(T, H, K, dt, seed=T + H + K)
     assert plan.startswith("gemm.tcgen05"), plan
     assert ("persistent=1" in plan) == (H <= 8192 and K >= 512), plan
+    assert ("pair=1" in plan) == (H <= 8192 and K >= 512 and T > 128), plan
 
 
 @pytest.mark.parametrize("ns,bk,ctas", [("256", "32", "2"), ("256", "64", "2"),
@@ -150,6 +151,54 @@ def test_gemm_tilings(ns, bk, ctas, monkeypatch):
         plan = run_case(T, H, K, "bf16", seed=K)
         assert f"cols_per_cta={ns}" in plan and f"bk={bk}" in plan, plan
         assert "persistent=0" in plan, plan
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_gemm_persistent_one_sm_and_sm_pairs(pair, monkeypatch):
+    """The persistent kernel forced onto one SM per 128 x 256 tile and onto
+    SM pairs (two-CTA clusters, cta_group::2 MMAs on 256 x 256 tiles, each CTA
+    staging half of the W slab): one row, ragged rows and K, a single K slab,
+    3 to 32 column tiles, and more tiles than pairs so that both accumulators
+    are reused."""
+    monkeypatch.setenv("RARN_GEMM_PERSIST", "1")
+    monkeypatch.setenv("RARN_GEMM_PAIR", pair)
+    for T, H, K, dt in ((1, 1024, 512, "bf16"), (200, 768, 520, "bf16"),
+                        (300, 2048, 1024, "f16"), (700, 1536, 64, "bf16"),
+                        (520, 8192, 192, "bf16"), (2500, 4096, 96, "bf16")):
+        plan = run_case(T, H, K, dt, seed=T + K + 7)
+        assert "persistent=1" in plan and f"pair={pair}" in plan, plan
+    # residual rows that do not all start on a 32-byte boundary (row stride
+    # 1032): the epilogue's 16-byte form
+    plan = run_case(300, 1024, 512, "bf16", seed=3, ldr=1032, ldy=1040)
+    assert "persistent=1" in plan and f"pair={pair}" in plan, plan
+
+
+@pytest.mark.parametrize("pair", ["0", "1"])
+def test_gemm_norm_in_epilogue_matches_norm_kernel(pair, monkeypatch):
+    """y written by the persistent kernel's epilogue (each tile waits on its
+    128-row block's counter) and by the separate norm kernel: bit-identical,
+    on shapes with more tiles than CTAs or pairs, so that row blocks straddle
+    two rounds of tiles, and with 32 column tiles per row."""
+    import torch
+    monkeypatch.setenv("RARN_GEMM_PAIR", pair)
+    for T, H, K in ((2500, 4096, 512), (1000, 8192, 576), (129, 2048, 1024)):
+        gen = torch.Generator(device="cuda").manual_seed(T + H + K)
+        a = torch.randn(T, K, device="cuda", generator=gen).to(torch.bfloat16)
+        w = (torch.randn(H, K, device="cuda", generator=gen) / K ** 0.5).to(torch.bfloat16)
+        r0 = torch.randn(T, H, device="cuda", generator=gen).to(torch.bfloat16)
+        g = (torch.rand(H, device="cuda", generator=gen) + 0.5).to(torch.bfloat16)
+        outs = {}
+        for fuse in ("1", "0"):
+            monkeypatch.setenv("RARN_GEMM_FUSE", fuse)
+            plan = rarn.plan_gemm(T, H, K)
+            assert ("norm in epilogue" in plan) == (fuse == "1"), plan
+            r = r0.clone()
+            y = rarn.gemm_add_rms_norm(a, w, r, g, 1e-6)
+            torch.cuda.synchronize()
+            assert rarn.watchdog(clear=True) == 0
+            outs[fuse] = (y, r)
+        assert torch.equal(outs["1"][0], outs["0"][0]), f"y differs at T{T} H{H} K{K}"
+        assert torch.equal(outs["1"][1], outs["0"][1]), f"residual differs at T{T} H{H} K{K}"
 
 
 def test_gemm_strides():

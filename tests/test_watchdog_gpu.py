@@ -36,13 +36,17 @@ def test_wait_runs_out_and_is_reported(fill):
     assert rarn.watchdog(clear=True) == 0
 
 
-@pytest.mark.parametrize("K,fill", [(1024, 0), (1024, 9), (256, 0), (256, 2)])
-def test_gemm_wait_runs_out_and_is_reported(K, fill):
-    """The GEMM form (persistent kernel for K = 1024, two-CTA kernel for
-    K = 256): one ring fill of CTA 0 never completes; every role's wait gives
-    up within the limit, the CTA drains what it issued and frees its tensor
-    memory, the watchdog bit is set, and the next call is correct."""
+@pytest.mark.parametrize("K,fill,pair", [(1024, 0, "1"), (1024, 9, "1"), (1024, 0, "0"),
+                                         (1024, 9, "0"), (256, 0, None), (256, 2, None)])
+def test_gemm_wait_runs_out_and_is_reported(K, fill, pair, monkeypatch):
+    """The GEMM form (persistent kernel for K = 1024, on SM pairs or on one SM
+    per tile; two CTAs per SM for K = 256): one ring fill of CTA 0 never
+    completes; every role's wait gives up within the limit, the CTA (or the
+    pair) drains what it issued and frees its tensor memory, the watchdog bit
+    is set, and the next call is correct."""
     import torch
+    if pair is not None:
+        monkeypatch.setenv("RARN_GEMM_PAIR", pair)
     T, H = 1000, 2048
     gen = torch.Generator(device="cuda").manual_seed(K + fill)
     a = torch.randn(T, K, device="cuda", generator=gen).to(torch.bfloat16)
