@@ -279,7 +279,7 @@ rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows parti
  * row's partials in tile order and writes y; otherwise a norm kernel does
  * that last step.  Both orders give identical bits.  `workspace` is
  * caller-owned device memory of at least rarn_gemm_workspace_bytes(T, H)
- * bytes (4-byte aligned); its contents are scratch and need no
+ * bytes (16-byte aligned); its contents are scratch and need no
  * initialisation.
  *
  * Matrices are rarn_rows (row-major, row_stride in elements), all of one

@@ -790,10 +790,11 @@ static GemmPlan gemm_plan_env(int64_t T, int64_t H, int64_t K, int num_sms = 152
     if (const char *v = getenv("RARN_GEMM_NS")) ns = atoi(v);
     if (const char *v = getenv("RARN_GEMM_CTAS")) ctas = atoi(v);
     if (const char *v = getenv("RARN_GEMM_PERSIST")) persist = atoi(v);
-    int pair = -1, fuse = -1;
+    int pair = -1, fuse = -1, split = -1;
     if (const char *v = getenv("RARN_GEMM_PAIR")) pair = atoi(v);
     if (const char *v = getenv("RARN_GEMM_FUSE")) fuse = atoi(v);
-    return plan_gemm(T, H, K, bk, ns, ctas, persist, num_sms, pair, fuse);
+    if (const char *v = getenv("RARN_GEMM_SPLIT")) split = atoi(v);
+    return plan_gemm(T, H, K, bk, ns, ctas, persist, num_sms, pair, fuse, split);
 }
 
 int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H) {
@@ -818,8 +819,8 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     if (T > (int64_t(1) << 31) - 128 || K > (int64_t(1) << 31) - 64) return RARN_ERR_UNSUPPORTED;
     const GemmPlan gp = gemm_plan_env(T, H, K);
     if (gp.ns == 0) return RARN_ERR_UNSUPPORTED;
-    const int64_t ws = gemm_workspace_bytes_for(T, gp.tiles_n);
-    if ((int64_t)workspace_bytes < ws || (reinterpret_cast<uintptr_t>(workspace) & 3u))
+    const int64_t ws = gemm_workspace_bytes_for(T, H);
+    if ((int64_t)workspace_bytes < ws || (reinterpret_cast<uintptr_t>(workspace) & 15u))
         return RARN_ERR_INVALID_ARG;
     auto al16 = [](const void *ptr, int64_t ld) { return aligned16(ptr) && (ld * 2) % 16 == 0; };
     if (!al16(a.data, a.row_stride) || !al16(w.data, w.row_stride) ||
@@ -864,7 +865,10 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     c.num_sms = d->num_sms;
     c.persistent = gp.persistent;
     c.pair = gp.pair;
-    c.fuse_norm = gp.fuse_norm;
+    // the launcher re-checks both against the clusters that fit on this GPU
+    c.fuse_norm = gp.fuse_norm || (gp.persistent && !(getenv("RARN_GEMM_FUSE") &&
+                                                      atoi(getenv("RARN_GEMM_FUSE")) == 0));
+    c.tail_split = !(getenv("RARN_GEMM_SPLIT") && atoi(getenv("RARN_GEMM_SPLIT")) == 0);
     c.wait_limit_ns = 2000000000ull;
     c.stall_fill = -1;
     {
@@ -897,7 +901,7 @@ rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w
     if (st != RARN_OK) return st;
     // rows per launch sequence that the scratch holds (partial sums and
     // row-block counters); later chunks reuse it in stream order
-    const int64_t chunk = (kGemmScratchFloats - 16) / (gp.tiles_n + 1) / 128 * 128;
+    const int64_t chunk = (kGemmScratchFloats - 16) / (H / 128 + 1) / 128 * 128;
     for (int64_t t0 = 0; t0 < T; t0 += chunk) {
         const int64_t rows = std::min(chunk, T - t0);
         auto shift = [t0](rarn_rows m) {
@@ -921,10 +925,10 @@ rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, char 
     }
     snprintf(out, cap,
              "gemm.tcgen05 cols_per_cta=%d col_tiles=%d bk=%d stages=%d smem=%d grid=%lld "
-             "kblocks=%lld persistent=%d pair=%d %s",
+             "kblocks=%lld persistent=%d pair=%d%s %s",
              gp.ns, gp.tiles_n, gp.bk, gp.stages, gp.smem, (long long)gp.grid,
              (long long)((K + gp.bk - 1) / gp.bk), (int)gp.persistent, (int)gp.pair,
-             gp.fuse_norm ? "norm in epilogue" : "+ norm");
+             gp.tail_split ? " tail=halves" : "", gp.fuse_norm ? "norm in epilogue" : "+ norm");
     return RARN_OK;
 }
 

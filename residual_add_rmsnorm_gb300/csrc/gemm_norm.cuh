@@ -76,7 +76,8 @@ struct Params {
     float *ss;         // workspace [T][C]: per row, each column tile's sum of squares of h
     int64_t T, H, K;
     int ns;            // columns per CTA
-    int C;             // column tiles (H / ns)
+    int C;             // column tiles (H / ns); the persistent kernels' partial sums
+                       // come in 2 C slots of 128 columns per row
     int stages;
     int kblocks;       // ceil(K / BK)
     unsigned int *watchdog;
@@ -89,6 +90,9 @@ struct Params {
     // by inv and gamma and writes y.  counters == nullptr: the norm kernel
     // writes y instead.
     unsigned int *counters;  // [ceil(T / 128)], zero when the kernel starts
+    // the pair kernel's items: tiles [0, full_items) whole, then the
+    // remaining tiles as two 128-column halves each (items in all)
+    int64_t full_items, items;
     void *y;
     int64_t ldy;
     const void *gamma;
@@ -100,9 +104,9 @@ struct NormParams {
     void *y;
     const void *h;     // the updated residual
     const void *gamma;
-    const float *ss;   // [T][C]
+    const float *ss;   // [T][C] partial sums of squares, added in order
     int64_t T, H, ldh, ldy;
-    int C;
+    int C;             // partial sums per row (at most 64)
     float eps;
 };
 
@@ -190,6 +194,24 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
             }
         }
     }
+}
+
+// Sum of a row's n partial sums (n even, the row 8-byte aligned), added in
+// order; loaded past L1 (other SMs wrote them) 16 at a time, so a row costs
+// n / 16 round trips to L2.
+__device__ __forceinline__ float row_sum(const float *sr, int n) {
+    float tot = 0.f;
+    for (int q0 = 0; q0 < n; q0 += 16) {
+        float2 x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            x[j] = q0 + 2 * j < n ? __ldcg(reinterpret_cast<const float2 *>(sr + q0) + j)
+                                  : make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (q0 + 2 * j < n) tot = (tot + x[j].x) + x[j].y;
+    }
+    return tot;
 }
 
 __device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int *p) {
@@ -414,8 +436,12 @@ struct EpiRow {
         }
     }
 
+    // The sum of squares is formed per 64 columns and those sums added in
+    // column order, so a 128-column slot has the same bits whether one
+    // thread or two warp halves (64 columns each) computed it.
     __device__ __forceinline__ float run(uint32_t taddr, T *res, bool live) {
-        float ss = 0.f;
+        static_assert(NC % 64 == 0, "64-column partial sums");
+        float ss = 0.f, part = 0.f;
 #pragma unroll
         for (int c = 0; c < NC; c += 32) {
             float v[32];
@@ -433,7 +459,7 @@ struct EpiRow {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         f[e] = DT<T>::round(v[8 * q + e] + f[e]);  // h: one rounding
-                        ss += f[e] * f[e];
+                        part += f[e] * f[e];
                     }
                     if constexpr (Wide) {
                         if (q & 1)
@@ -449,6 +475,10 @@ struct EpiRow {
                     st_global32(res + c, rv[c / 16].a, rv[c / 16].b);
                     st_global32(res + c + 16, rv[c / 16 + 1].a, rv[c / 16 + 1].b);
                 }
+            }
+            if (c % 64 == 32) {
+                ss += part;
+                part = 0.f;
             }
         }
         return ss;
@@ -855,36 +885,32 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             const float ss = er.run(taddr, res, live);
             tmem_fence_before();
             mbar_arrive(smem_u32(&tempty[acc]));  // the accumulator is free again
-            // the two column halves' sums meet in shared memory, added in
-            // column order (first half, then second)
-            half_ss[(warp - 2) * 32 + lane] = ss;
-            epi_barrier_ws();
-            if (c0 == 0 && live && !*abort_flag)
-                p.ss[t * C + ntile] = ss + half_ss[(warp + 2) * 32 + lane];
+            // each warp half's 128 columns are one partial-sum slot of the row
+            const int slots = 2 * C;
+            if (live && !*abort_flag) p.ss[t * slots + ntile * 2 + (c0 >> 7)] = ss;
             epi_barrier_ws();
             if (p.counters) {
-                // publish this tile's partials, then wait (bounded) for the
+                // publish this tile's two slots, then wait (bounded) for the
                 // other column tiles of the 128-row block
                 unsigned int *cnt = p.counters + (m0 / kBM);
                 if (warp == 2 && lane == 0) {
                     __threadfence();
-                    atomicAdd(cnt, 1u);
-                    *norm_ok = wait_count(cnt, (unsigned int)C, abort_flag, p.watchdog,
+                    atomicAdd(cnt, 2u);
+                    *norm_ok = wait_count(cnt, (unsigned int)slots, abort_flag, p.watchdog,
                                           p.wait_limit_ns)
                                    ? 1
                                    : 0;
                 }
                 epi_barrier_ws();
                 if (!*norm_ok) break;
-                if (live) {
-                    // the row's partials in tile order (read past L1: other SMs wrote them)
-                    const float *sr = p.ss + t * C;
-                    float tot = 0.f;
-                    for (int q = 0; q < C; ++q) tot += __ldcg(sr + q);
-                    const float inv = rsqrtf(tot / (float)p.H + p.eps);
-                    er.store_y(inv, reinterpret_cast<const T *>(p.gamma) + ntile * NS + c0,
+                // inv of each row, formed once (warp half 0) from the row's
+                // partials in column order and shared through shared memory
+                if (c0 == 0 && live)
+                    half_ss[row] = rsqrtf(row_sum(p.ss + t * slots, slots) / (float)p.H + p.eps);
+                epi_barrier_ws();
+                if (live)
+                    er.store_y(half_ss[row], reinterpret_cast<const T *>(p.gamma) + ntile * NS + c0,
                                reinterpret_cast<T *>(p.y) + t * p.ldy + ntile * NS + c0);
-                }
             }
         }
     }
@@ -997,11 +1023,103 @@ __device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t mask) {
 }
 
 // Instruction descriptor of the pair MMA: as instr_desc, M = 256.
-template <typename T>
+template <typename T, int N_>
 __host__ __device__ constexpr uint32_t instr_desc_pair() {
+    static_assert(N_ % 16 == 0 && N_ >= 32 && N_ <= 256, "M = 256 takes N = 32 .. 256");
     constexpr uint32_t ab = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
-    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(kMmaN >> 3) << 17) |
+    return (1u << 4) | (ab << 7) | (ab << 10) | ((uint32_t)(N_ >> 3) << 17) |
            ((uint32_t)(kPairBM >> 4) << 24);
+}
+
+// An item of the pair kernel: a whole 256 x 256 tile or, for the tiles of
+// the last partial round, one 128-column half of a tile (so that round fills
+// up to twice as many SM pairs for half as long).
+struct PairItem {
+    int64_t tile;
+    int col0;   // first column within the tile
+    int ncols;  // 256 or 128
+};
+
+__device__ __forceinline__ PairItem pair_item(int64_t item, int64_t full_items, int C) {
+    (void)C;
+    if (item < full_items) return PairItem{item, 0, kMmaN};
+    const int64_t h = item - full_items;
+    return PairItem{full_items + h / 2, (int)(h & 1) * (kMmaN / 2), kMmaN / 2};
+}
+
+// The pair kernel's epilogue for one item, in one CTA (8 warps): NC columns
+// per warp half (128 for a whole tile, 64 for a half).  Returns 0 when a wait
+// gave up (the epilogue stops), 1 otherwise.
+template <typename T, int NC, bool Wide>
+__device__ __forceinline__ int pair_epilogue(const Params &p, void *residual, int64_t ldr,
+                                             const PairItem &pi, int it, int64_t item,
+                                             int64_t npairs, int64_t items, int64_t m0,
+                                             uint32_t tbase, uint64_t *tfull, uint64_t *tempty,
+                                             volatile int *tile_ok, volatile int *norm_ok,
+                                             float *half_ss, volatile int *abort_flag) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wh = (warp - 2) >> 2;  // warp half
+    const int acc = it & 1;
+    const int ntile = (int)(pi.tile % p.C);
+    const int slots = 2 * p.C;  // 128-column partial sums per row
+    const int64_t t = m0 + (warp & 3) * 32 + lane;
+    const bool live = t < p.T;
+    const int c0 = pi.col0 + wh * NC;  // this warp half's first column in the tile
+    T *res = reinterpret_cast<T *>(residual) + (live ? t : 0) * ldr + ntile * kMmaN + c0;
+    // this thread's residual columns are loaded before the wait for the
+    // accumulator, so they arrive while the item's MMAs run
+    EpiRow<T, NC, Wide> er;
+    if (live) er.load(res);
+    // one thread waits (bounded) and the 8 warps leave together
+    if (warp == 2 && lane == 0)
+        *tile_ok = wait_phase(smem_u32(&tfull[acc]), (uint32_t)((it >> 1) & 1), abort_flag,
+                              p.watchdog, p.wait_limit_ns)
+                       ? 1
+                       : 0;
+    epi_barrier_ws();
+    if (!*tile_ok) return 0;
+    tmem_fence_after();
+    if (item + npairs >= items) grid_launch_dependents();
+    const float ss = er.run(tbase + wh * NC, res, live);
+    tmem_fence_before();
+    // this CTA's half of the accumulator is read: tell the leader
+    mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
+    const int slot = ntile * 2 + (c0 >> 7);
+    if (NC == 128) {
+        if (live && !*abort_flag) p.ss[t * slots + slot] = ss;
+    } else {
+        // both warp halves fill one slot: added in column order
+        half_ss[(warp - 2) * 32 + lane] = ss;
+        epi_barrier_ws();
+        if (wh == 0 && live && !*abort_flag)
+            p.ss[t * slots + slot] = ss + half_ss[(warp + 2) * 32 + lane];
+    }
+    epi_barrier_ws();
+    if (p.counters) {
+        // publish this item's slots, then wait (bounded) for the rest of the
+        // 128-row block's columns
+        unsigned int *cnt = p.counters + (m0 / kBM);
+        if (warp == 2 && lane == 0) {
+            __threadfence();
+            atomicAdd(cnt, (unsigned int)(pi.ncols >> 7));
+            *norm_ok = wait_count(cnt, (unsigned int)slots, abort_flag, p.watchdog,
+                                  p.wait_limit_ns)
+                           ? 1
+                           : 0;
+        }
+        epi_barrier_ws();
+        if (!*norm_ok) return 0;
+        // inv of each row, formed once (warp half 0) and shared through
+        // shared memory
+        const int row = (warp & 3) * 32 + lane;
+        if (wh == 0 && live)
+            half_ss[row] = rsqrtf(row_sum(p.ss + t * slots, slots) / (float)p.H + p.eps);
+        epi_barrier_ws();
+        if (live)
+            er.store_y(half_ss[row], reinterpret_cast<const T *>(p.gamma) + ntile * kMmaN + c0,
+                       reinterpret_cast<T *>(p.y) + t * p.ldy + ntile * kMmaN + c0);
+    }
+    return 1;
 }
 
 template <int BK = 64>
@@ -1024,7 +1142,8 @@ struct PairLayout {
 template <typename T, int BK, bool Wide>
 __global__ void __launch_bounds__(kWsThreads, 1)
     k_gemm_res_pair(const __grid_constant__ CUtensorMap map_a,
-                    const __grid_constant__ CUtensorMap map_w, void *residual, int64_t ldr,
+                    const __grid_constant__ CUtensorMap map_w,
+                    const __grid_constant__ CUtensorMap map_w_half, void *residual, int64_t ldr,
                     Params p) {
     static_assert(BK == 64, "K slab of 128 bytes");
     using Lay = PairLayout<BK>;
@@ -1049,8 +1168,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_rank();  // 0: leader (issues the MMAs)
     const int C = p.C;
-    const int64_t mtiles = (p.T + kPairBM - 1) / kPairBM;
-    const int64_t ntiles = mtiles * C;
+    const int64_t items = p.items;
     const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const int KB = p.kblocks;
 
@@ -1084,7 +1202,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const uint32_t tmem = ld_cluster_u32(map_to_rank(smem_u32(tmem_slot), 0));
     grid_dependency_wait();  // A, W and the residual may come from the previous kernel
 
-    int64_t kit = 0;  // producer: k-slabs issued so far (all tiles)
+    int64_t kit = 0;  // producer: k-slabs issued so far (all items)
     if (warp == 0) {
         if (lane == 0) {
             // ---- TMA producer (both CTAs) ----
@@ -1093,9 +1211,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             const uint32_t full0 = smem_u32(full), empty0 = smem_u32(empty), ring0 = smem_u32(smem);
             const uint32_t lead_full0 = map_to_rank(full0, 0);
             const uint64_t pol = l2_evict_last_policy();
-            for (int64_t tile = pair; tile < ntiles && !stop; tile += npairs) {
-                const int m0 = (int)((tile / C) * kPairBM + rank * kBM);
-                const int n0 = (int)((tile % C) * NS + rank * (NS / 2));
+            for (int64_t item = pair; item < items && !stop; item += npairs) {
+                const PairItem pi = pair_item(item, p.full_items, C);
+                const int m0 = (int)((pi.tile / C) * kPairBM + rank * kBM);
+                // this CTA's W rows: its half of the item's columns
+                const int n0 = (int)((pi.tile % C) * NS + pi.col0 + rank * (pi.ncols / 2));
+                const CUtensorMap *mw = pi.ncols == NS ? &map_w : &map_w_half;
+                const uint32_t bytes = 2 * (Lay::a_bytes + pi.ncols / 2 * BK * 2);
                 for (int kb = 0; kb < KB; ++kb, ++kit) {
                     if (kit >= S && !wait_phase(empty0 + 8 * s, ph ^ 1u, abort_flag, p.watchdog,
                                                 p.wait_limit_ns)) {
@@ -1104,12 +1226,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                     }
                     if (rank == 0)
                         mbar_arrive_expect_tx(
-                            full0 + 8 * s, 2 * Lay::stage_bytes +
-                                               (blockIdx.x == 0 && kit == p.stall_fill ? 16u : 0u));
+                            full0 + 8 * s, bytes + (blockIdx.x == 0 && kit == p.stall_fill ? 16u : 0u));
                     const uint32_t lead_fb = lead_full0 + 8 * s;
                     const uint32_t sa = ring0 + s * Lay::stage_bytes;
                     tma_load_2d_pair(sa, &map_a, kb * BK, m0, lead_fb, pol);
-                    tma_load_2d_pair(sa + Lay::a_bytes, &map_w, kb * BK, n0, lead_fb, pol);
+                    tma_load_2d_pair(sa + Lay::a_bytes, mw, kb * BK, n0, lead_fb, pol);
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
@@ -1121,7 +1242,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     } else if (warp == 1) {
         if (lane == 0 && rank == 0) {
             // ---- MMA issuer (leader only) ----
-            const uint32_t idesc = instr_desc_pair<T>();
+            const uint32_t idesc_full = instr_desc_pair<T, NS>();
+            const uint32_t idesc_half = instr_desc_pair<T, NS / 2>();
             const uint64_t adesc0 = smem_desc(smem_u32(smem), BK * 2);
             const uint64_t bdesc0 = smem_desc(smem_u32(smem) + Lay::a_bytes, BK * 2);
             constexpr uint32_t kStageDesc = Lay::stage_bytes >> 4;
@@ -1129,8 +1251,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             uint32_t s = 0, ph = 0;
             int it = 0;
             bool stop = false;
-            for (int64_t tile = pair; tile < ntiles && !stop; tile += npairs, ++it) {
+            for (int64_t item = pair; item < items && !stop; item += npairs, ++it) {
                 const int acc = it & 1;
+                const uint32_t idesc = item < p.full_items ? idesc_full : idesc_half;
                 if (it >= 2 &&
                     !wait_phase<true>(smem_u32(&tempty[acc]), (uint32_t)(((it >> 1) - 1) & 1),
                                       abort_flag, p.watchdog, p.wait_limit_ns))
@@ -1162,67 +1285,23 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         }
         __syncwarp();
     } else {
-        // ---- epilogue: warps 2-9 of both CTAs, each on its CTA's 128 rows ----
-        const int quarter = warp & 3;
-        const int row = quarter * 32 + lane;
-        const int c0 = ((warp - 2) >> 2) * (NS / 2);
+        // ---- epilogue: warps 2-9 of both CTAs, each on its CTA's 128 rows;
+        // warp half (warp - 2) / 4 takes half of the item's columns ----
         int it = 0;
-        for (int64_t tile = pair; tile < ntiles; tile += npairs, ++it) {
-            const int acc = it & 1;
-            const int64_t m0 = (tile / C) * kPairBM + rank * kBM;
-            const int ntile = (int)(tile % C);
-            const int64_t t = m0 + row;
-            const bool live = t < p.T;
-            T *res = reinterpret_cast<T *>(residual) + (live ? t : 0) * ldr + ntile * NS + c0;
-            // this thread's residual columns are loaded before the wait for
-            // the accumulator, so they arrive while the tile's MMAs run
-            EpiRow<T, NS / 2, Wide> er;
-            if (live) er.load(res);
-            // one thread waits (bounded) and the 8 warps leave together
-            if (warp == 2 && lane == 0)
-                *tile_ok = wait_phase(smem_u32(&tfull[acc]), (uint32_t)((it >> 1) & 1), abort_flag,
-                                      p.watchdog, p.wait_limit_ns)
-                               ? 1
-                               : 0;
-            epi_barrier_ws();
-            if (!*tile_ok) break;
-            tmem_fence_after();
-            if (tile + npairs >= ntiles) grid_launch_dependents();
-            const uint32_t taddr =
-                tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * NS + c0;
-            const float ss = er.run(taddr, res, live);
-            tmem_fence_before();
-            // this CTA's half of the accumulator is read: tell the leader
-            mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
-            half_ss[(warp - 2) * 32 + lane] = ss;
-            epi_barrier_ws();
-            if (c0 == 0 && live && !*abort_flag)
-                p.ss[t * C + ntile] = ss + half_ss[(warp + 2) * 32 + lane];
-            epi_barrier_ws();
-            if (p.counters) {
-                // publish this tile's partials, then wait (bounded) for the
-                // other column tiles of the 128-row block
-                unsigned int *cnt = p.counters + (m0 / kBM);
-                if (warp == 2 && lane == 0) {
-                    __threadfence();
-                    atomicAdd(cnt, 1u);
-                    *norm_ok = wait_count(cnt, (unsigned int)C, abort_flag, p.watchdog,
-                                          p.wait_limit_ns)
-                                   ? 1
-                                   : 0;
-                }
-                epi_barrier_ws();
-                if (!*norm_ok) break;
-                if (live) {
-                    // the row's partials in tile order (read past L1: other SMs wrote them)
-                    const float *sr = p.ss + t * C;
-                    float tot = 0.f;
-                    for (int q = 0; q < C; ++q) tot += __ldcg(sr + q);
-                    const float inv = rsqrtf(tot / (float)p.H + p.eps);
-                    er.store_y(inv, reinterpret_cast<const T *>(p.gamma) + ntile * NS + c0,
-                               reinterpret_cast<T *>(p.y) + t * p.ldy + ntile * NS + c0);
-                }
-            }
+        for (int64_t item = pair; item < items; item += npairs, ++it) {
+            const PairItem pi = pair_item(item, p.full_items, C);
+            const int64_t m0 = (pi.tile / C) * kPairBM + rank * kBM;
+            const uint32_t tbase =
+                tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + (it & 1) * NS;
+            const int ok =
+                pi.ncols == NS
+                    ? pair_epilogue<T, NS / 2, Wide>(p, residual, ldr, pi, it, item, npairs, items,
+                                                     m0, tbase, tfull, tempty, tile_ok, norm_ok,
+                                                     half_ss, abort_flag)
+                    : pair_epilogue<T, NS / 4, Wide>(p, residual, ldr, pi, it, item, npairs, items,
+                                                     m0, tbase, tfull, tempty, tile_ok, norm_ok,
+                                                     half_ss, abort_flag);
+            if (!ok) break;
         }
     }
     tmem_fence_before();
@@ -1241,7 +1320,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const int64_t kmax = kit > kp ? kit : kp;
         for (int64_t k = kmax - S > 0 ? kmax - S : 0; k < kmax; ++k) {
             const int s = (int)(k % S);
-            if (k >= kit) mbar_arrive_expect_tx(smem_u32(&full[s]), Lay::stage_bytes);
+            if (k >= kit) {
+                // the item of fill k: this pair's (k / KB)-th
+                const PairItem pi = pair_item(pair + (k / KB) * npairs, p.full_items, C);
+                mbar_arrive_expect_tx(smem_u32(&full[s]), Lay::a_bytes + pi.ncols / 2 * BK * 2);
+            }
             wait_phase(smem_u32(&full[s]), (uint32_t)((k / S) & 1), abort_flag, p.watchdog,
                        p.wait_limit_ns, true);
         }
@@ -1295,11 +1378,13 @@ __global__ void __launch_bounds__(kNormThreads) k_norm_ss(NormParams p) {
             const int j = j0 + lane + 32 * k;
             if (j < nv) hv[k] = ld_stream(h + (int64_t)j * EPV);
         }
-        // lane q holds tile q's partial (C <= 32); every lane adds them in
-        // tile order
-        const float part = lane < p.C ? p.ss[t * p.C + lane] : 0.f;
+        // lanes q and q + 32 hold partials q and q + 32 (C <= 64); every lane
+        // adds them in column order
+        const float part0 = lane < p.C ? p.ss[t * p.C + lane] : 0.f;
+        const float part1 = lane + 32 < p.C ? p.ss[t * p.C + lane + 32] : 0.f;
         float tot = 0.f;
-        for (int q = 0; q < p.C; ++q) tot += __shfl_sync(0xffffffffu, part, q);
+        for (int q = 0; q < p.C; ++q)
+            tot += __shfl_sync(0xffffffffu, q < 32 ? part0 : part1, q & 31);
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
         T *y = reinterpret_cast<T *>(p.y) + t * p.ldy;
 #pragma unroll

@@ -106,18 +106,21 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     p.wait_limit_ns = c.wait_limit_ns;
     p.stall_fill = c.stall_fill;
     const int64_t mblocks = (c.T + kBM - 1) / kBM;
+    const bool pair_path = BK == 64 && c.persistent && c.ns == 256 && c.pair;
+    const bool single_path = BK == 64 && c.persistent && c.ns == 256 && !c.pair;
+    PairSchedule ps;
+    if (pair_path) {
+        ps = pair_schedule(c.T, p.C, pair_clusters<T>(c.num_sms), c.tail_split);
+        p.full_items = ps.full_items;
+        p.items = ps.items;
+    }
     // y in the persistent kernels' epilogue: the row-block counters follow the
     // partial sums in the workspace and start each call at zero
-    // (walkers: CTAs, or pairs, of the persistent grid; a tile waits only on
-    // later tiles of its row block, which at least tiles_n walkers reach first)
-    const int64_t walkers =
-        c.pair ? std::min<int64_t>(((c.T + kPairBM - 1) / kPairBM) * p.C, pair_clusters<T>(c.num_sms))
-               : std::min<int64_t>(mblocks * p.C, c.num_sms);
-    const bool fused = c.fuse_norm && c.persistent && BK == 64 && c.ns == 256 && walkers >= p.C;
+    const bool fused = c.fuse_norm && ((pair_path && ps.fuse_ok) ||
+                                       (single_path && single_fuse_ok(c.T, p.C, c.num_sms)));
     p.counters = nullptr;
     if (fused) {
-        p.counters = reinterpret_cast<unsigned int *>(c.workspace +
-                                                      gemm_counters_offset(c.T, p.C));
+        p.counters = reinterpret_cast<unsigned int *>(c.workspace + gemm_counters_offset(c.T, c.H));
         p.y = c.y;
         p.ldy = c.ldy;
         p.gamma = c.gamma;
@@ -133,21 +136,23 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     const bool wide = (reinterpret_cast<uintptr_t>(c.residual) & 31u) == 0 && c.ldr % 16 == 0 &&
                       (reinterpret_cast<uintptr_t>(c.y) & 31u) == 0 && c.ldy % 16 == 0;
     if constexpr (BK == 64) {  // the persistent kernels take 128-byte K slabs only
-        if (c.persistent && c.ns == 256 && c.pair) {
-            CUtensorMap mw2;  // each CTA of a pair stages 128 of the tile's 256 W rows
-            if (!encode_map(&mw2, c.w, c.H, c.K, c.ldw, kMmaN / 2, BK, bf16))
+        if (pair_path) {
+            // each CTA of a pair stages half of an item's W rows: 128 of a
+            // whole tile's 256, 64 of a half tile's 128
+            CUtensorMap mw2, mw4;
+            if (!encode_map(&mw2, c.w, c.H, c.K, c.ldw, kMmaN / 2, BK, bf16) ||
+                !encode_map(&mw4, c.w, c.H, c.K, c.ldw, kMmaN / 4, BK, bf16))
                 return cudaErrorInvalidValue;
-            const int64_t ptiles = ((c.T + kPairBM - 1) / kPairBM) * p.C;
-            const int64_t grid = 2 * std::min<int64_t>(ptiles, pair_clusters<T>(c.num_sms));
+            const int64_t grid = 2 * ps.walkers;
             auto kernel = wide ? k_gemm_res_pair<T, BK, true> : k_gemm_res_pair<T, BK, false>;
             constexpr int smem = PairLayout<BK>::total;
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e == cudaSuccess)
                 e = launch_kernel(kernel, dim3(static_cast<unsigned>(grid)), dim3(kWsThreads),
-                                  static_cast<size_t>(smem), st, c.pdl, 2, ma, mw2, c.residual,
-                                  c.ldr, p);
+                                  static_cast<size_t>(smem), st, c.pdl, 2, ma, mw2, mw4,
+                                  c.residual, c.ldr, p);
             launched = true;
-        } else if (c.persistent && c.ns == 256) {
+        } else if (single_path) {
             const int64_t grid = std::min<int64_t>(mblocks * p.C, c.num_sms);
             auto kernel = wide ? k_gemm_res_ws<T, 256, BK, true> : k_gemm_res_ws<T, 256, BK, false>;
             constexpr int smem = WsLayout<256, BK>::total;
@@ -179,7 +184,7 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
     q.H = c.H;
     q.ldh = c.ldr;
     q.ldy = c.ldy;
-    q.C = p.C;
+    q.C = (pair_path || single_path) ? 2 * p.C : p.C;  // 128-column slots, or tiles
     q.eps = c.eps;
     const int64_t slices = (c.H / DT<T>::EPV + 32 * kNormVPT - 1) / (32 * kNormVPT);
     const int64_t warps = c.T * slices;

@@ -27,7 +27,8 @@ struct GemmCall {
     int num_sms;
     bool persistent;     // the warp-specialised persistent kernel (256-column tiles)
     bool pair;           // ... on SM pairs: 256 x 256 tiles, cta_group::2 MMAs
-    bool fuse_norm;      // the persistent kernel writes y (no norm kernel)
+    bool fuse_norm;      // allow the persistent kernels to write y (no norm kernel)
+    bool tail_split;     // allow the pair kernel to split the last round's tiles
     bool pdl;
     unsigned int *watchdog;
     unsigned long long wait_limit_ns;  // bound on every shared-memory barrier wait
@@ -46,7 +47,37 @@ struct GemmPlan {
     bool persistent = false;
     bool pair = false;
     bool fuse_norm = false;
+    bool tail_split = false;
 };
+
+// The pair kernel's schedule: `walkers` two-CTA clusters walk items in
+// row-major order (item i, i + walkers, ...).  When the last partial round
+// holds at most half as many tiles as there are walkers, those tiles are
+// split into two 128-column halves each.  y in the epilogue (a tile waits for
+// the rest of its row block) needs at least as many walkers as a row block
+// has items: then a wait only ever depends on items that no walker reaches
+// through a wait on it.
+struct PairSchedule {
+    int64_t walkers = 0, full_items = 0, items = 0;
+    bool fuse_ok = false;
+};
+
+inline PairSchedule pair_schedule(int64_t T, int tiles_n, int64_t clusters, bool allow_split) {
+    PairSchedule s;
+    const int64_t ptiles = ((T + 255) / 256) * tiles_n;
+    s.walkers = std::min<int64_t>(ptiles, clusters);
+    const int64_t tail = ptiles % s.walkers;
+    const bool split = allow_split && tail > 0 && 2 * tail <= s.walkers;
+    s.full_items = split ? ptiles - tail : ptiles;
+    s.items = split ? ptiles + tail : ptiles;
+    s.fuse_ok = s.walkers >= (split ? 2 : 1) * (int64_t)tiles_n;
+    return s;
+}
+
+// The one-SM persistent kernel: CTAs walk 128 x 256 tiles in row-major order.
+inline bool single_fuse_ok(int64_t T, int tiles_n, int num_sms) {
+    return std::min<int64_t>(((T + 127) / 128) * tiles_n, num_sms) >= tiles_n;
+}
 
 constexpr int kGemmMaxTilesN = 32;
 
@@ -56,7 +87,8 @@ constexpr int kGemmMaxTilesN = 32;
 // wider than 32 tiles of 256 use 512-column tiles.
 inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
                           int ns_override = 0, int ctas_override = 0, int persist_override = -1,
-                          int num_sms = 152, int pair_override = -1, int fuse_override = -1) {
+                          int num_sms = 152, int pair_override = -1, int fuse_override = -1,
+                          int split_override = -1) {
     GemmPlan g;
     const bool fit256 = H % 256 == 0 && H / 256 <= kGemmMaxTilesN;
     const bool fit512 = H % 512 == 0 && H / 512 <= kGemmMaxTilesN;
@@ -96,37 +128,44 @@ inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
         g.stages = std::min(9, (227 * 1024 - 3 * 1024) / stage);
         g.smem = g.stages * stage + 3 * 1024;
         g.grid = std::min<int64_t>(g.grid, num_sms);
-        // SM pairs (256-row tiles, each CTA staging half of the W slab) once
-        // there is more than one 128-row block
-        g.pair = pair_override == 1 || (pair_override != 0 && T > 128);
+        // SM pairs (256-row tiles, each CTA staging half of the W slab) from
+        // 2048 rows; measured at K = H = 4096: T = 1024 30.4 us on one SM per
+        // tile against 34.8 on pairs, T = 2048 56.6 against 55.5, T = 4096
+        // 106.2 against 96.6
+        g.pair = pair_override == 1 || (pair_override != 0 && T >= 2048);
         if (g.pair) {
             const int half = (128 + g.ns / 2) * g.bk * 2;
             g.stages = std::min(8, (227 * 1024 - 3 * 1024) / half);
             g.smem = g.stages * half + 3 * 1024;
             g.grid = 2 * std::min<int64_t>(((T + 255) / 256) * g.tiles_n, num_sms / 2);
         }
-        // y in the epilogue: a tile waits for the other column tiles of its
-        // row block, which tiles walked in row-major order by at least
-        // tiles_n CTAs (or pairs) always reach without waiting on it
-        g.fuse_norm = fuse_override != 0 && g.grid / (g.pair ? 2 : 1) >= g.tiles_n;
+        if (g.pair) {
+            const PairSchedule ps = pair_schedule(T, g.tiles_n, num_sms / 2, split_override != 0);
+            g.tail_split = ps.items != ps.full_items;
+            g.fuse_norm = fuse_override != 0 && ps.fuse_ok;
+        } else {
+            g.fuse_norm = fuse_override != 0 && single_fuse_ok(T, g.tiles_n, num_sms);
+        }
     }
     return g;
 }
 
-// Workspace of the GEMM form: one binary32 per row and column tile (the
-// column tiling depends on H only), then, 16-byte aligned, one 32-bit counter
-// per 128-row block (-1: H not supported).
-inline int64_t gemm_counters_offset(int64_t T, int tiles_n) {  // in floats
-    return (T * tiles_n + 3) / 4 * 4;
+// Workspace of the GEMM form: partial sums of squares (one binary32 per row
+// and 128 columns: the persistent kernels' slots; the other kernel's 256- or
+// 512-column tiles use fewer), then, 16-byte aligned, one 32-bit counter per
+// 128-row block.
+inline int64_t gemm_counters_offset(int64_t T, int64_t H) {  // in floats
+    return (T * (H / 128) + 3) / 4 * 4;
 }
 
-inline int64_t gemm_workspace_bytes_for(int64_t T, int tiles_n) {
-    return (gemm_counters_offset(T, tiles_n) + (T + 127) / 128) * 4;
+inline int64_t gemm_workspace_bytes_for(int64_t T, int64_t H) {
+    return (gemm_counters_offset(T, H) + (T + 127) / 128) * 4;
 }
 
+// -1: H not supported.
 inline int64_t gemm_workspace_bytes(int64_t T, int64_t H) {
     const GemmPlan g = plan_gemm(T, H, 0);
-    return g.ns == 0 ? -1 : gemm_workspace_bytes_for(T, g.tiles_n);
+    return g.ns == 0 ? -1 : gemm_workspace_bytes_for(T, H);
 }
 
 }  // namespace rarn

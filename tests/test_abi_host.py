@@ -333,8 +333,9 @@ def test_gemm_form_argument_errors(lib):
     assert call(y, a, w, r, None, T, H, K, 1e-6) == INVALID                  # null gamma
     assert call(y, a, w, r, g, T, H, K, 1e-6, wsp=None) == INVALID           # no workspace
     need = lib.rarn_gemm_workspace_bytes(T, H)
-    assert need == (T * (H // 256) + 1) * 4   # partial sums, then one row-block counter
+    assert need == (T * (H // 128) + 1) * 4   # partial sums, then one row-block counter
     assert call(y, a, w, r, g, T, H, K, 1e-6, wsn=need - 4) == INVALID      # short workspace
+    assert call(y, a, w, r, g, T, H, K, 1e-6, wsp=ws + 8) == INVALID         # not 16-byte aligned
     assert call(_rows(A, 300, BF16), a, _rows(C, K, BF16), _rows(D, 300, BF16), g, T, 300, K,
                 1e-6) == UNSUPPORTED                                         # H = 300
     assert call(_rows(A, H, F32), _rows(B, K, F32), _rows(C, K, F32), _rows(D, H, F32), g, T, H,
@@ -356,8 +357,10 @@ def test_plan_gemm(monkeypatch):
     p = rarn.plan_gemm(4096, 4096, 4096)
     assert "cols_per_cta=256 col_tiles=16 bk=64 stages=7" in p and "grid=152" in p, p
     assert "kblocks=64 persistent=1 pair=1" in p, p
-    p = rarn.plan_gemm(300, 512, 4096)     # 2 x 2 pair tiles: 4 clusters
-    assert "grid=8 " in p and "pair=1" in p, p
+    p = rarn.plan_gemm(2100, 512, 4096)    # 9 x 2 pair tiles: 18 clusters
+    assert "grid=36 " in p and "pair=1" in p, p
+    p = rarn.plan_gemm(1024, 4096, 4096)   # below 2048 rows: one SM per tile
+    assert "persistent=1 pair=0" in p, p
     monkeypatch.setenv("RARN_GEMM_PAIR", "0")  # one CTA per SM walks 512 tiles of 128 x 256
     p = rarn.plan_gemm(4096, 4096, 4096)
     assert "cols_per_cta=256 col_tiles=16 bk=64 stages=4" in p and "grid=152" in p, p
@@ -371,7 +374,7 @@ def test_plan_gemm(monkeypatch):
     assert rarn.plan_gemm(8, 300, 64).startswith("none")
     assert rarn.plan_gemm(8, 16896, 64).startswith("none")   # 33 x 512: beyond 32 tiles
     assert rarn.plan_gemm(8, 4096, 64, "f32").startswith("none")
-    # partial sums [T][tiles], then one counter per 128-row block (16-byte aligned)
-    assert rarn.gemm_workspace_bytes(4096, 4096) == (4096 * 16 + 32) * 4
-    assert rarn.gemm_workspace_bytes(1, 768) == (4 + 1) * 4
+    # partial sums [T][H / 128], then one counter per 128-row block (16-byte aligned)
+    assert rarn.gemm_workspace_bytes(4096, 4096) == (4096 * 32 + 32) * 4
+    assert rarn.gemm_workspace_bytes(1, 768) == (8 + 1) * 4
     assert rarn.gemm_workspace_bytes(7, 300) == -1

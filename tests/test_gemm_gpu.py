@@ -133,7 +133,7 @@ def test_gemm_parity(T, H, K, dt):
     plan = run_case(T, H, K, dt, seed=T + H + K)
     assert plan.startswith("gemm.tcgen05"), plan
     assert ("persistent=1" in plan) == (H <= 8192 and K >= 512), plan
-    assert ("pair=1" in plan) == (H <= 8192 and K >= 512 and T > 128), plan
+    assert ("pair=1" in plan) == (H <= 8192 and K >= 512 and T >= 2048), plan
 
 
 @pytest.mark.parametrize("ns,bk,ctas", [("256", "32", "2"), ("256", "64", "2"),
@@ -199,6 +199,42 @@ def test_gemm_norm_in_epilogue_matches_norm_kernel(pair, monkeypatch):
             outs[fuse] = (y, r)
         assert torch.equal(outs["1"][0], outs["0"][0]), f"y differs at T{T} H{H} K{K}"
         assert torch.equal(outs["1"][1], outs["0"][1]), f"residual differs at T{T} H{H} K{K}"
+
+
+def test_gemm_pair_tail_halves(monkeypatch):
+    """The pair kernel's last partial round as 128-column halves (N = 128
+    MMAs; a round then fills up to twice as many SM pairs) against whole
+    tiles: bit-identical (the same K order per element, the same 128-column
+    partial sums); sampled rows against the oracle."""
+    import torch
+    monkeypatch.setenv("RARN_GEMM_PAIR", "1")
+    monkeypatch.setenv("RARN_GEMM_SPLIT", "1")
+    plan = run_case(1536, 4096, 512, "bf16", seed=9, sample_rows=np.arange(1280, 1536, 4))
+    assert "tail=halves" in plan, plan
+    for T, H, K in ((1536, 4096, 512), (2560, 2048, 576)):
+        gen = torch.Generator(device="cuda").manual_seed(T + K)
+        a = torch.randn(T, K, device="cuda", generator=gen).to(torch.bfloat16)
+        w = (torch.randn(H, K, device="cuda", generator=gen) / K ** 0.5).to(torch.bfloat16)
+        r0 = torch.randn(T, H, device="cuda", generator=gen).to(torch.bfloat16)
+        g = (torch.rand(H, device="cuda", generator=gen) + 0.5).to(torch.bfloat16)
+        outs = {}
+        for split in ("1", "0"):
+            monkeypatch.setenv("RARN_GEMM_SPLIT", split)
+            plan = rarn.plan_gemm(T, H, K)
+            assert ("tail=halves" in plan) == (split == "1") and "pair=1" in plan, plan
+            r = r0.clone()
+            y = rarn.gemm_add_rms_norm(a, w, r, g, 1e-6)
+            torch.cuda.synchronize()
+            assert rarn.watchdog(clear=True) == 0
+            outs[split] = (y, r)
+        dy = (outs["1"][0] != outs["0"][0])
+        dr = (outs["1"][1] != outs["0"][1])
+        rows_y = torch.nonzero(dy.any(1)).flatten().tolist()
+        cols_y = torch.nonzero(dy.any(0)).flatten().tolist()
+        assert not dy.any() and not dr.any(), (
+            f"T{T} H{H} K{K}: {int(dy.sum())} y / {int(dr.sum())} residual elements differ; "
+            f"rows {rows_y[:4]}..{rows_y[-4:]} ({len(rows_y)}), cols {cols_y[:4]}..{cols_y[-4:]} "
+            f"({len(cols_y)})")
 
 
 def test_gemm_strides():
