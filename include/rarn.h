@@ -308,14 +308,15 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
  * device synchronisation of cudaMalloc / cudaFree.  The paper has no
  * counterpart.
  *
- * Scratch: the per-row partial sums of squares live in a file-scope device
- * array of 2^20 binary32 values (4 MiB, 256-byte aligned) that the library
- * reserves on every GPU it is loaded on and keeps until the process exits.
- * A launch pair holds T times the column-tile count (H / 256, or H / 512
- * beyond 8192) of those values, so a call with more rows than the array
- * holds (32768 rows at the widest tiling) runs as several launch pairs on
- * `stream`, one after another.  Every value is written before it is read, so
- * nothing needs clearing between calls.
+ * Scratch: the per-row partial sums of squares and the row-block counters
+ * live in a file-scope device array of 2^20 binary32 values (4 MiB, 256-byte
+ * aligned) that the library reserves on every GPU it is loaded on and keeps
+ * until the process exits.  One launch sequence holds T (H / 128 + 1) of
+ * those values, so a call with more rows than the array holds (16128 rows at
+ * H = 8192, 7936 at H = 16384) runs as several launch sequences on `stream`,
+ * one after another.  Every partial sum is written before it is read and the
+ * counters are zeroed by the call itself, so nothing needs clearing between
+ * calls.
  *
  * Set-up: the first call on each device (with that device current) looks up
  * the array's device address with cudaGetSymbolAddress and keeps it; make
