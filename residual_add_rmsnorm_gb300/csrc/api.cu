@@ -164,6 +164,10 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms, int r
     const int64_t slots = (int64_t)num_sms * std::max(1, resident_threads / pl.block);
     const int64_t rounds = ceil_div(T, slots);
     pl.grid = (int)ceil_div(T, rounds);
+    if (const char *v = getenv("RARN_ROWS_GRID")) {  // measurements only
+        const int64_t f = atoll(v);
+        if (f > 0) pl.grid = (int)std::min<int64_t>(f, T);
+    }
     // Gamma in registers when every CTA has a single row (latency-bound: the
     // gamma load then overlaps the row's loads instead of following the row
     // reduction) and the kernel's register budget allows it.
@@ -529,6 +533,14 @@ rarn_status run_ex(Call c) {
     p.qscale = c.qscale;
     p.qfmt = c.qfmt;
     p.qmode = c.qmode;
+    // each CTA's (or warp's) first row prefetched into L2 before the
+    // dependency wait.  Measured (same process, CUDA-graph timing, µs, rows
+    // prefetched 0 / 1 / 2 / 4): fused [4096, 4096] 21.49 / 20.96-21.23 /
+    // 21.81 / 23.00 (more rows compete with the previous kernel's tail);
+    // plain fp32 [512, 2048] 3.06 / 2.77; fused [128, 5120] 3.51 / 2.90;
+    // fused [64, 16384] 4.52 / 3.71; the stream kernel unchanged
+    p.l2_rows = c.host_buffers ? 0 : 1;
+    if (const char *v = getenv("RARN_L2_ROWS")) p.l2_rows = atoi(v);  // measurements only
     if (pl.kind == KIND_STREAM) {
         const long long f = g_stall_fill.exchange(-1);
         if (f >= 0) {

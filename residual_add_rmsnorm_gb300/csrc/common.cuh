@@ -43,6 +43,8 @@ struct Problem {
     float *qscale;           // Q_TENSOR: the one scale (read); Q_ROW: [T] scales (written)
     int qfmt;                // QFormat
     int qmode;               // QMode
+    int l2_rows;             // rows each CTA (or warp) prefetches into L2 before waiting on
+                             // the previous kernel (0: none; device-memory inputs only)
 };
 
 // ---------------------------------------------------------------------------
@@ -54,6 +56,15 @@ struct Problem {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned address.
+// It only warms L2, the GPU's point of coherence, so it may be issued before
+// grid_dependency_wait() even where the preceding kernel is still writing
+// those bytes: the loads after the wait then find them in L2 instead of
+// paying the DRAM latency that otherwise opens every launch.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void grid_launch_dependents() {

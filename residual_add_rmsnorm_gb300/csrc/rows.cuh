@@ -434,6 +434,32 @@ struct ScalarBound {
 // Kernels
 // ---------------------------------------------------------------------------
 
+// Row t's inputs (x, or the R partials, and the residual) prefetched into L2
+// by one thread before grid_dependency_wait(); rows of the 16-byte kernels
+// start on 16-byte boundaries and are multiples of 16 bytes long.
+template <typename T, int OP, typename TR>
+__device__ __forceinline__ void prefetch_row_l2(const Problem &p, int64_t t) {
+    if (t >= p.T) return;
+    const T *src = reinterpret_cast<const T *>(p.src);
+    const uint32_t xb = static_cast<uint32_t>(p.H * sizeof(T));
+    if constexpr (OP == OP_REDUCE) {
+        for (int r = 0; r < p.R; ++r) prefetch_l2(src + r * p.slice + t * p.ldx, xb);
+    } else {
+        prefetch_l2(src + t * p.ldx, xb);
+    }
+    if constexpr (OP != OP_PLAIN)
+        prefetch_l2(reinterpret_cast<const TR *>(p.residual) + t * p.ldr,
+                    static_cast<uint32_t>(p.H * sizeof(TR)));
+}
+
+// Rows t0, t0 + step, ... (p.l2_rows of them, at most 32) of one CTA
+// prefetched into L2 before grid_dependency_wait(), one row per thread.
+template <typename T, int OP, typename TR>
+__device__ __forceinline__ void prefetch_rows_l2(const Problem &p, int64_t t0, int64_t step) {
+    if ((int)threadIdx.x < p.l2_rows && threadIdx.x < 32)
+        prefetch_row_l2<T, OP, TR>(p, t0 + (int64_t)threadIdx.x * step);
+}
+
 // One CTA per row, packs.  PG: gamma held in registers for all rows.  Q8:
 // 8-bit output; a per-row scale takes a second CTA reduction (max |v|).
 template <typename T, int VPT, int OP, bool PG, typename TR, bool Q8>
@@ -441,6 +467,7 @@ __global__ void __launch_bounds__(VecBound<T, VPT, OP, PG, TR>::value) k_cta_vec
     __shared__ float red[2][32];
     __shared__ float2 red2[Q8 ? 64 : 1];
     const int nv = (int)(p.H / DT<T>::EPV);
+    prefetch_rows_l2<T, OP, TR>(p, blockIdx.x, gridDim.x);
     grid_dependency_wait();
     QMul qm{1.f, 1.f};
     if constexpr (Q8) qm = quant_tensor(p);
@@ -540,6 +567,7 @@ __global__ void __launch_bounds__(PipeBound<T, VPT, OP, TR>::value) k_cta_pipe(P
     __shared__ float red[2][32];
     __shared__ float2 red2[Q8 ? 64 : 1];
     const int nv = (int)(p.H / DT<T>::EPV);
+    prefetch_rows_l2<T, OP, TR>(p, blockIdx.x, gridDim.x);
     grid_dependency_wait();
     QMul qm{1.f, 1.f};
     if constexpr (Q8) qm = quant_tensor(p);
@@ -581,6 +609,7 @@ __global__ void __launch_bounds__(256) k_warp_vec(Problem p) {
     const int wpb = blockDim.x >> 5;
     const int64_t first = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     const int64_t step = (int64_t)gridDim.x * wpb;
+    if (lane == 0 && p.l2_rows > 0) prefetch_row_l2<T, OP, TR>(p, first);
     grid_dependency_wait();
     QMul qm{1.f, 1.f};
     if constexpr (Q8) qm = quant_tensor(p);
@@ -606,6 +635,7 @@ __global__ void __launch_bounds__(256) k_warp_pipe(Problem p) {
     const int wpb = blockDim.x >> 5;
     const int64_t first = (int64_t)blockIdx.x * wpb + (threadIdx.x >> 5);
     const int64_t step = (int64_t)gridDim.x * wpb;
+    if (lane == 0 && p.l2_rows > 0) prefetch_row_l2<T, OP, TR>(p, first);
     grid_dependency_wait();
     QMul qm{1.f, 1.f};
     if constexpr (Q8) qm = quant_tensor(p);

@@ -161,6 +161,17 @@ __global__ void __launch_bounds__(threads(G), 1) k_stream(Problem p, int stages)
         reinterpret_cast<volatile int *>(red_all + G * 2 * kConsumerWarps);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the first row's streams prefetched into L2 before the wait (L2 is the
+    // point of coherence: correct while the previous kernel still writes them)
+    if (p.l2_rows > 0 && threadIdx.x < ns && (int64_t)blockIdx.x < p.T) {
+        const int64_t t = blockIdx.x;
+        const T *src = reinterpret_cast<const T *>(p.src);
+        const void *row = threadIdx.x < ns - (OP == OP_PLAIN ? 0 : 1)
+                              ? static_cast<const void *>(src + threadIdx.x * p.slice + t * p.ldx)
+                              : static_cast<const void *>(reinterpret_cast<const T *>(p.residual) +
+                                                          t * p.ldr);
+        prefetch_l2(row, (uint32_t)row_bytes);
+    }
     grid_dependency_wait();
     if (threadIdx.x == 0) {
         for (int s = 0; s < G * stages; ++s) {
