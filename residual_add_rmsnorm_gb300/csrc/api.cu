@@ -877,10 +877,14 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     c.num_sms = d->num_sms;
     c.persistent = gp.persistent;
     c.pair = gp.pair;
-    // the launcher re-checks both against the clusters that fit on this GPU
-    c.fuse_norm = gp.fuse_norm || (gp.persistent && !(getenv("RARN_GEMM_FUSE") &&
-                                                      atoi(getenv("RARN_GEMM_FUSE")) == 0));
-    c.tail_split = !(getenv("RARN_GEMM_SPLIT") && atoi(getenv("RARN_GEMM_SPLIT")) == 0);
+    // allowed unless switched off for measurements; the launcher decides both
+    // against the clusters that fit on this GPU
+    auto env_off = [](const char *name) {
+        const char *v = getenv(name);
+        return v && atoi(v) == 0;
+    };
+    c.fuse_norm = !env_off("RARN_GEMM_FUSE");
+    c.tail_split = !env_off("RARN_GEMM_SPLIT");
     c.wait_limit_ns = 2000000000ull;
     c.stall_fill = -1;
     {

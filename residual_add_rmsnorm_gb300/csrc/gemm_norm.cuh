@@ -1040,8 +1040,7 @@ struct PairItem {
     int ncols;  // 256 or 128
 };
 
-__device__ __forceinline__ PairItem pair_item(int64_t item, int64_t full_items, int C) {
-    (void)C;
+__device__ __forceinline__ PairItem pair_item(int64_t item, int64_t full_items) {
     if (item < full_items) return PairItem{item, 0, kMmaN};
     const int64_t h = item - full_items;
     return PairItem{full_items + h / 2, (int)(h & 1) * (kMmaN / 2), kMmaN / 2};
@@ -1212,7 +1211,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             const uint32_t lead_full0 = map_to_rank(full0, 0);
             const uint64_t pol = l2_evict_last_policy();
             for (int64_t item = pair; item < items && !stop; item += npairs) {
-                const PairItem pi = pair_item(item, p.full_items, C);
+                const PairItem pi = pair_item(item, p.full_items);
                 const int m0 = (int)((pi.tile / C) * kPairBM + rank * kBM);
                 // this CTA's W rows: its half of the item's columns
                 const int n0 = (int)((pi.tile % C) * NS + pi.col0 + rank * (pi.ncols / 2));
@@ -1289,7 +1288,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         // warp half (warp - 2) / 4 takes half of the item's columns ----
         int it = 0;
         for (int64_t item = pair; item < items; item += npairs, ++it) {
-            const PairItem pi = pair_item(item, p.full_items, C);
+            const PairItem pi = pair_item(item, p.full_items);
             const int64_t m0 = (pi.tile / C) * kPairBM + rank * kBM;
             const uint32_t tbase =
                 tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + (it & 1) * NS;
@@ -1322,7 +1321,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             const int s = (int)(k % S);
             if (k >= kit) {
                 // the item of fill k: this pair's (k / KB)-th
-                const PairItem pi = pair_item(pair + (k / KB) * npairs, p.full_items, C);
+                const PairItem pi = pair_item(pair + (k / KB) * npairs, p.full_items);
                 mbar_arrive_expect_tx(smem_u32(&full[s]), Lay::a_bytes + pi.ncols / 2 * BK * 2);
             }
             wait_phase(smem_u32(&full[s]), (uint32_t)((k / S) & 1), abort_flag, p.watchdog,

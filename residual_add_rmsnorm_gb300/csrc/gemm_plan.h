@@ -27,8 +27,8 @@ struct GemmCall {
     int num_sms;
     bool persistent;     // the warp-specialised persistent kernel (256-column tiles)
     bool pair;           // ... on SM pairs: 256 x 256 tiles, cta_group::2 MMAs
-    bool fuse_norm;      // allow the persistent kernels to write y (no norm kernel)
-    bool tail_split;     // allow the pair kernel to split the last round's tiles
+    bool fuse_norm;      // the persistent kernels may write y (no norm kernel)
+    bool tail_split;     // the pair kernel may split the last round's tiles
     bool pdl;
     unsigned int *watchdog;
     unsigned long long wait_limit_ns;  // bound on every shared-memory barrier wait
