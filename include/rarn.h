@@ -277,10 +277,16 @@ rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows parti
  * other column tiles of its 128-row block (a counter per block in the
  * workspace, zeroed by a one-CTA kernel launched just before), sums each
  * row's partials in tile order and writes y; otherwise a norm kernel does
- * that last step.  Both orders give identical bits.  `workspace` is
- * caller-owned device memory of at least rarn_gemm_workspace_bytes(T, H)
- * bytes (16-byte aligned); its contents are scratch and need no
- * initialisation.
+ * that last step.  Both orders give identical bits.  With T <= 128 and
+ * K >= 1024 the product is split over K instead: up to 9 CTAs per column
+ * tile write binary32 partial products into the workspace and a CTA per row
+ * adds them in split order, adds the residual (one rounding) and normalises
+ * (a different binary32 summation order, within the same accuracy bound);
+ * this needs the full rarn_gemm_workspace_bytes(T, H) and a 32-byte aligned
+ * workspace, else the call runs without split K.  `workspace` is
+ * caller-owned device memory of at least the bytes the non-split kernels use
+ * (rarn_gemm_workspace_bytes for T > 128; 16-byte aligned); its contents are
+ * scratch and need no initialisation.
  *
  * Matrices are rarn_rows (row-major, row_stride in elements), all of one
  * 16-bit type (RARN_BF16 or RARN_F16; RARN_F32 returns UNSUPPORTED); gamma is
@@ -328,18 +334,21 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
  * with no ordering between them) race on it and give wrong results; issue
  * them on one stream or synchronise the streams.
  *
- * Arguments, results (bit-identical to the workspace form) and other errors
- * as for rarn_gemm_add_rms_norm; H beyond the supported tilings returns
- * RARN_ERR_UNSUPPORTED.
+ * Arguments and errors as for rarn_gemm_add_rms_norm; H beyond the supported
+ * tilings returns RARN_ERR_UNSUPPORTED.  Results are bit-identical to the
+ * workspace form, except for T <= 128 where the workspace form splits K and
+ * the scratch cannot hold the split's partial products (9 T H binary32
+ * values): this entry point then runs without split K, a different binary32
+ * summation order within the same accuracy bound.
  */
 rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w,
                                            rarn_rows residual, const void *gamma, int64_t T,
                                            int64_t H, int64_t K, float eps, void *stream);
 
 /* Workspace bytes rarn_gemm_add_rms_norm needs for T rows of H: one binary32
- * per row and column tile (H / 256 tiles, or H / 512 beyond 8192), rounded up
- * to 16 bytes, then one 32-bit counter per 128-row block; -1 if H is not
- * supported. */
+ * per row and 128 columns, rounded up to 16 bytes, then one 32-bit counter
+ * per 128-row block; for T <= 128 (H <= 8192) also, from the next 256-byte
+ * boundary, 9 T H binary32 values for split K.  -1 if H is not supported. */
 int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H);
 
 /* Describe the GEMM kernels' tiling for a problem (pure host logic). */

@@ -796,17 +796,20 @@ rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows parti
 // GEMM producer + fused residual-add RMSNorm: every matrix 16-bit, one type;
 // 16-byte aligned bases and row strides; the caller's workspace holds the
 // column tiles' partial sums of squares.
-static GemmPlan gemm_plan_env(int64_t T, int64_t H, int64_t K, int num_sms = 152) {
+static GemmPlan gemm_plan_env(int64_t T, int64_t H, int64_t K, int num_sms = 152,
+                              bool no_splitk = false) {
     int bk = 0, ns = 0, ctas = 0, persist = -1;  // measurements only
     if (const char *v = getenv("RARN_GEMM_BK")) bk = atoi(v);
     if (const char *v = getenv("RARN_GEMM_NS")) ns = atoi(v);
     if (const char *v = getenv("RARN_GEMM_CTAS")) ctas = atoi(v);
     if (const char *v = getenv("RARN_GEMM_PERSIST")) persist = atoi(v);
-    int pair = -1, fuse = -1, split = -1;
+    int pair = -1, fuse = -1, split = -1, splitk = -1;
     if (const char *v = getenv("RARN_GEMM_PAIR")) pair = atoi(v);
     if (const char *v = getenv("RARN_GEMM_FUSE")) fuse = atoi(v);
     if (const char *v = getenv("RARN_GEMM_SPLIT")) split = atoi(v);
-    return plan_gemm(T, H, K, bk, ns, ctas, persist, num_sms, pair, fuse, split);
+    if (const char *v = getenv("RARN_GEMM_SPLITK")) splitk = atoi(v);
+    if (no_splitk) splitk = 0;
+    return plan_gemm(T, H, K, bk, ns, ctas, persist, num_sms, pair, fuse, split, splitk);
 }
 
 int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H) {
@@ -829,9 +832,13 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
         return RARN_ERR_INVALID_ARG;
     if (dt == RARN_F32) return RARN_ERR_UNSUPPORTED;  // the tensor path takes 16-bit operands
     if (T > (int64_t(1) << 31) - 128 || K > (int64_t(1) << 31) - 64) return RARN_ERR_UNSUPPORTED;
-    const GemmPlan gp = gemm_plan_env(T, H, K);
+    GemmPlan gp = gemm_plan_env(T, H, K);
     if (gp.ns == 0) return RARN_ERR_UNSUPPORTED;
-    const int64_t ws = gemm_workspace_bytes_for(T, H);
+    // split K only where the workspace holds its partial products
+    if (gp.splitk && ((int64_t)workspace_bytes < gemm_splitk_bytes(T, H, gp.splitk) ||
+                      (reinterpret_cast<uintptr_t>(workspace) & 31u)))
+        gp = gemm_plan_env(T, H, K, 152, /*no_splitk=*/true);
+    const int64_t ws = gp.splitk ? gemm_splitk_bytes(T, H, gp.splitk) : gemm_workspace_bytes_for(T, H);
     if ((int64_t)workspace_bytes < ws || (reinterpret_cast<uintptr_t>(workspace) & 15u))
         return RARN_ERR_INVALID_ARG;
     auto al16 = [](const void *ptr, int64_t ld) { return aligned16(ptr) && (ld * 2) % 16 == 0; };
@@ -877,6 +884,8 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     c.num_sms = d->num_sms;
     c.persistent = gp.persistent;
     c.pair = gp.pair;
+    c.splitk = gp.splitk;
+    c.part = gp.splitk ? static_cast<float *>(workspace) + gemm_splitk_offset(T, H) : nullptr;
     // allowed unless switched off for measurements; the launcher decides both
     // against the clusters that fit on this GPU
     auto env_off = [](const char *name) {
@@ -938,6 +947,14 @@ rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, char 
     if (gp.ns == 0) {
         snprintf(out, cap, "none: unsupported shape or type");
         return RARN_ERR_UNSUPPORTED;
+    }
+    if (gp.splitk) {
+        snprintf(out, cap,
+                 "gemm.tcgen05 cols_per_cta=%d col_tiles=%d bk=%d stages=%d smem=%d grid=%lld "
+                 "kblocks=%lld splitk=%d + split-K sum and norm",
+                 gp.ns, gp.tiles_n, gp.bk, gp.stages, gp.smem, (long long)gp.grid,
+                 (long long)((K + gp.bk - 1) / gp.bk), gp.splitk);
+        return RARN_OK;
     }
     snprintf(out, cap,
              "gemm.tcgen05 cols_per_cta=%d col_tiles=%d bk=%d stages=%d smem=%d grid=%lld "

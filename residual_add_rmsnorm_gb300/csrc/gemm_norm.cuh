@@ -93,6 +93,11 @@ struct Params {
     // the pair kernel's items: tiles [0, full_items) whole, then the
     // remaining tiles as two 128-column halves each (items in all)
     int64_t full_items, items;
+    // split K (T <= 128): CTA (tile n, split s) multiplies K slabs
+    // [s * kb_per_split, ...) and writes its binary32 partial products to
+    // part[s][row][column]
+    float *part;
+    int splits, kb_per_split;
     void *y;
     int64_t ldy;
     const void *gamma;
@@ -1334,6 +1339,208 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512)
                      : "memory");
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Split K for few rows (T <= 128, a single 128-row block): with only H / 256
+// column tiles the tiled kernels would stream W through as many SMs; here
+// CTA (n, s) of a C x splits grid multiplies the K slabs of split s for
+// column tile n (4-stage TMA ring, M = 128, N = 256 MMAs into TMEM, as
+// k_gemm_res) and writes its binary32 partial products for the live rows.
+// k_splitk_norm then adds the splits in order, adds the residual (one
+// rounding), and normalises.
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_splitk(const __grid_constant__ CUtensorMap map_a,
+                  const __grid_constant__ CUtensorMap map_w, Params p) {
+    constexpr int BK = 64, NS = kMmaN, S = 4;
+    constexpr int kRowBytes = BK * 2;
+    constexpr Layout L = layout(S, NS, BK);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.ctl_off);
+    uint64_t *empty = full + S;
+    uint64_t *accum = empty + S;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(accum + 1 + kMaxChunks);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntile = (int)(blockIdx.x % p.C);
+    const int split = (int)(blockIdx.x / p.C);
+    const int n0 = ntile * NS;
+    const int kb0 = split * p.kb_per_split;
+    const int kb1 = min(p.kblocks, kb0 + p.kb_per_split);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
+        }
+        mbar_init(smem_u32(accum), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_slot)),
+                     "r"(NS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    grid_dependency_wait();  // A and W may come from the previous kernel
+
+    int issued = 0;  // producer: fills issued
+    if (warp == 0 && lane == 0) {
+        // ---- TMA producer ----
+        uint32_t s = 0, ph = 0;
+        for (int kb = kb0; kb < kb1; ++kb, ++issued) {
+            if (issued >= S && !wait_phase(smem_u32(&empty[s]), ph ^ 1u, abort_flag, p.watchdog,
+                                           p.wait_limit_ns))
+                break;
+            const uint32_t fb = smem_u32(&full[s]);
+            mbar_arrive_expect_tx(
+                fb, L.stage_bytes + (blockIdx.x == 0 && issued == p.stall_fill ? 16u : 0u));
+            const uint32_t sa = smem_u32(smem + s * L.stage_bytes);
+            tma_load_2d(sa, &map_a, kb * BK, 0, fb);
+            tma_load_2d(sa + L.a_bytes, &map_w, kb * BK, n0, fb);
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ---- MMA issuer ----
+        const uint32_t idesc = instr_desc<T>();
+        const uint64_t adesc0 = smem_desc(smem_u32(smem), kRowBytes);
+        const uint64_t bdesc0 = smem_desc(smem_u32(smem) + L.a_bytes, kRowBytes);
+        constexpr uint32_t kStageDesc = L.stage_bytes >> 4;
+        uint32_t s = 0, ph = 0;
+        for (int kb = kb0; kb < kb1; ++kb) {
+            if (!wait_phase(smem_u32(&full[s]), ph, abort_flag, p.watchdog, p.wait_limit_ns))
+                break;
+            tmem_fence_after();
+            const uint64_t ad = adesc0 + s * kStageDesc, bd = bdesc0 + s * kStageDesc;
+            mma_f16(tmem, ad, bd, idesc, kb != kb0);
+#pragma unroll
+            for (int kk = 1; kk < BK / kMmaK; ++kk)
+                mma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
+            mma_commit(smem_u32(&empty[s]));
+            if (++s == S) {
+                s = 0;
+                ph ^= 1u;
+            }
+        }
+        mma_commit(smem_u32(accum));  // arrives once every MMA issued has completed
+    }
+    __syncwarp();
+
+    // ---- epilogue: thread i = row i; live rows write their partial products ----
+    wait_phase(smem_u32(accum), 0, abort_flag, p.watchdog, p.wait_limit_ns, true);
+    tmem_fence_after();
+    __syncthreads();
+    const bool ok = !*abort_flag;
+    grid_launch_dependents();
+    const int r = threadIdx.x;
+    const uint32_t tbase = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    float *dst = p.part + ((int64_t)split * p.T + r) * p.H + n0;
+    for (int c = 0; c < NS; c += 32) {
+        float v[32];
+        tmem_ld32(tbase + c, v);  // warp-wide: every lane takes part
+        if (ok && r < p.T) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 a = make_uint4(__float_as_uint(v[8 * q]), __float_as_uint(v[8 * q + 1]),
+                                           __float_as_uint(v[8 * q + 2]),
+                                           __float_as_uint(v[8 * q + 3]));
+                const uint4 b = make_uint4(
+                    __float_as_uint(v[8 * q + 4]), __float_as_uint(v[8 * q + 5]),
+                    __float_as_uint(v[8 * q + 6]), __float_as_uint(v[8 * q + 7]));
+                st_global32(dst + c + 8 * q, a, b);
+            }
+        }
+    }
+    if (threadIdx.x == 0 && *abort_flag) {
+        // after an abort, the fills issued land before this CTA's memory goes
+        // away (bounded)
+        for (int k = issued - S > 0 ? issued - S : 0; k < issued; ++k)
+            wait_phase(smem_u32(&full[k % S]), (uint32_t)((k / S) & 1), abort_flag, p.watchdog,
+                       p.wait_limit_ns, true);
+    }
+    tmem_fence_before();
+    __syncthreads();
+    tmem_fence_after();
+    if (warp == 0) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NS)
+                     : "memory");
+    }
+}
+
+// The split-K sum and the fused residual-add RMSNorm: a CTA per row, VPT
+// 8-column packs per thread.  P = ((p_0 + p_1) + ...) + p_{S-1} in binary32,
+// h = RN(P + r) (one rounding), the residual updated, Σh² over the CTA, y from
+// the h held in registers.
+template <typename T, int VPT>
+__global__ void __launch_bounds__(256) k_splitk_norm(NormParams q, const float *part, int splits,
+                                                      void *residual) {
+    __shared__ float red[32];
+    const int nv = (int)(q.H / 8);
+    const int64_t t = blockIdx.x;
+    grid_dependency_wait();
+    grid_launch_dependents();
+    T *res = reinterpret_cast<T *>(residual) + t * q.ldh;
+    uint4 hv[VPT];
+    float ss = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = threadIdx.x + k * blockDim.x;
+        if (j < nv) {
+            float acc[8];
+            const float *src = part + t * q.H + (int64_t)j * 8;
+            const Pack32 p0 = ld_stream32(src);
+            acc[0] = __uint_as_float(p0.a.x), acc[1] = __uint_as_float(p0.a.y);
+            acc[2] = __uint_as_float(p0.a.z), acc[3] = __uint_as_float(p0.a.w);
+            acc[4] = __uint_as_float(p0.b.x), acc[5] = __uint_as_float(p0.b.y);
+            acc[6] = __uint_as_float(p0.b.z), acc[7] = __uint_as_float(p0.b.w);
+            for (int s = 1; s < splits; ++s) {
+                const Pack32 ps = ld_stream32(src + (int64_t)s * q.T * q.H);
+                acc[0] += __uint_as_float(ps.a.x), acc[1] += __uint_as_float(ps.a.y);
+                acc[2] += __uint_as_float(ps.a.z), acc[3] += __uint_as_float(ps.a.w);
+                acc[4] += __uint_as_float(ps.b.x), acc[5] += __uint_as_float(ps.b.y);
+                acc[6] += __uint_as_float(ps.b.z), acc[7] += __uint_as_float(ps.b.w);
+            }
+            float f[8];
+            DT<T>::unpack(ld_stream(res + (int64_t)j * 8), f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                f[e] = DT<T>::round(acc[e] + f[e]);  // h: one rounding of P + r
+                ss += f[e] * f[e];
+            }
+            hv[k] = DT<T>::pack(f);
+            st_global(res + (int64_t)j * 8, hv[k]);
+        }
+    }
+    const float inv = rsqrtf(block_sum(ss, red) / (float)q.H + q.eps);
+    T *y = reinterpret_cast<T *>(q.y) + t * q.ldy;
+    const T *g = reinterpret_cast<const T *>(q.gamma);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int j = threadIdx.x + k * blockDim.x;
+        if (j < nv) {
+            float f[8], w[8];
+            DT<T>::unpack(hv[k], f);
+            DT<T>::unpack(ld_keep(g + (int64_t)j * 8), w);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = (f[e] * inv) * w[e];
+            st_global(y + (int64_t)j * 8, DT<T>::pack(f));
+        }
     }
 }
 

@@ -194,9 +194,67 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
                          c.pdl, 1, q);
 }
 
+// Split K (T <= 128): C x splits CTAs write binary32 partial products, then a
+// CTA per row sums them in split order, adds the residual and normalises.
+template <typename T>
+static cudaError_t launch_gemm_splitk(const GemmCall &c, cudaStream_t st) {
+    using namespace gemm;
+    const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+    CUtensorMap ma, mw;
+    if (!encode_map(&ma, c.a, c.T, c.K, c.lda, kBM, 64, bf16) ||
+        !encode_map(&mw, c.w, c.H, c.K, c.ldw, kMmaN, 64, bf16))
+        return cudaErrorInvalidValue;
+    Params p{};
+    p.T = c.T;
+    p.H = c.H;
+    p.K = c.K;
+    p.ns = kMmaN;
+    p.C = static_cast<int>(c.H / kMmaN);
+    p.stages = 4;
+    p.kblocks = static_cast<int>((c.K + 63) / 64);
+    p.watchdog = c.watchdog;
+    p.wait_limit_ns = c.wait_limit_ns;
+    p.stall_fill = c.stall_fill;
+    p.part = c.part;
+    p.kb_per_split = (p.kblocks + c.splitk - 1) / c.splitk;
+    // splits that hold K slabs (ceil(kblocks / per split) <= splitk)
+    const int used = (p.kblocks + p.kb_per_split - 1) / p.kb_per_split;
+    p.splits = used;
+    auto kernel = k_gemm_splitk<T>;
+    constexpr int smem = layout(4, kMmaN, 64).total;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = launch_kernel(kernel, dim3(static_cast<unsigned>(p.C * used)), dim3(kThreads),
+                          static_cast<size_t>(smem), st, c.pdl, 1, ma, mw, p);
+    if (e != cudaSuccess) return e;
+    NormParams q{};
+    q.y = c.y;
+    q.h = c.residual;
+    q.gamma = c.gamma;
+    q.T = c.T;
+    q.H = c.H;
+    q.ldh = c.ldr;
+    q.ldy = c.ldy;
+    q.eps = c.eps;
+    const int nv = static_cast<int>(c.H / 8);
+    const dim3 g2(static_cast<unsigned>(c.T));
+    if (nv <= 256)
+        return launch_kernel(k_splitk_norm<T, 1>, g2, dim3((nv + 31) / 32 * 32), 0, st, c.pdl, 1, q,
+                             static_cast<const float *>(c.part), used, c.residual);
+    if (nv <= 512)
+        return launch_kernel(k_splitk_norm<T, 2>, g2, dim3(256), 0, st, c.pdl, 1, q,
+                             static_cast<const float *>(c.part), used, c.residual);
+    return launch_kernel(k_splitk_norm<T, 4>, g2, dim3(256), 0, st, c.pdl, 1, q,
+                         static_cast<const float *>(c.part), used, c.residual);
+}
+
 template <typename T>
 cudaError_t launch_gemm_norm(const GemmCall &c, cudaStream_t st) {
     if (c.T == 0) return cudaSuccess;
+    if (c.splitk >= 2) {
+        const cudaError_t e = launch_gemm_splitk<T>(c, st);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     const cudaError_t e = c.bk == 64 ? launch_gemm_bk<T, 64>(c, st) : launch_gemm_bk<T, 32>(c, st);
     return e != cudaSuccess ? e : cudaGetLastError();
 }

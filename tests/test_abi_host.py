@@ -333,8 +333,12 @@ def test_gemm_form_argument_errors(lib):
     assert call(y, a, w, r, None, T, H, K, 1e-6) == INVALID                  # null gamma
     assert call(y, a, w, r, g, T, H, K, 1e-6, wsp=None) == INVALID           # no workspace
     need = lib.rarn_gemm_workspace_bytes(T, H)
-    assert need == (T * (H // 128) + 1) * 4   # partial sums, then one row-block counter
-    assert call(y, a, w, r, g, T, H, K, 1e-6, wsn=need - 4) == INVALID      # short workspace
+    # partial sums [T][H / 128], one row-block counter, then (T <= 128) room for
+    # split K: 9 x T x H binary32 partial products from a 256-byte boundary
+    base = (T * (H // 128) + 1) * 4
+    assert need == ((base // 4 + 63) // 64 * 64 + 9 * T * H) * 4
+    # less than the split-K room only turns split K off; less than the base fails
+    assert call(y, a, w, r, g, T, H, K, 1e-6, wsn=base - 4) == INVALID      # short workspace
     assert call(y, a, w, r, g, T, H, K, 1e-6, wsp=ws + 8) == INVALID         # not 16-byte aligned
     assert call(_rows(A, 300, BF16), a, _rows(C, K, BF16), _rows(D, 300, BF16), g, T, 300, K,
                 1e-6) == UNSUPPORTED                                         # H = 300
@@ -366,15 +370,28 @@ def test_plan_gemm(monkeypatch):
     assert "cols_per_cta=256 col_tiles=16 bk=64 stages=4" in p and "grid=152" in p, p
     assert "kblocks=64 persistent=1 pair=0" in p, p
     monkeypatch.delenv("RARN_GEMM_PAIR")
-    p = rarn.plan_gemm(100, 768, 1000)     # one 128-row block: no pair
-    assert "cols_per_cta=256 col_tiles=3" in p and "persistent=1" in p and "grid=3" in p, p
+    p = rarn.plan_gemm(200, 768, 1000)     # two 128-row blocks: one SM per tile
+    assert "cols_per_cta=256 col_tiles=3" in p and "persistent=1" in p and "grid=6" in p, p
     assert "pair=0" in p, p
+    # one 128-row block: K split over the idle SMs, at least 8 K slabs each, at
+    # most 9 splits
+    p = rarn.plan_gemm(100, 768, 1000)
+    assert "col_tiles=3" in p and "splitk=2" in p and "grid=6" in p, p
+    p = rarn.plan_gemm(1, 4096, 4096)
+    assert "col_tiles=16" in p and "splitk=8" in p and "grid=128" in p, p
+    p = rarn.plan_gemm(16, 2048, 8192)
+    assert "splitk=9" in p and "grid=72" in p, p
+    monkeypatch.setenv("RARN_GEMM_SPLITK", "0")
+    assert "persistent=1" in rarn.plan_gemm(1, 4096, 4096)
+    monkeypatch.delenv("RARN_GEMM_SPLITK")
     p = rarn.plan_gemm(8, 16384, 64)   # beyond 32 tiles of 256: 512-column tiles
     assert "cols_per_cta=512 col_tiles=32 bk=32 stages=5" in p and "persistent=0" in p, p
     assert rarn.plan_gemm(8, 300, 64).startswith("none")
     assert rarn.plan_gemm(8, 16896, 64).startswith("none")   # 33 x 512: beyond 32 tiles
     assert rarn.plan_gemm(8, 4096, 64, "f32").startswith("none")
-    # partial sums [T][H / 128], then one counter per 128-row block (16-byte aligned)
+    # partial sums [T][H / 128], then one counter per 128-row block (16-byte
+    # aligned); up to 128 rows also room for 9-way split K
     assert rarn.gemm_workspace_bytes(4096, 4096) == (4096 * 32 + 32) * 4
-    assert rarn.gemm_workspace_bytes(1, 768) == (8 + 1) * 4
+    assert rarn.gemm_workspace_bytes(1, 768) == (64 + 9 * 768) * 4
+    assert rarn.gemm_workspace_bytes(129, 768) == ((129 * 6 + 3) // 4 * 4 + 2) * 4
     assert rarn.gemm_workspace_bytes(7, 300) == -1

@@ -132,7 +132,9 @@ def run_case(T, H, K, dt="bf16", seed=0, lda=None, ldw=None, ldr=None, ldy=None,
 def test_gemm_parity(T, H, K, dt):
     plan = run_case(T, H, K, dt, seed=T + H + K)
     assert plan.startswith("gemm.tcgen05"), plan
-    assert ("persistent=1" in plan) == (H <= 8192 and K >= 512), plan
+    splitk = H <= 8192 and T <= 128 and K >= 1024
+    assert ("splitk=" in plan) == splitk, plan
+    assert ("persistent=1" in plan) == (H <= 8192 and K >= 512 and not splitk), plan
     assert ("pair=1" in plan) == (H <= 8192 and K >= 512 and T >= 2048), plan
 
 
@@ -235,6 +237,32 @@ def test_gemm_pair_tail_halves(monkeypatch):
             f"T{T} H{H} K{K}: {int(dy.sum())} y / {int(dr.sum())} residual elements differ; "
             f"rows {rows_y[:4]}..{rows_y[-4:]} ({len(rows_y)}), cols {cols_y[:4]}..{cols_y[-4:]} "
             f"({len(cols_y)})")
+
+
+@pytest.mark.parametrize("T,H,K,dt", [
+    (1, 4096, 4096, "bf16"),    # decode: 16 column tiles x 8 splits
+    (16, 768, 1000, "bf16"),    # ragged K, 2 splits
+    (100, 2048, 4096, "f16"),   # 8 splits of 8 slabs
+    (128, 8192, 2048, "bf16"),  # 32 column tiles x 4 splits
+    (5, 2048, 8192, "bf16"),    # 9 splits (the most), 15 slabs each, the last 8
+])
+def test_gemm_splitk(T, H, K, dt):
+    """Split K for a single 128-row block (T <= 128): C x splits CTAs write
+    binary32 partial products, a CTA per row adds them in split order, adds
+    the residual (one rounding) and normalises; against the oracle with the
+    accumulation bound (at most 8 extra binary32 additions per element)."""
+    plan = run_case(T, H, K, dt, seed=T * 7 + K)
+    assert "splitk=" in plan, plan
+
+
+def test_gemm_splitk_off_matches_oracle_too(monkeypatch):
+    """The same single-row-block shapes without split K (the persistent
+    kernel): both stay within the bound; split K is a different, equally
+    valid binary32 summation order."""
+    monkeypatch.setenv("RARN_GEMM_SPLITK", "0")
+    for T, H, K in ((1, 4096, 4096), (100, 2048, 4096)):
+        plan = run_case(T, H, K, "bf16", seed=T * 7 + K)
+        assert "splitk=" not in plan and "persistent=1" in plan, plan
 
 
 def test_gemm_strides():

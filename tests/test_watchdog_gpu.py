@@ -36,18 +36,20 @@ def test_wait_runs_out_and_is_reported(fill):
     assert rarn.watchdog(clear=True) == 0
 
 
-@pytest.mark.parametrize("K,fill,pair", [(1024, 0, "1"), (1024, 9, "1"), (1024, 0, "0"),
-                                         (1024, 9, "0"), (256, 0, None), (256, 2, None)])
-def test_gemm_wait_runs_out_and_is_reported(K, fill, pair, monkeypatch):
+@pytest.mark.parametrize("K,fill,pair,T", [(1024, 0, "1", 1000), (1024, 9, "1", 1000),
+                                           (1024, 0, "0", 1000), (1024, 9, "0", 1000),
+                                           (256, 0, None, 1000), (256, 2, None, 1000),
+                                           (2048, 0, None, 64), (2048, 5, None, 64)])
+def test_gemm_wait_runs_out_and_is_reported(K, fill, pair, T, monkeypatch):
     """The GEMM form (persistent kernel for K = 1024, on SM pairs or on one SM
-    per tile; two CTAs per SM for K = 256): one ring fill of CTA 0 never
-    completes; every role's wait gives up within the limit, the CTA (or the
-    pair) drains what it issued and frees its tensor memory, the watchdog bit
-    is set, and the next call is correct."""
+    per tile; two CTAs per SM for K = 256; split K for 64 rows): one ring
+    fill of CTA 0 never completes; every role's wait gives up within the
+    limit, the CTA (or the pair) drains what it issued and frees its tensor
+    memory, the watchdog bit is set, and the next call is correct."""
     import torch
     if pair is not None:
         monkeypatch.setenv("RARN_GEMM_PAIR", pair)
-    T, H = 1000, 2048
+    H = 2048
     gen = torch.Generator(device="cuda").manual_seed(K + fill)
     a = torch.randn(T, K, device="cuda", generator=gen).to(torch.bfloat16)
     w = (torch.randn(H, K, device="cuda", generator=gen) / K ** 0.5).to(torch.bfloat16)

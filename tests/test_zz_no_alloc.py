@@ -17,6 +17,7 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("T,H,K", [
+    (8, 4096, 4096),     # split K: its partial products fit the scratch too
     (300, 1024, 512),
     (4096, 4096, 1024),
     (40000, 8192, 64),   # 32 column tiles: more rows than the scratch holds (two launch pairs)
