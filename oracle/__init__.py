@@ -84,6 +84,9 @@ class Oracle:
         lib.oracle_rows_fp8.argtypes = [c_int, c_int, i64, i64, i32, p, i64, i64, p, i64, p, f32,
                                         c_int, f32, p, i64, p, p]
         lib.oracle_rows_fp8.restype = c_int
+        lib.oracle_reduce_fp8in.argtypes = [c_int, c_int, i64, i64, i32, p, p, p, p, f32, p, p, p,
+                                            p, c_int]
+        lib.oracle_reduce_fp8in.restype = c_int
         lib.oracle_decode_fp8.argtypes = [c_int, p, p, i64]
         lib.oracle_decode_fp8.restype = c_int
         lib.oracle_round_fp8.argtypes = [c_int, p, p, i64]
@@ -194,6 +197,27 @@ class Oracle:
                                         _ptr(u64)))
         return codes.reshape(T, ldq), rs, u64
 
+    def reduce_fp8in(self, codes, scales, residual, gamma, eps, dtype, fmt, *, want_y64=False,
+                     threads=0) -> Result:
+        """Reduce + residual + RMSNorm over R partials of 8-bit codes
+        (``codes`` uint8 [R, T, H], ``fmt`` "e4m3" / "e5m2") with one binary32
+        scale per partial (``scales`` [R])."""
+        codes = np.ascontiguousarray(codes, np.uint8)
+        scales = np.ascontiguousarray(scales, np.float32)
+        residual = self._as_storage(residual, dtype)
+        gamma = self._as_storage(gamma, dtype)
+        R, T, H = codes.shape
+        if scales.shape != (R,) or residual.shape != (T, H):
+            raise ValueError("shape mismatch")
+        y = np.zeros_like(residual)
+        res_out = np.zeros_like(residual)  # zeros: a row never stored shows
+        inv = np.empty(T, np.float64)
+        y64 = np.empty((T, H), np.float64) if want_y64 else None
+        n = _check(self.lib.oracle_reduce_fp8in(
+            DTYPES[dtype], FP8[fmt], T, H, R, _ptr(codes), _ptr(scales), _ptr(residual),
+            _ptr(gamma), float(eps), _ptr(res_out), _ptr(y), _ptr(inv), _ptr(y64), threads))
+        return Result(y, res_out, inv, y64, n)
+
     def decode_fp8(self, codes, fmt) -> np.ndarray:
         """8-bit codes -> binary64 values (the oracle's own decoder)."""
         codes = np.ascontiguousarray(codes, np.uint8)
@@ -276,6 +300,10 @@ def rows_ex(*a, **k) -> Result:
 
 def rows_fp8(*a, **k):
     return default().rows_fp8(*a, **k)
+
+
+def reduce_fp8in(*a, **k) -> Result:
+    return default().reduce_fp8in(*a, **k)
 
 
 def gemm_add_rms_norm(*a, **k) -> Result:

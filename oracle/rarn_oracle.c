@@ -44,6 +44,15 @@
  * pages give no formula for the scale; this is the plainest reading of a
  * per-row (dynamic) scale.
  *
+ * 8-bit partials (oracle_reduce_fp8in): the reduce form with each partial
+ * given as e4m3 / e5m2 codes c_r and a binary32 scale s_r per partial buffer
+ * ("Block All Reduce", FP8 section: reductions over 8-bit inputs with a
+ * binary32 accumulator).  Its value enters the sum as fl32(dec(c_r) * s_r),
+ * one binary32 rounding of the product; then acc = that value for r = 0,
+ * acc = fl32(acc + fl32(dec(c_r) * s_r)) for r = 1 .. R-1, acc = fl32(acc +
+ * r_i), h_i = RN_dt(acc), and steps 2-4 as above.  The pages fix no scale
+ * rule; a per-buffer (per-tensor) scale is the plainest reading.
+ *
  * Build flags must keep binary32 arithmetic exact IEEE: no -ffast-math, and
  * -ffp-contract=off (there is no multiply in the binary32 part, but the flag
  * documents the intent).
@@ -465,6 +474,64 @@ int oracle_rows_fp8(int dt, int fmt, int64_t T, int64_t H, int32_t R, const void
     free(h);
     free(v);
     return 1;
+}
+
+/* Reduce + residual + RMSNorm over R partials of 8-bit codes (dense
+ * [R, T, H]) with one binary32 scale per partial; residual [T, H] of type dt
+ * updated in residual_out; y, gamma of type dt. */
+typedef struct {
+    int dt, fmt;
+    int64_t T, H;
+    int32_t R;
+    const uint8_t *codes;
+    const float *scales;
+    const void *residual_in;
+    const void *gamma;
+    float eps;
+    void *residual_out;
+    void *y;
+    double *inv_out;
+    double *y64_out;
+} fp8in_job_t;
+
+static void fp8in_row(const void *ctx, int64_t t, double *h) {
+    const fp8in_job_t *j = (const fp8in_job_t *)ctx;
+    const fp8_format *f = &FP8[j->fmt];
+    const int64_t H = j->H, row = t * H;
+    for (int64_t i = 0; i < H; ++i) {
+        /* each dequantised partial: one binary32 rounding of code * scale */
+        float acc = (float)decode_fp8(f, j->codes[row + i]) * j->scales[0];
+        for (int32_t r = 1; r < j->R; ++r) {
+            const float v = (float)decode_fp8(f, j->codes[(int64_t)r * j->T * H + row + i]) *
+                            j->scales[r];
+            acc = acc + v;
+        }
+        acc = acc + (float)load_elem(j->dt, j->residual_in, row + i);
+        h[i] = round_dt(j->dt, (double)acc);
+    }
+    if (j->residual_out)
+        for (int64_t i = 0; i < H; ++i) store_exact(j->dt, j->residual_out, row + i, h[i]);
+    double ss = 0.0;
+    for (int64_t i = 0; i < H; ++i) ss += h[i] * h[i];
+    const double inv = 1.0 / sqrt(ss / (double)H + (double)j->eps);
+    if (j->inv_out) j->inv_out[t] = inv;
+    for (int64_t i = 0; i < H; ++i) {
+        const double v = (h[i] * inv) * load_elem(j->dt, j->gamma, i);
+        if (j->y64_out) j->y64_out[row + i] = v;
+        store_exact(j->dt, j->y, row + i, round_dt(j->dt, v));
+    }
+}
+
+int oracle_reduce_fp8in(int dt, int fmt, int64_t T, int64_t H, int32_t R, const uint8_t *codes,
+                        const float *scales, const void *residual_in, const void *gamma, float eps,
+                        void *residual_out, void *y, double *inv_out, double *y64_out,
+                        int nthreads) {
+    if (T < 0 || H <= 0 || R < 1 || (fmt != 0 && fmt != 1) || !codes || !scales ||
+        !residual_in || !gamma || !y)
+        return -2;
+    fp8in_job_t j = {dt, fmt, T, H, R, codes, scales, residual_in, gamma, eps,
+                     residual_out, y, inv_out, y64_out};
+    return run_rows(&j, fp8in_row, T, H, nthreads);
 }
 
 int oracle_decode_fp8(int fmt, const uint8_t *src, double *dst, int64_t n) {

@@ -17,7 +17,9 @@ What the pins rest on (none of it is the oracle's own code):
     nearest search over the code table;
   * for the GEMM producer, numpy's binary64 matrix product, the identity
     weight (reduces to the fused form), a constructed single-rounding case and
-    exact rational brute force.
+    exact rational brute force;
+  * for the 8-bit partials, the pinned reduce over the same values (power-of-
+    two scales, torch's float8 decoders) and exact rational brute force.
 """
 from __future__ import annotations
 
@@ -829,6 +831,69 @@ def pin_gemm_strides(O):
         assert np.array_equal(pad, np.full_like(pad, GARBAGE[dt])), dt
 
 
+# ---------------------------------------------------------------------------
+# Pins on the 8-bit partials (reduce over e4m3 / e5m2 codes with a scale each)
+# ---------------------------------------------------------------------------
+
+def _finite_codes(rng, fmt, shape, top=None):
+    """Random codes of finite values (optionally |value| <= top), both signs."""
+    vals, codes = _fp8_table(fmt)
+    pick = codes if top is None else codes[vals <= top]
+    c = rng.choice(pick, size=shape).astype(np.uint8)
+    return c | (rng.integers(0, 2, size=shape, dtype=np.uint8) << 7)
+
+
+def pin_fp8in_power_of_two_scales_are_reduce(O):
+    """With power-of-two scales every dequantised partial code * 2^k is exact,
+    so the 8-bit form must equal the (pinned) 16-bit / binary32 reduce over
+    partials holding those values, bit for bit, residual and y; the values
+    come from torch's float8 decoders, not the oracle's."""
+    rng = np.random.default_rng(21)
+    for dt in ("bf16", "f16", "f32"):
+        for fmt in ("e4m3", "e5m2"):
+            R, T, H = 5, 3, 70
+            top = 448.0 if fmt == "e4m3" else (4096.0 if dt == "f16" else None)
+            codes = _finite_codes(rng, fmt, (R, T, H), top)
+            ks = rng.integers(-3, 4, size=R) if dt != "f16" else rng.integers(-3, 1, size=R)
+            scales = np.exp2(ks).astype(np.float32)
+            r = _rand_bits(rng, (T, H), dt)
+            g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+            vals = lib_decode_fp8(codes, fmt) * scales[:, None, None].astype(np.float64)
+            p16 = bits_of(vals, dt).reshape(R, T, H)
+            assert np.array_equal(lib_decode(p16, dt), vals), (dt, fmt)  # exact in dt
+            got = O.reduce_fp8in(codes, scales, r, g, 1e-6, dt, fmt)
+            want = O.reduce_add_rms_norm(p16, r, g, 1e-6, dt)
+            assert np.array_equal(got.residual, want.residual), (dt, fmt)
+            assert np.array_equal(got.y, want.y), (dt, fmt)
+
+
+def pin_fp8in_brute_force(O):
+    """Arbitrary scales: each partial enters as code * scale rounded once to
+    binary32, summed in order p0 .. p{R-1}, then the residual, each add in
+    binary32, one rounding to the storage type -- in exact rationals."""
+    rng = np.random.default_rng(22)
+    for dt in ("bf16", "f16", "f32"):
+        for fmt in ("e4m3", "e5m2"):
+            R, T, H = 4, 2, 11
+            codes = _finite_codes(rng, fmt, (R, T, H), 448.0)
+            scales = rng.uniform(1e-3, 3.0, size=R).astype(np.float32)
+            r = _rand_bits(rng, (T, H), dt)
+            res = O.reduce_fp8in(codes, scales, r, bits_of(np.ones(H), dt), 1e-6, dt, fmt)
+            dec = lib_decode_fp8(codes, fmt)
+            rv = lib_decode(r, dt)
+            want = np.empty((T, H))
+            for t in range(T):
+                for i in range(H):
+                    v = [Fraction(rn_exact(Fraction(dec[k, t, i]) * Fraction(float(scales[k])),
+                                           "f32")) for k in range(R)]
+                    acc = v[0]
+                    for k in range(1, R):
+                        acc = Fraction(rn_exact(acc + v[k], "f32"))
+                    acc = Fraction(rn_exact(acc + Fraction(rv[t, i]), "f32"))
+                    want[t, i] = rn_exact(acc, dt)
+            assert np.array_equal(lib_decode(res.residual, dt), want), (dt, fmt)
+
+
 ALL_PINS = [
     pin_decode_all_patterns,
     pin_round_matches_library,
@@ -857,4 +922,6 @@ ALL_PINS = [
     pin_gemm_one_rounding,
     pin_gemm_brute_force_tiny,
     pin_gemm_strides,
+    pin_fp8in_power_of_two_scales_are_reduce,
+    pin_fp8in_brute_force,
 ]

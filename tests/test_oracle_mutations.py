@@ -101,6 +101,21 @@ MUTATIONS = {
     "gemm_residual_not_stored": (
         "for (int64_t i = 0; i < H; ++i) store_exact(g->dt, g->residual, t * g->ldr + i, h[i]);",
         ""),
+    # 8-bit partials: scale dropped / one scale for all / scale after the sum,
+    # wrong partial stride, binary64 accumulator, the other format, residual
+    # dropped or not stored
+    "fp8in_no_scale": ("float acc = (float)decode_fp8(f, j->codes[row + i]) * j->scales[0];",
+                       "float acc = (float)decode_fp8(f, j->codes[row + i]);"),
+    "fp8in_scale0_for_all": ("j->scales[r];", "j->scales[0];"),
+    "fp8in_partial_stride": ("j->codes[(int64_t)r * j->T * H + row + i]",
+                             "j->codes[(int64_t)r * H + row + i]"),
+    "fp8in_wide_accumulator": ("float acc = (float)decode_fp8", "double acc = (float)decode_fp8"),
+    "fp8in_other_format": ("const fp8_format *f = &FP8[j->fmt];",
+                           "const fp8_format *f = &FP8[1 - j->fmt];"),
+    "fp8in_no_residual": ("acc = acc + (float)load_elem(j->dt, j->residual_in, row + i);", ""),
+    "fp8in_residual_not_stored": (
+        "if (j->residual_out)\n        for (int64_t i = 0; i < H; ++i) store_exact(j->dt, "
+        "j->residual_out, row + i, h[i]);", ""),
     "gemm_gamma_index": ("round_dt(g->dt, (h[i] * inv) * load_elem(g->dt, g->gamma, i))",
                          "round_dt(g->dt, (h[i] * inv) * load_elem(g->dt, g->gamma, 0))"),
 }
