@@ -260,6 +260,33 @@ rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows parti
                                          void *stream);
 
 /*
+ * Reduce + residual add + RMSNorm over R partials stored as 8-bit codes, with
+ * one binary32 scale per partial buffer ("Block All Reduce", FP8 section:
+ * reductions over e4m3 / e5m2 inputs with a binary32 accumulator;
+ * "Tokenweave fused-RMSNorm-AR kernel", Code walkthrough, for the reduce,
+ * residual and norm steps):
+ *
+ *   v_r = fl32(dec(c_r) * scales[r])      each partial dequantised, one rounding
+ *   acc = v_0; acc = fl32(acc + v_r) for r = 1 .. R-1; acc = fl32(acc + residual)
+ *   h = RN(acc); residual <- h; y = RN((h * rsqrt(mean(h^2) + eps)) * gamma)
+ *
+ * partials: R x T x H bytes of codes in `format`, dense (partial r starts at
+ * byte r * T * H), 8-byte aligned; scales: R binary32 values in device memory;
+ * residual (updated in place), gamma [H] and y [T, H] in `dt`, dense, 16-byte
+ * aligned.  All device memory owned by the caller; asynchronous on `stream`.
+ *
+ * Errors: NULL pointers with T > 0, T < 0, H <= 0, R < 1, a NaN / negative /
+ * infinite eps, an unknown type or format: RARN_ERR_INVALID_ARG; R > 16, H not
+ * a multiple of 8, H > 16384 (binary32: 8192) or misaligned pointers:
+ * RARN_ERR_UNSUPPORTED; y or the residual overlapping each other or an input:
+ * RARN_ERR_ALIAS.  T = 0 returns RARN_OK.
+ */
+rarn_status rarn_reduce_add_rms_norm_fp8in(void *y, const void *partials, int32_t R,
+                                           rarn_fp8_format format, const float *scales,
+                                           void *residual, const void *gamma, int64_t T,
+                                           int64_t H, float eps, rarn_dtype dt, void *stream);
+
+/*
  * GEMM producer with the fused residual-add RMSNorm as its epilogue: the
  * partial that the fused form adds to the residual is the product of the
  * activations A [T, K] and a linear layer's weight W [H, K]:

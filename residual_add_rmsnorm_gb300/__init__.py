@@ -29,7 +29,7 @@ __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_ho
            "DTYPE_CODES", "rms_norm_ex", "fused_add_rms_norm_ex", "reduce_add_rms_norm_ex",
            "rms_norm_fp8", "fused_add_rms_norm_fp8", "reduce_add_rms_norm_fp8", "plan_fp8",
            "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm",
-           "gemm_workspace_bytes", "gemm_add_rms_norm_noalloc"]
+           "gemm_workspace_bytes", "gemm_add_rms_norm_noalloc", "reduce_add_rms_norm_fp8in"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
@@ -136,6 +136,9 @@ def library() -> ctypes.CDLL:
     lib.rarn_gemm_add_rms_norm_noalloc.argtypes = [Rows, Rows, Rows, Rows, vp, i64, i64, i64,
                                                    f32, vp]
     lib.rarn_gemm_add_rms_norm_noalloc.restype = c_int
+    lib.rarn_reduce_add_rms_norm_fp8in.argtypes = [vp, vp, i32, c_int, vp, vp, vp, i64, i64, f32,
+                                                   c_int, vp]
+    lib.rarn_reduce_add_rms_norm_fp8in.restype = c_int
     lib.rarn_gemm_workspace_bytes.argtypes = [i64, i64]
     lib.rarn_gemm_workspace_bytes.restype = i64
     lib.rarn_plan_gemm.argtypes = [i64, i64, i64, c_int, ctypes.c_char_p, ctypes.c_size_t]
@@ -552,6 +555,39 @@ def gemm_add_rms_norm_noalloc(a, w, residual, gamma, eps: float, out=None):
             _rows("out", out, dev), _rows("a", a, dev), _rows("w", w, dev),
             _rows("residual", residual, dev), gamma.data_ptr(), T, H, K, float(eps),
             _stream(dev)), "rarn_gemm_add_rms_norm_noalloc")
+    return out
+
+
+def reduce_add_rms_norm_fp8in(codes, scales, residual, gamma, eps: float, fmt: str = "e4m3",
+                              out=None):
+    """reduce_add_rms_norm over R partials stored as 8-bit codes: ``codes``
+    [R, ...rows..., H] (uint8, or a torch float8 tensor of the format),
+    ``scales`` [R] binary32 on the same device (partial r is code * scales[r]),
+    ``residual`` [...rows..., H] updated in place; returns y like the
+    residual."""
+    import torch
+    if codes.dtype in (getattr(torch, "float8_e4m3fn", None), getattr(torch, "float8_e5m2", None)):
+        codes = codes.view(torch.uint8)
+    if codes.dtype != torch.uint8:
+        raise TypeError("codes must be uint8 or float8")
+    R, H = codes.shape[0], residual.shape[-1]
+    dev = residual.device
+    if tuple(codes.shape[1:]) != tuple(residual.shape) or gamma.numel() != H:
+        raise ValueError("shape mismatch")
+    if scales.dtype != torch.float32 or scales.numel() != R or scales.device != dev:
+        raise ValueError("scales must be R binary32 values on the residual's device")
+    for n, t in (("codes", codes), ("residual", residual), ("scales", scales)):
+        if t.device != dev or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous tensor on {dev}")
+    _check_tensor("gamma", gamma, residual.dtype, dev)
+    if out is None:
+        out = torch.empty_like(residual)
+    T = residual.numel() // H if H else 0
+    with torch.cuda.device(dev):
+        _check(library().rarn_reduce_add_rms_norm_fp8in(
+            out.data_ptr(), codes.data_ptr(), R, FP8_FORMATS[fmt], scales.data_ptr(),
+            residual.data_ptr(), gamma.data_ptr(), T, H, float(eps), _dtype_code(residual),
+            _stream(dev)), "rarn_reduce_add_rms_norm_fp8in")
     return out
 
 

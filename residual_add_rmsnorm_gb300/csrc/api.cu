@@ -14,6 +14,7 @@
 #include "../../include/rarn.h"
 #include "gemm_plan.h"
 #include "plan.h"
+#include "q8in.cuh"
 
 using namespace rarn;
 
@@ -937,6 +938,53 @@ rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w
                                     eps, scratch, kGemmScratchFloats * 4, stream);
         if (st != RARN_OK) return st;
     }
+    return RARN_OK;
+}
+
+rarn_status rarn_reduce_add_rms_norm_fp8in(void *y, const void *partials, int32_t R,
+                                           rarn_fp8_format format, const float *scales,
+                                           void *residual, const void *gamma, int64_t T,
+                                           int64_t H, float eps, rarn_dtype dt, void *stream) {
+    if (!dtype_ok(dt) || (format != RARN_E4M3 && format != RARN_E5M2)) return RARN_ERR_INVALID_ARG;
+    if (T < 0 || H <= 0 || R < 1 || !(eps >= 0.f) || std::isinf(eps)) return RARN_ERR_INVALID_ARG;
+    if (T == 0) return RARN_OK;
+    if (!y || !partials || !scales || !residual || !gamma) return RARN_ERR_INVALID_ARG;
+    const int s = elem_size(dt);
+    if (R > 16 || H % 8 != 0 || H > (dt == RARN_F32 ? 8192 : 16384)) return RARN_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(partials) & 7u) || !aligned16(residual) ||
+        !aligned16(gamma) || !aligned16(y) || (reinterpret_cast<uintptr_t>(scales) & 3u))
+        return RARN_ERR_UNSUPPORTED;
+    const int64_t rows = T * H * s;
+    const void *ins[3] = {partials, scales, gamma};
+    const int64_t inb[3] = {(int64_t)R * T * H, (int64_t)R * 4, H * s};
+    if (overlaps(y, rows, residual, rows)) return RARN_ERR_ALIAS;
+    for (int i = 0; i < 3; ++i)
+        if (overlaps(y, rows, ins[i], inb[i]) || overlaps(residual, rows, ins[i], inb[i]))
+            return RARN_ERR_ALIAS;
+    DeviceInfo *d = nullptr;
+    rarn_status st = device_info(&d);
+    if (st != RARN_OK) return st;
+    q8in::Params p{};
+    p.y = y;
+    p.codes = static_cast<const uint8_t *>(partials);
+    p.scales = scales;
+    p.residual = residual;
+    p.gamma = gamma;
+    p.T = T;
+    p.H = H;
+    p.R = R;
+    p.fmt = format == RARN_E4M3 ? 0 : 1;
+    p.eps = eps;
+    p.l2_rows = 1;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool pdl = g_pdl.load() != 0;
+    cudaError_t e;
+    switch (dt) {
+    case RARN_BF16: e = launch_q8in<__nv_bfloat16>(p, d->num_sms, pdl, cs); break;
+    case RARN_F16: e = launch_q8in<__half>(p, d->num_sms, pdl, cs); break;
+    default: e = launch_q8in<float>(p, d->num_sms, pdl, cs); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e);
     return RARN_OK;
 }
 

@@ -1,0 +1,6 @@
+// q8in_f32.cu -- reduce over 8-bit partials instantiated for float.
+#include "q8in.cuh"
+
+namespace rarn {
+template cudaError_t launch_q8in<float>(const q8in::Params &, int, bool, cudaStream_t);
+}  // namespace rarn

@@ -314,6 +314,40 @@ def test_plan_fp8():
         rarn.set_path("auto")
 
 
+def test_fp8_partials_argument_errors(lib):
+    """Reduce over 8-bit partials: types, sizes, alignment and aliasing are
+    checked before any CUDA call."""
+    f = lib.rarn_reduce_add_rms_norm_fp8in
+    T, H, R = 8, 1024, 4
+    y, p, sc, r, g = A, B, C, D, D + (1 << 30)
+
+    def call(y=y, p=p, R=R, fmt=0, sc=sc, r=r, g=g, T=T, H=H, eps=1e-6, dt=BF16):
+        return f(y, p, R, fmt, sc, r, g, T, H, eps, dt, None)
+
+    assert call(dt=7) == INVALID                       # unknown type
+    assert call(fmt=2) == INVALID                      # unknown format
+    assert call(R=0) == INVALID
+    assert call(T=-1) == INVALID
+    assert call(H=0) == INVALID
+    assert call(eps=float("nan")) == INVALID
+    assert call(eps=-1.0) == INVALID
+    assert call(T=0, y=None, p=None, sc=None, r=None, g=None) == OK  # nothing to do
+    assert call(sc=None) == INVALID
+    assert call(p=None) == INVALID
+    assert call(R=17) == UNSUPPORTED                   # at most 16 partials
+    assert call(H=1020) == UNSUPPORTED                 # H a multiple of 8
+    assert call(H=16392) == UNSUPPORTED                # at most 16384
+    assert call(H=8200, dt=F32) == UNSUPPORTED         # binary32: at most 8192
+    assert call(p=B + 4) == UNSUPPORTED                # codes 8-byte aligned
+    assert call(r=D + 8) == UNSUPPORTED                # residual 16-byte aligned
+    assert call(y=A + 8) == UNSUPPORTED
+    assert call(sc=C + 2) == UNSUPPORTED
+    assert call(y=D) == ALIAS                          # y over the residual
+    assert call(r=B + 64) == ALIAS                     # residual over the codes
+    assert call(y=C - 16) == ALIAS                     # y over the scales
+    assert call(r=g - 16) == ALIAS                     # residual over gamma
+
+
 def test_gemm_form_argument_errors(lib):
     """GEMM-producer form: types, shapes, workspace, alignment and aliasing
     are checked before any CUDA call."""
