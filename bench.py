@@ -509,6 +509,39 @@ def time_gemm(gw, device, rarn):
             "plan": rarn.plan_gemm(gw.T, gw.H, gw.K, gw.dtype)}
 
 
+FP8IN_NAME = "reduce8_e4m3in_bf16_T8192_H8192"
+
+
+def time_fp8in(device, rarn, R=8, T=8192, H=8192):
+    """The reduce over 8-bit partials (e4m3 codes, one binary32 scale per
+    partial) on the headline shape: seeded synthetic codes (N(0, 1) scaled to
+    the format's range, cast to e4m3), scales U(0.5, 1.5), residual N(0, 1)
+    bf16.  Algorithmic bytes: R T H codes + residual read and written + y +
+    gamma + scales; the inputs (0.9 GB) exceed L2, so launches read cold data."""
+    import torch
+    gen = torch.Generator(device=device).manual_seed(0)
+    codes = torch.empty(R, T, H, dtype=torch.uint8, device=device)
+    for r in range(R):
+        v = torch.randn(T, H, device=device, generator=gen) * (448.0 / 16)
+        codes[r] = v.to(torch.float8_e4m3fn).view(torch.uint8)
+        del v
+    scales = torch.rand(R, device=device, generator=gen) + 0.5
+    res = torch.randn(T, H, device=device, generator=gen).to(torch.bfloat16)
+    g = (torch.rand(H, device=device, generator=gen) + 0.5).to(torch.bfloat16)
+    y = torch.empty_like(res)
+    us = _graph_us(lambda: rarn.reduce_add_rms_norm_fp8in(codes, scales, res, g, 1e-6, "e4m3",
+                                                          out=y))
+    alg = R * T * H + 3 * T * H * 2 + H * 2 + R * 4
+    peak, _ = measured_hbm_peak()
+    gbs = alg / (us / 1e6) / 1e9
+    del codes, res, y
+    torch.cuda.empty_cache()
+    return {"kind": "widened (8-bit partials)", "us_per_launch": us, "gbs": gbs,
+            "rows_per_s": T / (us / 1e6), "frac_of_peak": gbs / peak, "algorithmic_bytes": alg,
+            "timing": "CUDA graph of 10 launches, best of 3 (inputs larger than L2)",
+            "plan": "q8in 16-element packs, R = 8, e4m3"}
+
+
 def e2e_steps(w, data, steps, device, stream):
     """End to end through the public host-buffer API: the inputs start in
     pinned host memory and the outputs end there.  Each step is one call of
@@ -659,6 +692,7 @@ def main():
             torch.cuda.empty_cache()
         for gw in W.GEMM_CONFIGS:
             per_config[gw.name] = time_gemm(gw, device, rarn)
+        per_config[FP8IN_NAME] = time_fp8in(device, rarn)
         if rarn.watchdog(clear=True):
             watchdog = 1
 
