@@ -195,6 +195,20 @@ __global__ void __launch_bounds__(256) k_q8in(Params p) {
     }
 }
 
+// Grid: every row-CTA resident at once (the kernel's occupancy times the SMs),
+// at most one per row.
+template <typename K>
+static dim3 resident_grid(K kernel, dim3 block, const Params &p, int num_sms) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, (int)block.x, 0) !=
+            cudaSuccess ||
+        per_sm < 1) {
+        (void)cudaGetLastError();
+        per_sm = 1;
+    }
+    return dim3(static_cast<unsigned>(std::min<int64_t>(p.T, (int64_t)num_sms * per_sm)));
+}
+
 // 2 codes -> 2 binary32 values, exact (through binary16).
 template <int FMT>
 __device__ __forceinline__ float2 decode2(uint32_t two) {
@@ -316,20 +330,6 @@ __global__ void __launch_bounds__(256) k_q8in16(Params p) {
     }
 }
 
-// Grid: every row-CTA resident at once (the kernel's occupancy times the SMs),
-// at most one per row.
-template <typename K>
-static dim3 resident_grid(K kernel, dim3 block, const Params &p, int num_sms) {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, (int)block.x, 0) !=
-            cudaSuccess ||
-        per_sm < 1) {
-        (void)cudaGetLastError();
-        per_sm = 1;
-    }
-    return dim3(static_cast<unsigned>(std::min<int64_t>(p.T, (int64_t)num_sms * per_sm)));
-}
-
 template <typename T, int VPT, int RMAX>
 static cudaError_t launch_fmt16(const Params &p, int num_sms, dim3 block, bool pdl,
                                 cudaStream_t st) {
@@ -347,17 +347,19 @@ static cudaError_t launch_r16(const Params &p, int num_sms, dim3 block, bool pdl
 }
 
 template <typename T, int VPT, int RMAX>
-static cudaError_t launch_fmt(const Params &p, dim3 grid, dim3 block, bool pdl, cudaStream_t st) {
-    return p.fmt == 0 ? launch_kernel(k_q8in<T, VPT, RMAX, 0>, grid, block, 0, st, pdl, 1, p)
-                      : launch_kernel(k_q8in<T, VPT, RMAX, 1>, grid, block, 0, st, pdl, 1, p);
+static cudaError_t launch_fmt(const Params &p, int num_sms, dim3 block, bool pdl,
+                              cudaStream_t st) {
+    auto kernel = p.fmt == 0 ? k_q8in<T, VPT, RMAX, 0> : k_q8in<T, VPT, RMAX, 1>;
+    return launch_kernel(kernel, resident_grid(kernel, block, p, num_sms), block, 0, st, pdl, 1, p);
 }
 
 template <typename T, int VPT>
-static cudaError_t launch_r(const Params &p, dim3 grid, dim3 block, bool pdl, cudaStream_t st) {
-    if (p.R <= 2) return launch_fmt<T, VPT, 2>(p, grid, block, pdl, st);
-    if (p.R <= 4) return launch_fmt<T, VPT, 4>(p, grid, block, pdl, st);
-    if (p.R <= 8) return launch_fmt<T, VPT, 8>(p, grid, block, pdl, st);
-    return launch_fmt<T, VPT, 16>(p, grid, block, pdl, st);
+static cudaError_t launch_r(const Params &p, int num_sms, dim3 block, bool pdl,
+                            cudaStream_t st) {
+    if (p.R <= 2) return launch_fmt<T, VPT, 2>(p, num_sms, block, pdl, st);
+    if (p.R <= 4) return launch_fmt<T, VPT, 4>(p, num_sms, block, pdl, st);
+    if (p.R <= 8) return launch_fmt<T, VPT, 8>(p, num_sms, block, pdl, st);
+    return launch_fmt<T, VPT, 16>(p, num_sms, block, pdl, st);
 }
 
 }  // namespace q8in
@@ -384,17 +386,16 @@ cudaError_t launch_q8in(const q8in::Params &p, int num_sms, bool pdl, cudaStream
     const int vpt = nv <= 256 ? 1 : nv <= 512 ? 2 : nv <= 1024 ? 4 : 8;
     if (vpt == 8 && sizeof(T) == 4) return cudaErrorInvalidValue;
     const dim3 block(static_cast<unsigned>((nv + vpt - 1) / vpt + 31) / 32 * 32);
-    const dim3 grid(static_cast<unsigned>(std::min<int64_t>(p.T, (int64_t)num_sms * 4)));
     cudaError_t e;
     switch (vpt) {
-    case 1: e = launch_r<T, 1>(p, grid, block, pdl, st); break;
-    case 2: e = launch_r<T, 2>(p, grid, block, pdl, st); break;
-    case 4: e = launch_r<T, 4>(p, grid, block, pdl, st); break;
+    case 1: e = launch_r<T, 1>(p, num_sms, block, pdl, st); break;
+    case 2: e = launch_r<T, 2>(p, num_sms, block, pdl, st); break;
+    case 4: e = launch_r<T, 4>(p, num_sms, block, pdl, st); break;
     default:
         if constexpr (sizeof(T) == 4) {
             e = cudaErrorInvalidValue;
         } else {
-            e = launch_r<T, 8>(p, grid, block, pdl, st);
+            e = launch_r<T, 8>(p, num_sms, block, pdl, st);
         }
     }
     return e != cudaSuccess ? e : cudaGetLastError();

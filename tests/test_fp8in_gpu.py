@@ -70,6 +70,16 @@ def test_fp8in_parity(dt, fmt, R, T, H):
     check(codes, scales, r, g, dt, fmt, f"{dt} {fmt} R{R} T{T} H{H}")
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_fp8in_eight_element_packs(dt, monkeypatch):
+    """The 8-element-pack kernel (the one H not a multiple of 16 takes)
+    forced on shapes the 16-element kernel would take: same results."""
+    monkeypatch.setenv("RARN_Q8IN_16", "0")
+    for R, T, H, fmt in ((8, 40, 4096, "e4m3"), (3, 7, 8192, "e5m2")):
+        codes, scales, r, g = fp8in_inputs(R, T, H, dt, fmt, seed=R + T + H)
+        check(codes, scales, r, g, dt, fmt, f"8-element packs {dt} {fmt} R{R} H{H}")
+
+
 def test_fp8in_power_of_two_scales_and_nan_codes():
     """Power-of-two scales (exact products), NaN codes (NaN rows in the
     residual and y), and a partial whose scale makes f16 overflow to inf."""
