@@ -9,27 +9,29 @@
 // epilogue, consumes the accumulator tile before anything is written;
 // "Tokenweave fused-RMSNorm-AR kernel", Code walkthrough, for the norm steps).
 //
-// Blackwell mapping (sm_103a), two kernels on one stream:
-//   1. k_gemm_res: one CTA per [128 x NS] tile of P (NS = 256 or 512
-//      columns), the accumulator in tensor memory (TMEM: 128 lanes = rows, NS
-//      columns of binary32).  Operands arrive by TMA (cp.async.bulk.tensor,
-//      2-D tiles, BK-element K slabs in the BK * 2-byte swizzle) into an
-//      S-stage ring; one thread issues tcgen05.mma (kind::f16, M = 128,
-//      N = 256, K = 16) and commits each stage back to the producer.  4 warps:
-//      warp 0 lane 0 produces, warp 1 lane 0 issues the MMAs, then all 128
-//      threads run the epilogue, thread i owning row i of the tile (TMEM lane
-//      i).  The operand ring is free once the MMAs are done, so it stages the
-//      epilogue: the residual tile arrives by TMA in [128 x 32] chunks
-//      (64-byte rows, 64-byte swizzle: a thread's 16-byte accesses to its own
-//      row are free of bank conflicts); each thread adds its accumulator row
-//      (tcgen05.ld), rounds once, writes h back into the chunk, which a TMA
-//      store returns to the residual; the tile's partial sum of squares of
-//      each row goes to a workspace slot [row][tile column] (no atomics).
-//      Tiles are independent: no cluster, every SM takes tiles.
-//   2. k_norm_ss: per row, the H / NS partial sums in tile order (fixed:
-//      deterministic), inv, and y = RN((h * inv) * gamma) from the stored
-//      residual (16-byte packs, a CTA per row).  Launched with programmatic
-//      dependent launch: it waits for kernel 1 to complete.
+// Blackwell mapping (sm_103a); the kernels of this file, by problem shape:
+//   * K >= 512, T >= 2048 (H <= 8192): k_gemm_res_pair, persistent on SM
+//     pairs (two-CTA clusters, tcgen05.mma.cta_group::2 on 256 x 256 tiles;
+//     the last partial round as 128-column halves), warp-specialised: a TMA
+//     producer, one MMA-issuing thread, 8 epilogue warps per CTA draining one
+//     of two TMEM accumulators while the next tile's MMAs run.  The epilogue
+//     adds the residual (one rounding), writes h, writes per-128-column
+//     partial sums of squares, and, once its 128-row block's counter shows
+//     every column (k_zero_counters zeroes the counters first), writes y.
+//   * K >= 512, 128 < T < 2048 (or T <= 128 with short K): k_gemm_res_ws,
+//     the same on one SM per 128 x 256 tile (M = 128 MMAs).
+//   * T <= 128, K >= 1024: k_gemm_splitk, C x S CTAs each multiplying a K
+//     range and writing binary32 partial products; k_splitk_norm sums them in
+//     split order, adds the residual and normalises.
+//   * K < 512: k_gemm_res, one CTA per [128 x NS] tile (NS = 256 or 512), the
+//     operand ring staging the epilogue: the residual tile arrives by TMA in
+//     [128 x 32] chunks (64-byte swizzle), each thread adds its accumulator
+//     row (tcgen05.ld), rounds once and writes h back for a TMA store; the
+//     tile's partial sums of squares go to the workspace; k_norm_ss (a warp
+//     per row slice, PDL-chained) then sums them in order and writes y.
+// In every form the accumulator is binary32 in TMEM, operands arrive by TMA
+// (cp.async.bulk.tensor, 2-D tiles in the 128- or 64-byte swizzle) and one
+// thread issues tcgen05.mma (kind::f16) and commits each ring stage back.
 //
 // Every mbarrier wait is bounded (global timer); a wait that runs out sets the
 // watchdog word and the CTA's abort flag, the CTA drains what it issued (also
