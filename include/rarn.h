@@ -299,11 +299,12 @@ rarn_status rarn_reduce_add_rms_norm_fp8in(void *y, const void *partials, int32_
  * Code walkthrough: the norm steps.)
  *
  * Kernels on `stream`: the tcgen05 GEMM whose epilogue writes h and, per row
- * and column tile, the partial sum of squares of h into `workspace`.  With
+ * and column block (128 columns in the persistent kernels, one tile of 256
+ * or 512 otherwise), the partial sum of squares of h into `workspace`.  With
  * K >= 512 (the persistent kernels) the same epilogue then waits for the
  * other column tiles of its 128-row block (a counter per block in the
  * workspace, zeroed by a one-CTA kernel launched just before), sums each
- * row's partials in tile order and writes y; otherwise a norm kernel does
+ * row's partials in column order and writes y; otherwise a norm kernel does
  * that last step.  Both orders give identical bits.  With T <= 128 and
  * K >= 1024 the product is split over K instead: up to 9 CTAs per column
  * tile write binary32 partial products into the workspace and a CTA per row

@@ -1555,10 +1555,10 @@ static __global__ void __launch_bounds__(256) k_zero_counters(unsigned int *cnt,
     grid_launch_dependents();
 }
 
-// Kernel 2: y from the stored h and the tiles' partial sums.  A warp per
-// (row, slice of up to 32 * VPT 16-byte packs): it loads its slice of h and
-// the row's column-tile partials at once, forms inv from the partials summed
-// in tile order (the same value in every slice of the row) and writes its
+// Kernel 2: y from the stored h and the column blocks' partial sums.  A warp
+// per (row, slice of up to 32 * VPT 16-byte packs): it loads its slice of h
+// and the row's C partials at once, forms inv from the partials summed in
+// column order (the same value in every slice of the row) and writes its
 // slice of y.  No barrier: every warp works alone, grid-stride over items.
 constexpr int kNormVPT = 4;
 constexpr int kNormThreads = 256;
