@@ -53,9 +53,10 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=[w.name for w in _configs()],
+                    choices=[w.name for w in _configs()] + [FP8IN_NAME],
                     help="the timed configuration; a widened workload (row strides, fp32 "
-                         "residual, 8-bit output) has no host-buffer (e2e) or CPU leg")
+                         "residual, 8-bit output or partials) has no host-buffer (e2e) or CPU "
+                         "leg")
     ap.add_argument("--path", choices=["auto", "rows", "stream", "cluster"], default="auto",
                     help="kernel family (default: the library's own choice)")
     ap.add_argument("--no-pdl", action="store_true",
@@ -512,12 +513,11 @@ def time_gemm(gw, device, rarn):
 FP8IN_NAME = "reduce8_e4m3in_bf16_T8192_H8192"
 
 
-def time_fp8in(device, rarn, R=8, T=8192, H=8192):
-    """The reduce over 8-bit partials (e4m3 codes, one binary32 scale per
-    partial) on the headline shape: seeded synthetic codes (N(0, 1) scaled to
-    the format's range, cast to e4m3), scales U(0.5, 1.5), residual N(0, 1)
-    bf16.  Algorithmic bytes: R T H codes + residual read and written + y +
-    gamma + scales; the inputs (0.9 GB) exceed L2, so launches read cold data."""
+def fp8in_tensors(device, R=8, T=8192, H=8192):
+    """Seeded synthetic inputs of the reduce over 8-bit partials: codes
+    N(0, 1) scaled to the e4m3 range and cast to e4m3, scales U(0.5, 1.5),
+    residual N(0, 1) bf16, gamma U(0.5, 1.5) bf16; and the algorithmic bytes
+    of one call (R T H codes, residual read and written, y, gamma, scales)."""
     import torch
     gen = torch.Generator(device=device).manual_seed(0)
     codes = torch.empty(R, T, H, dtype=torch.uint8, device=device)
@@ -528,10 +528,21 @@ def time_fp8in(device, rarn, R=8, T=8192, H=8192):
     scales = torch.rand(R, device=device, generator=gen) + 0.5
     res = torch.randn(T, H, device=device, generator=gen).to(torch.bfloat16)
     g = (torch.rand(H, device=device, generator=gen) + 0.5).to(torch.bfloat16)
+    return codes, scales, res, g, R * T * H + 3 * T * H * 2 + H * 2 + R * 4
+
+
+FP8IN_PLAN = ("q8in TMA-fed ring kernel (producer warp + 16 consumer warps per SM), R = 8, "
+              "e4m3")
+
+
+def time_fp8in(device, rarn, R=8, T=8192, H=8192):
+    """The reduce over 8-bit partials on the headline shape; the inputs
+    (0.9 GB) exceed L2, so launches read cold data."""
+    import torch
+    codes, scales, res, g, alg = fp8in_tensors(device, R, T, H)
     y = torch.empty_like(res)
     us = _graph_us(lambda: rarn.reduce_add_rms_norm_fp8in(codes, scales, res, g, 1e-6, "e4m3",
                                                           out=y))
-    alg = R * T * H + 3 * T * H * 2 + H * 2 + R * 4
     peak, _ = measured_hbm_peak()
     gbs = alg / (us / 1e6) / 1e9
     del codes, res, y
@@ -539,7 +550,49 @@ def time_fp8in(device, rarn, R=8, T=8192, H=8192):
     return {"kind": "widened (8-bit partials)", "us_per_launch": us, "gbs": gbs,
             "rows_per_s": T / (us / 1e6), "frac_of_peak": gbs / peak, "algorithmic_bytes": alg,
             "timing": "CUDA graph of 10 launches, best of 3 (inputs larger than L2)",
-            "plan": "q8in 16-element packs, R = 8, e4m3"}
+            "plan": FP8IN_PLAN}
+
+
+def main_fp8in(args, device, rank, world):
+    """The reduce over 8-bit partials as the timed step (one launch per
+    step; inputs resident in HBM and larger than L2).  No host-buffer entry
+    point and no oracle leg for this form."""
+    import torch
+
+    import residual_add_rmsnorm_gb300 as rarn
+    codes, scales, res, g, alg = fp8in_tensors(device)
+    y = torch.empty_like(res)
+    call = lambda: rarn.reduce_add_rms_norm_fp8in(codes, scales, res, g, 1e-6, "e4m3", out=y)
+    stream = torch.cuda.current_stream(device)
+    props = torch.cuda.get_device_properties(device)
+    gpu_id = str(getattr(props, "uuid", 0))
+    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id)
+    ms = time_steps(call, args.steps, args.warmup, stream)
+    clocks = sampler.stop()
+    ms = max_over_ranks(ms, device)
+    peak, kind = measured_hbm_peak()
+    gbs = world * alg * args.steps / (ms / 1e3) / 1e9
+    if rank != 0:
+        return
+    line = {
+        "metric": "achieved HBM GB/s (algorithmic bytes / time)", "value": gbs, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": FP8IN_NAME, "R": 8, "T": 8192, "H": 8192, "format": "e4m3",
+                   "storage": "bf16", "plan": FP8IN_PLAN,
+                   "l2": "inputs larger than L2 (0.9 GB)", "pdl": not args.no_pdl},
+        "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / world / peak,
+                     "traffic": ncu_traffic(FP8IN_NAME, FP8IN_PLAN), "peak_source": kind},
+        "cpu_baseline": None,
+        "e2e": {"value": None, "unit": "GB/s",
+                "note": "no host-buffer entry point for the 8-bit-partials form"},
+        "clocks": clocks, "gpu_launches": args.steps, "watchdog": rarn.watchdog(clear=True),
+    }
+    print(json.dumps(line), flush=True)
 
 
 def e2e_steps(w, data, steps, device, stream):
@@ -638,6 +691,9 @@ def main():
     gemm = {gw.name: gw for gw in W.GEMM_CONFIGS}
     if args.workload in gemm:
         main_gemm(args, gemm[args.workload], device, rank, world)
+        return
+    if args.workload == FP8IN_NAME:
+        main_fp8in(args, device, rank, world)
         return
     w = W.BY_NAME[args.workload]
     data = W.generate(w)

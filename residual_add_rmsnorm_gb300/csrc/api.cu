@@ -16,6 +16,14 @@
 #include "plan.h"
 #include "q8in.cuh"
 
+namespace rarn {
+// instantiated in q8in_{bf16,f16,f32}.cu
+extern template cudaError_t launch_q8in<__nv_bfloat16>(const q8in::Params &, int, bool,
+                                                       cudaStream_t);
+extern template cudaError_t launch_q8in<__half>(const q8in::Params &, int, bool, cudaStream_t);
+extern template cudaError_t launch_q8in<float>(const q8in::Params &, int, bool, cudaStream_t);
+}  // namespace rarn
+
 using namespace rarn;
 
 // Watchdog word: kernels with bounded waits record a timeout here.
@@ -976,6 +984,17 @@ rarn_status rarn_reduce_add_rms_norm_fp8in(void *y, const void *partials, int32_
     p.fmt = format == RARN_E4M3 ? 0 : 1;
     p.eps = eps;
     p.l2_rows = 1;
+    p.watchdog = d->watchdog;
+    p.wait_limit_ns = stream::kWaitLimitNs;
+    p.stall_fill = -1;
+    p.max_smem = d->max_smem_optin;
+    if (q8in::stream_plan_for(p, s, d->num_sms).ppt > 0) {
+        const long long f = g_stall_fill.exchange(-1);
+        if (f >= 0) {
+            p.stall_fill = f;
+            p.wait_limit_ns = g_stall_limit_ns.load();
+        }
+    }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
     const bool pdl = g_pdl.load() != 0;
     cudaError_t e;

@@ -9,11 +9,15 @@
 // binary32 accumulator; "Tokenweave fused-RMSNorm-AR kernel", Code
 // walkthrough: the reduce + residual + norm steps.)
 //
-// A CTA per row, VPT packs of 8 elements per thread: 8 bytes of codes per
-// partial (decoded exactly through binary16: every e4m3 / e5m2 value is a
-// binary16 value), the residual, gamma and y in the storage type.  The
-// partial loop is unrolled to RMAX so that every load of a pack is in flight
-// at once; the rounded row stays in registers for the normalise pass.
+// Two kernel forms.  Register kernels: a CTA per row, VPT packs of 8 (or 16)
+// elements per thread: 8 (16) bytes of codes per partial (decoded exactly
+// through binary16: every e4m3 / e5m2 value is a binary16 value), the
+// residual, gamma and y in the storage type; the partial loop is unrolled so
+// that a pack's loads are in flight together, and the rounded row stays in
+// registers for the normalise pass.  The TMA-fed kernel (more than 4
+// partials, many rows): a persistent CTA per SM whose producer warp streams
+// the rows' code chunks and residual into a shared-memory ring with bulk
+// copies while 16 consumer warps reduce and normalise.
 #pragma once
 
 #include <cuda_fp8.h>
@@ -22,6 +26,7 @@
 #include <cstdlib>
 
 #include "common.cuh"
+#include "stream.cuh"  // mbarrier / bulk-copy primitives and bounded waits
 
 namespace rarn {
 namespace q8in {
@@ -37,6 +42,11 @@ struct Params {
     int fmt;                // 0 e4m3, 1 e5m2
     float eps;
     int l2_rows;            // rows prefetched into L2 before the dependency wait
+    // TMA-fed kernel only
+    unsigned int *watchdog;          // device word for bounded-wait failures
+    unsigned long long wait_limit_ns;  // bound on every shared-memory barrier wait
+    long long stall_fill;            // test hook: in CTA 0 this fill never completes (-1: off)
+    int max_smem;                    // dynamic shared memory a CTA may opt into, bytes
 };
 
 // 8 elements of the storage type: one 16-byte pack (16-bit) or two (binary32).
@@ -362,6 +372,276 @@ static cudaError_t launch_r(const Params &p, int num_sms, dim3 block, bool pdl,
     return launch_fmt<T, VPT, 16>(p, num_sms, block, pdl, st);
 }
 
+// ---------------------------------------------------------------------------
+// TMA-fed persistent kernel (rows of a multiple of 16 elements, 16-byte
+// aligned partials; T >= 2 x #SM)
+// ---------------------------------------------------------------------------
+
+// v[e] = fl32(dec(c_e) * s) for 8 codes (exact decode through binary16).
+// (Measured on the TMA-fed kernel, R = 8, [8192, 8192]: the same speed or
+// slower were an integer re-layout of each code into binary32 bits, and
+// binary16 pairs widened by a mixed-precision add of -0.)
+template <int FMT>
+__device__ __forceinline__ void dequant8(uint2 c, float s, float (&v)[8]) {
+    float f[8];
+    decode8<FMT>(c, f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = __fmul_rn(f[e], s);
+}
+
+// Consumer warps of the TMA-fed kernel (16 measured faster than 8: R = 8,
+// [8192, 8192] bf16 157 vs 173 us; R = 4, [16384, 4096] 133 vs 161 us).
+constexpr int kStreamWarps = 16;
+
+// Shared-memory layout: `stages` stages, each R code chunks (8 bytes per
+// 8-element unit) and one residual chunk (8 elements of T per unit); the
+// rounded row; then the control words.  Offsets 128-byte aligned.
+struct SLayout {
+    int code_chunk, stage_bytes, row_off, ctl_off, total;
+};
+
+__host__ __device__ inline SLayout slayout(int stages, int R, int ppt, int s, int64_t H,
+                                           int warps) {
+    SLayout L;
+    L.code_chunk = 32 * warps * ppt * 8;
+    L.stage_bytes = stream::align128(R * L.code_chunk + L.code_chunk * s);
+    L.row_off = stages * L.stage_bytes;
+    L.ctl_off = L.row_off + stream::align128((int)(H * s));
+    L.total = L.ctl_off + 2 * stream::kMaxStages * 8 + 2 * warps * 4 + 16;
+    return L;
+}
+
+// One CTA per SM walks rows t = blockIdx.x, blockIdx.x + gridDim.x, ...
+// Warp 0 is the producer: one lane issues, per chunk of CU = 512 * PPT units
+// of 8 elements, R + 1 cp.async.bulk copies (the R partials' codes and the
+// residual) into the next stage of a shared-memory ring, guarded by a "full"
+// mbarrier (completed by the byte count) and an "empty" one (released by the
+// 16 consumer warps); it runs ahead across rows, so HBM reads stay in flight
+// while the consumers reduce and normalise.  Consumer thread j takes the
+// units c * CU + m * 512 + j of chunk c: it dequantises and sums the partials
+// in order, adds the residual (one rounding), writes the residual unit,
+// keeps it in the shared-memory row and accumulates its squares; after the
+// row a named barrier combines the warps' sums and each thread normalises
+// its own units (the same units, no further synchronisation).  Every wait is
+// bounded: on a timeout the kernel sets the watchdog word and the CTA's
+// abort word, stops issuing copies, drains the ones issued and returns.
+template <typename T, int PPT, int RMAX, int FMT>
+__global__ void __launch_bounds__(32 + 32 * kStreamWarps, 1) k_q8in_stream(Params p, int stages) {
+    using namespace stream;
+    constexpr int kConsumerWarps = kStreamWarps;
+    constexpr int kConsumers = 32 * kStreamWarps;
+    constexpr int CU = kConsumers * PPT;       // units per chunk
+    constexpr int UB = 8 * (int)sizeof(T);     // residual bytes per unit
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int nu = (int)(p.H / 8);
+    const int nchunks = (nu + CU - 1) / CU;
+    const int64_t plane = p.T * p.H;
+    const SLayout L = slayout(stages, p.R, PPT, (int)sizeof(T), p.H, kStreamWarps);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L.ctl_off);  // [stages]
+    uint64_t *empty = full + kMaxStages;                               // [stages]
+    float *red = reinterpret_cast<float *>(empty + kMaxStages);        // [2][kConsumerWarps]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 2 * kConsumerWarps);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // the first row's streams prefetched into L2 before the wait (L2 is the
+    // point of coherence: correct while the previous kernel still writes them)
+    if (p.l2_rows > 0 && (int)threadIdx.x <= p.R && (int64_t)blockIdx.x < p.T) {
+        const int64_t t = blockIdx.x;
+        if ((int)threadIdx.x < p.R)
+            prefetch_l2(p.codes + threadIdx.x * plane + t * p.H, (uint32_t)p.H);
+        else
+            prefetch_l2(reinterpret_cast<const T *>(p.residual) + t * p.H,
+                        (uint32_t)(p.H * (int64_t)sizeof(T)));
+    }
+    grid_dependency_wait();
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            mbar_init(smem_addr(&empty[s]), kConsumerWarps);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane != 0) return;
+        long long n = 0;  // fills issued
+        const long long stall_at = blockIdx.x == 0 ? p.stall_fill : -1;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; t < p.T && ok; t += gridDim.x) {
+            for (int c = 0; c < nchunks && ok; ++c, ++n) {
+                const int units = min(CU, nu - c * CU);
+                const uint32_t cb = (uint32_t)units * 8u, rb = (uint32_t)units * UB;
+                const int st = (int)(n % stages);
+                const uint32_t ph = (uint32_t)((n / stages) & 1);
+                ok = wait_bounded(smem_addr(&empty[st]), ph ^ 1u, abort_flag, p.watchdog,
+                                  kWatchProducer, p.wait_limit_ns);
+                if (!ok) break;
+                const uint32_t fb = smem_addr(&full[st]);
+                // test hook: expect 16 bytes more than the copies bring, so that
+                // this fill never completes and its consumers' wait runs out
+                const uint32_t extra = n == stall_at ? 16u : 0u;
+                mbar_arrive_expect_tx(fb, cb * (uint32_t)p.R + rb + extra);
+                const uint32_t dst = smem_addr(smem + (size_t)st * L.stage_bytes);
+                const int64_t off = t * p.H + (int64_t)c * CU * 8;  // element offset
+                for (int r = 0; r < p.R; ++r)
+                    bulk_g2s(dst + (uint32_t)(r * L.code_chunk), p.codes + r * plane + off, cb,
+                             fb);
+                bulk_g2s(dst + (uint32_t)(p.R * L.code_chunk),
+                         reinterpret_cast<const T *>(p.residual) + off, rb, fb);
+            }
+        }
+        grid_launch_dependents();
+        // Drain: the last min(stages, issued) fills must land before the CTA
+        // exits (one deadline for all of them).
+        const unsigned long long deadline = global_ns() + p.wait_limit_ns;
+        for (long long f = n > stages ? n - stages : 0; f < n; ++f)
+            wait_drain(smem_addr(&full[(int)(f % stages)]), (uint32_t)((f / stages) & 1),
+                       deadline, p.watchdog);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int cw = warp - 1;
+    const int j = (int)threadIdx.x - 32;
+    Pack8<T> *row_copy = reinterpret_cast<Pack8<T> *>(smem + L.row_off);
+    const T *gamma = reinterpret_cast<const T *>(p.gamma);
+    T *residual = reinterpret_cast<T *>(p.residual);
+    int stage = 0;
+    uint32_t phase = 0;
+    int par = 0;
+    for (int64_t t = blockIdx.x; t < p.T; t += gridDim.x, par ^= 1) {
+        float ss = 0.f;
+        if (t + gridDim.x >= p.T) grid_launch_dependents();
+        for (int c = 0; c < nchunks; ++c) {
+            const bool ok = wait_bounded(smem_addr(&full[stage]), phase, abort_flag, p.watchdog,
+                                         kWatchConsumer, p.wait_limit_ns);
+            const unsigned char *sbase = smem + (size_t)stage * L.stage_bytes;
+#pragma unroll
+            for (int m = 0; m < PPT; ++m) {
+                const int q = m * kConsumers + j;  // unit within the chunk
+                const int u = c * CU + q;          // unit within the row
+                if (!ok || u >= nu) continue;
+                float acc[8];
+#pragma unroll
+                for (int r = 0; r < RMAX; ++r) {
+                    if (r < p.R) {
+                        const uint2 code =
+                            *reinterpret_cast<const uint2 *>(sbase + r * L.code_chunk + q * 8);
+                        float v[8];
+                        dequant8<FMT>(code, __ldg(p.scales + r), v);
+                        // product and sum rounded separately (__fmul_rn /
+                        // __fadd_rn are never contracted into one FMA)
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[e] = r == 0 ? v[e] : __fadd_rn(acc[e], v[e]);
+                    }
+                }
+                Pack8<T> hv =
+                    *reinterpret_cast<const Pack8<T> *>(sbase + p.R * L.code_chunk + q * UB);
+                float rv[8];
+                hv.unpack(rv);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    acc[e] = DT<T>::round(__fadd_rn(acc[e], rv[e]));  // h: one rounding
+                    ss += acc[e] * acc[e];
+                }
+                hv.pack(acc);
+                hv.store(residual + t * p.H + 8 * (int64_t)u);
+                row_copy[u] = hv;
+            }
+            __syncwarp();
+            // release the stage only if this warp saw its fill complete (after
+            // an abort an unfinished fill's stage stays held)
+            if (lane == 0 && ok) mbar_arrive(smem_addr(&empty[stage]));
+            if (++stage == stages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        ss = warp_sum(ss);
+        if (lane == 0) red[par * kConsumerWarps + cw] = ss;
+        asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) tot += red[par * kConsumerWarps + w];
+        const float inv = rsqrtf(tot / (float)p.H + p.eps);
+        if (*abort_flag) continue;
+        T *y = reinterpret_cast<T *>(p.y) + t * p.H;
+        for (int u = j; u < nu; u += kConsumers) {
+            float h[8], w[8];
+            row_copy[u].unpack(h);
+            Pack8<T> gp;
+            gp.load_keep(gamma + 8 * (int64_t)u);
+            gp.unpack(w);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) h[e] = (h[e] * inv) * w[e];
+            Pack8<T> o;
+            o.pack(h);
+            o.store(y + 8 * (int64_t)u);
+        }
+    }
+}
+
+// Units per consumer thread per chunk (up to two, while at least 4 stages
+// fit) and the deepest ring that fits the shared memory.
+struct StreamPlan {
+    int ppt = 0, stages = 0, smem = 0;
+};
+
+inline StreamPlan plan_stream(int64_t H, int R, int s, int max_smem) {
+    StreamPlan sp;
+    const int64_t nu = H / 8;
+    for (int ppt = nu > 32 * kStreamWarps ? 2 : 1; ppt >= 1; ppt >>= 1) {
+        int stages = stream::kMaxStages;
+        while (stages >= 2 && slayout(stages, R, ppt, s, H, kStreamWarps).total > max_smem)
+            --stages;
+        if (stages < 2 || (ppt > 1 && stages < 4)) continue;
+        sp.ppt = ppt;
+        sp.stages = stages;
+        sp.smem = slayout(stages, R, ppt, s, H, kStreamWarps).total;
+        return sp;
+    }
+    return StreamPlan{};
+}
+
+// The TMA-fed kernel's plan when it runs (ppt > 0): rows of a multiple of 16
+// elements (16-byte code copies), 16-byte aligned codes, more than 4
+// partials and at least 8 rows per SM.  Measured (CUDA-graph timing, bf16
+// unless noted, register kernel / TMA-fed kernel, us): R = 8 [8192, 8192]
+// 233 / 157 (f16 234 / 156; binary32 [8192, 4096] 155 / 109); R = 16
+// [4096, 8192] 166 / 118; R = 6 [8192, 8192] 194 / 139; R = 4 [16384, 4096]
+// 132 / 133; R = 2 [32768, 4096] 188 / 243; R = 8 [304, 8192] 7.3 / 8.0.
+// RARN_Q8IN_STREAM = 0 / 1 switches it off / forces it (any shape it can
+// take) for measurements and tests.
+inline StreamPlan stream_plan_for(const Params &p, int s, int num_sms) {
+    const char *sv = getenv("RARN_Q8IN_STREAM");
+    const int force = sv && *sv ? atoi(sv) : -1;
+    if (force == 0 || p.H % 16 != 0 || (reinterpret_cast<uintptr_t>(p.codes) & 15u) != 0 ||
+        (force != 1 && (p.R <= 4 || p.T < 8 * (int64_t)num_sms)))
+        return StreamPlan{};
+    return plan_stream(p.H, p.R, s, p.max_smem);
+}
+
+template <typename T, int PPT, int RMAX>
+static cudaError_t launch_stream_fmt(const Params &p, const StreamPlan &sp, int grid, bool pdl,
+                                     cudaStream_t st) {
+    auto kernel = p.fmt == 0 ? k_q8in_stream<T, PPT, RMAX, 0> : k_q8in_stream<T, PPT, RMAX, 1>;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, sp.smem);
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kernel, dim3(grid), dim3(32 + 32 * kStreamWarps), sp.smem, st, pdl, 1,
+                         p, sp.stages);
+}
+
+template <typename T, int PPT>
+static cudaError_t launch_stream_r(const Params &p, const StreamPlan &sp, int grid, bool pdl,
+                                   cudaStream_t st) {
+    if (p.R <= 8) return launch_stream_fmt<T, PPT, 8>(p, sp, grid, pdl, st);
+    return launch_stream_fmt<T, PPT, 16>(p, sp, grid, pdl, st);
+}
+
 }  // namespace q8in
 
 // Packs per thread so that a row takes at most 256 threads (H <= 16384;
@@ -369,6 +649,13 @@ static cudaError_t launch_r(const Params &p, int num_sms, dim3 block, bool pdl,
 template <typename T>
 cudaError_t launch_q8in(const q8in::Params &p, int num_sms, bool pdl, cudaStream_t st) {
     using namespace q8in;
+    const StreamPlan sp = stream_plan_for(p, (int)sizeof(T), num_sms);
+    if (sp.ppt > 0) {
+        const int grid = (int)std::min<int64_t>(p.T, num_sms);
+        const cudaError_t e = sp.ppt == 2 ? launch_stream_r<T, 2>(p, sp, grid, pdl, st)
+                                          : launch_stream_r<T, 1>(p, sp, grid, pdl, st);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     if (p.H % 16 == 0 && !(getenv("RARN_Q8IN_16") && atoi(getenv("RARN_Q8IN_16")) == 0)) {
         // 16-element packs (measurements can switch them off)
         const int64_t nv = p.H / 16;

@@ -134,3 +134,59 @@ def test_fp8in_chained(pdl):
         assert_y_close(to_host(y2, "bf16"), o2.y, "bf16", "chained y")
     finally:
         rarn.set_pdl(True)
+
+
+def all_finite_codes(fmt):
+    """Every finite code of the format (both zeros, subnormals, normals)."""
+    c = np.arange(256, dtype=np.uint8)
+    special = (c & 0x7F) == 0x7F if fmt == "e4m3" else (c & 0x7C) == 0x7C
+    return c[~special]
+
+
+def test_fp8in_tma_fed_kernel(monkeypatch):
+    """The TMA-fed kernel forced on shapes the register kernels would take:
+    ragged last chunks, 1 to 16 partials, all three storage types, every
+    finite code, NaN and Inf codes, and overflow of the sum."""
+    monkeypatch.setenv("RARN_Q8IN_STREAM", "1")
+    for dt, fmt, R, T, H in (("bf16", "e4m3", 8, 40, 4096), ("f16", "e5m2", 3, 37, 1040),
+                             ("f32", "e4m3", 5, 9, 8192), ("bf16", "e5m2", 16, 5, 16384),
+                             ("bf16", "e4m3", 2, 300, 16), ("f16", "e4m3", 1, 11, 6144),
+                             ("f32", "e5m2", 4, 160, 2064)):
+        codes, scales, r, g = fp8in_inputs(R, T, H, dt, fmt, seed=R * 7 + T + H)
+        check(codes, scales, r, g, dt, fmt, f"tma-fed {dt} {fmt} R{R} T{T} H{H}")
+    for fmt in ("e4m3", "e5m2"):
+        fin = all_finite_codes(fmt)
+        R, T, H = 3, 6, 512
+        codes = np.stack([np.resize(np.roll(fin, 17 * k + t), H) for k in range(R)
+                          for t in range(T)]).reshape(R, T, H)
+        _, _, r, g = fp8in_inputs(R, T, H, "bf16", fmt, seed=21)
+        check(codes, np.float32([1.0, 0.37, 2.0 ** -10]), r, g, "bf16", fmt,
+              f"tma-fed every finite {fmt} code")
+    codes, _, r, g = fp8in_inputs(4, 6, 512, "bf16", "e4m3", seed=7, nan_codes=True)
+    check(codes, np.exp2([-3, 0, 2, 5]).astype(np.float32), r, g, "bf16", "e4m3",
+          "tma-fed NaN codes")
+    codes, _, r, g = fp8in_inputs(4, 6, 512, "f16", "e5m2", seed=8)
+    codes[1, :, 5] = 0x7C  # +Inf
+    codes[2, 2, 9] = 0xFC  # -Inf
+    check(codes, np.float32([4.0, 1.0, 1.0, 1.0]), r, g, "f16", "e5m2",
+          "tma-fed Inf codes, f16 overflow")
+
+
+@pytest.mark.parametrize("fill", [0, 3])
+def test_fp8in_wait_runs_out_and_is_reported(fill, monkeypatch):
+    """Failure detection without a GPU fault: the TMA-fed kernel's test hook
+    leaves one ring fill of CTA 0 without its last 16 bytes; the consumers'
+    wait gives up after 20 ms, the CTA drains its copies and returns, the
+    watchdog bit is set, and the next call is correct."""
+    import torch
+    monkeypatch.setenv("RARN_Q8IN_STREAM", "1")
+    rarn.watchdog(clear=True)
+    R, T, H = 4, 1000, 4096  # CTA 0 takes 7 rows, one fill each
+    codes, scales, r, g = fp8in_inputs(R, T, H, "bf16", "e4m3", seed=30 + fill)
+    assert rarn.library().rarn_test_stall(fill, 20_000_000) == 0
+    run_fp8in(codes, scales, r, g, "bf16", "e4m3")  # outputs not valid; the call returns
+    torch.cuda.synchronize()
+    flags = rarn.watchdog(clear=True)
+    assert flags & 1, f"consumer timeout not reported (flags={flags})"
+    check(codes, scales, r, g, "bf16", "e4m3", "after a watchdog timeout")
+    assert rarn.watchdog(clear=True) == 0
