@@ -386,6 +386,17 @@ rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w
  * boundary, 9 T H binary32 values for split K.  -1 if H is not supported. */
 int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H);
 
+/* Describe the kernel rarn_reduce_add_rms_norm_fp8in takes for a problem
+ * (pure host logic, no GPU needed): T rows of H, R partials, storage type dt,
+ * whether the codes are 16-byte aligned, and the device's SM count and opt-in
+ * shared memory per CTA in bytes.  Writes a NUL-terminated description
+ * ("q8in.ring ..." with the shared-memory ring's shape, or "q8in.rows ...")
+ * into out[cap].  Errors: NULL out, cap 0, bad arguments:
+ * RARN_ERR_INVALID_ARG; a shape the call rejects as unsupported:
+ * RARN_ERR_UNSUPPORTED (out says so). */
+rarn_status rarn_plan_fp8in(int64_t T, int64_t H, int32_t R, rarn_dtype dt, int codes_aligned16,
+                            int32_t num_sms, int32_t max_smem, char *out, size_t cap);
+
 /* Describe the GEMM kernels' tiling for a problem (pure host logic). */
 rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, char *out, size_t cap);
 

@@ -28,7 +28,7 @@ __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_ho
            "set_path", "get_path", "set_pdl", "get_pdl", "plan", "watchdog", "PATHS",
            "DTYPE_CODES", "rms_norm_ex", "fused_add_rms_norm_ex", "reduce_add_rms_norm_ex",
            "rms_norm_fp8", "fused_add_rms_norm_fp8", "reduce_add_rms_norm_fp8", "plan_fp8",
-           "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm",
+           "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm", "plan_fp8in",
            "gemm_workspace_bytes", "gemm_add_rms_norm_noalloc", "reduce_add_rms_norm_fp8in"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -143,6 +143,9 @@ def library() -> ctypes.CDLL:
     lib.rarn_gemm_workspace_bytes.restype = i64
     lib.rarn_plan_gemm.argtypes = [i64, i64, i64, c_int, ctypes.c_char_p, ctypes.c_size_t]
     lib.rarn_plan_gemm.restype = c_int
+    lib.rarn_plan_fp8in.argtypes = [i64, i64, ctypes.c_int32, c_int, c_int, ctypes.c_int32,
+                                    ctypes.c_int32, ctypes.c_char_p, ctypes.c_size_t]
+    lib.rarn_plan_fp8in.restype = c_int
     lib.rarn_set_pdl.argtypes = [c_int]
     lib.rarn_set_pdl.restype = c_int
     lib.rarn_get_pdl.argtypes = []
@@ -589,6 +592,19 @@ def reduce_add_rms_norm_fp8in(codes, scales, residual, gamma, eps: float, fmt: s
             residual.data_ptr(), gamma.data_ptr(), T, H, float(eps), _dtype_code(residual),
             _stream(dev)), "rarn_reduce_add_rms_norm_fp8in")
     return out
+
+
+def plan_fp8in(T: int, H: int, R: int, dtype: str = "bf16", codes_aligned16: bool = True,
+               num_sms: int = 152, max_smem: int = 232448) -> str:
+    """The kernel reduce_add_rms_norm_fp8in takes for a problem on a device
+    with `num_sms` SMs and `max_smem` bytes of opt-in shared memory per CTA
+    (host logic only; the defaults are a GB300's)."""
+    buf = ctypes.create_string_buffer(256)
+    st = library().rarn_plan_fp8in(T, H, R, DTYPE_CODES[dtype], int(codes_aligned16), num_sms,
+                                   max_smem, buf, 256)
+    if st not in (0, 2):
+        _check(st, "rarn_plan_fp8in")
+    return buf.value.decode()
 
 
 def plan_gemm(T: int, H: int, K: int, dtype: str = "bf16") -> str:

@@ -988,7 +988,7 @@ rarn_status rarn_reduce_add_rms_norm_fp8in(void *y, const void *partials, int32_
     p.wait_limit_ns = stream::kWaitLimitNs;
     p.stall_fill = -1;
     p.max_smem = d->max_smem_optin;
-    if (q8in::stream_plan_for(p, s, d->num_sms).ppt > 0) {
+    if (q8in::choose_kernel(p, s, d->num_sms).ring) {
         const long long f = g_stall_fill.exchange(-1);
         if (f >= 0) {
             p.stall_fill = f;
@@ -1004,6 +1004,34 @@ rarn_status rarn_reduce_add_rms_norm_fp8in(void *y, const void *partials, int32_
     default: e = launch_q8in<float>(p, d->num_sms, pdl, cs); break;
     }
     if (e != cudaSuccess) return cuda_fail(e);
+    return RARN_OK;
+}
+
+rarn_status rarn_plan_fp8in(int64_t T, int64_t H, int32_t R, rarn_dtype dt, int codes_aligned16,
+                            int32_t num_sms, int32_t max_smem, char *out, size_t cap) {
+    if (!out || cap == 0) return RARN_ERR_INVALID_ARG;
+    if (!dtype_ok(dt) || T < 0 || H <= 0 || R < 1 || num_sms < 1 || max_smem < 0)
+        return RARN_ERR_INVALID_ARG;
+    if (R > 16 || H % 8 != 0 || H > (dt == RARN_F32 ? 8192 : 16384)) {
+        snprintf(out, cap, "none: unsupported shape or type");
+        return RARN_ERR_UNSUPPORTED;
+    }
+    const int s = elem_size(dt);
+    const q8in::KernelChoice k =
+        q8in::choose_kernel(T, H, R, s, codes_aligned16 != 0, num_sms, max_smem);
+    if (k.ring) {
+        const q8in::SLayout L =
+            q8in::slayout(k.sp.stages, R, k.sp.ppt, s, H, q8in::kStreamWarps);
+        snprintf(out, cap,
+                 "q8in.ring warps=%d ppt=%d chunk_elems=%d stages=%d stage_bytes=%d smem=%d "
+                 "grid=%lld block=%d",
+                 q8in::kStreamWarps, k.sp.ppt, 32 * q8in::kStreamWarps * k.sp.ppt * 8,
+                 k.sp.stages, L.stage_bytes, k.sp.smem,
+                 (long long)std::min<int64_t>(T, num_sms), 32 + 32 * q8in::kStreamWarps);
+    } else {
+        snprintf(out, cap, "q8in.rows pack=%d vpt=%d block=%d grid=occupancy", k.pack, k.vpt,
+                 k.block);
+    }
     return RARN_OK;
 }
 

@@ -606,22 +606,53 @@ inline StreamPlan plan_stream(int64_t H, int R, int s, int max_smem) {
     return StreamPlan{};
 }
 
-// The TMA-fed kernel's plan when it runs (ppt > 0): rows of a multiple of 16
-// elements (16-byte code copies), 16-byte aligned codes, more than 4
-// partials and at least 8 rows per SM.  Measured (CUDA-graph timing, bf16
-// unless noted, register kernel / TMA-fed kernel, us): R = 8 [8192, 8192]
-// 233 / 157 (f16 234 / 156; binary32 [8192, 4096] 155 / 109); R = 16
-// [4096, 8192] 166 / 118; R = 6 [8192, 8192] 194 / 139; R = 4 [16384, 4096]
-// 132 / 133; R = 2 [32768, 4096] 188 / 243; R = 8 [304, 8192] 7.3 / 8.0.
-// RARN_Q8IN_STREAM = 0 / 1 switches it off / forces it (any shape it can
-// take) for measurements and tests.
-inline StreamPlan stream_plan_for(const Params &p, int s, int num_sms) {
+// Which kernel a call takes (pure host logic; the launcher and the plan query
+// share it).  The TMA-fed kernel (ring = true) needs rows of a multiple of 16
+// elements (16-byte code copies) and 16-byte aligned codes, and is chosen for
+// more than 4 partials and at least 8 rows per SM.  Measured (CUDA-graph
+// timing, bf16 unless noted, register kernel / TMA-fed kernel, us): R = 8
+// [8192, 8192] 233 / 157 (f16 234 / 156; binary32 [8192, 4096] 155 / 109);
+// R = 16 [4096, 8192] 166 / 118; R = 6 [8192, 8192] 194 / 139; R = 4
+// [16384, 4096] 132 / 133; R = 2 [32768, 4096] 188 / 243; R = 8 [304, 8192]
+// 7.3 / 8.0.  Otherwise a register kernel: 16-element packs where H is a
+// multiple of 16, else 8-element packs, `vpt` packs per thread so that a row
+// takes at most 256 threads (vpt = 0: H too long for the type).
+// RARN_Q8IN_STREAM = 0 / 1 switches the TMA-fed kernel off / forces it (any
+// shape it can take); RARN_Q8IN_16 = 0 switches the 16-element packs off; both
+// for measurements and tests.
+struct KernelChoice {
+    bool ring = false;
+    StreamPlan sp;       // ring
+    int pack = 0;        // register kernels: elements per pack (8 or 16)
+    int vpt = 0;         // register kernels: packs per thread
+    int block = 0;       // register kernels: threads per CTA
+};
+
+inline KernelChoice choose_kernel(int64_t T, int64_t H, int R, int s, bool codes_aligned16,
+                                  int num_sms, int max_smem) {
+    KernelChoice k;
     const char *sv = getenv("RARN_Q8IN_STREAM");
     const int force = sv && *sv ? atoi(sv) : -1;
-    if (force == 0 || p.H % 16 != 0 || (reinterpret_cast<uintptr_t>(p.codes) & 15u) != 0 ||
-        (force != 1 && (p.R <= 4 || p.T < 8 * (int64_t)num_sms)))
-        return StreamPlan{};
-    return plan_stream(p.H, p.R, s, p.max_smem);
+    if (force != 0 && H % 16 == 0 && codes_aligned16 &&
+        (force == 1 || (R > 4 && T >= 8 * (int64_t)num_sms))) {
+        k.sp = plan_stream(H, R, s, max_smem);
+        if (k.sp.ppt > 0) {
+            k.ring = true;
+            return k;
+        }
+    }
+    const char *v16 = getenv("RARN_Q8IN_16");
+    k.pack = H % 16 == 0 && !(v16 && atoi(v16) == 0) ? 16 : 8;
+    const int64_t nv = H / k.pack;
+    k.vpt = nv <= 256 ? 1 : nv <= 512 ? 2 : nv <= 1024 ? 4 : 8;
+    if ((k.pack == 16 && k.vpt == 8) || (k.vpt == 8 && s == 4)) k.vpt = 0;
+    if (k.vpt > 0) k.block = (int)(((nv + k.vpt - 1) / k.vpt + 31) / 32 * 32);
+    return k;
+}
+
+inline KernelChoice choose_kernel(const Params &p, int s, int num_sms) {
+    return choose_kernel(p.T, p.H, p.R, s, (reinterpret_cast<uintptr_t>(p.codes) & 15u) == 0,
+                         num_sms, p.max_smem);
 }
 
 template <typename T, int PPT, int RMAX>
@@ -644,45 +675,36 @@ static cudaError_t launch_stream_r(const Params &p, const StreamPlan &sp, int gr
 
 }  // namespace q8in
 
-// Packs per thread so that a row takes at most 256 threads (H <= 16384;
-// binary32 storage H <= 8192); grid-stride over rows with a few CTAs per SM.
+// Launch the kernel choose_kernel picks (H <= 16384; binary32 storage
+// H <= 8192); the register kernels grid-stride over rows with every CTA
+// resident, the TMA-fed kernel has one CTA per SM.
 template <typename T>
 cudaError_t launch_q8in(const q8in::Params &p, int num_sms, bool pdl, cudaStream_t st) {
     using namespace q8in;
-    const StreamPlan sp = stream_plan_for(p, (int)sizeof(T), num_sms);
-    if (sp.ppt > 0) {
+    const KernelChoice k = choose_kernel(p, (int)sizeof(T), num_sms);
+    cudaError_t e = cudaErrorInvalidValue;
+    if (k.ring) {
         const int grid = (int)std::min<int64_t>(p.T, num_sms);
-        const cudaError_t e = sp.ppt == 2 ? launch_stream_r<T, 2>(p, sp, grid, pdl, st)
-                                          : launch_stream_r<T, 1>(p, sp, grid, pdl, st);
-        return e != cudaSuccess ? e : cudaGetLastError();
-    }
-    if (p.H % 16 == 0 && !(getenv("RARN_Q8IN_16") && atoi(getenv("RARN_Q8IN_16")) == 0)) {
-        // 16-element packs (measurements can switch them off)
-        const int64_t nv = p.H / 16;
-        const int vpt = nv <= 256 ? 1 : nv <= 512 ? 2 : 4;
-        const dim3 block(static_cast<unsigned>((nv + vpt - 1) / vpt + 31) / 32 * 32);
-        cudaError_t e;
-        switch (vpt) {
+        e = k.sp.ppt == 2 ? launch_stream_r<T, 2>(p, k.sp, grid, pdl, st)
+                          : launch_stream_r<T, 1>(p, k.sp, grid, pdl, st);
+    } else if (k.pack == 16) {
+        const dim3 block(static_cast<unsigned>(k.block));
+        switch (k.vpt) {
         case 1: e = launch_r16<T, 1>(p, num_sms, block, pdl, st); break;
         case 2: e = launch_r16<T, 2>(p, num_sms, block, pdl, st); break;
-        default: e = launch_r16<T, 4>(p, num_sms, block, pdl, st); break;
+        case 4: e = launch_r16<T, 4>(p, num_sms, block, pdl, st); break;
+        default: break;
         }
-        return e != cudaSuccess ? e : cudaGetLastError();
-    }
-    const int64_t nv = p.H / 8;
-    const int vpt = nv <= 256 ? 1 : nv <= 512 ? 2 : nv <= 1024 ? 4 : 8;
-    if (vpt == 8 && sizeof(T) == 4) return cudaErrorInvalidValue;
-    const dim3 block(static_cast<unsigned>((nv + vpt - 1) / vpt + 31) / 32 * 32);
-    cudaError_t e;
-    switch (vpt) {
-    case 1: e = launch_r<T, 1>(p, num_sms, block, pdl, st); break;
-    case 2: e = launch_r<T, 2>(p, num_sms, block, pdl, st); break;
-    case 4: e = launch_r<T, 4>(p, num_sms, block, pdl, st); break;
-    default:
-        if constexpr (sizeof(T) == 4) {
-            e = cudaErrorInvalidValue;
-        } else {
-            e = launch_r<T, 8>(p, num_sms, block, pdl, st);
+    } else {
+        const dim3 block(static_cast<unsigned>(k.block));
+        switch (k.vpt) {
+        case 1: e = launch_r<T, 1>(p, num_sms, block, pdl, st); break;
+        case 2: e = launch_r<T, 2>(p, num_sms, block, pdl, st); break;
+        case 4: e = launch_r<T, 4>(p, num_sms, block, pdl, st); break;
+        case 8:
+            if constexpr (sizeof(T) != 4) e = launch_r<T, 8>(p, num_sms, block, pdl, st);
+            break;
+        default: break;
         }
     }
     return e != cudaSuccess ? e : cudaGetLastError();

@@ -387,6 +387,56 @@ def test_gemm_form_argument_errors(lib):
                 _rows(None, H, BF16), None, 0, H, K, 1e-6, wsp=None) == OK  # T = 0
 
 
+def test_plan_fp8in(monkeypatch):
+    """Which kernel the reduce over 8-bit partials takes (pure host logic; a
+    GB300's 152 SMs and 232448 bytes of opt-in shared memory per CTA)."""
+    monkeypatch.delenv("RARN_Q8IN_STREAM", raising=False)
+    monkeypatch.delenv("RARN_Q8IN_16", raising=False)
+    p = rarn.plan_fp8in(8192, 8192, 8)
+    # the bench shape: 5 stages of 8 code chunks + a residual chunk of 4096
+    # elements; the ncu capture of it reports 221.84 KB dynamic shared memory
+    assert p == ("q8in.ring warps=16 ppt=1 chunk_elems=4096 stages=5 stage_bytes=40960 "
+                 "smem=221840 grid=152 block=544"), p
+    assert rarn.plan_fp8in(8192, 8192, 4) == "q8in.rows pack=16 vpt=2 block=256 grid=occupancy"
+    assert rarn.plan_fp8in(8 * 152 - 1, 8192, 8).startswith("q8in.rows")  # < 8 rows per SM
+    assert rarn.plan_fp8in(8 * 152, 8192, 8).startswith("q8in.ring")
+    assert rarn.plan_fp8in(8192, 8200, 8) == "q8in.rows pack=8 vpt=8 block=160 grid=occupancy"
+    assert rarn.plan_fp8in(8192, 8192, 8, codes_aligned16=False).startswith("q8in.rows")
+    assert rarn.plan_fp8in(4096, 16384, 16).startswith("q8in.ring")
+    assert rarn.plan_fp8in(8, 1020, 2).startswith("none")
+    assert rarn.plan_fp8in(8, 16384, 2, "f32").startswith("none")
+    monkeypatch.setenv("RARN_Q8IN_16", "0")
+    assert rarn.plan_fp8in(64, 4096, 2) == "q8in.rows pack=8 vpt=2 block=256 grid=occupancy"
+    monkeypatch.setenv("RARN_Q8IN_STREAM", "1")
+    assert rarn.plan_fp8in(5, 512, 1).startswith("q8in.ring")
+    assert rarn.plan_fp8in(5, 520, 1).startswith("q8in.rows")  # H not a multiple of 16
+    monkeypatch.setenv("RARN_Q8IN_STREAM", "0")
+    assert rarn.plan_fp8in(8192, 8192, 8).startswith("q8in.rows")
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+def test_plan_fp8in_ring_fits(dt, monkeypatch):
+    """The TMA-fed kernel forced on every partial count and a spread of row
+    lengths: the ring always fits the opt-in shared memory with the row copy
+    and control words, keeps at least 2 stages (4 with two units per
+    thread), and every bulk copy is a whole number of 16-byte blocks."""
+    monkeypatch.setenv("RARN_Q8IN_STREAM", "1")
+    s = 4 if dt == "f32" else 2
+    for R in range(1, 17):
+        for H in (16, 1040, 4096, 8192, 8192 if dt == "f32" else 16384):
+            p = rarn.plan_fp8in(1000, H, R, dt)
+            assert p.startswith("q8in.ring"), (R, H, p)
+            kv = {k: int(v) for k, v in (f.split("=") for f in p.split()[1:])}
+            ppt, stages, sb, smem, chunk = (kv[k] for k in ("ppt", "stages", "stage_bytes",
+                                                               "smem", "chunk_elems"))
+            assert chunk == 512 * 8 * ppt
+            assert stages >= (4 if ppt == 2 else 2) and smem <= 232448
+            assert sb % 128 == 0 and sb >= R * chunk + chunk * s
+            assert smem >= stages * sb + H * s
+            last = H % chunk or chunk  # elements in a row's last chunk
+            assert (last * 1) % 16 == 0 and (last * s) % 16 == 0
+
+
 def test_plan_gemm(monkeypatch):
     """Columns per CTA from H; the K slab and ring depth fill one SM's shared
     memory; the workspace holds one float per row and column tile."""
