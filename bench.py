@@ -531,8 +531,13 @@ def fp8in_tensors(device, R=8, T=8192, H=8192):
     return codes, scales, res, g, R * T * H + 3 * T * H * 2 + H * 2 + R * 4
 
 
-FP8IN_PLAN = ("q8in TMA-fed ring kernel (producer warp + 16 consumer warps per SM), R = 8, "
-              "e4m3")
+def fp8in_plan(device, rarn, R=8, T=8192, H=8192) -> str:
+    """The library's description of the kernel the 8-bit-partials call takes
+    on this device (its SM count and opt-in shared memory per CTA)."""
+    import torch
+    props = torch.cuda.get_device_properties(device)
+    smem = getattr(props, "shared_memory_per_block_optin", 0) or 232448
+    return rarn.plan_fp8in(T, H, R, "bf16", True, props.multi_processor_count, smem)
 
 
 def time_fp8in(device, rarn, R=8, T=8192, H=8192):
@@ -550,7 +555,7 @@ def time_fp8in(device, rarn, R=8, T=8192, H=8192):
     return {"kind": "widened (8-bit partials)", "us_per_launch": us, "gbs": gbs,
             "rows_per_s": T / (us / 1e6), "frac_of_peak": gbs / peak, "algorithmic_bytes": alg,
             "timing": "CUDA graph of 10 launches, best of 3 (inputs larger than L2)",
-            "plan": FP8IN_PLAN}
+            "plan": fp8in_plan(device, rarn, R, T, H)}
 
 
 def main_fp8in(args, device, rank, world):
@@ -561,6 +566,7 @@ def main_fp8in(args, device, rank, world):
 
     import residual_add_rmsnorm_gb300 as rarn
     codes, scales, res, g, alg = fp8in_tensors(device)
+    plan = fp8in_plan(device, rarn)
     y = torch.empty_like(res)
     call = lambda: rarn.reduce_add_rms_norm_fp8in(codes, scales, res, g, 1e-6, "e4m3", out=y)
     stream = torch.cuda.current_stream(device)
@@ -582,11 +588,11 @@ def main_fp8in(args, device, rank, world):
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": FP8IN_NAME, "R": 8, "T": 8192, "H": 8192, "format": "e4m3",
-                   "storage": "bf16", "plan": FP8IN_PLAN,
+                   "storage": "bf16", "plan": plan,
                    "l2": "inputs larger than L2 (0.9 GB)", "pdl": not args.no_pdl},
         "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peak, "unit": "GB/s",
                      "frac": gbs / world / peak,
-                     "traffic": ncu_traffic(FP8IN_NAME, FP8IN_PLAN), "peak_source": kind},
+                     "traffic": ncu_traffic(FP8IN_NAME, plan), "peak_source": kind},
         "cpu_baseline": None,
         "e2e": {"value": None, "unit": "GB/s",
                 "note": "no host-buffer entry point for the 8-bit-partials form"},
