@@ -112,11 +112,14 @@ def test_fp8in_full_size_sampled():
     check(codes, scales, r, g, "bf16", "e4m3", "full size", rows=rows)
 
 
+@pytest.mark.parametrize("ring", ["0", "1"])
 @pytest.mark.parametrize("pdl", [True, False])
-def test_fp8in_chained(pdl):
+def test_fp8in_chained(pdl, ring, monkeypatch):
     """Two dependent launches: the second reduces on the residual the first
-    wrote; replayed on the CPU with the oracle."""
+    wrote (for the TMA-fed kernel, bulk copies of what the previous launch
+    stored); replayed on the CPU with the oracle."""
     import torch
+    monkeypatch.setenv("RARN_Q8IN_STREAM", ring)
     rarn.set_pdl(pdl)
     try:
         R, T, H = 3, 40, 2048
