@@ -109,6 +109,15 @@ CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reason
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
 
+def nvsmi_id(props, fallback: int) -> str:
+    """The `nvidia-smi -i` identifier of a torch device: its UUID as
+    nvidia-smi prints it ("GPU-..."), else the CUDA index."""
+    gpu_id = str(getattr(props, "uuid", fallback))
+    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
+        gpu_id = "GPU-" + gpu_id
+    return gpu_id
+
+
 class ClockSampler:
     """nvidia-smi sampling every 200 ms while the measurement runs."""
 
@@ -570,11 +579,7 @@ def main_fp8in(args, device, rank, world):
     y = torch.empty_like(res)
     call = lambda: rarn.reduce_add_rms_norm_fp8in(codes, scales, res, g, 1e-6, "e4m3", out=y)
     stream = torch.cuda.current_stream(device)
-    props = torch.cuda.get_device_properties(device)
-    gpu_id = str(getattr(props, "uuid", 0))
-    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
-        gpu_id = "GPU-" + gpu_id
-    sampler = ClockSampler(gpu_id)
+    sampler = ClockSampler(nvsmi_id(torch.cuda.get_device_properties(device), device.index or 0))
     ms = time_steps(call, args.steps, args.warmup, stream)
     clocks = sampler.stop()
     ms = max_over_ranks(ms, device)
@@ -641,11 +646,7 @@ def main_gemm(args, gw, device, rank, world):
                      device=device)
     call = lambda: rarn.gemm_add_rms_norm(a, w, r, g, gw.eps, out=y, workspace=ws)
     stream = torch.cuda.current_stream(device)
-    props = torch.cuda.get_device_properties(device)
-    gpu_id = str(getattr(props, "uuid", 0))
-    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
-        gpu_id = "GPU-" + gpu_id
-    sampler = ClockSampler(gpu_id)
+    sampler = ClockSampler(nvsmi_id(torch.cuda.get_device_properties(device), device.index or 0))
     ms = time_steps(call, args.steps, args.warmup, stream)
     clocks = sampler.stop()
     ms = max_over_ranks(ms, device)
@@ -710,10 +711,7 @@ def main():
     dense = w in W.CONFIGS  # the forms the host-buffer entry points and the oracle leg cover
 
     props = torch.cuda.get_device_properties(device)
-    gpu_id = str(getattr(props, "uuid", local_rank))
-    if gpu_id and not gpu_id.startswith("GPU-") and "-" in gpu_id:
-        gpu_id = "GPU-" + gpu_id
-    sampler = ClockSampler(gpu_id)
+    sampler = ClockSampler(nvsmi_id(props, local_rank))
     ms = time_steps(call, args.steps, args.warmup, stream)
     clocks = sampler.stop()
     ms = max_over_ranks(ms, device)

@@ -47,3 +47,16 @@ def test_traffic_lookup_keys(bench, tmp_path, monkeypatch):
     entry["source_sha"] = "0" * 64
     f.write_text(json.dumps({"entries": [entry]}))
     assert bench.ncu_traffic("w", "p") is None
+
+
+def test_nvsmi_id(bench):
+    """nvidia-smi is given the device's UUID with its "GPU-" prefix, or the
+    CUDA index when torch reports no UUID."""
+    class P:
+        pass
+    p = P()
+    assert bench.nvsmi_id(p, 3) == "3"
+    p.uuid = "1a2b3c4d-0000-1111-2222-333344445555"
+    assert bench.nvsmi_id(p, 3) == "GPU-1a2b3c4d-0000-1111-2222-333344445555"
+    p.uuid = "GPU-1a2b"
+    assert bench.nvsmi_id(p, 0) == "GPU-1a2b"
