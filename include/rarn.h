@@ -425,10 +425,11 @@ rarn_status rarn_set_pdl(int enable);
 int rarn_get_pdl(void);
 
 /*
- * Test hook for the watchdog: in the next launch (on any thread) of the
- * stream kernel or of the GEMM form, CTA 0 expects 16 bytes more for pipeline
- * fill number `fill` (0-based, in issue order) than its copies bring, so that
- * fill never completes; every shared-memory barrier wait of that launch is
+ * Test hook for the watchdog: in the next launch (on any thread) of a stream
+ * kernel (16-bit partials, or the TMA-fed kernel of
+ * rarn_reduce_add_rms_norm_fp8in) or of the GEMM form, CTA 0 expects 16 bytes
+ * more for pipeline fill number `fill` (0-based, in issue order) than its
+ * copies bring, so that fill never completes; every shared-memory barrier wait of that launch is
  * bounded by `wait_limit_ns` (1 ns .. 2 s).  The waits on that fill run out:
  * the kernel sets the watchdog word (bit 0 / 1: stream consumer / producer;
  * bit 2: GEMM kernel) and returns with its outputs invalid, and the context
