@@ -516,7 +516,7 @@ def time_gemm(gw, device, rarn):
             "unfused_us": us_unfused, "cublas_matmul_us": us_mm,
             "timing": "CUDA graph of 10 launches, best of 3 (operands L2-resident after the "
                       "first launch)",
-            "plan": rarn.plan_gemm(gw.T, gw.H, gw.K, gw.dtype)}
+            "plan": rarn.plan_gemm(gw.T, gw.H, gw.K, gw.dtype, num_sms=0)}
 
 
 FP8IN_NAME = "reduce8_e4m3in_bf16_T8192_H8192"
@@ -660,7 +660,7 @@ def main_gemm(args, gw, device, rank, world):
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": gw.dtype, "data": "synthetic",
         "config": {"workload": gw.name, "T": gw.T, "H": gw.H, "K": gw.K,
-                   "plan": rarn.plan_gemm(gw.T, gw.H, gw.K, gw.dtype),
+                   "plan": rarn.plan_gemm(gw.T, gw.H, gw.K, gw.dtype, num_sms=0),
                    "l2": "operands L2-resident after the first step (64 MB)",
                    "pdl": not args.no_pdl},
         "roofline": {"bound": "tensor", "achieved": tflops / world, "peak": peak,

@@ -353,11 +353,11 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
  * live in a file-scope device array of 2^20 binary32 values (4 MiB, 256-byte
  * aligned) that the library reserves on every GPU it is loaded on and keeps
  * until the process exits.  One launch sequence holds T (H / 128 + 1) of
- * those values, so a call with more rows than the array holds (16128 rows at
- * H = 8192, 7936 at H = 16384) runs as several launch sequences on `stream`,
- * one after another.  Every partial sum is written before it is read and the
- * counters are zeroed by the call itself, so nothing needs clearing between
- * calls.
+ * those values, so a call with more rows than the array holds
+ * (rarn_gemm_noalloc_rows(H): 16128 rows at H = 8192, 8064 at H = 16384)
+ * runs as several launch sequences on `stream`, one after another.  Every
+ * partial sum is written before it is read and the counters are zeroed by
+ * the call itself, so nothing needs clearing between calls.
  *
  * Set-up: the first call on each device (with that device current) looks up
  * the array's device address with cudaGetSymbolAddress and keeps it; make
@@ -369,12 +369,20 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
  * with no ordering between them) race on it and give wrong results; issue
  * them on one stream or synchronise the streams.
  *
- * Arguments and errors as for rarn_gemm_add_rms_norm; H beyond the supported
- * tilings returns RARN_ERR_UNSUPPORTED.  Results are bit-identical to the
- * workspace form, except for T <= 128 where the workspace form splits K and
- * the scratch cannot hold the split's partial products (9 T H binary32
- * values): this entry point then runs without split K, a different binary32
- * summation order within the same accuracy bound.
+ * Arguments and errors as for rarn_gemm_add_rms_norm, checked once over all
+ * T rows before anything is enqueued: overlaps between rows that different
+ * launch sequences would cover return RARN_ERR_ALIAS like any other, and an
+ * argument error leaves every buffer untouched.  (A launch failure, reported
+ * as RARN_ERR_CUDA, can still come after earlier sequences were enqueued.)
+ * Results are bit-identical to the workspace form's, with one exception:
+ * for T <= 128 the workspace form splits K over S <= 9 CTAs per column tile
+ * (S = the split count rarn_plan_gemm reports), and this entry point does
+ * the same only where the split's partial products fit in the array next to
+ * the partial sums, i.e. where
+ *   64 * ceil((4 * ceil(T * H / 512) + ceil(T / 128)) / 64) + S * T * H <= 2^20
+ * binary32 values (T = 8, H = 4096, S = 8 fits; T = 128, H = 4096 does not).
+ * Otherwise it runs without split K: a different binary32 summation order,
+ * within the same accuracy bound.
  */
 rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w,
                                            rarn_rows residual, const void *gamma, int64_t T,
@@ -397,8 +405,18 @@ int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H);
 rarn_status rarn_plan_fp8in(int64_t T, int64_t H, int32_t R, rarn_dtype dt, int codes_aligned16,
                             int32_t num_sms, int32_t max_smem, char *out, size_t cap);
 
-/* Describe the GEMM kernels' tiling for a problem (pure host logic). */
-rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, char *out, size_t cap);
+/* Rows that one launch sequence of rarn_gemm_add_rms_norm_noalloc covers for
+ * a row length H: floor(floor((2^20 - 16) / (H / 128 + 1)) / 128) * 128
+ * (16128 at H = 8192, 8064 at H = 16384); -1 if H is not supported. */
+int64_t rarn_gemm_noalloc_rows(int64_t H);
+
+/* Describe the GEMM kernels' tiling for a problem on a device with `num_sms`
+ * SMs (if <= 0 the current device is queried; pure host logic when > 0),
+ * under the current tuning knobs.  Writes a NUL-terminated description into
+ * out[cap]; RARN_ERR_UNSUPPORTED (out says so) for a shape or type the GEMM
+ * form rejects. */
+rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, int32_t num_sms,
+                           char *out, size_t cap);
 
 /* Static text for a status code. */
 const char *rarn_status_string(rarn_status s);
@@ -423,6 +441,52 @@ rarn_path rarn_get_path(void);
  */
 rarn_status rarn_set_pdl(int enable);
 int rarn_get_pdl(void);
+
+/*
+ * Planner overrides for measurements and tests (process-wide, read by every
+ * later call from any thread).  Each knob holds -1 ("the planner's own
+ * choice", the default) or one of the values listed beside it; the planner
+ * still applies its own limits after an override (a register budget, the
+ * shared memory that fits, the shapes a kernel can take), so an override can
+ * only steer the choice among kernels that can run the call.  Results are
+ * the same under every setting, up to the documented summation-order
+ * differences between kernel families.  Nothing here is read from the
+ * environment.
+ */
+typedef enum rarn_tuning {
+    RARN_TUNE_ROWS_PER_THREAD = 0,  /* 1, 2, 4, 8 (16: scalar rows): 16-byte packs per
+                                       thread of the CTA-per-row kernels (grown again
+                                       until the row fits the register budget) */
+    RARN_TUNE_ROWS_GRID = 1,        /* 1 .. 2^31-1: CTAs of the CTA-per-row kernels
+                                       (at most T) */
+    RARN_TUNE_ROWS_PIPELINE = 2,    /* 0: no software pipelining across rows */
+    RARN_TUNE_L2_ROWS = 3,          /* 0 .. 8: rows each CTA prefetches into L2 before
+                                       its dependency wait (device buffers) */
+    RARN_TUNE_STREAM_PACKS = 4,     /* 1, 2, 4: 16-byte packs per consumer thread and
+                                       pipeline chunk of the stream kernel */
+    RARN_TUNE_STREAM_GROUPS = 5,    /* 1, 2: consumer groups of the stream kernel when
+                                       RARN_PATH_STREAM is forced */
+    RARN_TUNE_GEMM_COLS = 6,        /* 256, 512: columns per CTA tile of the GEMM form */
+    RARN_TUNE_GEMM_SLAB = 7,        /* 32, 64: K slab of the GEMM form, in elements */
+    RARN_TUNE_GEMM_CTAS_PER_SM = 8, /* 1, 2: the non-persistent GEMM kernel */
+    RARN_TUNE_GEMM_PERSISTENT = 9,  /* 0, 1: the persistent warp-specialised kernels */
+    RARN_TUNE_GEMM_PAIR = 10,       /* 0, 1: SM pairs (cta_group::2) */
+    RARN_TUNE_GEMM_NORM_IN_EPILOGUE = 11, /* 0: y from a separate norm kernel */
+    RARN_TUNE_GEMM_TAIL_SPLIT = 12, /* 0: no 128-column halves in the last round */
+    RARN_TUNE_GEMM_SPLIT_K = 13,    /* 0: no split K for few rows */
+    RARN_TUNE_FP8IN_RING = 14,      /* 0: register kernels only; 1: the TMA-fed ring
+                                       kernel wherever the shape allows it */
+    RARN_TUNE_FP8IN_PACK16 = 15,    /* 0: 8-element packs in the register kernels */
+    RARN_TUNE_COUNT = 16
+} rarn_tuning;
+
+/* Set one knob (-1 restores the planner's choice).  An unknown knob or a
+ * value outside its list returns RARN_ERR_INVALID_ARG and changes nothing. */
+rarn_status rarn_set_tuning(rarn_tuning knob, int64_t value);
+/* Current value of a knob into *value (-1: the planner's choice). */
+rarn_status rarn_get_tuning(rarn_tuning knob, int64_t *value);
+/* Every knob back to -1. */
+rarn_status rarn_reset_tuning(void);
 
 /*
  * Test hook for the watchdog: in the next launch (on any thread) of a stream

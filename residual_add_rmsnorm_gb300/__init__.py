@@ -29,7 +29,8 @@ __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_ho
            "DTYPE_CODES", "rms_norm_ex", "fused_add_rms_norm_ex", "reduce_add_rms_norm_ex",
            "rms_norm_fp8", "fused_add_rms_norm_fp8", "reduce_add_rms_norm_fp8", "plan_fp8",
            "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm", "plan_fp8in",
-           "gemm_workspace_bytes", "gemm_add_rms_norm_noalloc", "reduce_add_rms_norm_fp8in"]
+           "gemm_workspace_bytes", "gemm_add_rms_norm_noalloc", "reduce_add_rms_norm_fp8in",
+           "TUNING", "set_tuning", "get_tuning", "reset_tuning", "tuning", "gemm_noalloc_rows"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
@@ -39,6 +40,12 @@ OP_CODES = {"rms_norm": 0, "fused_add_rms_norm": 1, "reduce_add_rms_norm": 2}
 PATHS = {"auto": 0, "rows": 1, "stream": 2, "cluster": 3}
 FP8_FORMATS = {"e4m3": 0, "e5m2": 1}
 SCALE_MODES = {"tensor": 0, "row": 1}
+# rarn_tuning knobs (planner overrides; -1 is the planner's own choice)
+TUNING = {"rows_per_thread": 0, "rows_grid": 1, "rows_pipeline": 2, "l2_rows": 3,
+          "stream_packs": 4, "stream_groups": 5, "gemm_cols": 6, "gemm_slab": 7,
+          "gemm_ctas_per_sm": 8, "gemm_persistent": 9, "gemm_pair": 10,
+          "gemm_norm_in_epilogue": 11, "gemm_tail_split": 12, "gemm_split_k": 13,
+          "fp8in_ring": 14, "fp8in_pack16": 15}
 STATUS = {0: "RARN_OK", 1: "RARN_ERR_INVALID_ARG", 2: "RARN_ERR_UNSUPPORTED",
           3: "RARN_ERR_ALIAS", 4: "RARN_ERR_CUDA"}
 
@@ -141,7 +148,8 @@ def library() -> ctypes.CDLL:
     lib.rarn_reduce_add_rms_norm_fp8in.restype = c_int
     lib.rarn_gemm_workspace_bytes.argtypes = [i64, i64]
     lib.rarn_gemm_workspace_bytes.restype = i64
-    lib.rarn_plan_gemm.argtypes = [i64, i64, i64, c_int, ctypes.c_char_p, ctypes.c_size_t]
+    lib.rarn_plan_gemm.argtypes = [i64, i64, i64, c_int, ctypes.c_int32, ctypes.c_char_p,
+                                   ctypes.c_size_t]
     lib.rarn_plan_gemm.restype = c_int
     lib.rarn_plan_fp8in.argtypes = [i64, i64, ctypes.c_int32, c_int, c_int, ctypes.c_int32,
                                     ctypes.c_int32, ctypes.c_char_p, ctypes.c_size_t]
@@ -152,6 +160,14 @@ def library() -> ctypes.CDLL:
     lib.rarn_get_pdl.restype = c_int
     lib.rarn_test_stall.argtypes = [ctypes.c_longlong, ctypes.c_ulonglong]
     lib.rarn_test_stall.restype = c_int
+    lib.rarn_set_tuning.argtypes = [c_int, i64]
+    lib.rarn_set_tuning.restype = c_int
+    lib.rarn_get_tuning.argtypes = [c_int, ctypes.POINTER(i64)]
+    lib.rarn_get_tuning.restype = c_int
+    lib.rarn_reset_tuning.argtypes = []
+    lib.rarn_reset_tuning.restype = c_int
+    lib.rarn_gemm_noalloc_rows.argtypes = [i64]
+    lib.rarn_gemm_noalloc_rows.restype = i64
     _lib = lib
     return lib
 
@@ -497,6 +513,12 @@ def plan_fp8(op: str, T: int, H: int, R: int, dtype: str, vec_ok: bool = True,
     return buf.value.decode()
 
 
+def gemm_noalloc_rows(H: int) -> int:
+    """Rows one launch sequence of gemm_add_rms_norm_noalloc covers at row
+    length H (-1: H unsupported)."""
+    return int(library().rarn_gemm_noalloc_rows(H))
+
+
 def gemm_workspace_bytes(T: int, H: int) -> int:
     """Workspace bytes the GEMM form needs for T rows of H (-1: H unsupported)."""
     return int(library().rarn_gemm_workspace_bytes(T, H))
@@ -607,13 +629,52 @@ def plan_fp8in(T: int, H: int, R: int, dtype: str = "bf16", codes_aligned16: boo
     return buf.value.decode()
 
 
-def plan_gemm(T: int, H: int, K: int, dtype: str = "bf16") -> str:
-    """The GEMM kernel's tiling for a problem (host logic only)."""
+def plan_gemm(T: int, H: int, K: int, dtype: str = "bf16", num_sms: int = 152) -> str:
+    """The GEMM kernel's tiling for a problem on a device with ``num_sms`` SMs
+    (host logic only; the default is a GB300's; 0 queries the current
+    device)."""
     buf = ctypes.create_string_buffer(256)
-    st = library().rarn_plan_gemm(T, H, K, DTYPE_CODES[dtype], buf, 256)
+    st = library().rarn_plan_gemm(T, H, K, DTYPE_CODES[dtype], num_sms, buf, 256)
     if st not in (0, 2):
         _check(st, "rarn_plan_gemm")
     return buf.value.decode()
+
+
+def set_tuning(name: str, value: int) -> None:
+    """Set one planner override (``TUNING`` names it; -1 restores the
+    planner's choice).  Raises RarnError for a value outside the knob's list."""
+    _check(library().rarn_set_tuning(TUNING[name], int(value)), f"rarn_set_tuning({name})")
+
+
+def get_tuning(name: str) -> int:
+    v = ctypes.c_int64(0)
+    _check(library().rarn_get_tuning(TUNING[name], ctypes.byref(v)), "rarn_get_tuning")
+    return v.value
+
+
+def reset_tuning() -> None:
+    """Every planner override back to the planner's choice."""
+    _check(library().rarn_reset_tuning(), "rarn_reset_tuning")
+
+
+class tuning:
+    """Context manager: ``with tuning(gemm_pair=0): ...`` sets the named
+    knobs and restores their previous values on exit."""
+
+    def __init__(self, **knobs):
+        self.knobs = knobs
+        self.saved = {}
+
+    def __enter__(self):
+        for k, v in self.knobs.items():
+            self.saved[k] = get_tuning(k)
+            set_tuning(k, v)
+        return self
+
+    def __exit__(self, *exc):
+        for k, v in self.saved.items():
+            set_tuning(k, v)
+        return False
 
 
 def set_pdl(enable: bool) -> None:

@@ -18,10 +18,13 @@
 
 namespace rarn {
 // instantiated in q8in_{bf16,f16,f32}.cu
-extern template cudaError_t launch_q8in<__nv_bfloat16>(const q8in::Params &, int, bool,
+extern template cudaError_t launch_q8in<__nv_bfloat16>(const q8in::Params &,
+                                                       const q8in::KernelChoice &, int, bool,
                                                        cudaStream_t);
-extern template cudaError_t launch_q8in<__half>(const q8in::Params &, int, bool, cudaStream_t);
-extern template cudaError_t launch_q8in<float>(const q8in::Params &, int, bool, cudaStream_t);
+extern template cudaError_t launch_q8in<__half>(const q8in::Params &, const q8in::KernelChoice &,
+                                                int, bool, cudaStream_t);
+extern template cudaError_t launch_q8in<float>(const q8in::Params &, const q8in::KernelChoice &,
+                                               int, bool, cudaStream_t);
 }  // namespace rarn
 
 using namespace rarn;
@@ -45,6 +48,40 @@ std::atomic<int> g_pdl{1};
 // kernel or of the GEMM form
 std::atomic<long long> g_stall_fill{-1};
 std::atomic<unsigned long long> g_stall_limit_ns{0};
+
+// Planner overrides (rarn_set_tuning): -1 is the planner's own choice.
+struct Tuning {
+    std::atomic<long long> v[RARN_TUNE_COUNT];
+    Tuning() { reset(); }
+    void reset() {
+        for (auto &x : v) x.store(-1);
+    }
+    long long operator[](rarn_tuning k) const { return v[k].load(std::memory_order_relaxed); }
+};
+Tuning g_tune;
+
+// The values each knob accepts besides -1.
+bool tuning_value_ok(rarn_tuning k, long long x) {
+    switch (k) {
+    case RARN_TUNE_ROWS_PER_THREAD: return x == 1 || x == 2 || x == 4 || x == 8 || x == 16;
+    case RARN_TUNE_ROWS_GRID: return x >= 1 && x <= 0x7fffffffLL;
+    case RARN_TUNE_L2_ROWS: return x >= 0 && x <= 8;
+    case RARN_TUNE_STREAM_PACKS: return x == 1 || x == 2 || x == 4;
+    case RARN_TUNE_STREAM_GROUPS: return x == 1 || x == 2;
+    case RARN_TUNE_GEMM_COLS: return x == 256 || x == 512;
+    case RARN_TUNE_GEMM_SLAB: return x == 32 || x == 64;
+    case RARN_TUNE_GEMM_CTAS_PER_SM: return x == 1 || x == 2;
+    case RARN_TUNE_GEMM_PERSISTENT:
+    case RARN_TUNE_GEMM_PAIR:
+    case RARN_TUNE_FP8IN_RING: return x == 0 || x == 1;
+    case RARN_TUNE_ROWS_PIPELINE:
+    case RARN_TUNE_GEMM_NORM_IN_EPILOGUE:
+    case RARN_TUNE_GEMM_TAIL_SPLIT:
+    case RARN_TUNE_GEMM_SPLIT_K:
+    case RARN_TUNE_FP8IN_PACK16: return x == 0;
+    default: return false;
+    }
+}
 
 constexpr int kMaxDevices = 64;
 
@@ -135,10 +172,7 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms, int r
         const int64_t rounds = ceil_div(T, slots);
         pl.grid = (int)ceil_div(ceil_div(T, rounds), pl.block / 32);
         // pipelined across rows (plain / fused) when every warp has several
-        pl.pipe = op != OP_REDUCE && rounds >= 2;
-        if (const char *v = getenv("RARN_ROWS_PIPE")) {  // measurements only
-            if (*v == '0') pl.pipe = false;
-        }
+        pl.pipe = op != OP_REDUCE && rounds >= 2 && g_tune[RARN_TUNE_ROWS_PIPELINE] != 0;
         return pl;
     }
     // values per thread: aim at 256 threads per row, powers of two, within
@@ -153,10 +187,7 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms, int r
     // [8192, 8192])
     const int target = (op == OP_REDUCE && rn == 2) ? 512 : 256;
     int pt = std::min(max_pt, pow2_at_least(ceil_div(n, target)));
-    if (const char *v = getenv("RARN_ROWS_PT")) {  // measurements only
-        const int f = atoi(v);
-        if (f >= 1 && f <= max_pt && (f & (f - 1)) == 0) pt = f;
-    }
+    if (const long long f = g_tune[RARN_TUNE_ROWS_PER_THREAD]; f >= 1 && f <= max_pt) pt = (int)f;
     while (pt < max_pt && ceil_div(n, pt) > max_block(pt, false)) pt <<= 1;
     if (ceil_div(n, pt) > max_block(pt, false)) {
         pl.kind = KIND_TWO_PASS;
@@ -173,10 +204,8 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms, int r
     const int64_t slots = (int64_t)num_sms * std::max(1, resident_threads / pl.block);
     const int64_t rounds = ceil_div(T, slots);
     pl.grid = (int)ceil_div(T, rounds);
-    if (const char *v = getenv("RARN_ROWS_GRID")) {  // measurements only
-        const int64_t f = atoll(v);
-        if (f > 0) pl.grid = (int)std::min<int64_t>(f, T);
-    }
+    if (const long long f = g_tune[RARN_TUNE_ROWS_GRID]; f > 0)
+        pl.grid = (int)std::min<int64_t>(f, T);
     // Gamma in registers when every CTA has a single row (latency-bound: the
     // gamma load then overlaps the row's loads instead of following the row
     // reduction) and the kernel's register budget allows it.
@@ -188,10 +217,7 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms, int r
         const int streams = op == OP_PLAIN ? 1 : 1 + rn;
         const int pipe_max = rows_max_block(rows_regs_vec(pl.per_thread, epv, op, false, rn) +
                                             pl.per_thread * 4 * streams);
-        pl.pipe = pl.block <= pipe_max;
-        if (const char *v = getenv("RARN_ROWS_PIPE")) {  // measurements only
-            if (*v == '0') pl.pipe = false;
-        }
+        pl.pipe = pl.block <= pipe_max && g_tune[RARN_TUNE_ROWS_PIPELINE] != 0;
     }
     return pl;
 }
@@ -202,8 +228,8 @@ constexpr int64_t kStreamMaxRowBytes = 96 * 1024;
 constexpr int kDefaultMaxSmem = 232448;  // opt-in shared memory per CTA on sm_100 / sm_103
 
 // Packs per consumer thread per chunk: up to two (fewer, larger copies per
-// producer iteration) while at least 4 stages fit.  RARN_STREAM_PPT (1, 2, 4)
-// overrides it for measurements.
+// producer iteration) while at least 4 stages fit; RARN_TUNE_STREAM_PACKS
+// overrides it.
 Plan plan_stream(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_sms,
                  int max_smem, int groups) {
     Plan pl;
@@ -213,10 +239,7 @@ Plan plan_stream(int op, int64_t T, int64_t H, int R, int s, bool vec, int num_s
     const int64_t nv = row_bytes / 16;
     // two packs per thread measured best or equal everywhere (4 only for tests)
     int ppt = std::min<int64_t>(2, pow2_at_least(ceil_div(nv, stream::kConsumers)));
-    if (const char *v = getenv("RARN_STREAM_PPT")) {
-        const int f = atoi(v);
-        if (f == 1 || f == 2 || f == 4) ppt = f;
-    }
+    if (const long long f = g_tune[RARN_TUNE_STREAM_PACKS]; f > 0) ppt = (int)f;
     for (; ppt >= 1; ppt >>= 1) {
         const int chunk = stream::chunk_bytes(ppt);
         for (int g = groups; g >= 1; --g) {
@@ -276,13 +299,11 @@ Plan plan_cluster(int op, int64_t T, int64_t H, int s, bool vec, int num_sms, in
     return pl;
 }
 
-// Consumer groups of the stream kernel when it is forced: RARN_STREAM_GROUPS
-// (1..2) overrides the default for measurements; read on every plan.
+// Consumer groups of the stream kernel when it is forced (RARN_TUNE_STREAM_GROUPS).
 int stream_groups(int fallback) {
-    const char *v = getenv("RARN_STREAM_GROUPS");
-    if (!v || !*v) return fallback;
-    const int g = atoi(v);
-    return g < 1 ? 1 : g > stream::kMaxGroups ? stream::kMaxGroups : g;
+    const long long g = g_tune[RARN_TUNE_STREAM_GROUPS];
+    if (g < 1) return fallback;
+    return g > stream::kMaxGroups ? stream::kMaxGroups : (int)g;
 }
 
 // The automatic choice, from measurements on GB300 (cold L2, CUDA-graph
@@ -549,7 +570,7 @@ rarn_status run_ex(Call c) {
     // plain fp32 [512, 2048] 3.06 / 2.77; fused [128, 5120] 3.51 / 2.90;
     // fused [64, 16384] 4.52 / 3.71; the stream kernel unchanged
     p.l2_rows = c.host_buffers ? 0 : 1;
-    if (const char *v = getenv("RARN_L2_ROWS")) p.l2_rows = atoi(v);  // measurements only
+    if (const long long f = g_tune[RARN_TUNE_L2_ROWS]; f >= 0 && !c.host_buffers) p.l2_rows = (int)f;
     if (pl.kind == KIND_STREAM) {
         const long long f = g_stall_fill.exchange(-1);
         if (f >= 0) {
@@ -805,20 +826,16 @@ rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows parti
 // GEMM producer + fused residual-add RMSNorm: every matrix 16-bit, one type;
 // 16-byte aligned bases and row strides; the caller's workspace holds the
 // column tiles' partial sums of squares.
-static GemmPlan gemm_plan_env(int64_t T, int64_t H, int64_t K, int num_sms = 152,
-                              bool no_splitk = false) {
-    int bk = 0, ns = 0, ctas = 0, persist = -1;  // measurements only
-    if (const char *v = getenv("RARN_GEMM_BK")) bk = atoi(v);
-    if (const char *v = getenv("RARN_GEMM_NS")) ns = atoi(v);
-    if (const char *v = getenv("RARN_GEMM_CTAS")) ctas = atoi(v);
-    if (const char *v = getenv("RARN_GEMM_PERSIST")) persist = atoi(v);
-    int pair = -1, fuse = -1, split = -1, splitk = -1;
-    if (const char *v = getenv("RARN_GEMM_PAIR")) pair = atoi(v);
-    if (const char *v = getenv("RARN_GEMM_FUSE")) fuse = atoi(v);
-    if (const char *v = getenv("RARN_GEMM_SPLIT")) split = atoi(v);
-    if (const char *v = getenv("RARN_GEMM_SPLITK")) splitk = atoi(v);
-    if (no_splitk) splitk = 0;
-    return plan_gemm(T, H, K, bk, ns, ctas, persist, num_sms, pair, fuse, split, splitk);
+static GemmPlan gemm_plan_tuned(int64_t T, int64_t H, int64_t K, int num_sms,
+                                bool no_splitk = false) {
+    auto knob = [](rarn_tuning k) { return (int)g_tune[k]; };
+    const int bk = std::max(0, knob(RARN_TUNE_GEMM_SLAB));
+    const int ns = std::max(0, knob(RARN_TUNE_GEMM_COLS));
+    const int ctas = std::max(0, knob(RARN_TUNE_GEMM_CTAS_PER_SM));
+    const int splitk = no_splitk ? 0 : knob(RARN_TUNE_GEMM_SPLIT_K);
+    return plan_gemm(T, H, K, bk, ns, ctas, knob(RARN_TUNE_GEMM_PERSISTENT), num_sms,
+                     knob(RARN_TUNE_GEMM_PAIR), knob(RARN_TUNE_GEMM_NORM_IN_EPILOGUE),
+                     knob(RARN_TUNE_GEMM_TAIL_SPLIT), splitk);
 }
 
 int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H) {
@@ -826,9 +843,13 @@ int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H) {
     return gemm_workspace_bytes(T, H);
 }
 
-rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_rows residual,
-                                   const void *gamma, int64_t T, int64_t H, int64_t K, float eps,
-                                   void *workspace, size_t workspace_bytes, void *stream) {
+// Every check of the GEMM form that does not involve the workspace, over all
+// T rows: types, sizes, alignment, and overlaps between the outputs (y, the
+// residual) and every other matrix.  RARN_OK with T == 0 means "nothing to
+// do"; the workspace form adds its own workspace checks.
+static rarn_status gemm_check(const rarn_rows &y, const rarn_rows &a, const rarn_rows &w,
+                              const rarn_rows &residual, const void *gamma, int64_t T, int64_t H,
+                              int64_t K, float eps) {
     const rarn_dtype dt = a.dtype;
     if (!dtype_ok(dt) || !dtype_ok(w.dtype) || !dtype_ok(y.dtype) || !dtype_ok(residual.dtype))
         return RARN_ERR_INVALID_ARG;
@@ -837,19 +858,10 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     if (a.row_stride < K || w.row_stride < K || residual.row_stride < H || y.row_stride < H)
         return RARN_ERR_INVALID_ARG;
     if (T == 0) return RARN_OK;
-    if (!y.data || !a.data || !w.data || !residual.data || !gamma || !workspace)
-        return RARN_ERR_INVALID_ARG;
+    if (!y.data || !a.data || !w.data || !residual.data || !gamma) return RARN_ERR_INVALID_ARG;
     if (dt == RARN_F32) return RARN_ERR_UNSUPPORTED;  // the tensor path takes 16-bit operands
     if (T > (int64_t(1) << 31) - 128 || K > (int64_t(1) << 31) - 64) return RARN_ERR_UNSUPPORTED;
-    GemmPlan gp = gemm_plan_env(T, H, K);
-    if (gp.ns == 0) return RARN_ERR_UNSUPPORTED;
-    // split K only where the workspace holds its partial products
-    if (gp.splitk && ((int64_t)workspace_bytes < gemm_splitk_bytes(T, H, gp.splitk) ||
-                      (reinterpret_cast<uintptr_t>(workspace) & 31u)))
-        gp = gemm_plan_env(T, H, K, 152, /*no_splitk=*/true);
-    const int64_t ws = gp.splitk ? gemm_splitk_bytes(T, H, gp.splitk) : gemm_workspace_bytes_for(T, H);
-    if ((int64_t)workspace_bytes < ws || (reinterpret_cast<uintptr_t>(workspace) & 15u))
-        return RARN_ERR_INVALID_ARG;
+    if (plan_gemm(T, H, K).ns == 0) return RARN_ERR_UNSUPPORTED;
     auto al16 = [](const void *ptr, int64_t ld) { return aligned16(ptr) && (ld * 2) % 16 == 0; };
     if (!al16(a.data, a.row_stride) || !al16(w.data, w.row_stride) ||
         !al16(residual.data, residual.row_stride) || !al16(y.data, y.row_stride) ||
@@ -857,21 +869,26 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
         return RARN_ERR_UNSUPPORTED;
     const int64_t yb = span_bytes(T, H, y.row_stride, 2), rb = span_bytes(T, H, residual.row_stride, 2);
     const int64_t ab = span_bytes(T, K, a.row_stride, 2), wb = span_bytes(H, K, w.row_stride, 2);
-    const void *outs[3] = {y.data, residual.data, workspace};
-    const int64_t outb[3] = {yb, rb, ws};
     const void *ins[3] = {a.data, w.data, gamma};
     const int64_t inb[3] = {ab, wb, H * 2};
-    for (int i = 0; i < 3; ++i) {
-        for (int j = 0; j < 3; ++j)
-            if (overlaps(outs[i], outb[i], ins[j], inb[j])) return RARN_ERR_ALIAS;
-        for (int j = i + 1; j < 3; ++j)
-            if (overlaps(outs[i], outb[i], outs[j], outb[j])) return RARN_ERR_ALIAS;
-    }
+    for (int j = 0; j < 3; ++j)
+        if (overlaps(y.data, yb, ins[j], inb[j]) || overlaps(residual.data, rb, ins[j], inb[j]))
+            return RARN_ERR_ALIAS;
+    if (overlaps(y.data, yb, residual.data, rb)) return RARN_ERR_ALIAS;
+    return RARN_OK;
+}
 
-    DeviceInfo *d = nullptr;
-    rarn_status st = device_info(&d);
-    if (st != RARN_OK) return st;
-
+// One validated GEMM-form call over T rows with a workspace of ws_bytes.
+static rarn_status gemm_launch(const rarn_rows &y, const rarn_rows &a, const rarn_rows &w,
+                               const rarn_rows &residual, const void *gamma, int64_t T, int64_t H,
+                               int64_t K, float eps, void *workspace, size_t workspace_bytes,
+                               const DeviceInfo *d, void *stream) {
+    GemmPlan gp = gemm_plan_tuned(T, H, K, d->num_sms);
+    if (gp.ns == 0) return RARN_ERR_UNSUPPORTED;
+    // split K only where the workspace holds its partial products
+    if (gp.splitk && ((int64_t)workspace_bytes < gemm_splitk_bytes(T, H, gp.splitk) ||
+                      (reinterpret_cast<uintptr_t>(workspace) & 31u)))
+        gp = gemm_plan_tuned(T, H, K, d->num_sms, /*no_splitk=*/true);
     GemmCall c{};
     c.a = a.data;
     c.lda = a.row_stride;
@@ -895,14 +912,10 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     c.pair = gp.pair;
     c.splitk = gp.splitk;
     c.part = gp.splitk ? static_cast<float *>(workspace) + gemm_splitk_offset(T, H) : nullptr;
-    // allowed unless switched off for measurements; the launcher decides both
+    // allowed unless switched off by a tuning knob; the launcher decides both
     // against the clusters that fit on this GPU
-    auto env_off = [](const char *name) {
-        const char *v = getenv(name);
-        return v && atoi(v) == 0;
-    };
-    c.fuse_norm = !env_off("RARN_GEMM_FUSE");
-    c.tail_split = !env_off("RARN_GEMM_SPLIT");
+    c.fuse_norm = g_tune[RARN_TUNE_GEMM_NORM_IN_EPILOGUE] != 0;
+    c.tail_split = g_tune[RARN_TUNE_GEMM_TAIL_SPLIT] != 0;
     c.wait_limit_ns = 2000000000ull;
     c.stall_fill = -1;
     {
@@ -915,35 +928,72 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     c.pdl = g_pdl.load() != 0;
     c.watchdog = d->watchdog;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    const cudaError_t e = dt == RARN_BF16 ? launch_gemm_norm<__nv_bfloat16>(c, cs)
-                                          : launch_gemm_norm<__half>(c, cs);
+    const cudaError_t e = a.dtype == RARN_BF16 ? launch_gemm_norm<__nv_bfloat16>(c, cs)
+                                               : launch_gemm_norm<__half>(c, cs);
     if (e != cudaSuccess) return cuda_fail(e);
     return RARN_OK;
 }
 
+rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_rows residual,
+                                   const void *gamma, int64_t T, int64_t H, int64_t K, float eps,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    rarn_status st = gemm_check(y, a, w, residual, gamma, T, H, K, eps);
+    if (st != RARN_OK || T == 0) return st;
+    if (!workspace) return RARN_ERR_INVALID_ARG;
+    // at least the non-split kernels' workspace (split K runs only where the
+    // workspace also holds its partial products); the span checked for
+    // overlaps is what any plan could use of the workspace given
+    const int64_t base = gemm_workspace_bytes_for(T, H);
+    if ((int64_t)workspace_bytes < base || (reinterpret_cast<uintptr_t>(workspace) & 15u))
+        return RARN_ERR_INVALID_ARG;
+    const int64_t most = T <= 128 ? gemm_splitk_bytes(T, H, kGemmMaxSplitK) : base;
+    const int64_t ws = std::min<int64_t>((int64_t)workspace_bytes, most);
+    const void *others[5] = {y.data, residual.data, a.data, w.data, gamma};
+    const int64_t ob[5] = {span_bytes(T, H, y.row_stride, 2),
+                           span_bytes(T, H, residual.row_stride, 2),
+                           span_bytes(T, K, a.row_stride, 2), span_bytes(H, K, w.row_stride, 2),
+                           H * 2};
+    for (int j = 0; j < 5; ++j)
+        if (overlaps(workspace, ws, others[j], ob[j])) return RARN_ERR_ALIAS;
+    DeviceInfo *d = nullptr;
+    if ((st = device_info(&d)) != RARN_OK) return st;
+    return gemm_launch(y, a, w, residual, gamma, T, H, K, eps, workspace, workspace_bytes, d,
+                       stream);
+}
+
+// Rows one launch sequence of the allocation-free GEMM entry point covers:
+// its scratch holds one partial sum per row and 128 columns plus a counter per
+// 128-row block; -1 for an unsupported H.
+static int64_t noalloc_rows(int64_t H) {
+    if (H <= 0 || plan_gemm(1, H, 64).ns == 0) return -1;
+    return (kGemmScratchFloats - 16) / (H / 128 + 1) / 128 * 128;
+}
+
+int64_t rarn_gemm_noalloc_rows(int64_t H) { return noalloc_rows(H); }
+
 rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w,
                                            rarn_rows residual, const void *gamma, int64_t T,
                                            int64_t H, int64_t K, float eps, void *stream) {
-    if (T <= 0 || H <= 0) {  // argument errors and the empty call, as the workspace form
-        return rarn_gemm_add_rms_norm(y, a, w, residual, gamma, T, H, K, eps, nullptr, 0,
-                                      stream);
-    }
-    const GemmPlan gp = gemm_plan_env(T, H, K);
-    if (gp.ns == 0) return RARN_ERR_UNSUPPORTED;
+    // the whole call is checked once, over all T rows, before anything runs:
+    // an overlap between different chunks' rows is refused like any other,
+    // and no chunk is launched unless every chunk would be
+    rarn_status st = gemm_check(y, a, w, residual, gamma, T, H, K, eps);
+    if (st != RARN_OK || T == 0) return st;
+    DeviceInfo *d = nullptr;
+    if ((st = device_info(&d)) != RARN_OK) return st;
     float *scratch = nullptr;
-    rarn_status st = gemm_scratch(&scratch);
-    if (st != RARN_OK) return st;
+    if ((st = gemm_scratch(&scratch)) != RARN_OK) return st;
     // rows per launch sequence that the scratch holds (partial sums and
     // row-block counters); later chunks reuse it in stream order
-    const int64_t chunk = (kGemmScratchFloats - 16) / (H / 128 + 1) / 128 * 128;
+    const int64_t chunk = noalloc_rows(H);
     for (int64_t t0 = 0; t0 < T; t0 += chunk) {
         const int64_t rows = std::min(chunk, T - t0);
         auto shift = [t0](rarn_rows m) {
-            if (m.data) m.data = static_cast<char *>(m.data) + t0 * m.row_stride * 2;
+            m.data = static_cast<char *>(m.data) + t0 * m.row_stride * 2;
             return m;
         };
-        st = rarn_gemm_add_rms_norm(shift(y), shift(a), w, shift(residual), gamma, rows, H, K,
-                                    eps, scratch, kGemmScratchFloats * 4, stream);
+        st = gemm_launch(shift(y), shift(a), w, shift(residual), gamma, rows, H, K, eps, scratch,
+                         kGemmScratchFloats * 4, d, stream);
         if (st != RARN_OK) return st;
     }
     return RARN_OK;
@@ -988,7 +1038,10 @@ rarn_status rarn_reduce_add_rms_norm_fp8in(void *y, const void *partials, int32_
     p.wait_limit_ns = stream::kWaitLimitNs;
     p.stall_fill = -1;
     p.max_smem = d->max_smem_optin;
-    if (q8in::choose_kernel(p, s, d->num_sms).ring) {
+    const q8in::KernelChoice kc =
+        q8in::choose_kernel(p, s, d->num_sms, (int)g_tune[RARN_TUNE_FP8IN_RING],
+                            g_tune[RARN_TUNE_FP8IN_PACK16] != 0);
+    if (kc.ring) {
         const long long f = g_stall_fill.exchange(-1);
         if (f >= 0) {
             p.stall_fill = f;
@@ -999,9 +1052,9 @@ rarn_status rarn_reduce_add_rms_norm_fp8in(void *y, const void *partials, int32_
     const bool pdl = g_pdl.load() != 0;
     cudaError_t e;
     switch (dt) {
-    case RARN_BF16: e = launch_q8in<__nv_bfloat16>(p, d->num_sms, pdl, cs); break;
-    case RARN_F16: e = launch_q8in<__half>(p, d->num_sms, pdl, cs); break;
-    default: e = launch_q8in<float>(p, d->num_sms, pdl, cs); break;
+    case RARN_BF16: e = launch_q8in<__nv_bfloat16>(p, kc, d->num_sms, pdl, cs); break;
+    case RARN_F16: e = launch_q8in<__half>(p, kc, d->num_sms, pdl, cs); break;
+    default: e = launch_q8in<float>(p, kc, d->num_sms, pdl, cs); break;
     }
     if (e != cudaSuccess) return cuda_fail(e);
     return RARN_OK;
@@ -1018,7 +1071,8 @@ rarn_status rarn_plan_fp8in(int64_t T, int64_t H, int32_t R, rarn_dtype dt, int 
     }
     const int s = elem_size(dt);
     const q8in::KernelChoice k =
-        q8in::choose_kernel(T, H, R, s, codes_aligned16 != 0, num_sms, max_smem);
+        q8in::choose_kernel(T, H, R, s, codes_aligned16 != 0, num_sms, max_smem,
+                            (int)g_tune[RARN_TUNE_FP8IN_RING], g_tune[RARN_TUNE_FP8IN_PACK16] != 0);
     if (k.ring) {
         const q8in::SLayout L =
             q8in::slayout(k.sp.stages, R, k.sp.ppt, s, H, q8in::kStreamWarps);
@@ -1035,10 +1089,17 @@ rarn_status rarn_plan_fp8in(int64_t T, int64_t H, int32_t R, rarn_dtype dt, int 
     return RARN_OK;
 }
 
-rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, char *out, size_t cap) {
+rarn_status rarn_plan_gemm(int64_t T, int64_t H, int64_t K, rarn_dtype dt, int32_t num_sms,
+                           char *out, size_t cap) {
     if (!out || cap == 0) return RARN_ERR_INVALID_ARG;
     if (!dtype_ok(dt) || T < 0 || H <= 0 || K <= 0) return RARN_ERR_INVALID_ARG;
-    const GemmPlan gp = dt == RARN_F32 ? GemmPlan{} : gemm_plan_env(T, H, K);
+    if (num_sms <= 0) {
+        DeviceInfo *d = nullptr;
+        const rarn_status st = device_info(&d);
+        if (st != RARN_OK) return st;
+        num_sms = d->num_sms;
+    }
+    const GemmPlan gp = dt == RARN_F32 ? GemmPlan{} : gemm_plan_tuned(T, H, K, num_sms);
     if (gp.ns == 0) {
         snprintf(out, cap, "none: unsupported shape or type");
         return RARN_ERR_UNSUPPORTED;
@@ -1087,6 +1148,24 @@ rarn_status rarn_set_pdl(int enable) {
 }
 
 int rarn_get_pdl(void) { return g_pdl.load(); }
+
+rarn_status rarn_set_tuning(rarn_tuning knob, int64_t value) {
+    if ((int)knob < 0 || (int)knob >= RARN_TUNE_COUNT) return RARN_ERR_INVALID_ARG;
+    if (value != -1 && !tuning_value_ok(knob, value)) return RARN_ERR_INVALID_ARG;
+    g_tune.v[knob].store(value);
+    return RARN_OK;
+}
+
+rarn_status rarn_get_tuning(rarn_tuning knob, int64_t *value) {
+    if (!value || (int)knob < 0 || (int)knob >= RARN_TUNE_COUNT) return RARN_ERR_INVALID_ARG;
+    *value = g_tune[knob];
+    return RARN_OK;
+}
+
+rarn_status rarn_reset_tuning(void) {
+    g_tune.reset();
+    return RARN_OK;
+}
 
 rarn_status rarn_test_stall(long long fill, unsigned long long wait_limit_ns) {
     if (fill < 0 || wait_limit_ns == 0 || wait_limit_ns > stream::kWaitLimitNs)
@@ -1170,6 +1249,6 @@ int rarn_host_access(void) {
     return pageable ? 2 : (mapped ? 1 : 0);
 }
 
-int rarn_version(void) { return (1 << 16) | 1; }
+int rarn_version(void) { return (1 << 16) | 2; }
 
 }  // extern "C"

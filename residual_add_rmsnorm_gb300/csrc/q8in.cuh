@@ -617,9 +617,9 @@ inline StreamPlan plan_stream(int64_t H, int R, int s, int max_smem) {
 // 7.3 / 8.0.  Otherwise a register kernel: 16-element packs where H is a
 // multiple of 16, else 8-element packs, `vpt` packs per thread so that a row
 // takes at most 256 threads (vpt = 0: H too long for the type).
-// RARN_Q8IN_STREAM = 0 / 1 switches the TMA-fed kernel off / forces it (any
-// shape it can take); RARN_Q8IN_16 = 0 switches the 16-element packs off; both
-// for measurements and tests.
+// ring_override = 0 / 1 switches the TMA-fed kernel off / takes it for any
+// shape it can run; pack16 = false switches the 16-element packs off (the
+// RARN_TUNE_FP8IN_RING / RARN_TUNE_FP8IN_PACK16 knobs).
 struct KernelChoice {
     bool ring = false;
     StreamPlan sp;       // ring
@@ -629,10 +629,10 @@ struct KernelChoice {
 };
 
 inline KernelChoice choose_kernel(int64_t T, int64_t H, int R, int s, bool codes_aligned16,
-                                  int num_sms, int max_smem) {
+                                  int num_sms, int max_smem, int ring_override = -1,
+                                  bool pack16 = true) {
     KernelChoice k;
-    const char *sv = getenv("RARN_Q8IN_STREAM");
-    const int force = sv && *sv ? atoi(sv) : -1;
+    const int force = ring_override;
     if (force != 0 && H % 16 == 0 && codes_aligned16 &&
         (force == 1 || (R > 4 && T >= 8 * (int64_t)num_sms))) {
         k.sp = plan_stream(H, R, s, max_smem);
@@ -641,8 +641,7 @@ inline KernelChoice choose_kernel(int64_t T, int64_t H, int R, int s, bool codes
             return k;
         }
     }
-    const char *v16 = getenv("RARN_Q8IN_16");
-    k.pack = H % 16 == 0 && !(v16 && atoi(v16) == 0) ? 16 : 8;
+    k.pack = H % 16 == 0 && pack16 ? 16 : 8;
     const int64_t nv = H / k.pack;
     k.vpt = nv <= 256 ? 1 : nv <= 512 ? 2 : nv <= 1024 ? 4 : 8;
     if ((k.pack == 16 && k.vpt == 8) || (k.vpt == 8 && s == 4)) k.vpt = 0;
@@ -650,9 +649,10 @@ inline KernelChoice choose_kernel(int64_t T, int64_t H, int R, int s, bool codes
     return k;
 }
 
-inline KernelChoice choose_kernel(const Params &p, int s, int num_sms) {
+inline KernelChoice choose_kernel(const Params &p, int s, int num_sms, int ring_override = -1,
+                                  bool pack16 = true) {
     return choose_kernel(p.T, p.H, p.R, s, (reinterpret_cast<uintptr_t>(p.codes) & 15u) == 0,
-                         num_sms, p.max_smem);
+                         num_sms, p.max_smem, ring_override, pack16);
 }
 
 template <typename T, int PPT, int RMAX>
@@ -675,13 +675,13 @@ static cudaError_t launch_stream_r(const Params &p, const StreamPlan &sp, int gr
 
 }  // namespace q8in
 
-// Launch the kernel choose_kernel picks (H <= 16384; binary32 storage
+// Launch the kernel choose_kernel picked for p (H <= 16384; binary32 storage
 // H <= 8192); the register kernels grid-stride over rows with every CTA
 // resident, the TMA-fed kernel has one CTA per SM.
 template <typename T>
-cudaError_t launch_q8in(const q8in::Params &p, int num_sms, bool pdl, cudaStream_t st) {
+cudaError_t launch_q8in(const q8in::Params &p, const q8in::KernelChoice &k, int num_sms, bool pdl,
+                        cudaStream_t st) {
     using namespace q8in;
-    const KernelChoice k = choose_kernel(p, (int)sizeof(T), num_sms);
     cudaError_t e = cudaErrorInvalidValue;
     if (k.ring) {
         const int grid = (int)std::min<int64_t>(p.T, num_sms);

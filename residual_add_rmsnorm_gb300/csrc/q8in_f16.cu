@@ -2,5 +2,7 @@
 #include "q8in.cuh"
 
 namespace rarn {
-template cudaError_t launch_q8in<__half>(const q8in::Params &, int, bool, cudaStream_t);
+template cudaError_t launch_q8in<__half>(const q8in::Params &,
+                                                const q8in::KernelChoice &, int, bool,
+                                                cudaStream_t);
 }  // namespace rarn

@@ -13,6 +13,22 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "slow: long-running CPU test")
 
 
+@pytest.fixture
+def tune():
+    """Planner overrides for one test: ``tune(gemm_pair=0)`` sets knobs
+    through rarn_set_tuning; every knob is reset when the test ends."""
+    import residual_add_rmsnorm_gb300 as rarn
+
+    def set_knobs(**knobs):
+        for k, v in knobs.items():
+            rarn.set_tuning(k, v)
+
+    try:
+        yield set_knobs
+    finally:
+        rarn.reset_tuning()
+
+
 def pytest_collection_modifyitems(config, items):
     try:
         import torch

@@ -387,11 +387,9 @@ def test_gemm_form_argument_errors(lib):
                 _rows(None, H, BF16), None, 0, H, K, 1e-6, wsp=None) == OK  # T = 0
 
 
-def test_plan_fp8in(monkeypatch):
+def test_plan_fp8in(tune):
     """Which kernel the reduce over 8-bit partials takes (pure host logic; a
     GB300's 152 SMs and 232448 bytes of opt-in shared memory per CTA)."""
-    monkeypatch.delenv("RARN_Q8IN_STREAM", raising=False)
-    monkeypatch.delenv("RARN_Q8IN_16", raising=False)
     p = rarn.plan_fp8in(8192, 8192, 8)
     # the bench shape: 5 stages of 8 code chunks + a residual chunk of 4096
     # elements; the ncu capture of it reports 221.84 KB dynamic shared memory
@@ -405,22 +403,22 @@ def test_plan_fp8in(monkeypatch):
     assert rarn.plan_fp8in(4096, 16384, 16).startswith("q8in.ring")
     assert rarn.plan_fp8in(8, 1020, 2).startswith("none")
     assert rarn.plan_fp8in(8, 16384, 2, "f32").startswith("none")
-    monkeypatch.setenv("RARN_Q8IN_16", "0")
+    tune(fp8in_pack16=0)
     assert rarn.plan_fp8in(64, 4096, 2) == "q8in.rows pack=8 vpt=2 block=256 grid=occupancy"
-    monkeypatch.setenv("RARN_Q8IN_STREAM", "1")
+    tune(fp8in_ring=1)
     assert rarn.plan_fp8in(5, 512, 1).startswith("q8in.ring")
     assert rarn.plan_fp8in(5, 520, 1).startswith("q8in.rows")  # H not a multiple of 16
-    monkeypatch.setenv("RARN_Q8IN_STREAM", "0")
+    tune(fp8in_ring=0)
     assert rarn.plan_fp8in(8192, 8192, 8).startswith("q8in.rows")
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
-def test_plan_fp8in_ring_fits(dt, monkeypatch):
+def test_plan_fp8in_ring_fits(dt, tune):
     """The TMA-fed kernel forced on every partial count and a spread of row
     lengths: the ring always fits the opt-in shared memory with the row copy
     and control words, keeps at least 2 stages (4 with two units per
     thread), and every bulk copy is a whole number of 16-byte blocks."""
-    monkeypatch.setenv("RARN_Q8IN_STREAM", "1")
+    tune(fp8in_ring=1)
     s = 4 if dt == "f32" else 2
     for R in range(1, 17):
         for H in (16, 1040, 4096, 8192, 8192 if dt == "f32" else 16384):
@@ -437,7 +435,7 @@ def test_plan_fp8in_ring_fits(dt, monkeypatch):
             assert (last * 1) % 16 == 0 and (last * s) % 16 == 0
 
 
-def test_plan_gemm(monkeypatch):
+def test_plan_gemm(tune):
     """Columns per CTA from H; the K slab and ring depth fill one SM's shared
     memory; the workspace holds one float per row and column tile."""
     # persistent on SM pairs: 76 two-CTA clusters walk 256 tiles of 256 x 256,
@@ -449,11 +447,11 @@ def test_plan_gemm(monkeypatch):
     assert "grid=36 " in p and "pair=1" in p, p
     p = rarn.plan_gemm(1024, 4096, 4096)   # below 2048 rows: one SM per tile
     assert "persistent=1 pair=0" in p, p
-    monkeypatch.setenv("RARN_GEMM_PAIR", "0")  # one CTA per SM walks 512 tiles of 128 x 256
+    tune(gemm_pair=0)  # one CTA per SM walks 512 tiles of 128 x 256
     p = rarn.plan_gemm(4096, 4096, 4096)
     assert "cols_per_cta=256 col_tiles=16 bk=64 stages=4" in p and "grid=152" in p, p
     assert "kblocks=64 persistent=1 pair=0" in p, p
-    monkeypatch.delenv("RARN_GEMM_PAIR")
+    tune(gemm_pair=-1)
     p = rarn.plan_gemm(200, 768, 1000)     # two 128-row blocks: one SM per tile
     assert "cols_per_cta=256 col_tiles=3" in p and "persistent=1" in p and "grid=6" in p, p
     assert "pair=0" in p, p
@@ -465,9 +463,9 @@ def test_plan_gemm(monkeypatch):
     assert "col_tiles=16" in p and "splitk=8" in p and "grid=128" in p, p
     p = rarn.plan_gemm(16, 2048, 8192)
     assert "splitk=9" in p and "grid=72" in p, p
-    monkeypatch.setenv("RARN_GEMM_SPLITK", "0")
+    tune(gemm_split_k=0)
     assert "persistent=1" in rarn.plan_gemm(1, 4096, 4096)
-    monkeypatch.delenv("RARN_GEMM_SPLITK")
+    tune(gemm_split_k=-1)
     p = rarn.plan_gemm(8, 16384, 64)   # beyond 32 tiles of 256: 512-column tiles
     assert "cols_per_cta=512 col_tiles=32 bk=32 stages=5" in p and "persistent=0" in p, p
     assert rarn.plan_gemm(8, 300, 64).startswith("none")
@@ -479,3 +477,134 @@ def test_plan_gemm(monkeypatch):
     assert rarn.gemm_workspace_bytes(1, 768) == (64 + 9 * 768) * 4
     assert rarn.gemm_workspace_bytes(129, 768) == ((129 * 6 + 3) // 4 * 4 + 2) * 4
     assert rarn.gemm_workspace_bytes(7, 300) == -1
+
+
+# values each knob accepts besides -1 (include/rarn.h, rarn_tuning)
+TUNING_OK = {
+    "rows_per_thread": [1, 2, 4, 8, 16], "rows_grid": [1, 4096, 2 ** 31 - 1],
+    "rows_pipeline": [0], "l2_rows": list(range(9)), "stream_packs": [1, 2, 4],
+    "stream_groups": [1, 2], "gemm_cols": [256, 512], "gemm_slab": [32, 64],
+    "gemm_ctas_per_sm": [1, 2], "gemm_persistent": [0, 1], "gemm_pair": [0, 1],
+    "gemm_norm_in_epilogue": [0], "gemm_tail_split": [0], "gemm_split_k": [0],
+    "fp8in_ring": [0, 1], "fp8in_pack16": [0],
+}
+TUNING_BAD = {
+    "rows_per_thread": [0, 3, 32], "rows_grid": [0, 2 ** 31], "rows_pipeline": [1, -2],
+    "l2_rows": [9, -2], "stream_packs": [0, 3, 8], "stream_groups": [0, 3],
+    "gemm_cols": [128, 384], "gemm_slab": [16, 128], "gemm_ctas_per_sm": [0, 3],
+    "gemm_persistent": [2], "gemm_pair": [2], "gemm_norm_in_epilogue": [1],
+    "gemm_tail_split": [1], "gemm_split_k": [1, 9], "fp8in_ring": [2], "fp8in_pack16": [1],
+}
+
+
+def test_tuning_knobs_validated(lib):
+    """rarn_set_tuning accepts -1 and each knob's listed values, refuses
+    everything else (status INVALID, the knob unchanged), and
+    rarn_reset_tuning puts every knob back to -1."""
+    assert set(TUNING_OK) == set(rarn.TUNING) == set(TUNING_BAD)
+    assert sorted(rarn.TUNING.values()) == list(range(16))
+    rarn.reset_tuning()
+    try:
+        for name, good in TUNING_OK.items():
+            assert rarn.get_tuning(name) == -1
+            for v in good:
+                rarn.set_tuning(name, v)
+                assert rarn.get_tuning(name) == v
+            keep = good[0]
+            rarn.set_tuning(name, keep)
+            for v in TUNING_BAD[name]:
+                with pytest.raises(rarn.RarnError) as e:
+                    rarn.set_tuning(name, v)
+                assert e.value.status == INVALID
+                assert rarn.get_tuning(name) == keep, name
+            rarn.set_tuning(name, -1)
+        v = ctypes.c_int64(0)
+        assert lib.rarn_set_tuning(16, 0) == INVALID   # no such knob
+        assert lib.rarn_set_tuning(-1, 0) == INVALID
+        assert lib.rarn_get_tuning(16, ctypes.byref(v)) == INVALID
+        assert lib.rarn_get_tuning(0, None) == INVALID
+        rarn.set_tuning("gemm_pair", 0)
+        rarn.set_tuning("rows_grid", 7)
+        rarn.reset_tuning()
+        assert all(rarn.get_tuning(n) == -1 for n in rarn.TUNING)
+    finally:
+        rarn.reset_tuning()
+
+
+def test_tuning_steers_the_planners(tune):
+    """Knobs reach the row, stream, GEMM and 8-bit-partials planners (pure
+    host logic: the plan queries with a GB300's SM count)."""
+    base = rarn.plan("fused_add_rms_norm", 4096, 4096, 1, "bf16", num_sms=152)
+    assert "pipe=1" in base and "per_thread=2" in base, base
+    tune(rows_pipeline=0, rows_per_thread=4, rows_grid=300)
+    p = rarn.plan("fused_add_rms_norm", 4096, 4096, 1, "bf16", num_sms=152)
+    assert "pipe=0" in p and "per_thread=4" in p and "grid=300" in p, p
+    tune(stream_packs=1)
+    p = rarn.plan("reduce_add_rms_norm", 8192, 8192, 8, "bf16", num_sms=152)
+    assert p.startswith("stream") and "chunk=4096" in p, p
+    tune(gemm_cols=512, gemm_slab=64, gemm_ctas_per_sm=1)
+    p = rarn.plan_gemm(4096, 4096, 4096)
+    assert "cols_per_cta=512" in p and "bk=64" in p and "persistent=0" in p, p
+    tune(fp8in_ring=0)
+    assert rarn.plan_fp8in(8192, 8192, 8).startswith("q8in.rows")
+    rarn.reset_tuning()
+    assert rarn.plan("fused_add_rms_norm", 4096, 4096, 1, "bf16", num_sms=152) == base
+
+
+def test_plan_gemm_takes_the_sm_count():
+    """The GEMM planner sizes its persistent grid and split K from the SM
+    count it is given (the compute call passes the device's)."""
+    p = rarn.plan_gemm(4096, 4096, 4096, num_sms=132)
+    assert "grid=132" in p and "pair=1" in p, p
+    p = rarn.plan_gemm(1, 4096, 4096, num_sms=64)   # 64 SMs / 16 column tiles: 4 splits
+    assert "splitk=4" in p and "grid=64" in p, p
+    assert "splitk=8" in rarn.plan_gemm(1, 4096, 4096, num_sms=152)
+
+
+def test_noalloc_rows_match_the_header(lib):
+    """The rows one launch sequence of the allocation-free GEMM entry point
+    covers: floor(floor((2^20 - 16) / (H / 128 + 1)) / 128) * 128, and the
+    figures the header quotes for H = 8192 and 16384."""
+    with open(HEADER) as f:
+        text = f.read()
+    assert "16128 rows at H = 8192, 8064 at H = 16384" in text
+    assert rarn.gemm_noalloc_rows(8192) == 16128
+    assert rarn.gemm_noalloc_rows(16384) == 8064
+    for H in (256, 512, 768, 1024, 4096, 5120, 8192, 12288, 16384):
+        assert rarn.gemm_noalloc_rows(H) == (2 ** 20 - 16) // (H // 128 + 1) // 128 * 128, H
+        rows = rarn.gemm_noalloc_rows(H)
+        # partial sums [rows][H / 128], then one counter per 128-row block
+        assert (rows * (H // 128) + 3) // 4 * 4 + rows // 128 <= 2 ** 20
+    assert rarn.gemm_noalloc_rows(300) == -1
+    assert rarn.gemm_noalloc_rows(16896) == -1
+
+
+def test_noalloc_checks_the_whole_call_first(lib):
+    """The allocation-free GEMM entry point validates all T rows before it
+    launches any chunk: outputs of one chunk overlapping another chunk's
+    inputs are refused (RARN_ERR_ALIAS), as the workspace form refuses them,
+    and so are argument errors that only a later chunk would meet.  No call
+    here reaches the GPU."""
+    H, K = 8192, 64
+    chunk = rarn.gemm_noalloc_rows(H)
+    T = 2 * chunk
+    f = lib.rarn_gemm_add_rms_norm_noalloc
+    g = D + (1 << 36)
+    a, w = _rows(B, K, BF16), _rows(C, K, BF16)
+    r = _rows(A, H, BF16)
+    # y starts where the second chunk's residual rows start: chunk 0 would
+    # overwrite rows that chunk 1 then reads
+    y = _rows(A + chunk * H * 2, H, BF16)
+    assert f(y, a, w, r, g, T, H, K, 1e-6, None) == ALIAS
+    ws = D + (1 << 38)
+    assert lib.rarn_gemm_add_rms_norm(y, a, w, r, g, T, H, K, 1e-6, ws, 1 << 30, None) == ALIAS
+    # A's last chunk over y's first rows
+    y2 = _rows(D, H, BF16)
+    a2 = _rows(D - (T - 1) * K * 2, K, BF16)
+    assert f(y2, a2, w, r, g, T, H, K, 1e-6, None) == ALIAS
+    # the other argument errors of the workspace form, before any CUDA call
+    assert f(y2, a, w, r, g, T, H, K, -1.0, None) == INVALID
+    assert f(y2, a, _rows(C, K, F16), r, g, T, H, K, 1e-6, None) == UNSUPPORTED
+    assert f(y2, a, w, r, g, T, 300, K, 1e-6, None) == UNSUPPORTED
+    assert f(y2, _rows(B + 2, K, BF16), w, r, g, T, H, K, 1e-6, None) == UNSUPPORTED
+    assert f(_rows(None, H, BF16), a, w, r, g, 0, H, K, 1e-6, None) == OK  # T = 0

@@ -71,10 +71,10 @@ def test_fp8in_parity(dt, fmt, R, T, H):
 
 
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
-def test_fp8in_eight_element_packs(dt, monkeypatch):
+def test_fp8in_eight_element_packs(dt, tune):
     """The 8-element-pack kernel (the one H not a multiple of 16 takes)
     forced on shapes the 16-element kernel would take: same results."""
-    monkeypatch.setenv("RARN_Q8IN_16", "0")
+    tune(fp8in_pack16=0)
     for R, T, H, fmt in ((8, 40, 4096, "e4m3"), (3, 7, 8192, "e5m2")):
         codes, scales, r, g = fp8in_inputs(R, T, H, dt, fmt, seed=R + T + H)
         check(codes, scales, r, g, dt, fmt, f"8-element packs {dt} {fmt} R{R} H{H}")
@@ -112,14 +112,14 @@ def test_fp8in_full_size_sampled():
     check(codes, scales, r, g, "bf16", "e4m3", "full size", rows=rows)
 
 
-@pytest.mark.parametrize("ring", ["0", "1"])
+@pytest.mark.parametrize("ring", [0, 1])
 @pytest.mark.parametrize("pdl", [True, False])
-def test_fp8in_chained(pdl, ring, monkeypatch):
+def test_fp8in_chained(pdl, ring, tune):
     """Two dependent launches: the second reduces on the residual the first
     wrote (for the TMA-fed kernel, bulk copies of what the previous launch
     stored); replayed on the CPU with the oracle."""
     import torch
-    monkeypatch.setenv("RARN_Q8IN_STREAM", ring)
+    tune(fp8in_ring=ring)
     rarn.set_pdl(pdl)
     try:
         R, T, H = 3, 40, 2048
@@ -146,11 +146,11 @@ def all_finite_codes(fmt):
     return c[~special]
 
 
-def test_fp8in_tma_fed_kernel(monkeypatch):
+def test_fp8in_tma_fed_kernel(tune):
     """The TMA-fed kernel forced on shapes the register kernels would take:
     ragged last chunks, 1 to 16 partials, all three storage types, every
     finite code, NaN and Inf codes, and overflow of the sum."""
-    monkeypatch.setenv("RARN_Q8IN_STREAM", "1")
+    tune(fp8in_ring=1)
     for dt, fmt, R, T, H in (("bf16", "e4m3", 8, 40, 4096), ("f16", "e5m2", 3, 37, 1040),
                              ("f32", "e4m3", 5, 9, 8192), ("bf16", "e5m2", 16, 5, 16384),
                              ("bf16", "e4m3", 2, 300, 16), ("f16", "e4m3", 1, 11, 6144),
@@ -176,13 +176,13 @@ def test_fp8in_tma_fed_kernel(monkeypatch):
 
 
 @pytest.mark.parametrize("fill", [0, 3])
-def test_fp8in_wait_runs_out_and_is_reported(fill, monkeypatch):
+def test_fp8in_wait_runs_out_and_is_reported(fill, tune):
     """Failure detection without a GPU fault: the TMA-fed kernel's test hook
     leaves one ring fill of CTA 0 without its last 16 bytes; the consumers'
     wait gives up after 20 ms, the CTA drains its copies and returns, the
     watchdog bit is set, and the next call is correct."""
     import torch
-    monkeypatch.setenv("RARN_Q8IN_STREAM", "1")
+    tune(fp8in_ring=1)
     rarn.watchdog(clear=True)
     R, T, H = 4, 1000, 4096  # CTA 0 takes 7 rows, one fill each
     codes, scales, r, g = fp8in_inputs(R, T, H, "bf16", "e4m3", seed=30 + fill)

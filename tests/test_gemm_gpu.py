@@ -138,32 +138,28 @@ def test_gemm_parity(T, H, K, dt):
     assert ("pair=1" in plan) == (H <= 8192 and K >= 512 and T >= 2048), plan
 
 
-@pytest.mark.parametrize("ns,bk,ctas", [("256", "32", "2"), ("256", "64", "2"),
-                                        ("256", "64", "1"), ("512", "32", "1"),
-                                        ("512", "64", "1")])
-def test_gemm_tilings(ns, bk, ctas, monkeypatch):
+@pytest.mark.parametrize("ns,bk,ctas", [(256, 32, 2), (256, 64, 2), (256, 64, 1), (512, 32, 1),
+                                        (512, 64, 1)])
+def test_gemm_tilings(ns, bk, ctas, tune):
     """The non-persistent kernel in every tiling the planner can choose
-    (measurement switches): 256 / 512 columns per CTA, 64-byte and 128-byte
+    (tuning knobs): 256 / 512 columns per CTA, 64-byte and 128-byte
     swizzled K slabs, one or two CTAs per SM.  (The default, persistent kernel
     runs in every other test.)"""
-    monkeypatch.setenv("RARN_GEMM_NS", ns)
-    monkeypatch.setenv("RARN_GEMM_BK", bk)
-    monkeypatch.setenv("RARN_GEMM_CTAS", ctas)
+    tune(gemm_cols=ns, gemm_slab=bk, gemm_ctas_per_sm=ctas)
     for T, H, K in ((256, 1024, 448), (64, 512, 1000), (300, 2048, 2048)):
         plan = run_case(T, H, K, "bf16", seed=K)
         assert f"cols_per_cta={ns}" in plan and f"bk={bk}" in plan, plan
         assert "persistent=0" in plan, plan
 
 
-@pytest.mark.parametrize("pair", ["0", "1"])
-def test_gemm_persistent_one_sm_and_sm_pairs(pair, monkeypatch):
+@pytest.mark.parametrize("pair", [0, 1])
+def test_gemm_persistent_one_sm_and_sm_pairs(pair, tune):
     """The persistent kernel forced onto one SM per 128 x 256 tile and onto
     SM pairs (two-CTA clusters, cta_group::2 MMAs on 256 x 256 tiles, each CTA
     staging half of the W slab): one row, ragged rows and K, a single K slab,
     3 to 32 column tiles, and more tiles than pairs so that both accumulators
     are reused."""
-    monkeypatch.setenv("RARN_GEMM_PERSIST", "1")
-    monkeypatch.setenv("RARN_GEMM_PAIR", pair)
+    tune(gemm_persistent=1, gemm_pair=pair)
     for T, H, K, dt in ((1, 1024, 512, "bf16"), (200, 768, 520, "bf16"),
                         (300, 2048, 1024, "f16"), (700, 1536, 64, "bf16"),
                         (520, 8192, 192, "bf16"), (2500, 4096, 96, "bf16")):
@@ -175,14 +171,14 @@ def test_gemm_persistent_one_sm_and_sm_pairs(pair, monkeypatch):
     assert "persistent=1" in plan and f"pair={pair}" in plan, plan
 
 
-@pytest.mark.parametrize("pair", ["0", "1"])
-def test_gemm_norm_in_epilogue_matches_norm_kernel(pair, monkeypatch):
+@pytest.mark.parametrize("pair", [0, 1])
+def test_gemm_norm_in_epilogue_matches_norm_kernel(pair, tune):
     """y written by the persistent kernel's epilogue (each tile waits on its
     128-row block's counter) and by the separate norm kernel: bit-identical,
     on shapes with more tiles than CTAs or pairs, so that row blocks straddle
     two rounds of tiles, and with 32 column tiles per row."""
     import torch
-    monkeypatch.setenv("RARN_GEMM_PAIR", pair)
+    tune(gemm_pair=pair)
     for T, H, K in ((2500, 4096, 512), (1000, 8192, 576), (129, 2048, 1024)):
         gen = torch.Generator(device="cuda").manual_seed(T + H + K)
         a = torch.randn(T, K, device="cuda", generator=gen).to(torch.bfloat16)
@@ -190,27 +186,26 @@ def test_gemm_norm_in_epilogue_matches_norm_kernel(pair, monkeypatch):
         r0 = torch.randn(T, H, device="cuda", generator=gen).to(torch.bfloat16)
         g = (torch.rand(H, device="cuda", generator=gen) + 0.5).to(torch.bfloat16)
         outs = {}
-        for fuse in ("1", "0"):
-            monkeypatch.setenv("RARN_GEMM_FUSE", fuse)
+        for fuse in (-1, 0):
+            tune(gemm_norm_in_epilogue=fuse)
             plan = rarn.plan_gemm(T, H, K)
-            assert ("norm in epilogue" in plan) == (fuse == "1"), plan
+            assert ("norm in epilogue" in plan) == (fuse == -1), plan
             r = r0.clone()
             y = rarn.gemm_add_rms_norm(a, w, r, g, 1e-6)
             torch.cuda.synchronize()
             assert rarn.watchdog(clear=True) == 0
             outs[fuse] = (y, r)
-        assert torch.equal(outs["1"][0], outs["0"][0]), f"y differs at T{T} H{H} K{K}"
-        assert torch.equal(outs["1"][1], outs["0"][1]), f"residual differs at T{T} H{H} K{K}"
+        assert torch.equal(outs[-1][0], outs[0][0]), f"y differs at T{T} H{H} K{K}"
+        assert torch.equal(outs[-1][1], outs[0][1]), f"residual differs at T{T} H{H} K{K}"
 
 
-def test_gemm_pair_tail_halves(monkeypatch):
+def test_gemm_pair_tail_halves(tune):
     """The pair kernel's last partial round as 128-column halves (N = 128
     MMAs; a round then fills up to twice as many SM pairs) against whole
     tiles: bit-identical (the same K order per element, the same 128-column
     partial sums); sampled rows against the oracle."""
     import torch
-    monkeypatch.setenv("RARN_GEMM_PAIR", "1")
-    monkeypatch.setenv("RARN_GEMM_SPLIT", "1")
+    tune(gemm_pair=1)
     plan = run_case(1536, 4096, 512, "bf16", seed=9, sample_rows=np.arange(1280, 1536, 4))
     assert "tail=halves" in plan, plan
     for T, H, K in ((1536, 4096, 512), (2560, 2048, 576)):
@@ -220,17 +215,17 @@ def test_gemm_pair_tail_halves(monkeypatch):
         r0 = torch.randn(T, H, device="cuda", generator=gen).to(torch.bfloat16)
         g = (torch.rand(H, device="cuda", generator=gen) + 0.5).to(torch.bfloat16)
         outs = {}
-        for split in ("1", "0"):
-            monkeypatch.setenv("RARN_GEMM_SPLIT", split)
+        for split in (-1, 0):
+            tune(gemm_tail_split=split)
             plan = rarn.plan_gemm(T, H, K)
-            assert ("tail=halves" in plan) == (split == "1") and "pair=1" in plan, plan
+            assert ("tail=halves" in plan) == (split == -1) and "pair=1" in plan, plan
             r = r0.clone()
             y = rarn.gemm_add_rms_norm(a, w, r, g, 1e-6)
             torch.cuda.synchronize()
             assert rarn.watchdog(clear=True) == 0
             outs[split] = (y, r)
-        dy = (outs["1"][0] != outs["0"][0])
-        dr = (outs["1"][1] != outs["0"][1])
+        dy = (outs[-1][0] != outs[0][0])
+        dr = (outs[-1][1] != outs[0][1])
         rows_y = torch.nonzero(dy.any(1)).flatten().tolist()
         cols_y = torch.nonzero(dy.any(0)).flatten().tolist()
         assert not dy.any() and not dr.any(), (
@@ -255,11 +250,11 @@ def test_gemm_splitk(T, H, K, dt):
     assert "splitk=" in plan, plan
 
 
-def test_gemm_splitk_off_matches_oracle_too(monkeypatch):
+def test_gemm_splitk_off_matches_oracle_too(tune):
     """The same single-row-block shapes without split K (the persistent
     kernel): both stay within the bound; split K is a different, equally
     valid binary32 summation order."""
-    monkeypatch.setenv("RARN_GEMM_SPLITK", "0")
+    tune(gemm_split_k=0)
     for T, H, K in ((1, 4096, 4096), (100, 2048, 4096)):
         plan = run_case(T, H, K, "bf16", seed=T * 7 + K)
         assert "splitk=" not in plan and "persistent=1" in plan, plan

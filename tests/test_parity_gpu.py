@@ -250,13 +250,12 @@ def test_watchdog_clear_after_everything():
 
 @pytest.mark.parametrize("ppt", [1, 2, 4])
 @pytest.mark.parametrize("groups", [1, 2])
-def test_stream_consumer_groups(groups, ppt, monkeypatch):
+def test_stream_consumer_groups(groups, ppt, tune):
     """The TMA-fed kernel with 1 and 2 consumer groups (rows handed out
     round-robin) and 1, 2, 4 packs per thread per chunk, including row
     counts that are not a multiple of the grid times the group count, and
     rows of one, several and a partial chunk."""
-    monkeypatch.setenv("RARN_STREAM_GROUPS", str(groups))
-    monkeypatch.setenv("RARN_STREAM_PPT", str(ppt))
+    tune(stream_groups=groups, stream_packs=ppt)
     rarn.set_path("stream")
     for op, dt, T, H, R in (("fused_add_rms_norm", "bf16", 1001, 4096, 1),
                             ("reduce_add_rms_norm", "bf16", 777, 2048, 8),

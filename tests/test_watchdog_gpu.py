@@ -36,11 +36,11 @@ def test_wait_runs_out_and_is_reported(fill):
     assert rarn.watchdog(clear=True) == 0
 
 
-@pytest.mark.parametrize("K,fill,pair,T", [(1024, 0, "1", 1000), (1024, 9, "1", 1000),
-                                           (1024, 0, "0", 1000), (1024, 9, "0", 1000),
+@pytest.mark.parametrize("K,fill,pair,T", [(1024, 0, 1, 1000), (1024, 9, 1, 1000),
+                                           (1024, 0, 0, 1000), (1024, 9, 0, 1000),
                                            (256, 0, None, 1000), (256, 2, None, 1000),
                                            (2048, 0, None, 64), (2048, 5, None, 64)])
-def test_gemm_wait_runs_out_and_is_reported(K, fill, pair, T, monkeypatch):
+def test_gemm_wait_runs_out_and_is_reported(K, fill, pair, T, tune):
     """The GEMM form (persistent kernel for K = 1024, on SM pairs or on one SM
     per tile; two CTAs per SM for K = 256; split K for 64 rows): one ring
     fill of CTA 0 never completes; every role's wait gives up within the
@@ -48,7 +48,7 @@ def test_gemm_wait_runs_out_and_is_reported(K, fill, pair, T, monkeypatch):
     memory, the watchdog bit is set, and the next call is correct."""
     import torch
     if pair is not None:
-        monkeypatch.setenv("RARN_GEMM_PAIR", pair)
+        tune(gemm_pair=pair)
     H = 2048
     gen = torch.Generator(device="cuda").manual_seed(K + fill)
     a = torch.randn(T, K, device="cuda", generator=gen).to(torch.bfloat16)

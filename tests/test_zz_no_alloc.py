@@ -20,7 +20,8 @@ pytestmark = pytest.mark.gpu
     (8, 4096, 4096),     # split K: its partial products fit the scratch too
     (300, 1024, 512),
     (4096, 4096, 1024),
-    (40000, 8192, 64),   # 32 column tiles: more rows than the scratch holds (two launch pairs)
+    (40000, 8192, 64),   # 32 column tiles: more rows than the scratch holds (three launch
+                         # sequences of 16128, 16128 and 7744 rows)
 ])
 def test_noalloc_matches_workspace_entry_two_calls(T, H, K):
     import torch
