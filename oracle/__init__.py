@@ -18,6 +18,11 @@ Sources followed (by page title and section):
     squares of that stored value, rsqrt(variance / hidden_size + eps), then
     scale by the reciprocal RMS and the weight.
 
+The tensor-parallel form (``tp_reduce_add_rms_norm``) follows the tokenweave
+kernel's reduce-scatter / norm / all-gather over N ranks' buffers, with rank r
+owning rows floor(rT/N) .. floor((r+1)T/N)-1 and the partials summed in rank
+order.
+
 The 8-bit output (``rows_fp8``) follows "Block All Reduce", FP8 section: e4m3
 and e5m2 codes, converted with saturation to the largest finite value; the
 scale is a given per-tensor value or max |v| / maxf per row.
@@ -94,6 +99,11 @@ class Oracle:
         lib.oracle_gemm_add_rms_norm.argtypes = [c_int, i64, i64, i64, p, i64, p, i64, p, i64, p,
                                                  f32, p, i64, p, p, p, c_int]
         lib.oracle_gemm_add_rms_norm.restype = c_int
+        lib.oracle_tp_reduce_add_rms_norm.argtypes = [c_int, i64, i64, i32, p, p, p, f32, p, p,
+                                                      p, p, c_int]
+        lib.oracle_tp_reduce_add_rms_norm.restype = c_int
+        lib.oracle_tp_rows.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+        lib.oracle_tp_rows.restype = None
         lib.oracle_decode.argtypes = [c_int, p, p, i64]
         lib.oracle_decode.restype = None
         lib.oracle_round.argtypes = [c_int, p, p, i64]
@@ -256,6 +266,40 @@ class Oracle:
         r.p64, r.abs64 = p64, a64
         return r
 
+    def tp_rows(self, T, N, r):
+        """Rows [r0, r1) that rank r of N owns in the tensor-parallel form."""
+        r0, r1 = ctypes.c_int64(0), ctypes.c_int64(0)
+        self.lib.oracle_tp_rows(T, N, r, ctypes.byref(r0), ctypes.byref(r1))
+        return r0.value, r1.value
+
+    def tp_reduce_add_rms_norm(self, bufs, residual, gamma, eps, dtype, *, want_y64=False,
+                               threads=0):
+        """Tensor-parallel form over N ranks: ``bufs`` is N partials [T, H]
+        (one per rank), ``residual`` [T, H] the ranks' residual rows stacked in
+        rank order.  Returns a Result whose ``ys`` is the N ranks' output
+        buffers after the all-gather (``y`` is rank 0's) and ``residual`` the
+        updated residual."""
+        bufs = [self._as_storage(b, dtype) for b in bufs]
+        residual = self._as_storage(residual, dtype)
+        gamma = self._as_storage(gamma, dtype)
+        N = len(bufs)
+        T, H = residual.shape
+        if any(b.shape != (T, H) for b in bufs):
+            raise ValueError("every rank's buffer must be [T, H]")
+        ys = [np.zeros_like(residual) for _ in range(N)]
+        res_out = np.zeros_like(residual)
+        inv = np.empty(T, np.float64)
+        y64 = np.empty((T, H), np.float64) if want_y64 else None
+        bp = (ctypes.c_void_p * N)(*[b.ctypes.data for b in bufs])
+        yp = (ctypes.c_void_p * N)(*[y.ctypes.data for y in ys])
+        n = _check(self.lib.oracle_tp_reduce_add_rms_norm(
+            DTYPES[dtype], T, H, N, ctypes.cast(bp, ctypes.c_void_p), _ptr(residual),
+            _ptr(gamma), float(eps), _ptr(res_out), ctypes.cast(yp, ctypes.c_void_p), _ptr(inv),
+            _ptr(y64), threads))
+        r = Result(ys[0], res_out, inv, y64, n)
+        r.ys = ys
+        return r
+
     def decode(self, bits, dtype) -> np.ndarray:
         """Storage bits -> binary64 values (the oracle's own decoder)."""
         bits = self._as_storage(bits, dtype)
@@ -308,6 +352,14 @@ def reduce_fp8in(*a, **k) -> Result:
 
 def gemm_add_rms_norm(*a, **k) -> Result:
     return default().gemm_add_rms_norm(*a, **k)
+
+
+def tp_reduce_add_rms_norm(*a, **k) -> Result:
+    return default().tp_reduce_add_rms_norm(*a, **k)
+
+
+def tp_rows(*a, **k):
+    return default().tp_rows(*a, **k)
 
 
 def decode(*a, **k) -> np.ndarray:

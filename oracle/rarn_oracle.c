@@ -53,6 +53,17 @@
  * r_i), h_i = RN_dt(acc), and steps 2-4 as above.  The pages fix no scale
  * rule; a per-buffer (per-tensor) scale is the plainest reading.
  *
+ * Tensor-parallel form (oracle_tp_reduce_add_rms_norm): N ranks each hold a
+ * partial [T, H] (the output of a row-parallel layer) and the residual rows
+ * of their own block of tokens; "Tokenweave fused-RMSNorm-AR kernel", Code
+ * walkthrough: each rank reduces its tokens' rows over every rank's buffer
+ * (the reduce-scatter), adds its residual, stores it, normalises, and writes
+ * the normalised row into every rank's buffer (the all-gather).  Readings:
+ * rank r owns rows floor(r T / N) .. floor((r + 1) T / N) - 1 (contiguous,
+ * in rank order); the partials are summed in rank order 0 .. N-1 in binary32
+ * (the pages leave the order to the switch's multimem reduction), then the
+ * residual, one rounding -- the reduce form with R = N.
+ *
  * Build flags must keep binary32 arithmetic exact IEEE: no -ffast-math, and
  * -ffp-contract=off (there is no multiply in the binary32 part, but the flag
  * documents the intent).
@@ -348,6 +359,93 @@ int oracle_rows_ex(int dt, int rdt, int64_t T, int64_t H, int32_t R, const void 
     job_t j = {dt, rdt, T, H, R, x, ldx, slice, R >= 1 ? residual_in : NULL, ldr, gamma, eps,
                R >= 1 ? residual_out : NULL, y, ldy, inv_out, y64_out};
     return run(&j, nthreads);
+}
+
+/* ----------------------------------------------------------------------- */
+/* Tensor-parallel form: reduce-scatter, residual + norm, all-gather        */
+/* ----------------------------------------------------------------------- */
+
+/* Rows of rank r among N: [floor(r T / N), floor((r + 1) T / N)). */
+void oracle_tp_rows(int64_t T, int32_t N, int32_t r, int64_t *r0, int64_t *r1) {
+    *r0 = T * (int64_t)r / N;
+    *r1 = T * (int64_t)(r + 1) / N;
+}
+
+typedef struct {
+    int dt;
+    int64_t H;
+    int32_t N;
+    const void *const *bufs; /* N partials [T, H] */
+    const void *residual_in; /* [T, H]: the ranks' blocks of rows, stacked */
+    void *residual_out;
+    const void *gamma;
+    float eps;
+    void *const *y_out;      /* N outputs [T, H], one per rank */
+    double *inv_out;
+    double *y64_out;
+} tp_job_t;
+
+/* Row t, computed by the rank that owns it. */
+static void tp_row(const void *ctx, int64_t t, double *h) {
+    const tp_job_t *j = (const tp_job_t *)ctx;
+    const int64_t H = j->H, row = t * H;
+    /* reduce-scatter: this rank's row over every rank's buffer, rank order */
+    for (int64_t i = 0; i < H; ++i) {
+        float rank_sum = (float)load_elem(j->dt, j->bufs[0], row + i);
+        for (int32_t q = 1; q < j->N; ++q)
+            rank_sum = rank_sum + (float)load_elem(j->dt, j->bufs[q], row + i);
+        rank_sum = rank_sum + (float)load_elem(j->dt, j->residual_in, row + i);
+        h[i] = round_dt(j->dt, (double)rank_sum);
+    }
+    for (int64_t i = 0; i < H; ++i) store_exact(j->dt, j->residual_out, row + i, h[i]);
+    double ss = 0.0;
+    for (int64_t i = 0; i < H; ++i) ss += h[i] * h[i];
+    const double inv = 1.0 / sqrt(ss / (double)H + (double)j->eps);
+    if (j->inv_out) j->inv_out[t] = inv;
+    /* all-gather: the normalised row into every rank's buffer */
+    for (int64_t i = 0; i < H; ++i) {
+        const double v = (h[i] * inv) * load_elem(j->dt, j->gamma, i);
+        if (j->y64_out) j->y64_out[row + i] = v;
+        const double yv = round_dt(j->dt, v);
+        for (int32_t q = 0; q < j->N; ++q) store_exact(j->dt, j->y_out[q], row + i, yv);
+    }
+}
+
+/* Each rank's block of rows in turn (rows within a block over host threads).
+ * Returns the threads used, or a negative value on error. */
+int oracle_tp_reduce_add_rms_norm(int dt, int64_t T, int64_t H, int32_t N,
+                                  const void *const *bufs, const void *residual_in,
+                                  const void *gamma, float eps, void *residual_out,
+                                  void *const *y_out, double *inv_out, double *y64_out,
+                                  int nthreads) {
+    if (T < 0 || H <= 0 || N < 1 || !bufs || !residual_in || !residual_out || !gamma || !y_out)
+        return -2;
+    tp_job_t j = {dt, H, N, bufs, residual_in, residual_out, gamma, eps, y_out, inv_out, y64_out};
+    int used = 0;
+    for (int32_t r = 0; r < N; ++r) {
+        int64_t r0, r1;
+        oracle_tp_rows(T, N, r, &r0, &r1);
+        /* run_rows numbers rows from 0: shift this rank's block there */
+        tp_job_t jr = j;
+        const int64_t off = r0 * H * elem_size(dt);
+        const void *bq[64];
+        void *yq[64];
+        if (N > 64) return -2;
+        for (int32_t q = 0; q < N; ++q) {
+            bq[q] = (const char *)bufs[q] + off;
+            yq[q] = (char *)y_out[q] + off;
+        }
+        jr.bufs = bq;
+        jr.y_out = yq;
+        jr.residual_in = (const char *)residual_in + off;
+        jr.residual_out = (char *)residual_out + off;
+        jr.inv_out = inv_out ? inv_out + r0 : NULL;
+        jr.y64_out = y64_out ? y64_out + r0 * H : NULL;
+        const int rc = run_rows(&jr, tp_row, r1 - r0, H, nthreads);
+        if (rc < 0) return rc;
+        if (rc > used) used = rc;
+    }
+    return used;
 }
 
 /* ----------------------------------------------------------------------- */

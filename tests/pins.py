@@ -19,7 +19,10 @@ What the pins rest on (none of it is the oracle's own code):
     weight (reduces to the fused form), a constructed single-rounding case and
     exact rational brute force;
   * for the 8-bit partials, the pinned reduce over the same values (power-of-
-    two scales, torch's float8 decoders) and exact rational brute force.
+    two scales, torch's float8 decoders) and exact rational brute force;
+  * for the tensor-parallel form, the pinned reduce over the ranks' stacked
+    partials, a worked example of the rank order, and the properties a
+    partition of the rows into contiguous rank blocks must have.
 """
 from __future__ import annotations
 
@@ -894,6 +897,65 @@ def pin_fp8in_brute_force(O):
             assert np.array_equal(lib_decode(res.residual, dt), want), (dt, fmt)
 
 
+# ---------------------------------------------------------------------------
+# Tensor-parallel form (reduce-scatter, residual + norm, all-gather)
+# ---------------------------------------------------------------------------
+
+def pin_tp_partition(O):
+    """Rank r's rows: contiguous blocks in rank order that cover 0 .. T-1
+    exactly once, sizes differing by at most one (T = qN + m: m blocks of
+    q + 1 rows, N - m of q), for every N up to 9 and T up to 40."""
+    for N in range(1, 10):
+        for T in range(0, 41):
+            blocks = [O.tp_rows(T, N, r) for r in range(N)]
+            assert blocks[0][0] == 0 and blocks[-1][1] == T, (T, N, blocks)
+            for (a0, a1), (b0, b1) in zip(blocks, blocks[1:]):
+                assert a1 == b0, (T, N, blocks)
+            sizes = sorted(b - a for a, b in blocks)
+            q, m = divmod(T, N)
+            assert sizes == [q] * (N - m) + [q + 1] * m, (T, N, blocks)
+
+
+def pin_tp_is_reduce_over_ranks(O):
+    """The N ranks' partials give, in every rank's buffer, the y of the
+    (pinned) reduce over those partials stacked in rank order, and the same
+    updated residual: the reduce-scatter, norm and all-gather compute the
+    reduce form with R = N, row by row whoever owns the row."""
+    rng = np.random.default_rng(31)
+    for dt in ("bf16", "f16", "f32"):
+        for N, T, H in ((1, 5, 24), (2, 7, 40), (3, 10, 33), (5, 4, 16), (8, 19, 64)):
+            bufs = [_rand_bits(rng, (T, H), dt, 1.0 / math.sqrt(N)) for _ in range(N)]
+            r = _rand_bits(rng, (T, H), dt)
+            g = bits_of(rng.uniform(0.5, 1.5, H), dt)
+            got = O.tp_reduce_add_rms_norm(bufs, r, g, 1e-6, dt)
+            want = O.reduce_add_rms_norm(np.stack(bufs), r, g, 1e-6, dt)
+            assert np.array_equal(got.residual, want.residual), (dt, N)
+            assert len(got.ys) == N
+            for q, y in enumerate(got.ys):
+                assert np.array_equal(y, want.y), (dt, N, q)
+
+
+def pin_tp_rank_order_worked_example(O):
+    """Three ranks hold 2^24, 1 and -2^24 (binary32): in rank order
+    fl32(fl32(2^24 + 1) - 2^24) = 0, while the exact sum, and the reverse
+    order, give 1.  With a zero residual the stored residual is 0 and y is 0
+    in every rank's buffer."""
+    T, H = 4, 8
+    vals = [2.0 ** 24, 1.0, -(2.0 ** 24)]
+    bufs = [np.full((T, H), v, np.float32) for v in vals]
+    r = np.zeros((T, H), np.float32)
+    g = np.ones(H, np.float32)
+    got = O.tp_reduce_add_rms_norm(bufs, r, g, 1e-6, "f32")
+    assert np.array_equal(got.residual, np.zeros((T, H), np.float32)), got.residual
+    for y in got.ys:
+        assert np.array_equal(y, np.zeros((T, H), np.float32))
+    # the residual joins after the last rank: (2^24 + 1) + 1 = 2^24 + 2 in one
+    # rounding would give 2^24 + 2; in order it is fl32(2^24 + 1) + 1 = 2^24
+    bufs = [np.full((T, H), 2.0 ** 24, np.float32), np.ones((T, H), np.float32)]
+    got = O.tp_reduce_add_rms_norm(bufs, np.ones((T, H), np.float32), g, 1e-6, "f32")
+    assert np.all(got.residual == np.float32(2.0 ** 24)), got.residual
+
+
 ALL_PINS = [
     pin_decode_all_patterns,
     pin_round_matches_library,
@@ -924,4 +986,7 @@ ALL_PINS = [
     pin_gemm_strides,
     pin_fp8in_power_of_two_scales_are_reduce,
     pin_fp8in_brute_force,
+    pin_tp_partition,
+    pin_tp_is_reduce_over_ranks,
+    pin_tp_rank_order_worked_example,
 ]

@@ -116,6 +116,28 @@ MUTATIONS = {
     "fp8in_residual_not_stored": (
         "if (j->residual_out)\n        for (int64_t i = 0; i < H; ++i) store_exact(j->dt, "
         "j->residual_out, row + i, h[i]);", ""),
+    # tensor-parallel form: ranks summed in reverse order, rank 0 skipped, the
+    # residual dropped or read from rank 0's block, y gathered into rank 0's
+    # buffer only, blocks of rows that overlap or leave gaps
+    "tp_reverse_rank_order": (
+        "float rank_sum = (float)load_elem(j->dt, j->bufs[0], row + i);\n"
+        "        for (int32_t q = 1; q < j->N; ++q)\n"
+        "            rank_sum = rank_sum + (float)load_elem(j->dt, j->bufs[q], row + i);",
+        "float rank_sum = (float)load_elem(j->dt, j->bufs[j->N - 1], row + i);\n"
+        "        for (int32_t q = j->N - 2; q >= 0; --q)\n"
+        "            rank_sum = rank_sum + (float)load_elem(j->dt, j->bufs[q], row + i);"),
+    "tp_skip_rank0": ("float rank_sum = (float)load_elem(j->dt, j->bufs[0], row + i);",
+                      "float rank_sum = 0.0f;"),
+    "tp_no_residual": ("rank_sum = rank_sum + (float)load_elem(j->dt, j->residual_in, row + i);",
+                       ""),
+    "tp_residual_block": ("jr.residual_in = (const char *)residual_in + off;",
+                          "jr.residual_in = residual_in;"),
+    "tp_gather_rank0_only": (
+        "for (int32_t q = 0; q < j->N; ++q) store_exact(j->dt, j->y_out[q], row + i, yv);",
+        "store_exact(j->dt, j->y_out[0], row + i, yv);"),
+    "tp_blocks_ceil": ("*r0 = T * (int64_t)r / N;", "*r0 = (T * (int64_t)r + N - 1) / N;"),
+    "tp_blocks_short": ("*r1 = T * (int64_t)(r + 1) / N;", "*r1 = T * (int64_t)(r + 1) / N - 1;"),
+    "tp_wide_accumulator": ("float rank_sum = (float)load_elem", "double rank_sum = (float)load_elem"),
     "gemm_gamma_index": ("round_dt(g->dt, (h[i] * inv) * load_elem(g->dt, g->gamma, i))",
                          "round_dt(g->dt, (h[i] * inv) * load_elem(g->dt, g->gamma, 0))"),
 }
