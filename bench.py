@@ -66,6 +66,11 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--clock-window", type=float, default=1.0,
+                    help="seconds of untimed back-to-back steps after the timed ones, over "
+                         "which nvidia-smi samples the clocks")
+    ap.add_argument("--config-clock-window", type=float, default=0.5,
+                    help="seconds of untimed replays per configuration for its clock record")
     return ap.parse_args()
 
 
@@ -104,9 +109,11 @@ def max_over_ranks(v: float, device=None) -> float:
 # clocks during the timed region
 # ---------------------------------------------------------------------------
 
-CLOCK_FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
-                "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+CLOCK_FIELDS = ["timestamp", "clocks.sm", "clocks.max.sm", "power.draw",
+                "clocks_event_reasons.active", "clocks_event_reasons.hw_slowdown",
+                "clocks_event_reasons.hw_thermal_slowdown",
                 "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
 
 def nvsmi_id(props, fallback: int) -> str:
@@ -118,51 +125,99 @@ def nvsmi_id(props, fallback: int) -> str:
     return gpu_id
 
 
-class ClockSampler:
-    """nvidia-smi sampling every 200 ms while the measurement runs."""
+def parse_clock_line(line: str):
+    """One nvidia-smi sample: (epoch seconds, SM MHz, max SM MHz, active
+    throttle reasons) or None.  nvidia-smi prints local time."""
+    import datetime
+    cols = [c.strip() for c in line.split(",")]
+    if len(cols) != len(CLOCK_FIELDS):
+        return None
+    try:
+        ts = datetime.datetime.strptime(cols[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        sm, smax = float(cols[1]), float(cols[2])
+    except ValueError:
+        return None
+    reasons = {n for n, v in zip(REASONS, cols[5:]) if v.lower() == "active"}
+    return ts, sm, smax, reasons
 
-    def __init__(self, gpu_id: str):
+
+def clock_stats(samples) -> dict:
+    if not samples:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    return {"sm_mhz": statistics.median(s[1] for s in samples),
+            "sm_max_mhz": max(s[2] for s in samples),
+            "reasons": sorted(set().union(*(s[3] for s in samples))), "samples": len(samples)}
+
+
+class ClockSampler:
+    """nvidia-smi sampling every 100 ms for the whole measurement; named
+    phases (wall-clock intervals) select the samples taken while a given
+    kernel ran."""
+
+    def __init__(self, gpu_id: str, interval_ms: int = 100):
         self.proc = None
         self.path = None
+        self.phases = {}
         try:
             fd, self.path = tempfile.mkstemp(prefix="rarn_clocks_", suffix=".csv")
             self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + ",".join(CLOCK_FIELDS),
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
-    def stop(self) -> dict | None:
+    def wait_ready(self, timeout_s: float = 5.0) -> None:
+        """Block until nvidia-smi has written its first sample (it starts in a
+        few hundred ms), so that the first phase is not missed."""
+        t_end = time.time() + timeout_s
+        while self.proc is not None and time.time() < t_end:
+            self.fh.flush()
+            if os.path.getsize(self.path) > 0:
+                return
+            time.sleep(0.02)
+
+    def begin(self, name: str) -> None:
+        self.phases[name] = [time.time(), None]
+
+    def end(self, name: str) -> None:
+        if name in self.phases:
+            self.phases[name][1] = time.time()
+
+    def stop(self) -> dict:
+        """Stop sampling; every phase's statistics (None without nvidia-smi)."""
         if self.proc is None:
-            return None
+            return {}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
-            for line in f:
-                cols = [c.strip() for c in line.split(",")]
-                if len(cols) != len(CLOCK_FIELDS):
-                    continue
-                try:
-                    sm.append(float(cols[0]))
-                    smax.append(float(cols[1]))
-                except ValueError:
-                    continue
-                for name, val in zip(names, cols[4:]):
-                    if val.lower() == "active":
-                        reasons.add(name)
+            samples = [s for s in map(parse_clock_line, f) if s]
         os.unlink(self.path)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {}
+        for name, (t0, t1) in self.phases.items():
+            t1 = t1 if t1 is not None else time.time()
+            out[name] = clock_stats([s for s in samples if t0 <= s[0] <= t1])
+        return out
+
+
+def hold_clock_window(fn, seconds: float, sync_every: int = 50) -> int:
+    """Keep launching fn() back to back for about `seconds` of wall time (an
+    untimed window in which nvidia-smi samples the clocks this load runs
+    at); returns the launches made."""
+    import torch
+    n = 0
+    t_end = time.time() + seconds
+    while time.time() < t_end:
+        for _ in range(sync_every):
+            fn()
+        n += sync_every
+        torch.cuda.synchronize()
+    return n
 
 
 # ---------------------------------------------------------------------------
@@ -191,6 +246,26 @@ def kernel_source_sha(files=None) -> str:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()
+
+
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal
+
+
+def configs_summary(per_config: dict, peak: float) -> dict:
+    """The method's configurations in a compact form: per workload
+    [us per launch, GB/s, fraction of the measured peak, fraction of the
+    nominal 8 TB/s, launch floor us (latency-bound ones), median SM MHz]."""
+    from residual_add_rmsnorm_gb300 import workloads as W
+    out = {"fields": ["us", "GB/s", "frac_measured", "frac_8TBps", "floor_us", "sm_mhz"]}
+    for w in W.CONFIGS:
+        e = per_config.get(w.name)
+        if not e:
+            continue
+        f = e.get("floor_us")
+        out[w.name] = [round(e["us_per_launch"], 2), round(e["gbs"], 0),
+                       round(e["gbs"] / peak, 3), round(e["gbs"] / NOMINAL_HBM_GBS, 3),
+                       None if f is None else round(f, 2), e.get("sm_mhz")]
+    return out
 
 
 def measured_hbm_peak():
@@ -332,9 +407,24 @@ def cpu_baseline(w, target_s: float) -> dict:
         r = oracle_call(w, d)
     el = time.perf_counter() - t0
     nbytes = rows * row_bytes(w) * reps
-    return {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": r.threads, "kind": "oracle",
-            "sample": f"rows 0..{rows - 1} of {w.name}, {reps} repetitions, {el:.1f} s",
-            "rows_per_s": rows * reps / el}
+    out = {"value": nbytes / el / 1e9, "unit": "GB/s", "cores": r.threads, "kind": "oracle",
+           "sample": f"rows 0..{rows - 1} of {w.name}, {reps} repetitions, {el:.1f} s",
+           "rows_per_s": rows * reps / el}
+    # the same oracle on one core, on fewer rows
+    rows1 = min(w.T, 32)
+    d1 = W.generate(w, rows=(0, rows1))
+    t0 = time.perf_counter()
+    oracle_call(w, d1, threads=1)
+    one = time.perf_counter() - t0
+    reps1 = max(1, min(200, int(target_s / 3 / max(one, 1e-6))))
+    t0 = time.perf_counter()
+    for _ in range(reps1):
+        oracle_call(w, d1, threads=1)
+    el1 = time.perf_counter() - t0
+    out["value_1core"] = rows1 * row_bytes(w) * reps1 / el1 / 1e9
+    out["rows_per_s_1core"] = rows1 * reps1 / el1
+    out["sample_1core"] = f"rows 0..{rows1 - 1} of {w.name}, {reps1} repetitions, {el1:.1f} s"
+    return out
 
 
 def run_reference(args):
@@ -387,7 +477,13 @@ def run_reference(args):
 # GPU measurement
 # ---------------------------------------------------------------------------
 
-def time_steps(call, steps, warmup, stream):
+def time_steps(call, steps, warmup, stream, sampler=None, window_s=0.0):
+    """ms for exactly `steps` calls between CUDA events on `stream`, after
+    `warmup` untimed calls, with a barrier and a synchronize on both sides.
+    With a sampler, the phase "timed" covers the timed calls and the phase
+    "load" also an untimed window of `window_s` seconds of the same calls
+    right after them (a timed region of a few ms is shorter than the
+    sampling interval)."""
     import torch
     for _ in range(warmup):
         call()
@@ -396,17 +492,38 @@ def time_steps(call, steps, warmup, stream):
     torch.cuda.synchronize()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    if sampler:
+        sampler.begin("load")
+        sampler.begin("timed")
     start.record(stream)
     for _ in range(steps):
         call()
     end.record(stream)
     torch.cuda.synchronize()
+    if sampler:
+        sampler.end("timed")
+        if window_s > 0:
+            hold_clock_window(call, window_s)
+        sampler.end("load")
     barrier()
     torch.cuda.synchronize()
     return start.elapsed_time(end)  # ms
 
 
-def time_graph(w, data, device, l2_bytes, min_launches=200):
+def line_clocks(phases: dict, window_s: float) -> dict | None:
+    """The JSON line's clock record: samples over the timed steps and the
+    untimed window of the same steps right after them."""
+    if not phases:
+        return None
+    load = dict(phases.get("load") or clock_stats([]))
+    load["samples_in_timed_region"] = (phases.get("timed") or {}).get("samples", 0)
+    load["window_s"] = window_s
+    load["how"] = ("nvidia-smi every 100 ms over the timed steps and a window of the same "
+                   "back-to-back steps right after them")
+    return load
+
+
+def time_graph(w, data, device, l2_bytes, min_launches=200, sampler=None, hold_s=0.0):
     """Per-launch device time of one configuration without host overhead and
     with a cold L2: enough copies of the inputs and outputs to cover 2 x L2
     are launched round-robin inside one CUDA graph, so no launch finds its
@@ -451,8 +568,64 @@ def time_graph(w, data, device, l2_bytes, min_launches=200):
         e.record()
         e.synchronize()
         times.append(s.elapsed_time(e))
+    if sampler and hold_s > 0:  # clocks under this load, untimed
+        sampler.begin(w.name)
+        hold_clock_window(graph.replay, hold_s, sync_every=max(1, int(2000 // n)))
+        sampler.end(w.name)
     del graph, sets, calls
     return 1e3 * statistics.median(times) / n, copies, n
+
+
+def plan_field(plan: str, key: str) -> int | None:
+    import re
+    m = re.search(rf"\b{key}=(\d+)", plan)
+    return int(m.group(1)) if m else None
+
+
+def time_floor(w, plan: str, device, l2_bytes, min_launches=200):
+    """The launch floor of a configuration: its plan's grid and block of the
+    library's empty kernel (one row per CTA prefetched into L2, the
+    dependency wait and the trigger, the same PDL setting), timed like the
+    configuration itself (CUDA graph, rows cycled so each launch prefetches
+    cold rows).  None if the plan has no grid."""
+    import math
+
+    import torch
+
+    import residual_add_rmsnorm_gb300 as rarn
+    from residual_add_rmsnorm_gb300 import workloads as W
+    grid, block = plan_field(plan, "grid"), plan_field(plan, "block")
+    if not grid or not block:
+        return None
+    # a CTA's first row: its inputs (x, the residual, the partials)
+    row_bytes = (w.n_inputs * W.ELEM_SIZE[w.dtype] * w.H + 15) // 16 * 16
+    row_bytes = min(row_bytes, 1 << 20)
+    copies = max(1, min(64, math.ceil(2 * l2_bytes / (grid * row_bytes))))
+    buf = torch.empty(copies * grid * row_bytes, dtype=torch.uint8, device=device)
+    views = [buf[i * grid * row_bytes:(i + 1) * grid * row_bytes] for i in range(copies)]
+    passes = max(1, math.ceil(min_launches / copies))
+    for v in views:
+        rarn.launch_floor(grid, block, v, row_bytes)
+    torch.cuda.synchronize(device)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(passes):
+            for v in views:
+                rarn.launch_floor(grid, block, v, row_bytes)
+    n = passes * copies
+    graph.replay()
+    torch.cuda.synchronize(device)
+    times = []
+    for _ in range(3):
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record()
+        graph.replay()
+        e.record()
+        e.synchronize()
+        times.append(s.elapsed_time(e))
+    del graph, views, buf
+    return 1e3 * statistics.median(times) / n
 
 
 def measured_tensor_peak():
@@ -468,8 +641,10 @@ def measured_tensor_peak():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def _graph_us(fn, launches=10, reps=3):
-    """Per-launch device time of fn() replayed in a CUDA graph (best of reps)."""
+def _graph_us(fn, launches=10, reps=3, sampler=None, phase=None, hold_s=0.0):
+    """Per-launch device time of fn() replayed in a CUDA graph (best of reps);
+    with a sampler, the graph is then replayed untimed for hold_s seconds
+    under the phase name, so the clocks of this load are sampled."""
     import torch
     for _ in range(2):
         fn()
@@ -490,10 +665,14 @@ def _graph_us(fn, launches=10, reps=3):
         e.synchronize()
         t = 1e3 * s.elapsed_time(e) / launches
         best = t if best is None else min(best, t)
+    if sampler and phase and hold_s > 0:
+        sampler.begin(phase)
+        hold_clock_window(graph.replay, hold_s, sync_every=5)
+        sampler.end(phase)
     return best
 
 
-def time_gemm(gw, device, rarn):
+def time_gemm(gw, device, rarn, sampler=None, hold_s=0.0):
     """The GEMM-producer form: one tcgen05 kernel (matrix product, residual
     add, RMSNorm) timed against the unfused sequence the same library offers
     a user (cuBLAS product through torch.matmul, then the fused norm kernel);
@@ -504,7 +683,8 @@ def time_gemm(gw, device, rarn):
     a, w, r, g = (to_device(d[k], gw.dtype, device) for k in ("a", "w", "residual", "gamma"))
     y = torch.empty_like(r)
     part = torch.empty_like(r)
-    us = _graph_us(lambda: rarn.gemm_add_rms_norm(a, w, r, g, gw.eps, out=y))
+    us = _graph_us(lambda: rarn.gemm_add_rms_norm(a, w, r, g, gw.eps, out=y), sampler=sampler,
+                   phase=gw.name, hold_s=hold_s)
     us_mm = _graph_us(lambda: torch.matmul(a, w.t(), out=part))
     us_unfused = _graph_us(lambda: (torch.matmul(a, w.t(), out=part),
                                     rarn.fused_add_rms_norm(part, r, g, gw.eps, out=y)))
@@ -549,14 +729,15 @@ def fp8in_plan(device, rarn, R=8, T=8192, H=8192) -> str:
     return rarn.plan_fp8in(T, H, R, "bf16", True, props.multi_processor_count, smem)
 
 
-def time_fp8in(device, rarn, R=8, T=8192, H=8192):
+def time_fp8in(device, rarn, R=8, T=8192, H=8192, sampler=None, hold_s=0.0):
     """The reduce over 8-bit partials on the headline shape; the inputs
     (0.9 GB) exceed L2, so launches read cold data."""
     import torch
     codes, scales, res, g, alg = fp8in_tensors(device, R, T, H)
     y = torch.empty_like(res)
     us = _graph_us(lambda: rarn.reduce_add_rms_norm_fp8in(codes, scales, res, g, 1e-6, "e4m3",
-                                                          out=y))
+                                                          out=y),
+                   sampler=sampler, phase=FP8IN_NAME, hold_s=hold_s)
     peak, _ = measured_hbm_peak()
     gbs = alg / (us / 1e6) / 1e9
     del codes, res, y
@@ -580,8 +761,9 @@ def main_fp8in(args, device, rank, world):
     call = lambda: rarn.reduce_add_rms_norm_fp8in(codes, scales, res, g, 1e-6, "e4m3", out=y)
     stream = torch.cuda.current_stream(device)
     sampler = ClockSampler(nvsmi_id(torch.cuda.get_device_properties(device), device.index or 0))
-    ms = time_steps(call, args.steps, args.warmup, stream)
-    clocks = sampler.stop()
+    sampler.wait_ready()
+    ms = time_steps(call, args.steps, args.warmup, stream, sampler, args.clock_window)
+    clocks = line_clocks(sampler.stop(), args.clock_window)
     ms = max_over_ranks(ms, device)
     peak, kind = measured_hbm_peak()
     gbs = world * alg * args.steps / (ms / 1e3) / 1e9
@@ -647,8 +829,9 @@ def main_gemm(args, gw, device, rank, world):
     call = lambda: rarn.gemm_add_rms_norm(a, w, r, g, gw.eps, out=y, workspace=ws)
     stream = torch.cuda.current_stream(device)
     sampler = ClockSampler(nvsmi_id(torch.cuda.get_device_properties(device), device.index or 0))
-    ms = time_steps(call, args.steps, args.warmup, stream)
-    clocks = sampler.stop()
+    sampler.wait_ready()
+    ms = time_steps(call, args.steps, args.warmup, stream, sampler, args.clock_window)
+    clocks = line_clocks(sampler.stop(), args.clock_window)
     ms = max_over_ranks(ms, device)
     peak, kind = measured_tensor_peak()
     tflops = world * gw.flops() * args.steps / (ms / 1e3) / 1e12
@@ -712,8 +895,8 @@ def main():
 
     props = torch.cuda.get_device_properties(device)
     sampler = ClockSampler(nvsmi_id(props, local_rank))
-    ms = time_steps(call, args.steps, args.warmup, stream)
-    clocks = sampler.stop()
+    sampler.wait_ready()
+    ms = time_steps(call, args.steps, args.warmup, stream, sampler, args.clock_window)
     ms = max_over_ranks(ms, device)
     alg = w.algorithmic_bytes()
     per_launch_s = ms / 1e3 / args.steps
@@ -732,6 +915,7 @@ def main():
     watchdog = rarn.watchdog(clear=True)
 
     per_config = {}
+    hold = args.config_clock_window
     if not args.no_configs:
         l2 = int(getattr(props, "L2_cache_size", 128 << 20))
         del tensors, call
@@ -739,22 +923,37 @@ def main():
         rarn.set_path("auto")
         for cw in W.CONFIGS + W.EXTENDED:
             cd = W.generate(cw)
-            us, copies, n = time_graph(cw, cd, device, l2)
+            us, copies, n = time_graph(cw, cd, device, l2, sampler=sampler, hold_s=hold)
             cb = cw.algorithmic_bytes()
             gbs = cb / (us / 1e6) / 1e9
+            plan = plan_of(cw, rarn)
             per_config[cw.name] = {
                 "kind": "widened" if cw in W.EXTENDED else "config",
                 "us_per_launch": us, "gbs": gbs, "rows_per_s": cw.T / (us / 1e6),
-                "frac_of_peak": gbs / peak, "algorithmic_bytes": cb,
+                "frac_of_peak": gbs / peak, "frac_of_nominal": gbs / NOMINAL_HBM_GBS,
+                "algorithmic_bytes": cb,
                 "timing": f"CUDA graph of {n} launches over {copies} input copies (cold L2)",
-                "plan": plan_of(cw, rarn)}
+                "plan": plan}
+            if cw in W.CONFIGS and cw.algorithmic_bytes() < 64e6:
+                # latency-bound: the launch floor of the same grid and block
+                floor = time_floor(cw, plan, device, l2)
+                per_config[cw.name]["floor_us"] = floor
+                per_config[cw.name]["us_above_floor"] = None if floor is None else us - floor
             del cd
             torch.cuda.empty_cache()
         for gw in W.GEMM_CONFIGS:
-            per_config[gw.name] = time_gemm(gw, device, rarn)
-        per_config[FP8IN_NAME] = time_fp8in(device, rarn)
+            per_config[gw.name] = time_gemm(gw, device, rarn, sampler=sampler, hold_s=hold)
+        per_config[FP8IN_NAME] = time_fp8in(device, rarn, sampler=sampler, hold_s=hold)
         if rarn.watchdog(clear=True):
             watchdog = 1
+    phases = sampler.stop()
+    clocks = line_clocks(phases, args.clock_window)
+    for name, entry in per_config.items():
+        st = phases.get(name)
+        if st:
+            entry["sm_mhz"] = st["sm_mhz"]
+            entry["clock_samples"] = st["samples"]
+            entry["clock_reasons"] = st["reasons"]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline and dense:
@@ -782,6 +981,9 @@ def main():
         "gpu_launches": args.steps,
         "watchdog": watchdog,
         "per_config": per_config,
+        # last, so that a tail of the output still carries it: every
+        # configuration of the method in a few numbers
+        "configs_summary": configs_summary(per_config, peak),
     }
     print(json.dumps(line), flush=True)
 

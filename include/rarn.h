@@ -537,6 +537,23 @@ rarn_status rarn_watchdog(uint32_t *flags, int clear);
  * memory only; 0 = none; -1 = the query failed (no device). */
 int rarn_host_access(void);
 
+/*
+ * Measurement aid: the launch floor of the row kernels.  Launches `grid` CTAs
+ * of `block` threads of a kernel that does only what every row kernel does
+ * besides its row work: one thread per CTA prefetches `row_bytes` bytes at
+ * rows + blockIdx * row_bytes into L2 (skipped when rows is NULL), the CTA
+ * waits for the previous kernel on the stream (griddepcontrol.wait) and lets
+ * the next one launch, under the same programmatic-dependent-launch setting
+ * (rarn_set_pdl) as the compute calls.  Timed in the same harness as a
+ * compute call, it gives the time no schedule of that call can go below.
+ * `rows` (device memory, 16-byte aligned) must span grid * row_bytes bytes;
+ * row_bytes is a multiple of 16 up to 2^20.  Nothing is written.  Errors:
+ * grid < 1, block outside 1..1024 or a bad row argument: RARN_ERR_INVALID_ARG;
+ * a failed launch: RARN_ERR_CUDA.  The pages have no counterpart.
+ */
+rarn_status rarn_launch_floor(const void *rows, int64_t row_bytes, int32_t grid, int32_t block,
+                              void *stream);
+
 /* ABI version: (major << 16) | minor. */
 int rarn_version(void);
 

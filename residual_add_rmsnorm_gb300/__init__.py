@@ -30,7 +30,8 @@ __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_ho
            "rms_norm_fp8", "fused_add_rms_norm_fp8", "reduce_add_rms_norm_fp8", "plan_fp8",
            "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm", "plan_fp8in",
            "gemm_workspace_bytes", "gemm_add_rms_norm_noalloc", "reduce_add_rms_norm_fp8in",
-           "TUNING", "set_tuning", "get_tuning", "reset_tuning", "tuning", "gemm_noalloc_rows"]
+           "TUNING", "set_tuning", "get_tuning", "reset_tuning", "tuning", "gemm_noalloc_rows",
+           "launch_floor"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
@@ -166,6 +167,8 @@ def library() -> ctypes.CDLL:
     lib.rarn_get_tuning.restype = c_int
     lib.rarn_reset_tuning.argtypes = []
     lib.rarn_reset_tuning.restype = c_int
+    lib.rarn_launch_floor.argtypes = [vp, i64, i32, i32, vp]
+    lib.rarn_launch_floor.restype = c_int
     lib.rarn_gemm_noalloc_rows.argtypes = [i64]
     lib.rarn_gemm_noalloc_rows.restype = i64
     _lib = lib
@@ -638,6 +641,21 @@ def plan_gemm(T: int, H: int, K: int, dtype: str = "bf16", num_sms: int = 152) -
     if st not in (0, 2):
         _check(st, "rarn_plan_gemm")
     return buf.value.decode()
+
+
+def launch_floor(grid: int, block: int, rows=None, row_bytes: int = 0) -> None:
+    """The row kernels' launch floor on the current stream of ``rows``'s
+    device (else the current device): ``grid`` CTAs of ``block`` threads that
+    only prefetch one row each (``row_bytes`` bytes of ``rows`` per CTA),
+    wait for the previous kernel and let the next launch.  A measurement aid."""
+    import torch
+    dev = rows.device if rows is not None else torch.device("cuda", torch.cuda.current_device())
+    if rows is not None and rows.numel() * rows.element_size() < grid * row_bytes:
+        raise ValueError("rows must hold grid * row_bytes bytes")
+    with torch.cuda.device(dev):
+        _check(library().rarn_launch_floor(rows.data_ptr() if rows is not None else None,
+                                           row_bytes, grid, block, _stream(dev)),
+               "rarn_launch_floor")
 
 
 def set_tuning(name: str, value: int) -> None:

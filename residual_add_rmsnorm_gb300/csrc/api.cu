@@ -39,6 +39,15 @@ __device__ unsigned int g_rarn_watchdog = 0;
 constexpr int64_t kGemmScratchFloats = int64_t(1) << 20;
 static __device__ __align__(256) float g_rarn_gemm_scratch[kGemmScratchFloats];
 
+// Launch floor (rarn_launch_floor): everything a row kernel does besides its
+// row work -- one thread per CTA prefetches the CTA's first row into L2, the
+// CTA waits for the previous grid and lets the next one launch.
+__global__ void k_launch_floor(const char *rows, uint32_t row_bytes) {
+    if (threadIdx.x == 0 && rows) prefetch_l2(rows + (size_t)blockIdx.x * row_bytes, row_bytes);
+    grid_dependency_wait();
+    grid_launch_dependents();
+}
+
 namespace {
 
 thread_local int t_last_cuda_error = 0;
@@ -1247,6 +1256,19 @@ int rarn_host_access(void) {
                                dev) != cudaSuccess)
         return -1;
     return pageable ? 2 : (mapped ? 1 : 0);
+}
+
+rarn_status rarn_launch_floor(const void *rows, int64_t row_bytes, int32_t grid, int32_t block,
+                              void *stream) {
+    if (grid < 1 || block < 1 || block > 1024) return RARN_ERR_INVALID_ARG;
+    if (rows && (row_bytes < 16 || row_bytes % 16 || row_bytes > (1 << 20) || !aligned16(rows)))
+        return RARN_ERR_INVALID_ARG;
+    const cudaError_t e =
+        launch_kernel(k_launch_floor, dim3((unsigned)grid), dim3((unsigned)block), 0,
+                      static_cast<cudaStream_t>(stream), g_pdl.load() != 0, 1,
+                      static_cast<const char *>(rows), static_cast<uint32_t>(rows ? row_bytes : 0));
+    if (e != cudaSuccess) return cuda_fail(e);
+    return RARN_OK;
 }
 
 int rarn_version(void) { return (1 << 16) | 2; }

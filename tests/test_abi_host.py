@@ -608,3 +608,16 @@ def test_noalloc_checks_the_whole_call_first(lib):
     assert f(y2, a, w, r, g, T, 300, K, 1e-6, None) == UNSUPPORTED
     assert f(y2, _rows(B + 2, K, BF16), w, r, g, T, H, K, 1e-6, None) == UNSUPPORTED
     assert f(_rows(None, H, BF16), a, w, r, g, 0, H, K, 1e-6, None) == OK  # T = 0
+
+
+def test_launch_floor_argument_errors(lib):
+    """The launch-floor measurement aid rejects bad shapes and row arguments
+    before any CUDA call."""
+    f = lib.rarn_launch_floor
+    assert f(None, 0, 0, 256, None) == INVALID
+    assert f(None, 0, 4, 0, None) == INVALID
+    assert f(None, 0, 4, 1025, None) == INVALID
+    assert f(A, 0, 4, 256, None) == INVALID           # row of 0 bytes
+    assert f(A, 24, 4, 256, None) == INVALID          # not a multiple of 16
+    assert f(A, 2 ** 20 + 16, 4, 256, None) == INVALID
+    assert f(A + 8, 16, 4, 256, None) == INVALID      # not 16-byte aligned
