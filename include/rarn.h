@@ -405,6 +405,99 @@ int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H);
 rarn_status rarn_plan_fp8in(int64_t T, int64_t H, int32_t R, rarn_dtype dt, int codes_aligned16,
                             int32_t num_sms, int32_t max_smem, char *out, size_t cap);
 
+/*
+ * Tensor-parallel form: reduce-scatter, residual add + RMSNorm, all-gather
+ * over N ranks (one GPU each), as the tokenweave fused-RMSNorm-AR kernel does
+ * ("Tokenweave fused-RMSNorm-AR kernel", Code walkthrough).  Every rank q
+ * holds a buffer of T x H elements (dense, row-major, type dt) that every
+ * rank can address (a peer mapping, e.g. through rarn_ipc_import): on entry
+ * it holds rank q's partial (the output of its row-parallel layer); on exit
+ * it holds y for all T rows.  Rank r owns rows floor(r T / N) .. floor((r + 1)
+ * T / N) - 1 (rarn_tp_rows) and keeps the residual of those rows only.  For
+ * each of its rows rank r computes
+ *   h = RN(((p_0 + p_1) + ... + p_{N-1}) + residual)   (binary32 adds in rank
+ *       order, one rounding; residual <- h)
+ *   y = RN((h * rsqrt(mean(h^2) + eps)) * gamma)
+ * and writes y into row t of every rank's buffer, so that the reduce form over
+ * the N ranks' partials (R = N) is what every rank ends up with, bit for bit.
+ * The reads and writes of other ranks' buffers are plain 16-byte loads and
+ * stores (no multimem, no TMA).
+ *
+ * Ordering between ranks.  With signal pads (signals[q] non-NULL for every q:
+ * RARN_TP_SIGNAL_BYTES of device memory per rank, zeroed once before first
+ * use, addressable by every rank like the buffers), CTA b of every rank meets
+ * CTA b of every other rank at entry -- so every rank's partial is complete
+ * before any rank reads it -- and at exit -- so all rows of y are in this
+ * rank's buffer before anything after the call on `stream` runs.  Every wait
+ * is bounded (10 s); one that runs out sets watchdog bit 3 (rarn_watchdog),
+ * that CTA's rows are not computed, and the pads must be zeroed again on
+ * every rank before the next call.  With signals[0] == NULL there is no
+ * device wait at all: the caller must order the call after every rank's
+ * partial is complete and order any use of the buffer after every rank's
+ * call has completed (e.g. host barriers around the call).  Every rank must
+ * make the call with the same T, H, dt and signal setting on the same GPU
+ * model (CTA b pairs with CTA b).
+ *
+ * Errors: a NULL group, world_size outside 1 .. RARN_TP_MAX_RANKS, rank
+ * outside 0 .. N-1, a NULL buffer or gamma with T > 0, a NULL residual for a
+ * rank that owns rows (a rank without rows, T < N, may pass NULL), signal pads
+ * given for some ranks only, T < 0, H <= 0, a NaN / negative / infinite eps,
+ * an unknown dt: RARN_ERR_INVALID_ARG; H * sizeof(dt) not a multiple of 16,
+ * more than 2048 16-byte packs per row, pointers not 16-byte aligned (pads: 4
+ * bytes): RARN_ERR_UNSUPPORTED; buffers overlapping each other, the residual
+ * or gamma: RARN_ERR_ALIAS.  T = 0 returns RARN_OK.  Asynchronous on `stream`.
+ */
+#define RARN_TP_MAX_RANKS 8
+#define RARN_TP_SIGNAL_BYTES (1024 * RARN_TP_MAX_RANKS * 4)
+
+typedef struct rarn_tp_group {
+    int32_t world_size;                       /* N */
+    int32_t rank;                             /* this rank, 0 .. N-1 */
+    void *buffers[RARN_TP_MAX_RANKS];         /* rank q's [T, H] buffer, as this process
+                                                 addresses it */
+    uint32_t *signals[RARN_TP_MAX_RANKS];     /* rank q's signal pad, or all NULL */
+} rarn_tp_group;
+
+/* Rows [*r0, *r1) that rank r of N owns: floor(r T / N), floor((r + 1) T / N).
+ * RARN_ERR_INVALID_ARG for T < 0, N < 1, r outside 0 .. N-1 or NULL outputs. */
+rarn_status rarn_tp_rows(int64_t T, int32_t world_size, int32_t rank, int64_t *r0, int64_t *r1);
+
+/* This rank's part: `residual` holds this rank's rows of the residual
+ * ([r1 - r0, H], dense, updated in place); gamma [H]. */
+rarn_status rarn_tp_reduce_add_rms_norm(const rarn_tp_group *group, void *residual,
+                                        const void *gamma, int64_t T, int64_t H, float eps,
+                                        rarn_dtype dt, void *stream);
+
+/* Every rank's part in one launch on the current device: every buffer (and
+ * pad) is memory this device addresses, residuals[q] holds rank q's rows of
+ * the residual, group->rank is ignored.  With signal pads the launch is
+ * cooperative (every CTA resident at once, so the ranks' CTAs can meet in
+ * their barriers); RARN_ERR_CUDA if the ranks' CTAs do not fit on the device
+ * at once.  For a process that holds every rank's buffers on one GPU, and to
+ * check the barrier on one GPU. */
+rarn_status rarn_tp_reduce_add_rms_norm_world(const rarn_tp_group *group, void *const *residuals,
+                                              const void *gamma, int64_t T, int64_t H, float eps,
+                                              rarn_dtype dt, void *stream);
+
+/*
+ * Sharing device memory between the ranks' processes (CUDA IPC): a handle of
+ * RARN_IPC_HANDLE_BYTES bytes names the allocation that contains `ptr` and
+ * the offset of `ptr` in it, so that any pointer returned by an allocator
+ * (a caching allocator's block inside a larger allocation included) can be
+ * shared.  rarn_ipc_export writes the handle of `ptr` (device memory of the
+ * current device); rarn_ipc_import opens a handle made by ANOTHER process
+ * (CUDA cannot open a process's own handles) and returns the pointer through
+ * which this process addresses that memory (peer access enabled lazily);
+ * rarn_ipc_close releases what rarn_ipc_import opened.  The exporting
+ * process must keep the memory allocated while any importer uses it.
+ * Errors: NULL arguments: RARN_ERR_INVALID_ARG; a handle this library did not
+ * write: RARN_ERR_INVALID_ARG; a failed CUDA call: RARN_ERR_CUDA.
+ */
+#define RARN_IPC_HANDLE_BYTES 96
+rarn_status rarn_ipc_export(const void *ptr, void *handle);
+rarn_status rarn_ipc_import(const void *handle, void **ptr);
+rarn_status rarn_ipc_close(void *ptr);
+
 /* Rows that one launch sequence of rarn_gemm_add_rms_norm_noalloc covers for
  * a row length H: floor(floor((2^20 - 16) / (H / 128 + 1)) / 128) * 128
  * (16128 at H = 8192, 8064 at H = 16384); -1 if H is not supported. */
@@ -497,7 +590,10 @@ rarn_status rarn_reset_tuning(void);
  * bounded by `wait_limit_ns` (1 ns .. 2 s).  The waits on that fill run out:
  * the kernel sets the watchdog word (bit 0 / 1: stream consumer / producer;
  * bit 2: GEMM kernel) and returns with its outputs invalid, and the context
- * stays usable.  Returns RARN_ERR_INVALID_ARG for a negative fill or a limit
+ * stays usable.  In the next tensor-parallel launch with signal pads instead,
+ * CTA 0 of rank `fill` (modulo N) never signals at entry, so the other ranks'
+ * CTA 0 (and its own) wait out the limit (bit 3); the pads must then be
+ * zeroed before the next call.  Returns RARN_ERR_INVALID_ARG for a negative fill or a limit
  * out of range.  Not for production use.
  */
 rarn_status rarn_test_stall(long long fill, unsigned long long wait_limit_ns);
@@ -523,10 +619,11 @@ rarn_status rarn_plan_fp8(rarn_op op, int64_t T, int64_t H, int32_t R, rarn_dtyp
 
 /*
  * Watchdog word of the current device.  Kernels that wait on shared-memory
- * barriers give up after a bounded time, set a bit here and return without
- * hanging; their outputs are then not valid.  Bit 0: a stream-kernel consumer
- * wait timed out; bit 1: a stream-kernel producer wait; bit 2: a wait in a
- * GEMM-form kernel.  Synchronises the device.  If
+ * barriers or on other ranks give up after a bounded time, set a bit here and
+ * return without hanging; their outputs are then not valid.  Bit 0: a
+ * stream-kernel consumer wait timed out; bit 1: a stream-kernel producer
+ * wait; bit 2: a wait in a GEMM-form kernel; bit 3: a wait of the
+ * tensor-parallel form's barrier between ranks.  Synchronises the device.  If
  * `clear` is nonzero the word is reset to 0 after reading.
  */
 rarn_status rarn_watchdog(uint32_t *flags, int clear);

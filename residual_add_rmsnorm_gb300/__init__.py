@@ -31,7 +31,9 @@ __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_ho
            "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm", "plan_fp8in",
            "gemm_workspace_bytes", "gemm_add_rms_norm_noalloc", "reduce_add_rms_norm_fp8in",
            "TUNING", "set_tuning", "get_tuning", "reset_tuning", "tuning", "gemm_noalloc_rows",
-           "launch_floor"]
+           "launch_floor", "tp_rows", "tp_reduce_add_rms_norm", "tp_reduce_add_rms_norm_world",
+           "ipc_export", "ipc_import", "ipc_close", "TP_MAX_RANKS", "TP_SIGNAL_BYTES",
+           "IPC_HANDLE_BYTES"]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "librarn.so")
@@ -67,6 +69,19 @@ class Rows(ctypes.Structure):
     """``rarn_rows``: data pointer, row stride in elements, storage type."""
     _fields_ = [("data", ctypes.c_void_p), ("row_stride", ctypes.c_int64),
                 ("dtype", ctypes.c_int)]
+
+
+TP_MAX_RANKS = 8
+TP_SIGNAL_BYTES = 1024 * TP_MAX_RANKS * 4
+IPC_HANDLE_BYTES = 96
+
+
+class TpGroup(ctypes.Structure):
+    """``rarn_tp_group``: world size, rank, every rank's buffer and signal pad
+    as this process addresses them."""
+    _fields_ = [("world_size", ctypes.c_int32), ("rank", ctypes.c_int32),
+                ("buffers", ctypes.c_void_p * TP_MAX_RANKS),
+                ("signals", ctypes.c_void_p * TP_MAX_RANKS)]
 
 
 class Fp8Rows(ctypes.Structure):
@@ -167,6 +182,19 @@ def library() -> ctypes.CDLL:
     lib.rarn_get_tuning.restype = c_int
     lib.rarn_reset_tuning.argtypes = []
     lib.rarn_reset_tuning.restype = c_int
+    tg = ctypes.POINTER(TpGroup)
+    lib.rarn_tp_rows.argtypes = [i64, i32, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]
+    lib.rarn_tp_rows.restype = c_int
+    lib.rarn_tp_reduce_add_rms_norm.argtypes = [tg, vp, vp, i64, i64, f32, c_int, vp]
+    lib.rarn_tp_reduce_add_rms_norm.restype = c_int
+    lib.rarn_tp_reduce_add_rms_norm_world.argtypes = [tg, vp, vp, i64, i64, f32, c_int, vp]
+    lib.rarn_tp_reduce_add_rms_norm_world.restype = c_int
+    lib.rarn_ipc_export.argtypes = [vp, vp]
+    lib.rarn_ipc_export.restype = c_int
+    lib.rarn_ipc_import.argtypes = [vp, ctypes.POINTER(vp)]
+    lib.rarn_ipc_import.restype = c_int
+    lib.rarn_ipc_close.argtypes = [vp]
+    lib.rarn_ipc_close.restype = c_int
     lib.rarn_launch_floor.argtypes = [vp, i64, i32, i32, vp]
     lib.rarn_launch_floor.restype = c_int
     lib.rarn_gemm_noalloc_rows.argtypes = [i64]
@@ -656,6 +684,104 @@ def launch_floor(grid: int, block: int, rows=None, row_bytes: int = 0) -> None:
         _check(library().rarn_launch_floor(rows.data_ptr() if rows is not None else None,
                                            row_bytes, grid, block, _stream(dev)),
                "rarn_launch_floor")
+
+
+def _addr(x) -> int:
+    """A device address: a tensor's data pointer, or an int as given."""
+    return x.data_ptr() if hasattr(x, "data_ptr") else int(x)
+
+
+def tp_rows(T: int, world_size: int, rank: int):
+    """Rows [r0, r1) that ``rank`` of ``world_size`` owns in the tensor-parallel
+    form."""
+    r0, r1 = ctypes.c_int64(0), ctypes.c_int64(0)
+    _check(library().rarn_tp_rows(T, world_size, rank, ctypes.byref(r0), ctypes.byref(r1)),
+           "rarn_tp_rows")
+    return r0.value, r1.value
+
+
+def _tp_group(buffers, rank, signals):
+    g = TpGroup()
+    g.world_size = len(buffers)
+    g.rank = rank
+    if len(buffers) > TP_MAX_RANKS:
+        raise ValueError(f"at most {TP_MAX_RANKS} ranks")
+    for q, b in enumerate(buffers):
+        g.buffers[q] = _addr(b)
+    if signals is not None:
+        if len(signals) != len(buffers):
+            raise ValueError("one signal pad per rank")
+        for q, sg in enumerate(signals):
+            g.signals[q] = _addr(sg)
+    return g
+
+
+def tp_reduce_add_rms_norm(buffers, rank: int, residual, gamma, eps: float, T: int,
+                           signals=None):
+    """This rank's part of the tensor-parallel form: ``buffers`` lists every
+    rank's [T, H] buffer (tensors or device addresses as this process sees
+    them; partial in, y for all T rows out), ``residual`` this rank's rows
+    [r1 - r0, H] (updated in place), ``gamma`` [H]; ``signals`` every rank's
+    pad (TP_SIGNAL_BYTES each) for the in-kernel barrier between ranks, or
+    None when the caller orders the ranks.  Runs on the current stream of
+    residual's device."""
+    import torch
+    H = gamma.numel()
+    dev = residual.device
+    _check_tensor("gamma", gamma, residual.dtype, dev)
+    r0, r1 = tp_rows(T, len(buffers), rank)
+    if tuple(residual.shape) != (r1 - r0, H) or not residual.is_contiguous():
+        raise ValueError(f"residual must be this rank's rows, [{r1 - r0}, {H}], contiguous")
+    g = _tp_group(buffers, rank, signals)
+    with torch.cuda.device(dev):
+        _check(library().rarn_tp_reduce_add_rms_norm(
+            ctypes.byref(g), residual.data_ptr(), gamma.data_ptr(), T, H, float(eps),
+            _dtype_code(residual), _stream(dev)), "rarn_tp_reduce_add_rms_norm")
+
+
+def tp_reduce_add_rms_norm_world(buffers, residuals, gamma, eps: float, T: int, signals=None):
+    """Every rank's part in one launch on this device (all buffers, residual
+    rows and pads on it): ``residuals[q]`` is rank q's rows of the residual."""
+    import torch
+    H = gamma.numel()
+    N = len(buffers)
+    dev = gamma.device
+    if len(residuals) != N:
+        raise ValueError("one residual block per rank")
+    for q, r in enumerate(residuals):
+        r0, r1 = tp_rows(T, N, q)
+        _check_tensor(f"residuals[{q}]", r, gamma.dtype, dev)
+        if tuple(r.shape) != (r1 - r0, H):
+            raise ValueError(f"residuals[{q}] must be [{r1 - r0}, {H}]")
+    g = _tp_group(buffers, 0, signals)
+    rp = (ctypes.c_void_p * N)(*[r.data_ptr() for r in residuals])
+    with torch.cuda.device(dev):
+        _check(library().rarn_tp_reduce_add_rms_norm_world(
+            ctypes.byref(g), ctypes.cast(rp, ctypes.c_void_p), gamma.data_ptr(), T, H,
+            float(eps), _dtype_code(gamma), _stream(dev)), "rarn_tp_reduce_add_rms_norm_world")
+
+
+def ipc_export(x) -> bytes:
+    """A handle (IPC_HANDLE_BYTES bytes) through which another process can
+    address the device memory at ``x`` (a tensor or a device address)."""
+    buf = ctypes.create_string_buffer(IPC_HANDLE_BYTES)
+    _check(library().rarn_ipc_export(_addr(x), buf), "rarn_ipc_export")
+    return buf.raw
+
+
+def ipc_import(handle: bytes) -> int:
+    """The address at which this process reaches the memory another process
+    exported as ``handle``."""
+    if len(handle) != IPC_HANDLE_BYTES:
+        raise ValueError(f"an IPC handle has {IPC_HANDLE_BYTES} bytes")
+    p = ctypes.c_void_p(0)
+    _check(library().rarn_ipc_import(handle, ctypes.byref(p)), "rarn_ipc_import")
+    return int(p.value)
+
+
+def ipc_close(ptr: int) -> None:
+    """Release a mapping ipc_import opened."""
+    _check(library().rarn_ipc_close(ptr), "rarn_ipc_close")
 
 
 def set_tuning(name: str, value: int) -> None:

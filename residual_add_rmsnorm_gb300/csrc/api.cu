@@ -10,11 +10,17 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <vector>
+
+#include <cuda.h>
+
+#include <unordered_map>
 
 #include "../../include/rarn.h"
 #include "gemm_plan.h"
 #include "plan.h"
 #include "q8in.cuh"
+#include "tp.cuh"
 
 namespace rarn {
 // instantiated in q8in_{bf16,f16,f32}.cu
@@ -25,9 +31,20 @@ extern template cudaError_t launch_q8in<__half>(const q8in::Params &, const q8in
                                                 int, bool, cudaStream_t);
 extern template cudaError_t launch_q8in<float>(const q8in::Params &, const q8in::KernelChoice &,
                                                int, bool, cudaStream_t);
+// instantiated in tp_{bf16,f16,f32}.cu
+extern template cudaError_t tp_blocks_per_sm<__nv_bfloat16>(int64_t, int *);
+extern template cudaError_t tp_blocks_per_sm<__half>(int64_t, int *);
+extern template cudaError_t tp_blocks_per_sm<float>(int64_t, int *);
+extern template cudaError_t launch_tp<__nv_bfloat16>(const tp::Params &, int, bool, bool,
+                                                    cudaStream_t);
+extern template cudaError_t launch_tp<__half>(const tp::Params &, int, bool, bool, cudaStream_t);
+extern template cudaError_t launch_tp<float>(const tp::Params &, int, bool, bool, cudaStream_t);
 }  // namespace rarn
 
 using namespace rarn;
+
+static_assert(RARN_TP_MAX_RANKS == tp::kMaxRanks, "rank limit");
+static_assert(RARN_TP_SIGNAL_BYTES == tp::kMaxCtas * tp::kMaxRanks * 4, "signal pad size");
 
 // Watchdog word: kernels with bounded waits record a timeout here.
 __device__ unsigned int g_rarn_watchdog = 0;
@@ -193,8 +210,13 @@ Plan plan_rows(int op, int64_t T, int64_t H, int s, bool vec, int num_sms, int r
     const int max_pt = vec ? 8 : 16;
     // a binary32 residual doubles the registers per pack of a reduce row:
     // spread it over twice the threads (measured: 293 vs 366 us at R = 8,
-    // [8192, 8192])
-    const int target = (op == OP_REDUCE && rn == 2) ? 512 : 256;
+    // [8192, 8192]); plain / fused rows with at most one CTA per SM (one
+    // latency-bound wave) over up to 1024 threads, so each thread issues
+    // fewer loads before the row reduction (measured, fused bf16, us:
+    // [1, 5120] 2.25 -> 1.97, [128, 5120] 2.91 -> 2.45, [64, 16384] 3.72 ->
+    // 3.56)
+    const int target = (op == OP_REDUCE && rn == 2) ? 512
+                       : (op != OP_REDUCE && T <= num_sms) ? 1024 : 256;
     int pt = std::min(max_pt, pow2_at_least(ceil_div(n, target)));
     if (const long long f = g_tune[RARN_TUNE_ROWS_PER_THREAD]; f >= 1 && f <= max_pt) pt = (int)f;
     while (pt < max_pt && ceil_div(n, pt) > max_block(pt, false)) pt <<= 1;
@@ -1256,6 +1278,207 @@ int rarn_host_access(void) {
                                dev) != cudaSuccess)
         return -1;
     return pageable ? 2 : (mapped ? 1 : 0);
+}
+
+
+// ---------------------------------------------------------------------------
+// Tensor-parallel form
+// ---------------------------------------------------------------------------
+
+rarn_status rarn_tp_rows(int64_t T, int32_t world_size, int32_t rank, int64_t *r0, int64_t *r1) {
+    if (T < 0 || world_size < 1 || rank < 0 || rank >= world_size || !r0 || !r1)
+        return RARN_ERR_INVALID_ARG;
+    tp::rows_of(T, world_size, rank, *r0, *r1);
+    return RARN_OK;
+}
+
+// Checks of a tensor-parallel call (every rank's in the world launch, else
+// group->rank's): before any CUDA call.
+static rarn_status tp_check(const rarn_tp_group *g, void *const *residuals, const void *gamma,
+                            int64_t T, int64_t H, float eps, rarn_dtype dt, bool world) {
+    if (!g || g->world_size < 1 || g->world_size > RARN_TP_MAX_RANKS) return RARN_ERR_INVALID_ARG;
+    const int N = g->world_size;
+    if (!world && (g->rank < 0 || g->rank >= N)) return RARN_ERR_INVALID_ARG;
+    if (!dtype_ok(dt) || T < 0 || H <= 0 || !(eps >= 0.f) || std::isinf(eps))
+        return RARN_ERR_INVALID_ARG;
+    if (T == 0) return RARN_OK;
+    const int nsig = (int)std::count_if(g->signals, g->signals + N, [](uint32_t *s) { return s; });
+    if (nsig != 0 && nsig != N) return RARN_ERR_INVALID_ARG;
+    if (!gamma) return RARN_ERR_INVALID_ARG;
+    // the residual of every rank this call runs that owns rows
+    bool has_res[RARN_TP_MAX_RANKS] = {};
+    for (int q = 0; q < N; ++q) {
+        int64_t r0, r1;
+        tp::rows_of(T, N, q, r0, r1);
+        has_res[q] = (world || q == g->rank) && r1 > r0;
+        if (!g->buffers[q]) return RARN_ERR_INVALID_ARG;
+        if (has_res[q] && !residuals[q]) return RARN_ERR_INVALID_ARG;
+    }
+    const int s = elem_size(dt);
+    if ((H * s) % 16 || H * s / 16 > tp::kMaxPacks) return RARN_ERR_UNSUPPORTED;
+    if (!aligned16(gamma)) return RARN_ERR_UNSUPPORTED;
+    for (int q = 0; q < N; ++q) {
+        if (!aligned16(g->buffers[q])) return RARN_ERR_UNSUPPORTED;
+        if (nsig && (reinterpret_cast<uintptr_t>(g->signals[q]) & 3u)) return RARN_ERR_UNSUPPORTED;
+        if (has_res[q] && !aligned16(residuals[q])) return RARN_ERR_UNSUPPORTED;
+    }
+    // buffers, residual rows, gamma and pads: no two overlap
+    const int64_t bb = T * H * s;
+    std::vector<std::pair<const void *, int64_t>> spans;
+    for (int q = 0; q < N; ++q) {
+        spans.push_back({g->buffers[q], bb});
+        if (has_res[q]) {
+            int64_t r0, r1;
+            tp::rows_of(T, N, q, r0, r1);
+            spans.push_back({residuals[q], (r1 - r0) * H * s});
+        }
+        if (nsig) spans.push_back({g->signals[q], RARN_TP_SIGNAL_BYTES});
+    }
+    spans.push_back({gamma, H * s});
+    for (size_t i = 0; i < spans.size(); ++i)
+        for (size_t j = i + 1; j < spans.size(); ++j)
+            if (overlaps(spans[i].first, spans[i].second, spans[j].first, spans[j].second))
+                return RARN_ERR_ALIAS;
+    return RARN_OK;
+}
+
+static rarn_status tp_run(const rarn_tp_group *g, void *const *residuals, const void *gamma,
+                          int64_t T, int64_t H, float eps, rarn_dtype dt, void *stream,
+                          bool world) {
+    rarn_status st = tp_check(g, residuals, gamma, T, H, eps, dt, world);
+    if (st != RARN_OK || T == 0) return st;
+    DeviceInfo *d = nullptr;
+    if ((st = device_info(&d)) != RARN_OK) return st;
+    const int N = g->world_size;
+    int per_sm = 0;
+    cudaError_t e = dt == RARN_BF16 ? tp_blocks_per_sm<__nv_bfloat16>(H, &per_sm)
+                    : dt == RARN_F16 ? tp_blocks_per_sm<__half>(H, &per_sm)
+                                     : tp_blocks_per_sm<float>(H, &per_sm);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (per_sm < 1) return RARN_ERR_UNSUPPORTED;
+    // CTAs per rank: every CTA of a rank resident at once (a CTA waits on its
+    // counterparts only), all ranks' in the one grid of the world launch; the
+    // rows of the largest block spread evenly; the same on every rank
+    const int64_t rows_max = (T + N - 1) / N;
+    int64_t slots = (int64_t)d->num_sms * per_sm / (world ? N : 1);
+    slots = std::max<int64_t>(1, std::min<int64_t>(slots, tp::kMaxCtas));
+    const int64_t rounds = ceil_div(rows_max, slots);
+    const int ctas = (int)std::max<int64_t>(1, ceil_div(rows_max, rounds));
+    tp::Params p{};
+    const bool sync = g->signals[0] != nullptr;
+    for (int q = 0; q < N; ++q) {
+        p.bufs[q] = g->buffers[q];
+        p.signals[q] = sync ? g->signals[q] : nullptr;
+        p.residual[q] = (world || q == g->rank) ? residuals[q] : nullptr;
+    }
+    p.gamma = gamma;
+    p.T = T;
+    p.H = H;
+    p.N = N;
+    p.rank = world ? -1 : g->rank;
+    p.ctas = ctas;
+    p.eps = eps;
+    p.watchdog = d->watchdog;
+    p.wait_limit_ns = tp::kWaitLimitNs;
+    p.stall_rank = -1;
+    if (sync) {
+        const long long f = g_stall_fill.exchange(-1);
+        if (f >= 0) {
+            p.stall_rank = (int)(f % N);
+            p.wait_limit_ns = g_stall_limit_ns.load();
+        }
+    }
+    const int grid = world ? ctas * N : ctas;
+    const bool coop = world && sync;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const bool pdl = g_pdl.load() != 0;
+    e = dt == RARN_BF16 ? launch_tp<__nv_bfloat16>(p, grid, coop, pdl, cs)
+        : dt == RARN_F16 ? launch_tp<__half>(p, grid, coop, pdl, cs)
+                         : launch_tp<float>(p, grid, coop, pdl, cs);
+    if (e != cudaSuccess) return cuda_fail(e);
+    return RARN_OK;
+}
+
+rarn_status rarn_tp_reduce_add_rms_norm(const rarn_tp_group *group, void *residual,
+                                        const void *gamma, int64_t T, int64_t H, float eps,
+                                        rarn_dtype dt, void *stream) {
+    void *res[RARN_TP_MAX_RANKS] = {};
+    if (group && group->rank >= 0 && group->rank < RARN_TP_MAX_RANKS) res[group->rank] = residual;
+    return tp_run(group, res, gamma, T, H, eps, dt, stream, false);
+}
+
+rarn_status rarn_tp_reduce_add_rms_norm_world(const rarn_tp_group *group, void *const *residuals,
+                                              const void *gamma, int64_t T, int64_t H, float eps,
+                                              rarn_dtype dt, void *stream) {
+    if (!residuals) return RARN_ERR_INVALID_ARG;
+    return tp_run(group, residuals, gamma, T, H, eps, dt, stream, true);
+}
+
+// IPC handles: a magic word, the CUDA handle of the allocation holding the
+// pointer, and the pointer's offset in it.
+namespace {
+constexpr uint64_t kIpcMagic = 0x52524e4950433031ull;  // "RRNIPC01"
+struct IpcHandle {
+    uint64_t magic;
+    cudaIpcMemHandle_t mem;
+    uint64_t offset;
+};
+static_assert(sizeof(IpcHandle) <= RARN_IPC_HANDLE_BYTES, "handle size");
+std::mutex g_ipc_mu;
+std::unordered_map<uintptr_t, void *> g_ipc_open;  // returned pointer -> mapping base
+
+using AddressRangeFn = CUresult (*)(CUdeviceptr *, size_t *, CUdeviceptr);
+}  // namespace
+
+rarn_status rarn_ipc_export(const void *ptr, void *handle) {
+    if (!ptr || !handle) return RARN_ERR_INVALID_ARG;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (!fn || q != cudaDriverEntryPointSuccess) return cuda_fail(cudaErrorNotSupported);
+    CUdeviceptr base = 0;
+    size_t size = 0;
+    if (reinterpret_cast<AddressRangeFn>(fn)(&base, &size, reinterpret_cast<CUdeviceptr>(ptr)) !=
+        CUDA_SUCCESS)
+        return RARN_ERR_INVALID_ARG;  // not device memory of this context
+    IpcHandle h{};
+    h.magic = kIpcMagic;
+    h.offset = reinterpret_cast<uintptr_t>(ptr) - (uintptr_t)base;
+    if ((e = cudaIpcGetMemHandle(&h.mem, reinterpret_cast<void *>(base))) != cudaSuccess)
+        return cuda_fail(e);
+    memset(handle, 0, RARN_IPC_HANDLE_BYTES);
+    memcpy(handle, &h, sizeof(h));
+    return RARN_OK;
+}
+
+rarn_status rarn_ipc_import(const void *handle, void **ptr) {
+    if (!handle || !ptr) return RARN_ERR_INVALID_ARG;
+    IpcHandle h;
+    memcpy(&h, handle, sizeof(h));
+    if (h.magic != kIpcMagic) return RARN_ERR_INVALID_ARG;
+    void *base = nullptr;
+    const cudaError_t e = cudaIpcOpenMemHandle(&base, h.mem, cudaIpcMemLazyEnablePeerAccess);
+    if (e != cudaSuccess) return cuda_fail(e);
+    *ptr = static_cast<char *>(base) + h.offset;
+    std::lock_guard<std::mutex> lock(g_ipc_mu);
+    g_ipc_open[reinterpret_cast<uintptr_t>(*ptr)] = base;
+    return RARN_OK;
+}
+
+rarn_status rarn_ipc_close(void *ptr) {
+    if (!ptr) return RARN_ERR_INVALID_ARG;
+    void *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_ipc_mu);
+        auto it = g_ipc_open.find(reinterpret_cast<uintptr_t>(ptr));
+        if (it == g_ipc_open.end()) return RARN_ERR_INVALID_ARG;
+        base = it->second;
+        g_ipc_open.erase(it);
+    }
+    const cudaError_t e = cudaIpcCloseMemHandle(base);
+    return e == cudaSuccess ? RARN_OK : cuda_fail(e);
 }
 
 rarn_status rarn_launch_floor(const void *rows, int64_t row_bytes, int32_t grid, int32_t block,

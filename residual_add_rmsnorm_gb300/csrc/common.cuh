@@ -183,11 +183,14 @@ struct DT<__nv_bfloat16> {
 // Global memory access with cache hints (inline PTX)
 // ---------------------------------------------------------------------------
 
-// Streaming load: data read once (x, partials, residual).  Coherent, so it is
-// also correct for buffers this kernel writes (residual, y aliasing x).
+// Load of data read once (x, partials, residual): a plain weak load, which
+// sees this thread's own earlier stores and everything the kernels before the
+// dependency wait wrote (residual, y aliasing x).  Measured against the
+// evict-first (.cs) form, CUDA-graph timing, cold L2: fused bf16 [4096, 4096]
+// 20.94 -> 20.75 us, [32768, 5120] 201.7 -> 200.8 us.
 __device__ __forceinline__ uint4 ld_stream(const void *p) {
     uint4 v;
-    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
                  : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                  : "l"(p));
     return v;

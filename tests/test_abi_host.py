@@ -173,10 +173,16 @@ def test_plan_auto_policy():
     assert p.startswith("stream") and "groups=2" in p, p
     # few rows: never the persistent kernel
     assert _plan("reduce_add_rms_norm", 64, 8192, 8, "bf16").startswith("rows")
-    # 32 KB rows, few of them: one CTA per row still holds the row (8 packs
-    # per thread); 64 KB rows need a cluster per row
+    # 32 KB rows, few of them: one CTA per row still holds the row (one row
+    # per SM at most: as many threads as the register budget allows, 512 of 4
+    # packs); 64 KB rows need a cluster per row
     p = _plan("fused_add_rms_norm", 64, 16384, 1, "bf16")
-    assert p.startswith("rows.cta") and "per_thread=8" in p, p
+    assert p.startswith("rows.cta") and "per_thread=4 block=512" in p, p
+    # one wave of rows: up to 1024 threads per row; more rows than SMs: 256
+    assert "per_thread=1 block=640" in _plan("fused_add_rms_norm", 128, 5120, 1, "bf16")
+    assert "per_thread=1 block=1024" in _plan("rms_norm", 152, 8192, 0, "bf16")
+    assert "per_thread=4 block=160" in _plan("fused_add_rms_norm", 153, 5120, 1, "bf16")
+    assert "per_thread=2 block=256" in _plan("reduce_add_rms_norm", 64, 4096, 8, "bf16")
     p = _plan("fused_add_rms_norm", 64, 32768, 1, "bf16")
     assert p.startswith("cluster"), p
     # a single wave keeps gamma in registers; many rounds read it from L1
