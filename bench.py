@@ -53,7 +53,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE,
-                    choices=[w.name for w in _configs()] + [FP8IN_NAME],
+                    choices=[w.name for w in _configs()] + [FP8IN_NAME, TP_NAME],
                     help="the timed configuration; a widened workload (row strides, fp32 "
                          "residual, 8-bit output or partials) has no host-buffer (e2e) or CPU "
                          "leg")
@@ -700,6 +700,51 @@ def time_gemm(gw, device, rarn, sampler=None, hold_s=0.0):
 
 
 FP8IN_NAME = "reduce8_e4m3in_bf16_T8192_H8192"
+TP_NAME = "tp8_world_bf16_T8192_H8192"
+
+
+def tp_tensors(device, N=8, T=8192, H=8192):
+    """The tensor-parallel form over N ranks' buffers held on this one GPU
+    (the reduce configuration's shape): N partials N(0, 1/N) bf16, the
+    residual N(0, 1) split into the ranks' row blocks, gamma U(0.5, 1.5),
+    zeroed signal pads; and the algorithmic bytes of one call (every rank's
+    row block read from every buffer, the residual read and written, y
+    written into every buffer, gamma)."""
+    import torch
+
+    import residual_add_rmsnorm_gb300 as rarn
+    gen = torch.Generator(device=device).manual_seed(0)
+    bufs = [(torch.randn(T, H, device=device, generator=gen) / N ** 0.5).to(torch.bfloat16)
+            for _ in range(N)]
+    res = []
+    for q in range(N):
+        r0, r1 = rarn.tp_rows(T, N, q)
+        res.append(torch.randn(r1 - r0, H, device=device, generator=gen).to(torch.bfloat16))
+    g = (torch.rand(H, device=device, generator=gen) + 0.5).to(torch.bfloat16)
+    pads = [torch.zeros(rarn.TP_SIGNAL_BYTES // 4, dtype=torch.int32, device=device)
+            for _ in range(N)]
+    alg = (N * T * H + 2 * T * H + N * T * H) * 2 + H * 2
+    return bufs, res, g, pads, alg
+
+
+def time_tp(device, rarn, N=8, T=8192, H=8192, sampler=None, hold_s=0.0):
+    """Every rank's part in one launch with the signal-pad barrier: the
+    data path and the synchronisation on this GPU's memory (no NVLink
+    traffic: an emulation of N GPUs, not a multi-GPU measurement)."""
+    import torch
+    bufs, res, g, pads, alg = tp_tensors(device, N, T, H)
+    us = _graph_us(lambda: rarn.tp_reduce_add_rms_norm_world(bufs, res, g, 1e-6, T,
+                                                             signals=pads),
+                   sampler=sampler, phase=TP_NAME, hold_s=hold_s)
+    peak, _ = measured_hbm_peak()
+    gbs = alg / (us / 1e6) / 1e9
+    del bufs, res, pads
+    torch.cuda.empty_cache()
+    return {"kind": "widened (tensor-parallel, N ranks' buffers on one GPU)",
+            "us_per_launch": us, "gbs": gbs, "rows_per_s": T / (us / 1e6),
+            "frac_of_peak": gbs / peak, "algorithmic_bytes": alg, "ranks": N,
+            "timing": "CUDA graph of 10 launches, best of 3 (inputs larger than L2)",
+            "plan": f"tp.world ranks={N} barrier=signal pads"}
 
 
 def fp8in_tensors(device, R=8, T=8192, H=8192):
@@ -783,6 +828,47 @@ def main_fp8in(args, device, rank, world):
         "cpu_baseline": None,
         "e2e": {"value": None, "unit": "GB/s",
                 "note": "no host-buffer entry point for the 8-bit-partials form"},
+        "clocks": clocks, "gpu_launches": args.steps, "watchdog": rarn.watchdog(clear=True),
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main_tp(args, device, rank, world):
+    """The tensor-parallel form as the timed step: eight ranks' buffers on
+    this GPU, every rank's part in one launch with the barrier (one launch
+    per step; inputs resident in HBM, larger than L2).  No host-buffer entry
+    point and no oracle leg for this form."""
+    import torch
+
+    import residual_add_rmsnorm_gb300 as rarn
+    N, T, H = 8, 8192, 8192
+    bufs, res, g, pads, alg = tp_tensors(device, N, T, H)
+    call = lambda: rarn.tp_reduce_add_rms_norm_world(bufs, res, g, 1e-6, T, signals=pads)
+    stream = torch.cuda.current_stream(device)
+    sampler = ClockSampler(nvsmi_id(torch.cuda.get_device_properties(device), device.index or 0))
+    sampler.wait_ready()
+    ms = time_steps(call, args.steps, args.warmup, stream, sampler, args.clock_window)
+    clocks = line_clocks(sampler.stop(), args.clock_window)
+    ms = max_over_ranks(ms, device)
+    peak, kind = measured_hbm_peak()
+    gbs = world * alg * args.steps / (ms / 1e3) / 1e9
+    if rank != 0:
+        return
+    line = {
+        "metric": "achieved HBM GB/s (algorithmic bytes / time)", "value": gbs, "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": TP_NAME, "ranks": N, "T": T, "H": H, "storage": "bf16",
+                   "plan": f"tp.world ranks={N} barrier=signal pads",
+                   "l2": "inputs larger than L2 (1.2 GB)", "pdl": not args.no_pdl,
+                   "note": "the N ranks' buffers are on this one GPU: no NVLink traffic"},
+        "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peak, "unit": "GB/s",
+                     "frac": gbs / world / peak, "traffic": ncu_traffic(TP_NAME, "tp.world"),
+                     "peak_source": kind},
+        "cpu_baseline": None,
+        "e2e": {"value": None, "unit": "GB/s",
+                "note": "no host-buffer entry point for the tensor-parallel form"},
         "clocks": clocks, "gpu_launches": args.steps, "watchdog": rarn.watchdog(clear=True),
     }
     print(json.dumps(line), flush=True)
@@ -885,6 +971,9 @@ def main():
     if args.workload == FP8IN_NAME:
         main_fp8in(args, device, rank, world)
         return
+    if args.workload == TP_NAME:
+        main_tp(args, device, rank, world)
+        return
     w = W.BY_NAME[args.workload]
     data = W.generate(w)
     tensors = device_tensors(w, data, device)
@@ -944,6 +1033,7 @@ def main():
         for gw in W.GEMM_CONFIGS:
             per_config[gw.name] = time_gemm(gw, device, rarn, sampler=sampler, hold_s=hold)
         per_config[FP8IN_NAME] = time_fp8in(device, rarn, sampler=sampler, hold_s=hold)
+        per_config[TP_NAME] = time_tp(device, rarn, sampler=sampler, hold_s=hold)
         if rarn.watchdog(clear=True):
             watchdog = 1
     phases = sampler.stop()

@@ -392,6 +392,10 @@ __device__ __forceinline__ void dequant8(uint2 c, float s, float (&v)[8]) {
 // Consumer warps of the TMA-fed kernel (16 measured faster than 8: R = 8,
 // [8192, 8192] bf16 157 vs 173 us; R = 4, [16384, 4096] 133 vs 161 us).
 constexpr int kStreamWarps = 16;
+// Units of 8 elements per row the TMA-fed kernel takes (H <= 16384; binary32
+// storage H <= 8192).
+template <typename T>
+constexpr int max_units() { return sizeof(T) == 4 ? 1024 : 2048; }
 
 // Shared-memory layout: `stages` stages, each R code chunks (8 bytes per
 // 8-element unit) and one residual chunk (8 elements of T per unit); the
@@ -509,6 +513,17 @@ __global__ void __launch_bounds__(32 + 32 * kStreamWarps, 1) k_q8in_stream(Param
     Pack8<T> *row_copy = reinterpret_cast<Pack8<T> *>(smem + L.row_off);
     const T *gamma = reinterpret_cast<const T *>(p.gamma);
     T *residual = reinterpret_cast<T *>(p.residual);
+    // the partials' scales and this thread's gamma units in registers, read
+    // once (they were global loads inside the unit loops: long-scoreboard
+    // stalls under ncu)
+    float scale[RMAX];
+#pragma unroll
+    for (int r = 0; r < RMAX; ++r) scale[r] = r < p.R ? __ldg(p.scales + r) : 0.f;
+    constexpr int GU = max_units<T>() / kConsumers;  // gamma units per thread
+    Pack8<T> gk[GU];
+#pragma unroll
+    for (int k = 0; k < GU; ++k)
+        if (j + k * kConsumers < nu) gk[k].load_keep(gamma + 8 * (int64_t)(j + k * kConsumers));
     int stage = 0;
     uint32_t phase = 0;
     int par = 0;
@@ -531,7 +546,7 @@ __global__ void __launch_bounds__(32 + 32 * kStreamWarps, 1) k_q8in_stream(Param
                         const uint2 code =
                             *reinterpret_cast<const uint2 *>(sbase + r * L.code_chunk + q * 8);
                         float v[8];
-                        dequant8<FMT>(code, __ldg(p.scales + r), v);
+                        dequant8<FMT>(code, scale[r], v);
                         // product and sum rounded separately (__fmul_rn /
                         // __fadd_rn are never contracted into one FMA)
 #pragma unroll
@@ -569,12 +584,13 @@ __global__ void __launch_bounds__(32 + 32 * kStreamWarps, 1) k_q8in_stream(Param
         const float inv = rsqrtf(tot / (float)p.H + p.eps);
         if (*abort_flag) continue;
         T *y = reinterpret_cast<T *>(p.y) + t * p.H;
-        for (int u = j; u < nu; u += kConsumers) {
+#pragma unroll
+        for (int k = 0; k < GU; ++k) {
+            const int u = j + k * kConsumers;
+            if (u >= nu) break;
             float h[8], w[8];
             row_copy[u].unpack(h);
-            Pack8<T> gp;
-            gp.load_keep(gamma + 8 * (int64_t)u);
-            gp.unpack(w);
+            gk[k].unpack(w);
 #pragma unroll
             for (int e = 0; e < 8; ++e) h[e] = (h[e] * inv) * w[e];
             Pack8<T> o;
