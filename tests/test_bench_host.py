@@ -20,7 +20,7 @@ def bench():
 def test_traffic_table_well_formed(bench):
     with open(bench.TRAFFIC_FILE) as f:
         data = json.load(f)
-    names = {w.name for w in bench._configs()} | {bench.FP8IN_NAME}
+    names = {w.name for w in bench._configs()} | {bench.FP8IN_NAME, bench.TP_NAME}
     csrc = os.path.join(ROOT, "residual_add_rmsnorm_gb300", "csrc")
     for e in data["entries"]:
         assert e["workload"] in names, e["workload"]
