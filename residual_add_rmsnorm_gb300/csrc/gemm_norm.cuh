@@ -443,10 +443,12 @@ struct EpiRow {
         }
     }
 
-    // The sum of squares is formed per 64 columns and those sums added in
-    // column order, so a 128-column slot has the same bits whether one
-    // thread or two warp halves (64 columns each) computed it.
-    __device__ __forceinline__ float run(uint32_t taddr, T *res, bool live) {
+    // h = RN(accumulator + residual) into rv, and the row's sum of squares
+    // of h.  The sum of squares is formed per 64 columns and those sums
+    // added in column order, so a 128-column slot has the same bits whether
+    // one thread or two warp halves (64 columns each) computed it.  h is
+    // stored by store_h, once the accumulator is released.
+    __device__ __forceinline__ float run(uint32_t taddr, bool live) {
         static_assert(NC % 64 == 0, "64-column partial sums");
         float ss = 0.f, part = 0.f;
 #pragma unroll
@@ -475,12 +477,7 @@ struct EpiRow {
                             rv[c / 16 + q / 2].a = DT<T>::pack(f);
                     } else {
                         rv[c / 8 + q] = DT<T>::pack(f);
-                        st_global(res + c + 8 * q, rv[c / 8 + q]);
                     }
-                }
-                if constexpr (Wide) {
-                    st_global32(res + c, rv[c / 16].a, rv[c / 16].b);
-                    st_global32(res + c + 16, rv[c / 16 + 1].a, rv[c / 16 + 1].b);
                 }
             }
             if (c % 64 == 32) {
@@ -489,6 +486,17 @@ struct EpiRow {
             }
         }
         return ss;
+    }
+
+    // After run(): h back into the residual's row.
+    __device__ __forceinline__ void store_h(T *res) const {
+#pragma unroll
+        for (int q = 0; q < kPacks; ++q) {
+            if constexpr (Wide)
+                st_global32(res + 16 * q, rv[q].a, rv[q].b);
+            else
+                st_global(res + 8 * q, rv[q]);
+        }
     }
 
     // After run(): y = RN((h * inv) * gamma) for the same columns.
@@ -889,9 +897,11 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (tile + gridDim.x >= ntiles) grid_launch_dependents();
             const uint32_t taddr =
                 tmem + (static_cast<uint32_t>(quarter * 32) << 16) + acc * NS + c0;
-            const float ss = er.run(taddr, res, live);
+            const float ss = er.run(taddr, live);
             tmem_fence_before();
             mbar_arrive(smem_u32(&tempty[acc]));  // the accumulator is free again
+            // h stored only now, off the accumulator's critical path
+            if (live) er.store_h(res);
             // each warp half's 128 columns are one partial-sum slot of the row
             const int slots = 2 * C;
             if (live && !*abort_flag) p.ss[t * slots + ntile * 2 + (c0 >> 7)] = ss;
@@ -1086,10 +1096,12 @@ __device__ __forceinline__ int pair_epilogue(const Params &p, void *residual, in
     if (!*tile_ok) return 0;
     tmem_fence_after();
     if (item + npairs >= items) grid_launch_dependents();
-    const float ss = er.run(tbase + wh * NC, res, live);
+    const float ss = er.run(tbase + wh * NC, live);
     tmem_fence_before();
     // this CTA's half of the accumulator is read: tell the leader
     mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
+    // h stored only now, off the accumulator's critical path
+    if (live) er.store_h(res);
     const int slot = ntile * 2 + (c0 >> 7);
     if (NC == 128) {
         if (live && !*abort_flag) p.ss[t * slots + slot] = ss;
@@ -1133,8 +1145,10 @@ struct PairLayout {
     static constexpr int a_bytes = kBM * BK * 2;           // 16 KB: this CTA's 128 rows of A
     static constexpr int b_bytes = (kMmaN / 2) * BK * 2;   // 16 KB: its 128 columns of W
     static constexpr int stage_bytes = a_bytes + b_bytes;  // 32 KB
-    static constexpr int stages =
-        (227 * 1024 - 3 * 1024) / stage_bytes > 8 ? 8 : (227 * 1024 - 3 * 1024) / stage_bytes;
+    // 6 stages (192 KB of the 227 KB), measured faster than the 7 that fit:
+    // T = K = H = 4096 98.5 -> 96.3 us, [8192, 4096, 4096] 170.6 -> 167.5,
+    // [16384, 5120, 5120] 506 -> 499.6 (5 stages: 97.3, 168, 505.5; 4: 104.5)
+    static constexpr int stages = 6;
     static constexpr int ctl_off = stages * stage_bytes;
     // full[S], empty[S], tfull[2], tempty[2], mma_done (8 B each); tmem slot,
     // abort word, the peer's fill count, tile_ok, norm_ok; the epilogue's
