@@ -43,7 +43,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 
 def _configs():
     from residual_add_rmsnorm_gb300 import workloads as W
-    return W.CONFIGS + W.EXTENDED + W.GEMM_CONFIGS
+    return W.CONFIGS + W.EXTENDED + W.GEMM_CONFIGS + W.GEMM_WIDER
 
 
 def parse_args():
@@ -964,7 +964,7 @@ def main():
 
     rarn.set_path(args.path)
     rarn.set_pdl(not args.no_pdl)
-    gemm = {gw.name: gw for gw in W.GEMM_CONFIGS}
+    gemm = {gw.name: gw for gw in W.GEMM_CONFIGS + W.GEMM_WIDER}
     if args.workload in gemm:
         main_gemm(args, gemm[args.workload], device, rank, world)
         return
@@ -1030,7 +1030,7 @@ def main():
                 per_config[cw.name]["us_above_floor"] = None if floor is None else us - floor
             del cd
             torch.cuda.empty_cache()
-        for gw in W.GEMM_CONFIGS:
+        for gw in W.GEMM_CONFIGS + W.GEMM_WIDER:
             per_config[gw.name] = time_gemm(gw, device, rarn, sampler=sampler, hold_s=hold)
         per_config[FP8IN_NAME] = time_fp8in(device, rarn, sampler=sampler, hold_s=hold)
         per_config[TP_NAME] = time_tp(device, rarn, sampler=sampler, hold_s=hold)

@@ -140,8 +140,11 @@ __global__ void __launch_bounds__(512) k_tp_rows(Params p) {
         int par = 0;
         for (int64_t t = r0 + b; t < r1; t += p.ctas, par ^= 1) {
             // reduce-scatter: this row of every rank's buffer, in rank order,
-            // RB ranks' loads in flight at a time
-            constexpr int RB = VPT <= 2 ? 4 : 2;
+            // RB ranks' loads in flight at a time: all eight with two packs per
+            // thread (8 ranks, [8192, 8192] on one GPU: 473 -> 462 us); four
+            // with one (eight cost the second CTA per SM: [8192, 4096] 205 ->
+            // 258 us); two with four (more spill)
+            constexpr int RB = VPT == 2 ? 8 : VPT == 1 ? 4 : 2;
             float acc[VPT][EPV];
 #pragma unroll
             for (int q0 = 0; q0 < kMaxRanks; q0 += RB) {

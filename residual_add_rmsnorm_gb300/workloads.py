@@ -164,6 +164,11 @@ class GemmWorkload:
 # its partial produced by a 4096 x 4096 projection.
 GEMM_CONFIGS = [GemmWorkload("gemm_fused_bf16_T4096_K4096_H4096", "bf16", 4096, 4096, 4096, 1e-6)]
 
+# Wider GEMM-producer shapes, timed beside it: twice the tokens, and a
+# [16384 tokens, 5120] projection (C5's row length).
+GEMM_WIDER = [GemmWorkload("gemm_fused_bf16_T8192_K4096_H4096", "bf16", 8192, 4096, 4096, 1e-6),
+              GemmWorkload("gemm_fused_bf16_T16384_K5120_H5120", "bf16", 16384, 5120, 5120, 1e-6)]
+
 
 def generate_gemm(w: GemmWorkload, rows: tuple[int, int] | None = None) -> dict:
     """Inputs of a GEMM workload as storage bits: 'a' [T', K], 'w' [H, K],
