@@ -1140,15 +1140,20 @@ __device__ __forceinline__ int pair_epilogue(const Params &p, void *residual, in
     return 1;
 }
 
-template <int BK = 64>
+// AT: K slabs of BK elements per ring stage (each a 128-byte-swizzled atom of
+// the operand, the next atom 16 KB further on).
+template <int BK = 64, int AT = 1>
 struct PairLayout {
-    static constexpr int a_bytes = kBM * BK * 2;           // 16 KB: this CTA's 128 rows of A
-    static constexpr int b_bytes = (kMmaN / 2) * BK * 2;   // 16 KB: its 128 columns of W
-    static constexpr int stage_bytes = a_bytes + b_bytes;  // 32 KB
-    // 6 stages (192 KB of the 227 KB), measured faster than the 7 that fit:
-    // T = K = H = 4096 98.5 -> 96.3 us, [8192, 4096, 4096] 170.6 -> 167.5,
-    // [16384, 5120, 5120] 506 -> 499.6 (5 stages: 97.3, 168, 505.5; 4: 104.5)
-    static constexpr int stages = 6;
+    static constexpr int atom_a = kBM * BK * 2;            // 16 KB: this CTA's 128 rows of A
+    static constexpr int atom_b = (kMmaN / 2) * BK * 2;    // 16 KB: its 128 columns of W
+    static constexpr int a_bytes = AT * atom_a;
+    static constexpr int b_bytes = AT * atom_b;
+    static constexpr int stage_bytes = a_bytes + b_bytes;  // AT x 32 KB
+    // 192 KB of the 227 KB: with one K slab per stage, 6 stages measured
+    // faster than the 7 that fit (T = K = H = 4096 98.5 -> 96.3 us,
+    // [8192, 4096, 4096] 170.6 -> 167.5, [16384, 5120, 5120] 506 -> 499.6;
+    // 5 stages: 97.3, 168, 505.5; 4: 104.5); with AT slabs, 6 / AT stages
+    static constexpr int stages = 6 / AT;
     static constexpr int ctl_off = stages * stage_bytes;
     // full[S], empty[S], tfull[2], tempty[2], mma_done (8 B each); tmem slot,
     // abort word, the peer's fill count, tile_ok, norm_ok; the epilogue's
@@ -1159,14 +1164,14 @@ struct PairLayout {
     static_assert(total <= 227 * 1024, "one CTA per SM");
 };
 
-template <typename T, int BK, bool Wide>
+template <typename T, int BK, bool Wide, int AT = 1>
 __global__ void __launch_bounds__(kWsThreads, 1)
     k_gemm_res_pair(const __grid_constant__ CUtensorMap map_a,
                     const __grid_constant__ CUtensorMap map_w,
                     const __grid_constant__ CUtensorMap map_w_half, void *residual, int64_t ldr,
                     Params p) {
     static_assert(BK == 64, "K slab of 128 bytes");
-    using Lay = PairLayout<BK>;
+    using Lay = PairLayout<BK, AT>;
     constexpr int S = Lay::stages;
     constexpr int NS = kMmaN;  // columns of a tile
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1190,7 +1195,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     const int C = p.C;
     const int64_t items = p.items;
     const int64_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
-    const int KB = p.kblocks;
+    const int KB = (p.kblocks + AT - 1) / AT;  // ring fills per item
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -1237,7 +1242,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 // this CTA's W rows: its half of the item's columns
                 const int n0 = (int)((pi.tile % C) * NS + pi.col0 + rank * (pi.ncols / 2));
                 const CUtensorMap *mw = pi.ncols == NS ? &map_w : &map_w_half;
-                const uint32_t bytes = 2 * (Lay::a_bytes + pi.ncols / 2 * BK * 2);
+                const uint32_t bytes = 2 * AT * (Lay::atom_a + pi.ncols / 2 * BK * 2);
                 for (int kb = 0; kb < KB; ++kb, ++kit) {
                     if (kit >= S && !wait_phase(empty0 + 8 * s, ph ^ 1u, abort_flag, p.watchdog,
                                                 p.wait_limit_ns)) {
@@ -1249,8 +1254,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                             full0 + 8 * s, bytes + (blockIdx.x == 0 && kit == p.stall_fill ? 16u : 0u));
                     const uint32_t lead_fb = lead_full0 + 8 * s;
                     const uint32_t sa = ring0 + s * Lay::stage_bytes;
-                    tma_load_2d_pair(sa, &map_a, kb * BK, m0, lead_fb, pol);
-                    tma_load_2d_pair(sa + Lay::a_bytes, mw, kb * BK, n0, lead_fb, pol);
+#pragma unroll
+                    for (int at = 0; at < AT; ++at) {  // K slabs past K read as zeros
+                        const int kx = (kb * AT + at) * BK;
+                        tma_load_2d_pair(sa + at * Lay::atom_a, &map_a, kx, m0, lead_fb, pol);
+                        tma_load_2d_pair(sa + Lay::a_bytes + at * Lay::atom_b, mw, kx, n0,
+                                         lead_fb, pol);
+                    }
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
@@ -1291,6 +1301,14 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 #pragma unroll
                     for (int kk = 1; kk < BK / kMmaK; ++kk)
                         mma_f16_pair(d, ad + 2 * kk, bd + 2 * kk, idesc, 1u);
+#pragma unroll
+                    for (int at = 1; at < AT; ++at) {
+                        const uint64_t aa = ad + (at * Lay::atom_a >> 4);
+                        const uint64_t ba = bd + (at * Lay::atom_b >> 4);
+#pragma unroll
+                        for (int kk = 0; kk < BK / kMmaK; ++kk)
+                            mma_f16_pair(d, aa + 2 * kk, ba + 2 * kk, idesc, 1u);
+                    }
                     mma_commit_pair(empty0 + 8 * s, 3);  // frees the stage in both CTAs
                     if (++s == S) {
                         s = 0;
@@ -1343,7 +1361,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             if (k >= kit) {
                 // the item of fill k: this pair's (k / KB)-th
                 const PairItem pi = pair_item(pair + (k / KB) * npairs, p.full_items);
-                mbar_arrive_expect_tx(smem_u32(&full[s]), Lay::a_bytes + pi.ncols / 2 * BK * 2);
+                mbar_arrive_expect_tx(smem_u32(&full[s]), AT * (Lay::atom_a + pi.ncols / 2 * BK * 2));
             }
             wait_phase(smem_u32(&full[s]), (uint32_t)((k / S) & 1), abort_flag, p.watchdog,
                        p.wait_limit_ns, true);

@@ -13,6 +13,12 @@
 
 namespace rarn {
 
+// K slabs (of 64 elements) per ring stage of the pair kernel: two (three
+// 64 KB stages, eight MMAs per stage and per handshake) measured faster than
+// one (six 32 KB stages): T = K = H = 4096 98.4 -> 96.6 us, [8192, 4096,
+// 4096] 171.6 -> 168.4, [16384, 5120, 5120] 502.9 -> 496.5.
+constexpr int kPairSlabsPerStage = 2;
+
 inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -56,8 +62,8 @@ static int pair_clusters(int num_sms) {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kDevs) return num_sms / 2;
     int n = cache[dev].load();
     if (n > 0) return n;
-    auto kernel = gemm::k_gemm_res_pair<T, 64, false>;
-    constexpr int smem = gemm::PairLayout<64>::total;
+    auto kernel = gemm::k_gemm_res_pair<T, 64, false, kPairSlabsPerStage>;
+    constexpr int smem = gemm::PairLayout<64, kPairSlabsPerStage>::total;
     n = num_sms / 2;
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
         cudaSuccess) {
@@ -144,8 +150,9 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
                 !encode_map(&mw4, c.w, c.H, c.K, c.ldw, kMmaN / 4, BK, bf16))
                 return cudaErrorInvalidValue;
             const int64_t grid = 2 * ps.walkers;
-            auto kernel = wide ? k_gemm_res_pair<T, BK, true> : k_gemm_res_pair<T, BK, false>;
-            constexpr int smem = PairLayout<BK>::total;
+            auto kernel = wide ? k_gemm_res_pair<T, BK, true, kPairSlabsPerStage>
+                               : k_gemm_res_pair<T, BK, false, kPairSlabsPerStage>;
+            constexpr int smem = PairLayout<BK, kPairSlabsPerStage>::total;
             e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e == cudaSuccess)
                 e = launch_kernel(kernel, dim3(static_cast<unsigned>(grid)), dim3(kWsThreads),

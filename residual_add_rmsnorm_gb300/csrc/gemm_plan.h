@@ -165,11 +165,11 @@ inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
         // 106.2 against 96.6
         g.pair = pair_override == 1 || (pair_override != 0 && T >= 2048);
         if (g.pair) {
-            // the pair kernel's ring: 6 stages of 32 KB (measured faster
-            // than the 7 that fit; gemm_norm.cuh PairLayout)
+            // the pair kernel's ring: 3 stages of two K slabs, 64 KB each
+            // (gemm_norm.cuh PairLayout, gemm_norm_launch.cuh)
             const int half = (128 + g.ns / 2) * g.bk * 2;
-            g.stages = 6;
-            g.smem = g.stages * half + 3 * 1024;
+            g.stages = 3;
+            g.smem = g.stages * 2 * half + 3 * 1024;
             g.grid = 2 * std::min<int64_t>(((T + 255) / 256) * g.tiles_n, num_sms / 2);
         }
         if (g.pair) {
