@@ -436,7 +436,10 @@ rarn_status rarn_plan_fp8in(int64_t T, int64_t H, int32_t R, rarn_dtype dt, int 
  * partial is complete and order any use of the buffer after every rank's
  * call has completed (e.g. host barriers around the call).  Every rank must
  * make the call with the same T, H, dt and signal setting on the same GPU
- * model (CTA b pairs with CTA b).
+ * model (CTA b pairs with CTA b).  With signal pads the ranks must run on
+ * different GPUs: a per-rank call whose other ranks' buffers are memory of
+ * the current device returns RARN_ERR_UNSUPPORTED (on one GPU, use the world
+ * launch, whose ranks share one cooperative grid).
  *
  * Errors: a NULL group, world_size outside 1 .. RARN_TP_MAX_RANKS, rank
  * outside 0 .. N-1, a NULL buffer or gamma with T > 0, a NULL residual for a

@@ -1350,6 +1350,23 @@ static rarn_status tp_run(const rarn_tp_group *g, void *const *residuals, const 
     DeviceInfo *d = nullptr;
     if ((st = device_info(&d)) != RARN_OK) return st;
     const int N = g->world_size;
+    if (!world && g->signals[0]) {
+        // ranks that meet in the barrier run on different GPUs: two ranks'
+        // launches on one GPU that wait on each other may never run at the
+        // same time (the world launch is the one-GPU form)
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        for (int q = 0; q < N; ++q) {
+            if (q == g->rank) continue;
+            cudaPointerAttributes a{};
+            if (cudaPointerGetAttributes(&a, g->buffers[q]) != cudaSuccess) {
+                cudaGetLastError();  // not a sticky error: clear it
+                return RARN_ERR_INVALID_ARG;
+            }
+            if (a.type == cudaMemoryTypeDevice && a.device == dev) return RARN_ERR_UNSUPPORTED;
+        }
+    }
     int per_sm = 0;
     cudaError_t e = dt == RARN_BF16 ? tp_blocks_per_sm<__nv_bfloat16>(H, &per_sm)
                     : dt == RARN_F16 ? tp_blocks_per_sm<__half>(H, &per_sm)

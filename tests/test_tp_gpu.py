@@ -103,6 +103,23 @@ def test_tp_ranks_one_after_another(N, T, H, dt):
     _check(bufs, res, ref, N, T, dt, f"N{N} T{T} H{H} {dt} in turn")
 
 
+def test_tp_per_rank_barrier_on_one_gpu_is_refused():
+    """Per-rank calls that meet in signal-pad barriers need their ranks on
+    different GPUs; with every buffer on this one the call returns
+    UNSUPPORTED before launching, and the buffers are untouched."""
+    import torch
+    N, T, H, dt = 2, 64, 1024, "bf16"
+    d = _inputs(N, T, H, dt, seed=21)
+    bufs, res, g, pads = _device_group(d, N, T, H, dt, True)
+    with pytest.raises(rarn.RarnError) as e:
+        rarn.tp_reduce_add_rms_norm(bufs, 0, res[0], g, EPS, T, signals=pads)
+    assert e.value.status == 2
+    torch.cuda.synchronize()
+    for q in range(N):
+        assert_bits_equal(to_host(bufs[q], dt), d["partials"][q], f"rank {q}'s buffer")
+        assert int(pads[q].abs().sum()) == 0
+
+
 @pytest.mark.parametrize("signals", [False, True])
 @pytest.mark.parametrize("pdl", [True, False])
 def test_tp_two_steps(pdl, signals):
@@ -203,6 +220,7 @@ def _ipc_rank(rank, world, port, q):
         from gpu_util import assert_y_close as ayc
         from gpu_util import to_device as td
         from gpu_util import to_host as th
+        import residual_add_rmsnorm_gb300 as rarn_mod
         from residual_add_rmsnorm_gb300.tp import TPGroup
         torch.cuda.set_device(0)
         dist.init_process_group("gloo", rank=rank, world_size=world)
@@ -210,6 +228,18 @@ def _ipc_rank(rank, world, port, q):
         d = _inputs(N, T, H, dt, seed=11)
         ref = orc.tp_reduce_add_rms_norm([d["partials"][k] for k in range(N)], d["residual"],
                                          d["gamma"], EPS, dt)
+        # with signal pads the two ranks' calls would wait on each other on one
+        # GPU: the per-rank entry point refuses that before launching anything
+        probe = TPGroup(T, H, dt, "cuda:0", signals=True)
+        r0_, r1_ = probe.rows
+        try:
+            probe(torch.zeros(r1_ - r0_, H, dtype=torch.bfloat16, device="cuda"),
+                  torch.ones(H, dtype=torch.bfloat16, device="cuda"), EPS)
+            raise AssertionError("a barrier between ranks on one GPU was not refused")
+        except rarn_mod.RarnError as e:
+            assert e.status == 2, e
+        dist.barrier()
+        probe.close()
         grp = TPGroup(T, H, dt, "cuda:0", signals=False)
         grp.buffer.copy_(td(d["partials"][rank], dt))
         r0, r1 = grp.rows
