@@ -204,18 +204,18 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 }
 
 // Sum of a row's n partial sums (n even, the row 8-byte aligned), added in
-// order; loaded past L1 (other SMs wrote them) 16 at a time, so a row costs
-// n / 16 round trips to L2.
+// order; loaded past L1 (other SMs wrote them) 32 at a time, so a row costs
+// n / 32 round trips to L2.
 __device__ __forceinline__ float row_sum(const float *sr, int n) {
     float tot = 0.f;
-    for (int q0 = 0; q0 < n; q0 += 16) {
-        float2 x[8];
+    for (int q0 = 0; q0 < n; q0 += 32) {
+        float2 x[16];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < 16; ++j)
             x[j] = q0 + 2 * j < n ? __ldcg(reinterpret_cast<const float2 *>(sr + q0) + j)
                                   : make_float2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
+        for (int j = 0; j < 16; ++j)
             if (q0 + 2 * j < n) tot = (tot + x[j].x) + x[j].y;
     }
     return tot;
@@ -1063,25 +1063,133 @@ __device__ __forceinline__ PairItem pair_item(int64_t item, int64_t full_items) 
     return PairItem{full_items + h / 2, (int)(h & 1) * (kMmaN / 2), kMmaN / 2};
 }
 
+// A whole item of the pair kernel whose y waits for the next round (its
+// 256-row block has items there): its epilogue writes h and publishes its
+// partial sums as usual, and its y is formed during the pair's next item, so
+// that the wait for the rest of the row block does not hold up the next
+// accumulator.  m0 < 0: none.
+struct PairPending {
+    int64_t m0;  // first row of this CTA's 128-row block
+    int ntile;   // column tile
+    int gbuf;    // shared-memory gamma buffer holding its columns
+};
+
+// Warp 2 copies the item's gamma columns (16 bytes a lane) into shared memory.
+template <typename T>
+__device__ __forceinline__ void stage_gamma(const Params &p, const PairItem &pi, int ntile,
+                                            uint32_t dst) {
+    static_assert(sizeof(T) == 2, "16-bit operands");
+    const int lane = threadIdx.x & 31;
+    if (lane * 8 < pi.ncols)
+        sts128(dst + lane * 16,
+               ld_keep(reinterpret_cast<const T *>(p.gamma) + ntile * kMmaN + pi.col0 + lane * 8));
+}
+
+// y = RN((h * inv) * gamma) for 8 columns, gamma from shared memory.
+template <typename T>
+__device__ __forceinline__ uint4 scale_smem(const uint4 &h, float inv, uint32_t g) {
+    float f[8], w[8];
+    DT<T>::unpack(h, f);
+    DT<T>::unpack(lds128(g), w);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) f[e] = (f[e] * inv) * w[e];
+    return DT<T>::pack(f);
+}
+
+// y for NC columns of this thread's row from h held in `er` (after run()).
+template <typename T, int NC, bool Wide>
+__device__ __forceinline__ void store_y_smem(const EpiRow<T, NC, Wide> &er, float inv,
+                                             uint32_t g, T *y) {
+#pragma unroll
+    for (int q = 0; q < EpiRow<T, NC, Wide>::kPacks; ++q) {
+        if constexpr (Wide)
+            st_global32(y + 16 * q, scale_smem<T>(er.rv[q].a, inv, g + 32 * q),
+                        scale_smem<T>(er.rv[q].b, inv, g + 32 * q + 16));
+        else
+            st_global(y + 8 * q, scale_smem<T>(er.rv[q], inv, g + 16 * q));
+    }
+}
+
+// y for NC columns of this thread's row from h re-read from global memory
+// (this thread's own earlier stores), a few packs in flight at a time.
+template <typename T, int NC, bool Wide>
+__device__ __forceinline__ void store_y_reload(const T *h, float inv, uint32_t g, T *y) {
+    constexpr int kPacks = EpiRow<T, NC, Wide>::kPacks;
+    constexpr int kGroup = Wide ? 4 : 8;
+    static_assert(kPacks % kGroup == 0, "whole groups");
+#pragma unroll
+    for (int q0 = 0; q0 < kPacks; q0 += kGroup) {
+        typename EpiRow<T, NC, Wide>::Pk v[kGroup];
+#pragma unroll
+        for (int q = 0; q < kGroup; ++q) {
+            if constexpr (Wide)
+                v[q] = ld_stream32(h + 16 * (q0 + q));
+            else
+                v[q] = ld_stream(h + 8 * (q0 + q));
+        }
+#pragma unroll
+        for (int q = 0; q < kGroup; ++q) {
+            if constexpr (Wide)
+                st_global32(y + 16 * (q0 + q), scale_smem<T>(v[q].a, inv, g + 32 * (q0 + q)),
+                            scale_smem<T>(v[q].b, inv, g + 32 * (q0 + q) + 16));
+            else
+                st_global(y + 8 * (q0 + q), scale_smem<T>(v[q], inv, g + 16 * (q0 + q)));
+        }
+    }
+}
+
+// Waits (bounded, one thread) until the counter of the 128-row block at m0
+// shows every column published, then leaves inv of each of its rows in
+// rinv[row] (warp half 0 forms it; both halves read it).  Returns false when
+// the wait gave up.
+__device__ __forceinline__ bool block_inv(const Params &p, int64_t m0, float *rinv,
+                                          volatile int *norm_ok, volatile int *abort_flag) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int slots = 2 * p.C;
+    if (warp == 2 && lane == 0)
+        *norm_ok = wait_count(p.counters + (m0 / kBM), (unsigned int)slots, abort_flag,
+                              p.watchdog, p.wait_limit_ns)
+                       ? 1
+                       : 0;
+    epi_barrier_ws();
+    if (!*norm_ok) return false;
+    const int row = (warp & 3) * 32 + lane;
+    const int64_t t = m0 + row;
+    if (warp < 2 + kWsEpiWarps / 2 && t < p.T)
+        rinv[row] = rsqrtf(row_sum(p.ss + t * slots, slots) / (float)p.H + p.eps);
+    epi_barrier_ws();
+    return true;
+}
+
 // The pair kernel's epilogue for one item, in one CTA (8 warps): NC columns
-// per warp half (128 for a whole tile, 64 for a half).  Returns 0 when a wait
-// gave up (the epilogue stops), 1 otherwise.
+// per warp half (128 for a whole tile, 64 for a half).  Order: the
+// accumulator is read and released, the partial sums published (the rest of
+// the row block may be waiting on them), h stored, the y of a deferred
+// earlier item written, and then this item's y -- or, when its row block
+// ends in the next round and the pair has a next item, this item is
+// deferred in turn.  Returns 0 when a wait gave up (the epilogue stops), 1
+// otherwise.
 template <typename T, int NC, bool Wide>
 __device__ __forceinline__ int pair_epilogue(const Params &p, void *residual, int64_t ldr,
                                              const PairItem &pi, int it, int64_t item,
                                              int64_t npairs, int64_t items, int64_t m0,
                                              uint32_t tbase, uint64_t *tfull, uint64_t *tempty,
                                              volatile int *tile_ok, volatile int *norm_ok,
-                                             float *half_ss, volatile int *abort_flag) {
+                                             float *half_ss, uint32_t gam0, PairPending &pend,
+                                             volatile int *abort_flag) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wh = (warp - 2) >> 2;  // warp half
     const int acc = it & 1;
     const int ntile = (int)(pi.tile % p.C);
     const int slots = 2 * p.C;  // 128-column partial sums per row
-    const int64_t t = m0 + (warp & 3) * 32 + lane;
+    const int row = (warp & 3) * 32 + lane;
+    const int64_t t = m0 + row;
     const bool live = t < p.T;
     const int c0 = pi.col0 + wh * NC;  // this warp half's first column in the tile
+    constexpr uint32_t kGamBytes = kMmaN * 2;
+    const uint32_t gam = gam0 + (uint32_t)(it & 1) * kGamBytes;
     T *res = reinterpret_cast<T *>(residual) + (live ? t : 0) * ldr + ntile * kMmaN + c0;
+    if (p.counters && warp == 2) stage_gamma<T>(p, pi, ntile, gam);
     // this thread's residual columns are loaded before the wait for the
     // accumulator, so they arrive while the item's MMAs run
     EpiRow<T, NC, Wide> er;
@@ -1100,8 +1208,6 @@ __device__ __forceinline__ int pair_epilogue(const Params &p, void *residual, in
     tmem_fence_before();
     // this CTA's half of the accumulator is read: tell the leader
     mbar_arrive_remote(map_to_rank(smem_u32(&tempty[acc]), 0));
-    // h stored only now, off the accumulator's critical path
-    if (live) er.store_h(res);
     const int slot = ntile * 2 + (c0 >> 7);
     if (NC == 128) {
         if (live && !*abort_flag) p.ss[t * slots + slot] = ss;
@@ -1113,30 +1219,42 @@ __device__ __forceinline__ int pair_epilogue(const Params &p, void *residual, in
             p.ss[t * slots + slot] = ss + half_ss[(warp + 2) * 32 + lane];
     }
     epi_barrier_ws();
-    if (p.counters) {
-        // publish this item's slots, then wait (bounded) for the rest of the
-        // 128-row block's columns
-        unsigned int *cnt = p.counters + (m0 / kBM);
-        if (warp == 2 && lane == 0) {
-            __threadfence();
-            atomicAdd(cnt, (unsigned int)(pi.ncols >> 7));
-            *norm_ok = wait_count(cnt, (unsigned int)slots, abort_flag, p.watchdog,
-                                  p.wait_limit_ns)
-                           ? 1
-                           : 0;
-        }
-        epi_barrier_ws();
-        if (!*norm_ok) return 0;
-        // inv of each row, formed once (warp half 0) and shared through
-        // shared memory
-        const int row = (warp & 3) * 32 + lane;
-        if (wh == 0 && live)
-            half_ss[row] = rsqrtf(row_sum(p.ss + t * slots, slots) / (float)p.H + p.eps);
-        epi_barrier_ws();
-        if (live)
-            er.store_y(half_ss[row], reinterpret_cast<const T *>(p.gamma) + ntile * kMmaN + c0,
-                       reinterpret_cast<T *>(p.y) + t * p.ldy + ntile * kMmaN + c0);
+    if (p.counters && warp == 2 && lane == 0) {
+        // publish this item's slots (the counter of its 128-row block)
+        __threadfence();
+        atomicAdd(p.counters + (m0 / kBM), (unsigned int)(pi.ncols >> 7));
     }
+    // h stored only now, off the accumulator's and the row block's paths
+    if (live) er.store_h(res);
+    if (!p.counters) return 1;
+    if (pend.m0 >= 0) {
+        // the deferred whole item: its row block ended in this round
+        if (!block_inv(p, pend.m0, half_ss, norm_ok, abort_flag)) return 0;
+        const int64_t tp = pend.m0 + row;
+        if (tp < p.T) {
+            const int64_t col = (int64_t)pend.ntile * kMmaN + wh * 128;
+            store_y_reload<T, 128, Wide>(reinterpret_cast<const T *>(residual) + tp * ldr + col,
+                                         half_ss[row],
+                                         gam0 + (uint32_t)pend.gbuf * kGamBytes + wh * 256,
+                                         reinterpret_cast<T *>(p.y) + tp * p.ldy + col);
+        }
+        pend.m0 = -1;
+    }
+    if (item + npairs < items) {
+        // the item index of the last tile of this 256-row block; the
+        // block's tiles of the last partial round run as two halves each
+        const int64_t last = (pi.tile / p.C) * p.C + p.C - 1;
+        const int64_t last_item =
+            last < p.full_items ? last : p.full_items + 2 * (last - p.full_items) + 1;
+        if (last_item / npairs > item / npairs) {
+            pend = PairPending{m0, ntile, it & 1};
+            return 1;
+        }
+    }
+    if (!block_inv(p, m0, half_ss, norm_ok, abort_flag)) return 0;
+    if (live)
+        store_y_smem<T, NC, Wide>(er, half_ss[row], gam + (uint32_t)(wh * NC) * 2,
+                                  reinterpret_cast<T *>(p.y) + t * p.ldy + ntile * kMmaN + c0);
     return 1;
 }
 
@@ -1157,10 +1275,12 @@ struct PairLayout {
     static constexpr int ctl_off = stages * stage_bytes;
     // full[S], empty[S], tfull[2], tempty[2], mma_done (8 B each); tmem slot,
     // abort word, the peer's fill count, tile_ok, norm_ok; the epilogue's
-    // half-row sums
+    // half-row sums (and each row's inv)
     static constexpr int words_off = ctl_off + (2 * stages + 5) * 8;
     static constexpr int half_off = words_off + 32;
-    static constexpr int total = half_off + kWsEpiWarps * 32 * 4 + 1024;
+    // two buffers of one tile's gamma columns (items alternate)
+    static constexpr int gam_off = (half_off + kWsEpiWarps * 32 * 4 + 15) / 16 * 16;
+    static constexpr int total = gam_off + 2 * kMmaN * 2 + 1024;
     static_assert(total <= 227 * 1024, "one CTA per SM");
 };
 
@@ -1326,6 +1446,8 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         // ---- epilogue: warps 2-9 of both CTAs, each on its CTA's 128 rows;
         // warp half (warp - 2) / 4 takes half of the item's columns ----
         int it = 0;
+        PairPending pend{-1, 0, 0};
+        const uint32_t gam0 = smem_u32(smem + Lay::gam_off);
         for (int64_t item = pair; item < items; item += npairs, ++it) {
             const PairItem pi = pair_item(item, p.full_items);
             const int64_t m0 = (pi.tile / C) * kPairBM + rank * kBM;
@@ -1335,10 +1457,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
                 pi.ncols == NS
                     ? pair_epilogue<T, NS / 2, Wide>(p, residual, ldr, pi, it, item, npairs, items,
                                                      m0, tbase, tfull, tempty, tile_ok, norm_ok,
-                                                     half_ss, abort_flag)
+                                                     half_ss, gam0, pend, abort_flag)
                     : pair_epilogue<T, NS / 4, Wide>(p, residual, ldr, pi, it, item, npairs, items,
                                                      m0, tbase, tfull, tempty, tile_ok, norm_ok,
-                                                     half_ss, abort_flag);
+                                                     half_ss, gam0, pend, abort_flag);
             if (!ok) break;
         }
     }
@@ -1580,11 +1702,13 @@ __global__ void __launch_bounds__(256) k_splitk_norm(NormParams q, const float *
 
 // Zeroes the row-block counters of the norm in the persistent kernels'
 // epilogue, after the previous kernel on the stream (which may be the previous
-// call's GEMM, still counting) has finished.
+// call's GEMM, still counting) has finished.  The GEMM may launch at once (its
+// prologue overlaps this kernel): its own wait for this grid covers these
+// stores, and this grid ends only after the previous kernel has.
 static __global__ void __launch_bounds__(256) k_zero_counters(unsigned int *cnt, int64_t n) {
+    grid_launch_dependents();
     grid_dependency_wait();
     for (int64_t i = threadIdx.x; i < n; i += blockDim.x) cnt[i] = 0u;
-    grid_launch_dependents();
 }
 
 // Kernel 2: y from the stored h and the column blocks' partial sums.  A warp

@@ -169,7 +169,7 @@ inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
             // (gemm_norm.cuh PairLayout, gemm_norm_launch.cuh)
             const int half = (128 + g.ns / 2) * g.bk * 2;
             g.stages = 3;
-            g.smem = g.stages * 2 * half + 3 * 1024;
+            g.smem = g.stages * 2 * half + 4 * 1024;
             g.grid = 2 * std::min<int64_t>(((T + 255) / 256) * g.tiles_n, num_sms / 2);
         }
         if (g.pair) {
