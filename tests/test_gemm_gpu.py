@@ -176,10 +176,13 @@ def test_gemm_norm_in_epilogue_matches_norm_kernel(pair, tune):
     """y written by the persistent kernel's epilogue (each tile waits on its
     128-row block's counter) and by the separate norm kernel: bit-identical,
     on shapes with more tiles than CTAs or pairs, so that row blocks straddle
-    two rounds of tiles, and with 32 column tiles per row."""
+    two rounds of tiles, and with 32 column tiles per row.  At 4096 rows on
+    pairs some pairs defer the y of two items in a row (a row block
+    straddling rounds 0 and 1, another rounds 1 and 2), the case where the
+    staged gamma must not be overwritten while a deferred y still reads it."""
     import torch
     tune(gemm_pair=pair)
-    for T, H, K in ((2500, 4096, 512), (1000, 8192, 576), (129, 2048, 1024)):
+    for T, H, K in ((2500, 4096, 512), (1000, 8192, 576), (129, 2048, 1024), (4096, 4096, 512)):
         gen = torch.Generator(device="cuda").manual_seed(T + H + K)
         a = torch.randn(T, K, device="cuda", generator=gen).to(torch.bfloat16)
         w = (torch.randn(H, K, device="cuda", generator=gen) / K ** 0.5).to(torch.bfloat16)
