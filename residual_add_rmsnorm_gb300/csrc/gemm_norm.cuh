@@ -205,9 +205,36 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 
 // Sum of a row's n partial sums (n even, the row 8-byte aligned), added in
 // order; loaded past L1 (other SMs wrote them) 32 at a time, so a row costs
-// n / 32 round trips to L2.
+// n / 32 round trips to L2.  Rows of a multiple of 8 sums that start on a
+// 32-byte boundary are read a whole sector per load (8-byte loads would
+// touch each sector four times).
 __device__ __forceinline__ float row_sum(const float *sr, int n) {
     float tot = 0.f;
+    if (n % 8 == 0 && (reinterpret_cast<uintptr_t>(sr) & 31u) == 0) {
+        for (int q0 = 0; q0 < n; q0 += 32) {
+            uint32_t x[4][8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (q0 + 8 * j < n) {
+                    asm volatile("ld.global.cg.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                                 : "=r"(x[j][0]), "=r"(x[j][1]), "=r"(x[j][2]), "=r"(x[j][3]),
+                                   "=r"(x[j][4]), "=r"(x[j][5]), "=r"(x[j][6]), "=r"(x[j][7])
+                                 : "l"(sr + q0 + 8 * j));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[j][e] = 0u;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (q0 + 8 * j < n) {
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2)
+                        tot = (tot + __uint_as_float(x[j][e])) + __uint_as_float(x[j][e + 1]);
+                }
+        }
+        return tot;
+    }
     for (int q0 = 0; q0 < n; q0 += 32) {
         float2 x[16];
 #pragma unroll
