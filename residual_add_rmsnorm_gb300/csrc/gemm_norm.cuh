@@ -15,9 +15,12 @@
 //     the last partial round as 128-column halves), warp-specialised: a TMA
 //     producer, one MMA-issuing thread, 8 epilogue warps per CTA draining one
 //     of two TMEM accumulators while the next tile's MMAs run.  The epilogue
-//     adds the residual (one rounding), writes h, writes per-128-column
-//     partial sums of squares, and, once its 128-row block's counter shows
-//     every column (k_zero_counters zeroes the counters first), writes y.
+//     adds the residual (one rounding), publishes per-128-column partial
+//     sums of squares (adding to its 128-row block's counter, which
+//     k_zero_counters zeroes first), writes h, and once the counter shows
+//     every column writes y -- for a tile whose row block ends in the next
+//     round of tiles, during the pair's next tile.  The epilogue's streams
+//     (residual in, h and y out) carry an L2 evict-first policy.
 //   * K >= 512, 128 < T < 2048 (or T <= 128 with short K): k_gemm_res_ws,
 //     the same on one SM per 128 x 256 tile (M = 128 MMAs).
 //   * T <= 128, K >= 1024: k_gemm_splitk, C x S CTAs each multiplying a K
