@@ -312,16 +312,18 @@ rarn_status rarn_reduce_add_rms_norm_fp8in(void *y, const void *partials, int32_
  * other column tiles of its 128-row block (a counter per block in the
  * workspace, zeroed by a one-CTA kernel launched just before), sums each
  * row's partials in column order and writes y; otherwise a norm kernel does
- * that last step.  Both orders give identical bits.  With T <= 128 and
- * K >= 1024 the product is split over K instead: up to 9 CTAs per column
- * tile write binary32 partial products into the workspace and a CTA per row
- * adds them in split order, adds the residual (one rounding) and normalises
- * (a different binary32 summation order, within the same accuracy bound);
- * this needs the full rarn_gemm_workspace_bytes(T, H) and a 32-byte aligned
+ * that last step.  Both orders give identical bits.  With K >= 1024 and so
+ * few 128 x 256 tiles (ceil(T / 128) row blocks of H / 256) that they leave
+ * at least half of the SMs idle, the product is split over K instead: S =
+ * min(9, floor(min(SMs, 152) / tiles), floor(ceil(K / 64) / 8)) CTAs per tile
+ * write binary32 partial products into the workspace and a CTA per row adds
+ * them in split order, adds the residual (one rounding) and normalises (a
+ * different binary32 summation order, within the same accuracy bound); this
+ * needs the full rarn_gemm_workspace_bytes(T, H) and a 32-byte aligned
  * workspace, else the call runs without split K.  `workspace` is
  * caller-owned device memory of at least the bytes the non-split kernels use
- * (rarn_gemm_workspace_bytes for T > 128; 16-byte aligned); its contents are
- * scratch and need no initialisation.
+ * (rarn_gemm_workspace_bytes where split K cannot apply; 16-byte aligned);
+ * its contents are scratch and need no initialisation.
  *
  * Matrices are rarn_rows (row-major, row_stride in elements), all of one
  * 16-bit type (RARN_BF16 or RARN_F16; RARN_F32 returns UNSUPPORTED); gamma is
@@ -375,8 +377,8 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
  * argument error leaves every buffer untouched.  (A launch failure, reported
  * as RARN_ERR_CUDA, can still come after earlier sequences were enqueued.)
  * Results are bit-identical to the workspace form's, with one exception:
- * for T <= 128 the workspace form splits K over S <= 9 CTAs per column tile
- * (S = the split count rarn_plan_gemm reports), and this entry point does
+ * where the workspace form splits K over S <= 9 CTAs per tile (S = the
+ * split count rarn_plan_gemm reports), this entry point does
  * the same only where the split's partial products fit in the array next to
  * the partial sums, i.e. where
  *   64 * ceil((4 * ceil(T * H / 512) + ceil(T / 128)) / 64) + S * T * H <= 2^20
@@ -390,8 +392,10 @@ rarn_status rarn_gemm_add_rms_norm_noalloc(rarn_rows y, rarn_rows a, rarn_rows w
 
 /* Workspace bytes rarn_gemm_add_rms_norm needs for T rows of H: one binary32
  * per row and 128 columns, rounded up to 16 bytes, then one 32-bit counter
- * per 128-row block; for T <= 128 (H <= 8192) also, from the next 256-byte
- * boundary, 9 T H binary32 values for split K.  -1 if H is not supported. */
+ * per 128-row block; where split K can apply (H <= 8192 and ceil(T / 128) *
+ * H / 256 tiles leave at least half of 152 SMs idle) also, from the next
+ * 256-byte boundary, S T H binary32 values for split K, S = min(9,
+ * floor(152 / tiles)).  -1 if H is not supported. */
 int64_t rarn_gemm_workspace_bytes(int64_t T, int64_t H);
 
 /* Describe the kernel rarn_reduce_add_rms_norm_fp8in takes for a problem

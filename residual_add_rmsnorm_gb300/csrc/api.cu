@@ -977,7 +977,8 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
     const int64_t base = gemm_workspace_bytes_for(T, H);
     if ((int64_t)workspace_bytes < base || (reinterpret_cast<uintptr_t>(workspace) & 15u))
         return RARN_ERR_INVALID_ARG;
-    const int64_t most = T <= 128 ? gemm_splitk_bytes(T, H, kGemmMaxSplitK) : base;
+    const int room = H % 256 == 0 && H / 256 <= kGemmMaxTilesN ? splitk_room(T, (int)(H / 256)) : 0;
+    const int64_t most = room ? gemm_splitk_bytes(T, H, room) : base;
     const int64_t ws = std::min<int64_t>((int64_t)workspace_bytes, most);
     const void *others[5] = {y.data, residual.data, a.data, w.data, gamma};
     const int64_t ob[5] = {span_bytes(T, H, y.row_stride, 2),

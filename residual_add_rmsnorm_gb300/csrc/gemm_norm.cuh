@@ -23,9 +23,11 @@
 //     (residual in, h and y out) carry an L2 evict-first policy.
 //   * K >= 512, 128 < T < 2048 (or T <= 128 with short K): k_gemm_res_ws,
 //     the same on one SM per 128 x 256 tile (M = 128 MMAs).
-//   * T <= 128, K >= 1024: k_gemm_splitk, C x S CTAs each multiplying a K
-//     range and writing binary32 partial products; k_splitk_norm sums them in
-//     split order, adds the residual and normalises.
+//   * K >= 1024 and so few 128 x 256 tiles that they leave half of the SMs
+//     idle (T <= 128 at H = 4096, up to 512 rows at H = 2048): k_gemm_splitk,
+//     M x C x S CTAs each multiplying a K range of one tile and writing
+//     binary32 partial products; k_splitk_norm sums them in split order, adds
+//     the residual and normalises.
 //   * K < 512: k_gemm_res, one CTA per [128 x NS] tile (NS = 256 or 512), the
 //     operand ring staging the epilogue: the residual tile arrives by TMA in
 //     [128 x 32] chunks (64-byte swizzle), each thread adds its accumulator
@@ -98,7 +100,7 @@ struct Params {
     // the pair kernel's items: tiles [0, full_items) whole, then the
     // remaining tiles as two 128-column halves each (items in all)
     int64_t full_items, items;
-    // split K (T <= 128): CTA (tile n, split s) multiplies K slabs
+    // split K (few row blocks): CTA (row block m, tile n, split s) multiplies K slabs
     // [s * kb_per_split, ...) and writes its binary32 partial products to
     // part[s][row][column]
     float *part;
@@ -1565,9 +1567,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 }
 
 // ---------------------------------------------------------------------------
-// Split K for few rows (T <= 128, a single 128-row block): with only H / 256
-// column tiles the tiled kernels would stream W through as many SMs; here
-// CTA (n, s) of a C x splits grid multiplies the K slabs of split s for
+// Split K for few rows (ceil(T / 128) row blocks whose tiles leave at least
+// half of the SMs idle): with only M x H / 256 tiles the tiled kernels would
+// stream the operands through as many SMs; here CTA (m, n, s) of an
+// M x C x splits grid multiplies the K slabs of split s for row block m and
 // column tile n (4-stage TMA ring, M = 128, N = 256 MMAs into TMEM, as
 // k_gemm_res) and writes its binary32 partial products for the live rows.
 // k_splitk_norm then adds the splits in order, adds the residual (one
@@ -1590,8 +1593,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mblocks = (int)((p.T + kBM - 1) / kBM);
     const int ntile = (int)(blockIdx.x % p.C);
-    const int split = (int)(blockIdx.x / p.C);
+    const int mblk = (int)((blockIdx.x / p.C) % mblocks);
+    const int split = (int)(blockIdx.x / ((unsigned)p.C * mblocks));
     const int n0 = ntile * NS;
     const int kb0 = split * p.kb_per_split;
     const int kb1 = min(p.kblocks, kb0 + p.kb_per_split);
@@ -1631,7 +1636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive_expect_tx(
                 fb, L.stage_bytes + (blockIdx.x == 0 && issued == p.stall_fill ? 16u : 0u));
             const uint32_t sa = smem_u32(smem + s * L.stage_bytes);
-            tma_load_2d(sa, &map_a, kb * BK, 0, fb);
+            tma_load_2d(sa, &map_a, kb * BK, mblk * kBM, fb);
             tma_load_2d(sa + L.a_bytes, &map_w, kb * BK, n0, fb);
             if (++s == S) {
                 s = 0;
@@ -1670,7 +1675,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     const bool ok = !*abort_flag;
     grid_launch_dependents();
-    const int r = threadIdx.x;
+    const int64_t r = (int64_t)mblk * kBM + threadIdx.x;
     const uint32_t tbase = tmem + (static_cast<uint32_t>(warp * 32) << 16);
     float *dst = p.part + ((int64_t)split * p.T + r) * p.H + n0;
     for (int c = 0; c < NS; c += 32) {

@@ -201,7 +201,7 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
                          c.pdl, 1, q);
 }
 
-// Split K (T <= 128): C x splits CTAs write binary32 partial products, then a
+// Split K (few row blocks): M x C x splits CTAs write binary32 partial products, then a
 // CTA per row sums them in split order, adds the residual and normalises.
 template <typename T>
 static cudaError_t launch_gemm_splitk(const GemmCall &c, cudaStream_t st) {
@@ -231,7 +231,9 @@ static cudaError_t launch_gemm_splitk(const GemmCall &c, cudaStream_t st) {
     constexpr int smem = layout(4, kMmaN, 64).total;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
-        e = launch_kernel(kernel, dim3(static_cast<unsigned>(p.C * used)), dim3(kThreads),
+        e = launch_kernel(kernel,
+                          dim3(static_cast<unsigned>(p.C * ((c.T + kBM - 1) / kBM) * used)),
+                          dim3(kThreads),
                           static_cast<size_t>(smem), st, c.pdl, 1, ma, mw, p);
     if (e != cudaSuccess) return e;
     NormParams q{};

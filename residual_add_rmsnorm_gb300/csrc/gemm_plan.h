@@ -53,16 +53,32 @@ struct GemmPlan {
     int splitk = 0;  // K split over this many CTAs per column tile (0: none)
 };
 
-// Split K applies to a single 128-row block (T <= 128) of 256-column tiles,
-// using up to the SMs the column tiles leave idle, each split at least 8
-// K slabs of 64 and at most 9 splits (the parity bound allows 8 extra binary32
-// roundings per element).
+// Split K applies while the 128 x 256 tiles of the ceil(T / 128) row blocks
+// leave at least half of the SMs idle, using up to the SMs they leave idle
+// (counted as at most 152, the count the workspace is sized for), each split
+// at least 8 K slabs of 64 and at most 9 splits (the parity bound allows 8
+// extra binary32 roundings per element).  Measured (bf16, K = H = 4096,
+// against the one-SM persistent kernel, us): T = 192 28.8 -> 15.2, T = 256
+// 29.2 -> 15.6, T = 384 29.4 -> 18.8, T = 512 29.6 -> 21.6; T = 256,
+// K = H = 8192 60.6 -> 44.1; T = 640 (no split) 30.3.
 constexpr int kGemmMaxSplitK = 9;
+constexpr int kGemmSplitKSMs = 152;
+
+// Splits the workspace of T x H has room for (K unknown): 0 where split K
+// cannot apply.
+inline int splitk_room(int64_t T, int tiles_n) {
+    if (tiles_n <= 0) return 0;
+    const int64_t tiles = ((T + 127) / 128) * tiles_n;
+    const int64_t s = std::min<int64_t>(kGemmMaxSplitK, kGemmSplitKSMs / tiles);
+    return s >= 2 ? (int)s : 0;
+}
 
 inline int plan_splitk(int64_t T, int tiles_n, int64_t K, int num_sms) {
-    if (T > 128 || tiles_n <= 0) return 0;
+    if (tiles_n <= 0) return 0;
+    const int64_t tiles = ((T + 127) / 128) * tiles_n;
     const int64_t kb = (K + 63) / 64;
-    int64_t s = std::min<int64_t>(kGemmMaxSplitK, std::min<int64_t>(num_sms / tiles_n, kb / 8));
+    const int64_t sms = std::min<int64_t>(num_sms, kGemmSplitKSMs);
+    int64_t s = std::min<int64_t>(kGemmMaxSplitK, std::min<int64_t>(sms / tiles, kb / 8));
     return s >= 2 ? (int)s : 0;
 }
 
@@ -143,7 +159,7 @@ inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
             g.bk = 64;
             g.stages = 4;
             g.smem = 4 * (128 + 256) * 64 * 2 + 2048;
-            g.grid = (int64_t)g.tiles_n * g.splitk;
+            g.grid = ((T + 127) / 128) * g.tiles_n * g.splitk;
             return g;
         }
     }
@@ -195,7 +211,7 @@ inline int64_t gemm_workspace_bytes_for(int64_t T, int64_t H) {
     return (gemm_counters_offset(T, H) + (T + 127) / 128) * 4;
 }
 
-// Split K (T <= 128): the partial products follow, 256-byte aligned, as
+// Split K (few row blocks): the partial products follow, 256-byte aligned, as
 // splits x T x H binary32 values.
 inline int64_t gemm_splitk_offset(int64_t T, int64_t H) {  // in floats
     return (gemm_workspace_bytes_for(T, H) / 4 + 63) / 64 * 64;
@@ -209,9 +225,9 @@ inline int64_t gemm_splitk_bytes(int64_t T, int64_t H, int splits) {
 inline int64_t gemm_workspace_bytes(int64_t T, int64_t H) {
     const GemmPlan g = plan_gemm(T, H, 0);
     if (g.ns == 0) return -1;
-    // room for split K at its largest whenever it can apply (T <= 128)
-    return T <= 128 && g.ns == 256 ? gemm_splitk_bytes(T, H, kGemmMaxSplitK)
-                                   : gemm_workspace_bytes_for(T, H);
+    // room for split K at its largest whenever it can apply
+    const int room = g.ns == 256 ? splitk_room(T, (int)(H / 256)) : 0;
+    return room ? gemm_splitk_bytes(T, H, room) : gemm_workspace_bytes_for(T, H);
 }
 
 }  // namespace rarn

@@ -449,7 +449,7 @@ def test_plan_gemm(tune):
     p = rarn.plan_gemm(4096, 4096, 4096)
     assert "cols_per_cta=256 col_tiles=16 bk=64 stages=3" in p and "grid=152" in p, p
     assert "kblocks=64 persistent=1 pair=1" in p, p
-    p = rarn.plan_gemm(2100, 512, 4096)    # 9 x 2 pair tiles: 18 clusters
+    p = rarn.plan_gemm(2100, 512, 512)     # 9 x 2 pair tiles: 18 clusters
     assert "grid=36 " in p and "pair=1" in p, p
     p = rarn.plan_gemm(1024, 4096, 4096)   # below 2048 rows: one SM per tile
     assert "persistent=1 pair=0" in p, p
@@ -458,11 +458,17 @@ def test_plan_gemm(tune):
     assert "cols_per_cta=256 col_tiles=16 bk=64 stages=4" in p and "grid=152" in p, p
     assert "kblocks=64 persistent=1 pair=0" in p, p
     tune(gemm_pair=-1)
-    p = rarn.plan_gemm(200, 768, 1000)     # two 128-row blocks: one SM per tile
+    p = rarn.plan_gemm(200, 768, 960)      # two 128-row blocks, 15 K slabs: one SM per tile
     assert "cols_per_cta=256 col_tiles=3" in p and "persistent=1" in p and "grid=6" in p, p
     assert "pair=0" in p, p
-    # one 128-row block: K split over the idle SMs, at least 8 K slabs each, at
-    # most 9 splits
+    # tiles that leave half of the SMs idle: K split over the idle SMs, at
+    # least 8 K slabs each, at most 9 splits, every row block
+    p = rarn.plan_gemm(256, 4096, 4096)    # 2 x 16 tiles, 152 // 32 = 4 splits
+    assert "splitk=4" in p and "grid=128" in p, p
+    p = rarn.plan_gemm(512, 4096, 4096)    # 4 x 16 tiles: 2 splits
+    assert "splitk=2" in p and "grid=128" in p, p
+    p = rarn.plan_gemm(640, 4096, 4096)    # 5 x 16 tiles: more than half of the SMs
+    assert "splitk" not in p and "persistent=1" in p, p
     p = rarn.plan_gemm(100, 768, 1000)
     assert "col_tiles=3" in p and "splitk=2" in p and "grid=6" in p, p
     p = rarn.plan_gemm(1, 4096, 4096)
@@ -478,10 +484,15 @@ def test_plan_gemm(tune):
     assert rarn.plan_gemm(8, 16896, 64).startswith("none")   # 33 x 512: beyond 32 tiles
     assert rarn.plan_gemm(8, 4096, 64, "f32").startswith("none")
     # partial sums [T][H / 128], then one counter per 128-row block (16-byte
-    # aligned); up to 128 rows also room for 9-way split K
+    # aligned); where split K can apply also room for min(9, 152 // tiles)
+    # splits of T x H binary32 products from the next 256-byte boundary
     assert rarn.gemm_workspace_bytes(4096, 4096) == (4096 * 32 + 32) * 4
     assert rarn.gemm_workspace_bytes(1, 768) == (64 + 9 * 768) * 4
-    assert rarn.gemm_workspace_bytes(129, 768) == ((129 * 6 + 3) // 4 * 4 + 2) * 4
+    base129 = (129 * 6 + 3) // 4 * 4 + 2
+    assert rarn.gemm_workspace_bytes(129, 768) == ((base129 + 63) // 64 * 64 + 9 * 129 * 768) * 4
+    base512 = 512 * 32 + 4
+    assert rarn.gemm_workspace_bytes(512, 4096) == ((base512 + 63) // 64 * 64 + 2 * 512 * 4096) * 4
+    assert rarn.gemm_workspace_bytes(640, 4096) == (640 * 32 + 5) * 4
     assert rarn.gemm_workspace_bytes(7, 300) == -1
 
 

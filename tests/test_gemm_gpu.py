@@ -132,7 +132,9 @@ def run_case(T, H, K, dt="bf16", seed=0, lda=None, ldw=None, ldr=None, ldy=None,
 def test_gemm_parity(T, H, K, dt):
     plan = run_case(T, H, K, dt, seed=T + H + K)
     assert plan.startswith("gemm.tcgen05"), plan
-    splitk = H <= 8192 and T <= 128 and K >= 1024
+    # split K where the 128 x 256 tiles leave at least half of the 152 SMs idle
+    tiles = -(-T // 128) * (H // 256)
+    splitk = H <= 8192 and min(9, 152 // tiles, -(-K // 64) // 8) >= 2
     assert ("splitk=" in plan) == splitk, plan
     assert ("persistent=1" in plan) == (H <= 8192 and K >= 512 and not splitk), plan
     assert ("pair=1" in plan) == (H <= 8192 and K >= 512 and T >= 2048), plan
@@ -181,7 +183,7 @@ def test_gemm_norm_in_epilogue_matches_norm_kernel(pair, tune):
     straddling rounds 0 and 1, another rounds 1 and 2), the case where the
     staged gamma must not be overwritten while a deferred y still reads it."""
     import torch
-    tune(gemm_pair=pair)
+    tune(gemm_pair=pair, gemm_split_k=0)  # the persistent kernels, not split K
     for T, H, K in ((2500, 4096, 512), (1000, 8192, 576), (129, 2048, 1024), (4096, 4096, 512)):
         gen = torch.Generator(device="cuda").manual_seed(T + H + K)
         a = torch.randn(T, K, device="cuda", generator=gen).to(torch.bfloat16)
@@ -243,12 +245,16 @@ def test_gemm_pair_tail_halves(tune):
     (100, 2048, 4096, "f16"),   # 8 splits of 8 slabs
     (128, 8192, 2048, "bf16"),  # 32 column tiles x 4 splits
     (5, 2048, 8192, "bf16"),    # 9 splits (the most), 15 slabs each, the last 8
+    (256, 4096, 4096, "bf16"),  # 2 row blocks x 16 column tiles x 4 splits
+    (300, 2048, 1024, "f16"),   # 3 row blocks (the last ragged) x 8 tiles x 2 splits
+    (512, 4096, 2048, "bf16"),  # 4 row blocks x 16 tiles x 2 splits
 ])
 def test_gemm_splitk(T, H, K, dt):
-    """Split K for a single 128-row block (T <= 128): C x splits CTAs write
-    binary32 partial products, a CTA per row adds them in split order, adds
-    the residual (one rounding) and normalises; against the oracle with the
-    accumulation bound (at most 8 extra binary32 additions per element)."""
+    """Split K where the 128 x 256 tiles leave half of the SMs idle: M x C x
+    splits CTAs (row block, column tile, K range) write binary32 partial
+    products, a CTA per row adds them in split order, adds the residual (one
+    rounding) and normalises; against the oracle with the accumulation bound
+    (at most 8 extra binary32 additions per element)."""
     plan = run_case(T, H, K, dt, seed=T * 7 + K)
     assert "splitk=" in plan, plan
 
