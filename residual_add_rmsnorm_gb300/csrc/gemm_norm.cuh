@@ -1714,7 +1714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 8-column packs per thread.  P = ((p_0 + p_1) + ...) + p_{S-1} in binary32,
 // h = RN(P + r) (one rounding), the residual updated, Σh² over the CTA, y from
 // the h held in registers.
-template <typename T, int VPT>
+template <typename T, int VPT, int SMAX>
 __global__ void __launch_bounds__(256) k_splitk_norm(NormParams q, const float *part, int splits,
                                                       void *residual) {
     __shared__ float red[32];
@@ -1731,17 +1731,25 @@ __global__ void __launch_bounds__(256) k_splitk_norm(NormParams q, const float *
         if (j < nv) {
             float acc[8];
             const float *src = part + t * q.H + (int64_t)j * 8;
-            const Pack32 p0 = ld_stream32(src);
-            acc[0] = __uint_as_float(p0.a.x), acc[1] = __uint_as_float(p0.a.y);
-            acc[2] = __uint_as_float(p0.a.z), acc[3] = __uint_as_float(p0.a.w);
-            acc[4] = __uint_as_float(p0.b.x), acc[5] = __uint_as_float(p0.b.y);
-            acc[6] = __uint_as_float(p0.b.z), acc[7] = __uint_as_float(p0.b.w);
-            for (int s = 1; s < splits; ++s) {
-                const Pack32 ps = ld_stream32(src + (int64_t)s * q.T * q.H);
-                acc[0] += __uint_as_float(ps.a.x), acc[1] += __uint_as_float(ps.a.y);
-                acc[2] += __uint_as_float(ps.a.z), acc[3] += __uint_as_float(ps.a.w);
-                acc[4] += __uint_as_float(ps.b.x), acc[5] += __uint_as_float(ps.b.y);
-                acc[6] += __uint_as_float(ps.b.z), acc[7] += __uint_as_float(ps.b.w);
+            // the pack's S <= SMAX partials loaded together (one round trip;
+            // K = H = 4096: T = 1 11.3 -> 10.1 us, T = 16 9.7 -> 8.2, T = 128
+            // 14.8 -> 13.3), then added in split order
+            Pack32 v[SMAX];
+#pragma unroll
+            for (int s = 0; s < SMAX; ++s)
+                if (s < splits) v[s] = ld_stream32(src + (int64_t)s * q.T * q.H);
+            acc[0] = __uint_as_float(v[0].a.x), acc[1] = __uint_as_float(v[0].a.y);
+            acc[2] = __uint_as_float(v[0].a.z), acc[3] = __uint_as_float(v[0].a.w);
+            acc[4] = __uint_as_float(v[0].b.x), acc[5] = __uint_as_float(v[0].b.y);
+            acc[6] = __uint_as_float(v[0].b.z), acc[7] = __uint_as_float(v[0].b.w);
+#pragma unroll
+            for (int s = 1; s < SMAX; ++s) {
+                if (s < splits) {
+                    acc[0] += __uint_as_float(v[s].a.x), acc[1] += __uint_as_float(v[s].a.y);
+                    acc[2] += __uint_as_float(v[s].a.z), acc[3] += __uint_as_float(v[s].a.w);
+                    acc[4] += __uint_as_float(v[s].b.x), acc[5] += __uint_as_float(v[s].b.y);
+                    acc[6] += __uint_as_float(v[s].b.z), acc[7] += __uint_as_float(v[s].b.w);
+                }
             }
             float f[8];
             DT<T>::unpack(ld_stream(res + (int64_t)j * 8), f);

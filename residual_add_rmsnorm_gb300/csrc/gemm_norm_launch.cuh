@@ -201,6 +201,23 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
                          c.pdl, 1, q);
 }
 
+// k_splitk_norm with registers for at most SMAX splits' partials (a CTA per row).
+template <typename T, int SMAX>
+static cudaError_t launch_splitk_norm(const gemm::NormParams &q, const GemmCall &c, int nv,
+                                      int used, cudaStream_t st) {
+    using namespace gemm;
+    const dim3 g2(static_cast<unsigned>(c.T));
+    const float *part = static_cast<const float *>(c.part);
+    if (nv <= 256)
+        return launch_kernel(k_splitk_norm<T, 1, SMAX>, g2, dim3((nv + 31) / 32 * 32), 0, st,
+                             c.pdl, 1, q, part, used, c.residual);
+    if (nv <= 512)
+        return launch_kernel(k_splitk_norm<T, 2, SMAX>, g2, dim3(256), 0, st, c.pdl, 1, q, part,
+                             used, c.residual);
+    return launch_kernel(k_splitk_norm<T, 4, SMAX>, g2, dim3(256), 0, st, c.pdl, 1, q, part,
+                         used, c.residual);
+}
+
 // Split K (few row blocks): M x C x splits CTAs write binary32 partial products, then a
 // CTA per row sums them in split order, adds the residual and normalises.
 template <typename T>
@@ -246,15 +263,9 @@ static cudaError_t launch_gemm_splitk(const GemmCall &c, cudaStream_t st) {
     q.ldy = c.ldy;
     q.eps = c.eps;
     const int nv = static_cast<int>(c.H / 8);
-    const dim3 g2(static_cast<unsigned>(c.T));
-    if (nv <= 256)
-        return launch_kernel(k_splitk_norm<T, 1>, g2, dim3((nv + 31) / 32 * 32), 0, st, c.pdl, 1, q,
-                             static_cast<const float *>(c.part), used, c.residual);
-    if (nv <= 512)
-        return launch_kernel(k_splitk_norm<T, 2>, g2, dim3(256), 0, st, c.pdl, 1, q,
-                             static_cast<const float *>(c.part), used, c.residual);
-    return launch_kernel(k_splitk_norm<T, 4>, g2, dim3(256), 0, st, c.pdl, 1, q,
-                         static_cast<const float *>(c.part), used, c.residual);
+    if (used <= 2) return launch_splitk_norm<T, 2>(q, c, nv, used, st);
+    if (used <= 4) return launch_splitk_norm<T, 4>(q, c, nv, used, st);
+    return launch_splitk_norm<T, kGemmMaxSplitK>(q, c, nv, used, st);
 }
 
 template <typename T>
