@@ -105,6 +105,8 @@ struct Params {
     // part[s][row][column]
     float *part;
     int splits, kb_per_split;
+    int a_rows;  // rows of A each fill brings (a multiple of 8 up to 128; the
+                 // MMA's other rows of the tile are not written out)
     void *y;
     int64_t ldy;
     const void *gamma;
@@ -1633,8 +1635,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            p.wait_limit_ns))
                 break;
             const uint32_t fb = smem_u32(&full[s]);
-            mbar_arrive_expect_tx(
-                fb, L.stage_bytes + (blockIdx.x == 0 && issued == p.stall_fill ? 16u : 0u));
+            mbar_arrive_expect_tx(fb, (uint32_t)(p.a_rows * kRowBytes + L.b_bytes) +
+                                          (blockIdx.x == 0 && issued == p.stall_fill ? 16u : 0u));
             const uint32_t sa = smem_u32(smem + s * L.stage_bytes);
             tma_load_2d(sa, &map_a, kb * BK, mblk * kBM, fb);
             tma_load_2d(sa + L.a_bytes, &map_w, kb * BK, n0, fb);

@@ -225,7 +225,7 @@ static cudaError_t launch_gemm_splitk(const GemmCall &c, cudaStream_t st) {
     using namespace gemm;
     const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
     CUtensorMap ma, mw;
-    if (!encode_map(&ma, c.a, c.T, c.K, c.lda, kBM, 64, bf16) ||
+    if (!encode_map(&ma, c.a, c.T, c.K, c.lda, c.T < kBM ? (int)((c.T + 7) / 8 * 8) : kBM, 64, bf16) ||
         !encode_map(&mw, c.w, c.H, c.K, c.ldw, kMmaN, 64, bf16))
         return cudaErrorInvalidValue;
     Params p{};
@@ -235,6 +235,10 @@ static cudaError_t launch_gemm_splitk(const GemmCall &c, cudaStream_t st) {
     p.ns = kMmaN;
     p.C = static_cast<int>(c.H / kMmaN);
     p.stages = 4;
+    // with one row block, each fill brings only the rows up to T (in 8-row
+    // units of the 128-byte swizzle; the MMA rows past them are never
+    // written out): T = 1 moves 1 KB of A per fill instead of 16
+    p.a_rows = c.T < kBM ? (int)((c.T + 7) / 8 * 8) : kBM;
     p.kblocks = static_cast<int>((c.K + 63) / 64);
     p.watchdog = c.watchdog;
     p.wait_limit_ns = c.wait_limit_ns;
