@@ -1781,6 +1781,78 @@ __global__ void __launch_bounds__(256) k_splitk_norm(NormParams q, const float *
     }
 }
 
+// The same for very few rows: a cluster of kSplitNormCS CTAs per row, CTA c
+// taking the row's packs [c P, (c + 1) P), P = H / 8 / kSplitNormCS, one per
+// thread; each CTA's sum of squares (block order) goes to its shared memory
+// and every CTA adds the cluster's in rank order (distributed shared memory)
+// before writing y.  With one row, one CTA would carry all of the row's
+// S x H partials alone.
+constexpr int kSplitNormCS = 8;
+
+template <typename T, int SMAX>
+__global__ void __launch_bounds__(256) k_splitk_norm_cluster(NormParams q, const float *part,
+                                                              int splits, void *residual) {
+    __shared__ float red[32];
+    __shared__ float seg_ss;
+    const uint32_t rank = cluster_rank();
+    const int64_t t = blockIdx.x / kSplitNormCS;
+    const int per = (int)(q.H / 8 / kSplitNormCS);  // packs per CTA
+    const int j = (int)rank * per + (int)threadIdx.x;
+    const bool act = (int)threadIdx.x < per;
+    grid_dependency_wait();
+    grid_launch_dependents();
+    T *res = reinterpret_cast<T *>(residual) + t * q.ldh;
+    uint4 hv = make_uint4(0u, 0u, 0u, 0u);
+    float ss = 0.f;
+    if (act) {
+        const float *src = part + t * q.H + (int64_t)j * 8;
+        Pack32 v[SMAX];
+#pragma unroll
+        for (int s = 0; s < SMAX; ++s)
+            if (s < splits) v[s] = ld_stream32(src + (int64_t)s * q.T * q.H);
+        float acc[8];
+        acc[0] = __uint_as_float(v[0].a.x), acc[1] = __uint_as_float(v[0].a.y);
+        acc[2] = __uint_as_float(v[0].a.z), acc[3] = __uint_as_float(v[0].a.w);
+        acc[4] = __uint_as_float(v[0].b.x), acc[5] = __uint_as_float(v[0].b.y);
+        acc[6] = __uint_as_float(v[0].b.z), acc[7] = __uint_as_float(v[0].b.w);
+#pragma unroll
+        for (int s = 1; s < SMAX; ++s) {
+            if (s < splits) {
+                acc[0] += __uint_as_float(v[s].a.x), acc[1] += __uint_as_float(v[s].a.y);
+                acc[2] += __uint_as_float(v[s].a.z), acc[3] += __uint_as_float(v[s].a.w);
+                acc[4] += __uint_as_float(v[s].b.x), acc[5] += __uint_as_float(v[s].b.y);
+                acc[6] += __uint_as_float(v[s].b.z), acc[7] += __uint_as_float(v[s].b.w);
+            }
+        }
+        float f[8];
+        DT<T>::unpack(ld_stream(res + (int64_t)j * 8), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            f[e] = DT<T>::round(acc[e] + f[e]);  // h: one rounding of P + r
+            ss += f[e] * f[e];
+        }
+        hv = DT<T>::pack(f);
+        st_global(res + (int64_t)j * 8, hv);
+    }
+    const float mine = block_sum(ss, red);
+    if (threadIdx.x == 0) seg_ss = mine;
+    cluster_sync();  // every CTA's sum is in its shared memory
+    float tot = 0.f;
+#pragma unroll
+    for (int c = 0; c < kSplitNormCS; ++c)
+        tot += __uint_as_float(ld_cluster_u32(map_to_rank(smem_u32(&seg_ss), (uint32_t)c)));
+    const float inv = rsqrtf(tot / (float)q.H + q.eps);
+    if (act) {
+        float f[8], w[8];
+        DT<T>::unpack(hv, f);
+        DT<T>::unpack(ld_keep(reinterpret_cast<const T *>(q.gamma) + (int64_t)j * 8), w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = (f[e] * inv) * w[e];
+        st_global(reinterpret_cast<T *>(q.y) + t * q.ldy + (int64_t)j * 8, DT<T>::pack(f));
+    }
+    cluster_sync();  // no CTA leaves while another still reads its sum
+}
+
 // Zeroes the row-block counters of the norm in the persistent kernels'
 // epilogue, after the previous kernel on the stream (which may be the previous
 // call's GEMM, still counting) has finished.  The GEMM may launch at once (its
