@@ -248,7 +248,7 @@ def test_gemm_pair_tail_halves(tune):
     (256, 4096, 4096, "bf16"),  # 2 row blocks x 16 column tiles x 4 splits
     (300, 2048, 1024, "f16"),   # 3 row blocks (the last ragged) x 8 tiles x 2 splits
     (512, 4096, 2048, "bf16"),  # 4 row blocks x 16 tiles x 2 splits
-    (3, 1024, 4096, "f16"),     # the split sum and norm on a cluster of 8 CTAs per row
+    (3, 4096, 2048, "f16"),     # the split sum and norm on a cluster of 8 CTAs per row
     (12, 8192, 2048, "bf16"),   # ... for up to 16 rows of 8192 columns
 ])
 def test_gemm_splitk(T, H, K, dt):
