@@ -209,11 +209,12 @@ static cudaError_t launch_splitk_norm(const gemm::NormParams &q, const GemmCall 
     const dim3 g2(static_cast<unsigned>(c.T));
     const float *part = static_cast<const float *>(c.part);
     // a cluster of CTAs per row for up to 8 rows of at least 4096 columns,
-    // or 16 of at least 8192 (measured, µs, split K + norm against a CTA per
+    // or 128 of at least 8192 (measured, µs, split K + norm against a CTA per
     // row: K = H = 4096 T = 1 8.1 -> 7.3, T = 8 8.2 -> 7.8, T = 16 8.2 ->
-    // 8.2-8.5; K = H = 8192 T = 1 30.1 -> 27.0, T = 16 30.7 -> 27.7;
-    // T = 1, H = 2048, K = 8192 8.7 -> 9.1)
-    if ((c.T <= 8 && c.H >= 4096) || (c.T <= 16 && c.H >= 8192)) {
+    // 8.2-8.5, T = 64 11.2 -> 11.1, T = 256 15.5 -> 17.9; K = H = 8192 T = 1
+    // 30.1 -> 27.0, T = 16 30.7 -> 27.7, T = 64 33.3 -> 32.1, T = 128 37.5
+    // -> 36.1; T = 1, H = 2048, K = 8192 8.7 -> 9.1)
+    if ((c.T <= 8 && c.H >= 4096) || (c.T <= 128 && c.H >= 8192)) {
         const int per = nv / kSplitNormCS;
         return launch_kernel(k_splitk_norm_cluster<T, SMAX>,
                              dim3(static_cast<unsigned>(c.T * kSplitNormCS)),
