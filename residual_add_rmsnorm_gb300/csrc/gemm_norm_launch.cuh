@@ -201,7 +201,9 @@ static cudaError_t launch_gemm_bk(const GemmCall &c, cudaStream_t st) {
                          c.pdl, 1, q);
 }
 
-// k_splitk_norm with registers for at most SMAX splits' partials (a CTA per row).
+// The split-K sum and norm with registers for at most SMAX splits' partials:
+// k_splitk_norm_cluster (a cluster of CTAs per row) for few wide rows, else
+// k_splitk_norm (a CTA per row).
 template <typename T, int SMAX>
 static cudaError_t launch_splitk_norm(const gemm::NormParams &q, const GemmCall &c, int nv,
                                       int used, cudaStream_t st) {
@@ -232,7 +234,8 @@ static cudaError_t launch_splitk_norm(const gemm::NormParams &q, const GemmCall 
 }
 
 // Split K (few row blocks): M x C x splits CTAs write binary32 partial products, then a
-// CTA per row sums them in split order, adds the residual and normalises.
+// CTA (or a cluster of CTAs) per row sums them in split order, adds the residual and
+// normalises.
 template <typename T>
 static cudaError_t launch_gemm_splitk(const GemmCall &c, cudaStream_t st) {
     using namespace gemm;
