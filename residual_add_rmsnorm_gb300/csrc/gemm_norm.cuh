@@ -26,7 +26,9 @@
 //   * K >= 1024 and so few 128 x 256 tiles that they leave half of the SMs
 //     idle (T <= 128 at H = 4096, up to 512 rows at H = 2048): k_gemm_splitk,
 //     M x C x S CTAs each multiplying a K range of one tile and writing
-//     binary32 partial products; k_splitk_norm sums them in split order, adds
+//     binary32 partial products; k_splitk_norm (a CTA per row, or
+//     k_splitk_norm_cluster, 8 per row, for few wide rows) sums them in
+//     split order, adds
 //     the residual and normalises.
 //   * K < 512: k_gemm_res, one CTA per [128 x NS] tile (NS = 256 or 512), the
 //     operand ring staging the epilogue: the residual tile arrives by TMA in
