@@ -24,12 +24,11 @@
 //   * K >= 512, 128 < T < 2048 (or T <= 128 with short K): k_gemm_res_ws,
 //     the same on one SM per 128 x 256 tile (M = 128 MMAs).
 //   * K >= 1024 and so few 128 x 256 tiles that they leave half of the SMs
-//     idle (T <= 128 at H = 4096, up to 512 rows at H = 2048): k_gemm_splitk,
+//     idle (up to 512 rows at H = 4096, 1152 at H = 2048): k_gemm_splitk,
 //     M x C x S CTAs each multiplying a K range of one tile and writing
 //     binary32 partial products; k_splitk_norm (a CTA per row, or
 //     k_splitk_norm_cluster, 8 per row, for few wide rows) sums them in
-//     split order, adds
-//     the residual and normalises.
+//     split order, adds the residual and normalises.
 //   * K < 512: k_gemm_res, one CTA per [128 x NS] tile (NS = 256 or 512), the
 //     operand ring staging the epilogue: the residual tile arrives by TMA in
 //     [128 x 32] chunks (64-byte swizzle), each thread adds its accumulator
