@@ -10,7 +10,9 @@
 // "Tokenweave fused-RMSNorm-AR kernel", Code walkthrough, for the norm steps).
 //
 // Blackwell mapping (sm_103a); the kernels of this file, by problem shape:
-//   * K >= 512, T >= 2048 (H <= 8192): k_gemm_res_pair, persistent on SM
+//   * K >= 512, T >= 2048 (H <= 8192; also fewer rows with K >= 2048 when
+//     one SM per 128 x 256 tile would need more than a round of the SMs):
+//     k_gemm_res_pair, persistent on SM
 //     pairs (two-CTA clusters, tcgen05.mma.cta_group::2 on 256 x 256 tiles;
 //     the last partial round as 128-column halves), warp-specialised: a TMA
 //     producer, one MMA-issuing thread, 8 epilogue warps per CTA draining one

@@ -176,10 +176,16 @@ inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
         g.smem = g.stages * stage + 3 * 1024;
         g.grid = std::min<int64_t>(g.grid, num_sms);
         // SM pairs (256-row tiles, each CTA staging half of the W slab) from
-        // 2048 rows; measured at K = H = 4096: T = 1024 30.4 us on one SM per
-        // tile against 34.8 on pairs, T = 2048 56.6 against 55.5, T = 4096
-        // 106.2 against 96.6
-        g.pair = pair_override == 1 || (pair_override != 0 && T >= 2048);
+        // 2048 rows, or, for K >= 2048, wherever one SM per 128-row tile
+        // would take more than one round of the SMs; measured (one SM per
+        // tile / pairs, us): K = H = 4096 T = 768 31.0 / 31.3, T = 1024
+        // 31.6 / 32.2, T = 1280 52.1 / 45.6, T = 1536 52.7 / 45.8, T = 1792
+        // 53.4 / 50.1, T = 2048 56.4 / 53.1; T = 1024, K = H = 8192
+        // 112.4 / 100.9; T = 1536, K = H = 5120 69.8 / 64.2; but T = 1200,
+        // H = 4096, K = 1024 23.9 / 27.1
+        g.pair = pair_override == 1 ||
+                 (pair_override != 0 &&
+                  (T >= 2048 || (K >= 2048 && ((T + 127) / 128) * g.tiles_n > num_sms)));
         if (g.pair) {
             // the pair kernel's ring: 3 stages of two K slabs, 64 KB each
             // (gemm_norm.cuh PairLayout, gemm_norm_launch.cuh)

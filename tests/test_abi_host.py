@@ -451,7 +451,11 @@ def test_plan_gemm(tune):
     assert "kblocks=64 persistent=1 pair=1" in p, p
     p = rarn.plan_gemm(2100, 512, 512)     # 9 x 2 pair tiles: 18 clusters
     assert "grid=36 " in p and "pair=1" in p, p
-    p = rarn.plan_gemm(1024, 4096, 4096)   # below 2048 rows: one SM per tile
+    p = rarn.plan_gemm(1024, 4096, 4096)   # below 2048 rows, one round of 128 tiles: one SM per tile
+    assert "persistent=1 pair=0" in p, p
+    p = rarn.plan_gemm(1536, 4096, 4096)   # 192 one-SM tiles, more than a round: pairs
+    assert "persistent=1 pair=1" in p, p
+    p = rarn.plan_gemm(1536, 4096, 1024)   # ... but not for K below 2048
     assert "persistent=1 pair=0" in p, p
     tune(gemm_pair=0)  # one CTA per SM walks 512 tiles of 128 x 256
     p = rarn.plan_gemm(4096, 4096, 4096)
