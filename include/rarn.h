@@ -571,7 +571,10 @@ typedef enum rarn_tuning {
     RARN_TUNE_GEMM_CTAS_PER_SM = 8, /* 1, 2: the non-persistent GEMM kernel */
     RARN_TUNE_GEMM_PERSISTENT = 9,  /* 0, 1: the persistent warp-specialised kernels */
     RARN_TUNE_GEMM_PAIR = 10,       /* 0, 1: SM pairs (cta_group::2) */
-    RARN_TUNE_GEMM_NORM_IN_EPILOGUE = 11, /* 0: y from a separate norm kernel */
+    RARN_TUNE_GEMM_NORM_IN_EPILOGUE = 11, /* 0: y from a separate norm kernel; 1: y in the
+                                             persistent kernels' epilogue wherever it can run
+                                             there (default: where K >= 3072, or K >= 2048
+                                             with T >= 4096) */
     RARN_TUNE_GEMM_TAIL_SPLIT = 12, /* 0: no 128-column halves in the last round */
     RARN_TUNE_GEMM_SPLIT_K = 13,    /* 0: no split K for few rows */
     RARN_TUNE_FP8IN_RING = 14,      /* 0: register kernels only; 1: the TMA-fed ring

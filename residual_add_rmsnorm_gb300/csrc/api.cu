@@ -99,9 +99,9 @@ bool tuning_value_ok(rarn_tuning k, long long x) {
     case RARN_TUNE_GEMM_CTAS_PER_SM: return x == 1 || x == 2;
     case RARN_TUNE_GEMM_PERSISTENT:
     case RARN_TUNE_GEMM_PAIR:
+    case RARN_TUNE_GEMM_NORM_IN_EPILOGUE:
     case RARN_TUNE_FP8IN_RING: return x == 0 || x == 1;
     case RARN_TUNE_ROWS_PIPELINE:
-    case RARN_TUNE_GEMM_NORM_IN_EPILOGUE:
     case RARN_TUNE_GEMM_TAIL_SPLIT:
     case RARN_TUNE_GEMM_SPLIT_K:
     case RARN_TUNE_FP8IN_PACK16: return x == 0;
@@ -943,9 +943,10 @@ static rarn_status gemm_launch(const rarn_rows &y, const rarn_rows &a, const rar
     c.pair = gp.pair;
     c.splitk = gp.splitk;
     c.part = gp.splitk ? static_cast<float *>(workspace) + gemm_splitk_offset(T, H) : nullptr;
-    // allowed unless switched off by a tuning knob; the launcher decides both
-    // against the clusters that fit on this GPU
-    c.fuse_norm = g_tune[RARN_TUNE_GEMM_NORM_IN_EPILOGUE] != 0;
+    // y in the epilogue where the planner picks it (long K, or a knob); the
+    // launcher confirms it, and the tail split, against the clusters that
+    // fit on this GPU
+    c.fuse_norm = gp.fuse_norm;
     c.tail_split = g_tune[RARN_TUNE_GEMM_TAIL_SPLIT] != 0;
     c.wait_limit_ns = 2000000000ull;
     c.stall_fill = -1;

@@ -194,12 +194,20 @@ inline GemmPlan plan_gemm(int64_t T, int64_t H, int64_t K, int bk_override = 0,
             g.smem = g.stages * 2 * half + 4 * 1024;
             g.grid = 2 * std::min<int64_t>(((T + 255) / 256) * g.tiles_n, num_sms / 2);
         }
+        // y in the epilogue only where the main loop is long enough to hide
+        // it; with short K a separate norm kernel costs less (y separate /
+        // in the epilogue, us): K = H = 4096 T = 4096 K = 4096 94.0 / 88.6,
+        // K = 3072 75.3 / 71.6, K = 1024 43.5 / 49.8, K = 512 39.0 / 45.8;
+        // T = 2048, K = 3072 43.2 / 41.7, K = 2048 34.1 / 35.0; T = 8192,
+        // K = 2048 108.2 / 104.2; T = 1536, K = 1024 23.0 / 27.4
+        const bool fuse_wanted =
+            fuse_override == 1 || (fuse_override == -1 && (K >= 3072 || (K >= 2048 && T >= 4096)));
         if (g.pair) {
             const PairSchedule ps = pair_schedule(T, g.tiles_n, num_sms / 2, split_override != 0);
             g.tail_split = ps.items != ps.full_items;
-            g.fuse_norm = fuse_override != 0 && ps.fuse_ok;
+            g.fuse_norm = fuse_wanted && ps.fuse_ok;
         } else {
-            g.fuse_norm = fuse_override != 0 && single_fuse_ok(T, g.tiles_n, num_sms);
+            g.fuse_norm = fuse_wanted && single_fuse_ok(T, g.tiles_n, num_sms);
         }
     }
     return g;

@@ -506,14 +506,14 @@ TUNING_OK = {
     "rows_pipeline": [0], "l2_rows": list(range(9)), "stream_packs": [1, 2, 4],
     "stream_groups": [1, 2], "gemm_cols": [256, 512], "gemm_slab": [32, 64],
     "gemm_ctas_per_sm": [1, 2], "gemm_persistent": [0, 1], "gemm_pair": [0, 1],
-    "gemm_norm_in_epilogue": [0], "gemm_tail_split": [0], "gemm_split_k": [0],
+    "gemm_norm_in_epilogue": [0, 1], "gemm_tail_split": [0], "gemm_split_k": [0],
     "fp8in_ring": [0, 1], "fp8in_pack16": [0],
 }
 TUNING_BAD = {
     "rows_per_thread": [0, 3, 32], "rows_grid": [0, 2 ** 31], "rows_pipeline": [1, -2],
     "l2_rows": [9, -2], "stream_packs": [0, 3, 8], "stream_groups": [0, 3],
     "gemm_cols": [128, 384], "gemm_slab": [16, 128], "gemm_ctas_per_sm": [0, 3],
-    "gemm_persistent": [2], "gemm_pair": [2], "gemm_norm_in_epilogue": [1],
+    "gemm_persistent": [2], "gemm_pair": [2], "gemm_norm_in_epilogue": [2],
     "gemm_tail_split": [1], "gemm_split_k": [1, 9], "fp8in_ring": [2], "fp8in_pack16": [1],
 }
 

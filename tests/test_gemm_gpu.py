@@ -191,17 +191,17 @@ def test_gemm_norm_in_epilogue_matches_norm_kernel(pair, tune):
         r0 = torch.randn(T, H, device="cuda", generator=gen).to(torch.bfloat16)
         g = (torch.rand(H, device="cuda", generator=gen) + 0.5).to(torch.bfloat16)
         outs = {}
-        for fuse in (-1, 0):
+        for fuse in (1, 0):
             tune(gemm_norm_in_epilogue=fuse)
             plan = rarn.plan_gemm(T, H, K)
-            assert ("norm in epilogue" in plan) == (fuse == -1), plan
+            assert ("norm in epilogue" in plan) == (fuse == 1), plan
             r = r0.clone()
             y = rarn.gemm_add_rms_norm(a, w, r, g, 1e-6)
             torch.cuda.synchronize()
             assert rarn.watchdog(clear=True) == 0
             outs[fuse] = (y, r)
-        assert torch.equal(outs[-1][0], outs[0][0]), f"y differs at T{T} H{H} K{K}"
-        assert torch.equal(outs[-1][1], outs[0][1]), f"residual differs at T{T} H{H} K{K}"
+        assert torch.equal(outs[1][0], outs[0][0]), f"y differs at T{T} H{H} K{K}"
+        assert torch.equal(outs[1][1], outs[0][1]), f"residual differs at T{T} H{H} K{K}"
 
 
 def test_gemm_pair_tail_halves(tune):

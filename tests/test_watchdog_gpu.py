@@ -50,7 +50,8 @@ def test_gemm_wait_runs_out_and_is_reported(K, fill, pair, T, tune):
     memory, the watchdog bit is set, and the next call is correct."""
     import torch
     if pair is not None:
-        tune(gemm_pair=pair, gemm_split_k=0)  # the persistent kernels, not split K
+        # the persistent kernels, not split K, with y in their epilogue
+        tune(gemm_pair=pair, gemm_split_k=0, gemm_norm_in_epilogue=1)
     H = 2048
     gen = torch.Generator(device="cuda").manual_seed(K + fill)
     a = torch.randn(T, K, device="cuda", generator=gen).to(torch.bfloat16)
