@@ -308,7 +308,8 @@ rarn_status rarn_reduce_add_rms_norm_fp8in(void *y, const void *partials, int32_
  * Kernels on `stream`: the tcgen05 GEMM whose epilogue writes h and, per row
  * and column block (128 columns in the persistent kernels, one tile of 256
  * or 512 otherwise), the partial sum of squares of h into `workspace`.  With
- * K >= 512 (the persistent kernels) the same epilogue then waits for the
+ * K >= 3072, or K >= 2048 and T >= 4096 (in the persistent kernels, K >=
+ * 512; RARN_TUNE_GEMM_NORM_IN_EPILOGUE overrides) the same epilogue then waits for the
  * other column tiles of its 128-row block (a counter per block in the
  * workspace, zeroed by a one-CTA kernel launched just before), sums each
  * row's partials in column order and writes y; otherwise a norm kernel does

@@ -21,7 +21,8 @@
 //     sums of squares (adding to its 128-row block's counter, which
 //     k_zero_counters zeroes first), writes h, and once the counter shows
 //     every column writes y -- for a tile whose row block ends in the next
-//     round of tiles, during the pair's next tile.  The epilogue's streams
+//     round of tiles, during the pair's next tile.  (Where K is short,
+//     k_norm_ss writes y after the kernel instead.)  The epilogue's streams
 //     (residual in, h and y out) carry an L2 evict-first policy.
 //   * K >= 512, 128 < T < 2048 (or T <= 128 with short K): k_gemm_res_ws,
 //     the same on one SM per 128 x 256 tile (M = 128 MMAs).
