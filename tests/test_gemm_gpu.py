@@ -137,7 +137,21 @@ def test_gemm_parity(T, H, K, dt):
     splitk = H <= 8192 and min(9, 152 // tiles, -(-K // 64) // 8) >= 2
     assert ("splitk=" in plan) == splitk, plan
     assert ("persistent=1" in plan) == (H <= 8192 and K >= 512 and not splitk), plan
-    assert ("pair=1" in plan) == (H <= 8192 and K >= 512 and T >= 2048), plan
+    pair = H <= 8192 and K >= 512 and not splitk and (
+        T >= 2048 or (K >= 2048 and -(-T // 128) * (H // 256) > 152))
+    assert ("pair=1" in plan) == pair, plan
+
+
+@pytest.mark.parametrize("T,H,K,fused", [
+    (1280, 4096, 2048, False),   # pairs below 2048 rows (160 one-SM tiles), y by the norm kernel
+    (1536, 5120, 3072, True),    # ... with y in the epilogue (K >= 3072)
+])
+def test_gemm_mid_rows_on_pairs(T, H, K, fused):
+    """The planner's SM pairs where one SM per 128-row tile would need more
+    than one round of the SMs, and its choice of where y is formed; sampled
+    rows against the oracle."""
+    plan = run_case(T, H, K, "bf16", seed=T + K, sample_rows=np.arange(0, T, 13))
+    assert "pair=1" in plan and ("norm in epilogue" in plan) == fused, plan
 
 
 @pytest.mark.parametrize("ns,bk,ctas", [(256, 32, 2), (256, 64, 2), (256, 64, 1), (512, 32, 1),
