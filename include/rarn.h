@@ -349,8 +349,9 @@ rarn_status rarn_gemm_add_rms_norm(rarn_rows y, rarn_rows a, rarn_rows w, rarn_r
  * that owns every byte of device memory and hands out no allocator, runtimes
  * that plan all memory before they start serving and forbid allocation
  * afterwards, and latency-critical code that cannot afford the implicit
- * device synchronisation of cudaMalloc / cudaFree.  The paper has no
- * counterpart.
+ * device synchronisation of cudaMalloc / cudaFree.  None of the source
+ * pages ("RMSNorm kernel", "Tokenweave fused-RMSNorm-AR kernel", "sm80 GEMM
+ * + ReduceScatter") has a counterpart.
  *
  * Scratch: the per-row partial sums of squares and the row-block counters
  * live in a file-scope device array of 2^20 binary32 values (4 MiB, 256-byte

@@ -1302,7 +1302,7 @@ __device__ __forceinline__ int pair_epilogue(const Params &p, void *residual, in
     if (live) er.store_h(res);
     if (!p.counters) return 1;
     if (pend.m0 >= 0) {
-        // the deferred whole item: its row block ended in this round
+        // the deferred whole item: its row block ended in this round of tiles
         if (!block_inv(p, pend.m0, half_ss, norm_ok, abort_flag)) return 0;
         const int64_t tp = pend.m0 + row;
         if (tp < p.T) {
