@@ -457,6 +457,17 @@ def test_plan_gemm(tune):
     assert "persistent=1 pair=1" in p, p
     p = rarn.plan_gemm(1536, 4096, 1024)   # ... but not for K below 2048
     assert "persistent=1 pair=0" in p, p
+    # y in the epilogue where K >= 3072, or K >= 2048 with T >= 4096; else the
+    # norm kernel after the GEMM
+    for T, K, fused in ((4096, 4096, True), (4096, 3072, True), (4096, 2048, True),
+                        (2048, 2048, False), (4096, 1024, False), (1536, 3072, True)):
+        p = rarn.plan_gemm(T, 4096, K)
+        assert ("norm in epilogue" in p) == fused and ("+ norm" in p) != fused, (T, K, p)
+    tune(gemm_norm_in_epilogue=1)
+    assert "norm in epilogue" in rarn.plan_gemm(4096, 4096, 1024)
+    tune(gemm_norm_in_epilogue=0)
+    assert "+ norm" in rarn.plan_gemm(4096, 4096, 4096)
+    tune(gemm_norm_in_epilogue=-1)
     tune(gemm_pair=0)  # one CTA per SM walks 512 tiles of 128 x 256
     p = rarn.plan_gemm(4096, 4096, 4096)
     assert "cols_per_cta=256 col_tiles=16 bk=64 stages=4" in p and "grid=152" in p, p
