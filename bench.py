@@ -744,7 +744,7 @@ def time_tp(device, rarn, N=8, T=8192, H=8192, sampler=None, hold_s=0.0):
             "us_per_launch": us, "gbs": gbs, "rows_per_s": T / (us / 1e6),
             "frac_of_peak": gbs / peak, "algorithmic_bytes": alg, "ranks": N,
             "timing": "CUDA graph of 10 launches, best of 3 (inputs larger than L2)",
-            "plan": f"tp.world ranks={N} barrier=signal pads"}
+            "plan": rarn.plan_tp(T, H, N, "bf16", True, 0, 0) + " barrier=signal pads"}
 
 
 def fp8in_tensors(device, R=8, T=8192, H=8192):
@@ -860,7 +860,7 @@ def main_tp(args, device, rank, world):
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": TP_NAME, "ranks": N, "T": T, "H": H, "storage": "bf16",
-                   "plan": f"tp.world ranks={N} barrier=signal pads",
+                   "plan": rarn.plan_tp(T, H, N, "bf16", True, 0, 0) + " barrier=signal pads",
                    "l2": "inputs larger than L2 (1.2 GB)", "pdl": not args.no_pdl,
                    "note": "the N ranks' buffers are on this one GPU: no NVLink traffic"},
         "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": peak, "unit": "GB/s",

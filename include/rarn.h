@@ -471,6 +471,27 @@ typedef struct rarn_tp_group {
  * RARN_ERR_INVALID_ARG for T < 0, N < 1, r outside 0 .. N-1 or NULL outputs. */
 rarn_status rarn_tp_rows(int64_t T, int32_t world_size, int32_t rank, int64_t *r0, int64_t *r1);
 
+/* The launch a tensor-parallel call of T rows of H elements over N ranks
+ * makes (world != 0: every rank's part in one launch, as
+ * rarn_tp_reduce_add_rms_norm_world; 0: one rank's, as
+ * rarn_tp_reduce_add_rms_norm) on a device with num_sms SMs (<= 0: the
+ * current device's) that holds blocks_per_sm CTAs of the kernel per SM (<= 0:
+ * the current device's occupancy for H and dt).  Writes a NUL-terminated
+ * description into out[cap]: "tp.world ranks=N ctas=C block=B vpt=V
+ * blocks_per_sm=P prefetch=F" ("tp.rank ..." for one rank), C CTAs per rank
+ * of B threads, V 16-byte packs per thread, F = 1 when each CTA prefetches
+ * its next row's streams into L2 while it works on the current one: where
+ * the loads an SM holds in flight, P (N + 1) rows of H elements, come to at
+ * most 64 KB, or 80 KB with one CTA per SM (RARN_TUNE_TP_PREFETCH
+ * overrides).  The prefetch is only issued for streams in memory of the
+ * launching device.  Pure host logic when num_sms and blocks_per_sm are
+ * given.  Errors: NULL out, cap 0, T <= 0, H <= 0, N outside 1 ..
+ * RARN_TP_MAX_RANKS, an unknown dt: RARN_ERR_INVALID_ARG; rows that the call
+ * rejects as unsupported: RARN_ERR_UNSUPPORTED (out says so); a failed
+ * device query: RARN_ERR_CUDA. */
+rarn_status rarn_plan_tp(int64_t T, int64_t H, int32_t world_size, rarn_dtype dt, int world,
+                         int32_t num_sms, int32_t blocks_per_sm, char *out, size_t cap);
+
 /* This rank's part: `residual` holds this rank's rows of the residual
  * ([r1 - r0, H], dense, updated in place); gamma [H]. */
 rarn_status rarn_tp_reduce_add_rms_norm(const rarn_tp_group *group, void *residual,
@@ -582,7 +603,10 @@ typedef enum rarn_tuning {
     RARN_TUNE_FP8IN_RING = 14,      /* 0: register kernels only; 1: the TMA-fed ring
                                        kernel wherever the shape allows it */
     RARN_TUNE_FP8IN_PACK16 = 15,    /* 0: 8-element packs in the register kernels */
-    RARN_TUNE_COUNT = 16
+    RARN_TUNE_TP_PREFETCH = 16,     /* 0, 1: whether each CTA of the tensor-parallel form
+                                       prefetches its next row into L2 (only streams in
+                                       memory of the current device) */
+    RARN_TUNE_COUNT = 17
 } rarn_tuning;
 
 /* Set one knob (-1 restores the planner's choice).  An unknown knob or a

@@ -28,7 +28,7 @@ __all__ = ["rms_norm", "fused_add_rms_norm", "reduce_add_rms_norm", "rms_norm_ho
            "set_path", "get_path", "set_pdl", "get_pdl", "plan", "watchdog", "PATHS",
            "DTYPE_CODES", "rms_norm_ex", "fused_add_rms_norm_ex", "reduce_add_rms_norm_ex",
            "rms_norm_fp8", "fused_add_rms_norm_fp8", "reduce_add_rms_norm_fp8", "plan_fp8",
-           "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm", "plan_fp8in",
+           "FP8_FORMATS", "SCALE_MODES", "gemm_add_rms_norm", "plan_gemm", "plan_fp8in", "plan_tp",
            "gemm_workspace_bytes", "gemm_add_rms_norm_noalloc", "reduce_add_rms_norm_fp8in",
            "TUNING", "set_tuning", "get_tuning", "reset_tuning", "tuning", "gemm_noalloc_rows",
            "launch_floor", "tp_rows", "tp_reduce_add_rms_norm", "tp_reduce_add_rms_norm_world",
@@ -48,7 +48,7 @@ TUNING = {"rows_per_thread": 0, "rows_grid": 1, "rows_pipeline": 2, "l2_rows": 3
           "stream_packs": 4, "stream_groups": 5, "gemm_cols": 6, "gemm_slab": 7,
           "gemm_ctas_per_sm": 8, "gemm_persistent": 9, "gemm_pair": 10,
           "gemm_norm_in_epilogue": 11, "gemm_tail_split": 12, "gemm_split_k": 13,
-          "fp8in_ring": 14, "fp8in_pack16": 15}
+          "fp8in_ring": 14, "fp8in_pack16": 15, "tp_prefetch": 16}
 STATUS = {0: "RARN_OK", 1: "RARN_ERR_INVALID_ARG", 2: "RARN_ERR_UNSUPPORTED",
           3: "RARN_ERR_ALIAS", 4: "RARN_ERR_CUDA"}
 
@@ -170,6 +170,9 @@ def library() -> ctypes.CDLL:
     lib.rarn_plan_fp8in.argtypes = [i64, i64, ctypes.c_int32, c_int, c_int, ctypes.c_int32,
                                     ctypes.c_int32, ctypes.c_char_p, ctypes.c_size_t]
     lib.rarn_plan_fp8in.restype = c_int
+    lib.rarn_plan_tp.argtypes = [i64, i64, ctypes.c_int32, c_int, c_int, ctypes.c_int32,
+                                 ctypes.c_int32, ctypes.c_char_p, ctypes.c_size_t]
+    lib.rarn_plan_tp.restype = c_int
     lib.rarn_set_pdl.argtypes = [c_int]
     lib.rarn_set_pdl.restype = c_int
     lib.rarn_get_pdl.argtypes = []
@@ -657,6 +660,20 @@ def plan_fp8in(T: int, H: int, R: int, dtype: str = "bf16", codes_aligned16: boo
                                    max_smem, buf, 256)
     if st not in (0, 2):
         _check(st, "rarn_plan_fp8in")
+    return buf.value.decode()
+
+
+def plan_tp(T: int, H: int, N: int, dtype: str = "bf16", world: bool = True, num_sms: int = 152,
+            blocks_per_sm: int = 0) -> str:
+    """The launch a tensor-parallel call over N ranks makes (``world``: every
+    rank's part in one launch) on a device with ``num_sms`` SMs that holds
+    ``blocks_per_sm`` CTAs of the kernel per SM; 0 for either queries the
+    current device (host logic only when both are given)."""
+    buf = ctypes.create_string_buffer(256)
+    st = library().rarn_plan_tp(T, H, N, DTYPE_CODES[dtype], int(world), num_sms, blocks_per_sm,
+                                buf, 256)
+    if st not in (0, 2):
+        _check(st, "rarn_plan_tp")
     return buf.value.decode()
 
 

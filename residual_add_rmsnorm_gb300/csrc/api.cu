@@ -100,7 +100,8 @@ bool tuning_value_ok(rarn_tuning k, long long x) {
     case RARN_TUNE_GEMM_PERSISTENT:
     case RARN_TUNE_GEMM_PAIR:
     case RARN_TUNE_GEMM_NORM_IN_EPILOGUE:
-    case RARN_TUNE_FP8IN_RING: return x == 0 || x == 1;
+    case RARN_TUNE_FP8IN_RING:
+    case RARN_TUNE_TP_PREFETCH: return x == 0 || x == 1;
     case RARN_TUNE_ROWS_PIPELINE:
     case RARN_TUNE_GEMM_TAIL_SPLIT:
     case RARN_TUNE_GEMM_SPLIT_K:
@@ -1294,6 +1295,47 @@ rarn_status rarn_tp_rows(int64_t T, int32_t world_size, int32_t rank, int64_t *r
     return RARN_OK;
 }
 
+// Whether the tensor-parallel kernel prefetches each CTA's next row into L2:
+// the knob, else tp::prefetch_wanted.
+static bool tp_prefetch(int per_sm, int N, int64_t row_bytes) {
+    const long long f = g_tune[RARN_TUNE_TP_PREFETCH];
+    return f >= 0 ? f != 0 : tp::prefetch_wanted(per_sm, N, row_bytes);
+}
+
+rarn_status rarn_plan_tp(int64_t T, int64_t H, int32_t world_size, rarn_dtype dt, int world,
+                         int32_t num_sms, int32_t blocks_per_sm, char *out, size_t cap) {
+    if (!out || cap == 0) return RARN_ERR_INVALID_ARG;
+    if (!dtype_ok(dt) || T <= 0 || H <= 0 || world_size < 1 || world_size > RARN_TP_MAX_RANKS)
+        return RARN_ERR_INVALID_ARG;
+    const int s = elem_size(dt);
+    if ((H * s) % 16 || H * s / 16 > tp::kMaxPacks) {
+        snprintf(out, cap, "none: rows of H * sizeof(dt) bytes must be 16-byte packs, at most %d",
+                 tp::kMaxPacks);
+        return RARN_ERR_UNSUPPORTED;
+    }
+    if (num_sms <= 0) {
+        DeviceInfo *d = nullptr;
+        const rarn_status st = device_info(&d);
+        if (st != RARN_OK) return st;
+        num_sms = d->num_sms;
+    }
+    if (blocks_per_sm <= 0) {
+        const cudaError_t e = dt == RARN_BF16 ? tp_blocks_per_sm<__nv_bfloat16>(H, &blocks_per_sm)
+                              : dt == RARN_F16 ? tp_blocks_per_sm<__half>(H, &blocks_per_sm)
+                                               : tp_blocks_per_sm<float>(H, &blocks_per_sm);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (blocks_per_sm < 1) return RARN_ERR_UNSUPPORTED;
+    }
+    int vpt = 0, block = 0;
+    tp::tp_shape(H * s / 16, vpt, block);
+    const int N = world_size;
+    const int ctas = tp::ctas_per_rank(T, N, num_sms, blocks_per_sm, world != 0);
+    snprintf(out, cap, "tp.%s ranks=%d ctas=%d block=%d vpt=%d blocks_per_sm=%d prefetch=%d",
+             world ? "world" : "rank", N, ctas, block, vpt, blocks_per_sm,
+             tp_prefetch(blocks_per_sm, N, H * s) ? 1 : 0);
+    return RARN_OK;
+}
+
 // Checks of a tensor-parallel call (every rank's in the world launch, else
 // group->rank's): before any CUDA call.
 static rarn_status tp_check(const rarn_tp_group *g, void *const *residuals, const void *gamma,
@@ -1344,6 +1386,31 @@ static rarn_status tp_check(const rarn_tp_group *g, void *const *residuals, cons
     return RARN_OK;
 }
 
+// Bit q: rank q's buffer, bit 8 + q: rank q's residual, for the streams that
+// are memory of the current device (the prefetch is only issued for those).
+static uint32_t tp_local_mask(const tp::Params &p, int N) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0u;
+    }
+    auto local = [dev](const void *ptr) {
+        if (!ptr) return false;
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+            cudaGetLastError();  // not a sticky error: clear it
+            return false;
+        }
+        return a.type == cudaMemoryTypeDevice && a.device == dev;
+    };
+    uint32_t m = 0;
+    for (int q = 0; q < N; ++q) {
+        if (local(p.bufs[q])) m |= 1u << q;
+        if (local(p.residual[q])) m |= 1u << (8 + q);
+    }
+    return m;
+}
+
 static rarn_status tp_run(const rarn_tp_group *g, void *const *residuals, const void *gamma,
                           int64_t T, int64_t H, float eps, rarn_dtype dt, void *stream,
                           bool world) {
@@ -1375,14 +1442,7 @@ static rarn_status tp_run(const rarn_tp_group *g, void *const *residuals, const 
                                      : tp_blocks_per_sm<float>(H, &per_sm);
     if (e != cudaSuccess) return cuda_fail(e);
     if (per_sm < 1) return RARN_ERR_UNSUPPORTED;
-    // CTAs per rank: every CTA of a rank resident at once (a CTA waits on its
-    // counterparts only), all ranks' in the one grid of the world launch; the
-    // rows of the largest block spread evenly; the same on every rank
-    const int64_t rows_max = (T + N - 1) / N;
-    int64_t slots = (int64_t)d->num_sms * per_sm / (world ? N : 1);
-    slots = std::max<int64_t>(1, std::min<int64_t>(slots, tp::kMaxCtas));
-    const int64_t rounds = ceil_div(rows_max, slots);
-    const int ctas = (int)std::max<int64_t>(1, ceil_div(rows_max, rounds));
+    const int ctas = tp::ctas_per_rank(T, N, d->num_sms, per_sm, world);
     tp::Params p{};
     const bool sync = g->signals[0] != nullptr;
     for (int q = 0; q < N; ++q) {
@@ -1400,6 +1460,8 @@ static rarn_status tp_run(const rarn_tp_group *g, void *const *residuals, const 
     p.watchdog = d->watchdog;
     p.wait_limit_ns = tp::kWaitLimitNs;
     p.stall_rank = -1;
+    p.prefetch_mask =
+        tp_prefetch(per_sm, N, H * elem_size(dt)) ? tp_local_mask(p, N) : 0u;
     if (sync) {
         const long long f = g_stall_fill.exchange(-1);
         if (f >= 0) {

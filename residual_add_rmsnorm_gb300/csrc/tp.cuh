@@ -43,6 +43,10 @@ struct Params {
     unsigned int *watchdog;
     unsigned long long wait_limit_ns;  // bound on every barrier wait
     int stall_rank;  // test hook: this rank's CTA 0 never signals at entry (-1: off)
+    // streams whose next row a CTA prefetches into L2 while it works on the
+    // current one: bit q rank q's buffer, bit 8 + q rank q's residual; set
+    // only for memory of the launching device
+    uint32_t prefetch_mask;
 };
 
 // Rows [r0, r1) of rank r among N.
@@ -139,6 +143,19 @@ __global__ void __launch_bounds__(512) k_tp_rows(Params p) {
         T *res = reinterpret_cast<T *>(p.residual[rank]);
         int par = 0;
         for (int64_t t = r0 + b; t < r1; t += p.ctas, par ^= 1) {
+            // this CTA's next row into L2, one bulk prefetch per stream: one
+            // CTA of 512 threads per SM holds one row in registers, so with
+            // few ranks it has few loads in flight
+            const int64_t tn = t + p.ctas;
+            if (tn < r1 && (int)threadIdx.x <= p.N) {
+                const uint32_t rb = (uint32_t)(p.H * (int64_t)sizeof(T));
+                if ((int)threadIdx.x < p.N) {
+                    if ((p.prefetch_mask >> threadIdx.x) & 1u)
+                        prefetch_l2(reinterpret_cast<const T *>(p.bufs[threadIdx.x]) + tn * p.H, rb);
+                } else if ((p.prefetch_mask >> (8 + rank)) & 1u) {
+                    prefetch_l2(res + (tn - r0) * p.H, rb);
+                }
+            }
             // the residual row first: its loads are in flight with the
             // ranks' (8 ranks, [8192, 8192] on one GPU: 459.5 -> 372.5 us;
             // 4 ranks 292.7 -> 228.4; 2 ranks on [16384, 8192] 408 -> 306)
@@ -230,6 +247,36 @@ __global__ void __launch_bounds__(512) k_tp_rows(Params p) {
 inline void tp_shape(int64_t nv, int &vpt, int &block) {
     vpt = nv <= 512 ? 1 : nv <= 1024 ? 2 : 4;
     block = (int)(((nv + vpt - 1) / vpt + 31) / 32 * 32);
+}
+
+// CTAs per rank (T > 0): every CTA of a rank resident at once (a CTA waits
+// on its counterparts only), all ranks' in the one grid of the world launch;
+// the rows of the largest block spread evenly; the same on every rank.
+inline int ctas_per_rank(int64_t T, int N, int num_sms, int per_sm, bool world) {
+    const int64_t rows_max = (T + N - 1) / N;
+    int64_t slots = (int64_t)num_sms * per_sm / (world ? N : 1);
+    if (slots > kMaxCtas) slots = kMaxCtas;
+    if (slots < 1) slots = 1;
+    const int64_t rounds = (rows_max + slots - 1) / slots;
+    const int64_t c = (rows_max + rounds - 1) / rounds;
+    return c < 1 ? 1 : (int)c;
+}
+
+// Whether each CTA prefetches its next row into L2.  A CTA holds its row's
+// N + 1 loads (the residual and the N ranks', each a row of row_bytes) in
+// flight before it reduces, so an SM has per_sm (N + 1) rows of loads out.
+// Measured on a GB300, eight to two ranks' buffers on one GPU, prefetch off
+// -> on: with one CTA per SM a gain up to 64 KB in flight (bf16 H = 8192, two
+// ranks 160.5 -> 125.7 us; H = 5120, four ranks 188.5 -> 148.8; H = 8192,
+// three ranks 194.4 -> 170.5), mostly a gain at 80 KB (four ranks at H =
+// 8192: bf16 228.9 -> 214.0, f16 220.6 -> 213.0; f32 H = 4096 211.3 ->
+// 213.2), a loss from 96 KB (eight ranks at H = 8192: 378 -> 436; f32 H =
+// 8192, two ranks 244.4 -> 257.2); with two or four CTAs per SM a gain at
+// 48 KB (bf16 H = 4096, two ranks 77.0 -> 71.2), none at 64 KB and a loss at
+// 80 KB (H = 4096, four ranks 110.6 -> 117.8; H = 2048 111.0 -> 120.5).
+inline bool prefetch_wanted(int per_sm, int N, int64_t row_bytes) {
+    const int64_t inflight = (int64_t)per_sm * (N + 1) * row_bytes;
+    return inflight <= 64 * 1024 || (per_sm == 1 && inflight <= 80 * 1024);
 }
 
 }  // namespace tp

@@ -518,7 +518,7 @@ TUNING_OK = {
     "stream_groups": [1, 2], "gemm_cols": [256, 512], "gemm_slab": [32, 64],
     "gemm_ctas_per_sm": [1, 2], "gemm_persistent": [0, 1], "gemm_pair": [0, 1],
     "gemm_norm_in_epilogue": [0, 1], "gemm_tail_split": [0], "gemm_split_k": [0],
-    "fp8in_ring": [0, 1], "fp8in_pack16": [0],
+    "fp8in_ring": [0, 1], "fp8in_pack16": [0], "tp_prefetch": [0, 1],
 }
 TUNING_BAD = {
     "rows_per_thread": [0, 3, 32], "rows_grid": [0, 2 ** 31], "rows_pipeline": [1, -2],
@@ -526,6 +526,7 @@ TUNING_BAD = {
     "gemm_cols": [128, 384], "gemm_slab": [16, 128], "gemm_ctas_per_sm": [0, 3],
     "gemm_persistent": [2], "gemm_pair": [2], "gemm_norm_in_epilogue": [2],
     "gemm_tail_split": [1], "gemm_split_k": [1, 9], "fp8in_ring": [2], "fp8in_pack16": [1],
+    "tp_prefetch": [2, -2],
 }
 
 
@@ -534,7 +535,7 @@ def test_tuning_knobs_validated(lib):
     everything else (status INVALID, the knob unchanged), and
     rarn_reset_tuning puts every knob back to -1."""
     assert set(TUNING_OK) == set(rarn.TUNING) == set(TUNING_BAD)
-    assert sorted(rarn.TUNING.values()) == list(range(16))
+    assert sorted(rarn.TUNING.values()) == list(range(17))
     rarn.reset_tuning()
     try:
         for name, good in TUNING_OK.items():
@@ -551,9 +552,9 @@ def test_tuning_knobs_validated(lib):
                 assert rarn.get_tuning(name) == keep, name
             rarn.set_tuning(name, -1)
         v = ctypes.c_int64(0)
-        assert lib.rarn_set_tuning(16, 0) == INVALID   # no such knob
+        assert lib.rarn_set_tuning(17, 0) == INVALID   # no such knob
         assert lib.rarn_set_tuning(-1, 0) == INVALID
-        assert lib.rarn_get_tuning(16, ctypes.byref(v)) == INVALID
+        assert lib.rarn_get_tuning(17, ctypes.byref(v)) == INVALID
         assert lib.rarn_get_tuning(0, None) == INVALID
         rarn.set_tuning("gemm_pair", 0)
         rarn.set_tuning("rows_grid", 7)

@@ -84,6 +84,50 @@ def test_tp_world_matches_oracle(N, T, H, dt, signals):
             assert int(p.abs().sum()) == 0
 
 
+@pytest.mark.parametrize("prefetch", [0, 1])
+@pytest.mark.parametrize("N,T,H,dt,signals", [
+    (2, 2048, 8192, "bf16", True),    # 14 rows per CTA
+    (2, 2047, 5120, "bf16", False),   # ragged: rank 0 owns 1023 rows, rank 1 1024
+    (4, 4000, 4096, "f32", True),
+    (1, 1500, 2048, "f16", False),
+    (8, 3000, 8192, "bf16", True),
+])
+def test_tp_next_row_prefetch(N, T, H, dt, signals, prefetch, tune):
+    """Each CTA works through many rows with the next-row L2 prefetch forced
+    off and on: the same results as the oracle either way (the prefetch only
+    moves data into L2 earlier)."""
+    import torch
+    tune(tp_prefetch=prefetch)
+    plan = rarn.plan_tp(T, H, N, dt, True, 0, 0)
+    assert f"prefetch={prefetch}" in plan, plan
+    d = _inputs(N, T, H, dt, seed=31 + N + T)
+    ref = oracle.tp_reduce_add_rms_norm([d["partials"][q] for q in range(N)], d["residual"],
+                                        d["gamma"], EPS, dt)
+    bufs, res, g, pads = _device_group(d, N, T, H, dt, signals)
+    rarn.tp_reduce_add_rms_norm_world(bufs, res, g, EPS, T, signals=pads)
+    torch.cuda.synchronize()
+    assert rarn.watchdog(clear=True) == 0
+    _check(bufs, res, ref, N, T, dt, f"N{N} T{T} H{H} {dt} prefetch={prefetch}")
+
+
+def test_tp_ranks_in_turn_with_prefetch(tune):
+    """The per-rank entry point with the prefetch forced on: each rank's
+    launch prefetches its own residual and every buffer (all of this
+    device's memory here)."""
+    import torch
+    tune(tp_prefetch=1)
+    N, T, H, dt = 2, 3000, 4096, "bf16"
+    d = _inputs(N, T, H, dt, seed=77)
+    ref = oracle.tp_reduce_add_rms_norm([d["partials"][q] for q in range(N)], d["residual"],
+                                        d["gamma"], EPS, dt)
+    bufs, res, g, _ = _device_group(d, N, T, H, dt, False)
+    for r in range(N):
+        rarn.tp_reduce_add_rms_norm(bufs, r, res[r], g, EPS, T)
+    torch.cuda.synchronize()
+    assert rarn.watchdog(clear=True) == 0
+    _check(bufs, res, ref, N, T, dt, "in turn, prefetch on")
+
+
 @pytest.mark.parametrize("N,T,H,dt", [(2, 100, 4096, "bf16"), (4, 1000, 8192, "bf16"),
                                       (3, 7, 2048, "f16"), (5, 64, 768, "f32")])
 def test_tp_ranks_one_after_another(N, T, H, dt):

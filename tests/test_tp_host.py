@@ -77,6 +77,77 @@ def test_tp_argument_errors():
              BF16, None) == INVALID                            # a rank's residual missing
 
 
+def _plan_fields(text):
+    head, *kv = text.split()
+    return head, {k: int(v) for k, v in (f.split("=") for f in kv)}
+
+
+# (N, H, dtype, CTAs per SM) -> whether each CTA prefetches its next row: the
+# shapes of the prefetch A/B on a GB300 (two to eight ranks' buffers on one
+# GPU), on the side the measurement came out
+PREFETCH_CASES = [
+    (1, 8192, "bf16", 1, 1), (2, 8192, "bf16", 1, 1), (3, 8192, "bf16", 1, 1),
+    (4, 8192, "bf16", 1, 1), (4, 8192, "f16", 1, 1), (2, 5120, "bf16", 1, 1),
+    (4, 5120, "bf16", 1, 1), (2, 4096, "f32", 1, 1), (2, 4096, "bf16", 2, 1),
+    (2, 2048, "bf16", 4, 1),
+    (5, 8192, "bf16", 1, 0), (6, 8192, "bf16", 1, 0), (8, 8192, "bf16", 1, 0),
+    (2, 8192, "f32", 1, 0), (4, 8192, "f32", 1, 0), (4, 4096, "bf16", 2, 0),
+    (8, 4096, "bf16", 2, 0), (4, 2048, "bf16", 4, 0),
+]
+
+
+@pytest.mark.parametrize("N,H,dt,per_sm,want", PREFETCH_CASES)
+def test_plan_tp_prefetch_rule(N, H, dt, per_sm, want, tune):
+    """The next-row L2 prefetch is on where an SM's loads in flight, per_sm
+    CTAs x (N + 1) rows, come to at most 64 KB, or 80 KB with one CTA per
+    SM; the knob forces it either way."""
+    size = {"f32": 4, "f16": 2, "bf16": 2}[dt]
+    inflight = per_sm * (N + 1) * H * size
+    assert want == int(inflight <= 65536 or (per_sm == 1 and inflight <= 81920))
+    head, f = _plan_fields(rarn.plan_tp(8192, H, N, dt, True, 152, per_sm))
+    assert head == "tp.world" and f["ranks"] == N and f["blocks_per_sm"] == per_sm
+    assert f["prefetch"] == want
+    for v in (0, 1):
+        tune(tp_prefetch=v)
+        assert _plan_fields(rarn.plan_tp(8192, H, N, dt, True, 152, per_sm))[1]["prefetch"] == v
+
+
+def test_plan_tp_launch_shape():
+    """CTAs per rank: the SMs' resident CTAs shared among the ranks of the
+    world launch (all of them for one rank's launch), at most 1024, and the
+    largest row block spread evenly over as few rounds as that allows; the
+    thread shape: the fewest 16-byte packs per thread (1, 2, 4) that keep a
+    CTA within 512 threads."""
+    for T, H, N, dt, world, sms, per_sm in [
+            (8192, 8192, 8, "bf16", True, 152, 1), (8192, 4096, 8, "bf16", True, 152, 2),
+            (16384, 8192, 2, "bf16", True, 152, 1), (100, 2048, 4, "f32", True, 152, 2),
+            (3, 512, 8, "f16", True, 152, 4), (8192, 8192, 8, "bf16", False, 152, 1),
+            (1 << 20, 1024, 1, "f32", False, 152, 8), (4097, 16384, 2, "bf16", True, 7, 1)]:
+        head, f = _plan_fields(rarn.plan_tp(T, H, N, dt, world, sms, per_sm))
+        assert head == ("tp.world" if world else "tp.rank")
+        rows_max = -(-T // N)
+        slots = max(1, min(1024, sms * per_sm // (N if world else 1)))
+        rounds = -(-rows_max // slots)
+        assert f["ctas"] == -(-rows_max // rounds) <= slots, (T, H, N, f)
+        if world:
+            assert f["ctas"] * N <= sms * per_sm or f["ctas"] == 1
+        nv = H * {"f32": 4, "f16": 2, "bf16": 2}[dt] // 16
+        vpt = 1 if nv <= 512 else 2 if nv <= 1024 else 4
+        assert f["vpt"] == vpt, f
+        assert f["block"] == (-(-nv // vpt) + 31) // 32 * 32 <= 512, f
+    lib = rarn.library()
+    buf = ctypes.create_string_buffer(128)
+    plan = lib.rarn_plan_tp
+    assert plan(64, 4096, 2, BF16, 1, 152, 1, None, 128) == INVALID
+    assert plan(64, 4096, 2, BF16, 1, 152, 1, buf, 0) == INVALID
+    for bad in ((0, 4096, 2, BF16), (64, 0, 2, BF16), (64, 4096, 0, BF16), (64, 4096, 9, BF16),
+                (64, 4096, 2, 7)):
+        assert plan(*bad, 1, 152, 1, buf, 128) == INVALID, bad
+    assert plan(64, 4092, 2, BF16, 1, 152, 1, buf, 128) == UNSUPPORTED
+    assert buf.value.startswith(b"none")
+    assert plan(64, 16392, 2, BF16, 1, 152, 1, buf, 128) == UNSUPPORTED
+
+
 def test_ipc_handle_checks():
     lib = rarn.library()
     h = ctypes.create_string_buffer(rarn.IPC_HANDLE_BYTES)
