@@ -274,10 +274,10 @@ rarn_status rarn_reduce_add_rms_norm_fp8(const rarn_fp8_rows *y, rarn_rows parti
  * byte r * T * H), 8-byte aligned; scales: R binary32 values in device memory;
  * residual (updated in place), gamma [H] and y [T, H] in `dt`, dense, 16-byte
  * aligned.  All device memory owned by the caller; asynchronous on `stream`.
- * With R > 4, H a multiple of 16, 16-byte aligned codes and at least 8 rows
- * per SM a persistent kernel streams the codes and the residual through
- * shared memory with bulk copies; otherwise a CTA per row holds it in
- * registers.  Both give the same residual bits (y may differ in the last
+ * With H a multiple of 16, 16-byte aligned codes, at least 8 rows per SM and
+ * either R >= 4 with H >= 4096, R >= 8, or R = 3 with H >= 8192, a persistent
+ * kernel streams the codes and the residual through shared memory with bulk
+ * copies; otherwise a CTA per row holds it in registers.  Both give the same residual bits (y may differ in the last
  * place: the row's sum of squares is reduced in another order).  The
  * persistent kernel's waits are bounded; one that runs out sets the
  * watchdog word (rarn_watchdog) and that CTA's outputs are invalid.

@@ -624,13 +624,19 @@ inline StreamPlan plan_stream(int64_t H, int R, int s, int max_smem) {
 
 // Which kernel a call takes (pure host logic; the launcher and the plan query
 // share it).  The TMA-fed kernel (ring = true) needs rows of a multiple of 16
-// elements (16-byte code copies) and 16-byte aligned codes, and is chosen for
-// more than 4 partials and at least 8 rows per SM.  Measured (CUDA-graph
-// timing, bf16 unless noted, register kernel / TMA-fed kernel, us): R = 8
-// [8192, 8192] 233 / 157 (f16 234 / 156; binary32 [8192, 4096] 155 / 109);
-// R = 16 [4096, 8192] 166 / 118; R = 6 [8192, 8192] 194 / 139; R = 4
-// [16384, 4096] 132 / 133; R = 2 [32768, 4096] 188 / 243; R = 8 [304, 8192]
-// 7.3 / 8.0.  Otherwise a register kernel: 16-element packs where H is a
+// elements (16-byte code copies) and 16-byte aligned codes, and is chosen
+// with at least 8 rows per SM: for more than 4 partials where H >= 4096 (8 or
+// more where the rows are shorter), for 4 partials with H >= 4096 and for 3
+// with H >= 8192.  Measured (CUDA-graph timing, bf16
+// unless noted, register kernel / TMA-fed kernel, us): R = 8 [8192, 8192]
+// 234.5 / 139.8 (f16 234 / 156 and binary32 [8192, 4096] 155 / 109 with an
+// earlier ring); R = 16 [4096, 8192] 167.0 / 110.2; R = 6 [8192, 8192]
+// 193.7 / 125.3; R = 4 [4096, 16384] 140.8 / 116.2, [8192, 8192] 146.6 /
+// 115.2, [16384, 4096] 129.7 / 121.5, [32768, 2048] 124.4 / 196.6; R = 3
+// [8192, 8192] 126.7 / 97.3, [16384, 4096] 113.2 / 116.2, [32768, 2048]
+// 108.1 / 190.2, [4096, 16384] 125.7 / 104.7; R = 2 [32768, 4096] 186.8 /
+// 222.1; at H = 2048, [32768, 2048]: R = 6 188.3 / 208.3, R = 8 230.6 /
+// 224.6; R = 8 [304, 8192] 7.3 / 8.0.  Otherwise a register kernel: 16-element packs where H is a
 // multiple of 16, else 8-element packs, `vpt` packs per thread so that a row
 // takes at most 256 threads (vpt = 0: H too long for the type).
 // ring_override = 0 / 1 switches the TMA-fed kernel off / takes it for any
@@ -650,7 +656,9 @@ inline KernelChoice choose_kernel(int64_t T, int64_t H, int R, int s, bool codes
     KernelChoice k;
     const int force = ring_override;
     if (force != 0 && H % 16 == 0 && codes_aligned16 &&
-        (force == 1 || (R > 4 && T >= 8 * (int64_t)num_sms))) {
+        (force == 1 || (T >= 8 * (int64_t)num_sms &&
+                        ((R > 4 && (H >= 4096 || R >= 8)) || (R == 4 && H >= 4096) ||
+                         (R == 3 && H >= 8192))))) {
         k.sp = plan_stream(H, R, s, max_smem);
         if (k.sp.ppt > 0) {
             k.ring = true;

@@ -401,7 +401,19 @@ def test_plan_fp8in(tune):
     # elements; the ncu capture of it reports 221.84 KB dynamic shared memory
     assert p == ("q8in.ring warps=16 ppt=1 chunk_elems=4096 stages=5 stage_bytes=40960 "
                  "smem=221840 grid=152 block=544"), p
-    assert rarn.plan_fp8in(8192, 8192, 4) == "q8in.rows pack=16 vpt=2 block=256 grid=occupancy"
+    # four or three partials: the ring where the rows are long enough
+    assert rarn.plan_fp8in(8192, 8192, 4).startswith("q8in.ring")
+    assert rarn.plan_fp8in(16384, 4096, 4).startswith("q8in.ring")
+    assert rarn.plan_fp8in(32768, 2048, 4) == "q8in.rows pack=16 vpt=1 block=128 grid=occupancy"
+    assert rarn.plan_fp8in(8192, 8192, 3).startswith("q8in.ring")
+    assert rarn.plan_fp8in(16384, 4096, 3) == "q8in.rows pack=16 vpt=1 block=256 grid=occupancy"
+    assert rarn.plan_fp8in(32768, 4096, 2).startswith("q8in.rows")
+    assert rarn.plan_fp8in(8 * 152 - 1, 8192, 4).startswith("q8in.rows")
+    # rows shorter than 4096: the ring only from 8 partials
+    assert rarn.plan_fp8in(32768, 2048, 6).startswith("q8in.rows")
+    assert rarn.plan_fp8in(32768, 2048, 7).startswith("q8in.rows")
+    assert rarn.plan_fp8in(32768, 2048, 8).startswith("q8in.ring")
+    assert rarn.plan_fp8in(32768, 4096, 5).startswith("q8in.ring")
     assert rarn.plan_fp8in(8 * 152 - 1, 8192, 8).startswith("q8in.rows")  # < 8 rows per SM
     assert rarn.plan_fp8in(8 * 152, 8192, 8).startswith("q8in.ring")
     assert rarn.plan_fp8in(8192, 8200, 8) == "q8in.rows pack=8 vpt=8 block=160 grid=occupancy"

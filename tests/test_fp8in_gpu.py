@@ -112,6 +112,26 @@ def test_fp8in_full_size_sampled():
     check(codes, scales, r, g, "bf16", "e4m3", "full size", rows=rows)
 
 
+@pytest.mark.parametrize("R,T,H,kernel", [
+    (4, 2048, 4096, "q8in.ring"),    # four partials, rows of 4096: the ring
+    (3, 1300, 8192, "q8in.ring"),    # three partials, rows of 8192: the ring
+    (6, 1300, 2048, "q8in.rows"),    # rows under 4096, fewer than 8 partials
+])
+def test_fp8in_planner_choice(R, T, H, kernel):
+    """Shapes with at least 8 rows per SM that the planner sends to the ring
+    or keeps on the register kernel by the partial count and row length:
+    the plan says which, and the result matches the oracle on every row."""
+    import torch
+    props = torch.cuda.get_device_properties(0)
+    if T < 8 * props.multi_processor_count:
+        pytest.skip("fewer than 8 rows per SM on this device")
+    smem = getattr(props, "shared_memory_per_block_optin", 0) or 232448
+    plan = rarn.plan_fp8in(T, H, R, "bf16", True, props.multi_processor_count, smem)
+    assert plan.startswith(kernel), plan
+    codes, scales, r, g = fp8in_inputs(R, T, H, "bf16", "e4m3", seed=R * 31 + T)
+    check(codes, scales, r, g, "bf16", "e4m3", f"R{R} T{T} H{H} ({kernel})")
+
+
 @pytest.mark.parametrize("ring", [0, 1])
 @pytest.mark.parametrize("pdl", [True, False])
 def test_fp8in_chained(pdl, ring, tune):
