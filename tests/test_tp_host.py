@@ -148,6 +148,24 @@ def test_plan_tp_launch_shape():
     assert plan(64, 16392, 2, BF16, 1, 152, 1, buf, 128) == UNSUPPORTED
 
 
+def test_plan_tp_device_queries():
+    """With the SM count or the occupancy left to the device, the plan query
+    asks the current device: RARN_ERR_CUDA where there is none (this host),
+    the same answer as the explicit form where there is one."""
+    import torch
+    lib = rarn.library()
+    buf = ctypes.create_string_buffer(128)
+    for sms, per_sm in ((0, 1), (152, 0), (0, 0)):
+        st = lib.rarn_plan_tp(8192, 8192, 2, BF16, 1, sms, per_sm, buf, 128)
+        if torch.cuda.is_available():
+            assert st == OK and buf.value.startswith(b"tp.world"), (sms, per_sm, buf.value)
+        else:
+            assert st == 4, (sms, per_sm, st)   # RARN_ERR_CUDA: no device to ask
+            assert lib.rarn_last_cuda_error() != 0
+    # argument errors come first, device or not
+    assert lib.rarn_plan_tp(8192, 8192, 9, BF16, 1, 0, 0, buf, 128) == INVALID
+
+
 def test_ipc_handle_checks():
     lib = rarn.library()
     h = ctypes.create_string_buffer(rarn.IPC_HANDLE_BYTES)
