@@ -427,7 +427,8 @@ rarn_status rarn_plan_fp8in(int64_t T, int64_t H, int32_t R, rarn_dtype dt, int 
  * and writes y into row t of every rank's buffer, so that the reduce form over
  * the N ranks' partials (R = N) is what every rank ends up with, bit for bit.
  * The reads and writes of other ranks' buffers are plain 16-byte loads and
- * stores (no multimem, no TMA).
+ * stores (no multimem, no TMA copies); buffers in memory of the current
+ * device may also be prefetched into L2 (rarn_plan_tp).
  *
  * Ordering between ranks.  With signal pads (signals[q] non-NULL for every q:
  * RARN_TP_SIGNAL_BYTES of device memory per rank, zeroed once before first

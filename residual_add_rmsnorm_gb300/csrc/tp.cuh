@@ -9,7 +9,8 @@
 // with all T rows of y.  Here the reduction is N plain 16-byte loads per pack
 // (one per rank, summed in binary32 in rank order 0 .. N-1, then the
 // residual, one rounding) and the all-gather N plain 16-byte stores; no
-// multimem / NVLS, no TMA.  Rank r owns rows floor(r T / N) ..
+// multimem / NVLS, no TMA copies (only a bulk L2 prefetch of the next row
+// where that row is memory of this device).  Rank r owns rows floor(r T / N) ..
 // floor((r + 1) T / N) - 1.
 //
 // Ordering between ranks: with signal pads, CTA b of every rank meets CTA b
